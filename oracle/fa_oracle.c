@@ -1,0 +1,455 @@
+/*
+ * FP64 CPU oracle for FlashAttention forward. TEST INFRASTRUCTURE ONLY: the
+ * product library never links or calls it (see fa_oracle.h).
+ *
+ * Page references used below:
+ *   [ops-transformer]  "ops-transformer" operator-library overview
+ *                      (gitcode.csdn.net), section 二.1 "FlashAttention算子":
+ *                      the traditional-attention listing and the tiled
+ *                      online-softmax loop with a single final normalisation.
+ *   [Ascend-FA]        zwxr.cn article on ops-transformer, section 3.1
+ *                      "FlashAttention的昇腾魔改": per-block recurrence for
+ *                      (m, l, O); section 5.1: softmax denominator in FP32.
+ *   [boost]            "ascend-transformer-boost 实战" (ai6s.net):
+ *                      scenario 2 (paged KV cache, 256-token pages),
+ *                      scenario 3 (sliding window 2048 + 64 global tokens),
+ *                      scenario 4 (splitting one attention into several
+ *                      calls is mathematically equivalent).
+ *
+ * Parity status of each function (what pins it, in tests/test_oracle_pins.py):
+ *   or_elem/or_decode      pinned against numpy's IEEE half / bf16 decoding
+ *   or_visible             pinned by hand-enumerated small masks and closed-form
+ *                          pair counts
+ *   or_count_visible       pinned by closed-form pair counts
+ *   or_tile_class          pinned by hand-classified small grids
+ *   or_attention           pinned by closed forms (constant scores, one-hot,
+ *                          causal row 0, hand-worked examples), invariances,
+ *                          special cases and a library routine (torch SDPA in
+ *                          float64 with an explicit boolean mask)
+ *   or_online_attention    pinned against or_attention and against the closed
+ *                          forms; the literal page-2 update is shown to differ
+ *   or_decode_paged        pinned by special cases (ctx = 1, identity table)
+ *   or_combine_partials    pinned by split invariance against unsplit softmax
+ *   or_decode_split_tokens pinned by partition invariants (cover, disjoint)
+ */
+#include "fa_oracle.h"
+
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* ------------------------------------------------------------------ */
+/* element decoding: the exact value of each stored input element       */
+/* ------------------------------------------------------------------ */
+
+/* IEEE 754 binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits. */
+static double half_bits_value(uint16_t h) {
+    int sign = (h >> 15) & 1;
+    int e = (h >> 10) & 0x1f;
+    int f = h & 0x3ff;
+    double v;
+    if (e == 0)
+        v = ldexp((double)f, -24); /* subnormal: f * 2^(1-15-10) */
+    else if (e == 31)
+        v = f ? NAN : INFINITY;
+    else
+        v = ldexp((double)(1024 + f), e - 25); /* (1.f) * 2^(e-15) */
+    return sign ? -v : v;
+}
+
+/* bfloat16 is the upper half of an IEEE binary32. */
+static double bf16_bits_value(uint16_t b) {
+    uint32_t u = (uint32_t)b << 16;
+    float x;
+    memcpy(&x, &u, sizeof x);
+    return (double)x;
+}
+
+double or_elem(const void* base, int64_t idx, int dtype) {
+    switch (dtype) {
+    case OR_F16: return half_bits_value(((const uint16_t*)base)[idx]);
+    case OR_BF16: return bf16_bits_value(((const uint16_t*)base)[idx]);
+    case OR_F32: return (double)((const float*)base)[idx];
+    default: return ((const double*)base)[idx];
+    }
+}
+
+void or_decode(const void* src, double* dst, int64_t n, int dtype) {
+    for (int64_t i = 0; i < n; ++i) dst[i] = or_elem(src, i, dtype);
+}
+
+/* ------------------------------------------------------------------ */
+/* the mask                                                            */
+/* ------------------------------------------------------------------ */
+
+/*
+ * Vis(i): which keys j query i may attend to. Queries and keys are aligned at
+ * the bottom-right (delta = Sk - Sq), so query i sits at key position i+delta.
+ *   NONE           every key.
+ *   CAUSAL         j <= i+delta                    ([ops-transformer] section 四,
+ *                                                   causal=True).
+ *   CAUSAL_WINDOW  j <= i+delta and (i+delta-j < window or j < n_global)
+ *                  ([boost] scenario 3: a sliding window plus global tokens
+ *                  such as BOS, read causally: the window holds `window` keys
+ *                  counting the query's own position; the global tokens are
+ *                  the first n_global key positions).
+ */
+int or_visible(int64_t i, int64_t j, int64_t Sq, int64_t Sk, int mask_mode,
+               int64_t window, int64_t n_global) {
+    int64_t pos = i + (Sk - Sq);
+    if (i < 0 || i >= Sq || j < 0 || j >= Sk) return 0;
+    if (mask_mode == OR_MASK_NONE) return 1;
+    if (j > pos) return 0;
+    if (mask_mode == OR_MASK_CAUSAL) return 1;
+    return (pos - j < window) || (j < n_global);
+}
+
+int64_t or_count_visible(int64_t Sq, int64_t Sk, int mask_mode, int64_t window,
+                         int64_t n_global) {
+    int64_t total = 0;
+    for (int64_t i = 0; i < Sq; ++i)
+        for (int64_t j = 0; j < Sk; ++j)
+            total += or_visible(i, j, Sq, Sk, mask_mode, window, n_global);
+    return total;
+}
+
+/*
+ * Class of the (mb, nb) tile of BM query rows x BN key columns, by brute force
+ * over its pairs. A pair outside [0,Sq) x [0,Sk) counts as not visible, so a
+ * tile that hangs over the end of either sequence is never FULL.
+ */
+int or_tile_class(int64_t mb, int64_t nb, int64_t BM, int64_t BN, int64_t Sq,
+                  int64_t Sk, int mask_mode, int64_t window, int64_t n_global) {
+    int64_t vis = 0;
+    for (int64_t i = mb * BM; i < mb * BM + BM; ++i)
+        for (int64_t j = nb * BN; j < nb * BN + BN; ++j)
+            vis += or_visible(i, j, Sq, Sk, mask_mode, window, n_global);
+    if (vis == 0) return OR_TILE_EMPTY;
+    if (vis == BM * BN) return OR_TILE_FULL;
+    return OR_TILE_PARTIAL;
+}
+
+/* ------------------------------------------------------------------ */
+/* attention by its definition                                         */
+/* ------------------------------------------------------------------ */
+
+/*
+ * One query row against an explicit list of key/value rows, by the definition:
+ *   s_j = scale * sum_c q_c k_jc,  m = max_j s_j,
+ *   P_j = exp(s_j - m) / sum_t exp(s_t - m),  O = sum_j P_j v_j,
+ *   LSE = m + ln sum_t exp(s_t - m).
+ * An empty list gives O = 0 and LSE = -inf.
+ * kidx[t] / vidx[t] are element offsets of the t-th key / value row.
+ */
+static void attend_row(const double* q, const void* k, const void* v, int dtype,
+                       const int64_t* kidx, const int64_t* vidx, int64_t n,
+                       int64_t d, double scale, double* s, double* o,
+                       double* lse, double* psum_err) {
+    for (int64_t c = 0; c < d; ++c) o[c] = 0.0;
+    if (n == 0) {
+        *lse = -INFINITY;
+        *psum_err = 0.0;
+        return;
+    }
+    double m = -INFINITY;
+    for (int64_t t = 0; t < n; ++t) {
+        double dot = 0.0;
+        for (int64_t c = 0; c < d; ++c) dot += q[c] * or_elem(k, kidx[t] + c, dtype);
+        s[t] = scale * dot;
+        if (s[t] > m) m = s[t];
+    }
+    double z = 0.0;
+    for (int64_t t = 0; t < n; ++t) z += exp(s[t] - m);
+    double psum = 0.0;
+    for (int64_t t = 0; t < n; ++t) {
+        double p = exp(s[t] - m) / z;
+        psum += p;
+        for (int64_t c = 0; c < d; ++c) o[c] += p * or_elem(v, vidx[t] + c, dtype);
+    }
+    *lse = m + log(z);
+    *psum_err = fabs(1.0 - psum);
+}
+
+/*
+ * Attention over [B,H,Sq,d] queries and [B,H,Sk,d] keys/values (contiguous).
+ * rows == NULL: every row; o is [B,H,Sq,d] and lse [B,H,Sq].
+ * otherwise rows[r] = (b*H + h)*Sq + i and o is [nrows,d], lse [nrows].
+ * max_psum_err (may be NULL) receives max over rows of |1 - sum_j P_j|.
+ * Returns 0, or -1 on a bad argument.
+ */
+int or_attention(const void* q, const void* k, const void* v, int dtype,
+                 double* o, double* lse, int64_t B, int64_t H, int64_t Sq,
+                 int64_t Sk, int64_t d, double scale, int mask_mode,
+                 int64_t window, int64_t n_global, const int64_t* rows,
+                 int64_t nrows, double* max_psum_err, int nthreads) {
+    if (B < 0 || H < 0 || Sq < 0 || Sk < 0 || d <= 0) return -1;
+    if (mask_mode < OR_MASK_NONE || mask_mode > OR_MASK_CAUSAL_WINDOW) return -1;
+    if (mask_mode == OR_MASK_CAUSAL_WINDOW && (window < 1 || n_global < 0)) return -1;
+    int64_t n_out = rows ? nrows : B * H * Sq;
+    double worst = 0.0;
+    int bad = 0;
+#ifdef _OPENMP
+    if (nthreads <= 0) nthreads = omp_get_max_threads();
+#pragma omp parallel num_threads(nthreads) reduction(max : worst) reduction(| : bad)
+#endif
+    {
+        double* qrow = (double*)malloc(sizeof(double) * (size_t)d);
+        double* s = (double*)malloc(sizeof(double) * (size_t)(Sk > 0 ? Sk : 1));
+        int64_t* kidx = (int64_t*)malloc(sizeof(int64_t) * (size_t)(Sk > 0 ? Sk : 1));
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 16)
+#endif
+        for (int64_t r = 0; r < n_out; ++r) {
+            int64_t row = rows ? rows[r] : r;
+            if (row < 0 || row >= B * H * Sq) {
+                bad = 1;
+                continue;
+            }
+            int64_t bh = row / Sq, i = row % Sq;
+            for (int64_t c = 0; c < d; ++c) qrow[c] = or_elem(q, row * d + c, dtype);
+            int64_t n = 0;
+            for (int64_t j = 0; j < Sk; ++j)
+                if (or_visible(i, j, Sq, Sk, mask_mode, window, n_global))
+                    kidx[n++] = (bh * Sk + j) * d;
+            double err;
+            attend_row(qrow, k, v, dtype, kidx, kidx, n, d, scale, s, o + r * d,
+                       lse + r, &err);
+            if (err > worst) worst = err;
+        }
+        free(qrow);
+        free(s);
+        free(kidx);
+    }
+    if (max_psum_err) *max_psum_err = worst;
+    return bad ? -1 : 0;
+}
+
+/* ------------------------------------------------------------------ */
+/* the blocked online recurrence, in the pages' order                  */
+/* ------------------------------------------------------------------ */
+
+/*
+ * The tiled loop of [ops-transformer] 二.1 for every row: walk the keys in
+ * blocks of block_n, keep a running maximum m and running sum l, and fold each
+ * block into the output. Three forms of the per-block update:
+ *
+ *   OR_REC_UNNORMALISED  ([ops-transformer]: statistics updated per block,
+ *       one normalisation at the end). The accumulator and l share a
+ *       reference maximum m_ref; when a block raises the running maximum by
+ *       more than tau (natural-log units) both are multiplied by
+ *       exp(m_ref - m_new) and m_ref moves up. tau = 0 rescales on every
+ *       increase. p_j = exp(s_j - m_ref); l += sum p; acc += sum p_j v_j;
+ *       at the end O = acc / l, LSE = m_ref + ln l.
+ *   OR_REC_NORMALISED    ([Ascend-FA] 3.1 read with its lost factor restored):
+ *       m_new = max(m, block max); l_new = exp(m - m_new) l + sum exp(s - m_new);
+ *       O = (l exp(m - m_new) O + sum exp(s_j - m_new) v_j) / l_new.
+ *   OR_REC_LITERAL_P2    ([Ascend-FA] 3.1 as printed): the old-output term is
+ *       divided by l_new without the factor l. Kept only so that a test can
+ *       show this printed form is not the softmax.
+ *
+ * Output layout as or_attention with rows == NULL.
+ */
+int or_online_attention(const void* q, const void* k, const void* v, int dtype,
+                        double* o, double* lse, int64_t B, int64_t H,
+                        int64_t Sq, int64_t Sk, int64_t d, double scale,
+                        int mask_mode, int64_t window, int64_t n_global,
+                        int64_t block_n, double tau, int variant) {
+    if (block_n < 1 || d <= 0 || B < 0 || H < 0 || Sq < 0 || Sk < 0) return -1;
+    double* qrow = (double*)malloc(sizeof(double) * (size_t)d);
+    double* acc = (double*)malloc(sizeof(double) * (size_t)d);
+    double* s = (double*)malloc(sizeof(double) * (size_t)block_n);
+    int* vis = (int*)malloc(sizeof(int) * (size_t)block_n);
+    for (int64_t bh = 0; bh < B * H; ++bh) {
+        for (int64_t i = 0; i < Sq; ++i) {
+            int64_t row = bh * Sq + i;
+            for (int64_t c = 0; c < d; ++c) {
+                qrow[c] = or_elem(q, row * d + c, dtype);
+                acc[c] = 0.0;
+            }
+            double m = -INFINITY, l = 0.0;
+            for (int64_t j0 = 0; j0 < Sk; j0 += block_n) {
+                int64_t nb = (Sk - j0 < block_n) ? Sk - j0 : block_n;
+                double bmax = -INFINITY;
+                for (int64_t t = 0; t < nb; ++t) {
+                    int64_t j = j0 + t;
+                    vis[t] = or_visible(i, j, Sq, Sk, mask_mode, window, n_global);
+                    if (!vis[t]) continue;
+                    double dot = 0.0;
+                    for (int64_t c = 0; c < d; ++c)
+                        dot += qrow[c] * or_elem(k, (bh * Sk + j) * d + c, dtype);
+                    s[t] = scale * dot;
+                    if (s[t] > bmax) bmax = s[t];
+                }
+                if (bmax == -INFINITY) continue; /* nothing visible in this block */
+                double m_new = bmax > m ? bmax : m;
+                if (variant == OR_REC_UNNORMALISED) {
+                    if (m == -INFINITY) {
+                        m = m_new; /* first visible block: m is the reference */
+                    } else if (m_new - m > tau) {
+                        double a = exp(m - m_new);
+                        l *= a;
+                        for (int64_t c = 0; c < d; ++c) acc[c] *= a;
+                        m = m_new;
+                    }
+                    for (int64_t t = 0; t < nb; ++t) {
+                        if (!vis[t]) continue;
+                        double p = exp(s[t] - m);
+                        l += p;
+                        for (int64_t c = 0; c < d; ++c)
+                            acc[c] += p * or_elem(v, (bh * Sk + j0 + t) * d + c, dtype);
+                    }
+                } else {
+                    double a = (m == -INFINITY) ? 0.0 : exp(m - m_new);
+                    double bsum = 0.0;
+                    for (int64_t t = 0; t < nb; ++t)
+                        if (vis[t]) bsum += exp(s[t] - m_new);
+                    double l_new = a * l + bsum;
+                    double keep = (variant == OR_REC_NORMALISED) ? l * a / l_new : a / l_new;
+                    for (int64_t c = 0; c < d; ++c) {
+                        double pv = 0.0;
+                        for (int64_t t = 0; t < nb; ++t)
+                            if (vis[t])
+                                pv += exp(s[t] - m_new) *
+                                      or_elem(v, (bh * Sk + j0 + t) * d + c, dtype);
+                        acc[c] = acc[c] * keep + pv / l_new;
+                    }
+                    m = m_new;
+                    l = l_new;
+                }
+            }
+            double* orow = o + row * d;
+            if (l == 0.0) {
+                for (int64_t c = 0; c < d; ++c) orow[c] = 0.0;
+                lse[row] = -INFINITY;
+            } else if (variant == OR_REC_UNNORMALISED) {
+                for (int64_t c = 0; c < d; ++c) orow[c] = acc[c] / l;
+                lse[row] = m + log(l);
+            } else {
+                for (int64_t c = 0; c < d; ++c) orow[c] = acc[c];
+                lse[row] = m + log(l);
+            }
+        }
+    }
+    free(qrow);
+    free(acc);
+    free(s);
+    free(vis);
+    return 0;
+}
+
+/* ------------------------------------------------------------------ */
+/* paged-KV decode                                                     */
+/* ------------------------------------------------------------------ */
+
+/*
+ * Decode over a paged KV cache ([boost] scenario 2: the cache is split into
+ * fixed-size pages, 256 tokens each in the pages' example). Sequence b has
+ * ctx_lens[b] cached tokens; token t lives in physical page
+ * block_table[b*max_pages_per_seq + t/page_size] at offset t % page_size.
+ * Pools are [num_pages, H, page_size, d]; q and o are [B,H,d]; lse [B,H].
+ * The single new query sits at position ctx-1 and sees every cached token,
+ * so the result is the definition above over the gathered rows.
+ * bh_list == NULL: all B*H pairs; else only bh_list[r] = b*H + h, packed.
+ * Returns 0, or -1 if a needed table entry is out of range.
+ */
+int or_decode_paged(const void* q, const void* k_pages, const void* v_pages,
+                    int dtype, const int32_t* block_table,
+                    const int32_t* ctx_lens, double* o, double* lse, int64_t B,
+                    int64_t H, int64_t d, int64_t page_size,
+                    int64_t max_pages_per_seq, int64_t num_pages, double scale,
+                    const int64_t* bh_list, int64_t n_bh, int nthreads) {
+    if (B < 0 || H < 0 || d <= 0 || page_size <= 0) return -1;
+    int64_t n_out = bh_list ? n_bh : B * H;
+    int64_t max_ctx = page_size * max_pages_per_seq;
+    int bad = 0;
+#ifdef _OPENMP
+    if (nthreads <= 0) nthreads = omp_get_max_threads();
+#pragma omp parallel num_threads(nthreads) reduction(| : bad)
+#endif
+    {
+        double* qrow = (double*)malloc(sizeof(double) * (size_t)d);
+        double* s = (double*)malloc(sizeof(double) * (size_t)(max_ctx > 0 ? max_ctx : 1));
+        int64_t* idx = (int64_t*)malloc(sizeof(int64_t) * (size_t)(max_ctx > 0 ? max_ctx : 1));
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 1)
+#endif
+        for (int64_t r = 0; r < n_out; ++r) {
+            int64_t bh = bh_list ? bh_list[r] : r;
+            if (bh < 0 || bh >= B * H) {
+                bad = 1;
+                continue;
+            }
+            int64_t b = bh / H, h = bh % H;
+            int64_t ctx = ctx_lens[b];
+            if (ctx < 0 || ctx > max_ctx) {
+                bad = 1;
+                continue;
+            }
+            /* gather: the element offset of token t's row for head h */
+            int64_t n = 0;
+            for (int64_t t = 0; t < ctx; ++t) {
+                int64_t page = block_table[b * max_pages_per_seq + t / page_size];
+                if (page < 0 || page >= num_pages) {
+                    bad = 1;
+                    break;
+                }
+                idx[n++] = ((page * H + h) * page_size + t % page_size) * d;
+            }
+            if (n != ctx) continue;
+            for (int64_t c = 0; c < d; ++c) qrow[c] = or_elem(q, bh * d + c, dtype);
+            double err;
+            attend_row(qrow, k_pages, v_pages, dtype, idx, idx, n, d, scale, s,
+                       o + r * d, lse + r, &err);
+        }
+        free(qrow);
+        free(s);
+        free(idx);
+    }
+    return bad ? -1 : 0;
+}
+
+/*
+ * Merge softmax partials computed over disjoint key subsets. Split s holds
+ *   m_s = max of its scores, l_s = sum exp(s_j - m_s), acc_s = sum exp(s_j - m_s) v_j.
+ * The merged result is the same recurrence as the per-block update of
+ * [ops-transformer] 二.1 / [Ascend-FA] 3.1, applied across splits:
+ *   M = max m_s;  L = sum l_s exp(m_s - M);  O = sum exp(m_s - M) acc_s / L;
+ *   LSE = M + ln L.  Splits with l_s = 0 contribute nothing; if all are empty,
+ *   O = 0 and LSE = -inf.
+ */
+void or_combine_partials(const double* m, const double* l, const double* acc,
+                         int64_t nsplit, int64_t d, double* o, double* lse) {
+    double M = -INFINITY;
+    for (int64_t s = 0; s < nsplit; ++s)
+        if (l[s] > 0.0 && m[s] > M) M = m[s];
+    for (int64_t c = 0; c < d; ++c) o[c] = 0.0;
+    if (M == -INFINITY) {
+        *lse = -INFINITY;
+        return;
+    }
+    double L = 0.0;
+    for (int64_t s = 0; s < nsplit; ++s)
+        if (l[s] > 0.0) L += l[s] * exp(m[s] - M);
+    for (int64_t s = 0; s < nsplit; ++s) {
+        if (!(l[s] > 0.0)) continue;
+        double w = exp(m[s] - M) / L;
+        for (int64_t c = 0; c < d; ++c) o[c] += w * acc[s * d + c];
+    }
+    *lse = M + log(L);
+}
+
+/*
+ * The token range [t0, t1) that decode split `split` covers when a sequence
+ * of ctx_len tokens is cut into runs of pages_per_split whole pages.
+ */
+void or_decode_split_tokens(int64_t ctx_len, int64_t page_size,
+                            int64_t pages_per_split, int64_t split, int64_t* t0,
+                            int64_t* t1) {
+    int64_t span = page_size * pages_per_split;
+    int64_t a = split * span, b = a + span;
+    *t0 = a < ctx_len ? a : ctx_len;
+    *t1 = b < ctx_len ? b : ctx_len;
+}

@@ -1,0 +1,74 @@
+/*
+ * FP64 CPU oracle for FlashAttention forward (prefill and paged decode).
+ *
+ * TEST INFRASTRUCTURE ONLY. Nothing in the product library links, includes or
+ * calls this code; only the test suite, the smoke check and the benchmark's
+ * CPU-baseline leg load it. It shares no source with the CUDA path.
+ *
+ * What it computes is the plain definition of attention that the pages start
+ * from ("ops-transformer" overview on gitcode.csdn.net, section 二.1
+ * "FlashAttention算子", the "traditional attention" listing):
+ *     O = softmax(scale * Q K^T + mask) V,   per (batch, head),
+ * with the score row materialised in double precision. The log-sum-exp
+ * LSE_i = m_i + ln sum_j exp(s_ij - m_i) is returned beside O.
+ *
+ * Inputs are read as their exact stored values: 16-bit floats are decoded
+ * bit by bit into doubles here, so input rounding is never counted as error.
+ */
+#ifndef FA_ORACLE_H
+#define FA_ORACLE_H
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* element types the oracle can read */
+enum { OR_F16 = 0, OR_BF16 = 1, OR_F32 = 2, OR_F64 = 3 };
+/* mask modes (same numbering as the library's public enum, chosen independently) */
+enum { OR_MASK_NONE = 0, OR_MASK_CAUSAL = 1, OR_MASK_CAUSAL_WINDOW = 2 };
+/* tile classes */
+enum { OR_TILE_EMPTY = 0, OR_TILE_PARTIAL = 1, OR_TILE_FULL = 2 };
+/* online-recurrence variants (see or_online_attention) */
+enum { OR_REC_UNNORMALISED = 0, OR_REC_NORMALISED = 1, OR_REC_LITERAL_P2 = 2 };
+
+double or_elem(const void* base, int64_t idx, int dtype);
+void or_decode(const void* src, double* dst, int64_t n, int dtype);
+
+int or_visible(int64_t i, int64_t j, int64_t Sq, int64_t Sk, int mask_mode,
+               int64_t window, int64_t n_global);
+int64_t or_count_visible(int64_t Sq, int64_t Sk, int mask_mode, int64_t window,
+                         int64_t n_global);
+int or_tile_class(int64_t mb, int64_t nb, int64_t BM, int64_t BN, int64_t Sq,
+                  int64_t Sk, int mask_mode, int64_t window, int64_t n_global);
+
+int or_attention(const void* q, const void* k, const void* v, int dtype,
+                 double* o, double* lse, int64_t B, int64_t H, int64_t Sq,
+                 int64_t Sk, int64_t d, double scale, int mask_mode,
+                 int64_t window, int64_t n_global, const int64_t* rows,
+                 int64_t nrows, double* max_psum_err, int nthreads);
+
+int or_online_attention(const void* q, const void* k, const void* v, int dtype,
+                        double* o, double* lse, int64_t B, int64_t H,
+                        int64_t Sq, int64_t Sk, int64_t d, double scale,
+                        int mask_mode, int64_t window, int64_t n_global,
+                        int64_t block_n, double tau, int variant);
+
+int or_decode_paged(const void* q, const void* k_pages, const void* v_pages,
+                    int dtype, const int32_t* block_table,
+                    const int32_t* ctx_lens, double* o, double* lse, int64_t B,
+                    int64_t H, int64_t d, int64_t page_size,
+                    int64_t max_pages_per_seq, int64_t num_pages, double scale,
+                    const int64_t* bh_list, int64_t n_bh, int nthreads);
+
+void or_combine_partials(const double* m, const double* l, const double* acc,
+                         int64_t nsplit, int64_t d, double* o, double* lse);
+
+void or_decode_split_tokens(int64_t ctx_len, int64_t page_size,
+                            int64_t pages_per_split, int64_t split,
+                            int64_t* t0, int64_t* t1);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

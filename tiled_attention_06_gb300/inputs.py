@@ -1,0 +1,94 @@
+"""Seeded synthetic inputs shaped like the pages' workloads.
+
+This module only draws random numbers and lays them out; it holds none of the
+attention arithmetic, so the CUDA path and the CPU oracle can both take their
+inputs from it without sharing any of the method.
+
+All draws use a CPU ``torch.Generator`` seeded explicitly, in a fixed order, so
+that the same bytes can be handed to the GPU and to the oracle.
+"""
+from dataclasses import dataclass
+
+import torch
+
+DTYPES = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}
+
+
+def prefill_inputs(B, H, Sq, Sk, d, dtype=torch.float16, factor=1.0, seed=0):
+    """q [B,H,Sq,d], k and v [B,H,Sk,d]: i.i.d. N(0,1) * factor in float32, then cast.
+
+    Draw order: q, k, v.
+    """
+    g = torch.Generator().manual_seed(seed)
+    q = (torch.randn(B, H, Sq, d, generator=g) * factor).to(dtype)
+    k = (torch.randn(B, H, Sk, d, generator=g) * factor).to(dtype)
+    v = (torch.randn(B, H, Sk, d, generator=g) * factor).to(dtype)
+    return q, k, v
+
+
+@dataclass
+class DecodeInputs:
+    q: torch.Tensor            # [B,H,d]
+    k_pages: torch.Tensor      # [num_pages,H,page_size,d]
+    v_pages: torch.Tensor      # [num_pages,H,page_size,d]
+    block_table: torch.Tensor  # int32 [B,max_pages_per_seq], unused entries -1
+    ctx_lens: torch.Tensor     # int32 [B]
+    page_size: int
+
+    @property
+    def B(self):
+        return self.q.shape[0]
+
+    @property
+    def H(self):
+        return self.q.shape[1]
+
+    @property
+    def d(self):
+        return self.q.shape[2]
+
+
+def decode_inputs(B=32, H=32, d=128, page_size=256, num_pages=1200, max_ctx=8192,
+                  dtype=torch.float16, seed=0, ctx_lens=None, poison=True):
+    """A paged KV cache with randomly scattered pages.
+
+    Draw order: ctx_lens ~ U{1..max_ctx} (unless given), perm = randperm(num_pages),
+    q, then for every referenced page in table order (sequence b ascending, page
+    index ascending) its K block [H,page_size,d] then its V block.
+    Sequence b takes the next ceil(ctx_b / page_size) entries of perm.
+    Unused table entries are -1. With poison=True, unreferenced pages and the
+    slots past ctx_b in a sequence's last page hold NaN, so that any read of a
+    token the query may not see shows up in the output.
+    """
+    g = torch.Generator().manual_seed(seed)
+    max_pages = (max_ctx + page_size - 1) // page_size
+    if ctx_lens is None:
+        ctx = torch.randint(1, max_ctx + 1, (B,), generator=g, dtype=torch.int64)
+    else:
+        ctx = torch.as_tensor(ctx_lens, dtype=torch.int64).clone()
+        if ctx.numel() != B or (B > 0 and (int(ctx.max()) > max_ctx or int(ctx.min()) < 0)):
+            raise ValueError("ctx_lens must have B entries, each in [0, max_ctx]")
+    perm = torch.randperm(num_pages, generator=g)
+    npages = [(int(c) + page_size - 1) // page_size for c in ctx]
+    if sum(npages) > num_pages:
+        raise ValueError("the pool is too small for these context lengths")
+    table = torch.full((B, max_pages), -1, dtype=torch.int32)
+    off = 0
+    for b in range(B):
+        table[b, :npages[b]] = perm[off:off + npages[b]].to(torch.int32)
+        off += npages[b]
+    q = torch.randn(B, H, d, generator=g).to(dtype)
+    fill = float("nan") if poison else 0.0
+    kp = torch.full((num_pages, H, page_size, d), fill, dtype=dtype)
+    vp = torch.full((num_pages, H, page_size, d), fill, dtype=dtype)
+    for b in range(B):
+        for p in range(npages[b]):
+            pg = int(table[b, p])
+            kp[pg] = torch.randn(H, page_size, d, generator=g).to(dtype)
+            vp[pg] = torch.randn(H, page_size, d, generator=g).to(dtype)
+        tail = int(ctx[b]) - (npages[b] - 1) * page_size
+        if poison and npages[b] > 0 and tail < page_size:
+            pg = int(table[b, npages[b] - 1])
+            kp[pg, :, tail:, :] = float("nan")
+            vp[pg, :, tail:, :] = float("nan")
+    return DecodeInputs(q, kp, vp, table, ctx.to(torch.int32), page_size)
