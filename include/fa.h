@@ -1,0 +1,188 @@
+/*
+ * fa.h - FlashAttention forward for one NVIDIA GB300 (sm_103a): C ABI.
+ *
+ * What is computed. For every (batch b, head h) and query row i:
+ *     O[b,h,i,:] = sum_j P_ij V[b,h,j,:],
+ *     P_ij = exp(scale * Q_i.K_j) / sum_{t in Vis(i)} exp(scale * Q_i.K_t),  j in Vis(i),
+ *     LSE[b,h,i] = ln sum_{t in Vis(i)} exp(scale * Q_i.K_t)      (natural log),
+ * i.e. O = softmax(scale * Q K^T + mask) V, the definition in the ops-transformer
+ * overview (gitcode.csdn.net, section 二.1 "FlashAttention算子", the traditional-
+ * attention listing), computed the way its tiled loop describes: the score tile is
+ * produced on chip and never written to memory, the running max and sum are
+ * updated block by block (softmax denominator in FP32, zwxr.cn article section 5.1)
+ * and the output is normalised once at the end.
+ *
+ * Masks (Vis(i)); queries are aligned to the LAST Sq key positions, delta = Sk - Sq:
+ *   FA_MASK_NONE           every key.
+ *   FA_MASK_CAUSAL         j <= i + delta                (ops-transformer overview,
+ *                                                        section 四, causal=True).
+ *   FA_MASK_CAUSAL_WINDOW  j <= i + delta and (i + delta - j < window or j < n_global):
+ *                          a causal sliding window of `window` keys (the query's own
+ *                          position included) plus the first `n_global` keys as
+ *                          global tokens ("ascend-transformer-boost 实战" (ai6s.net),
+ *                          scenario 3, window_size=2048, global_tokens=64).
+ * A query that sees no key gets O = 0 and LSE = -inf.
+ *
+ * Conventions for every call:
+ *   - Pointers are DEVICE pointers unless stated otherwise, 16-byte aligned, and
+ *     owned by the caller. The library allocates no memory in any call.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream) and never synchronises the host.
+ *   - Argument errors are detected on the host before anything is launched and
+ *     return FA_ERR_INVALID_ARG or FA_ERR_UNSUPPORTED; nothing runs in that case.
+ *   - Faults found on the device (a page-table entry out of range, a pipeline wait
+ *     that ran past its time limit) are recorded in a device status word and
+ *     reported by fa_get_device_status().
+ *   - fa_last_error_string() describes the last non-FA_OK status of this thread.
+ */
+#ifndef FA_H
+#define FA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* fa_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1, /* a null pointer, a negative size, misalignment, ... */
+  FA_ERR_UNSUPPORTED = 2, /* valid but not built: d not in {64,128}, an unknown dtype */
+  FA_ERR_CUDA = 3,        /* a CUDA runtime call failed (see fa_last_error_string) */
+  FA_ERR_TIMEOUT = 4,     /* a kernel gave up on a pipeline wait (device status) */
+  FA_ERR_BAD_PAGE = 5     /* a block-table entry or context length was out of range */
+} fa_status;
+
+enum { FA_F16 = 0, FA_BF16 = 1 };
+enum { FA_MASK_NONE = 0, FA_MASK_CAUSAL = 1, FA_MASK_CAUSAL_WINDOW = 2 };
+
+/*
+ * fa_fwd - attention forward (prefill) over contiguous BHSD tensors.
+ *   q      [B, H, Sq, d]  dtype (fp16 or bf16), row-major (d fastest)
+ *   k, v   [B, H, Sk, d]  dtype
+ *   o      [B, H, Sq, d]  dtype, written (RN from the FP32 accumulator)
+ *   lse    [B, H, Sq]     float32, natural log; may be NULL
+ *   d      64 or 128;  B, H >= 1;  Sq, Sk >= 0. q and o may be NULL when Sq == 0 (the
+ *          call then does nothing); k and v may be NULL when Sk == 0 (every row then
+ *          sees no key).
+ *   scale  the softmax scale (typically 1/sqrt(d))
+ *   mask_mode / window / n_global as above (window >= 1 and n_global >= 0 for
+ *          FA_MASK_CAUSAL_WINDOW; ignored otherwise)
+ *   dtype  FA_F16 or FA_BF16 (added before `stream`: a signature without it could
+ *          not tell fp16 inputs from bf16 inputs)
+ */
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                 int Sq, int Sk, int d, float scale, int mask_mode, int window, int n_global,
+                 int dtype, fa_stream_t stream);
+
+/* Extended form of fa_fwd: tile size, grid size, time limit and a debug trace. */
+typedef struct fa_fwd_params {
+  const void* q;
+  const void* k;
+  const void* v;
+  void* o;
+  float* lse;
+  int B, H, Sq, Sk, d;
+  float scale;
+  int mask_mode, window, n_global, dtype;
+  int block_n;        /* key-block size: 0 = default (128), else 64 or 128 */
+  int num_ctas;       /* persistent grid size: 0 = one CTA per SM */
+  int group_heads;    /* (batch, head) pairs scheduled together: 0 = sized for L2 */
+  uint32_t timeout_us; /* per-wait time limit: 0 = 1 s */
+  /* Optional visit log, int32 [B*H, ceil(Sq/128), ceil(Sk/block_n)], zeroed by the
+   * caller. Every visited tile adds 16 + class (1 partial, 2 full); tiles the mask
+   * skips stay 0. */
+  int32_t* trace;
+} fa_fwd_params;
+
+fa_status fa_fwd_ex(const fa_fwd_params* params, fa_stream_t stream);
+
+/* Query-block height of the prefill kernel (rows per work item), for sizing traces. */
+int fa_fwd_block_m(void);
+
+/*
+ * fa_decode_paged - one query token per sequence against a paged KV cache
+ * ("ascend-transformer-boost 实战" (ai6s.net), scenario 2: the cache is cut into
+ * fixed-size pages, 256 tokens in the pages' example, and new pages are taken as a
+ * sequence grows). The query of sequence b sits at position ctx_lens[b]-1 and sees
+ * all ctx_lens[b] cached tokens; token t is stored in physical page
+ * block_table[b, t / page_size] at offset t % page_size.
+ *   q            [B, H, d]  dtype
+ *   k_pages      [num_pages, H, page_size, d]  dtype (one (page, head) run is contiguous)
+ *   v_pages      [num_pages, H, page_size, d]  dtype
+ *   block_table  int32 [B, max_pages_per_seq]; entries past a sequence's last page
+ *                are not read. An entry outside [0, num_pages) that would be read is
+ *                skipped on the device and reported as FA_ERR_BAD_PAGE.
+ *   ctx_lens     int32 [B], each in [0, page_size * max_pages_per_seq]; a value outside
+ *                that range is clamped into it on the device and reported as
+ *                FA_ERR_BAD_PAGE.
+ *   o            [B, H, d]  dtype;  lse [B, H] float32 (may be NULL)
+ *   d            64 or 128;  page_size a multiple of 16 in [16, 4096]
+ *   workspace    device scratch of at least fa_decode_workspace_size(...) bytes,
+ *                owned by the caller; its contents need no initialisation.
+ * Two kernels run on `stream`: split-K partial attention over runs of pages, then
+ * the merge of the partials.
+ */
+fa_status fa_decode_paged(const void* q, const void* k_pages, const void* v_pages,
+                          const int32_t* block_table, const int32_t* ctx_lens, void* o, float* lse,
+                          int B, int H, int d, int page_size, int max_pages_per_seq, int num_pages,
+                          float scale, int dtype, void* workspace, size_t workspace_bytes,
+                          fa_stream_t stream);
+
+/* Bytes of workspace fa_decode_paged needs for these sizes (any split choice). */
+size_t fa_decode_workspace_size(int B, int H, int d, int max_pages_per_seq, int page_size);
+
+/* Extended form of fa_decode_paged: split size and debug traces. */
+typedef struct fa_decode_params {
+  const void* q;
+  const void* k_pages;
+  const void* v_pages;
+  const int32_t* block_table;
+  const int32_t* ctx_lens;
+  void* o;
+  float* lse;
+  int B, H, d, page_size, max_pages_per_seq, num_pages;
+  float scale;
+  int dtype;
+  void* workspace;
+  size_t workspace_bytes;
+  int pages_per_split; /* pages per split-K partial: 0 = default */
+  /* Optional int32 [B*H, max_pages_per_seq], filled with -1 by the caller: the
+   * physical page each logical page was read from. */
+  int32_t* trace_pages;
+  /* Optional int32 [B*H, ceil(max_pages_per_seq / pages_per_split), 2]: the token
+   * range [t0, t1) of every split. */
+  int32_t* trace_splits;
+} fa_decode_params;
+
+fa_status fa_decode_paged_ex(const fa_decode_params* params, fa_stream_t stream);
+
+/* Pages per split that fa_decode_paged picks for these sizes. */
+int fa_decode_default_pages_per_split(int B, int H, int max_pages_per_seq);
+
+/*
+ * fa_get_device_status - synchronise `stream`, then read and clear the device
+ * status word. Returns FA_OK, FA_ERR_BAD_PAGE or FA_ERR_TIMEOUT (FA_ERR_CUDA if the
+ * stream itself failed).
+ */
+fa_status fa_get_device_status(fa_stream_t stream);
+
+/*
+ * fa_selftest_timeout - launch one tiny kernel that waits on a pipeline barrier
+ * nothing will ever complete, with the given time limit (microseconds, 1..10^6).
+ * The wait runs out, the kernel records FA_ERR_TIMEOUT in the device status word
+ * and returns; the context stays usable. For testing the failure path.
+ */
+fa_status fa_selftest_timeout(uint32_t timeout_us, fa_stream_t stream);
+
+const char* fa_last_error_string(void);
+int fa_version(void); /* major*10000 + minor*100 + patch */
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H */

@@ -81,6 +81,10 @@ void or_decode(const void* src, double* dst, int64_t n, int dtype) {
     for (int64_t i = 0; i < n; ++i) dst[i] = or_elem(src, i, dtype);
 }
 
+static size_t elem_size(int dtype) {
+    return dtype == OR_F64 ? 8 : dtype == OR_F32 ? 4 : 2;
+}
+
 /* ------------------------------------------------------------------ */
 /* the mask                                                            */
 /* ------------------------------------------------------------------ */
@@ -142,12 +146,12 @@ int or_tile_class(int64_t mb, int64_t nb, int64_t BM, int64_t BN, int64_t Sq,
  *   P_j = exp(s_j - m) / sum_t exp(s_t - m),  O = sum_j P_j v_j,
  *   LSE = m + ln sum_t exp(s_t - m).
  * An empty list gives O = 0 and LSE = -inf.
- * kidx[t] / vidx[t] are element offsets of the t-th key / value row.
+ * krows[t] / vrows[t] point at the t-th key / value row (already decoded).
  */
-static void attend_row(const double* q, const void* k, const void* v, int dtype,
-                       const int64_t* kidx, const int64_t* vidx, int64_t n,
-                       int64_t d, double scale, double* s, double* o,
-                       double* lse, double* psum_err) {
+static void attend_row(const double* q, const double* const* krows,
+                       const double* const* vrows, int64_t n, int64_t d,
+                       double scale, double* s, double* o, double* lse,
+                       double* psum_err) {
     for (int64_t c = 0; c < d; ++c) o[c] = 0.0;
     if (n == 0) {
         *lse = -INFINITY;
@@ -157,7 +161,7 @@ static void attend_row(const double* q, const void* k, const void* v, int dtype,
     double m = -INFINITY;
     for (int64_t t = 0; t < n; ++t) {
         double dot = 0.0;
-        for (int64_t c = 0; c < d; ++c) dot += q[c] * or_elem(k, kidx[t] + c, dtype);
+        for (int64_t c = 0; c < d; ++c) dot += q[c] * krows[t][c];
         s[t] = scale * dot;
         if (s[t] > m) m = s[t];
     }
@@ -167,10 +171,15 @@ static void attend_row(const double* q, const void* k, const void* v, int dtype,
     for (int64_t t = 0; t < n; ++t) {
         double p = exp(s[t] - m) / z;
         psum += p;
-        for (int64_t c = 0; c < d; ++c) o[c] += p * or_elem(v, vidx[t] + c, dtype);
+        for (int64_t c = 0; c < d; ++c) o[c] += p * vrows[t][c];
     }
     *lse = m + log(z);
     *psum_err = fabs(1.0 - psum);
+}
+
+static int cmp_i64(const void* a, const void* b) {
+    int64_t x = *(const int64_t*)a, y = *(const int64_t*)b;
+    return (x > y) - (x < y);
 }
 
 /*
@@ -178,6 +187,7 @@ static void attend_row(const double* q, const void* k, const void* v, int dtype,
  * rows == NULL: every row; o is [B,H,Sq,d] and lse [B,H,Sq].
  * otherwise rows[r] = (b*H + h)*Sq + i and o is [nrows,d], lse [nrows].
  * max_psum_err (may be NULL) receives max over rows of |1 - sum_j P_j|.
+ * The work is split by (batch, head): each slice of K and V is decoded once.
  * Returns 0, or -1 on a bad argument.
  */
 int or_attention(const void* q, const void* k, const void* v, int dtype,
@@ -189,42 +199,72 @@ int or_attention(const void* q, const void* k, const void* v, int dtype,
     if (mask_mode < OR_MASK_NONE || mask_mode > OR_MASK_CAUSAL_WINDOW) return -1;
     if (mask_mode == OR_MASK_CAUSAL_WINDOW && (window < 1 || n_global < 0)) return -1;
     int64_t n_out = rows ? nrows : B * H * Sq;
+    /* order[r] = output index r, sorted by the row it asks for, so that the rows
+       of one (batch, head) are contiguous */
+    int64_t* order = (int64_t*)malloc(sizeof(int64_t) * 2 * (size_t)(n_out > 0 ? n_out : 1));
+    for (int64_t r = 0; r < n_out; ++r) {
+        int64_t row = rows ? rows[r] : r;
+        if (row < 0 || row >= B * H * Sq) {
+            free(order);
+            return -1;
+        }
+        order[2 * r] = row;
+        order[2 * r + 1] = r;
+    }
+    qsort(order, (size_t)n_out, 2 * sizeof(int64_t), cmp_i64);
     double worst = 0.0;
-    int bad = 0;
 #ifdef _OPENMP
     if (nthreads <= 0) nthreads = omp_get_max_threads();
-#pragma omp parallel num_threads(nthreads) reduction(max : worst) reduction(| : bad)
+#pragma omp parallel num_threads(nthreads) reduction(max : worst)
 #endif
     {
         double* qrow = (double*)malloc(sizeof(double) * (size_t)d);
+        size_t skd = (size_t)(Sk > 0 ? Sk : 1) * (size_t)d;
+        double* kd = (double*)malloc(sizeof(double) * skd);
+        double* vd = (double*)malloc(sizeof(double) * skd);
         double* s = (double*)malloc(sizeof(double) * (size_t)(Sk > 0 ? Sk : 1));
-        int64_t* kidx = (int64_t*)malloc(sizeof(int64_t) * (size_t)(Sk > 0 ? Sk : 1));
+        const double** kr = (const double**)malloc(sizeof(double*) * (size_t)(Sk > 0 ? Sk : 1));
+        const double** vr = (const double**)malloc(sizeof(double*) * (size_t)(Sk > 0 ? Sk : 1));
 #ifdef _OPENMP
-#pragma omp for schedule(dynamic, 16)
+#pragma omp for schedule(dynamic, 1)
 #endif
-        for (int64_t r = 0; r < n_out; ++r) {
-            int64_t row = rows ? rows[r] : r;
-            if (row < 0 || row >= B * H * Sq) {
-                bad = 1;
-                continue;
+        for (int64_t bh = 0; bh < B * H; ++bh) {
+            /* the output rows that belong to this (batch, head) */
+            int64_t lo = 0, hi = n_out;
+            while (lo < hi) {
+                int64_t mid = (lo + hi) / 2;
+                if (order[2 * mid] < bh * Sq) lo = mid + 1; else hi = mid;
             }
-            int64_t bh = row / Sq, i = row % Sq;
-            for (int64_t c = 0; c < d; ++c) qrow[c] = or_elem(q, row * d + c, dtype);
-            int64_t n = 0;
-            for (int64_t j = 0; j < Sk; ++j)
-                if (or_visible(i, j, Sq, Sk, mask_mode, window, n_global))
-                    kidx[n++] = (bh * Sk + j) * d;
-            double err;
-            attend_row(qrow, k, v, dtype, kidx, kidx, n, d, scale, s, o + r * d,
-                       lse + r, &err);
-            if (err > worst) worst = err;
+            int64_t first = lo;
+            if (first >= n_out || order[2 * first] >= (bh + 1) * Sq) continue;
+            or_decode((const char*)k + (size_t)(bh * Sk * d) * elem_size(dtype), kd, Sk * d, dtype);
+            or_decode((const char*)v + (size_t)(bh * Sk * d) * elem_size(dtype), vd, Sk * d, dtype);
+            for (int64_t r = first; r < n_out && order[2 * r] < (bh + 1) * Sq; ++r) {
+                int64_t row = order[2 * r], out = order[2 * r + 1];
+                int64_t i = row - bh * Sq;
+                for (int64_t c = 0; c < d; ++c) qrow[c] = or_elem(q, row * d + c, dtype);
+                int64_t n = 0;
+                for (int64_t j = 0; j < Sk; ++j)
+                    if (or_visible(i, j, Sq, Sk, mask_mode, window, n_global)) {
+                        kr[n] = kd + j * d;
+                        vr[n] = vd + j * d;
+                        ++n;
+                    }
+                double err;
+                attend_row(qrow, kr, vr, n, d, scale, s, o + out * d, lse + out, &err);
+                if (err > worst) worst = err;
+            }
         }
         free(qrow);
+        free(kd);
+        free(vd);
         free(s);
-        free(kidx);
+        free(kr);
+        free(vr);
     }
+    free(order);
     if (max_psum_err) *max_psum_err = worst;
-    return bad ? -1 : 0;
+    return 0;
 }
 
 /* ------------------------------------------------------------------ */
@@ -370,9 +410,13 @@ int or_decode_paged(const void* q, const void* k_pages, const void* v_pages,
 #pragma omp parallel num_threads(nthreads) reduction(| : bad)
 #endif
     {
+        size_t cap = (size_t)(max_ctx > 0 ? max_ctx : 1);
         double* qrow = (double*)malloc(sizeof(double) * (size_t)d);
-        double* s = (double*)malloc(sizeof(double) * (size_t)(max_ctx > 0 ? max_ctx : 1));
-        int64_t* idx = (int64_t*)malloc(sizeof(int64_t) * (size_t)(max_ctx > 0 ? max_ctx : 1));
+        double* s = (double*)malloc(sizeof(double) * cap);
+        double* kd = (double*)malloc(sizeof(double) * cap * (size_t)d);
+        double* vd = (double*)malloc(sizeof(double) * cap * (size_t)d);
+        const double** kr = (const double**)malloc(sizeof(double*) * cap);
+        const double** vr = (const double**)malloc(sizeof(double*) * cap);
 #ifdef _OPENMP
 #pragma omp for schedule(dynamic, 1)
 #endif
@@ -388,7 +432,7 @@ int or_decode_paged(const void* q, const void* k_pages, const void* v_pages,
                 bad = 1;
                 continue;
             }
-            /* gather: the element offset of token t's row for head h */
+            /* gather: token t of sequence b, head h, into row t of kd / vd */
             int64_t n = 0;
             for (int64_t t = 0; t < ctx; ++t) {
                 int64_t page = block_table[b * max_pages_per_seq + t / page_size];
@@ -396,17 +440,26 @@ int or_decode_paged(const void* q, const void* k_pages, const void* v_pages,
                     bad = 1;
                     break;
                 }
-                idx[n++] = ((page * H + h) * page_size + t % page_size) * d;
+                int64_t src = ((page * H + h) * page_size + t % page_size) * d;
+                for (int64_t c = 0; c < d; ++c) {
+                    kd[t * d + c] = or_elem(k_pages, src + c, dtype);
+                    vd[t * d + c] = or_elem(v_pages, src + c, dtype);
+                }
+                kr[n] = kd + t * d;
+                vr[n] = vd + t * d;
+                ++n;
             }
             if (n != ctx) continue;
             for (int64_t c = 0; c < d; ++c) qrow[c] = or_elem(q, bh * d + c, dtype);
             double err;
-            attend_row(qrow, k_pages, v_pages, dtype, idx, idx, n, d, scale, s,
-                       o + r * d, lse + r, &err);
+            attend_row(qrow, kr, vr, n, d, scale, s, o + r * d, lse + r, &err);
         }
         free(qrow);
         free(s);
-        free(idx);
+        free(kd);
+        free(vd);
+        free(kr);
+        free(vr);
     }
     return bad ? -1 : 0;
 }

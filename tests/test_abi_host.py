@@ -1,0 +1,163 @@
+"""Host-side checks of the C-ABI library that need no GPU: it builds, loads, exports
+every function include/fa.h declares, its parameter structs match the binding's
+layout, and it rejects bad arguments before touching CUDA."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import tiled_attention_06_gb300 as fa
+from tiled_attention_06_gb300 import build as fa_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fa.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    fa_build.build()
+    return fa.lib()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fa_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_exports_every_declared_function(L):
+    names = _declared_functions()
+    assert "fa_fwd" in names and "fa_decode_paged" in names
+    out = subprocess.run(["nm", "-D", "--defined-only", fa.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\s[TW]\s+(\w+)$", out, flags=re.M))
+    missing = [n for n in names if n not in exported]
+    assert not missing, missing
+    for n in names:
+        getattr(L, n)
+
+
+def test_struct_layouts_match_header(tmp_path):
+    src = tmp_path / "layout.c"
+    fields = {"fa_fwd_params": [f for f, _ in fa.FwdParams._fields_],
+              "fa_decode_params": [f for f, _ in fa.DecodeParams._fields_]}
+    lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "fa.h"', "int main(void){"]
+    for st, fs in fields.items():
+        lines.append(f'printf("{st} %zu\\n", sizeof({st}));')
+        for f in fs:
+            lines.append(f'printf("{st}.{f} %zu\\n", offsetof({st}, {f}));')
+    lines.append("return 0;}")
+    src.write_text("\n".join(lines))
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)],
+                   check=True)
+    got = dict(l.split() for l in subprocess.run([str(exe)], capture_output=True, text=True,
+                                                 check=True).stdout.splitlines())
+    for st, cls in (("fa_fwd_params", fa.FwdParams), ("fa_decode_params", fa.DecodeParams)):
+        assert int(got[st]) == ctypes.sizeof(cls)
+        for f, _ in cls._fields_:
+            assert int(got[f"{st}.{f}"]) == getattr(cls, f).offset, (st, f)
+
+
+def test_version_and_block_m(L):
+    assert L.fa_version() >= 100
+    assert L.fa_fwd_block_m() == 128
+
+
+def test_workspace_size_and_split_rule(L):
+    assert L.fa_decode_workspace_size(32, 32, 128, 32, 256) == 32 * 32 * 32 * 130 * 4
+    assert L.fa_decode_workspace_size(0, 32, 128, 32, 256) == 0
+    for B, H, mp in [(32, 32, 32), (1, 1, 1), (4, 8, 100), (64, 64, 64)]:
+        pps = L.fa_decode_default_pages_per_split(B, H, mp)
+        assert 1 <= pps <= max(1, mp)
+
+
+A = 0x10000  # a 16-byte aligned fake device address: validation never dereferences it
+
+
+def _fwd(L, **kw):
+    args = dict(q=A, k=A, v=A, o=A, lse=None, B=1, H=1, Sq=4, Sk=4, d=64, scale=0.125,
+                mask_mode=0, window=0, n_global=0, dtype=0)
+    args.update(kw)
+    return L.fa_fwd(args["q"], args["k"], args["v"], args["o"], args["lse"], args["B"],
+                    args["H"], args["Sq"], args["Sk"], args["d"], args["scale"],
+                    args["mask_mode"], args["window"], args["n_global"], args["dtype"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), fa.FA_ERR_INVALID_ARG),
+    (dict(o=None), fa.FA_ERR_INVALID_ARG),
+    (dict(k=A + 8), fa.FA_ERR_INVALID_ARG),
+    (dict(lse=A + 2), fa.FA_ERR_INVALID_ARG),
+    (dict(B=0), fa.FA_ERR_INVALID_ARG),
+    (dict(Sq=-1), fa.FA_ERR_INVALID_ARG),
+    (dict(d=96), fa.FA_ERR_UNSUPPORTED),
+    (dict(d=256), fa.FA_ERR_UNSUPPORTED),
+    (dict(dtype=2), fa.FA_ERR_UNSUPPORTED),
+    (dict(mask_mode=3), fa.FA_ERR_INVALID_ARG),
+    (dict(mask_mode=2, window=0), fa.FA_ERR_INVALID_ARG),
+    (dict(mask_mode=2, window=4, n_global=-1), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), fa.FA_ERR_INVALID_ARG),
+    (dict(B=1 << 20, H=1 << 20), fa.FA_ERR_INVALID_ARG),
+])
+def test_fwd_rejects_bad_arguments(L, kw, code):
+    assert _fwd(L, **kw) == code
+    assert fa.fa_last_error_string() != ""
+
+
+def test_fwd_empty_query_is_a_no_op(L):
+    assert _fwd(L, Sq=0) == fa.FA_OK
+
+
+def test_fwd_ex_rejects_bad_plan(L):
+    p = fa.FwdParams(A, A, A, A, None, 1, 1, 4, 4, 64, 0.125, 0, 0, 0, 0, 96, 0, 0, 0, None)
+    assert L.fa_fwd_ex(ctypes.byref(p), None) == fa.FA_ERR_UNSUPPORTED
+    assert L.fa_fwd_ex(None, None) == fa.FA_ERR_INVALID_ARG
+
+
+def _dec(L, **kw):
+    args = dict(q=A, kp=A, vp=A, bt=A, cl=A, o=A, lse=None, B=2, H=2, d=128, page=256, mp=4,
+                np_=8, scale=0.1, dtype=0, ws=A, wsb=1 << 20)
+    args.update(kw)
+    return L.fa_decode_paged(args["q"], args["kp"], args["vp"], args["bt"], args["cl"], args["o"],
+                             args["lse"], args["B"], args["H"], args["d"], args["page"],
+                             args["mp"], args["np_"], args["scale"], args["dtype"], args["ws"],
+                             args["wsb"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(bt=None), fa.FA_ERR_INVALID_ARG),
+    (dict(ws=None), fa.FA_ERR_INVALID_ARG),
+    (dict(q=A + 4), fa.FA_ERR_INVALID_ARG),
+    (dict(bt=A + 2), fa.FA_ERR_INVALID_ARG),
+    (dict(B=0), fa.FA_ERR_INVALID_ARG),
+    (dict(np_=0), fa.FA_ERR_INVALID_ARG),
+    (dict(d=80), fa.FA_ERR_UNSUPPORTED),
+    (dict(page=100), fa.FA_ERR_UNSUPPORTED),
+    (dict(page=8), fa.FA_ERR_UNSUPPORTED),
+    (dict(dtype=5), fa.FA_ERR_UNSUPPORTED),
+    (dict(wsb=16), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=float("inf")), fa.FA_ERR_INVALID_ARG),
+])
+def test_decode_rejects_bad_arguments(L, kw, code):
+    assert _dec(L, **kw) == code
+
+
+def test_decode_ex_rejects_bad_split(L):
+    p = fa.DecodeParams(A, A, A, A, A, A, None, 2, 2, 128, 256, 4, 8, 0.1, 0, A, 1 << 20, 5,
+                        None, None)
+    assert L.fa_decode_paged_ex(ctypes.byref(p), None) == fa.FA_ERR_INVALID_ARG
+
+
+def test_selftest_rejects_bad_limit(L):
+    assert L.fa_selftest_timeout(0, None) == fa.FA_ERR_INVALID_ARG
+    assert L.fa_selftest_timeout(2_000_000, None) == fa.FA_ERR_INVALID_ARG
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(fa, "_lib", None)
+    monkeypatch.setattr(fa, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(fa.FaError):
+        fa.lib()

@@ -1,0 +1,184 @@
+"""GPU parity of fa_fwd (through the C ABI) against the FP64 CPU oracle."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import tiled_attention_06_gb300 as fa
+from tiled_attention_06_gb300 import inputs
+
+from _util import compare, pick_rows, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+DT = {"f16": torch.float16, "bf16": torch.bfloat16}
+MASKS = {"none": (fa.FA_MASK_NONE, 0, 0), "causal": (fa.FA_MASK_CAUSAL, 0, 0)}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from tiled_attention_06_gb300 import build
+    build.build()
+    fa.lib()
+
+
+def run_fwd(q, k, v, scale, mode, window=0, n_global=0, **ex):
+    dev = torch.device("cuda")
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    o = torch.empty_like(qd)
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+    if ex:
+        fa.fa_fwd_ex(qd, kd, vd, o, lse, scale, mode, window, n_global, **ex)
+    else:
+        fa.fa_fwd(qd, kd, vd, o, lse, scale, mode, window, n_global)
+    torch.cuda.synchronize()
+    assert fa.fa_get_device_status() == fa.FA_OK
+    return o, lse
+
+
+def test_tiny_noncausal_config():
+    """B=1, H=2, Sq=Sk=128, d=64, fp16, N(0,1), scale 1/sqrt(d); O[1,2,128,64] plus LSE."""
+    q, k, v = inputs.prefill_inputs(1, 2, 128, 128, 64, torch.float16, seed=0)
+    o, lse = run_fwd(q, k, v, 1 / 8, fa.FA_MASK_NONE)
+    assert o.shape == (1, 2, 128, 64)
+    ref_o, ref_l = oracle.attention(q, k, v, 1 / 8, oracle.MASK_NONE)
+    compare(o, lse, ref_o, ref_l, "tiny")
+
+
+SHAPES = [(1, 1), (63, 63), (65, 65), (127, 129), (129, 127), (200, 333), (257, 64), (64, 257),
+          (384, 384)]
+
+
+@pytest.mark.parametrize("Sq,Sk", SHAPES)
+@pytest.mark.parametrize("d,dt", [(64, "f16"), (128, "bf16"), (128, "f16")])
+@pytest.mark.parametrize("mask", ["none", "causal", "window"])
+@pytest.mark.parametrize("bn", [64, 128])
+def test_small_shapes(Sq, Sk, d, dt, mask, bn):
+    q, k, v = inputs.prefill_inputs(2, 3, Sq, Sk, d, DT[dt], seed=Sq * 1000 + Sk)
+    if mask == "window":
+        mode, w, g = fa.FA_MASK_CAUSAL_WINDOW, 50, 5
+    else:
+        mode, w, g = MASKS[mask]
+    scale = 1 / math.sqrt(d)
+    o, lse = run_fwd(q, k, v, scale, mode, w, g, block_n=bn)
+    ref_o, ref_l = oracle.attention(q, k, v, scale, mode, w, g)
+    compare(o, lse, ref_o, ref_l, f"{Sq}x{Sk} d{d} {dt} {mask} bn{bn}")
+
+
+@pytest.mark.parametrize("mask,w,g", [("causal", 0, 0), ("window", 200, 70), ("window", 1, 0),
+                                      ("window", 129, 300), ("none", 0, 0)])
+@pytest.mark.parametrize("Sq,Sk,bn", [(1000, 1000, 128), (700, 1100, 64), (1100, 700, 128)])
+def test_tile_trace_is_bit_exact(mask, w, g, Sq, Sk, bn):
+    """The tiles the kernel visits, and the class it gives each, equal the oracle's
+    brute-force tile classification; no tile is visited twice."""
+    mode = {"none": fa.FA_MASK_NONE, "causal": fa.FA_MASK_CAUSAL,
+            "window": fa.FA_MASK_CAUSAL_WINDOW}[mask]
+    B, H, d = 1, 2, 64
+    q, k, v = inputs.prefill_inputs(B, H, Sq, Sk, d, torch.float16, seed=3)
+    BM = fa.fa_fwd_block_m()
+    nmb, nnb = -(-Sq // BM), -(-Sk // bn)
+    trace = torch.zeros(B * H * nmb * nnb, dtype=torch.int32, device="cuda")
+    o, lse = run_fwd(q, k, v, 0.125, mode, w, g, block_n=bn, trace=trace)
+    got = trace.cpu().numpy().reshape(B * H, nmb, nnb)
+    want = np.zeros((nmb, nnb), dtype=np.int32)
+    for mb in range(nmb):
+        for nb in range(nnb):
+            c = oracle.tile_class(mb, nb, BM, bn, Sq, Sk, mode, w, g)
+            want[mb, nb] = 0 if c == oracle.TILE_EMPTY else 16 + c
+    for bh in range(B * H):
+        assert np.array_equal(got[bh], want), f"bh {bh}"
+    ref_o, ref_l = oracle.attention(q, k, v, 0.125, mode, w, g)
+    compare(o, lse, ref_o, ref_l, "trace case")
+
+
+def test_guard_regions_untouched_and_outputs_finite():
+    """Inputs and outputs live inside NaN-filled buffers; the call must read no NaN
+    (outputs finite) and write nothing outside o and lse."""
+    B, H, S, d = 2, 2, 300, 128
+    q, k, v = inputs.prefill_inputs(B, H, S, S, d, torch.bfloat16, seed=5)
+    G = 4096
+    dev = "cuda"
+
+    def guarded(t):
+        buf = torch.full((t.numel() + 2 * G,), float("nan"), dtype=t.dtype, device=dev)
+        buf[G:G + t.numel()] = t.reshape(-1).to(dev)
+        return buf, buf[G:G + t.numel()].view(t.shape)
+
+    (bq, qd), (bk, kd), (bv, vd) = guarded(q), guarded(k), guarded(v)
+    bo = torch.full((q.numel() + 2 * G,), float("nan"), dtype=q.dtype, device=dev)
+    od = bo[G:G + q.numel()].view(q.shape)
+    bl = torch.full((B * H * S + 2 * G,), float("nan"), dtype=torch.float32, device=dev)
+    ld = bl[G:G + B * H * S].view(B, H, S)
+    for mode in (fa.FA_MASK_NONE, fa.FA_MASK_CAUSAL, fa.FA_MASK_CAUSAL_WINDOW):
+        fa.fa_fwd(qd, kd, vd, od, ld, 1 / math.sqrt(d), mode, 77, 3)
+        torch.cuda.synchronize()
+        assert torch.isfinite(od.float()).all() and torch.isfinite(ld).all()
+        for buf in (bo, bl):
+            assert torch.isnan(buf[:G].float()).all() and torch.isnan(buf[-G:].float()).all()
+        ref_o, ref_l = oracle.attention(q, k, v, 1 / math.sqrt(d), mode, 77, 3)
+        compare(od, ld, ref_o, ref_l, f"guarded mode {mode}")
+
+
+def test_empty_and_fully_masked():
+    # Sk = 0: every row sees nothing
+    q, k, v = inputs.prefill_inputs(1, 2, 70, 0, 64, torch.float16, seed=7)
+    o, lse = run_fwd(q, k.reshape(1, 2, 0, 64), v.reshape(1, 2, 0, 64), 0.125, fa.FA_MASK_NONE)
+    assert torch.all(o == 0) and torch.all(torch.isneginf(lse))
+    # Sq > Sk under a causal mask: the first Sq-Sk rows see nothing
+    q, k, v = inputs.prefill_inputs(1, 2, 300, 100, 64, torch.float16, seed=8)
+    o, lse = run_fwd(q, k, v, 0.125, fa.FA_MASK_CAUSAL)
+    ref_o, ref_l = oracle.attention(q, k, v, 0.125, oracle.MASK_CAUSAL)
+    compare(o, lse, ref_o, ref_l, "Sq>Sk causal")
+    # Sq = 0: nothing to do, nothing written
+    q = torch.empty(1, 2, 0, 64, dtype=torch.float16)
+    k = torch.randn(1, 2, 5, 64).half()
+    o, lse = run_fwd(q, k, k, 0.125, fa.FA_MASK_CAUSAL)
+    assert o.numel() == 0
+
+
+def test_schedule_does_not_change_results():
+    """Every work item is computed the same way whatever CTA runs it: outputs are
+    bit-identical for any persistent grid size and head grouping."""
+    q, k, v = inputs.prefill_inputs(2, 5, 700, 700, 128, torch.bfloat16, seed=9)
+    o0, l0 = run_fwd(q, k, v, 0.088, fa.FA_MASK_CAUSAL)
+    for ctas, hg in [(1, 1), (7, 3), (37, 0), (1000, 10)]:
+        o1, l1 = run_fwd(q, k, v, 0.088, fa.FA_MASK_CAUSAL, num_ctas=ctas, group_heads=hg)
+        assert torch.equal(o0, o1) and torch.equal(l0, l1)
+
+
+def test_causal_2k_fp16_full():
+    """B=4, H=32, Sq=Sk=2048, d=128, fp16, causal, N(0,1)*0.5, scale 1/sqrt(128): every row."""
+    q, k, v = inputs.prefill_inputs(4, 32, 2048, 2048, 128, torch.float16, factor=0.5, seed=0)
+    scale = 1 / math.sqrt(128)
+    o, lse = run_fwd(q, k, v, scale, fa.FA_MASK_CAUSAL)
+    ref_o, ref_l = oracle.attention(q, k, v, scale, oracle.MASK_CAUSAL)
+    compare(o, lse, ref_o, ref_l, "causal 2k")
+
+
+@pytest.mark.parametrize("mode", [fa.FA_MASK_CAUSAL, fa.FA_MASK_NONE])
+def test_long_4k_bf16_sampled(mode):
+    """B=4, H=32, Sq=Sk=4096, d=128, bf16, N(0,1), causal and non-causal; the oracle
+    checks the first and last query block of every head and 256 random rows."""
+    B, H, S, d = 4, 32, 4096, 128
+    q, k, v = inputs.prefill_inputs(B, H, S, S, d, torch.bfloat16, seed=0)
+    scale = 1 / math.sqrt(d)
+    o, lse = run_fwd(q, k, v, scale, mode)
+    rows = sample_rows(B, H, S, fa.fa_fwd_block_m(), n_random=256, seed=1)
+    ref_o, ref_l = oracle.attention(q, k, v, scale, mode, rows=rows)
+    compare(pick_rows(o, rows, S), pick_rows(lse, rows, S), ref_o, ref_l, f"4k mode {mode}")
+
+
+def test_sliding_window_32k_sampled():
+    """B=1, H=32, S=32768, d=128, bf16, causal window 2048 + 64 global keys; sampled rows
+    include the window and global-token edges."""
+    B, H, S, d = 1, 32, 32768, 128
+    q, k, v = inputs.prefill_inputs(B, H, S, S, d, torch.bfloat16, seed=0)
+    scale = 1 / math.sqrt(d)
+    o, lse = run_fwd(q, k, v, scale, fa.FA_MASK_CAUSAL_WINDOW, 2048, 64)
+    rows = sample_rows(B, H, S, fa.fa_fwd_block_m(), n_random=256, extra=range(2040, 2121),
+                       seed=2)
+    ref_o, ref_l = oracle.attention(q, k, v, scale, oracle.MASK_CAUSAL_WINDOW, 2048, 64,
+                                    rows=rows)
+    compare(pick_rows(o, rows, S), pick_rows(lse, rows, S), ref_o, ref_l, "window 32k")

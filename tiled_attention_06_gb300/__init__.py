@@ -1,1 +1,213 @@
-"""FlashAttention forward (prefill + paged decode) for GB300."""
+"""FlashAttention forward (prefill + paged decode) for one NVIDIA GB300 (sm_103a).
+
+A thin ctypes binding over the C-ABI library ``libfa.so`` (declared in
+``include/fa.h``). The functions keep the C names; they only marshal torch
+tensors into pointers, sizes and the current CUDA stream. Every step of the
+computation runs in the library's CUDA kernels: there is no fallback, and a
+missing library raises ``FaError``.
+"""
+import ctypes
+import os
+
+import torch
+
+__all__ = [
+    "FaError", "lib", "fa_fwd", "fa_fwd_ex", "fa_decode_paged", "fa_decode_paged_ex",
+    "fa_decode_workspace_size", "fa_decode_default_pages_per_split", "fa_get_device_status",
+    "fa_selftest_timeout", "fa_last_error_string", "fa_version", "fa_fwd_block_m",
+    "FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_CUDA", "FA_ERR_TIMEOUT",
+    "FA_ERR_BAD_PAGE", "FA_F16", "FA_BF16", "FA_MASK_NONE", "FA_MASK_CAUSAL",
+    "FA_MASK_CAUSAL_WINDOW",
+]
+
+FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT, FA_ERR_BAD_PAGE = range(6)
+FA_F16, FA_BF16 = 0, 1
+FA_MASK_NONE, FA_MASK_CAUSAL, FA_MASK_CAUSAL_WINDOW = 0, 1, 2
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libfa.so")
+
+_vp = ctypes.c_void_p
+_i = ctypes.c_int
+_f = ctypes.c_float
+_u32 = ctypes.c_uint32
+_sz = ctypes.c_size_t
+
+
+class FaError(RuntimeError):
+    def __init__(self, status, msg):
+        super().__init__(f"fa status {status}: {msg}")
+        self.status = status
+
+
+class FwdParams(ctypes.Structure):
+    _fields_ = [("q", _vp), ("k", _vp), ("v", _vp), ("o", _vp), ("lse", _vp),
+                ("B", _i), ("H", _i), ("Sq", _i), ("Sk", _i), ("d", _i), ("scale", _f),
+                ("mask_mode", _i), ("window", _i), ("n_global", _i), ("dtype", _i),
+                ("block_n", _i), ("num_ctas", _i), ("group_heads", _i), ("timeout_us", _u32),
+                ("trace", _vp)]
+
+
+class DecodeParams(ctypes.Structure):
+    _fields_ = [("q", _vp), ("k_pages", _vp), ("v_pages", _vp), ("block_table", _vp),
+                ("ctx_lens", _vp), ("o", _vp), ("lse", _vp), ("B", _i), ("H", _i), ("d", _i),
+                ("page_size", _i), ("max_pages_per_seq", _i), ("num_pages", _i), ("scale", _f),
+                ("dtype", _i), ("workspace", _vp), ("workspace_bytes", _sz),
+                ("pages_per_split", _i), ("trace_pages", _vp), ("trace_splits", _vp)]
+
+
+_lib = None
+
+
+def lib():
+    """The loaded libfa.so (raises FaError when it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise FaError(FA_ERR_CUDA, f"{LIB_PATH} is missing: build it with "
+                          "tiled_attention_06_gb300.build.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        L.fa_fwd.restype = _i
+        L.fa_fwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _i, _i, _i, _vp]
+        L.fa_fwd_ex.restype = _i
+        L.fa_fwd_ex.argtypes = [ctypes.POINTER(FwdParams), _vp]
+        L.fa_fwd_block_m.restype = _i
+        L.fa_fwd_block_m.argtypes = []
+        L.fa_decode_paged.restype = _i
+        L.fa_decode_paged.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i,
+                                      _f, _i, _vp, _sz, _vp]
+        L.fa_decode_paged_ex.restype = _i
+        L.fa_decode_paged_ex.argtypes = [ctypes.POINTER(DecodeParams), _vp]
+        L.fa_decode_workspace_size.restype = _sz
+        L.fa_decode_workspace_size.argtypes = [_i, _i, _i, _i, _i]
+        L.fa_decode_default_pages_per_split.restype = _i
+        L.fa_decode_default_pages_per_split.argtypes = [_i, _i, _i]
+        L.fa_get_device_status.restype = _i
+        L.fa_get_device_status.argtypes = [_vp]
+        L.fa_selftest_timeout.restype = _i
+        L.fa_selftest_timeout.argtypes = [_u32, _vp]
+        L.fa_last_error_string.restype = ctypes.c_char_p
+        L.fa_last_error_string.argtypes = []
+        L.fa_version.restype = _i
+        L.fa_version.argtypes = []
+        _lib = L
+    return _lib
+
+
+def _check(status):
+    if status != FA_OK:
+        raise FaError(status, fa_last_error_string())
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _dtype_code(t):
+    if t.dtype == torch.float16:
+        return FA_F16
+    if t.dtype == torch.bfloat16:
+        return FA_BF16
+    raise FaError(FA_ERR_UNSUPPORTED, f"dtype {t.dtype} (float16 or bfloat16)")
+
+
+def _need_cuda_contig(**ts):
+    for name, t in ts.items():
+        if t is None:
+            continue
+        if not t.is_cuda:
+            raise FaError(FA_ERR_INVALID_ARG, f"{name} must be a CUDA tensor")
+        if not t.is_contiguous():
+            raise FaError(FA_ERR_INVALID_ARG, f"{name} must be contiguous")
+
+
+def fa_last_error_string():
+    return lib().fa_last_error_string().decode()
+
+
+def fa_version():
+    return lib().fa_version()
+
+
+def fa_fwd_block_m():
+    return lib().fa_fwd_block_m()
+
+
+def fa_fwd(q, k, v, o, lse, scale, mask_mode=FA_MASK_NONE, window=0, n_global=0, stream=None):
+    """O = softmax(scale Q K^T + mask) V into `o` (and LSE into `lse`, may be None).
+
+    q [B,H,Sq,d], k/v [B,H,Sk,d], o like q, lse float32 [B,H,Sq]; CUDA, contiguous.
+    """
+    _need_cuda_contig(q=q, k=k, v=v, o=o, lse=lse)
+    B, H, Sq, d = q.shape
+    Sk = k.shape[2]
+    _check(lib().fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), _ptr(lse), B, H,
+                        Sq, Sk, d, float(scale), mask_mode, window, n_global, _dtype_code(q),
+                        _stream(stream)))
+
+
+def fa_fwd_ex(q, k, v, o, lse, scale, mask_mode=FA_MASK_NONE, window=0, n_global=0,
+              block_n=0, num_ctas=0, group_heads=0, timeout_us=0, trace=None, stream=None):
+    _need_cuda_contig(q=q, k=k, v=v, o=o, lse=lse, trace=trace)
+    B, H, Sq, d = q.shape
+    p = FwdParams(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), _ptr(lse), B, H, Sq,
+                  k.shape[2], d, float(scale), mask_mode, window, n_global, _dtype_code(q),
+                  block_n, num_ctas, group_heads, timeout_us, _ptr(trace))
+    _check(lib().fa_fwd_ex(ctypes.byref(p), _stream(stream)))
+
+
+def fa_decode_workspace_size(B, H, d, max_pages_per_seq, page_size):
+    return lib().fa_decode_workspace_size(B, H, d, max_pages_per_seq, page_size)
+
+
+def fa_decode_default_pages_per_split(B, H, max_pages_per_seq):
+    return lib().fa_decode_default_pages_per_split(B, H, max_pages_per_seq)
+
+
+def fa_decode_paged(q, k_pages, v_pages, block_table, ctx_lens, o, lse, scale, workspace,
+                    stream=None):
+    """One query token per sequence against a paged KV cache.
+
+    q/o [B,H,d]; pools [num_pages,H,page_size,d]; block_table int32 [B,max_pages];
+    ctx_lens int32 [B]; lse float32 [B,H] or None; workspace a CUDA byte tensor.
+    """
+    _need_cuda_contig(q=q, k_pages=k_pages, v_pages=v_pages, block_table=block_table,
+                      ctx_lens=ctx_lens, o=o, lse=lse, workspace=workspace)
+    B, H, d = q.shape
+    P, _, page, _ = k_pages.shape
+    _check(lib().fa_decode_paged(q.data_ptr(), k_pages.data_ptr(), v_pages.data_ptr(),
+                                 block_table.data_ptr(), ctx_lens.data_ptr(), o.data_ptr(),
+                                 _ptr(lse), B, H, d, page, block_table.shape[1], P, float(scale),
+                                 _dtype_code(q), workspace.data_ptr(),
+                                 workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def fa_decode_paged_ex(q, k_pages, v_pages, block_table, ctx_lens, o, lse, scale, workspace,
+                       pages_per_split=0, trace_pages=None, trace_splits=None, stream=None):
+    _need_cuda_contig(q=q, k_pages=k_pages, v_pages=v_pages, block_table=block_table,
+                      ctx_lens=ctx_lens, o=o, lse=lse, workspace=workspace,
+                      trace_pages=trace_pages, trace_splits=trace_splits)
+    B, H, d = q.shape
+    P, _, page, _ = k_pages.shape
+    p = DecodeParams(q.data_ptr(), k_pages.data_ptr(), v_pages.data_ptr(), block_table.data_ptr(),
+                     ctx_lens.data_ptr(), o.data_ptr(), _ptr(lse), B, H, d, page,
+                     block_table.shape[1], P, float(scale), _dtype_code(q), workspace.data_ptr(),
+                     workspace.numel() * workspace.element_size(), pages_per_split,
+                     _ptr(trace_pages), _ptr(trace_splits))
+    _check(lib().fa_decode_paged_ex(ctypes.byref(p), _stream(stream)))
+
+
+def fa_get_device_status(stream=None):
+    """Synchronise the stream, read and clear the device status word; returns the code."""
+    return lib().fa_get_device_status(_stream(stream))
+
+
+def fa_selftest_timeout(timeout_us, stream=None):
+    _check(lib().fa_selftest_timeout(timeout_us, _stream(stream)))

@@ -1,0 +1,349 @@
+// The C ABI (include/fa.h): argument validation, launch planning, TMA tensor-map
+// encoding and the device status word. Every check here runs on the host before
+// anything is launched; a rejected call launches nothing.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "fa.h"
+#include "fa_internal.h"
+
+namespace {
+
+__device__ uint32_t g_status_word;
+
+thread_local std::string t_last_error = "no error";
+
+fa_status fail(fa_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  t_last_error = buf;
+  return s;
+}
+
+fa_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(FA_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+  bool ready = false;
+  int sms = 0;
+  uint32_t* status = nullptr;
+};
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+
+// Per-device facts, looked up once per device with that device current.
+fa_status device_info(DeviceInfo* out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(FA_ERR_UNSUPPORTED, "device index %d", dev);
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.ready) {
+    e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_status_word);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(status)");
+    d.status = static_cast<uint32_t*>(p);
+    d.ready = true;
+  }
+  *out = d;
+  return FA_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// A [BH, S, D] tensor of 16-bit elements as a 3-D TMA map with 128-byte swizzle;
+// one box is 64 elements of d by `rows` rows of one (batch, head).
+fa_status make_map(CUtensorMap* m, const void* ptr, bool bf16, int D, int S, int BH, int rows) {
+  auto enc = encode_fn();
+  if (!enc) return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(S > 0 ? S : 1),
+                              static_cast<cuuint64_t>(BH)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2,
+                                 static_cast<cuuint64_t>(S > 0 ? S : 1) * D * 2};
+  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(rows), 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+                   const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return FA_OK;
+}
+
+fa_status check_fwd(const fa_fwd_params& p) {
+  // q and o may be null only when Sq == 0, k and v only when Sk == 0
+  if ((p.Sq > 0 && (!p.q || !p.o)) || (p.Sk > 0 && (!p.k || !p.v)))
+    return fail(FA_ERR_INVALID_ARG, "q, k, v and o must be non-null");
+  if (!aligned16(p.q) || !aligned16(p.k) || !aligned16(p.v) || !aligned16(p.o))
+    return fail(FA_ERR_INVALID_ARG, "q, k, v and o must be 16-byte aligned");
+  if (p.lse && !aligned4(p.lse)) return fail(FA_ERR_INVALID_ARG, "lse must be 4-byte aligned");
+  if (p.B < 1 || p.H < 1 || p.Sq < 0 || p.Sk < 0)
+    return fail(FA_ERR_INVALID_ARG, "need B >= 1, H >= 1, Sq >= 0, Sk >= 0 (got %d %d %d %d)", p.B,
+                p.H, p.Sq, p.Sk);
+  if (p.d != 64 && p.d != 128) return fail(FA_ERR_UNSUPPORTED, "head dim %d (supported: 64, 128)", p.d);
+  if (p.dtype != FA_F16 && p.dtype != FA_BF16) return fail(FA_ERR_UNSUPPORTED, "dtype %d", p.dtype);
+  if (!std::isfinite(p.scale)) return fail(FA_ERR_INVALID_ARG, "scale must be finite");
+  if (p.mask_mode < FA_MASK_NONE || p.mask_mode > FA_MASK_CAUSAL_WINDOW)
+    return fail(FA_ERR_INVALID_ARG, "mask_mode %d", p.mask_mode);
+  if (p.mask_mode == FA_MASK_CAUSAL_WINDOW && (p.window < 1 || p.n_global < 0))
+    return fail(FA_ERR_INVALID_ARG, "CAUSAL_WINDOW needs window >= 1 and n_global >= 0");
+  const long long BH = static_cast<long long>(p.B) * p.H;
+  const long long S = p.Sq > p.Sk ? p.Sq : p.Sk;
+  if (BH > (1LL << 30) || S > (1LL << 30) || BH * ((S + 63) / 64) > (1LL << 31) - 1)
+    return fail(FA_ERR_INVALID_ARG, "problem too large for 32-bit tile indices");
+  if (p.block_n != 0 && p.block_n != 64 && p.block_n != 128)
+    return fail(FA_ERR_UNSUPPORTED, "block_n %d (supported: 64, 128)", p.block_n);
+  if (p.num_ctas < 0 || p.group_heads < 0) return fail(FA_ERR_INVALID_ARG, "negative plan parameter");
+  return FA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fa_version(void) { return 100; }
+
+const char* fa_last_error_string(void) { return t_last_error.c_str(); }
+
+int fa_fwd_block_m(void) { return fa::prefill_block_m(); }
+
+fa_status fa_fwd_ex(const fa_fwd_params* params, fa_stream_t stream) {
+  if (!params) return fail(FA_ERR_INVALID_ARG, "params is null");
+  const fa_fwd_params& a = *params;
+  fa_status st = check_fwd(a);
+  if (st != FA_OK) return st;
+  if (a.Sq == 0) return FA_OK;  // nothing to compute
+  DeviceInfo dev;
+  if ((st = device_info(&dev)) != FA_OK) return st;
+
+  const int BM = fa::prefill_block_m();
+  const int BN = a.block_n ? a.block_n : 128;
+  const int BH = a.B * a.H;
+  fa::PrefillLaunch L;
+  std::memset(&L, 0, sizeof L);
+  fa::PrefillParams& p = L.p;
+  p.o = a.o;
+  p.lse = a.lse;
+  p.BH = BH;
+  p.Sq = a.Sq;
+  p.Sk = a.Sk;
+  p.nmb = (a.Sq + BM - 1) / BM;
+  p.nnb = (a.Sk + BN - 1) / BN;
+  p.mask_mode = a.mask_mode;
+  p.window = a.mask_mode == FA_MASK_CAUSAL_WINDOW ? a.window : 0;
+  p.n_global = a.mask_mode == FA_MASK_CAUSAL_WINDOW ? a.n_global : 0;
+  p.sl2 = a.scale * 1.4426950408889634f;
+  // Heads scheduled together so that their K/V stays resident in L2 (~48 MiB budget).
+  long long kv_keys = a.Sk;
+  if (a.mask_mode == FA_MASK_CAUSAL_WINDOW) {
+    const long long band = static_cast<long long>(a.window) + a.n_global + BM + BN;
+    if (band < kv_keys) kv_keys = band;
+  }
+  const long long kv_bytes = kv_keys * a.d * 4 + 1;
+  long long hg = a.group_heads ? a.group_heads : (48LL << 20) / kv_bytes;
+  if (hg < 1) hg = 1;
+  if (hg > BH) hg = BH;
+  p.group_heads = static_cast<int>(hg);
+  p.total_items = BH * p.nmb;
+  p.status = dev.status;
+  p.timeout_ns = static_cast<uint64_t>(a.timeout_us ? a.timeout_us : 1000000u) * 1000u;
+  p.trace = a.trace;
+  L.grid = a.num_ctas ? a.num_ctas : dev.sms;
+  if (L.grid > p.total_items) L.grid = p.total_items;
+
+  const bool bf16 = a.dtype == FA_BF16;
+  if ((st = make_map(&L.tmQ, a.q, bf16, a.d, a.Sq, BH, BM)) != FA_OK) return st;
+  // with Sk == 0 no key tile is ever loaded; the maps only need a valid address
+  if ((st = make_map(&L.tmK, a.Sk ? a.k : a.q, bf16, a.d, a.Sk, BH, BN)) != FA_OK) return st;
+  if ((st = make_map(&L.tmV, a.Sk ? a.v : a.q, bf16, a.d, a.Sk, BH, BN)) != FA_OK) return st;
+  cudaError_t e = fa::launch_prefill(L, a.d, BN, bf16, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+  return FA_OK;
+}
+
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                 int Sq, int Sk, int d, float scale, int mask_mode, int window, int n_global,
+                 int dtype, fa_stream_t stream) {
+  fa_fwd_params p;
+  std::memset(&p, 0, sizeof p);
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.o = o;
+  p.lse = lse;
+  p.B = B;
+  p.H = H;
+  p.Sq = Sq;
+  p.Sk = Sk;
+  p.d = d;
+  p.scale = scale;
+  p.mask_mode = mask_mode;
+  p.window = window;
+  p.n_global = n_global;
+  p.dtype = dtype;
+  return fa_fwd_ex(&p, stream);
+}
+
+int fa_decode_default_pages_per_split(int B, int H, int max_pages_per_seq) {
+  // Enough splits that the ragged mix of context lengths still fills the GPU
+  // several times over, without making the merge step large.
+  const long long bh = static_cast<long long>(B > 0 ? B : 1) * (H > 0 ? H : 1);
+  int pps = 1;
+  while (pps < max_pages_per_seq && bh * ((max_pages_per_seq + pps - 1) / pps) > 16384) pps *= 2;
+  return pps;
+}
+
+size_t fa_decode_workspace_size(int B, int H, int d, int max_pages_per_seq, int page_size) {
+  (void)page_size;
+  if (B < 1 || H < 1 || d < 1 || max_pages_per_seq < 1) return 0;
+  return static_cast<size_t>(B) * H * max_pages_per_seq * (d + 2) * sizeof(float);
+}
+
+fa_status fa_decode_paged_ex(const fa_decode_params* params, fa_stream_t stream) {
+  if (!params) return fail(FA_ERR_INVALID_ARG, "params is null");
+  const fa_decode_params& a = *params;
+  if (!a.q || !a.k_pages || !a.v_pages || !a.block_table || !a.ctx_lens || !a.o || !a.workspace)
+    return fail(FA_ERR_INVALID_ARG, "q, k_pages, v_pages, block_table, ctx_lens, o, workspace must be non-null");
+  if (!aligned16(a.q) || !aligned16(a.k_pages) || !aligned16(a.v_pages) || !aligned16(a.o) ||
+      !aligned16(a.workspace))
+    return fail(FA_ERR_INVALID_ARG, "q, pools, o and workspace must be 16-byte aligned");
+  if (!aligned4(a.block_table) || !aligned4(a.ctx_lens) || (a.lse && !aligned4(a.lse)))
+    return fail(FA_ERR_INVALID_ARG, "block_table, ctx_lens and lse must be 4-byte aligned");
+  if (a.B < 1 || a.H < 1 || a.max_pages_per_seq < 1 || a.num_pages < 1)
+    return fail(FA_ERR_INVALID_ARG, "need B, H, max_pages_per_seq, num_pages >= 1");
+  if (a.d != 64 && a.d != 128) return fail(FA_ERR_UNSUPPORTED, "head dim %d (supported: 64, 128)", a.d);
+  if (a.dtype != FA_F16 && a.dtype != FA_BF16) return fail(FA_ERR_UNSUPPORTED, "dtype %d", a.dtype);
+  if (a.page_size < 16 || a.page_size > 4096 || a.page_size % 16 != 0)
+    return fail(FA_ERR_UNSUPPORTED, "page_size %d (a multiple of 16 in [16, 4096])", a.page_size);
+  if (!std::isfinite(a.scale)) return fail(FA_ERR_INVALID_ARG, "scale must be finite");
+  const long long max_ctx = static_cast<long long>(a.page_size) * a.max_pages_per_seq;
+  const long long pool = static_cast<long long>(a.num_pages) * a.H * a.page_size * a.d;
+  if (max_ctx > (1LL << 30) || static_cast<long long>(a.B) * a.H > (1LL << 30) || pool > (1LL << 46))
+    return fail(FA_ERR_INVALID_ARG, "problem too large");
+  const size_t need = fa_decode_workspace_size(a.B, a.H, a.d, a.max_pages_per_seq, a.page_size);
+  if (a.workspace_bytes < need)
+    return fail(FA_ERR_INVALID_ARG, "workspace has %zu bytes, needs %zu", a.workspace_bytes, need);
+  int pps = a.pages_per_split ? a.pages_per_split
+                              : fa_decode_default_pages_per_split(a.B, a.H, a.max_pages_per_seq);
+  if (pps < 1 || pps > a.max_pages_per_seq) return fail(FA_ERR_INVALID_ARG, "pages_per_split %d", pps);
+  const long long nsplit = (a.max_pages_per_seq + pps - 1) / pps;
+  if (nsplit * a.B * a.H > (1LL << 31) - 1) return fail(FA_ERR_INVALID_ARG, "too many splits");
+  DeviceInfo dev;
+  fa_status st = device_info(&dev);
+  if (st != FA_OK) return st;
+
+  fa::DecodeParams p;
+  std::memset(&p, 0, sizeof p);
+  p.q = a.q;
+  p.k_pages = a.k_pages;
+  p.v_pages = a.v_pages;
+  p.block_table = a.block_table;
+  p.ctx_lens = a.ctx_lens;
+  p.o = a.o;
+  p.lse = a.lse;
+  p.part = static_cast<float*>(a.workspace);
+  p.B = a.B;
+  p.H = a.H;
+  p.page_size = a.page_size;
+  p.max_pages = a.max_pages_per_seq;
+  p.num_pages = a.num_pages;
+  p.pages_per_split = pps;
+  p.nsplit_max = static_cast<int>(nsplit);
+  p.sl2 = a.scale * 1.4426950408889634f;
+  p.status = dev.status;
+  p.trace_pages = a.trace_pages;
+  p.trace_splits = a.trace_splits;
+  cudaError_t e = fa::launch_decode(p, a.d, a.dtype == FA_BF16, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+  return FA_OK;
+}
+
+fa_status fa_decode_paged(const void* q, const void* k_pages, const void* v_pages,
+                          const int32_t* block_table, const int32_t* ctx_lens, void* o, float* lse,
+                          int B, int H, int d, int page_size, int max_pages_per_seq, int num_pages,
+                          float scale, int dtype, void* workspace, size_t workspace_bytes,
+                          fa_stream_t stream) {
+  fa_decode_params p;
+  std::memset(&p, 0, sizeof p);
+  p.q = q;
+  p.k_pages = k_pages;
+  p.v_pages = v_pages;
+  p.block_table = block_table;
+  p.ctx_lens = ctx_lens;
+  p.o = o;
+  p.lse = lse;
+  p.B = B;
+  p.H = H;
+  p.d = d;
+  p.page_size = page_size;
+  p.max_pages_per_seq = max_pages_per_seq;
+  p.num_pages = num_pages;
+  p.scale = scale;
+  p.dtype = dtype;
+  p.workspace = workspace;
+  p.workspace_bytes = workspace_bytes;
+  return fa_decode_paged_ex(&p, stream);
+}
+
+fa_status fa_get_device_status(fa_stream_t stream) {
+  DeviceInfo dev;
+  fa_status st = device_info(&dev);
+  if (st != FA_OK) return st;
+  cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  uint32_t word = 0;
+  e = cudaMemcpy(&word, dev.status, sizeof word, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the device status word");
+  const uint32_t zero = 0;
+  e = cudaMemcpy(dev.status, &zero, sizeof zero, cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) return cuda_fail(e, "clearing the device status word");
+  if (word & fa::FA_DEV_TIMEOUT) return fail(FA_ERR_TIMEOUT, "a kernel gave up on a pipeline wait");
+  if (word & fa::FA_DEV_BAD_PAGE) return fail(FA_ERR_BAD_PAGE, "a block-table entry or context length was out of range");
+  return FA_OK;
+}
+
+fa_status fa_selftest_timeout(uint32_t timeout_us, fa_stream_t stream) {
+  if (timeout_us < 1 || timeout_us > 1000000u)
+    return fail(FA_ERR_INVALID_ARG, "timeout_us must be in [1, 1000000]");
+  DeviceInfo dev;
+  fa_status st = device_info(&dev);
+  if (st != FA_OK) return st;
+  cudaError_t e = fa::launch_selftest_timeout(dev.status, static_cast<uint64_t>(timeout_us) * 1000u,
+                                              reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "selftest launch");
+  return FA_OK;
+}
+
+}  // extern "C"

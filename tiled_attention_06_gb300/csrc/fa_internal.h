@@ -1,0 +1,60 @@
+// Internal interface between the C-ABI layer (fa_api.cu) and the kernel translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+#include "fa.h"
+
+namespace fa {
+
+// bits of the device status word
+enum : uint32_t { FA_DEV_TIMEOUT = 1u, FA_DEV_BAD_PAGE = 2u };
+
+struct PrefillParams {
+  void* o;            // [B,H,Sq,D] 16-bit
+  float* lse;         // [B,H,Sq] or nullptr
+  int BH, Sq, Sk;
+  int nmb, nnb;       // query blocks (BM rows), key blocks (BN keys)
+  int mask_mode, window, n_global;
+  float sl2;          // scale * log2(e)
+  int group_heads;    // (batch, head) pairs per scheduling group
+  int total_items;    // BH * nmb
+  uint32_t* status;   // device status word
+  uint64_t timeout_ns;
+  int32_t* trace;     // optional [BH, nmb, nnb] visit log (16 + class per visit)
+};
+
+struct PrefillLaunch {
+  CUtensorMap tmQ, tmK, tmV;
+  PrefillParams p;
+  int grid;
+};
+
+int prefill_block_m();
+cudaError_t launch_prefill(const PrefillLaunch& L, int D, int BN, bool bf16, cudaStream_t stream);
+
+struct DecodeParams {
+  const void* q;            // [B,H,D]
+  const void* k_pages;      // [num_pages,H,page_size,D]
+  const void* v_pages;
+  const int32_t* block_table;  // [B,max_pages]
+  const int32_t* ctx_lens;     // [B]
+  void* o;                  // [B,H,D]
+  float* lse;               // [B,H] or nullptr
+  float* part;              // workspace [B*H, nsplit_max, D+2] FP32 partials
+  int B, H, page_size, max_pages, num_pages;
+  int pages_per_split, nsplit_max;
+  float sl2;                // scale * log2(e)
+  uint32_t* status;
+  int32_t* trace_pages;     // optional [B*H, max_pages]: physical page read per logical page
+  int32_t* trace_splits;    // optional [B*H, nsplit_max, 2]: token range per split
+};
+
+cudaError_t launch_decode(const DecodeParams& p, int D, bool bf16, cudaStream_t stream);
+cudaError_t launch_selftest_timeout(uint32_t* status, uint64_t timeout_ns, cudaStream_t stream);
+
+}  // namespace fa
