@@ -1,0 +1,651 @@
+#!/usr/bin/env python
+"""Benchmark of the FlashAttention forward hot path on GB300.
+
+One step = one pass of the whole hot path over one batch of synthetic input:
+  * prefill  fa_fwd, causal, B=4 H=32 Sq=Sk=4096 d=128 bf16, Q,K,V ~ N(0,1)
+  * decode   fa_decode_paged, B=32 H=32 d=128 fp16, ctx ~ U[1,8192], 256-token
+             pages scattered over a pool of 1200 pages by a random permutation
+`value` is the prefill throughput in TFLOP/s (4*B*H*d * visible pairs, masked pairs
+not counted), timed with CUDA events around each prefill launch; the decode
+throughput (algorithmic HBM bytes / time) is reported beside it under "decode".
+Inputs are larger than L2 (prefill Q+K+V 402 MB, decode K/V 2.2 GB), so no flush
+is needed between steps.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                       [--workload default|causal2k|causal4k|noncausal4k|window32k|decode|sweep]
+With --gpus N > 1 run under torchrun: every rank runs the same workload on its own
+GPU (replicas; no collective on the data path), value = N * units / max rank time.
+"""
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+PREFILL = {
+    "causal2k": dict(B=4, H=32, S=2048, d=128, dtype="f16", mode=1, window=0, n_global=0,
+                     factor=0.5),
+    "causal4k": dict(B=4, H=32, S=4096, d=128, dtype="bf16", mode=1, window=0, n_global=0,
+                     factor=1.0),
+    "noncausal4k": dict(B=4, H=32, S=4096, d=128, dtype="bf16", mode=0, window=0, n_global=0,
+                        factor=1.0),
+    "window32k": dict(B=1, H=32, S=32768, d=128, dtype="bf16", mode=2, window=2048,
+                      n_global=64, factor=1.0),
+}
+DECODE = dict(B=32, H=32, d=128, page=256, pool=1200, max_ctx=8192, dtype="f16")
+MODE_NAME = {0: "none", 1: "causal", 2: "causal_window"}
+
+# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu
+# capture of each kernel, with the SHA-256 of the kernel sources it was taken on; the
+# figure is reported only while those sources are unchanged. Summaries: profiles/.
+NCU_TRAFFIC = {
+    "prefill": {"bytes": None, "sources": ["fa_prefill.cu", "fa_ptx.cuh"], "sha256": None},
+    "decode": {"bytes": None, "sources": ["fa_decode.cu", "fa_ptx.cuh"], "sha256": None},
+}
+
+
+def sources_sha(names):
+    import hashlib
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "tiled_attention_06_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def ncu_traffic(kind, override):
+    if override is not None:
+        return override
+    t = NCU_TRAFFIC[kind]
+    if t["bytes"] is None or t["sha256"] != sources_sha(t["sources"]):
+        return None
+    return t["bytes"]
+
+
+# --------------------------------------------------------------------------- accounting
+def visible_pairs(Sq, Sk, mode, window=0, n_global=0):
+    """Number of (query, key) pairs the mask leaves visible (closed form per row)."""
+    delta = Sk - Sq
+    total = 0
+    for i in range(Sq):
+        pos = i + delta
+        if mode == 0:
+            total += Sk
+            continue
+        if pos < 0:
+            continue
+        hi = min(pos, Sk - 1) + 1
+        if mode == 1:
+            total += hi
+            continue
+        lo = max(0, pos - window + 1)
+        total += max(0, hi - lo) + max(0, min(n_global, hi, lo))
+    return total
+
+
+def prefill_flops(cfg):
+    return 4.0 * cfg["B"] * cfg["H"] * cfg["d"] * visible_pairs(cfg["S"], cfg["S"], cfg["mode"],
+                                                                cfg["window"], cfg["n_global"])
+
+
+def decode_bytes(ctx_lens, B, H, d, max_pages, elem=2):
+    kv = int(sum(int(c) for c in ctx_lens)) * H * d * elem * 2
+    return kv + 2 * B * H * d * elem + B * H * 4 + B * max_pages * 4 + B * 4
+
+
+def load_peaks():
+    if os.path.exists(PEAKS_FILE):
+        with open(PEAKS_FILE) as f:
+            pk = json.load(f)
+        return pk, "measured"
+    return FALLBACK, "fallback"
+
+
+# --------------------------------------------------------------------------- distributed
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+        rank = dist.get_rank()
+        if torch.cuda.is_available():
+            torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", rank)))
+        return rank, world
+    return 0, 1
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    """Largest value of x across ranks (host collective; not on the data path)."""
+    if world == 1:
+        return float(x)
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate(units_per_rank, max_seconds, world):
+    """Whole-job throughput: every rank processed units_per_rank in at most max_seconds."""
+    return units_per_rank * world / max_seconds
+
+
+# --------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.idx = device_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.idx}",
+                                          f"--query-gpu={self.FIELDS}", "--format=csv,noheader",
+                                          "-lms", "100"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        sms, mx, reasons, power = [], None, set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sms.append(float(parts[1].split()[0]))
+                mx = float(parts[2].split()[0])
+                power.append(float(parts[3].split()[0]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sms) if sms else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sms),
+                "power_w_max": max(power) if power else None}
+
+
+# --------------------------------------------------------------------------- our arm
+def make_prefill(cfg, dev, seed=0):
+    from tiled_attention_06_gb300 import inputs
+    dt = inputs.DTYPES[cfg["dtype"]]
+    q, k, v = inputs.prefill_inputs(cfg["B"], cfg["H"], cfg["S"], cfg["S"], cfg["d"], dt,
+                                    factor=cfg["factor"], seed=seed)
+    return q, k, v
+
+
+def make_decode(dev, seed=0):
+    from tiled_attention_06_gb300 import inputs
+    c = DECODE
+    return inputs.decode_inputs(B=c["B"], H=c["H"], d=c["d"], page_size=c["page"],
+                                num_pages=c["pool"], max_ctx=c["max_ctx"],
+                                dtype=inputs.DTYPES[c["dtype"]], seed=seed)
+
+
+def run_ours(args, rank, world):
+    import tiled_attention_06_gb300 as fa
+    from tiled_attention_06_gb300 import build
+    build.build()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    peaks, peak_kind = load_peaks()
+    stream = torch.cuda.current_stream()
+    workload = "default" if args.workload == "default" else args.workload
+    pcfg = PREFILL["causal4k" if workload in ("default", "sweep") else workload] \
+        if workload != "decode" else None
+    with_decode = workload in ("default", "decode")
+
+    # ---- inputs, resident in HBM before timing
+    if pcfg:
+        q, k, v = make_prefill(pcfg, dev)
+        qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+        od = torch.empty_like(qd)
+        ld = torch.empty(qd.shape[:3], dtype=torch.float32, device=dev)
+        pflops = prefill_flops(pcfg)
+        scale = 1 / math.sqrt(pcfg["d"])
+    if with_decode:
+        di = make_decode(dev)
+        dq, dk, dv = di.q.to(dev), di.k_pages.to(dev), di.v_pages.to(dev)
+        dbt, dcl = di.block_table.to(dev), di.ctx_lens.to(dev)
+        do = torch.empty_like(dq)
+        dl = torch.empty(dq.shape[:2], dtype=torch.float32, device=dev)
+        mp = dbt.shape[1]
+        ws = torch.empty(fa.fa_decode_workspace_size(DECODE["B"], DECODE["H"], DECODE["d"], mp,
+                                                     DECODE["page"]), dtype=torch.uint8,
+                         device=dev)
+        dbytes = decode_bytes(di.ctx_lens.tolist(), DECODE["B"], DECODE["H"], DECODE["d"], mp)
+        dscale = 1 / math.sqrt(DECODE["d"])
+
+    def prefill_call(**ex):
+        if ex:
+            fa.fa_fwd_ex(qd, kd, vd, od, ld, scale, pcfg["mode"], pcfg["window"],
+                         pcfg["n_global"], stream=stream, **ex)
+        else:
+            fa.fa_fwd(qd, kd, vd, od, ld, scale, pcfg["mode"], pcfg["window"], pcfg["n_global"],
+                      stream=stream)
+
+    def decode_call():
+        fa.fa_decode_paged(dq, dk, dv, dbt, dcl, do, dl, dscale, ws, stream=stream)
+
+    if workload == "sweep":
+        return run_sweep(args, fa, prefill_call, pflops, peaks, peak_kind, pcfg)
+
+    K, W = args.steps, args.warmup
+    for _ in range(W):
+        if pcfg:
+            prefill_call()
+        if with_decode:
+            decode_call()
+    torch.cuda.synchronize()
+    if fa.fa_get_device_status() != fa.FA_OK:
+        raise RuntimeError("device status after warm-up: " + fa.fa_last_error_string())
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    for i in range(K):
+        ev[i][0].record(stream)
+        if pcfg:
+            prefill_call()
+        ev[i][1].record(stream)
+        if with_decode:
+            decode_call()
+        ev[i][2].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    if fa.fa_get_device_status() != fa.FA_OK:
+        raise RuntimeError("device status after timing: " + fa.fa_last_error_string())
+    p_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
+    d_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
+    total_ms = ev[0][0].elapsed_time(ev[K - 1][2])
+    total_ms = max_over_ranks(total_ms, world)
+    launches = K * ((1 if pcfg else 0) + (2 if with_decode else 0))
+
+    res = {"n_gpus": world, "steps": K, "warmup": W, "ms_per_step": total_ms / K,
+           "scaling": "weak", "vs_baseline": None, "data": "synthetic (seeded N(0,1), "
+           "shapes of the pages' workloads; no dataset)", "gpu_launches": launches,
+           "clocks": clk}
+    hbm_peak = float(peaks["hbm_gbs"])
+    if pcfg:
+        p_sum = max_over_ranks(sum(p_ms) / 1e3, world)
+        p_avg = sum(p_ms) / K / 1e3
+        value = aggregate(pflops * K, p_sum, world) / 1e12
+        tc_peak = float(peaks["bf16_tflops"])
+        achieved = pflops / p_avg / 1e12
+        res.update({"metric": "attention fwd TFLOP/s (% BF16 TC peak); paged decode HBM GB/s "
+                              "(% of 8 TB/s)",
+                    "value": value, "unit": "TFLOP/s", "higher_is_better": True,
+                    "dtype": pcfg["dtype"]})
+        res["roofline"] = {"kernel": "prefill_kernel<128,128,bf16>" if pcfg["dtype"] == "bf16"
+                           else "prefill_kernel<128,128,f16>", "bound": "tensor",
+                           "achieved": achieved, "peak": tc_peak, "unit": "TFLOP/s",
+                           "frac": achieved / tc_peak,
+                           "peak_source": f"{peak_kind} bf16 burst (MEASURED_PEAKS.json)"
+                           if peak_kind == "measured" else "fallback 1.9 PFLOP/s",
+                           "traffic": ncu_traffic("prefill", args.prefill_traffic), "algorithmic_flops": pflops,
+                           "ms_per_launch": p_avg * 1e3}
+    if with_decode:
+        d_sum = max_over_ranks(sum(d_ms) / 1e3, world)
+        d_avg = sum(d_ms) / K / 1e3
+        dval = aggregate(dbytes * K, d_sum, world) / 1e9
+        dec = {"value": dval, "unit": "GB/s", "frac_of_8TBs": dval / world / 8000.0,
+               "roofline": {"kernel": "decode_split_kernel + decode_merge_kernel",
+                            "bound": "hbm", "achieved": dbytes / d_avg / 1e9, "peak": hbm_peak,
+                            "unit": "GB/s", "frac": dbytes / d_avg / 1e9 / hbm_peak,
+                            "peak_source": f"{peak_kind} copy bandwidth",
+                            "traffic": ncu_traffic("decode", args.decode_traffic), "algorithmic_bytes": dbytes,
+                            "ms_per_call": d_avg * 1e3}}
+        if pcfg:
+            res["decode"] = dec
+        else:
+            res.update({"metric": "paged decode HBM GB/s (% of 8 TB/s)", "value": dval,
+                        "unit": "GB/s", "higher_is_better": True, "dtype": "f16",
+                        "roofline": dec["roofline"]})
+    res["config"] = workload_config(pcfg, with_decode, world)
+
+    # ---- end to end through the public API with host buffers
+    res["e2e"] = e2e_prefill(fa, pcfg, q, k, v, pflops, scale, stream, world, args) if pcfg \
+        else e2e_decode(fa, di, dbytes, dscale, ws, dk, dv, stream, world, args)
+    # ---- CPU baseline: the oracle on a bounded sample, rank 0 only
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(pcfg, q if pcfg else None, k if pcfg else None,
+                                           v if pcfg else None,
+                                           di if with_decode else None)
+    return res
+
+
+def workload_config(pcfg, with_decode, world):
+    cfg = {}
+    if pcfg:
+        cfg["workload"] = (f"prefill {MODE_NAME[pcfg['mode']]} B{pcfg['B']} H{pcfg['H']} "
+                           f"S{pcfg['S']} d{pcfg['d']} {pcfg['dtype']}"
+                           + (f" window {pcfg['window']} global {pcfg['n_global']}"
+                              if pcfg["mode"] == 2 else ""))
+    if with_decode:
+        d = DECODE
+        dec = (f"paged decode B{d['B']} H{d['H']} d{d['d']} {d['dtype']} ctx~U[1,{d['max_ctx']}] "
+               f"page {d['page']} pool {d['pool']}")
+        cfg["workload"] = (cfg["workload"] + " + " + dec) if pcfg else dec
+    cfg["parallelism"] = f"replicas x{world}" if world > 1 else "single GPU"
+    cfg["l2"] = "inputs larger than L2 (no flush)"
+    return cfg
+
+
+def e2e_prefill(fa, pcfg, q, k, v, pflops, scale, stream, world, args):
+    dev = torch.device("cuda", torch.cuda.current_device())
+    hq, hk, hv = q.pin_memory(), k.pin_memory(), v.pin_memory()
+    ho = torch.empty(q.shape, dtype=q.dtype).pin_memory()
+    hl = torch.empty(q.shape[:3], dtype=torch.float32).pin_memory()
+    qd, kd, vd = torch.empty_like(hq, device=dev), torch.empty_like(hk, device=dev), \
+        torch.empty_like(hv, device=dev)
+    od = torch.empty_like(qd)
+    ld = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+
+    def step():
+        qd.copy_(hq, non_blocking=True)
+        kd.copy_(hk, non_blocking=True)
+        vd.copy_(hv, non_blocking=True)
+        fa.fa_fwd(qd, kd, vd, od, ld, scale, pcfg["mode"], pcfg["window"], pcfg["n_global"],
+                  stream=stream)
+        ho.copy_(od, non_blocking=True)
+        hl.copy_(ld, non_blocking=True)
+
+    K = max(3, min(args.steps, args.e2e_steps))
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    e0.record(stream)
+    for _ in range(K):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    secs = max_over_ranks(e0.elapsed_time(e1) / 1e3, world)
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
+    d2h = ho.numel() * ho.element_size() + hl.numel() * 4
+    return {"value": aggregate(pflops * K, secs, world) / 1e12, "unit": "TFLOP/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": K,
+            "api": "tiled_attention_06_gb300.fa_fwd (C ABI fa_fwd) with pinned host buffers"}
+
+
+def e2e_decode(fa, di, dbytes, dscale, ws, dk, dv, stream, world, args):
+    dev = torch.device("cuda", torch.cuda.current_device())
+    hq, hbt, hcl = di.q.pin_memory(), di.block_table.pin_memory(), di.ctx_lens.pin_memory()
+    ho = torch.empty(di.q.shape, dtype=di.q.dtype).pin_memory()
+    hl = torch.empty(di.q.shape[:2], dtype=torch.float32).pin_memory()
+    qd, btd, cld = (torch.empty_like(t, device=dev) for t in (hq, hbt, hcl))
+    od = torch.empty_like(qd)
+    ld = torch.empty(hl.shape, dtype=torch.float32, device=dev)
+
+    def step():
+        qd.copy_(hq, non_blocking=True)
+        btd.copy_(hbt, non_blocking=True)
+        cld.copy_(hcl, non_blocking=True)
+        fa.fa_decode_paged(qd, dk, dv, btd, cld, od, ld, dscale, ws, stream=stream)
+        ho.copy_(od, non_blocking=True)
+        hl.copy_(ld, non_blocking=True)
+
+    K = max(3, min(args.steps, args.e2e_steps))
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(K):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    secs = max_over_ranks(e0.elapsed_time(e1) / 1e3, world)
+    return {"value": aggregate(dbytes * K, secs, world) / 1e9, "unit": "GB/s",
+            "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in (hq, hbt, hcl)),
+            "d2h_bytes_per_step": ho.numel() * ho.element_size() + hl.numel() * 4, "steps": K,
+            "api": "tiled_attention_06_gb300.fa_decode_paged; the paged KV cache stays resident"}
+
+
+# --------------------------------------------------------------------------- oracle timing
+def oracle_prefill_sample(pcfg, q, k, v, n_heads):
+    """Time the FP64 oracle on every row of the first n_heads (batch 0) of the prefill."""
+    import numpy as np
+
+    import oracle
+    S = pcfg["S"]
+    rows = np.arange(n_heads * S, dtype=np.int64)
+    pairs = n_heads * visible_pairs(S, S, pcfg["mode"], pcfg["window"], pcfg["n_global"])
+    t0 = time.perf_counter()
+    oracle.attention(q, k, v, 1 / math.sqrt(pcfg["d"]), pcfg["mode"], pcfg["window"],
+                     pcfg["n_global"], rows=rows)
+    secs = time.perf_counter() - t0
+    return 4.0 * pairs * pcfg["d"], secs, oracle.threads_used()
+
+
+def visible_pairs_row(pos, Sk, pcfg):
+    if pcfg["mode"] == 0:
+        return Sk
+    hi = min(pos, Sk - 1) + 1
+    if pcfg["mode"] == 1:
+        return hi
+    lo = max(0, pos - pcfg["window"] + 1)
+    return max(0, hi - lo) + max(0, min(pcfg["n_global"], hi, lo))
+
+
+def oracle_decode_sample(di, n_seq):
+    """Time the FP64 oracle on the first n_seq sequences (all heads) of the decode."""
+    import numpy as np
+
+    import oracle
+    bh = np.arange(n_seq * di.H, dtype=np.int64)
+    nbytes = decode_bytes(di.ctx_lens[:n_seq].tolist(), n_seq, di.H, di.d,
+                          di.block_table.shape[1])
+    t0 = time.perf_counter()
+    oracle.decode_paged(di.q, di.k_pages, di.v_pages, di.block_table, di.ctx_lens,
+                        1 / math.sqrt(di.d), bh_list=bh)
+    return nbytes, time.perf_counter() - t0, oracle.threads_used()
+
+
+def cpu_model():
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name"):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+def cpu_baseline(pcfg, q, k, v, di):
+    out = {"kind": "oracle", "cpu": cpu_model()}
+    if pcfg:
+        n_heads = 16
+        flops, secs, cores = oracle_prefill_sample(pcfg, q, k, v, n_heads)
+        out.update({"value": flops / secs / 1e12, "unit": "TFLOP/s", "cores": cores,
+                    "seconds": secs,
+                    "sample": f"FP64 oracle, all {pcfg['S']} rows of {n_heads} of "
+                              f"{pcfg['B'] * pcfg['H']} (batch, head) pairs"})
+    if di is not None:
+        nbytes, secs, cores = oracle_decode_sample(di, 4)
+        dec = {"value": nbytes / secs / 1e9, "unit": "GB/s", "cores": cores, "seconds": secs,
+               "sample": f"FP64 oracle, 4 of {di.B} sequences, all {di.H} heads"}
+        if pcfg:
+            out["decode"] = dec
+        else:
+            out.update(dec)
+    return out
+
+
+# --------------------------------------------------------------------------- reference arm
+def run_reference(args, rank, world):
+    """The oracle as it stands, on the host cores: each step is a bounded sample of the
+    same workload (the last 256 query rows of one (batch, head) of the prefill, and
+    one sequence of the decode)."""
+    import numpy as np
+
+    import oracle
+    from tiled_attention_06_gb300 import inputs
+    workload = args.workload if args.workload not in ("sweep",) else "default"
+    pcfg = None if workload == "decode" else PREFILL["causal4k" if workload == "default"
+                                                     else workload]
+    res = {"impl": "reference", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+           "scaling": "weak", "vs_baseline": None, "data": "synthetic (seeded N(0,1))",
+           "gpu_launches": 0}
+    rows_per = 256
+    if pcfg:
+        q, k, v = make_prefill(pcfg, None)
+        S = pcfg["S"]
+        BH = pcfg["B"] * pcfg["H"]
+        pairs_per_step = sum(visible_pairs_row(i, S, pcfg) for i in range(S - rows_per, S))
+
+        def step(i):
+            bh = i % BH
+            rows = np.arange(bh * S + S - rows_per, bh * S + S, dtype=np.int64)
+            oracle.attention(q, k, v, 1 / math.sqrt(pcfg["d"]), pcfg["mode"], pcfg["window"],
+                             pcfg["n_global"], rows=rows)
+        units = 4.0 * pairs_per_step * pcfg["d"]
+        unit, scale_div, metric = "TFLOP/s", 1e12, ("attention fwd TFLOP/s (% BF16 TC peak); "
+                                                    "paged decode HBM GB/s (% of 8 TB/s)")
+        sample = f"last {rows_per} query rows of one (batch, head) per step"
+        dtype = pcfg["dtype"]
+    else:
+        di = make_decode(None)
+
+        def step(i):
+            b = i % di.B
+            oracle.decode_paged(di.q, di.k_pages, di.v_pages, di.block_table, di.ctx_lens,
+                                1 / math.sqrt(di.d), bh_list=np.arange(b * di.H, (b + 1) * di.H))
+        units = None
+        unit, scale_div, metric = "GB/s", 1e9, "paged decode HBM GB/s (% of 8 TB/s)"
+        sample = "one sequence (all heads) per step"
+        dtype = "f16"
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    total_units = 0.0
+    for i in range(args.steps):
+        step(i)
+        if units is None:
+            b = i % di.B
+            total_units += decode_bytes([int(di.ctx_lens[b])], 1, di.H, di.d,
+                                        di.block_table.shape[1])
+        else:
+            total_units += units
+    secs = time.perf_counter() - t0
+    value = total_units / secs / scale_div
+    res.update({"metric": metric, "value": value, "unit": unit, "higher_is_better": True,
+                "ms_per_step": secs / args.steps * 1e3, "dtype": dtype,
+                "config": workload_config(pcfg, pcfg is None, 1)})
+    res["cpu_baseline"] = {"kind": "oracle", "value": value, "unit": unit,
+                           "cores": oracle.threads_used(), "sample": sample, "cpu": cpu_model()}
+    res["e2e"] = {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+    return res
+
+
+# --------------------------------------------------------------------------- tile sweep
+def run_sweep(args, fa, prefill_call, pflops, peaks, peak_kind, pcfg):
+    """Key-block size sweep of the causal 4k prefill (the query block is 128 rows)."""
+    lines = []
+    for bn in (64, 128):
+        for _ in range(3):
+            prefill_call(block_n=bn)
+        torch.cuda.synchronize()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n = max(5, args.steps // 4)
+        s.record()
+        for _ in range(n):
+            prefill_call(block_n=bn)
+        e.record()
+        torch.cuda.synchronize()
+        ms = s.elapsed_time(e) / n
+        lines.append({"block_m": fa.fa_fwd_block_m(), "block_n": bn, "ms": ms,
+                      "tflops": pflops / ms / 1e9,
+                      "frac": pflops / ms / 1e9 / float(peaks["bf16_tflops"])})
+    return {"metric": "attention fwd TFLOP/s tile sweep", "value": max(l["tflops"] for l in lines),
+            "unit": "TFLOP/s", "sweep": lines, "config": workload_config(pcfg, False, 1),
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
+            "ms_per_step": min(l["ms"] for l in lines), "dtype": pcfg["dtype"],
+            "gpu_launches": 2 * (3 + max(5, args.steps // 4))}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="default",
+                    choices=["default", "causal2k", "causal4k", "noncausal4k", "window32k",
+                             "decode", "sweep"])
+    ap.add_argument("--batch", type=int, default=None, help="override B (small profiling cases)")
+    ap.add_argument("--heads", type=int, default=None, help="override H (small profiling cases)")
+    ap.add_argument("--pool", type=int, default=None, help="override the decode page pool size")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--prefill-traffic", type=float, default=None,
+                    help="DRAM bytes per prefill launch from an ncu capture of this kernel")
+    ap.add_argument("--decode-traffic", type=float, default=None,
+                    help="DRAM bytes per decode call from an ncu capture")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    for cfg in list(PREFILL.values()) + [DECODE]:
+        if args.batch:
+            cfg["B"] = args.batch
+        if args.heads:
+            cfg["H"] = args.heads
+    if args.pool:
+        DECODE["pool"] = args.pool
+    rank, world = dist_setup(args.gpus)
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        res = run_reference(args, rank, 1)
+    else:
+        if not torch.cuda.is_available():
+            raise SystemExit("bench.py needs a CUDA GPU (the product path has no CPU fallback)")
+        res = run_ours(args, rank, world)
+    if rank == 0:
+        print(json.dumps(res))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

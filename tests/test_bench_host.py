@@ -1,0 +1,63 @@
+"""Host-side checks of bench.py's bookkeeping: pair counts, byte counts and the
+multi-rank aggregation (world size 2 over gloo on the CPU)."""
+import os
+import socket
+
+import pytest
+import torch
+import torch.multiprocessing as mp
+
+import bench
+import oracle
+
+
+@pytest.mark.parametrize("Sq,Sk,mode,w,g", [(37, 37, 0, 0, 0), (37, 37, 1, 0, 0),
+                                            (20, 45, 1, 0, 0), (45, 20, 1, 0, 0),
+                                            (200, 200, 2, 16, 5), (100, 130, 2, 7, 40),
+                                            (64, 64, 2, 1, 0), (64, 64, 2, 100, 100)])
+def test_visible_pairs_matches_oracle_count(Sq, Sk, mode, w, g):
+    assert bench.visible_pairs(Sq, Sk, mode, w, g) == oracle.count_visible(Sq, Sk, mode, w, g)
+
+
+def test_headline_flop_counts():
+    assert bench.prefill_flops(bench.PREFILL["causal4k"]) == 4 * 128 * 128 * 8_390_656
+    assert bench.prefill_flops(bench.PREFILL["noncausal4k"]) == 4 * 128 * 128 * 4096 * 4096
+    assert bench.prefill_flops(bench.PREFILL["causal2k"]) == 4 * 128 * 128 * 2_098_176
+    assert bench.prefill_flops(bench.PREFILL["window32k"]) == 4 * 32 * 128 * 66_976_800
+
+
+def test_decode_bytes():
+    # 16384 bytes per context token (K and V, 32 heads x 128 x 2 bytes) plus q, o, lse, tables
+    assert bench.decode_bytes([1, 2], 2, 32, 128, 32) == 3 * 16384 + 2 * 2 * 32 * 128 * 2 \
+        + 2 * 32 * 4 + 2 * 32 * 4 + 2 * 4
+
+
+def _worker(rank, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE="2", LOCAL_RANK=str(rank))
+    import torch.distributed as dist
+    dist.init_process_group("gloo", rank=rank, world_size=2)
+    t = bench.max_over_ranks(1.5 + rank, 2)
+    v = bench.aggregate(100.0, t, 2)
+    bench.barrier(2)
+    out[rank] = (t, v)
+    dist.destroy_process_group()
+
+
+def test_two_rank_aggregation_over_gloo():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    ctx = mp.get_context("spawn")
+    mgr = ctx.Manager()
+    out = mgr.dict()
+    procs = [ctx.Process(target=_worker, args=(r, port, out)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    for r in range(2):
+        t, v = out[r]
+        assert t == 2.5                      # the slowest rank's time
+        assert v == pytest.approx(200.0 / 2.5)  # both ranks' units over that time
