@@ -164,6 +164,30 @@ fa_status fa_decode_paged_ex(const fa_decode_params* params, fa_stream_t stream)
 int fa_decode_default_pages_per_split(int B, int H, int max_pages_per_seq);
 
 /*
+ * fa_decode_paged_noalloc - fa_decode_paged for callers that cannot allocate device
+ * memory. The pages have no counterpart for this call; it exists for users of this
+ * library whose device memory is fixed when they start (a serving loop with a set
+ * budget) or owned entirely by a host program that gives its plug-ins no allocator,
+ * so they cannot provide the workspace fa_decode_paged needs.
+ *   Arguments, layouts and results are those of fa_decode_paged without `workspace`
+ *   and `workspace_bytes`; the caller still owns and passes every input and output.
+ *   The split partials go to a scratch array built into the library: 16 MiB on every
+ *   GPU that loads it, held until the process exits. The call allocates nothing.
+ *   The split size is fa_decode_paged's default, made coarser when needed to fit;
+ *   if even one split per sequence does not fit (B*H*(d+2)*4 bytes > 16 MiB) the call
+ *   returns FA_ERR_INVALID_ARG and launches nothing.
+ *   The first call on each device, with that device current, looks up the scratch
+ *   array's device address; make that first call before any stream capture.
+ *   Every call on a device shares the one array: calls whose kernels overlap on the
+ *   GPU (for example on two streams) race and must be ordered by the caller.
+ */
+fa_status fa_decode_paged_noalloc(const void* q, const void* k_pages, const void* v_pages,
+                                  const int32_t* block_table, const int32_t* ctx_lens, void* o,
+                                  float* lse, int B, int H, int d, int page_size,
+                                  int max_pages_per_seq, int num_pages, float scale, int dtype,
+                                  fa_stream_t stream);
+
+/*
  * fa_get_device_status - synchronise `stream`, then read and clear the device
  * status word. Returns FA_OK, FA_ERR_BAD_PAGE or FA_ERR_TIMEOUT (FA_ERR_CUDA if the
  * stream itself failed).

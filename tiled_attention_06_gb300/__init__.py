@@ -13,7 +13,8 @@ import torch
 
 __all__ = [
     "FaError", "lib", "fa_fwd", "fa_fwd_ex", "fa_decode_paged", "fa_decode_paged_ex",
-    "fa_decode_workspace_size", "fa_decode_default_pages_per_split", "fa_get_device_status",
+    "fa_decode_paged_noalloc", "fa_decode_workspace_size", "fa_decode_default_pages_per_split",
+    "fa_get_device_status",
     "fa_selftest_timeout", "fa_last_error_string", "fa_version", "fa_fwd_block_m",
     "FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_CUDA", "FA_ERR_TIMEOUT",
     "FA_ERR_BAD_PAGE", "FA_F16", "FA_BF16", "FA_MASK_NONE", "FA_MASK_CAUSAL",
@@ -77,6 +78,9 @@ def lib():
                                       _f, _i, _vp, _sz, _vp]
         L.fa_decode_paged_ex.restype = _i
         L.fa_decode_paged_ex.argtypes = [ctypes.POINTER(DecodeParams), _vp]
+        L.fa_decode_paged_noalloc.restype = _i
+        L.fa_decode_paged_noalloc.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i,
+                                              _i, _i, _f, _i, _vp]
         L.fa_decode_workspace_size.restype = _sz
         L.fa_decode_workspace_size.argtypes = [_i, _i, _i, _i, _i]
         L.fa_decode_default_pages_per_split.restype = _i
@@ -202,6 +206,23 @@ def fa_decode_paged_ex(q, k_pages, v_pages, block_table, ctx_lens, o, lse, scale
                      workspace.numel() * workspace.element_size(), pages_per_split,
                      _ptr(trace_pages), _ptr(trace_splits))
     _check(lib().fa_decode_paged_ex(ctypes.byref(p), _stream(stream)))
+
+
+def fa_decode_paged_noalloc(q, k_pages, v_pages, block_table, ctx_lens, o, lse, scale,
+                            stream=None):
+    """fa_decode_paged for callers that cannot allocate a workspace: the split partials
+    go to a fixed 16 MiB scratch array inside the library (one per GPU). Calls that
+    overlap on the GPU share that array and race; the first call on a device should
+    come before any stream capture."""
+    _need_cuda_contig(q=q, k_pages=k_pages, v_pages=v_pages, block_table=block_table,
+                      ctx_lens=ctx_lens, o=o, lse=lse)
+    B, H, d = q.shape
+    P, _, page, _ = k_pages.shape
+    _check(lib().fa_decode_paged_noalloc(q.data_ptr(), k_pages.data_ptr(), v_pages.data_ptr(),
+                                         block_table.data_ptr(), ctx_lens.data_ptr(),
+                                         o.data_ptr(), _ptr(lse), B, H, d, page,
+                                         block_table.shape[1], P, float(scale), _dtype_code(q),
+                                         _stream(stream)))
 
 
 def fa_get_device_status(stream=None):

@@ -317,6 +317,72 @@ fa_status fa_decode_paged(const void* q, const void* k_pages, const void* v_page
   return fa_decode_paged_ex(&p, stream);
 }
 
+fa_status fa_decode_paged_noalloc(const void* q, const void* k_pages, const void* v_pages,
+                                  const int32_t* block_table, const int32_t* ctx_lens, void* o,
+                                  float* lse, int B, int H, int d, int page_size,
+                                  int max_pages_per_seq, int num_pages, float scale, int dtype,
+                                  fa_stream_t stream) {
+  if (!q || !k_pages || !v_pages || !block_table || !ctx_lens || !o)
+    return fail(FA_ERR_INVALID_ARG, "q, k_pages, v_pages, block_table, ctx_lens and o must be non-null");
+  if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(o))
+    return fail(FA_ERR_INVALID_ARG, "q, pools and o must be 16-byte aligned");
+  if (!aligned4(block_table) || !aligned4(ctx_lens) || (lse && !aligned4(lse)))
+    return fail(FA_ERR_INVALID_ARG, "block_table, ctx_lens and lse must be 4-byte aligned");
+  if (B < 1 || H < 1 || max_pages_per_seq < 1 || num_pages < 1)
+    return fail(FA_ERR_INVALID_ARG, "need B, H, max_pages_per_seq, num_pages >= 1");
+  if (d != 64 && d != 128) return fail(FA_ERR_UNSUPPORTED, "head dim %d (supported: 64, 128)", d);
+  if (dtype != FA_F16 && dtype != FA_BF16) return fail(FA_ERR_UNSUPPORTED, "dtype %d", dtype);
+  if (page_size < 16 || page_size > 4096 || page_size % 16 != 0)
+    return fail(FA_ERR_UNSUPPORTED, "page_size %d (a multiple of 16 in [16, 4096])", page_size);
+  if (!std::isfinite(scale)) return fail(FA_ERR_INVALID_ARG, "scale must be finite");
+  const long long max_ctx = static_cast<long long>(page_size) * max_pages_per_seq;
+  const long long pool = static_cast<long long>(num_pages) * H * page_size * d;
+  if (max_ctx > (1LL << 30) || static_cast<long long>(B) * H > (1LL << 30) || pool > (1LL << 46))
+    return fail(FA_ERR_INVALID_ARG, "problem too large");
+  // Pick the split size as fa_decode_paged does, then coarsen it until the partials
+  // fit in the library's fixed scratch array.
+  const size_t cap = fa::noalloc_scratch_bytes();
+  auto partial_bytes = [&](int pps_) {
+    const long long ns = (max_pages_per_seq + pps_ - 1) / pps_;
+    return static_cast<size_t>(B) * H * ns * (d + 2) * sizeof(float);
+  };
+  int pps = fa_decode_default_pages_per_split(B, H, max_pages_per_seq);
+  while (partial_bytes(pps) > cap && pps < max_pages_per_seq) {
+    pps *= 2;
+    if (pps > max_pages_per_seq) pps = max_pages_per_seq;
+  }
+  if (partial_bytes(pps) > cap)
+    return fail(FA_ERR_INVALID_ARG,
+                "B*H*(d+2)*4 = %zu bytes of split partials exceed the %zu-byte scratch of "
+                "fa_decode_paged_noalloc; use fa_decode_paged with a workspace",
+                partial_bytes(pps), cap);
+  DeviceInfo dev;
+  fa_status st = device_info(&dev);
+  if (st != FA_OK) return st;
+  fa::DecodeParams p;
+  std::memset(&p, 0, sizeof p);
+  p.q = q;
+  p.k_pages = k_pages;
+  p.v_pages = v_pages;
+  p.block_table = block_table;
+  p.ctx_lens = ctx_lens;
+  p.o = o;
+  p.lse = lse;
+  p.B = B;
+  p.H = H;
+  p.page_size = page_size;
+  p.max_pages = max_pages_per_seq;
+  p.num_pages = num_pages;
+  p.pages_per_split = pps;
+  p.nsplit_max = (max_pages_per_seq + pps - 1) / pps;
+  p.sl2 = scale * 1.4426950408889634f;
+  p.status = dev.status;
+  cudaError_t e =
+      fa::launch_decode_noalloc(p, d, dtype == FA_BF16, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "decode (no-alloc) launch");
+  return FA_OK;
+}
+
 fa_status fa_get_device_status(fa_stream_t stream) {
   DeviceInfo dev;
   fa_status st = device_info(&dev);

@@ -286,3 +286,59 @@ cudaError_t launch_selftest_timeout(uint32_t* status, uint64_t timeout_ns, cudaS
 }
 
 }  // namespace fa
+
+// ---------------------------------------------------------------------------------------
+// Paged decode without a caller-provided workspace (fa_decode_paged_noalloc).
+//
+// Some callers cannot hand the library a device buffer: a serving loop whose device
+// memory budget is fixed when it starts, or a host program that owns every device
+// allocation and gives its plug-ins no allocator. For them the split partials live in
+// this file-scope array instead: 16 MiB of FP32, reserved on every GPU that loads the
+// library and held until the process exits. Nothing here calls cudaMalloc or cudaFree.
+//
+// The array's name is only a host-side stand-in for the device object, so host code
+// never passes it to a kernel directly: the first call on each device (with that device
+// current) looks up the real device address with cudaGetSymbolAddress and keeps it.
+// All calls on a device share the array and it keeps whatever the last call left;
+// no part of it has to start at zero, because every partial the merge kernel reads is
+// written by the split kernel earlier in the same call. Two calls whose kernels overlap
+// on the GPU (for example on different streams) race on the array.
+// ---------------------------------------------------------------------------------------
+#include <mutex>
+
+namespace fa {
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;
+static __device__ __align__(256) float g_noalloc_scratch[kNoAllocScratchBytes / sizeof(float)];
+
+std::mutex g_noalloc_mu;
+float* g_noalloc_ptr[64] = {};
+
+}  // namespace
+
+size_t noalloc_scratch_bytes() { return kNoAllocScratchBytes; }
+
+cudaError_t launch_decode_noalloc(const DecodeParams& p_in, int D, bool bf16,
+                                  cudaStream_t stream) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  float* scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+      void* addr = nullptr;
+      e = cudaGetSymbolAddress(&addr, g_noalloc_scratch);
+      if (e != cudaSuccess) return e;
+      g_noalloc_ptr[dev] = static_cast<float*>(addr);
+    }
+    scratch = g_noalloc_ptr[dev];
+  }
+  DecodeParams p = p_in;
+  p.part = scratch;
+  return launch_decode(p, D, bf16, stream);
+}
+
+}  // namespace fa

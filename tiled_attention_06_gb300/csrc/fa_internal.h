@@ -55,6 +55,9 @@ struct DecodeParams {
 };
 
 cudaError_t launch_decode(const DecodeParams& p, int D, bool bf16, cudaStream_t stream);
+// Decode with the split partials in the library's own file-scope scratch array.
+size_t noalloc_scratch_bytes();
+cudaError_t launch_decode_noalloc(const DecodeParams& p, int D, bool bf16, cudaStream_t stream);
 cudaError_t launch_selftest_timeout(uint32_t* status, uint64_t timeout_ns, cudaStream_t stream);
 
 }  // namespace fa
