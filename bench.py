@@ -249,6 +249,8 @@ def run_ours(args, rank, world):
         dscale = 1 / math.sqrt(DECODE["d"])
 
     def prefill_call(**ex):
+        if args.block_m and "block_m" not in ex:
+            ex["block_m"] = args.block_m
         if ex:
             fa.fa_fwd_ex(qd, kd, vd, od, ld, scale, pcfg["mode"], pcfg["window"],
                          pcfg["n_global"], stream=stream, **ex)
@@ -257,7 +259,11 @@ def run_ours(args, rank, world):
                       stream=stream)
 
     def decode_call():
-        fa.fa_decode_paged(dq, dk, dv, dbt, dcl, do, dl, dscale, ws, stream=stream)
+        if args.pages_per_split:
+            fa.fa_decode_paged_ex(dq, dk, dv, dbt, dcl, do, dl, dscale, ws,
+                                  pages_per_split=args.pages_per_split, stream=stream)
+        else:
+            fa.fa_decode_paged(dq, dk, dv, dbt, dcl, do, dl, dscale, ws, stream=stream)
 
     if workload == "sweep":
         return run_sweep(args, fa, prefill_call, pflops, peaks, peak_kind, pcfg)
@@ -312,8 +318,8 @@ def run_ours(args, rank, world):
                               "(% of 8 TB/s)",
                     "value": value, "unit": "TFLOP/s", "higher_is_better": True,
                     "dtype": pcfg["dtype"]})
-        res["roofline"] = {"kernel": "prefill_kernel<128,128,bf16>" if pcfg["dtype"] == "bf16"
-                           else "prefill_kernel<128,128,f16>", "bound": "tensor",
+        res["roofline"] = {"kernel": f"prefill_bm256_kernel<128,128,{pcfg['dtype']}>",
+                           "bound": "tensor",
                            "achieved": achieved, "peak": tc_peak, "unit": "TFLOP/s",
                            "frac": achieved / tc_peak,
                            "peak_source": f"{peak_kind} bf16 burst (MEASURED_PEAKS.json)"
@@ -578,28 +584,29 @@ def run_reference(args, rank, world):
 
 # --------------------------------------------------------------------------- tile sweep
 def run_sweep(args, fa, prefill_call, pflops, peaks, peak_kind, pcfg):
-    """Key-block size sweep of the causal 4k prefill (the query block is 128 rows)."""
+    """Tile-size sweep of the causal 4k prefill: query rows per work item (BLOCK_M 128 or
+    256; 64 is not built) x key-block size (BLOCK_N 64 or 128)."""
     lines = []
-    for bn in (64, 128):
-        for _ in range(3):
-            prefill_call(block_n=bn)
-        torch.cuda.synchronize()
-        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        n = max(5, args.steps // 4)
-        s.record()
-        for _ in range(n):
-            prefill_call(block_n=bn)
-        e.record()
-        torch.cuda.synchronize()
-        ms = s.elapsed_time(e) / n
-        lines.append({"block_m": fa.fa_fwd_block_m(), "block_n": bn, "ms": ms,
-                      "tflops": pflops / ms / 1e9,
-                      "frac": pflops / ms / 1e9 / float(peaks["bf16_tflops"])})
+    for bm in (128, 256):
+        for bn in (64, 128):
+            for _ in range(3):
+                prefill_call(block_n=bn, block_m=bm)
+            torch.cuda.synchronize()
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            n = max(5, args.steps // 4)
+            s.record()
+            for _ in range(n):
+                prefill_call(block_n=bn, block_m=bm)
+            e.record()
+            torch.cuda.synchronize()
+            ms = s.elapsed_time(e) / n
+            lines.append({"block_m": bm, "block_n": bn, "ms": ms, "tflops": pflops / ms / 1e9,
+                          "frac": pflops / ms / 1e9 / float(peaks["bf16_tflops"])})
     return {"metric": "attention fwd TFLOP/s tile sweep", "value": max(l["tflops"] for l in lines),
             "unit": "TFLOP/s", "sweep": lines, "config": workload_config(pcfg, False, 1),
             "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
             "ms_per_step": min(l["ms"] for l in lines), "dtype": pcfg["dtype"],
-            "gpu_launches": 2 * (3 + max(5, args.steps // 4))}
+            "gpu_launches": 4 * (3 + max(5, args.steps // 4))}
 
 
 def main(argv=None):
@@ -614,6 +621,10 @@ def main(argv=None):
     ap.add_argument("--batch", type=int, default=None, help="override B (small profiling cases)")
     ap.add_argument("--heads", type=int, default=None, help="override H (small profiling cases)")
     ap.add_argument("--pool", type=int, default=None, help="override the decode page pool size")
+    ap.add_argument("--block-m", type=int, default=0,
+                    help="prefill query rows per work item (128 or 256; 0 = library default)")
+    ap.add_argument("--pages-per-split", type=int, default=0,
+                    help="decode pages per split-K partial (0 = library default)")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--prefill-traffic", type=float, default=None,

@@ -89,18 +89,21 @@ typedef struct fa_fwd_params {
   float scale;
   int mask_mode, window, n_global, dtype;
   int block_n;        /* key-block size: 0 = default (128), else 64 or 128 */
+  int block_m;        /* query rows per work item: 0 = default (256: two 128-row tiles
+                         sharing every K/V tile), else 128 or 256 */
   int num_ctas;       /* persistent grid size: 0 = one CTA per SM */
   int group_heads;    /* (batch, head) pairs scheduled together: 0 = sized for L2 */
   uint32_t timeout_us; /* per-wait time limit: 0 = 1 s */
-  /* Optional visit log, int32 [B*H, ceil(Sq/128), ceil(Sk/block_n)], zeroed by the
-   * caller. Every visited tile adds 16 + class (1 partial, 2 full); tiles the mask
+  /* Optional visit log, int32 [B*H, ceil(Sq/128), ceil(Sk/block_n)] (one row per
+   * 128-query tile whatever block_m is), zeroed by the caller. Every tile the kernel
+   * computes for those 128 queries adds 16 + class (1 partial, 2 full); tiles the mask
    * skips stay 0. */
   int32_t* trace;
 } fa_fwd_params;
 
 fa_status fa_fwd_ex(const fa_fwd_params* params, fa_stream_t stream);
 
-/* Query-block height of the prefill kernel (rows per work item), for sizing traces. */
+/* Query rows per tensor-core tile (128): the row granularity of the fa_fwd_ex trace. */
 int fa_fwd_block_m(void);
 
 /*

@@ -55,22 +55,24 @@ SHAPES = [(1, 1), (63, 63), (65, 65), (127, 129), (129, 127), (200, 333), (257, 
 @pytest.mark.parametrize("d,dt", [(64, "f16"), (128, "bf16"), (128, "f16")])
 @pytest.mark.parametrize("mask", ["none", "causal", "window"])
 @pytest.mark.parametrize("bn", [64, 128])
-def test_small_shapes(Sq, Sk, d, dt, mask, bn):
+@pytest.mark.parametrize("bm", [128, 256])
+def test_small_shapes(Sq, Sk, d, dt, mask, bn, bm):
     q, k, v = inputs.prefill_inputs(2, 3, Sq, Sk, d, DT[dt], seed=Sq * 1000 + Sk)
     if mask == "window":
         mode, w, g = fa.FA_MASK_CAUSAL_WINDOW, 50, 5
     else:
         mode, w, g = MASKS[mask]
     scale = 1 / math.sqrt(d)
-    o, lse = run_fwd(q, k, v, scale, mode, w, g, block_n=bn)
+    o, lse = run_fwd(q, k, v, scale, mode, w, g, block_n=bn, block_m=bm)
     ref_o, ref_l = oracle.attention(q, k, v, scale, mode, w, g)
-    compare(o, lse, ref_o, ref_l, f"{Sq}x{Sk} d{d} {dt} {mask} bn{bn}")
+    compare(o, lse, ref_o, ref_l, f"{Sq}x{Sk} d{d} {dt} {mask} bn{bn} bm{bm}")
 
 
 @pytest.mark.parametrize("mask,w,g", [("causal", 0, 0), ("window", 200, 70), ("window", 1, 0),
                                       ("window", 129, 300), ("none", 0, 0)])
 @pytest.mark.parametrize("Sq,Sk,bn", [(1000, 1000, 128), (700, 1100, 64), (1100, 700, 128)])
-def test_tile_trace_is_bit_exact(mask, w, g, Sq, Sk, bn):
+@pytest.mark.parametrize("bm", [128, 256])
+def test_tile_trace_is_bit_exact(mask, w, g, Sq, Sk, bn, bm):
     """The tiles the kernel visits, and the class it gives each, equal the oracle's
     brute-force tile classification; no tile is visited twice."""
     mode = {"none": fa.FA_MASK_NONE, "causal": fa.FA_MASK_CAUSAL,
@@ -80,7 +82,7 @@ def test_tile_trace_is_bit_exact(mask, w, g, Sq, Sk, bn):
     BM = fa.fa_fwd_block_m()
     nmb, nnb = -(-Sq // BM), -(-Sk // bn)
     trace = torch.zeros(B * H * nmb * nnb, dtype=torch.int32, device="cuda")
-    o, lse = run_fwd(q, k, v, 0.125, mode, w, g, block_n=bn, trace=trace)
+    o, lse = run_fwd(q, k, v, 0.125, mode, w, g, block_n=bn, block_m=bm, trace=trace)
     got = trace.cpu().numpy().reshape(B * H, nmb, nnb)
     want = np.zeros((nmb, nnb), dtype=np.int32)
     for mb in range(nmb):
@@ -142,10 +144,12 @@ def test_schedule_does_not_change_results():
     """Every work item is computed the same way whatever CTA runs it: outputs are
     bit-identical for any persistent grid size and head grouping."""
     q, k, v = inputs.prefill_inputs(2, 5, 700, 700, 128, torch.bfloat16, seed=9)
-    o0, l0 = run_fwd(q, k, v, 0.088, fa.FA_MASK_CAUSAL)
-    for ctas, hg in [(1, 1), (7, 3), (37, 0), (1000, 10)]:
-        o1, l1 = run_fwd(q, k, v, 0.088, fa.FA_MASK_CAUSAL, num_ctas=ctas, group_heads=hg)
-        assert torch.equal(o0, o1) and torch.equal(l0, l1)
+    for bm in (128, 256):
+        o0, l0 = run_fwd(q, k, v, 0.088, fa.FA_MASK_CAUSAL, block_m=bm)
+        for ctas, hg in [(1, 1), (7, 3), (37, 0), (1000, 10)]:
+            o1, l1 = run_fwd(q, k, v, 0.088, fa.FA_MASK_CAUSAL, num_ctas=ctas, group_heads=hg,
+                             block_m=bm)
+            assert torch.equal(o0, o1) and torch.equal(l0, l1)
 
 
 def test_causal_2k_fp16_full():

@@ -44,7 +44,8 @@ class FwdParams(ctypes.Structure):
     _fields_ = [("q", _vp), ("k", _vp), ("v", _vp), ("o", _vp), ("lse", _vp),
                 ("B", _i), ("H", _i), ("Sq", _i), ("Sk", _i), ("d", _i), ("scale", _f),
                 ("mask_mode", _i), ("window", _i), ("n_global", _i), ("dtype", _i),
-                ("block_n", _i), ("num_ctas", _i), ("group_heads", _i), ("timeout_us", _u32),
+                ("block_n", _i), ("block_m", _i), ("num_ctas", _i), ("group_heads", _i),
+                ("timeout_us", _u32),
                 ("trace", _vp)]
 
 
@@ -158,12 +159,13 @@ def fa_fwd(q, k, v, o, lse, scale, mask_mode=FA_MASK_NONE, window=0, n_global=0,
 
 
 def fa_fwd_ex(q, k, v, o, lse, scale, mask_mode=FA_MASK_NONE, window=0, n_global=0,
-              block_n=0, num_ctas=0, group_heads=0, timeout_us=0, trace=None, stream=None):
+              block_n=0, block_m=0, num_ctas=0, group_heads=0, timeout_us=0, trace=None,
+              stream=None):
     _need_cuda_contig(q=q, k=k, v=v, o=o, lse=lse, trace=trace)
     B, H, Sq, d = q.shape
     p = FwdParams(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), _ptr(lse), B, H, Sq,
                   k.shape[2], d, float(scale), mask_mode, window, n_global, _dtype_code(q),
-                  block_n, num_ctas, group_heads, timeout_us, _ptr(trace))
+                  block_n, block_m, num_ctas, group_heads, timeout_us, _ptr(trace))
     _check(lib().fa_fwd_ex(ctypes.byref(p), _stream(stream)))
 
 

@@ -125,6 +125,8 @@ fa_status check_fwd(const fa_fwd_params& p) {
     return fail(FA_ERR_INVALID_ARG, "problem too large for 32-bit tile indices");
   if (p.block_n != 0 && p.block_n != 64 && p.block_n != 128)
     return fail(FA_ERR_UNSUPPORTED, "block_n %d (supported: 64, 128)", p.block_n);
+  if (p.block_m != 0 && p.block_m != 128 && p.block_m != 256)
+    return fail(FA_ERR_UNSUPPORTED, "block_m %d (supported: 128, 256)", p.block_m);
   if (p.num_ctas < 0 || p.group_heads < 0) return fail(FA_ERR_INVALID_ARG, "negative plan parameter");
   return FA_OK;
 }
@@ -137,7 +139,7 @@ int fa_version(void) { return 100; }
 
 const char* fa_last_error_string(void) { return t_last_error.c_str(); }
 
-int fa_fwd_block_m(void) { return fa::prefill_block_m(); }
+int fa_fwd_block_m(void) { return fa::prefill_tile_rows(); }
 
 fa_status fa_fwd_ex(const fa_fwd_params* params, fa_stream_t stream) {
   if (!params) return fail(FA_ERR_INVALID_ARG, "params is null");
@@ -148,7 +150,7 @@ fa_status fa_fwd_ex(const fa_fwd_params* params, fa_stream_t stream) {
   DeviceInfo dev;
   if ((st = device_info(&dev)) != FA_OK) return st;
 
-  const int BM = fa::prefill_block_m();
+  const int BM = a.block_m ? a.block_m : 256;
   const int BN = a.block_n ? a.block_n : 128;
   const int BH = a.B * a.H;
   fa::PrefillLaunch L;
@@ -184,11 +186,12 @@ fa_status fa_fwd_ex(const fa_fwd_params* params, fa_stream_t stream) {
   if (L.grid > p.total_items) L.grid = p.total_items;
 
   const bool bf16 = a.dtype == FA_BF16;
-  if ((st = make_map(&L.tmQ, a.q, bf16, a.d, a.Sq, BH, BM)) != FA_OK) return st;
+  if ((st = make_map(&L.tmQ, a.q, bf16, a.d, a.Sq, BH, fa::prefill_tile_rows())) != FA_OK)
+    return st;
   // with Sk == 0 no key tile is ever loaded; the maps only need a valid address
   if ((st = make_map(&L.tmK, a.Sk ? a.k : a.q, bf16, a.d, a.Sk, BH, BN)) != FA_OK) return st;
   if ((st = make_map(&L.tmV, a.Sk ? a.v : a.q, bf16, a.d, a.Sk, BH, BN)) != FA_OK) return st;
-  cudaError_t e = fa::launch_prefill(L, a.d, BN, bf16, reinterpret_cast<cudaStream_t>(stream));
+  cudaError_t e = fa::launch_prefill(L, a.d, BN, BM, bf16, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
   return FA_OK;
 }

@@ -18,14 +18,14 @@ struct PrefillParams {
   void* o;            // [B,H,Sq,D] 16-bit
   float* lse;         // [B,H,Sq] or nullptr
   int BH, Sq, Sk;
-  int nmb, nnb;       // query blocks (BM rows), key blocks (BN keys)
+  int nmb, nnb;       // query blocks (BM rows per work item), key blocks (BN keys)
   int mask_mode, window, n_global;
   float sl2;          // scale * log2(e)
   int group_heads;    // (batch, head) pairs per scheduling group
   int total_items;    // BH * nmb
   uint32_t* status;   // device status word
   uint64_t timeout_ns;
-  int32_t* trace;     // optional [BH, nmb, nnb] visit log (16 + class per visit)
+  int32_t* trace;     // optional [BH, ceil(Sq/128), nnb] visit log (16 + class per visit)
 };
 
 struct PrefillLaunch {
@@ -34,8 +34,9 @@ struct PrefillLaunch {
   int grid;
 };
 
-int prefill_block_m();
-cudaError_t launch_prefill(const PrefillLaunch& L, int D, int BN, bool bf16, cudaStream_t stream);
+int prefill_tile_rows();
+cudaError_t launch_prefill(const PrefillLaunch& L, int D, int BN, int BM, bool bf16,
+                           cudaStream_t stream);
 
 struct DecodeParams {
   const void* q;            // [B,H,D]
