@@ -89,8 +89,8 @@ typedef struct fa_fwd_params {
   float scale;
   int mask_mode, window, n_global, dtype;
   int block_n;        /* key-block size: 0 = default (128), else 64 or 128 */
-  int block_m;        /* query rows per work item: 0 = default (256: two 128-row tiles
-                         sharing every K/V tile), else 128 or 256 */
+  int block_m;        /* query rows per work item: 0 = default (128), or 256 (two
+                         128-row tiles sharing every K/V tile) */
   int num_ctas;       /* persistent grid size: 0 = one CTA per SM */
   int group_heads;    /* (batch, head) pairs scheduled together: 0 = sized for L2 */
   uint32_t timeout_us; /* per-wait time limit: 0 = 1 s */

@@ -5,15 +5,22 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <array>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <functional>
+#include <map>
+#include <memory>
 #include <mutex>
+#include <queue>
 #include <string>
+#include <vector>
 
 #include "fa.h"
 #include "fa_internal.h"
+#include "fa_plan.h"
 
 namespace {
 
@@ -102,6 +109,53 @@ fa_status make_map(CUtensorMap* m, const void* ptr, bool bf16, int D, int S, int
   return FA_OK;
 }
 
+// Per-CTA item lists for a persistent prefill launch. Items are taken in their numbering
+// order (head groups, then query blocks from most keys to fewest) and each goes to the CTA
+// that would be free first, with cost = visited key blocks + a fixed per-item overhead:
+// the list schedule a dynamic work queue would produce, fixed in advance so that the
+// kernel needs no global counter. Cached per shape; the kernel receives a copy at launch.
+constexpr double kItemOverheadTiles = 2.0;
+std::mutex g_plan_mu;
+std::map<std::array<int, 11>, std::unique_ptr<fa::PrefillSched>> g_plans;
+
+const fa::PrefillSched* plan_for(const fa::PrefillParams& p, int BM, int BN, int grid) {
+  const std::array<int, 11> key{p.BH, p.Sq, p.Sk, BM, BN, p.mask_mode, p.window, p.n_global,
+                                p.group_heads, grid, p.nmb};
+  std::lock_guard<std::mutex> lock(g_plan_mu);
+  auto it = g_plans.find(key);
+  if (it != g_plans.end()) return it->second.get();
+  if (g_plans.size() >= 256) g_plans.clear();  // launches copy their plan; old ones can go
+  auto plan = std::make_unique<fa::PrefillSched>();
+  std::memset(plan.get(), 0, sizeof(fa::PrefillSched));
+  if (grid <= fa::kSchedMaxCtas && p.total_items <= fa::kSchedMaxItems) {
+    using Slot = std::pair<double, int>;  // (busy until, cta)
+    std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> free_at;
+    for (int c = 0; c < grid; ++c) free_at.push({0.0, c});
+    std::vector<std::vector<uint16_t>> lists(grid);
+    for (int t = 0; t < p.total_items; ++t) {
+      int bh, mb;
+      fa::item_coords(t, p, bh, mb);
+      const fa::Range r = fa::key_range(mb * BM, std::min(mb * BM + BM, p.Sq), BN, p);
+      const int n = fa::range_count(r);
+      Slot s = free_at.top();
+      free_at.pop();
+      lists[s.second].push_back(static_cast<uint16_t>(t));
+      s.first += n + kItemOverheadTiles;
+      free_at.push(s);
+    }
+    int k = 0;
+    for (int c = 0; c < grid; ++c) {
+      plan->offs[c] = static_cast<uint16_t>(k);
+      for (uint16_t t : lists[c]) plan->items[k++] = t;
+    }
+    plan->offs[grid] = static_cast<uint16_t>(k);
+    plan->enabled = 1;
+  }
+  const fa::PrefillSched* out = plan.get();
+  g_plans.emplace(key, std::move(plan));
+  return out;
+}
+
 fa_status check_fwd(const fa_fwd_params& p) {
   // q and o may be null only when Sq == 0, k and v only when Sk == 0
   if ((p.Sq > 0 && (!p.q || !p.o)) || (p.Sk > 0 && (!p.k || !p.v)))
@@ -150,7 +204,7 @@ fa_status fa_fwd_ex(const fa_fwd_params* params, fa_stream_t stream) {
   DeviceInfo dev;
   if ((st = device_info(&dev)) != FA_OK) return st;
 
-  const int BM = a.block_m ? a.block_m : 256;
+  const int BM = a.block_m ? a.block_m : 128;
   const int BN = a.block_n ? a.block_n : 128;
   const int BH = a.B * a.H;
   fa::PrefillLaunch L;
@@ -184,6 +238,7 @@ fa_status fa_fwd_ex(const fa_fwd_params* params, fa_stream_t stream) {
   p.trace = a.trace;
   L.grid = a.num_ctas ? a.num_ctas : dev.sms;
   if (L.grid > p.total_items) L.grid = p.total_items;
+  L.sched = plan_for(p, BM, BN, L.grid);
 
   const bool bf16 = a.dtype == FA_BF16;
   if ((st = make_map(&L.tmQ, a.q, bf16, a.d, a.Sq, BH, fa::prefill_tile_rows())) != FA_OK)

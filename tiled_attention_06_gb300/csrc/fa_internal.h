@@ -28,9 +28,12 @@ struct PrefillParams {
   int32_t* trace;     // optional [BH, ceil(Sq/128), nnb] visit log (16 + class per visit)
 };
 
+struct PrefillSched;  // fa_plan.h
+
 struct PrefillLaunch {
   CUtensorMap tmQ, tmK, tmV;
   PrefillParams p;
+  const PrefillSched* sched;  // host copy of the per-CTA item lists (passed by value)
   int grid;
 };
 

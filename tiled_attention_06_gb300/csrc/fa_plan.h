@@ -1,0 +1,97 @@
+// Work-item planning shared by the host planner (fa_api.cu) and the prefill kernels:
+// which key blocks a block of query rows visits, how work items are numbered, and the
+// per-CTA item lists that balance a persistent launch.
+#pragma once
+
+#include <cstdint>
+
+#include "fa_internal.h"
+
+#if defined(__CUDACC__)
+#define FA_HD __host__ __device__ __forceinline__
+#else
+#define FA_HD inline
+#endif
+
+namespace fa {
+
+// Key blocks visited by the query rows [m0, m1): [0, a_end) then [b_start, b_end),
+// a_end <= b_start. Closed form of the mask: every block inside holds at least one
+// visible pair for these rows, every block outside holds none.
+struct Range {
+  int a_end, b_start, b_end;
+};
+
+FA_HD int imin(int a, int b) { return a < b ? a : b; }
+FA_HD int imax(int a, int b) { return a > b ? a : b; }
+
+FA_HD Range key_range(int m0, int m1, int BN, const PrefillParams& p) {
+  Range r{0, 0, p.nnb};
+  if (m0 >= m1) return Range{0, 0, 0};
+  if (p.mask_mode == FA_MASK_NONE) return r;
+  const int delta = p.Sk - p.Sq;
+  const int r_lo = m0 + delta;      // key position of the first row
+  const int r_hi = m1 - 1 + delta;  // key position of the last row
+  if (r_hi < 0) return Range{0, 0, 0};
+  r.b_end = imin(p.nnb, r_hi / BN + 1);
+  if (p.mask_mode == FA_MASK_CAUSAL_WINDOW) {
+    const int band_lo = imax(0, r_lo - p.window + 1);
+    r.b_start = imin(band_lo / BN, r.b_end);
+    const int g_keys = imin(imin(p.n_global, r_hi + 1), p.Sk);
+    r.a_end = g_keys > 0 ? (g_keys + BN - 1) / BN : 0;
+    if (r.a_end >= r.b_start) {  // the two ranges touch: one range [0, b_end)
+      r.a_end = 0;
+      r.b_start = 0;
+    }
+  }
+  return r;
+}
+
+FA_HD int range_count(const Range& r) { return r.a_end + r.b_end - r.b_start; }
+FA_HD int range_nb(const Range& r, int t) { return t < r.a_end ? t : r.b_start + (t - r.a_end); }
+FA_HD bool range_has(const Range& r, int nb) {
+  return nb < r.a_end || (nb >= r.b_start && nb < r.b_end);
+}
+
+// Work item t -> (batch*head, query block). Order: groups of `group_heads` heads; inside
+// a group, query blocks from the last (most keys under a causal mask) to the first;
+// inside that, the heads of the group.
+FA_HD void item_coords(int t, const PrefillParams& p, int& bh, int& mb) {
+  const int per_group = p.group_heads * p.nmb;
+  const int g = t / per_group;
+  const int gsize = imin(p.group_heads, p.BH - g * p.group_heads);
+  const int rem = t - g * per_group;
+  mb = p.nmb - 1 - rem / gsize;
+  bh = g * p.group_heads + rem % gsize;
+}
+
+// Snake assignment of items to persistent CTAs: round r covers items [r*G, r*G+G), walked
+// forwards on even rounds and backwards on odd ones.
+FA_HD int item_of_round(int r, int G, int cta) { return r * G + ((r & 1) ? (G - 1 - cta) : cta); }
+
+// Per-CTA item lists, passed to the kernel in its parameter space. CTA c runs
+// items[offs[c]] .. items[offs[c+1]-1] in that order. When `enabled` is 0 (more CTAs or
+// items than fit) the kernel falls back to the snake order above.
+constexpr int kSchedMaxCtas = 192;
+constexpr int kSchedMaxItems = 14336;
+struct PrefillSched {
+  int32_t enabled;
+  uint16_t offs[kSchedMaxCtas + 1];
+  uint16_t items[kSchedMaxItems];
+};
+
+// The k-th item of CTA `cta`: false when it has none left; t = -1 for an empty snake slot.
+FA_HD bool item_at(const PrefillSched& s, const PrefillParams& p, int cta, int G, int k, int& t) {
+  if (s.enabled) {
+    const int i = s.offs[cta] + k;
+    if (i >= s.offs[cta + 1]) return false;
+    t = s.items[i];
+    return true;
+  }
+  if (k * G >= p.total_items) return false;
+  t = item_of_round(k, G, cta);
+  if (t >= p.total_items) t = -1;
+  return true;
+}
+
+}  // namespace fa

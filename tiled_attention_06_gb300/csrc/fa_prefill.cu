@@ -39,6 +39,7 @@
 #include <cstdint>
 
 #include "fa_internal.h"
+#include "fa_plan.h"
 #include "fa_ptx.cuh"
 
 namespace fa {
@@ -55,62 +56,6 @@ constexpr int pow2_at_least(int x) {
 }
 
 // ------------------------------------------------------------------ shared helpers
-
-// Key blocks visited by the query rows [m0, m1): [0, a_end) then [b_start, b_end),
-// a_end <= b_start. Closed form of the mask: every block inside holds at least one
-// visible pair for these rows, every block outside holds none.
-struct Range {
-  int a_end, b_start, b_end;
-};
-
-template <int BN>
-__device__ __forceinline__ Range key_range(int m0, int m1, const PrefillParams& p) {
-  Range r{0, 0, p.nnb};
-  if (m0 >= m1) return Range{0, 0, 0};
-  if (p.mask_mode == FA_MASK_NONE) return r;
-  const int delta = p.Sk - p.Sq;
-  const int r_lo = m0 + delta;      // key position of the first row
-  const int r_hi = m1 - 1 + delta;  // key position of the last row
-  if (r_hi < 0) return Range{0, 0, 0};
-  r.b_end = min(p.nnb, r_hi / BN + 1);
-  if (p.mask_mode == FA_MASK_CAUSAL_WINDOW) {
-    const int band_lo = max(0, r_lo - p.window + 1);
-    r.b_start = min(band_lo / BN, r.b_end);
-    const int g_keys = min(min(p.n_global, r_hi + 1), p.Sk);
-    r.a_end = g_keys > 0 ? (g_keys + BN - 1) / BN : 0;
-    if (r.a_end >= r.b_start) {  // the two ranges touch: one range [0, b_end)
-      r.a_end = 0;
-      r.b_start = 0;
-    }
-  }
-  return r;
-}
-
-__device__ __forceinline__ int range_count(const Range& r) { return r.a_end + r.b_end - r.b_start; }
-__device__ __forceinline__ int range_nb(const Range& r, int t) {
-  return t < r.a_end ? t : r.b_start + (t - r.a_end);
-}
-__device__ __forceinline__ bool range_has(const Range& r, int nb) {
-  return nb < r.a_end || (nb >= r.b_start && nb < r.b_end);
-}
-
-// Work item t -> (batch*head, query block). Order: groups of `group_heads` heads; inside
-// a group, query blocks from the last (most keys under a causal mask) to the first;
-// inside that, the heads of the group.
-__device__ __forceinline__ void item_coords(int t, const PrefillParams& p, int& bh, int& mb) {
-  const int per_group = p.group_heads * p.nmb;
-  const int g = t / per_group;
-  const int gsize = min(p.group_heads, p.BH - g * p.group_heads);
-  const int rem = t - g * per_group;
-  mb = p.nmb - 1 - rem / gsize;
-  bh = g * p.group_heads + rem % gsize;
-}
-
-// Snake assignment of items to persistent CTAs: round r covers items [r*G, r*G+G), walked
-// forwards on even rounds and backwards on odd ones.
-__device__ __forceinline__ int item_of_round(int r, int G, int cta) {
-  return r * G + ((r & 1) ? (G - 1 - cta) : cta);
-}
 
 // True when every (row, key) pair of the 128-row tile at m0 and key block nb is in range
 // and visible.
@@ -135,21 +80,28 @@ __device__ __forceinline__ uint32_t pack2(float a, float b, bool bf16) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-// The online-softmax step for one S tile, by one thread for its row:
-// S (BN FP32 columns at s_col) is loaded from TMEM, masked unless the tile is full,
-// the running max is updated, O (D columns at o_col) and l are rescaled when the max
-// rose by more than kTau (warp-uniform decision; `before_rescale` makes O safe to touch
-// and returns false on abort), and P = 2^(S*sl2 - m) is written over the first BN/2
-// columns of S as packed 16-bit pairs. Returns false on abort.
-template <int D, int BN, bool BF16, typename PreRescale>
-__device__ __forceinline__ bool softmax_tile(uint32_t t_lane, uint32_t s_col, uint32_t o_col,
-                                             bool full, int n0, int pos_q,
+// The online-softmax step for one S tile, by one thread for NC columns of its row:
+// S (NC FP32 columns at s_col, keys n0..n0+NC-1) is loaded from TMEM and masked unless
+// the tile is full; `exchange` turns this thread's partial row maximum into the maximum
+// of the whole row (identity when NC covers the row); the running max is updated; O (ON
+// columns at o_col) and l are rescaled when the max rose by more than kTau (warp-uniform
+// decision; `before_rescale` makes O safe to touch and returns false on abort); and
+// P = 2^(S*sl2 - m) is written as packed 16-bit pairs to NC/2 columns at p_col.
+// l accumulates the sum over this thread's NC columns. Returns false on abort.
+template <int NC, int ON, bool BF16, typename Exchange, typename PreRescale>
+__device__ __forceinline__ bool softmax_cols(uint32_t t_lane, uint32_t s_col, uint32_t p_col,
+                                             uint32_t o_col, bool full, int n0, int pos_q,
                                              const PrefillParams& p, float& m_ref, float& l,
-                                             PreRescale before_rescale) {
-  uint32_t s[BN];
+                                             Exchange exchange, PreRescale before_rescale) {
+  static_assert(NC == 32 || NC % 64 == 0, "column count");
+  uint32_t s[NC];
+  if constexpr (NC == 32) {
+    tmem_ld32(t_lane + s_col, s);
+  } else {
 #pragma unroll
-  for (int c = 0; c < BN / 64; ++c) tmem_ld64(t_lane + s_col + c * 64, s + c * 64);
-  tmem_ld_wait<BN>(s);
+    for (int c = 0; c < NC / 64; ++c) tmem_ld64(t_lane + s_col + c * 64, s + c * 64);
+  }
+  tmem_ld_wait<NC>(s);
   if (!full) {
     int lim = min(pos_q, p.Sk - 1) - n0;
     if (p.mask_mode == FA_MASK_NONE) lim = p.Sk - 1 - n0;
@@ -159,21 +111,22 @@ __device__ __forceinline__ bool softmax_tile(uint32_t t_lane, uint32_t s_col, ui
       gl = p.n_global - n0;
     }
 #pragma unroll
-    for (int c = 0; c < BN; ++c) {
+    for (int c = 0; c < NC; ++c) {
       const bool vis = (c <= lim) && (c >= lo || c < gl);
       if (!vis) s[c] = __float_as_uint(-INFINITY);
     }
   }
-  // row max: four independent chains of three-input maxima, then combined
+  // partial row max: four independent chains of three-input maxima, then combined
+  // (columns 0-7 seed the chains; each later group of 8 adds two columns per chain)
   float mx[4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) mx[i] = __uint_as_float(s[i]);
+  for (int i = 0; i < 4; ++i) mx[i] = fmaxf(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1]));
 #pragma unroll
-  for (int c = 4; c < BN; c += 8)
+  for (int c = 8; c < NC; c += 8)
 #pragma unroll
     for (int i = 0; i < 4; ++i)
       mx[i] = max3f(mx[i], __uint_as_float(s[c + 2 * i]), __uint_as_float(s[c + 2 * i + 1]));
-  const float m_tile = max3f(mx[0], mx[1], fmaxf(mx[2], mx[3])) * p.sl2;
+  const float m_tile = exchange(max3f(mx[0], mx[1], fmaxf(mx[2], mx[3]))) * p.sl2;
   const float m_new = fmaxf(m_ref, m_tile);
   const bool need = (m_ref != -INFINITY) && (m_new > m_ref + kTau);
   if (m_ref == -INFINITY) m_ref = m_new;
@@ -185,7 +138,7 @@ __device__ __forceinline__ bool softmax_tile(uint32_t t_lane, uint32_t s_col, ui
       m_ref = m_new;
     }
 #pragma unroll 1
-    for (int c = 0; c < D / 32; ++c) {
+    for (int c = 0; c < ON / 32; ++c) {
       uint32_t ov[32];
       tmem_ld32(t_lane + o_col + c * 32, ov);
       tmem_ld_wait<32>(ov);
@@ -200,7 +153,7 @@ __device__ __forceinline__ bool softmax_tile(uint32_t t_lane, uint32_t s_col, ui
   const uint64_t scale2 = f2(p.sl2, p.sl2), neg_m2 = f2(-m_use, -m_use);
   uint64_t acc[4] = {0, 0, 0, 0};
 #pragma unroll
-  for (int c = 0; c < BN; c += 2) {
+  for (int c = 0; c < NC; c += 2) {
     const uint64_t x = f2_fma(f2(__uint_as_float(s[c]), __uint_as_float(s[c + 1])), scale2, neg_m2);
     float x0, x1;
     f2_split(x, x0, x1);
@@ -211,10 +164,24 @@ __device__ __forceinline__ bool softmax_tile(uint32_t t_lane, uint32_t s_col, ui
   float a0, a1;
   f2_split(f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3])), a0, a1);
   l += a0 + a1;
+  if constexpr (NC == 32) {
+    tmem_st16(t_lane + p_col, s);
+  } else {
 #pragma unroll
-  for (int c = 0; c < BN / 64; ++c) tmem_st32(t_lane + s_col + c * 32, s + c * 32);
+    for (int c = 0; c < NC / 64; ++c) tmem_st32(t_lane + p_col + c * 32, s + c * 32);
+  }
   tmem_st_wait();
   return true;
+}
+
+// A whole row per thread.
+template <int D, int BN, bool BF16, typename PreRescale>
+__device__ __forceinline__ bool softmax_tile(uint32_t t_lane, uint32_t s_col, uint32_t o_col,
+                                             bool full, int n0, int pos_q,
+                                             const PrefillParams& p, float& m_ref, float& l,
+                                             PreRescale before_rescale) {
+  return softmax_cols<BN, D, BF16>(t_lane, s_col, s_col, o_col, full, n0, pos_q, p, m_ref, l,
+                                   [](float m) { return m; }, before_rescale);
 }
 
 // Epilogue for one thread's row: O (D columns at o_col) / l rounded to the dtype, and
@@ -262,15 +229,23 @@ __device__ __forceinline__ void wait_quiet(uint32_t bar, uint32_t parity, const 
 
 // S = Q K^T for one 128-row tile: D/16 MMAs of K = 16, both operands K-major in
 // 128-byte-swizzled shared memory (rows of 128 bytes, 8-row groups 1024 bytes apart,
-// one region per 64 elements of d).
+// one region per 64 elements of d). The descriptors are built once; each MMA adds a
+// compile-time offset to the start-address field (addresses stay below 256 KB, so the
+// 14-bit field never carries), which keeps the issuing thread's dependency chain short.
 template <int D, int BN, bool BF16>
 __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_smem, uint32_t k_smem) {
   constexpr uint32_t id = idesc_f16(BF16, kTile, BN, false);
+  const uint64_t a0 = smem_desc_sw128(q_smem, 16, 1024);
+  const uint64_t b0 = smem_desc_sw128(k_smem, 16, 1024);
+  if constexpr (D == 128) {
+    constexpr int QC = kTile * 128 / 16, KC = BN * 128 / 16;  // next 64-element region
+    umma_ss8<2, 4, 6, QC, QC + 2, QC + 4, QC + 6, 2, 4, 6, KC, KC + 2, KC + 4, KC + 6>(d_tmem, a0,
+                                                                                       b0, id);
+  } else {
 #pragma unroll
-  for (int kk = 0; kk < D / 16; ++kk) {
-    const uint64_t a = smem_desc_sw128(q_smem + (kk / 4) * (kTile * 128) + (kk % 4) * 32, 16, 1024);
-    const uint64_t b = smem_desc_sw128(k_smem + (kk / 4) * (BN * 128) + (kk % 4) * 32, 16, 1024);
-    umma_ss(d_tmem, a, b, id, kk > 0);
+    for (int kk = 0; kk < D / 16; ++kk)
+      umma_ss(d_tmem, a0 + static_cast<uint64_t>(kk * 2), b0 + static_cast<uint64_t>(kk * 2), id,
+              kk > 0);
   }
 }
 
@@ -281,10 +256,14 @@ template <int D, int BN, bool BF16>
 __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint32_t v_smem,
                                          bool accumulate) {
   constexpr uint32_t id = idesc_f16(BF16, kTile, D, true);
+  const uint64_t b0 = smem_desc_sw128(v_smem, BN * 128, 1024);
+  if constexpr (BN == 128) {
+    umma_ts8<16 * 128 / 16>(o_tmem, p_tmem, b0, id, accumulate ? 1u : 0u);
+  } else {
 #pragma unroll
-  for (int kk = 0; kk < BN / 16; ++kk) {
-    const uint64_t b = smem_desc_sw128(v_smem + kk * 16 * 128, BN * 128, 1024);
-    umma_ts(o_tmem, p_tmem + kk * 8, b, id, (accumulate || kk > 0) ? 1u : 0u);
+    for (int kk = 0; kk < BN / 16; ++kk)
+      umma_ts(o_tmem, p_tmem + kk * 8, b0 + static_cast<uint64_t>(kk * 128), id,
+              (accumulate || kk > 0) ? 1u : 0u);
   }
 }
 
@@ -329,7 +308,8 @@ template <int D, int BN, bool BF16>
 __global__ void __launch_bounds__(kThreads256, 1)
     prefill_bm256_kernel(const __grid_constant__ CUtensorMap tmQ,
                          const __grid_constant__ CUtensorMap tmK,
-                         const __grid_constant__ CUtensorMap tmV, const PrefillParams p) {
+                         const __grid_constant__ CUtensorMap tmV, const PrefillParams p,
+                         const __grid_constant__ PrefillSched sched) {
   using C = Cfg256<D, BN>;
   constexpr int BM = 2 * kTile;
   extern __shared__ uint8_t smem_raw[];
@@ -388,12 +368,12 @@ __global__ void __launch_bounds__(kThreads256, 1)
       uint32_t fills[8] = {0, 0, 0, 0, 0, 0, 0, 0};
       uint32_t qfills[2] = {0, 0};
       bool ok = true;
-      for (int r = 0; ok && r * G < p.total_items; ++r) {
-        const int t = item_of_round(r, G, cta);
-        if (t >= p.total_items) continue;
+      int t;
+      for (int k = 0; ok && item_at(sched, p, cta, G, k, t); ++k) {
+        if (t < 0) continue;
         int bh, mb;
         item_coords(t, p, bh, mb);
-        const Range rg = key_range<BN>(mb * BM, min(mb * BM + BM, p.Sq), p);
+        const Range rg = key_range(mb * BM, min(mb * BM + BM, p.Sq), BN, p);
         const int n = range_count(rg);
         if (n == 0) continue;
         for (int q = 0; q < 2 && ok; ++q) {
@@ -434,12 +414,12 @@ __global__ void __launch_bounds__(kThreads256, 1)
       const uint32_t tO[2] = {tmem + 2 * BN, tmem + 2 * BN + D};
       uint32_t pos = 0, ii = 0, tc = 0;
       bool ok = true;
-      for (int r = 0; ok && r * G < p.total_items; ++r) {
-        const int t = item_of_round(r, G, cta);
-        if (t >= p.total_items) continue;
+      int t;
+      for (int k = 0; ok && item_at(sched, p, cta, G, k, t); ++k) {
+        if (t < 0) continue;
         int bh, mb;
         item_coords(t, p, bh, mb);
-        const Range rg = key_range<BN>(mb * BM, min(mb * BM + BM, p.Sq), p);
+        const Range rg = key_range(mb * BM, min(mb * BM + BM, p.Sq), BN, p);
         const int n = range_count(rg);
         if (n == 0) continue;
         {  // S_A(0), S_B(0) with K0
@@ -505,12 +485,12 @@ __global__ void __launch_bounds__(kThreads256, 1)
     const int delta = p.Sk - p.Sq;
     uint32_t ii = 0, tc = 0;
     bool ok = true;
-    for (int r = 0; ok && r * G < p.total_items; ++r) {
-      const int t = item_of_round(r, G, cta);
-      if (t >= p.total_items) continue;
+    int t;
+    for (int k = 0; ok && item_at(sched, p, cta, G, k, t); ++k) {
+      if (t < 0) continue;
       int bh, mb;
       item_coords(t, p, bh, mb);
-      const Range rg = key_range<BN>(mb * BM, min(mb * BM + BM, p.Sq), p);
+      const Range rg = key_range(mb * BM, min(mb * BM + BM, p.Sq), BN, p);
       const int n = range_count(rg);
       const int m0 = mb * BM + q * kTile;  // first row of this tile
       const int qrow = m0 + row;
@@ -519,7 +499,7 @@ __global__ void __launch_bounds__(kThreads256, 1)
         if (qrow < p.Sq) store_zero_row<D>(orow, p);
         continue;
       }
-      const Range mine = key_range<BN>(m0, min(m0 + kTile, p.Sq), p);
+      const Range mine = key_range(m0, min(m0 + kTile, p.Sq), BN, p);
       const int pos_q = qrow + delta;
       float m_ref = -INFINITY, l = 0.f;
       for (int j = 0; j < n; ++j) {
@@ -560,49 +540,101 @@ __global__ void __launch_bounds__(kThreads256, 1)
 }
 
 // ------------------------------------------------------------------ BM = 128 kernel
+//
+// One 128-row query tile per work item, and one continuous stream of tiles across the
+// items a CTA runs. Four warpgroups:
+//   warps 0-3   softmax, first half of every score row (keys 0..BN/2-1 of the tile)
+//   warps 4-7   softmax, second half; warps w and w+4 own the same 32 rows (TMEM lanes)
+//               and swap their partial row maxima through shared memory each tile, so
+//               that every scheduler has two independent softmax streams
+//   warps 8-11  epilogue: O / l from TMEM to global memory, LSE; it works on the
+//               previous item while the softmax warps start the next one
+//   warp 12     TMA producer, warp 13 MMA issuer (one thread each), warps 14-15 idle
+// TMEM: S0 [0,BN), S1 [BN,2BN) hold the score tiles of consecutive tiles; O0, O1
+// (D columns each, from 2BN) hold the outputs of consecutive items. Q is double
+// buffered in shared memory, so the first score tile of the next item is computed while
+// the softmax still works on the last tile of the current one. Tensor-pipe order:
+//   S(0) S(1) PV(0) S(2) PV(1) ... S(g+1) PV(g) ..., item boundaries included,
+// so S(g) is always issued after PV(g-2) (it reuses that tile's S buffer).
 
-constexpr int kThreads128 = 192;
-constexpr int kTmaWarp128 = 4;
-constexpr int kMmaWarp128 = 5;
+constexpr int kThreads128 = 512;
+constexpr int kTmaWarp128 = 12;
+constexpr int kMmaWarp128 = 13;
+// launched at 128 registers per thread: 128 x (152 + 152 + 104 + 104) = 512 x 128 = 65,536
+constexpr uint32_t kRegs128Softmax = 152;
+constexpr uint32_t kRegs128Epilogue = 104;
+constexpr uint32_t kRegs128Producer = 104;
 
 template <int D, int BN>
 struct Cfg128 {
   static constexpr int KCH = D / 64;
-  static constexpr int Q_BYTES = kTile * D * 2;
+  static constexpr int Q_BYTES = kTile * D * 2;  // one Q buffer
   static constexpr int TILE_BYTES = BN * D * 2;
+  static constexpr int STATS_BYTES = 2 * 2 * kTile * 8;  // (m, l) per row and half, two items
+  static constexpr int XMAX_BYTES = 2 * 2 * kTile * 4;   // partial row maxima, two tiles
   static constexpr int BAR_BYTES = 1024;
-  static constexpr int NSLOT_FIT = (int)((kSmemLimit - 1024 - BAR_BYTES - Q_BYTES) / TILE_BYTES);
+  static constexpr int NSLOT_FIT = (int)((kSmemLimit - 1024 - BAR_BYTES - STATS_BYTES -
+                                          XMAX_BYTES - 2 * Q_BYTES) / TILE_BYTES);
   static constexpr int NSLOT = NSLOT_FIT > 8 ? 8 : NSLOT_FIT;
-  static constexpr int SMEM = 1024 + Q_BYTES + NSLOT * TILE_BYTES + BAR_BYTES;
-  static constexpr int TMEM_COLS = pow2_at_least(2 * BN + D);
-  static constexpr int O_COL = 2 * BN;
-  static_assert(NSLOT >= 2, "shared memory ring too small");
+  static constexpr int SMEM =
+      1024 + 2 * Q_BYTES + NSLOT * TILE_BYTES + STATS_BYTES + XMAX_BYTES + BAR_BYTES;
+  static constexpr int TMEM_COLS = pow2_at_least(2 * BN + 2 * D);
+  static_assert(NSLOT >= 3, "shared memory ring too small");
   static_assert(SMEM <= (int)kSmemLimit, "shared memory over budget");
+  static_assert(2 * BN + 2 * D <= 512, "TMEM over budget");
 };
 
 struct Bars128 {
   uint64_t full[8], empty[8];
-  uint64_t q_full, q_empty;
+  uint64_t q_full[2], q_empty[2];
   uint64_t s_full[2], p_full[2], pv_done[2];
-  uint64_t o_empty, final_mma;
+  uint64_t o_full[2], o_empty[2], stats_full[2];
+  uint64_t xbar[2][4];  // row-max exchange between the two softmax halves, per tile parity
+  uint64_t final_mma;
   uint32_t tmem_base;
   uint32_t abort;
 };
+
+struct ItemRef {
+  int bh, mb, n;
+  Range rg;
+};
+
+// Next item of this CTA (empty ones included when `with_empty`): false when none is left.
+template <int BM>
+__device__ __forceinline__ bool next_item(const PrefillSched& s, const PrefillParams& p, int cta,
+                                          int G, int BN, int& k, ItemRef& it, bool with_empty) {
+  int t;
+  while (item_at(s, p, cta, G, k, t)) {
+    ++k;
+    if (t < 0) continue;
+    item_coords(t, p, it.bh, it.mb);
+    it.rg = key_range(it.mb * BM, min(it.mb * BM + BM, p.Sq), BN, p);
+    it.n = range_count(it.rg);
+    if (it.n > 0 || with_empty) return true;
+  }
+  return false;
+}
 
 template <int D, int BN, bool BF16>
 __global__ void __launch_bounds__(kThreads128, 1)
     prefill_bm128_kernel(const __grid_constant__ CUtensorMap tmQ,
                          const __grid_constant__ CUtensorMap tmK,
-                         const __grid_constant__ CUtensorMap tmV, const PrefillParams p) {
+                         const __grid_constant__ CUtensorMap tmV, const PrefillParams p,
+                         const __grid_constant__ PrefillSched sched) {
   using C = Cfg128<D, BN>;
   constexpr int BM = kTile;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* smem = smem_raw + (base - raw);
-  const uint32_t sQ = base;
-  const uint32_t sRing = base + C::Q_BYTES;
-  Bars128* bars = reinterpret_cast<Bars128*>(smem + C::Q_BYTES + C::NSLOT * C::TILE_BYTES);
+  const uint32_t sQ = base;  // two Q buffers
+  const uint32_t sRing = base + 2 * C::Q_BYTES;
+  float2* stats = reinterpret_cast<float2*>(smem + 2 * C::Q_BYTES + C::NSLOT * C::TILE_BYTES);
+  float* xmax = reinterpret_cast<float*>(smem + 2 * C::Q_BYTES + C::NSLOT * C::TILE_BYTES +
+                                         C::STATS_BYTES);
+  Bars128* bars = reinterpret_cast<Bars128*>(smem + 2 * C::Q_BYTES + C::NSLOT * C::TILE_BYTES +
+                                             C::STATS_BYTES + C::XMAX_BYTES);
   auto B = [&](uint64_t& b) { return smem_u32(&b); };
 
   const int warp = threadIdx.x / 32;
@@ -613,14 +645,17 @@ __global__ void __launch_bounds__(kThreads128, 1)
       mbar_init(B(bars->full[i]), 1);
       mbar_init(B(bars->empty[i]), 1);
     }
-    mbar_init(B(bars->q_full), 1);
-    mbar_init(B(bars->q_empty), 1);
     for (int i = 0; i < 2; ++i) {
+      mbar_init(B(bars->q_full[i]), 1);
+      mbar_init(B(bars->q_empty[i]), 1);
       mbar_init(B(bars->s_full[i]), 1);
-      mbar_init(B(bars->p_full[i]), 128);
+      mbar_init(B(bars->p_full[i]), 256);
       mbar_init(B(bars->pv_done[i]), 1);
+      mbar_init(B(bars->o_full[i]), 1);
+      mbar_init(B(bars->o_empty[i]), 128);
+      mbar_init(B(bars->stats_full[i]), 256);
+      for (int w = 0; w < 4; ++w) mbar_init(B(bars->xbar[i][w]), 64);
     }
-    mbar_init(B(bars->o_empty), 128);
     mbar_init(B(bars->final_mma), 1);
     bars->abort = 0;
     mbar_fence_init();
@@ -642,186 +677,254 @@ __global__ void __launch_bounds__(kThreads128, 1)
   const int G = gridDim.x;
   const int cta = blockIdx.x;
 
-  if (warp == kTmaWarp128) {
-    // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      uint32_t pos = 0, ii = 0, qfill = 0;
+  // The role branches never rejoin: each ends with the CTA-wide teardown barrier.
+  if (warp >= 12) {
+    regs_decrease<kRegs128Producer>();
+    if (warp == kTmaWarp128 && lane == 0) {
+      // ---------------------------------------------------------- TMA producer
+      // Loads in the MMA's consumption order: Q and K(0) of the first item, then per
+      // tile: K of the following tile (the next item's Q first when it starts one), V.
+      uint32_t pos = 0, ii = 0;
       uint32_t fills[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+      uint32_t qfills[2] = {0, 0};
       bool ok = true;
-      for (int r = 0; ok && r * G < p.total_items; ++r) {
-        const int t = item_of_round(r, G, cta);
-        if (t >= p.total_items) continue;
-        int bh, mb;
-        item_coords(t, p, bh, mb);
-        const Range rg = key_range<BN>(mb * BM, min(mb * BM + BM, p.Sq), p);
-        const int n = range_count(rg);
-        if (n == 0) continue;
-        if (ii > 0 && !(ok = mbar_wait(B(bars->q_empty), (ii - 1) & 1, wc))) break;
-        mbar_arrive_expect_tx(B(bars->q_full), C::Q_BYTES);
+      int kc = 0;
+      ItemRef cur, nxt;
+      auto load_q = [&](const ItemRef& it, uint32_t idx) {
+        const int qb = idx & 1;
+        if (idx >= 2 && !(ok = mbar_wait(B(bars->q_empty[qb]), ((idx >> 1) - 1) & 1, wc)))
+          return;
+        mbar_arrive_expect_tx(B(bars->q_full[qb]), C::Q_BYTES);
         for (int c = 0; c < C::KCH; ++c)
-          tma_load_3d(sQ + c * (kTile * 128), &tmQ, B(bars->q_full), c * 64, mb * BM, bh);
-        qfill = ii + 1;
-        // consumption order: K0, then for each j: K(j+1) (if any), V(j)
-        for (int s = 0; s < 2 * n && ok; ++s) {
-          int tile, is_v;
-          if (s == 0) {
-            tile = 0;
-            is_v = 0;
-          } else if (s == 2 * n - 1) {
-            tile = n - 1;
-            is_v = 1;
+          tma_load_3d(sQ + qb * C::Q_BYTES + c * (kTile * 128), &tmQ, B(bars->q_full[qb]), c * 64,
+                      it.mb * BM, it.bh);
+        qfills[qb] = (idx >> 1) + 1;
+      };
+      auto emit = [&](const ItemRef& it, int j, bool is_v) {
+        const int slot = pos % C::NSLOT;
+        const uint32_t use = pos / C::NSLOT;
+        if (!(ok = mbar_wait(B(bars->empty[slot]), (use & 1) ^ 1, wc))) return;
+        const uint32_t dst = sRing + slot * C::TILE_BYTES;
+        mbar_arrive_expect_tx(B(bars->full[slot]), C::TILE_BYTES);
+        const int n0 = range_nb(it.rg, j) * BN;
+        const void* map = is_v ? (const void*)&tmV : (const void*)&tmK;
+        for (int c = 0; c < C::KCH; ++c)
+          tma_load_3d(dst + c * (BN * 128), map, B(bars->full[slot]), c * 64, n0, it.bh);
+        fills[slot] = use + 1;
+        ++pos;
+      };
+      bool has = next_item<BM>(sched, p, cta, G, BN, kc, cur, false);
+      if (has) {
+        load_q(cur, 0);
+        if (ok) emit(cur, 0, false);
+      }
+      while (has && ok) {
+        bool has_nxt = false;
+        for (int j = 0; j < cur.n && ok; ++j) {
+          if (j + 1 < cur.n) {
+            emit(cur, j + 1, false);
           } else {
-            const int j = (s - 1) / 2;
-            is_v = (s - 1) & 1;
-            tile = is_v ? j : j + 1;
+            has_nxt = next_item<BM>(sched, p, cta, G, BN, kc, nxt, false);
+            if (has_nxt) {
+              load_q(nxt, ii + 1);
+              if (ok) emit(nxt, 0, false);
+            }
           }
-          const int slot = pos % C::NSLOT;
-          const uint32_t use = pos / C::NSLOT;
-          if (!(ok = mbar_wait(B(bars->empty[slot]), (use & 1) ^ 1, wc))) break;
-          const uint32_t dst = sRing + slot * C::TILE_BYTES;
-          mbar_arrive_expect_tx(B(bars->full[slot]), C::TILE_BYTES);
-          const int n0 = range_nb(rg, tile) * BN;
-          const void* map = is_v ? (const void*)&tmV : (const void*)&tmK;
-          for (int c = 0; c < C::KCH; ++c)
-            tma_load_3d(dst + c * (BN * 128), map, B(bars->full[slot]), c * 64, n0, bh);
-          fills[slot] = use + 1;
-          ++pos;
+          if (ok) emit(cur, j, true);
         }
         ++ii;
+        cur = nxt;
+        has = has_nxt;
       }
-      if (!ok) {
+      if (!ok) {  // wind down: every load this thread issued lands before the CTA exits
         for (int s = 0; s < C::NSLOT; ++s)
           if (fills[s] > 0) wait_quiet(B(bars->full[s]), (fills[s] - 1) & 1, wc);
-        if (qfill > 0) wait_quiet(B(bars->q_full), (qfill - 1) & 1, wc);
+        for (int q = 0; q < 2; ++q)
+          if (qfills[q] > 0) wait_quiet(B(bars->q_full[q]), (qfills[q] - 1) & 1, wc);
       }
-    }
-    __syncwarp();
-  } else if (warp == kMmaWarp128) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      uint32_t pos = 0, ii = 0, tc = 0;
+    } else if (warp == kMmaWarp128 && lane == 0) {
+      // ---------------------------------------------------------- MMA issuer
+      uint32_t pos = 0, ii = 0, g = 0;
       bool ok = true;
-      for (int r = 0; ok && r * G < p.total_items; ++r) {
-        const int t = item_of_round(r, G, cta);
-        if (t >= p.total_items) continue;
-        int bh, mb;
-        item_coords(t, p, bh, mb);
-        const Range rg = key_range<BN>(mb * BM, min(mb * BM + BM, p.Sq), p);
-        const int n = range_count(rg);
-        if (n == 0) continue;
-        if (!(ok = mbar_wait(B(bars->q_full), ii & 1, wc))) break;
+      int kc = 0;
+      ItemRef cur, nxt;
+      auto issue_s = [&](uint32_t sbuf, uint32_t qb) {
+        const int slot = pos % C::NSLOT;
+        if (!(ok = mbar_wait(B(bars->full[slot]), (pos / C::NSLOT) & 1, wc))) return;
         tc_fence_after();
-        {  // S_0
-          const int slot = pos % C::NSLOT;
-          if (!(ok = mbar_wait(B(bars->full[slot]), (pos / C::NSLOT) & 1, wc))) break;
+        issue_qk<D, BN, BF16>(tmem + sbuf * BN, sQ + qb * C::Q_BYTES, sRing + slot * C::TILE_BYTES);
+        umma_commit(B(bars->s_full[sbuf]));
+        umma_commit(B(bars->empty[slot]));
+        ++pos;
+      };
+      bool has = next_item<BM>(sched, p, cta, G, BN, kc, cur, false);
+      if (has) {
+        if ((ok = mbar_wait(B(bars->q_full[0]), 0, wc))) {
           tc_fence_after();
-          issue_qk<D, BN, BF16>(tmem + (tc & 1) * BN, sQ, sRing + slot * C::TILE_BYTES);
-          umma_commit(B(bars->s_full[tc & 1]));
-          umma_commit(B(bars->empty[slot]));
-          ++pos;
-          if (n == 1) umma_commit(B(bars->q_empty));
+          issue_s(0, 0);
+          if (ok && cur.n == 1) umma_commit(B(bars->q_empty[0]));
         }
-        for (int j = 0; j < n && ok; ++j) {
-          if (j + 1 < n) {  // S_{j+1} into the other buffer while softmax works on S_j
-            const int slot = pos % C::NSLOT;
-            if (!(ok = mbar_wait(B(bars->full[slot]), (pos / C::NSLOT) & 1, wc))) break;
-            tc_fence_after();
-            issue_qk<D, BN, BF16>(tmem + ((tc + 1) & 1) * BN, sQ, sRing + slot * C::TILE_BYTES);
-            umma_commit(B(bars->s_full[(tc + 1) & 1]));
-            umma_commit(B(bars->empty[slot]));
-            ++pos;
-            if (j + 2 == n) umma_commit(B(bars->q_empty));
+      }
+      while (has && ok) {
+        const uint32_t buf = ii & 1;
+        bool has_nxt = false;
+        for (int j = 0; j < cur.n && ok; ++j, ++g) {
+          // score tile of the following tile, into the other S buffer
+          if (j + 1 < cur.n) {
+            issue_s((g + 1) & 1, buf);
+            if (ok && j + 2 == cur.n) umma_commit(B(bars->q_empty[buf]));
+          } else {
+            has_nxt = next_item<BM>(sched, p, cta, G, BN, kc, nxt, false);
+            if (has_nxt) {
+              const uint32_t nb = (ii + 1) & 1;
+              if (!(ok = mbar_wait(B(bars->q_full[nb]), ((ii + 1) >> 1) & 1, wc))) break;
+              tc_fence_after();
+              issue_s((g + 1) & 1, nb);
+              if (ok && nxt.n == 1) umma_commit(B(bars->q_empty[nb]));
+            }
           }
-          if (!(ok = mbar_wait(B(bars->p_full[tc & 1]), (tc >> 1) & 1, wc))) break;
+          if (!ok) break;
+          // O(item) += P(g) V(g)
+          if (!(ok = mbar_wait(B(bars->p_full[g & 1]), (g >> 1) & 1, wc))) break;
           tc_fence_after();
-          if (j == 0 && ii > 0) {  // the previous item's epilogue has read O
-            if (!(ok = mbar_wait(B(bars->o_empty), (ii - 1) & 1, wc))) break;
+          if (j == 0 && ii >= 2) {  // the epilogue of two items back has read this O
+            if (!(ok = mbar_wait(B(bars->o_empty[buf]), ((ii >> 1) - 1) & 1, wc))) break;
             tc_fence_after();
           }
           const int slot = pos % C::NSLOT;
           if (!(ok = mbar_wait(B(bars->full[slot]), (pos / C::NSLOT) & 1, wc))) break;
           tc_fence_after();
-          issue_pv<D, BN, BF16>(tmem + C::O_COL, tmem + (tc & 1) * BN,
+          issue_pv<D, BN, BF16>(tmem + 2 * BN + buf * D, tmem + (g & 1) * BN,
                                 sRing + slot * C::TILE_BYTES, j > 0);
-          umma_commit(B(bars->pv_done[tc & 1]));
+          umma_commit(B(bars->pv_done[g & 1]));
           umma_commit(B(bars->empty[slot]));
           ++pos;
-          ++tc;
+          if (j + 1 == cur.n) umma_commit(B(bars->o_full[buf]));
         }
         ++ii;
+        cur = nxt;
+        has = has_nxt;
       }
-      umma_commit(B(bars->final_mma));
+      umma_commit(B(bars->final_mma));  // all MMAs done before TMEM is released
       wait_quiet(B(bars->final_mma), 0, wc);
     }
     __syncwarp();
-  } else {
-    // ------------------------------------------------------------ softmax warps 0-3
-    const int row = warp * 32 + lane;
-    const uint32_t t_lane = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-    const int delta = p.Sk - p.Sq;
-    uint32_t ii = 0, tc = 0;
+    tc_fence_before();
+    __syncthreads();  // teardown
+    return;
+  } else if (warp >= 8) {
+    regs_decrease<kRegs128Epilogue>();
+    // ------------------------------------------------------------ epilogue warps 8-11
+    const int row = (warp % 4) * 32 + lane;
+    const uint32_t t_lane = tmem + (static_cast<uint32_t>((warp % 4) * 32) << 16);
+    uint32_t ii = 0;
     bool ok = true;
-    for (int r = 0; ok && r * G < p.total_items; ++r) {
-      const int t = item_of_round(r, G, cta);
-      if (t >= p.total_items) continue;
-      int bh, mb;
-      item_coords(t, p, bh, mb);
-      const Range rg = key_range<BN>(mb * BM, min(mb * BM + BM, p.Sq), p);
-      const int n = range_count(rg);
-      const int m0 = mb * BM;
-      const int qrow = m0 + row;
-      const size_t orow = static_cast<size_t>(bh) * p.Sq + qrow;
-      if (n == 0) {
+    int kc = 0;
+    ItemRef it;
+    while (ok && next_item<BM>(sched, p, cta, G, BN, kc, it, true)) {
+      const int qrow = it.mb * BM + row;
+      const size_t orow = static_cast<size_t>(it.bh) * p.Sq + qrow;
+      if (it.n == 0) {  // no row of this item sees a key
         if (qrow < p.Sq) store_zero_row<D>(orow, p);
         continue;
       }
-      const int pos_q = qrow + delta;
+      const uint32_t buf = ii & 1, use = ii >> 1;
+      ok = mbar_wait(B(bars->stats_full[buf]), use & 1, wc);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      ok = mbar_wait(B(bars->o_full[buf]), use & 1, wc);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      const float2 h0 = stats[(buf * 2 + 0) * kTile + row];
+      const float2 h1 = stats[(buf * 2 + 1) * kTile + row];
+      store_row<D, BF16>(t_lane, 2 * BN + buf * D, qrow < p.Sq, orow, h0.x, h0.y + h1.y, p);
+      tc_fence_before();
+      mbar_arrive(B(bars->o_empty[buf]));
+      ++ii;
+    }
+    tc_fence_before();
+    __syncthreads();  // teardown
+    return;
+  } else {
+    regs_increase<kRegs128Softmax>();
+    // ------------------------------------------------------------ softmax warps 0-7
+    const int half = warp / 4;  // 0: keys [0, BN/2) of each tile, 1: keys [BN/2, BN)
+    const int row = (warp % 4) * 32 + lane;
+    const uint32_t t_lane = tmem + (static_cast<uint32_t>((warp % 4) * 32) << 16);
+    const int delta = p.Sk - p.Sq;
+    uint32_t ii = 0, g = 0;
+    bool ok = true;
+    int kc = 0;
+    ItemRef it;
+    while (ok && next_item<BM>(sched, p, cta, G, BN, kc, it, false)) {
+      const uint32_t buf = ii & 1;
+      const int m0 = it.mb * BM;
+      const int pos_q = m0 + row + delta;
       float m_ref = -INFINITY, l = 0.f;
-      for (int j = 0; j < n; ++j) {
-        const int nb = range_nb(rg, j);
+      for (int j = 0; j < it.n; ++j, ++g) {
+        const int nb = range_nb(it.rg, j);
         const bool full = tile_full<BN>(m0, nb, p);
-        ok = mbar_wait(B(bars->s_full[tc & 1]), (tc >> 1) & 1, wc);
+        ok = mbar_wait(B(bars->s_full[g & 1]), (g >> 1) & 1, wc);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_fence_after();
-        if (p.trace && row == 0)
-          atomicAdd(p.trace + (static_cast<size_t>(bh) * p.nmb + mb) * p.nnb + nb,
+        if (p.trace && half == 0 && row == 0)
+          atomicAdd(p.trace + (static_cast<size_t>(it.bh) * p.nmb + it.mb) * p.nnb + nb,
                     16 + (full ? 2 : 1));
-        // O must hold every earlier P.V product before it is rescaled
-        const uint32_t pc = tc - 1;
+        // The two halves of a row swap partial maxima (double buffered by tile parity,
+        // one barrier per warp pair: a bounded wait, so an abort cannot strand the
+        // partner). The barrier also guarantees that both halves hold their S values in
+        // registers before either writes P over the S columns.
+        bool x_ok = true;
+        auto exchange = [&](float mp) {
+          float* xm = xmax + (g & 1) * 2 * kTile;
+          xm[half * kTile + row] = mp;
+          const uint32_t xb = B(bars->xbar[g & 1][warp % 4]);
+          mbar_arrive(xb);
+          x_ok = mbar_wait(xb, (g >> 1) & 1, wc);
+          x_ok = __all_sync(0xffffffffu, x_ok);
+          return x_ok ? fmaxf(mp, xm[(1 - half) * kTile + row]) : mp;
+        };
+        // O must hold every earlier P.V product of this item before it is rescaled
+        const uint32_t pc = g - 1;
         auto wait_pv = [&]() {
           bool w = mbar_wait(B(bars->pv_done[pc & 1]), (pc >> 1) & 1, wc);
           w = __all_sync(0xffffffffu, w);
           if (w) tc_fence_after();
           return w;
         };
-        ok = softmax_tile<D, BN, BF16>(t_lane, (tc & 1) * BN, C::O_COL, full, nb * BN, pos_q, p,
-                                       m_ref, l, wait_pv);
-        if (!ok) break;
+        const uint32_t s_col = (g & 1) * BN;
+        ok = softmax_cols<BN / 2, D / 2, BF16>(t_lane, s_col + half * (BN / 2),
+                                               s_col + half * (BN / 4),
+                                               2 * BN + buf * D + half * (D / 2), full,
+                                               nb * BN + half * (BN / 2), pos_q, p, m_ref, l,
+                                               exchange, wait_pv);
+        if (!ok || !x_ok) {
+          ok = false;
+          break;
+        }
         tc_fence_before();
-        mbar_arrive(B(bars->p_full[tc & 1]));
-        ++tc;
+        mbar_arrive(B(bars->p_full[g & 1]));
       }
       if (!ok) break;
-      {
-        const uint32_t pc = tc - 1;
-        ok = mbar_wait(B(bars->pv_done[pc & 1]), (pc >> 1) & 1, wc);
+      // hand this row's statistics to the epilogue (its buffer is free once the
+      // epilogue of two items back is done)
+      if (ii >= 2) {
+        ok = mbar_wait(B(bars->o_empty[buf]), ((ii >> 1) - 1) & 1, wc);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
       }
-      tc_fence_after();
-      store_row<D, BF16>(t_lane, C::O_COL, qrow < p.Sq, orow, m_ref, l, p);
-      tc_fence_before();
-      mbar_arrive(B(bars->o_empty));
+      stats[(buf * 2 + half) * kTile + row] = make_float2(m_ref, l);
+      mbar_arrive(B(bars->stats_full[buf]));
       ++ii;
     }
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 0) {
-    tc_fence_after();
-    tmem_dealloc(tmem, C::TMEM_COLS);
+    tc_fence_before();
+    __syncthreads();  // teardown
+    if (warp == 0) {
+      tc_fence_after();
+      tmem_dealloc(tmem, C::TMEM_COLS);
+    }
   }
 }
 
@@ -840,13 +943,19 @@ cudaError_t launch_t(const PrefillLaunch& L, int BM, cudaStream_t stream) {
       return cudaErrorInvalidConfiguration;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    kern<<<L.grid, kThreads256, smem, stream>>>(L.tmQ, L.tmK, L.tmV, L.p);
+    kern<<<L.grid, kThreads256, smem, stream>>>(L.tmQ, L.tmK, L.tmV, L.p, *L.sched);
   } else {
     auto kern = prefill_bm128_kernel<D, BN, BF16>;
     constexpr int smem = Cfg128<D, BN>::SMEM;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaFuncAttributes fattr;
+    cudaError_t e = cudaFuncGetAttributes(&fattr, kern);
     if (e != cudaSuccess) return e;
-    kern<<<L.grid, kThreads128, smem, stream>>>(L.tmQ, L.tmK, L.tmV, L.p);
+    if (fattr.numRegs * kThreads128 <
+        128 * static_cast<int>(kRegs128Softmax + kRegs128Epilogue + kRegs128Producer))
+      return cudaErrorInvalidConfiguration;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    kern<<<L.grid, kThreads128, smem, stream>>>(L.tmQ, L.tmK, L.tmV, L.p, *L.sched);
   }
   return cudaGetLastError();
 }

@@ -163,6 +163,66 @@ __device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64
       : "memory");
 }
 
+// Eight SS MMAs into one accumulator, in one PTX block: operand descriptors are the
+// bases a0/b0 plus the immediate offsets A1..A7 / B1..B7 (in 16-byte units); the
+// first MMA overwrites D, the rest accumulate.
+#define FA_UMMA_SS8_BODY                                                              \
+  "{\n\t.reg .pred pf, pt;\n\t.reg .b64 da, db;\n\t"                              \
+  "setp.ne.b32 pf, %3, %3;\n\tsetp.eq.b32 pt, %3, %3;\n\t"                          \
+  "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, pf;\n\t"                     \
+  "add.s64 da, %1, %4;\n\tadd.s64 db, %2, %11;\n\t"                                 \
+  "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, pt;\n\t"                     \
+  "add.s64 da, %1, %5;\n\tadd.s64 db, %2, %12;\n\t"                                 \
+  "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, pt;\n\t"                     \
+  "add.s64 da, %1, %6;\n\tadd.s64 db, %2, %13;\n\t"                                 \
+  "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, pt;\n\t"                     \
+  "add.s64 da, %1, %7;\n\tadd.s64 db, %2, %14;\n\t"                                 \
+  "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, pt;\n\t"                     \
+  "add.s64 da, %1, %8;\n\tadd.s64 db, %2, %15;\n\t"                                 \
+  "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, pt;\n\t"                     \
+  "add.s64 da, %1, %9;\n\tadd.s64 db, %2, %16;\n\t"                                 \
+  "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, pt;\n\t"                     \
+  "add.s64 da, %1, %10;\n\tadd.s64 db, %2, %17;\n\t"                                \
+  "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, pt;\n\t}"
+
+template <int A1, int A2, int A3, int A4, int A5, int A6, int A7, int B1, int B2, int B3,
+          int B4, int B5, int B6, int B7>
+__device__ __forceinline__ void umma_ss8(uint32_t d_tmem, uint64_t a0, uint64_t b0,
+                                         uint32_t idesc) {
+  asm volatile(FA_UMMA_SS8_BODY::"r"(d_tmem), "l"(a0), "l"(b0), "r"(idesc), "n"(A1), "n"(A2),
+               "n"(A3), "n"(A4), "n"(A5), "n"(A6), "n"(A7), "n"(B1), "n"(B2), "n"(B3), "n"(B4),
+               "n"(B5), "n"(B6), "n"(B7)
+               : "memory");
+}
+
+// Eight TS MMAs (A from TMEM at a_tmem + 8k columns, B descriptor b0 + k*BSTEP): the
+// first accumulates when `accumulate` is non-zero, the rest always accumulate.
+template <int BSTEP>
+__device__ __forceinline__ void umma_ts8(uint32_t d_tmem, uint32_t a_tmem, uint64_t b0,
+                                         uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred pa, pt;\n\t.reg .b64 db;\n\t.reg .b32 ta;\n\t"
+      "setp.ne.b32 pa, %4, 0;\n\tsetp.eq.b32 pt, %3, %3;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, pa;\n\t"
+      "add.s32 ta, %1, 8;\n\tadd.s64 db, %2, %5;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %3, pt;\n\t"
+      "add.s32 ta, %1, 16;\n\tadd.s64 db, %2, %6;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %3, pt;\n\t"
+      "add.s32 ta, %1, 24;\n\tadd.s64 db, %2, %7;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %3, pt;\n\t"
+      "add.s32 ta, %1, 32;\n\tadd.s64 db, %2, %8;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %3, pt;\n\t"
+      "add.s32 ta, %1, 40;\n\tadd.s64 db, %2, %9;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %3, pt;\n\t"
+      "add.s32 ta, %1, 48;\n\tadd.s64 db, %2, %10;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %3, pt;\n\t"
+      "add.s32 ta, %1, 56;\n\tadd.s64 db, %2, %11;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %3, pt;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b0), "r"(idesc), "r"(accumulate), "n"(BSTEP), "n"(2 * BSTEP),
+      "n"(3 * BSTEP), "n"(4 * BSTEP), "n"(5 * BSTEP), "n"(6 * BSTEP), "n"(7 * BSTEP)
+      : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05 operation this thread issued so far is done.
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
   asm volatile(
@@ -195,6 +255,16 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
       "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
       "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
       "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15])
       : "memory");
 }
 
