@@ -503,16 +503,16 @@ def cpu_model():
 def cpu_baseline(pcfg, q, k, v, di):
     out = {"kind": "oracle", "cpu": cpu_model()}
     if pcfg:
-        n_heads = 16
+        n_heads = pcfg["B"] * pcfg["H"] if pcfg["S"] <= 4096 else 4  # ~10 s on 16 cores
         flops, secs, cores = oracle_prefill_sample(pcfg, q, k, v, n_heads)
         out.update({"value": flops / secs / 1e12, "unit": "TFLOP/s", "cores": cores,
                     "seconds": secs,
                     "sample": f"FP64 oracle, all {pcfg['S']} rows of {n_heads} of "
                               f"{pcfg['B'] * pcfg['H']} (batch, head) pairs"})
     if di is not None:
-        nbytes, secs, cores = oracle_decode_sample(di, 4)
+        nbytes, secs, cores = oracle_decode_sample(di, di.B)
         dec = {"value": nbytes / secs / 1e9, "unit": "GB/s", "cores": cores, "seconds": secs,
-               "sample": f"FP64 oracle, 4 of {di.B} sequences, all {di.H} heads"}
+               "sample": f"FP64 oracle, all {di.B} sequences, all {di.H} heads"}
         if pcfg:
             out["decode"] = dec
         else:
