@@ -53,6 +53,10 @@ def lib():
         L.or_decode_paged.argtypes = [_vp, _vp, _vp, ctypes.c_int, _vp, _vp, _vp, _vp, _i64,
                                       _i64, _i64, _i64, _i64, _i64, ctypes.c_double, _vp,
                                       _i64, ctypes.c_int]
+        L.or_attention_paged.restype = ctypes.c_int
+        L.or_attention_paged.argtypes = [_vp, _vp, _vp, ctypes.c_int, _vp, _vp, _vp, _vp, _i64,
+                                         _i64, _i64, _i64, _i64, _i64, _i64, ctypes.c_double,
+                                         ctypes.c_int, _i64, _i64, ctypes.c_int]
         L.or_combine_partials.restype = None
         L.or_combine_partials.argtypes = [_vp, _vp, _vp, _i64, _i64, _vp, _vp]
         L.or_decode_split_tokens.restype = None
@@ -167,6 +171,25 @@ def decode_paged(q, k_pages, v_pages, block_table, ctx_lens, scale, bh_list=None
                                float(scale), bp, nb, nthreads)
     if rc != 0:
         raise ValueError("or_decode_paged rejected its arguments")
+    return o, lse
+
+
+def attention_paged(q, k_pages, v_pages, block_table, ctx_lens, scale, mask_mode=MASK_NONE,
+                    window=0, n_global=0, nthreads=0):
+    """q [B,H,Sq,d] (the last Sq tokens of each sequence); pools [P,H,page,d]."""
+    q, k_pages, v_pages = _cpu(q), _cpu(k_pages), _cpu(v_pages)
+    bt = _cpu(block_table).to(torch.int32)
+    cl = _cpu(ctx_lens).to(torch.int32)
+    B, H, Sq, d = q.shape
+    P, _, page, _ = k_pages.shape
+    o = np.zeros((B, H, Sq, d))
+    lse = np.zeros((B, H, Sq))
+    rc = lib().or_attention_paged(q.data_ptr(), k_pages.data_ptr(), v_pages.data_ptr(),
+                                  _dtype_code(q, k_pages, v_pages), bt.data_ptr(), cl.data_ptr(),
+                                  o.ctypes.data, lse.ctypes.data, B, H, Sq, d, page, bt.shape[1],
+                                  P, float(scale), mask_mode, window, n_global, nthreads)
+    if rc != 0:
+        raise ValueError("or_attention_paged rejected its arguments")
     return o, lse
 
 

@@ -29,6 +29,8 @@
  *   or_online_attention    pinned against or_attention and against the closed
  *                          forms; the literal page-2 update is shown to differ
  *   or_decode_paged        pinned by special cases (ctx = 1, identity table)
+ *   or_attention_paged     pinned against or_attention on gathered keys (identity and
+ *                          permuted tables) and against or_decode_paged (Sq = 1)
  *   or_combine_partials    pinned by split invariance against unsplit softmax
  *   or_decode_split_tokens pinned by partition invariants (cover, disjoint)
  */
@@ -453,6 +455,86 @@ int or_decode_paged(const void* q, const void* k_pages, const void* v_pages,
             for (int64_t c = 0; c < d; ++c) qrow[c] = or_elem(q, bh * d + c, dtype);
             double err;
             attend_row(qrow, kr, vr, n, d, scale, s, o + r * d, lse + r, &err);
+        }
+        free(qrow);
+        free(s);
+        free(kd);
+        free(vd);
+        free(kr);
+        free(vr);
+    }
+    return bad ? -1 : 0;
+}
+
+/*
+ * Prefill against a paged cache: sequence b holds ctx_lens[b] keys in pages (as in
+ * or_decode_paged) and its Sq queries are its last Sq tokens, so query i of sequence b
+ * is row i of an attention with Sq queries and Sk = ctx_lens[b] keys under the given
+ * mask (bottom-right alignment, as or_visible). q and o are [B,H,Sq,d], lse [B,H,Sq].
+ * Returns 0, or -1 if a needed table entry is out of range.
+ */
+int or_attention_paged(const void* q, const void* k_pages, const void* v_pages, int dtype,
+                       const int32_t* block_table, const int32_t* ctx_lens, double* o,
+                       double* lse, int64_t B, int64_t H, int64_t Sq, int64_t d,
+                       int64_t page_size, int64_t max_pages_per_seq, int64_t num_pages,
+                       double scale, int mask_mode, int64_t window, int64_t n_global,
+                       int nthreads) {
+    if (B < 0 || H < 0 || Sq < 0 || d <= 0 || page_size <= 0) return -1;
+    int64_t max_ctx = page_size * max_pages_per_seq;
+    int bad = 0;
+#ifdef _OPENMP
+    if (nthreads <= 0) nthreads = omp_get_max_threads();
+#pragma omp parallel num_threads(nthreads) reduction(| : bad)
+#endif
+    {
+        size_t cap = (size_t)(max_ctx > 0 ? max_ctx : 1);
+        double* qrow = (double*)malloc(sizeof(double) * (size_t)d);
+        double* s = (double*)malloc(sizeof(double) * cap);
+        double* kd = (double*)malloc(sizeof(double) * cap * (size_t)d);
+        double* vd = (double*)malloc(sizeof(double) * cap * (size_t)d);
+        const double** kr = (const double**)malloc(sizeof(double*) * cap);
+        const double** vr = (const double**)malloc(sizeof(double*) * cap);
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 1)
+#endif
+        for (int64_t bh = 0; bh < B * H; ++bh) {
+            int64_t b = bh / H, h = bh % H;
+            int64_t ctx = ctx_lens[b];
+            if (ctx < 0 || ctx > max_ctx) {
+                bad = 1;
+                continue;
+            }
+            /* gather this sequence's keys and values for head h, in position order */
+            int ok = 1;
+            for (int64_t t = 0; t < ctx && ok; ++t) {
+                int64_t page = block_table[b * max_pages_per_seq + t / page_size];
+                if (page < 0 || page >= num_pages) {
+                    ok = 0;
+                    break;
+                }
+                int64_t src = ((page * H + h) * page_size + t % page_size) * d;
+                for (int64_t c = 0; c < d; ++c) {
+                    kd[t * d + c] = or_elem(k_pages, src + c, dtype);
+                    vd[t * d + c] = or_elem(v_pages, src + c, dtype);
+                }
+            }
+            if (!ok) {
+                bad = 1;
+                continue;
+            }
+            for (int64_t i = 0; i < Sq; ++i) {
+                int64_t row = bh * Sq + i;
+                for (int64_t c = 0; c < d; ++c) qrow[c] = or_elem(q, row * d + c, dtype);
+                int64_t n = 0;
+                for (int64_t j = 0; j < ctx; ++j)
+                    if (or_visible(i, j, Sq, ctx, mask_mode, window, n_global)) {
+                        kr[n] = kd + j * d;
+                        vr[n] = vd + j * d;
+                        ++n;
+                    }
+                double err;
+                attend_row(qrow, kr, vr, n, d, scale, s, o + row * d, lse + row, &err);
+            }
         }
         free(qrow);
         free(s);

@@ -61,6 +61,13 @@ int or_decode_paged(const void* q, const void* k_pages, const void* v_pages,
                     int64_t max_pages_per_seq, int64_t num_pages, double scale,
                     const int64_t* bh_list, int64_t n_bh, int nthreads);
 
+int or_attention_paged(const void* q, const void* k_pages, const void* v_pages, int dtype,
+                       const int32_t* block_table, const int32_t* ctx_lens, double* o,
+                       double* lse, int64_t B, int64_t H, int64_t Sq, int64_t d,
+                       int64_t page_size, int64_t max_pages_per_seq, int64_t num_pages,
+                       double scale, int mask_mode, int64_t window, int64_t n_global,
+                       int nthreads);
+
 void or_combine_partials(const double* m, const double* l, const double* acc,
                          int64_t nsplit, int64_t d, double* o, double* lse);
 

@@ -505,3 +505,46 @@ def test_brute_force_numpy_tiny():
         p = np.exp(s - s.max())
         np.testing.assert_allclose(o[0, 0, i], (p / p.sum()) @ V[js], rtol=0, atol=1e-13)
         np.testing.assert_allclose(lse[0, 0, i], s.max() + math.log(p.sum()), rtol=0, atol=1e-13)
+
+
+# --------------------------------------------------------------------------- #
+# prefill against a paged cache                                               #
+# --------------------------------------------------------------------------- #
+
+@pytest.mark.parametrize("mode,w,g", [(MASK_NONE, 0, 0), (MASK_CAUSAL, 0, 0),
+                                      (MASK_CAUSAL_WINDOW, 9, 2)])
+def test_paged_prefill_equals_attention_on_gathered_keys(mode, w, g):
+    """Each sequence's rows equal or_attention with Sk = its length over its keys
+    gathered in position order (random permutation table)."""
+    di = inputs.decode_inputs(B=4, H=2, d=16, page_size=8, num_pages=40, max_ctx=60,
+                              dtype=torch.bfloat16, seed=73, ctx_lens=[5, 60, 23, 8])
+    Sq = 5
+    q = inputs.prefill_inputs(4, 2, Sq, 1, 16, torch.bfloat16, seed=79)[0]
+    o, lse = oracle.attention_paged(q, di.k_pages, di.v_pages, di.block_table, di.ctx_lens,
+                                    0.3, mode, w, g)
+    for b, (kk, vv) in enumerate(_contiguous_kv(di)):
+        ob, lb = oracle.attention(q[b:b + 1], kk[None], vv[None], 0.3, mode, w, g)
+        np.testing.assert_allclose(o[b], ob[0], rtol=0, atol=1e-13)
+        np.testing.assert_allclose(lse[b], lb[0], rtol=0, atol=1e-13)
+
+
+def test_paged_prefill_identity_table_and_single_query():
+    H, d, P, S = 2, 8, 4, 16
+    _, k, v = inputs.prefill_inputs(1, H, 1, S, d, torch.float16, seed=83)
+    kp = k[0].reshape(H, S // P, P, d).permute(1, 0, 2, 3).contiguous()
+    vp = v[0].reshape(H, S // P, P, d).permute(1, 0, 2, 3).contiguous()
+    table = torch.arange(S // P, dtype=torch.int32)[None]
+    ctx = torch.tensor([S], dtype=torch.int32)
+    q = inputs.prefill_inputs(1, H, 6, 1, d, torch.float16, seed=89)[0]
+    o1, l1 = oracle.attention_paged(q, kp, vp, table, ctx, 0.4, MASK_CAUSAL)
+    o2, l2 = oracle.attention(q, k, v, 0.4, MASK_CAUSAL)
+    np.testing.assert_allclose(o1, o2, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(l1, l2, rtol=0, atol=1e-13)
+    # one query per sequence is the decode step
+    di = inputs.decode_inputs(B=3, H=2, d=8, page_size=4, num_pages=20, max_ctx=24,
+                              dtype=torch.float16, seed=97)
+    od, ld = oracle.decode_paged(di.q, di.k_pages, di.v_pages, di.block_table, di.ctx_lens, 0.5)
+    op, lp = oracle.attention_paged(di.q[:, :, None, :], di.k_pages, di.v_pages, di.block_table,
+                                    di.ctx_lens, 0.5, MASK_CAUSAL)
+    np.testing.assert_allclose(op[:, :, 0], od, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(lp[:, :, 0], ld, rtol=0, atol=1e-13)
