@@ -167,6 +167,65 @@ fa_status fa_decode_paged_ex(const fa_decode_params* params, fa_stream_t stream)
 int fa_decode_default_pages_per_split(int B, int H, int max_pages_per_seq);
 
 /*
+ * fa_kv_append - write a chunk of new tokens into a paged KV cache ("ascend-transformer-
+ * boost 实战" (ai6s.net), scenario 2: fixed-size pages, a new page taken as a sequence
+ * grows). Token t < n_b of sequence b (n_b = new_lens[b], or T when new_lens is NULL) is
+ * stored at position ctx_lens[b] + t: page block_table[b, pos / page_size], offset
+ * pos % page_size. The caller puts the pages the chunk needs into the table beforehand
+ * and adds n_b to ctx_lens afterwards (the call does not change ctx_lens). The slots of
+ * the chunk's last page after its last token are set to zero, so every slot a paged
+ * prefill may read past a sequence's end holds a finite value.
+ *   k_new, v_new  [B, H, T, d] dtype (contiguous)
+ *   k_pages, v_pages [num_pages, H, page_size, d] dtype, written in place
+ *   block_table   int32 [B, max_pages_per_seq];  ctx_lens int32 [B];  new_lens int32 [B] or NULL
+ *   d 64 or 128; page_size a multiple of 16 in [16, 4096].
+ * A table entry outside [0, num_pages), or ctx + n_b beyond page_size*max_pages_per_seq,
+ * is skipped on the device and reported as FA_ERR_BAD_PAGE.
+ */
+fa_status fa_kv_append(const void* k_new, const void* v_new, void* k_pages, void* v_pages,
+                       const int32_t* block_table, const int32_t* ctx_lens,
+                       const int32_t* new_lens, int B, int H, int T, int d, int page_size,
+                       int max_pages_per_seq, int num_pages, int dtype, fa_stream_t stream);
+
+/*
+ * fa_fwd_paged - chunked prefill against a paged KV cache: the Sq queries of sequence b
+ * are its last Sq tokens, at key positions ctx_lens[b]-Sq .. ctx_lens[b]-1, and attend
+ * to its ctx_lens[b] cached keys (K/V appended beforehand, e.g. with fa_kv_append) under
+ * the given mask, exactly as fa_fwd with Sk = ctx_lens[b] would over the gathered keys.
+ *   q, o          [B, H, Sq, d] dtype;  lse [B, H, Sq] float32 or NULL
+ *   k_pages, v_pages, block_table, ctx_lens, page_size, max_pages_per_seq, num_pages
+ *                 as for fa_decode_paged, except page_size: a multiple of 64 in [64, 4096]
+ *                 (a key tile never crosses a page)
+ *   mask_mode, window, n_global, scale, dtype as for fa_fwd.
+ * The key tiles of a sequence's last page are read whole: slots past ctx_lens[b] must
+ * hold finite values (fa_kv_append guarantees it). Lengths are read on the device; a
+ * length above page_size*max_pages_per_seq is clamped and an out-of-range page is
+ * replaced by page 0 and reported as FA_ERR_BAD_PAGE.
+ */
+fa_status fa_fwd_paged(const void* q, const void* k_pages, const void* v_pages,
+                       const int32_t* block_table, const int32_t* ctx_lens, void* o, float* lse,
+                       int B, int H, int Sq, int d, int page_size, int max_pages_per_seq,
+                       int num_pages, float scale, int mask_mode, int window, int n_global,
+                       int dtype, fa_stream_t stream);
+
+/*
+ * fa_merge_partials - combine two attention results that cover disjoint key sets of the
+ * same queries (for example the text-to-text causal call and the text-to-vision cross
+ * call of a multimodal layer). Splitting an attention into such calls is exact
+ * ("ascend-transformer-boost 实战" (ai6s.net), scenario 4); with M = max(lse_a, lse_b)
+ * and w_x = exp(lse_x - M):
+ *     o = (w_a o_a + w_b o_b) / (w_a + w_b),   lse = M + ln(w_a + w_b).
+ * A part whose LSE is -inf contributes nothing; two empty parts give o = 0, lse = -inf.
+ *   o_a, o_b, o   [rows, d] dtype (for example [B,H,Sq,d] flattened); o may alias o_a
+ *   lse_a, lse_b  [rows] float32 natural-log LSEs, as fa_fwd writes them
+ *   lse           [rows] float32, may be NULL; must not overlap lse_a or lse_b
+ *   d 64 or 128; dtype FA_F16 or FA_BF16.
+ */
+fa_status fa_merge_partials(const void* o_a, const float* lse_a, const void* o_b,
+                            const float* lse_b, void* o, float* lse, int64_t rows, int d,
+                            int dtype, fa_stream_t stream);
+
+/*
  * fa_decode_paged_noalloc - fa_decode_paged for callers that cannot allocate device
  * memory. The pages have no counterpart for this call; it exists for users of this
  * library whose device memory is fixed when they start (a serving loop with a set

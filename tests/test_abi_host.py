@@ -163,3 +163,13 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(fa, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(fa.FaError):
         fa.lib()
+
+
+def test_merge_rejects_bad_arguments(L):
+    assert L.fa_merge_partials(A, A, A, A, A, None, 10, 96, 0, None) == fa.FA_ERR_UNSUPPORTED
+    assert L.fa_merge_partials(A, A, A, A, A, None, 10, 64, 7, None) == fa.FA_ERR_UNSUPPORTED
+    assert L.fa_merge_partials(None, A, A, A, A, None, 10, 64, 0, None) == fa.FA_ERR_INVALID_ARG
+    assert L.fa_merge_partials(A + 8, A, A, A, A, None, 10, 64, 0, None) == fa.FA_ERR_INVALID_ARG
+    assert L.fa_merge_partials(A, A, A, A, A, None, -1, 64, 0, None) == fa.FA_ERR_INVALID_ARG
+    assert L.fa_merge_partials(None, None, None, None, None, None, 0, 64, 0, None) == fa.FA_OK
+

@@ -13,7 +13,8 @@ import torch
 
 __all__ = [
     "FaError", "lib", "fa_fwd", "fa_fwd_ex", "fa_decode_paged", "fa_decode_paged_ex",
-    "fa_decode_paged_noalloc", "fa_decode_workspace_size", "fa_decode_default_pages_per_split",
+    "fa_decode_paged_noalloc", "fa_merge_partials", "fa_fwd_paged", "fa_kv_append",
+    "fa_decode_workspace_size", "fa_decode_default_pages_per_split",
     "fa_get_device_status",
     "fa_selftest_timeout", "fa_last_error_string", "fa_version", "fa_fwd_block_m",
     "FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_CUDA", "FA_ERR_TIMEOUT",
@@ -82,6 +83,14 @@ def lib():
         L.fa_decode_paged_noalloc.restype = _i
         L.fa_decode_paged_noalloc.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i,
                                               _i, _i, _f, _i, _vp]
+        L.fa_fwd_paged.restype = _i
+        L.fa_fwd_paged.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i,
+                                   _f, _i, _i, _i, _i, _vp]
+        L.fa_kv_append.restype = _i
+        L.fa_kv_append.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i,
+                                   _i, _vp]
+        L.fa_merge_partials.restype = _i
+        L.fa_merge_partials.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_int64, _i, _i, _vp]
         L.fa_decode_workspace_size.restype = _sz
         L.fa_decode_workspace_size.argtypes = [_i, _i, _i, _i, _i]
         L.fa_decode_default_pages_per_split.restype = _i
@@ -225,6 +234,48 @@ def fa_decode_paged_noalloc(q, k_pages, v_pages, block_table, ctx_lens, o, lse, 
                                          o.data_ptr(), _ptr(lse), B, H, d, page,
                                          block_table.shape[1], P, float(scale), _dtype_code(q),
                                          _stream(stream)))
+
+
+def fa_fwd_paged(q, k_pages, v_pages, block_table, ctx_lens, o, lse, scale,
+                 mask_mode=FA_MASK_CAUSAL, window=0, n_global=0, stream=None):
+    """Chunked prefill against a paged cache: q/o [B,H,Sq,d] are the last Sq tokens of
+    each sequence; pools [num_pages,H,page,d]; block_table int32 [B,max_pages];
+    ctx_lens int32 [B] (cached tokens, the chunk included)."""
+    _need_cuda_contig(q=q, k_pages=k_pages, v_pages=v_pages, block_table=block_table,
+                      ctx_lens=ctx_lens, o=o, lse=lse)
+    B, H, Sq, d = q.shape
+    P, _, page, _ = k_pages.shape
+    _check(lib().fa_fwd_paged(q.data_ptr(), k_pages.data_ptr(), v_pages.data_ptr(),
+                              block_table.data_ptr(), ctx_lens.data_ptr(), o.data_ptr(),
+                              _ptr(lse), B, H, Sq, d, page, block_table.shape[1], P, float(scale),
+                              mask_mode, window, n_global, _dtype_code(q), _stream(stream)))
+
+
+def fa_kv_append(k_new, v_new, k_pages, v_pages, block_table, ctx_lens, new_lens=None,
+                 stream=None):
+    """Write k_new/v_new [B,H,T,d] at positions ctx_lens[b] + t of the paged cache
+    (t < new_lens[b], or all T); zero-fill the rest of each chunk's last page."""
+    _need_cuda_contig(k_new=k_new, v_new=v_new, k_pages=k_pages, v_pages=v_pages,
+                      block_table=block_table, ctx_lens=ctx_lens, new_lens=new_lens)
+    B, H, T, d = k_new.shape
+    P, _, page, _ = k_pages.shape
+    _check(lib().fa_kv_append(k_new.data_ptr(), v_new.data_ptr(), k_pages.data_ptr(),
+                              v_pages.data_ptr(), block_table.data_ptr(), ctx_lens.data_ptr(),
+                              _ptr(new_lens), B, H, T, d, page, block_table.shape[1], P,
+                              _dtype_code(k_new), _stream(stream)))
+
+
+def fa_merge_partials(o_a, lse_a, o_b, lse_b, o, lse=None, stream=None):
+    """Combine two attention results over disjoint key sets of the same queries by LSE.
+
+    o_* [..., d] (same shape, fp16/bf16), lse_* float32 with the leading shape of o.
+    """
+    _need_cuda_contig(o_a=o_a, lse_a=lse_a, o_b=o_b, lse_b=lse_b, o=o, lse=lse)
+    d = o_a.shape[-1]
+    rows = o_a.numel() // d
+    _check(lib().fa_merge_partials(o_a.data_ptr(), lse_a.data_ptr(), o_b.data_ptr(),
+                                   lse_b.data_ptr(), o.data_ptr(), _ptr(lse), rows, d,
+                                   _dtype_code(o_a), _stream(stream)))
 
 
 def fa_get_device_status(stream=None):

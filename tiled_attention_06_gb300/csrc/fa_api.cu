@@ -135,7 +135,7 @@ const fa::PrefillSched* plan_for(const fa::PrefillParams& p, int BM, int BN, int
     for (int t = 0; t < p.total_items; ++t) {
       int bh, mb;
       fa::item_coords(t, p, bh, mb);
-      const fa::Range r = fa::key_range(mb * BM, std::min(mb * BM + BM, p.Sq), BN, p);
+      const fa::Range r = fa::key_range(mb * BM, std::min(mb * BM + BM, p.Sq), BN, p.Sk, p);
       const int n = fa::range_count(r);
       Slot s = free_at.top();
       free_at.pop();
@@ -195,11 +195,23 @@ const char* fa_last_error_string(void) { return t_last_error.c_str(); }
 
 int fa_fwd_block_m(void) { return fa::prefill_tile_rows(); }
 
-fa_status fa_fwd_ex(const fa_fwd_params* params, fa_stream_t stream) {
-  if (!params) return fail(FA_ERR_INVALID_ARG, "params is null");
-  const fa_fwd_params& a = *params;
-  fa_status st = check_fwd(a);
-  if (st != FA_OK) return st;
+}  // extern "C"
+
+namespace {
+
+// K/V read through a page table (chunked prefill into a paged cache).
+struct PagedKV {
+  const void* k_pages;
+  const void* v_pages;
+  const int32_t* block_table;
+  const int32_t* ctx_lens;
+  int page_size, max_pages, num_pages;
+};
+
+// Plan and launch one prefill. `a` has passed check_fwd; with `pg` set, a.Sk is the
+// table's capacity and K/V come from the pools.
+fa_status run_fwd(const fa_fwd_params& a, const PagedKV* pg, fa_stream_t stream) {
+  fa_status st;
   if (a.Sq == 0) return FA_OK;  // nothing to compute
   DeviceInfo dev;
   if ((st = device_info(&dev)) != FA_OK) return st;
@@ -243,12 +255,84 @@ fa_status fa_fwd_ex(const fa_fwd_params* params, fa_stream_t stream) {
   const bool bf16 = a.dtype == FA_BF16;
   if ((st = make_map(&L.tmQ, a.q, bf16, a.d, a.Sq, BH, fa::prefill_tile_rows())) != FA_OK)
     return st;
-  // with Sk == 0 no key tile is ever loaded; the maps only need a valid address
-  if ((st = make_map(&L.tmK, a.Sk ? a.k : a.q, bf16, a.d, a.Sk, BH, BN)) != FA_OK) return st;
-  if ((st = make_map(&L.tmV, a.Sk ? a.v : a.q, bf16, a.d, a.Sk, BH, BN)) != FA_OK) return st;
+  if (pg) {
+    // pools [num_pages, H, page, d] seen as (d, page, num_pages*H); a tile is BN rows of
+    // one (page, head)
+    p.block_table = pg->block_table;
+    p.seq_k = pg->ctx_lens;
+    p.H = a.H;
+    p.page_size = pg->page_size;
+    p.max_pages = pg->max_pages;
+    p.num_pages = pg->num_pages;
+    const int zdim = pg->num_pages * a.H;
+    if ((st = make_map(&L.tmK, pg->k_pages, bf16, a.d, pg->page_size, zdim, BN)) != FA_OK)
+      return st;
+    if ((st = make_map(&L.tmV, pg->v_pages, bf16, a.d, pg->page_size, zdim, BN)) != FA_OK)
+      return st;
+  } else {
+    // with Sk == 0 no key tile is ever loaded; the maps only need a valid address
+    if ((st = make_map(&L.tmK, a.Sk ? a.k : a.q, bf16, a.d, a.Sk, BH, BN)) != FA_OK) return st;
+    if ((st = make_map(&L.tmV, a.Sk ? a.v : a.q, bf16, a.d, a.Sk, BH, BN)) != FA_OK) return st;
+  }
   cudaError_t e = fa::launch_prefill(L, a.d, BN, BM, bf16, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
   return FA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+fa_status fa_fwd_ex(const fa_fwd_params* params, fa_stream_t stream) {
+  if (!params) return fail(FA_ERR_INVALID_ARG, "params is null");
+  fa_status st = check_fwd(*params);
+  if (st != FA_OK) return st;
+  return run_fwd(*params, nullptr, stream);
+}
+
+fa_status fa_fwd_paged(const void* q, const void* k_pages, const void* v_pages,
+                       const int32_t* block_table, const int32_t* ctx_lens, void* o, float* lse,
+                       int B, int H, int Sq, int d, int page_size, int max_pages_per_seq,
+                       int num_pages, float scale, int mask_mode, int window, int n_global,
+                       int dtype, fa_stream_t stream) {
+  if (!k_pages || !v_pages || !block_table || !ctx_lens)
+    return fail(FA_ERR_INVALID_ARG, "k_pages, v_pages, block_table and ctx_lens must be non-null");
+  if (!aligned16(k_pages) || !aligned16(v_pages))
+    return fail(FA_ERR_INVALID_ARG, "pools must be 16-byte aligned");
+  if (!aligned4(block_table) || !aligned4(ctx_lens))
+    return fail(FA_ERR_INVALID_ARG, "block_table and ctx_lens must be 4-byte aligned");
+  if (max_pages_per_seq < 1 || num_pages < 1)
+    return fail(FA_ERR_INVALID_ARG, "need max_pages_per_seq, num_pages >= 1");
+  if (page_size < 64 || page_size > 4096 || page_size % 64 != 0)
+    return fail(FA_ERR_UNSUPPORTED, "page_size %d (a multiple of 64 in [64, 4096])", page_size);
+  const long long cap = static_cast<long long>(page_size) * max_pages_per_seq;
+  const long long zdim = static_cast<long long>(num_pages) * (H > 0 ? H : 1);
+  if (cap > (1LL << 30) || zdim > (1LL << 31) - 1)
+    return fail(FA_ERR_INVALID_ARG, "problem too large");
+  fa_fwd_params a;
+  std::memset(&a, 0, sizeof a);
+  a.q = q;
+  a.k = k_pages;
+  a.v = v_pages;
+  a.o = o;
+  a.lse = lse;
+  a.B = B;
+  a.H = H;
+  a.Sq = Sq;
+  a.Sk = static_cast<int>(cap);
+  a.d = d;
+  a.scale = scale;
+  a.mask_mode = mask_mode;
+  a.window = window;
+  a.n_global = n_global;
+  a.dtype = dtype;
+  a.block_m = 128;                         // per-sequence key counts: one-tile kernel
+  a.block_n = page_size % 128 == 0 ? 128 : 64;  // a K/V tile never crosses a page
+  fa_status st = check_fwd(a);
+  if (st != FA_OK) return st;
+  const PagedKV pg{k_pages, v_pages, block_table, ctx_lens, page_size, max_pages_per_seq,
+                   num_pages};
+  return run_fwd(a, &pg, stream);
 }
 
 fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
@@ -438,6 +522,61 @@ fa_status fa_decode_paged_noalloc(const void* q, const void* k_pages, const void
   cudaError_t e =
       fa::launch_decode_noalloc(p, d, dtype == FA_BF16, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "decode (no-alloc) launch");
+  return FA_OK;
+}
+
+fa_status fa_merge_partials(const void* o_a, const float* lse_a, const void* o_b,
+                            const float* lse_b, void* o, float* lse, int64_t rows, int d,
+                            int dtype, fa_stream_t stream) {
+  if (rows < 0) return fail(FA_ERR_INVALID_ARG, "rows must be >= 0");
+  if (d != 64 && d != 128) return fail(FA_ERR_UNSUPPORTED, "head dim %d (supported: 64, 128)", d);
+  if (dtype != FA_F16 && dtype != FA_BF16) return fail(FA_ERR_UNSUPPORTED, "dtype %d", dtype);
+  if (rows == 0) return FA_OK;
+  if (!o_a || !lse_a || !o_b || !lse_b || !o)
+    return fail(FA_ERR_INVALID_ARG, "o_a, lse_a, o_b, lse_b and o must be non-null");
+  if (!aligned16(o_a) || !aligned16(o_b) || !aligned16(o))
+    return fail(FA_ERR_INVALID_ARG, "outputs must be 16-byte aligned");
+  if (!aligned4(lse_a) || !aligned4(lse_b) || (lse && !aligned4(lse)))
+    return fail(FA_ERR_INVALID_ARG, "LSE arrays must be 4-byte aligned");
+  if (rows > (1LL << 40)) return fail(FA_ERR_INVALID_ARG, "too many rows");
+  DeviceInfo dev;
+  fa_status st = device_info(&dev);
+  if (st != FA_OK) return st;
+  cudaError_t e = fa::launch_merge(o_a, lse_a, o_b, lse_b, o, lse, rows, d, dtype == FA_BF16,
+                                   dev.sms, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "merge launch");
+  return FA_OK;
+}
+
+fa_status fa_kv_append(const void* k_new, const void* v_new, void* k_pages, void* v_pages,
+                       const int32_t* block_table, const int32_t* ctx_lens,
+                       const int32_t* new_lens, int B, int H, int T, int d, int page_size,
+                       int max_pages_per_seq, int num_pages, int dtype, fa_stream_t stream) {
+  if (B < 1 || H < 1 || T < 0 || max_pages_per_seq < 1 || num_pages < 1)
+    return fail(FA_ERR_INVALID_ARG, "need B, H, max_pages_per_seq, num_pages >= 1 and T >= 0");
+  if (d != 64 && d != 128) return fail(FA_ERR_UNSUPPORTED, "head dim %d (supported: 64, 128)", d);
+  if (dtype != FA_F16 && dtype != FA_BF16) return fail(FA_ERR_UNSUPPORTED, "dtype %d", dtype);
+  if (page_size < 16 || page_size > 4096 || page_size % 16 != 0)
+    return fail(FA_ERR_UNSUPPORTED, "page_size %d (a multiple of 16 in [16, 4096])", page_size);
+  if (T == 0) return FA_OK;
+  if (!k_new || !v_new || !k_pages || !v_pages || !block_table || !ctx_lens)
+    return fail(FA_ERR_INVALID_ARG, "k_new, v_new, pools, block_table and ctx_lens must be non-null");
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_pages) || !aligned16(v_pages))
+    return fail(FA_ERR_INVALID_ARG, "k_new, v_new and pools must be 16-byte aligned");
+  if (!aligned4(block_table) || !aligned4(ctx_lens) || (new_lens && !aligned4(new_lens)))
+    return fail(FA_ERR_INVALID_ARG, "block_table, ctx_lens and new_lens must be 4-byte aligned");
+  const long long cap = static_cast<long long>(page_size) * max_pages_per_seq;
+  if (cap > (1LL << 30) || static_cast<long long>(B) * H > (1LL << 31) - 1 ||
+      static_cast<long long>(B) * H * T * d > (1LL << 46))
+    return fail(FA_ERR_INVALID_ARG, "problem too large");
+  DeviceInfo dev;
+  fa_status st = device_info(&dev);
+  if (st != FA_OK) return st;
+  fa::KvAppendParams p{block_table, ctx_lens, new_lens, B, H, T, d, page_size, max_pages_per_seq,
+                       num_pages, dev.status};
+  cudaError_t e = fa::launch_kv_append(k_new, v_new, k_pages, v_pages, p,
+                                       reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "append launch");
   return FA_OK;
 }
 

@@ -26,6 +26,13 @@ struct PrefillParams {
   uint32_t* status;   // device status word
   uint64_t timeout_ns;
   int32_t* trace;     // optional [BH, ceil(Sq/128), nnb] visit log (16 + class per visit)
+  // Paged K/V (chunked prefill into a paged cache). block_table == nullptr: K and V are
+  // contiguous [B,H,Sk,d]. Otherwise K/V tile rows come from pools [num_pages,H,page,d]
+  // through block_table [B, max_pages], sequence b has seq_k[b] keys and Sk is only the
+  // upper bound max_pages*page_size (used for nnb and for planning).
+  const int32_t* block_table;
+  const int32_t* seq_k;
+  int H, page_size, max_pages, num_pages;
 };
 
 struct PrefillSched;  // fa_plan.h
@@ -62,6 +69,19 @@ cudaError_t launch_decode(const DecodeParams& p, int D, bool bf16, cudaStream_t 
 // Decode with the split partials in the library's own file-scope scratch array.
 size_t noalloc_scratch_bytes();
 cudaError_t launch_decode_noalloc(const DecodeParams& p, int D, bool bf16, cudaStream_t stream);
+cudaError_t launch_merge(const void* oa, const float* la, const void* ob, const float* lb,
+                         void* o, float* lse, int64_t rows, int D, bool bf16, int sms,
+                         cudaStream_t stream);
+struct KvAppendParams {
+  const int32_t* block_table;  // [B, max_pages]
+  const int32_t* ctx_lens;     // [B] tokens already cached
+  const int32_t* new_lens;     // [B] tokens to append (<= T), or nullptr for T each
+  int B, H, T, d, page_size, max_pages, num_pages;
+  uint32_t* status;
+};
+
+cudaError_t launch_kv_append(const void* k_new, const void* v_new, void* k_pages, void* v_pages,
+                             const KvAppendParams& p, cudaStream_t stream);
 cudaError_t launch_selftest_timeout(uint32_t* status, uint64_t timeout_ns, cudaStream_t stream);
 
 }  // namespace fa

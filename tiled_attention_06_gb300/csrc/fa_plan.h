@@ -25,19 +25,22 @@ struct Range {
 FA_HD int imin(int a, int b) { return a < b ? a : b; }
 FA_HD int imax(int a, int b) { return a > b ? a : b; }
 
-FA_HD Range key_range(int m0, int m1, int BN, const PrefillParams& p) {
-  Range r{0, 0, p.nnb};
-  if (m0 >= m1) return Range{0, 0, 0};
+// `sk` is the number of keys of this (batch, head): p.Sk for contiguous K/V, the
+// sequence's own length for a paged cache.
+FA_HD Range key_range(int m0, int m1, int BN, int sk, const PrefillParams& p) {
+  const int nnb = (sk + BN - 1) / BN;
+  Range r{0, 0, nnb};
+  if (m0 >= m1 || nnb == 0) return Range{0, 0, 0};
   if (p.mask_mode == FA_MASK_NONE) return r;
-  const int delta = p.Sk - p.Sq;
+  const int delta = sk - p.Sq;
   const int r_lo = m0 + delta;      // key position of the first row
   const int r_hi = m1 - 1 + delta;  // key position of the last row
   if (r_hi < 0) return Range{0, 0, 0};
-  r.b_end = imin(p.nnb, r_hi / BN + 1);
+  r.b_end = imin(nnb, r_hi / BN + 1);
   if (p.mask_mode == FA_MASK_CAUSAL_WINDOW) {
     const int band_lo = imax(0, r_lo - p.window + 1);
     r.b_start = imin(band_lo / BN, r.b_end);
-    const int g_keys = imin(imin(p.n_global, r_hi + 1), p.Sk);
+    const int g_keys = imin(imin(p.n_global, r_hi + 1), sk);
     r.a_end = g_keys > 0 ? (g_keys + BN - 1) / BN : 0;
     if (r.a_end >= r.b_start) {  // the two ranges touch: one range [0, b_end)
       r.a_end = 0;

@@ -60,11 +60,11 @@ constexpr int pow2_at_least(int x) {
 // True when every (row, key) pair of the 128-row tile at m0 and key block nb is in range
 // and visible.
 template <int BN>
-__device__ __forceinline__ bool tile_full(int m0, int nb, const PrefillParams& p) {
+__device__ __forceinline__ bool tile_full(int m0, int nb, int sk, const PrefillParams& p) {
   const int n0 = nb * BN, n1 = n0 + BN;
-  if (m0 + kTile > p.Sq || n1 > p.Sk) return false;
+  if (m0 + kTile > p.Sq || n1 > sk) return false;
   if (p.mask_mode == FA_MASK_NONE) return true;
-  const int delta = p.Sk - p.Sq;
+  const int delta = sk - p.Sq;
   const int r_lo = m0 + delta, r_hi = m0 + kTile - 1 + delta;
   if (n1 - 1 > r_lo) return false;
   if (p.mask_mode == FA_MASK_CAUSAL) return true;
@@ -91,8 +91,9 @@ __device__ __forceinline__ uint32_t pack2(float a, float b, bool bf16) {
 template <int NC, int ON, bool BF16, typename Exchange, typename PreRescale>
 __device__ __forceinline__ bool softmax_cols(uint32_t t_lane, uint32_t s_col, uint32_t p_col,
                                              uint32_t o_col, bool full, int n0, int pos_q,
-                                             const PrefillParams& p, float& m_ref, float& l,
-                                             Exchange exchange, PreRescale before_rescale) {
+                                             int sk, const PrefillParams& p, float& m_ref,
+                                             float& l, Exchange exchange,
+                                             PreRescale before_rescale) {
   static_assert(NC == 32 || NC % 64 == 0, "column count");
   uint32_t s[NC];
   if constexpr (NC == 32) {
@@ -103,8 +104,8 @@ __device__ __forceinline__ bool softmax_cols(uint32_t t_lane, uint32_t s_col, ui
   }
   tmem_ld_wait<NC>(s);
   if (!full) {
-    int lim = min(pos_q, p.Sk - 1) - n0;
-    if (p.mask_mode == FA_MASK_NONE) lim = p.Sk - 1 - n0;
+    int lim = min(pos_q, sk - 1) - n0;
+    if (p.mask_mode == FA_MASK_NONE) lim = sk - 1 - n0;
     int lo = INT_MIN, gl = INT_MIN;
     if (p.mask_mode == FA_MASK_CAUSAL_WINDOW) {
       lo = pos_q - p.window + 1 - n0;
@@ -180,8 +181,8 @@ __device__ __forceinline__ bool softmax_tile(uint32_t t_lane, uint32_t s_col, ui
                                              bool full, int n0, int pos_q,
                                              const PrefillParams& p, float& m_ref, float& l,
                                              PreRescale before_rescale) {
-  return softmax_cols<BN, D, BF16>(t_lane, s_col, s_col, o_col, full, n0, pos_q, p, m_ref, l,
-                                   [](float m) { return m; }, before_rescale);
+  return softmax_cols<BN, D, BF16>(t_lane, s_col, s_col, o_col, full, n0, pos_q, p.Sk, p, m_ref,
+                                   l, [](float m) { return m; }, before_rescale);
 }
 
 // Epilogue for one thread's row: O (D columns at o_col) / l rounded to the dtype, and
@@ -373,7 +374,7 @@ __global__ void __launch_bounds__(kThreads256, 1)
         if (t < 0) continue;
         int bh, mb;
         item_coords(t, p, bh, mb);
-        const Range rg = key_range(mb * BM, min(mb * BM + BM, p.Sq), BN, p);
+        const Range rg = key_range(mb * BM, min(mb * BM + BM, p.Sq), BN, p.Sk, p);
         const int n = range_count(rg);
         if (n == 0) continue;
         for (int q = 0; q < 2 && ok; ++q) {
@@ -419,7 +420,7 @@ __global__ void __launch_bounds__(kThreads256, 1)
         if (t < 0) continue;
         int bh, mb;
         item_coords(t, p, bh, mb);
-        const Range rg = key_range(mb * BM, min(mb * BM + BM, p.Sq), BN, p);
+        const Range rg = key_range(mb * BM, min(mb * BM + BM, p.Sq), BN, p.Sk, p);
         const int n = range_count(rg);
         if (n == 0) continue;
         {  // S_A(0), S_B(0) with K0
@@ -490,7 +491,7 @@ __global__ void __launch_bounds__(kThreads256, 1)
       if (t < 0) continue;
       int bh, mb;
       item_coords(t, p, bh, mb);
-      const Range rg = key_range(mb * BM, min(mb * BM + BM, p.Sq), BN, p);
+      const Range rg = key_range(mb * BM, min(mb * BM + BM, p.Sq), BN, p.Sk, p);
       const int n = range_count(rg);
       const int m0 = mb * BM + q * kTile;  // first row of this tile
       const int qrow = m0 + row;
@@ -499,12 +500,12 @@ __global__ void __launch_bounds__(kThreads256, 1)
         if (qrow < p.Sq) store_zero_row<D>(orow, p);
         continue;
       }
-      const Range mine = key_range(m0, min(m0 + kTile, p.Sq), BN, p);
+      const Range mine = key_range(m0, min(m0 + kTile, p.Sq), BN, p.Sk, p);
       const int pos_q = qrow + delta;
       float m_ref = -INFINITY, l = 0.f;
       for (int j = 0; j < n; ++j) {
         const int nb = range_nb(rg, j);
-        const bool full = tile_full<BN>(m0, nb, p);
+        const bool full = tile_full<BN>(m0, nb, p.Sk, p);
         ok = mbar_wait(B(bars->s_full[q]), tc & 1, wc);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
@@ -596,9 +597,17 @@ struct Bars128 {
 };
 
 struct ItemRef {
-  int bh, mb, n;
+  int bh, mb, n, sk;
   Range rg;
 };
+
+// Keys of (batch, head) bh: Sk for contiguous K/V; the sequence's own length (clamped
+// to the table's capacity) for a paged cache.
+__device__ __forceinline__ int item_sk(const PrefillParams& p, int bh) {
+  if (!p.block_table) return p.Sk;
+  const int c = p.seq_k[bh / p.H];
+  return c < 0 ? 0 : (c > p.Sk ? p.Sk : c);
+}
 
 // Next item of this CTA (empty ones included when `with_empty`): false when none is left.
 template <int BM>
@@ -609,7 +618,8 @@ __device__ __forceinline__ bool next_item(const PrefillSched& s, const PrefillPa
     ++k;
     if (t < 0) continue;
     item_coords(t, p, it.bh, it.mb);
-    it.rg = key_range(it.mb * BM, min(it.mb * BM + BM, p.Sq), BN, p);
+    it.sk = item_sk(p, it.bh);
+    it.rg = key_range(it.mb * BM, min(it.mb * BM + BM, p.Sq), BN, it.sk, p);
     it.n = range_count(it.rg);
     if (it.n > 0 || with_empty) return true;
   }
@@ -707,9 +717,20 @@ __global__ void __launch_bounds__(kThreads128, 1)
         const uint32_t dst = sRing + slot * C::TILE_BYTES;
         mbar_arrive_expect_tx(B(bars->full[slot]), C::TILE_BYTES);
         const int n0 = range_nb(it.rg, j) * BN;
+        int y = n0, z = it.bh;
+        if (p.block_table) {  // the tile's rows lie in one page: (page, offset) of key n0
+          const int b = it.bh / p.H, lp = n0 / p.page_size;
+          int phys = p.block_table[static_cast<size_t>(b) * p.max_pages + lp];
+          if (phys < 0 || phys >= p.num_pages) {  // skip the bad page: load page 0, report
+            atomicOr(p.status, FA_DEV_BAD_PAGE);
+            phys = 0;
+          }
+          y = n0 - lp * p.page_size;
+          z = phys * p.H + (it.bh - b * p.H);
+        }
         const void* map = is_v ? (const void*)&tmV : (const void*)&tmK;
         for (int c = 0; c < C::KCH; ++c)
-          tma_load_3d(dst + c * (BN * 128), map, B(bars->full[slot]), c * 64, n0, it.bh);
+          tma_load_3d(dst + c * (BN * 128), map, B(bars->full[slot]), c * 64, y, z);
         fills[slot] = use + 1;
         ++pos;
       };
@@ -852,7 +873,6 @@ __global__ void __launch_bounds__(kThreads128, 1)
     const int half = warp / 4;  // 0: keys [0, BN/2) of each tile, 1: keys [BN/2, BN)
     const int row = (warp % 4) * 32 + lane;
     const uint32_t t_lane = tmem + (static_cast<uint32_t>((warp % 4) * 32) << 16);
-    const int delta = p.Sk - p.Sq;
     uint32_t ii = 0, g = 0;
     bool ok = true;
     int kc = 0;
@@ -860,11 +880,11 @@ __global__ void __launch_bounds__(kThreads128, 1)
     while (ok && next_item<BM>(sched, p, cta, G, BN, kc, it, false)) {
       const uint32_t buf = ii & 1;
       const int m0 = it.mb * BM;
-      const int pos_q = m0 + row + delta;
+      const int pos_q = m0 + row + it.sk - p.Sq;  // key position of this query
       float m_ref = -INFINITY, l = 0.f;
       for (int j = 0; j < it.n; ++j, ++g) {
         const int nb = range_nb(it.rg, j);
-        const bool full = tile_full<BN>(m0, nb, p);
+        const bool full = tile_full<BN>(m0, nb, it.sk, p);
         ok = mbar_wait(B(bars->s_full[g & 1]), (g >> 1) & 1, wc);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
@@ -898,8 +918,8 @@ __global__ void __launch_bounds__(kThreads128, 1)
         ok = softmax_cols<BN / 2, D / 2, BF16>(t_lane, s_col + half * (BN / 2),
                                                s_col + half * (BN / 4),
                                                2 * BN + buf * D + half * (D / 2), full,
-                                               nb * BN + half * (BN / 2), pos_q, p, m_ref, l,
-                                               exchange, wait_pv);
+                                               nb * BN + half * (BN / 2), pos_q, it.sk, p, m_ref,
+                                               l, exchange, wait_pv);
         if (!ok || !x_ok) {
           ok = false;
           break;
