@@ -44,6 +44,7 @@ PREFILL = {
                       n_global=64, factor=1.0),
 }
 DECODE = dict(B=32, H=32, d=128, page=256, pool=1200, max_ctx=8192, dtype="f16")
+PREFIX_WORKLOADS = ("default", "decode", "causal2k", "causal4k", "noncausal4k", "window32k")
 MODE_NAME = {0: "none", 1: "causal", 2: "causal_window"}
 
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu
@@ -227,6 +228,8 @@ def run_ours(args, rank, world):
     peaks, peak_kind = load_peaks()
     stream = torch.cuda.current_stream()
     workload = "default" if args.workload == "default" else args.workload
+    if workload in ("chunked", "multimodal"):
+        return run_next_rows(args, fa, workload, peaks, peak_kind, stream, world)
     pcfg = PREFILL["causal4k" if workload in ("default", "sweep") else workload] \
         if workload != "decode" else None
     with_decode = workload in ("default", "decode")
@@ -520,6 +523,126 @@ def cpu_baseline(pcfg, q, k, v, di):
     return out
 
 
+# --------------------------------------------------------------------------- next rows
+CHUNKED = dict(B=8, H=32, d=128, page=256, pool=600, chunk=512, max_ctx0=7680, dtype="f16")
+MULTIMODAL = dict(B=4, H=32, d=128, V=576, T=2048, dtype="bf16")
+
+
+def timed(calls, K, W, stream):
+    """Run each zero-argument call per step; CUDA-event milliseconds of each, summed."""
+    for _ in range(W):
+        for c in calls:
+            c()
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)] for _ in range(K)]
+    for i in range(K):
+        ev[i][0].record(stream)
+        for j, c in enumerate(calls):
+            c()
+            ev[i][j + 1].record(stream)
+    torch.cuda.synchronize()
+    return [sum(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(K)) for j in range(len(calls))]
+
+
+def run_next_rows(args, fa, workload, peaks, peak_kind, stream, world):
+    """chunked: append a 512-token chunk to each of 8 paged sequences (contexts up to
+    7.7k, 256-token pages, fp16) and run its causal prefill through the block table.
+    multimodal: LLaVA-shaped vision 576 + text 2048 tokens (B=4, H=32, d=128, bf16) as
+    three calls (vision full, text causal, text-to-vision) plus the LSE merge; the same
+    layer as two calls (vision, text over [vision; text] keys) is timed beside it."""
+    from tiled_attention_06_gb300 import inputs
+    dev = torch.device("cuda", torch.cuda.current_device())
+    K, W = args.steps, args.warmup
+    tc_peak = float(peaks["bf16_tflops"])
+    res = {"n_gpus": world, "steps": K, "warmup": W, "scaling": "weak", "vs_baseline": None,
+           "higher_is_better": True, "data": "synthetic (seeded N(0,1))"}
+    if workload == "chunked":
+        c = CHUNKED
+        dt = inputs.DTYPES[c["dtype"]]
+        g = torch.Generator().manual_seed(0)
+        ctx0 = torch.randint(0, c["max_ctx0"] + 1, (c["B"],), generator=g)
+        total = (ctx0 + c["chunk"]).tolist()
+        npages = [-(-t // c["page"]) for t in total]
+        perm = torch.randperm(c["pool"], generator=g)
+        table = torch.full((c["B"], max(npages)), -1, dtype=torch.int32)
+        off = 0
+        for b in range(c["B"]):
+            table[b, :npages[b]] = perm[off:off + npages[b]].to(torch.int32)
+            off += npages[b]
+        B, H, d, T = c["B"], c["H"], c["d"], c["chunk"]
+        kp = torch.randn(c["pool"], H, c["page"], d, generator=g).to(dt).to(dev)
+        vp = torch.randn(c["pool"], H, c["page"], d, generator=g).to(dt).to(dev)
+        kn = torch.randn(B, H, T, d, generator=g).to(dt).to(dev)
+        vn = torch.randn(B, H, T, d, generator=g).to(dt).to(dev)
+        q = torch.randn(B, H, T, d, generator=g).to(dt).to(dev)
+        tab, c0 = table.to(dev), ctx0.to(torch.int32).to(dev)
+        ctx = torch.tensor(total, dtype=torch.int32, device=dev)
+        o = torch.empty_like(q)
+        lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+        scale = 1 / math.sqrt(d)
+        # every step appends the same chunk at the same place, then runs its prefill
+        ms = timed([lambda: fa.fa_kv_append(kn, vn, kp, vp, tab, c0, stream=stream),
+                    lambda: fa.fa_fwd_paged(q, kp, vp, tab, ctx, o, lse, scale,
+                                            fa.FA_MASK_CAUSAL, stream=stream)], K, W, stream)
+        assert fa.fa_get_device_status() == fa.FA_OK
+        pairs = sum(visible_pairs(T, t, 1) for t in total)
+        flops = 4.0 * H * d * pairs
+        app_bytes = 2 * 2 * B * H * T * d * 2  # read k/v chunk, write into pages
+        pf = flops * K / (ms[1] / 1e3) / 1e12
+        res.update({"metric": "chunked prefill through a paged KV cache TFLOP/s",
+                    "value": pf, "unit": "TFLOP/s", "dtype": c["dtype"],
+                    "ms_per_step": (ms[0] + ms[1]) / K, "gpu_launches": 2 * K,
+                    "roofline": {"kernel": "prefill_bm128_kernel (paged)", "bound": "tensor",
+                                 "achieved": pf, "peak": tc_peak, "unit": "TFLOP/s",
+                                 "frac": pf / tc_peak, "traffic": None,
+                                 "algorithmic_flops": flops},
+                    "append": {"value": app_bytes * K / (ms[0] / 1e3) / 1e9, "unit": "GB/s",
+                               "ms_per_call": ms[0] / K},
+                    "config": {"workload": f"append {T} tokens + causal chunked prefill, B{B} "
+                                           f"H{H} d{d} {c['dtype']}, ctx0~U[0,{c['max_ctx0']}], "
+                                           f"page {c['page']}, pool {c['pool']}"}})
+    else:
+        c = MULTIMODAL
+        dt = inputs.DTYPES[c["dtype"]]
+        B, H, d, V, T = c["B"], c["H"], c["d"], c["V"], c["T"]
+        q, k, v = inputs.prefill_inputs(B, H, V + T, V + T, d, dt, seed=0)
+        q, k, v = q.to(dev), k.to(dev), v.to(dev)
+        qv, qt = q[:, :, :V].contiguous(), q[:, :, V:].contiguous()
+        kv_, kt = k[:, :, :V].contiguous(), k[:, :, V:].contiguous()
+        vv, vt = v[:, :, :V].contiguous(), v[:, :, V:].contiguous()
+        scale = 1 / math.sqrt(d)
+        ov, lv = torch.empty_like(qv), torch.empty(B, H, V, device=dev)
+        ott, ltt = torch.empty_like(qt), torch.empty(B, H, T, device=dev)
+        otv, ltv = torch.empty_like(qt), torch.empty(B, H, T, device=dev)
+        ot, lt = torch.empty_like(qt), torch.empty(B, H, T, device=dev)
+        o1, l1 = torch.empty_like(qt), torch.empty(B, H, T, device=dev)
+        split = [lambda: fa.fa_fwd(qv, kv_, vv, ov, lv, scale, fa.FA_MASK_NONE, stream=stream),
+                 lambda: fa.fa_fwd(qt, kt, vt, ott, ltt, scale, fa.FA_MASK_CAUSAL, stream=stream),
+                 lambda: fa.fa_fwd(qt, kv_, vv, otv, ltv, scale, fa.FA_MASK_NONE, stream=stream),
+                 lambda: fa.fa_merge_partials(ott, ltt, otv, ltv, ot, lt, stream=stream)]
+        ms = timed(split, K, W, stream)
+        one = timed([lambda: fa.fa_fwd(qt, k, v, o1, l1, scale, fa.FA_MASK_CAUSAL,
+                                       stream=stream)], K, W, stream)
+        assert fa.fa_get_device_status() == fa.FA_OK
+        pairs = V * V + T * (T + 1) // 2 + T * V
+        flops = 4.0 * B * H * d * pairs
+        total_ms = sum(ms)
+        val = flops * K / (total_ms / 1e3) / 1e12
+        res.update({"metric": "multimodal attention layer TFLOP/s (three-call split + merge)",
+                    "value": val, "unit": "TFLOP/s", "dtype": c["dtype"],
+                    "ms_per_step": total_ms / K, "gpu_launches": 4 * K,
+                    "roofline": {"kernel": "prefill_bm128_kernel x3 + merge", "bound": "tensor",
+                                 "achieved": val, "peak": tc_peak, "unit": "TFLOP/s",
+                                 "frac": val / tc_peak, "traffic": None,
+                                 "algorithmic_flops": flops},
+                    "calls_ms": {"vision": ms[0] / K, "text_causal": ms[1] / K,
+                                 "text_to_vision": ms[2] / K, "merge": ms[3] / K},
+                    "text_rows_one_call_ms": one[0] / K,
+                    "config": {"workload": f"vision {V} + text {T} tokens, B{B} H{H} d{d} "
+                                           f"{c['dtype']}"}})
+    return res
+
+
 # --------------------------------------------------------------------------- reference arm
 def run_reference(args, rank, world):
     """The oracle as it stands, on the host cores: each step is a bounded sample of the
@@ -529,7 +652,7 @@ def run_reference(args, rank, world):
 
     import oracle
     from tiled_attention_06_gb300 import inputs
-    workload = args.workload if args.workload not in ("sweep",) else "default"
+    workload = args.workload if args.workload in PREFIX_WORKLOADS else "default"
     pcfg = None if workload == "decode" else PREFILL["causal4k" if workload == "default"
                                                      else workload]
     res = {"impl": "reference", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -621,6 +744,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="default",
                     choices=["default", "causal2k", "causal4k", "noncausal4k", "window32k",
+                             "chunked", "multimodal",
                              "decode", "sweep"])
     ap.add_argument("--batch", type=int, default=None, help="override B (small profiling cases)")
     ap.add_argument("--heads", type=int, default=None, help="override H (small profiling cases)")

@@ -15,7 +15,7 @@ import torch
 
 from . import build as _build
 
-MASK_NONE, MASK_CAUSAL, MASK_CAUSAL_WINDOW = 0, 1, 2
+MASK_NONE, MASK_CAUSAL, MASK_CAUSAL_WINDOW, MASK_BAND, MASK_PREFIX_LM = 0, 1, 2, 3, 4
 TILE_EMPTY, TILE_PARTIAL, TILE_FULL = 0, 1, 2
 REC_UNNORMALISED, REC_NORMALISED, REC_LITERAL_P2 = 0, 1, 2
 

@@ -102,12 +102,20 @@ static size_t elem_size(int dtype) {
  *                  such as BOS, read causally: the window holds `window` keys
  *                  counting the query's own position; the global tokens are
  *                  the first n_global key positions).
+ *   BAND           |i+delta - j| <= window: the diagonal band of [Ascend-FA]
+ *                  section 3.2, each token seeing the tokens within +-w of it.
+ *   PREFIX_LM      j <= i+delta or j < n_global: the first n_global keys (the
+ *                  prefix) are seen by every query, the rest causally (the
+ *                  prefix-LM variant [boost] scenario 3 lists by name; the
+ *                  pages define it no further).
  */
 int or_visible(int64_t i, int64_t j, int64_t Sq, int64_t Sk, int mask_mode,
                int64_t window, int64_t n_global) {
     int64_t pos = i + (Sk - Sq);
     if (i < 0 || i >= Sq || j < 0 || j >= Sk) return 0;
     if (mask_mode == OR_MASK_NONE) return 1;
+    if (mask_mode == OR_MASK_BAND) return (j - pos <= window) && (pos - j <= window);
+    if (mask_mode == OR_MASK_PREFIX_LM) return (j <= pos) || (j < n_global);
     if (j > pos) return 0;
     if (mask_mode == OR_MASK_CAUSAL) return 1;
     return (pos - j < window) || (j < n_global);
@@ -198,8 +206,10 @@ int or_attention(const void* q, const void* k, const void* v, int dtype,
                  int64_t window, int64_t n_global, const int64_t* rows,
                  int64_t nrows, double* max_psum_err, int nthreads) {
     if (B < 0 || H < 0 || Sq < 0 || Sk < 0 || d <= 0) return -1;
-    if (mask_mode < OR_MASK_NONE || mask_mode > OR_MASK_CAUSAL_WINDOW) return -1;
+    if (mask_mode < OR_MASK_NONE || mask_mode > OR_MASK_PREFIX_LM) return -1;
     if (mask_mode == OR_MASK_CAUSAL_WINDOW && (window < 1 || n_global < 0)) return -1;
+    if (mask_mode == OR_MASK_BAND && window < 0) return -1;
+    if (mask_mode == OR_MASK_PREFIX_LM && n_global < 0) return -1;
     int64_t n_out = rows ? nrows : B * H * Sq;
     /* order[r] = output index r, sorted by the row it asks for, so that the rows
        of one (batch, head) are contiguous */

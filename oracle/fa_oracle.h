@@ -26,7 +26,8 @@ extern "C" {
 /* element types the oracle can read */
 enum { OR_F16 = 0, OR_BF16 = 1, OR_F32 = 2, OR_F64 = 3 };
 /* mask modes (same numbering as the library's public enum, chosen independently) */
-enum { OR_MASK_NONE = 0, OR_MASK_CAUSAL = 1, OR_MASK_CAUSAL_WINDOW = 2 };
+enum { OR_MASK_NONE = 0, OR_MASK_CAUSAL = 1, OR_MASK_CAUSAL_WINDOW = 2, OR_MASK_BAND = 3,
+       OR_MASK_PREFIX_LM = 4 };
 /* tile classes */
 enum { OR_TILE_EMPTY = 0, OR_TILE_PARTIAL = 1, OR_TILE_FULL = 2 };
 /* online-recurrence variants (see or_online_attention) */

@@ -16,7 +16,7 @@ import pytest
 import torch
 
 import oracle
-from oracle import MASK_CAUSAL, MASK_CAUSAL_WINDOW, MASK_NONE
+from oracle import MASK_BAND, MASK_CAUSAL, MASK_CAUSAL_WINDOW, MASK_NONE, MASK_PREFIX_LM
 from tiled_attention_06_gb300 import inputs
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "hand_examples.json")
@@ -78,7 +78,13 @@ def _mask_by_ranges(Sq, Sk, mode, window=0, n_global=0):
     ones = torch.ones(Sq, Sk, dtype=torch.bool)
     if mode == MASK_NONE:
         return ones
+    if mode == MASK_BAND:   # |pos - j| <= window
+        return torch.tril(ones, diagonal=delta + window) & torch.triu(ones, diagonal=delta - window)
     causal = torch.tril(ones, diagonal=delta)
+    if mode == MASK_PREFIX_LM:
+        prefix = torch.zeros(Sq, Sk, dtype=torch.bool)
+        prefix[:, :min(n_global, Sk)] = True
+        return causal | prefix
     if mode == MASK_CAUSAL:
         return causal
     too_far = torch.tril(ones, diagonal=delta - window)   # pos - j >= window
@@ -107,7 +113,11 @@ def test_mask_hand_enumerated():
                                                   (MASK_CAUSAL_WINDOW, 1, 0),
                                                   (MASK_CAUSAL_WINDOW, 4, 3),
                                                   (MASK_CAUSAL_WINDOW, 100, 0),
-                                                  (MASK_CAUSAL_WINDOW, 3, 100)])
+                                                  (MASK_CAUSAL_WINDOW, 3, 100),
+                                                  (MASK_BAND, 0, 0), (MASK_BAND, 3, 0),
+                                                  (MASK_BAND, 100, 0), (MASK_PREFIX_LM, 0, 0),
+                                                  (MASK_PREFIX_LM, 0, 5),
+                                                  (MASK_PREFIX_LM, 0, 100)])
 def test_mask_matches_range_construction(Sq, Sk, mode, window, n_global):
     got = _mask_matrix(Sq, Sk, mode, window, n_global)
     want = _mask_by_ranges(Sq, Sk, mode, window, n_global).numpy()
@@ -133,6 +143,50 @@ def test_pair_counts_closed_forms():
         assert oracle.count_visible(S, S, MASK_CAUSAL_WINDOW, w, g) == _window_pairs_closed_form(S, w, g)
     # the long-context configuration: S=32768, window 2048, 64 global keys
     assert _window_pairs_closed_form(32768, 2048, 64) == 66_976_800
+
+
+def test_band_and_prefix_masks_hand_enumerated():
+    b = _mask_matrix(5, 5, MASK_BAND, window=1)
+    assert b.astype(int).tolist() == [[1, 1, 0, 0, 0],
+                                      [1, 1, 1, 0, 0],
+                                      [0, 1, 1, 1, 0],
+                                      [0, 0, 1, 1, 1],
+                                      [0, 0, 0, 1, 1]]
+    p = _mask_matrix(5, 5, MASK_PREFIX_LM, n_global=2)
+    assert p.astype(int).tolist() == [[1, 1, 0, 0, 0],
+                                      [1, 1, 0, 0, 0],
+                                      [1, 1, 1, 0, 0],
+                                      [1, 1, 1, 1, 0],
+                                      [1, 1, 1, 1, 1]]
+    # Sq < Sk: the queries sit at the last positions
+    assert _mask_matrix(2, 4, MASK_BAND, window=1).astype(int).tolist() == [[0, 1, 1, 1],
+                                                                            [0, 0, 1, 1]]
+
+
+def test_band_and_prefix_pair_counts():
+    for S, w in [(1, 0), (10, 0), (10, 3), (64, 20), (30, 100)]:
+        want = sum(min(i + w, S - 1) - max(i - w, 0) + 1 for i in range(S))
+        assert oracle.count_visible(S, S, MASK_BAND, w, 0) == want
+    for S, g in [(1, 0), (10, 3), (64, 20), (30, 100)]:
+        want = sum(max(i + 1, min(g, S)) for i in range(S))
+        assert oracle.count_visible(S, S, MASK_PREFIX_LM, 0, g) == want
+
+
+def test_band_and_prefix_special_cases():
+    S = 29
+    q, k, v = inputs.prefill_inputs(1, 2, S, S, 16, torch.float16, seed=101)
+    on, ln = oracle.attention(q, k, v, 0.25, MASK_NONE)
+    oc, lc = oracle.attention(q, k, v, 0.25, MASK_CAUSAL)
+    ob, lb = oracle.attention(q, k, v, 0.25, MASK_BAND, S, 0)        # band covers all
+    np.testing.assert_array_equal(ob, on)
+    np.testing.assert_array_equal(lb, ln)
+    o0, _ = oracle.attention(q, k, v, 0.25, MASK_BAND, 0, 0)         # only itself
+    np.testing.assert_array_equal(o0, v.double().numpy())
+    op, lp = oracle.attention(q, k, v, 0.25, MASK_PREFIX_LM, 0, 0)   # no prefix: causal
+    np.testing.assert_array_equal(op, oc)
+    np.testing.assert_array_equal(lp, lc)
+    op, lp = oracle.attention(q, k, v, 0.25, MASK_PREFIX_LM, 0, S)   # all prefix: none
+    np.testing.assert_array_equal(op, on)
 
 
 @pytest.mark.slow
@@ -267,7 +321,8 @@ def test_probabilities_sum_to_one():
 
 @pytest.mark.parametrize("Sq,Sk", [(33, 33), (17, 49), (64, 64)])
 @pytest.mark.parametrize("mode,w,g", [(MASK_NONE, 0, 0), (MASK_CAUSAL, 0, 0),
-                                      (MASK_CAUSAL_WINDOW, 6, 3)])
+                                      (MASK_CAUSAL_WINDOW, 6, 3), (MASK_BAND, 5, 0),
+                                      (MASK_PREFIX_LM, 0, 7)])
 @pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
 def test_matches_torch_sdpa_float64(Sq, Sk, mode, w, g, dtype):
     q, k, v = inputs.prefill_inputs(2, 2, Sq, Sk, 32, dtype, seed=11)
