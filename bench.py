@@ -42,10 +42,16 @@ PREFILL = {
                         factor=1.0),
     "window32k": dict(B=1, H=32, S=32768, d=128, dtype="bf16", mode=2, window=2048,
                       n_global=64, factor=1.0),
+    # the pages give no width for these two masks: band +-512 keys, a 1024-key prefix
+    "band4k": dict(B=4, H=32, S=4096, d=128, dtype="bf16", mode=3, window=512, n_global=0,
+                   factor=1.0),
+    "prefixlm4k": dict(B=4, H=32, S=4096, d=128, dtype="bf16", mode=4, window=0, n_global=1024,
+                       factor=1.0),
 }
 DECODE = dict(B=32, H=32, d=128, page=256, pool=1200, max_ctx=8192, dtype="f16")
-PREFIX_WORKLOADS = ("default", "decode", "causal2k", "causal4k", "noncausal4k", "window32k")
-MODE_NAME = {0: "none", 1: "causal", 2: "causal_window"}
+PREFIX_WORKLOADS = ("default", "decode", "causal2k", "causal4k", "noncausal4k", "window32k",
+                    "band4k", "prefixlm4k")
+MODE_NAME = {0: "none", 1: "causal", 2: "causal_window", 3: "band", 4: "prefix_lm"}
 
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu
 # capture of each kernel, with the SHA-256 of the kernel sources it was taken on; the
@@ -79,24 +85,27 @@ def ncu_traffic(kind, override):
 
 
 # --------------------------------------------------------------------------- accounting
+def row_visible(pos, Sk, mode, window=0, n_global=0):
+    """Keys visible to the query at key position `pos` (closed form of the mask)."""
+    if mode == 0:
+        return Sk
+    if mode == 3:  # |pos - j| <= window
+        return max(0, min(pos + window, Sk - 1) - max(pos - window, 0) + 1)
+    if mode == 4:  # j <= pos or j < n_global
+        return max(0, min(max(pos + 1, n_global), Sk))
+    if pos < 0:
+        return 0
+    hi = min(pos, Sk - 1) + 1
+    if mode == 1:
+        return hi
+    lo = max(0, pos - window + 1)
+    return max(0, hi - lo) + max(0, min(n_global, hi, lo))
+
+
 def visible_pairs(Sq, Sk, mode, window=0, n_global=0):
-    """Number of (query, key) pairs the mask leaves visible (closed form per row)."""
+    """Number of (query, key) pairs the mask leaves visible."""
     delta = Sk - Sq
-    total = 0
-    for i in range(Sq):
-        pos = i + delta
-        if mode == 0:
-            total += Sk
-            continue
-        if pos < 0:
-            continue
-        hi = min(pos, Sk - 1) + 1
-        if mode == 1:
-            total += hi
-            continue
-        lo = max(0, pos - window + 1)
-        total += max(0, hi - lo) + max(0, min(n_global, hi, lo))
-    return total
+    return sum(row_visible(i + delta, Sk, mode, window, n_global) for i in range(Sq))
 
 
 def prefill_flops(cfg):
@@ -325,7 +334,8 @@ def run_ours(args, rank, world):
                               "(% of 8 TB/s)",
                     "value": value, "unit": "TFLOP/s", "higher_is_better": True,
                     "dtype": pcfg["dtype"]})
-        res["roofline"] = {"kernel": f"prefill_bm256_kernel<128,128,{pcfg['dtype']}>",
+        bm = args.block_m or fa.fa_fwd_block_m()
+        res["roofline"] = {"kernel": f"prefill_bm{bm}_kernel<{pcfg['d']},128,{pcfg['dtype']}>",
                            "bound": "tensor",
                            "achieved": achieved, "peak": tc_peak, "unit": "TFLOP/s",
                            "frac": achieved / tc_peak,
@@ -469,13 +479,7 @@ def oracle_prefill_sample(pcfg, q, k, v, n_heads):
 
 
 def visible_pairs_row(pos, Sk, pcfg):
-    if pcfg["mode"] == 0:
-        return Sk
-    hi = min(pos, Sk - 1) + 1
-    if pcfg["mode"] == 1:
-        return hi
-    lo = max(0, pos - pcfg["window"] + 1)
-    return max(0, hi - lo) + max(0, min(pcfg["n_global"], hi, lo))
+    return row_visible(pos, Sk, pcfg["mode"], pcfg["window"], pcfg["n_global"])
 
 
 def oracle_decode_sample(di, n_seq):
@@ -744,7 +748,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="default",
                     choices=["default", "causal2k", "causal4k", "noncausal4k", "window32k",
-                             "chunked", "multimodal",
+                             "band4k", "prefixlm4k", "chunked", "multimodal",
                              "decode", "sweep"])
     ap.add_argument("--batch", type=int, default=None, help="override B (small profiling cases)")
     ap.add_argument("--heads", type=int, default=None, help="override H (small profiling cases)")

@@ -21,6 +21,14 @@
  *                          position included) plus the first `n_global` keys as
  *                          global tokens ("ascend-transformer-boost 实战" (ai6s.net),
  *                          scenario 3, window_size=2048, global_tokens=64).
+ *   FA_MASK_BAND           |i + delta - j| <= window: a two-sided band, each query
+ *                          seeing the keys within `window` positions of its own on
+ *                          either side (the diagonal band of the zwxr.cn article on
+ *                          ops-transformer, section 3.2); window >= 0.
+ *   FA_MASK_PREFIX_LM      j <= i + delta or j < n_global: the first n_global keys (the
+ *                          prefix) are seen by every query, the rest causally (the
+ *                          prefix-LM variant named in "ascend-transformer-boost 实战",
+ *                          scenario 3); n_global >= 0.
  * A query that sees no key gets O = 0 and LSE = -inf.
  *
  * Conventions for every call:
@@ -57,7 +65,13 @@ typedef enum {
 } fa_status;
 
 enum { FA_F16 = 0, FA_BF16 = 1 };
-enum { FA_MASK_NONE = 0, FA_MASK_CAUSAL = 1, FA_MASK_CAUSAL_WINDOW = 2 };
+enum {
+  FA_MASK_NONE = 0,
+  FA_MASK_CAUSAL = 1,
+  FA_MASK_CAUSAL_WINDOW = 2,
+  FA_MASK_BAND = 3,
+  FA_MASK_PREFIX_LM = 4
+};
 
 /*
  * fa_fwd - attention forward (prefill) over contiguous BHSD tensors.
@@ -69,8 +83,9 @@ enum { FA_MASK_NONE = 0, FA_MASK_CAUSAL = 1, FA_MASK_CAUSAL_WINDOW = 2 };
  *          call then does nothing); k and v may be NULL when Sk == 0 (every row then
  *          sees no key).
  *   scale  the softmax scale (typically 1/sqrt(d))
- *   mask_mode / window / n_global as above (window >= 1 and n_global >= 0 for
- *          FA_MASK_CAUSAL_WINDOW; ignored otherwise)
+ *   mask_mode / window / n_global as above: window >= 1 and n_global >= 0 for
+ *          FA_MASK_CAUSAL_WINDOW, window >= 0 for FA_MASK_BAND, n_global >= 0 for
+ *          FA_MASK_PREFIX_LM; a parameter the mode does not use is ignored.
  *   dtype  FA_F16 or FA_BF16 (added before `stream`: a signature without it could
  *          not tell fp16 inputs from bf16 inputs)
  */

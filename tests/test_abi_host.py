@@ -96,7 +96,10 @@ def _fwd(L, **kw):
     (dict(d=96), fa.FA_ERR_UNSUPPORTED),
     (dict(d=256), fa.FA_ERR_UNSUPPORTED),
     (dict(dtype=2), fa.FA_ERR_UNSUPPORTED),
-    (dict(mask_mode=3), fa.FA_ERR_INVALID_ARG),
+    (dict(mask_mode=5), fa.FA_ERR_INVALID_ARG),
+    (dict(mask_mode=-1), fa.FA_ERR_INVALID_ARG),
+    (dict(mask_mode=3, window=-1), fa.FA_ERR_INVALID_ARG),
+    (dict(mask_mode=4, n_global=-1), fa.FA_ERR_INVALID_ARG),
     (dict(mask_mode=2, window=0), fa.FA_ERR_INVALID_ARG),
     (dict(mask_mode=2, window=4, n_global=-1), fa.FA_ERR_INVALID_ARG),
     (dict(scale=float("nan")), fa.FA_ERR_INVALID_ARG),

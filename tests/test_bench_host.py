@@ -14,7 +14,12 @@ import oracle
 @pytest.mark.parametrize("Sq,Sk,mode,w,g", [(37, 37, 0, 0, 0), (37, 37, 1, 0, 0),
                                             (20, 45, 1, 0, 0), (45, 20, 1, 0, 0),
                                             (200, 200, 2, 16, 5), (100, 130, 2, 7, 40),
-                                            (64, 64, 2, 1, 0), (64, 64, 2, 100, 100)])
+                                            (64, 64, 2, 1, 0), (64, 64, 2, 100, 100),
+                                            (90, 90, 3, 0, 0), (90, 90, 3, 7, 0),
+                                            (40, 100, 3, 13, 0), (100, 40, 3, 13, 0),
+                                            (64, 64, 3, 1000, 0), (90, 90, 4, 0, 0),
+                                            (90, 90, 4, 0, 30), (40, 100, 4, 0, 70),
+                                            (100, 40, 4, 0, 20), (64, 64, 4, 0, 500)])
 def test_visible_pairs_matches_oracle_count(Sq, Sk, mode, w, g):
     assert bench.visible_pairs(Sq, Sk, mode, w, g) == oracle.count_visible(Sq, Sk, mode, w, g)
 
@@ -24,6 +29,13 @@ def test_headline_flop_counts():
     assert bench.prefill_flops(bench.PREFILL["noncausal4k"]) == 4 * 128 * 128 * 4096 * 4096
     assert bench.prefill_flops(bench.PREFILL["causal2k"]) == 4 * 128 * 128 * 2_098_176
     assert bench.prefill_flops(bench.PREFILL["window32k"]) == 4 * 32 * 128 * 66_976_800
+    # band +-512 over 4096 rows: 3072 interior rows of 1025 keys, 2 x 512 edge rows
+    # of 513..1024 keys
+    assert bench.prefill_flops(bench.PREFILL["band4k"]) == 4 * 128 * 128 * (
+        3072 * 1025 + 2 * (512 * 513 + 511 * 512 // 2))
+    # prefix 1024: the first 1024 rows see 1024 keys, row i >= 1024 sees i + 1
+    assert bench.prefill_flops(bench.PREFILL["prefixlm4k"]) == 4 * 128 * 128 * (
+        1024 * 1024 + 4096 * 4097 // 2 - 1024 * 1025 // 2)
 
 
 def test_decode_bytes():

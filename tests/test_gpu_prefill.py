@@ -14,7 +14,10 @@ from _util import compare, pick_rows, sample_rows
 pytestmark = pytest.mark.gpu
 
 DT = {"f16": torch.float16, "bf16": torch.bfloat16}
-MASKS = {"none": (fa.FA_MASK_NONE, 0, 0), "causal": (fa.FA_MASK_CAUSAL, 0, 0)}
+MASKS = {"none": (fa.FA_MASK_NONE, 0, 0), "causal": (fa.FA_MASK_CAUSAL, 0, 0),
+         "window": (fa.FA_MASK_CAUSAL_WINDOW, 50, 5), "band": (fa.FA_MASK_BAND, 40, 0),
+         "prefix": (fa.FA_MASK_PREFIX_LM, 0, 70)}
+MODES = {name: m[0] for name, m in MASKS.items()}
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -53,15 +56,12 @@ SHAPES = [(1, 1), (63, 63), (65, 65), (127, 129), (129, 127), (200, 333), (257, 
 
 @pytest.mark.parametrize("Sq,Sk", SHAPES)
 @pytest.mark.parametrize("d,dt", [(64, "f16"), (128, "bf16"), (128, "f16")])
-@pytest.mark.parametrize("mask", ["none", "causal", "window"])
+@pytest.mark.parametrize("mask", ["none", "causal", "window", "band", "prefix"])
 @pytest.mark.parametrize("bn", [64, 128])
 @pytest.mark.parametrize("bm", [128, 256])
 def test_small_shapes(Sq, Sk, d, dt, mask, bn, bm):
     q, k, v = inputs.prefill_inputs(2, 3, Sq, Sk, d, DT[dt], seed=Sq * 1000 + Sk)
-    if mask == "window":
-        mode, w, g = fa.FA_MASK_CAUSAL_WINDOW, 50, 5
-    else:
-        mode, w, g = MASKS[mask]
+    mode, w, g = MASKS[mask]
     scale = 1 / math.sqrt(d)
     o, lse = run_fwd(q, k, v, scale, mode, w, g, block_n=bn, block_m=bm)
     ref_o, ref_l = oracle.attention(q, k, v, scale, mode, w, g)
@@ -69,14 +69,14 @@ def test_small_shapes(Sq, Sk, d, dt, mask, bn, bm):
 
 
 @pytest.mark.parametrize("mask,w,g", [("causal", 0, 0), ("window", 200, 70), ("window", 1, 0),
-                                      ("window", 129, 300), ("none", 0, 0)])
+                                      ("window", 129, 300), ("none", 0, 0), ("band", 0, 0),
+                                      ("band", 150, 0), ("prefix", 0, 0), ("prefix", 0, 300)])
 @pytest.mark.parametrize("Sq,Sk,bn", [(1000, 1000, 128), (700, 1100, 64), (1100, 700, 128)])
 @pytest.mark.parametrize("bm", [128, 256])
 def test_tile_trace_is_bit_exact(mask, w, g, Sq, Sk, bn, bm):
     """The tiles the kernel visits, and the class it gives each, equal the oracle's
     brute-force tile classification; no tile is visited twice."""
-    mode = {"none": fa.FA_MASK_NONE, "causal": fa.FA_MASK_CAUSAL,
-            "window": fa.FA_MASK_CAUSAL_WINDOW}[mask]
+    mode = MODES[mask]
     B, H, d = 1, 2, 64
     q, k, v = inputs.prefill_inputs(B, H, Sq, Sk, d, torch.float16, seed=3)
     BM = fa.fa_fwd_block_m()
@@ -113,7 +113,8 @@ def test_guard_regions_untouched_and_outputs_finite():
     od = bo[G:G + q.numel()].view(q.shape)
     bl = torch.full((B * H * S + 2 * G,), float("nan"), dtype=torch.float32, device=dev)
     ld = bl[G:G + B * H * S].view(B, H, S)
-    for mode in (fa.FA_MASK_NONE, fa.FA_MASK_CAUSAL, fa.FA_MASK_CAUSAL_WINDOW):
+    for mode in (fa.FA_MASK_NONE, fa.FA_MASK_CAUSAL, fa.FA_MASK_CAUSAL_WINDOW, fa.FA_MASK_BAND,
+                 fa.FA_MASK_PREFIX_LM):
         fa.fa_fwd(qd, kd, vd, od, ld, 1 / math.sqrt(d), mode, 77, 3)
         torch.cuda.synchronize()
         assert torch.isfinite(od.float()).all() and torch.isfinite(ld).all()

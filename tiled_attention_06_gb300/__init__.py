@@ -19,12 +19,12 @@ __all__ = [
     "fa_selftest_timeout", "fa_last_error_string", "fa_version", "fa_fwd_block_m",
     "FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_CUDA", "FA_ERR_TIMEOUT",
     "FA_ERR_BAD_PAGE", "FA_F16", "FA_BF16", "FA_MASK_NONE", "FA_MASK_CAUSAL",
-    "FA_MASK_CAUSAL_WINDOW",
+    "FA_MASK_CAUSAL_WINDOW", "FA_MASK_BAND", "FA_MASK_PREFIX_LM",
 ]
 
 FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT, FA_ERR_BAD_PAGE = range(6)
 FA_F16, FA_BF16 = 0, 1
-FA_MASK_NONE, FA_MASK_CAUSAL, FA_MASK_CAUSAL_WINDOW = 0, 1, 2
+FA_MASK_NONE, FA_MASK_CAUSAL, FA_MASK_CAUSAL_WINDOW, FA_MASK_BAND, FA_MASK_PREFIX_LM = 0, 1, 2, 3, 4
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libfa.so")
 

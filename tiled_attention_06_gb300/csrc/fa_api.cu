@@ -169,10 +169,14 @@ fa_status check_fwd(const fa_fwd_params& p) {
   if (p.d != 64 && p.d != 128) return fail(FA_ERR_UNSUPPORTED, "head dim %d (supported: 64, 128)", p.d);
   if (p.dtype != FA_F16 && p.dtype != FA_BF16) return fail(FA_ERR_UNSUPPORTED, "dtype %d", p.dtype);
   if (!std::isfinite(p.scale)) return fail(FA_ERR_INVALID_ARG, "scale must be finite");
-  if (p.mask_mode < FA_MASK_NONE || p.mask_mode > FA_MASK_CAUSAL_WINDOW)
+  if (p.mask_mode < FA_MASK_NONE || p.mask_mode > FA_MASK_PREFIX_LM)
     return fail(FA_ERR_INVALID_ARG, "mask_mode %d", p.mask_mode);
   if (p.mask_mode == FA_MASK_CAUSAL_WINDOW && (p.window < 1 || p.n_global < 0))
     return fail(FA_ERR_INVALID_ARG, "CAUSAL_WINDOW needs window >= 1 and n_global >= 0");
+  if (p.mask_mode == FA_MASK_BAND && p.window < 0)
+    return fail(FA_ERR_INVALID_ARG, "BAND needs window >= 0");
+  if (p.mask_mode == FA_MASK_PREFIX_LM && p.n_global < 0)
+    return fail(FA_ERR_INVALID_ARG, "PREFIX_LM needs n_global >= 0");
   const long long BH = static_cast<long long>(p.B) * p.H;
   const long long S = p.Sq > p.Sk ? p.Sq : p.Sk;
   if (BH > (1LL << 30) || S > (1LL << 30) || BH * ((S + 63) / 64) > (1LL << 31) - 1)
@@ -230,13 +234,18 @@ fa_status run_fwd(const fa_fwd_params& a, const PagedKV* pg, fa_stream_t stream)
   p.nmb = (a.Sq + BM - 1) / BM;
   p.nnb = (a.Sk + BN - 1) / BN;
   p.mask_mode = a.mask_mode;
-  p.window = a.mask_mode == FA_MASK_CAUSAL_WINDOW ? a.window : 0;
-  p.n_global = a.mask_mode == FA_MASK_CAUSAL_WINDOW ? a.n_global : 0;
+  const bool uses_window = a.mask_mode == FA_MASK_CAUSAL_WINDOW || a.mask_mode == FA_MASK_BAND;
+  const bool uses_global = a.mask_mode == FA_MASK_CAUSAL_WINDOW || a.mask_mode == FA_MASK_PREFIX_LM;
+  p.window = uses_window ? a.window : 0;
+  p.n_global = uses_global ? a.n_global : 0;
   p.sl2 = a.scale * 1.4426950408889634f;
   // Heads scheduled together so that their K/V stays resident in L2 (~48 MiB budget).
   long long kv_keys = a.Sk;
   if (a.mask_mode == FA_MASK_CAUSAL_WINDOW) {
     const long long band = static_cast<long long>(a.window) + a.n_global + BM + BN;
+    if (band < kv_keys) kv_keys = band;
+  } else if (a.mask_mode == FA_MASK_BAND) {
+    const long long band = 2LL * a.window + BM + BN;
     if (band < kv_keys) kv_keys = band;
   }
   const long long kv_bytes = kv_keys * a.d * 4 + 1;

@@ -35,6 +35,18 @@ FA_HD Range key_range(int m0, int m1, int BN, int sk, const PrefillParams& p) {
   const int delta = sk - p.Sq;
   const int r_lo = m0 + delta;      // key position of the first row
   const int r_hi = m1 - 1 + delta;  // key position of the last row
+  if (p.mask_mode == FA_MASK_BAND) {  // keys [r_lo - w, r_hi + w], clipped to [0, sk)
+    const long long k_lo = static_cast<long long>(r_lo) - p.window;
+    const long long k_hi = static_cast<long long>(r_hi) + p.window;
+    if (k_hi < 0 || k_lo >= sk) return Range{0, 0, 0};
+    const int lo = k_lo > 0 ? static_cast<int>(k_lo) : 0;
+    const int hi = k_hi < sk - 1 ? static_cast<int>(k_hi) : sk - 1;
+    return Range{0, lo / BN, hi / BN + 1};
+  }
+  if (p.mask_mode == FA_MASK_PREFIX_LM) {  // keys [0, max(n_global, r_hi + 1)), clipped
+    const int keys = imin(sk, imax(p.n_global, r_hi + 1));
+    return keys > 0 ? Range{0, 0, (keys + BN - 1) / BN} : Range{0, 0, 0};
+  }
   if (r_hi < 0) return Range{0, 0, 0};
   r.b_end = imin(nnb, r_hi / BN + 1);
   if (p.mask_mode == FA_MASK_CAUSAL_WINDOW) {

@@ -66,6 +66,10 @@ __device__ __forceinline__ bool tile_full(int m0, int nb, int sk, const PrefillP
   if (p.mask_mode == FA_MASK_NONE) return true;
   const int delta = sk - p.Sq;
   const int r_lo = m0 + delta, r_hi = m0 + kTile - 1 + delta;
+  if (p.mask_mode == FA_MASK_BAND)  // the largest |pos - j| of the tile is within w
+    return static_cast<long long>(r_hi) - n0 <= p.window &&
+           static_cast<long long>(n1 - 1) - r_lo <= p.window;
+  if (p.mask_mode == FA_MASK_PREFIX_LM) return n1 <= p.n_global || n1 - 1 <= r_lo;
   if (n1 - 1 > r_lo) return false;
   if (p.mask_mode == FA_MASK_CAUSAL) return true;
   return n1 <= p.n_global || r_hi - max(n0, p.n_global) < p.window;
@@ -110,6 +114,13 @@ __device__ __forceinline__ bool softmax_cols(uint32_t t_lane, uint32_t s_col, ui
     if (p.mask_mode == FA_MASK_CAUSAL_WINDOW) {
       lo = pos_q - p.window + 1 - n0;
       gl = p.n_global - n0;
+    } else if (p.mask_mode == FA_MASK_BAND) {  // |pos - j| <= w, in 64 bits: w may be huge
+      const long long hi = static_cast<long long>(pos_q) + p.window;
+      lim = static_cast<int>((hi < sk - 1 ? hi : sk - 1) - n0);
+      const long long l0 = static_cast<long long>(pos_q) - p.window - n0;
+      lo = l0 < INT_MIN ? INT_MIN : static_cast<int>(l0);
+    } else if (p.mask_mode == FA_MASK_PREFIX_LM) {
+      lim = min(max(pos_q, p.n_global - 1), sk - 1) - n0;
     }
 #pragma unroll
     for (int c = 0; c < NC; ++c) {
