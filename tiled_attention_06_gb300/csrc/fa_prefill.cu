@@ -1,6 +1,6 @@
 // FlashAttention forward (prefill) for sm_103a: tcgen05 MMAs with TMEM accumulators,
 // TMA tile loads into a shared-memory ring, warp-specialised online softmax, tile
-// skipping for causal and sliding-window(+global) masks, and a persistent
+// skipping for causal, sliding-window(+global), band and prefix-LM masks, and a persistent
 // longest-first tile schedule.
 //
 // The method is the tiled loop of the ops-transformer overview (gitcode.csdn.net,
@@ -14,29 +14,29 @@
 //
 // Two kernels share the helpers in this file:
 //
-// prefill_bm256_kernel (default): a work item is 256 query rows of one (batch, head),
-// held as two 128-row tiles A and B that share every K/V tile.
-//   warps 0-3  softmax for tile A, warps 4-7 softmax for tile B: one thread per query
-//              row (= TMEM lane); S from TMEM, mask on partial tiles, m and l, P
-//              (16-bit) written back over S, lazy rescale of O, epilogue.
-//   warp 8     TMA producer: Q_A, Q_B, then K0, V0, K1, V1, ... through the ring.
-//   warp 9     MMA issuer (one thread). Tensor-pipe order:
-//                S_A(0) S_B(0) | PV_A(0) S_A(1) | PV_B(0) S_B(1) | PV_A(1) S_A(2) | ...
-//              so one tile's softmax runs while the tensor core works for the other,
-//              and S_A(j) is always issued after PV_A(j-1): once the softmax sees
-//              S_A(j) complete, O_A holds every earlier P.V product and can be
-//              rescaled without waiting.
-//   TMEM columns: S_A [0,BN), S_B [BN,2BN), O_A [2BN,2BN+D), O_B [2BN+D,2BN+2D).
+// prefill_bm128_kernel (default): a work item is 128 query rows of one (batch, head).
+//   warps 0-7   softmax: two warpgroups, each owning half of every score row (TMEM lane =
+//               row); partial row maxima are swapped through shared memory; P (16-bit)
+//               overwrites S in TMEM; lazy rescale of O.
+//   warps 8-11  epilogue: O / l and LSE of the previous item from the second O buffer.
+//   warp 12     TMA producer: Q (double buffered), then K(0), and per tile K(t+1), V(t)
+//               through a ring of shared-memory slots.
+//   warp 13     MMA issuer (one thread): S(t+1) = Q K(t+1)^T, then O += P(t) V(t).
+//   TMEM columns: S0 [0,BN), S1 [BN,2BN), O0 [2BN,2BN+D), O1 [2BN+D,2BN+2D).
 //
-// prefill_bm128_kernel: one 128-row tile per item, two S buffers so that S(j+1) is
-// computed while the softmax works on S(j); warps 0-3 softmax, 4 TMA, 5 MMA.
-//   TMEM columns: S0 [0,BN), S1 [BN,2BN), O [2BN,2BN+D).
+// prefill_bm256_kernel: a work item is 256 query rows held as two 128-row tiles A and B
+// that share every K/V tile; one softmax warpgroup per tile (a whole row per thread,
+// which also writes the epilogue), a TMA warp and an MMA warp. Tensor-pipe order
+//   S_A(0) S_B(0) | PV_A(0) S_A(1) | PV_B(0) S_B(1) | ...
+// so that one tile's softmax runs while the tensor core works for the other.
+//   TMEM columns: S_A [0,BN), S_B [BN,2BN), O_A [2BN,2BN+D), O_B [2BN+D,2BN+2D).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
 #include <climits>
 #include <cstdint>
+#include <type_traits>
 
 #include "fa_internal.h"
 #include "fa_plan.h"
@@ -47,6 +47,12 @@ namespace {
 
 constexpr int kTile = 128;                // rows of one tcgen05 M=128 tile (= TMEM lanes)
 constexpr float kTau = 8.0f;              // lazy-rescale threshold, log2 units
+#ifndef FA_EXP2_POLY_PAIRS
+#define FA_EXP2_POLY_PAIRS 0
+#endif
+// of every 8 exponential pairs on a full tile, how many use the polynomial exponential
+constexpr int kExp2Poly = FA_EXP2_POLY_PAIRS;
+static_assert(kExp2Poly >= 0 && kExp2Poly <= 8, "pairs out of 8");
 constexpr uint32_t kSmemLimit = 232448;   // 227 KB opt-in dynamic shared memory per CTA
 
 constexpr int pow2_at_least(int x) {
@@ -92,7 +98,7 @@ __device__ __forceinline__ uint32_t pack2(float a, float b, bool bf16) {
 // decision; `before_rescale` makes O safe to touch and returns false on abort); and
 // P = 2^(S*sl2 - m) is written as packed 16-bit pairs to NC/2 columns at p_col.
 // l accumulates the sum over this thread's NC columns. Returns false on abort.
-template <int NC, int ON, bool BF16, typename Exchange, typename PreRescale>
+template <int NC, int ON, bool BF16, int POLY, typename Exchange, typename PreRescale>
 __device__ __forceinline__ bool softmax_cols(uint32_t t_lane, uint32_t s_col, uint32_t p_col,
                                              uint32_t o_col, bool full, int n0, int pos_q,
                                              int sk, const PrefillParams& p, float& m_ref,
@@ -159,19 +165,38 @@ __device__ __forceinline__ bool softmax_cols(uint32_t t_lane, uint32_t s_col, ui
       tmem_st32(t_lane + o_col + c * 32, ov);
     }
   }
-  // P = 2^(S*sl2 - m): the exponent argument two lanes at a time, one ex2 per element,
-  // the row sum in four packed pairs.
+  // P = 2^(S*sl2 - m): the exponent argument two lanes at a time, one exponential per
+  // element, the row sum in four packed pairs. On full tiles (every S finite) POLY of
+  // every 8 pairs take the polynomial exponential, which runs on the FMA pipe, so that the
+  // MUFU unit (16 exponentials per clock per SM, as many cycles per 128x128 tile as its
+  // MMAs) is no longer the limit. Masked (-inf) entries always take ex2, which gives 0.
   const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
   const uint64_t scale2 = f2(p.sl2, p.sl2), neg_m2 = f2(-m_use, -m_use);
   uint64_t acc[4] = {0, 0, 0, 0};
+  auto exp_pairs = [&](auto use_poly) {
 #pragma unroll
-  for (int c = 0; c < NC; c += 2) {
-    const uint64_t x = f2_fma(f2(__uint_as_float(s[c]), __uint_as_float(s[c + 1])), scale2, neg_m2);
-    float x0, x1;
-    f2_split(x, x0, x1);
-    const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-    acc[(c / 2) & 3] = f2_add(acc[(c / 2) & 3], f2(p0, p1));
-    s[c / 2] = BF16 ? cvt_pack_bf16(p0, p1) : cvt_pack_f16(p0, p1);
+    for (int c = 0; c < NC; c += 2) {
+      const uint64_t x =
+          f2_fma(f2(__uint_as_float(s[c]), __uint_as_float(s[c + 1])), scale2, neg_m2);
+      float x0, x1, p0, p1;
+      f2_split(x, x0, x1);
+      if (decltype(use_poly)::value && ((c / 2) & 7) >= 8 - POLY) {
+        exp2_poly_x2(x0, x1, p0, p1);
+      } else {
+        p0 = ex2_approx(x0);
+        p1 = ex2_approx(x1);
+      }
+      acc[(c / 2) & 3] = f2_add(acc[(c / 2) & 3], f2(p0, p1));
+      s[c / 2] = BF16 ? cvt_pack_bf16(p0, p1) : cvt_pack_f16(p0, p1);
+    }
+  };
+  if constexpr (POLY > 0) {
+    if (full)
+      exp_pairs(std::true_type{});
+    else
+      exp_pairs(std::false_type{});
+  } else {
+    exp_pairs(std::false_type{});
   }
   float a0, a1;
   f2_split(f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3])), a0, a1);
@@ -192,7 +217,8 @@ __device__ __forceinline__ bool softmax_tile(uint32_t t_lane, uint32_t s_col, ui
                                              bool full, int n0, int pos_q,
                                              const PrefillParams& p, float& m_ref, float& l,
                                              PreRescale before_rescale) {
-  return softmax_cols<BN, D, BF16>(t_lane, s_col, s_col, o_col, full, n0, pos_q, p.Sk, p, m_ref,
+  // (a whole row of S in registers leaves no room for the polynomial's temporaries)
+  return softmax_cols<BN, D, BF16, 0>(t_lane, s_col, s_col, o_col, full, n0, pos_q, p.Sk, p, m_ref,
                                    l, [](float m) { return m; }, before_rescale);
 }
 
@@ -588,6 +614,7 @@ struct Cfg128 {
   static constexpr int NSLOT_FIT = (int)((kSmemLimit - 1024 - BAR_BYTES - STATS_BYTES -
                                           XMAX_BYTES - 2 * Q_BYTES) / TILE_BYTES);
   static constexpr int NSLOT = NSLOT_FIT > 8 ? 8 : NSLOT_FIT;
+  static constexpr bool kRelease = NSLOT == 4;  // slots released by s_full / pv_done
   static constexpr int SMEM =
       1024 + 2 * Q_BYTES + NSLOT * TILE_BYTES + STATS_BYTES + XMAX_BYTES + BAR_BYTES;
   static constexpr int TMEM_COLS = pow2_at_least(2 * BN + 2 * D);
@@ -708,6 +735,16 @@ __global__ void __launch_bounds__(kThreads128, 1)
       uint32_t pos = 0, ii = 0;
       uint32_t fills[8] = {0, 0, 0, 0, 0, 0, 0, 0};
       uint32_t qfills[2] = {0, 0};
+      // With a four-slot ring (two tiles) a slot is free again once the MMA that read
+      // its previous tile is complete: S(t) (s_full[t&1]) for K(t), P.V(t) (pv_done[t&1])
+      // for V(t), so the MMA issuer needs no per-slot commits. No barrier can be two
+      // phases ahead of such a wait, because the next MMA on it needs the tile about to
+      // be loaded. The one exception is the first reuse (V(1) into the slot of K(0)),
+      // which waits for S(1) instead (a commit covers every earlier MMA, and S(3) needs
+      // K(3)). A deeper ring reuses slots more than two tiles later, where a parity wait
+      // on those barriers would be ambiguous: it keeps one `empty` barrier per slot.
+      uint32_t rel_bar[C::NSLOT] = {}, rel_par[C::NSLOT] = {};
+      uint32_t nk = 0, nv = 0;  // K and V tiles loaded so far
       bool ok = true;
       int kc = 0;
       ItemRef cur, nxt;
@@ -723,8 +760,21 @@ __global__ void __launch_bounds__(kThreads128, 1)
       };
       auto emit = [&](const ItemRef& it, int j, bool is_v) {
         const int slot = pos % C::NSLOT;
-        const uint32_t use = pos / C::NSLOT;
-        if (!(ok = mbar_wait(B(bars->empty[slot]), (use & 1) ^ 1, wc))) return;
+        if constexpr (!C::kRelease) {
+          if (!(ok = mbar_wait(B(bars->empty[slot]), ((pos / C::NSLOT) & 1) ^ 1, wc))) return;
+        } else if (pos >= C::NSLOT && !(ok = mbar_wait(rel_bar[slot], rel_par[slot], wc))) {
+          return;
+        }
+        if (is_v) {
+          rel_bar[slot] = B(bars->pv_done[nv & 1]);
+          rel_par[slot] = (nv >> 1) & 1;
+          ++nv;
+        } else {
+          const uint32_t t = nk == 0 ? 1 : nk;  // K(0): released by S(1), see above
+          rel_bar[slot] = B(bars->s_full[t & 1]);
+          rel_par[slot] = (t >> 1) & 1;
+          ++nk;
+        }
         const uint32_t dst = sRing + slot * C::TILE_BYTES;
         mbar_arrive_expect_tx(B(bars->full[slot]), C::TILE_BYTES);
         const int n0 = range_nb(it.rg, j) * BN;
@@ -742,7 +792,7 @@ __global__ void __launch_bounds__(kThreads128, 1)
         const void* map = is_v ? (const void*)&tmV : (const void*)&tmK;
         for (int c = 0; c < C::KCH; ++c)
           tma_load_3d(dst + c * (BN * 128), map, B(bars->full[slot]), c * 64, y, z);
-        fills[slot] = use + 1;
+        fills[slot] = pos / C::NSLOT + 1;  // uses of this slot so far
         ++pos;
       };
       bool has = next_item<BM>(sched, p, cta, G, BN, kc, cur, false);
@@ -786,7 +836,7 @@ __global__ void __launch_bounds__(kThreads128, 1)
         tc_fence_after();
         issue_qk<D, BN, BF16>(tmem + sbuf * BN, sQ + qb * C::Q_BYTES, sRing + slot * C::TILE_BYTES);
         umma_commit(B(bars->s_full[sbuf]));
-        umma_commit(B(bars->empty[slot]));
+        if constexpr (!C::kRelease) umma_commit(B(bars->empty[slot]));
         ++pos;
       };
       bool has = next_item<BM>(sched, p, cta, G, BN, kc, cur, false);
@@ -829,7 +879,7 @@ __global__ void __launch_bounds__(kThreads128, 1)
           issue_pv<D, BN, BF16>(tmem + 2 * BN + buf * D, tmem + (g & 1) * BN,
                                 sRing + slot * C::TILE_BYTES, j > 0);
           umma_commit(B(bars->pv_done[g & 1]));
-          umma_commit(B(bars->empty[slot]));
+          if constexpr (!C::kRelease) umma_commit(B(bars->empty[slot]));
           ++pos;
           if (j + 1 == cur.n) umma_commit(B(bars->o_full[buf]));
         }
@@ -926,7 +976,7 @@ __global__ void __launch_bounds__(kThreads128, 1)
           return w;
         };
         const uint32_t s_col = (g & 1) * BN;
-        ok = softmax_cols<BN / 2, D / 2, BF16>(t_lane, s_col + half * (BN / 2),
+        ok = softmax_cols<BN / 2, D / 2, BF16, kExp2Poly>(t_lane, s_col + half * (BN / 2),
                                                s_col + half * (BN / 4),
                                                2 * BN + buf * D + half * (D / 2), full,
                                                nb * BN + half * (BN / 2), pos_q, it.sk, p, m_ref,
