@@ -728,8 +728,9 @@ __global__ void __launch_bounds__(kThreads128, 1)
   // The role branches never rejoin: each ends with the CTA-wide teardown barrier.
   if (warp >= 12) {
     regs_decrease<kRegs128Producer>();
-    if (warp == kTmaWarp128 && lane == 0) {
+    if (warp == kTmaWarp128) {
       // ---------------------------------------------------------- TMA producer
+      const bool leader = elect_one();
       // Loads in the MMA's consumption order: Q and K(0) of the first item, then per
       // tile: K of the following tile (the next item's Q first when it starts one), V.
       uint32_t pos = 0, ii = 0;
@@ -752,10 +753,12 @@ __global__ void __launch_bounds__(kThreads128, 1)
         const int qb = idx & 1;
         if (idx >= 2 && !(ok = mbar_wait(B(bars->q_empty[qb]), ((idx >> 1) - 1) & 1, wc)))
           return;
-        mbar_arrive_expect_tx(B(bars->q_full[qb]), C::Q_BYTES);
-        for (int c = 0; c < C::KCH; ++c)
-          tma_load_3d(sQ + qb * C::Q_BYTES + c * (kTile * 128), &tmQ, B(bars->q_full[qb]), c * 64,
-                      it.mb * BM, it.bh);
+        if (leader) {
+          mbar_arrive_expect_tx(B(bars->q_full[qb]), C::Q_BYTES);
+          for (int c = 0; c < C::KCH; ++c)
+            tma_load_3d(sQ + qb * C::Q_BYTES + c * (kTile * 128), &tmQ, B(bars->q_full[qb]),
+                        c * 64, it.mb * BM, it.bh);
+        }
         qfills[qb] = (idx >> 1) + 1;
       };
       auto emit = [&](const ItemRef& it, int j, bool is_v) {
@@ -776,22 +779,23 @@ __global__ void __launch_bounds__(kThreads128, 1)
           ++nk;
         }
         const uint32_t dst = sRing + slot * C::TILE_BYTES;
-        mbar_arrive_expect_tx(B(bars->full[slot]), C::TILE_BYTES);
+        if (leader) mbar_arrive_expect_tx(B(bars->full[slot]), C::TILE_BYTES);
         const int n0 = range_nb(it.rg, j) * BN;
         int y = n0, z = it.bh;
         if (p.block_table) {  // the tile's rows lie in one page: (page, offset) of key n0
           const int b = it.bh / p.H, lp = n0 / p.page_size;
           int phys = p.block_table[static_cast<size_t>(b) * p.max_pages + lp];
           if (phys < 0 || phys >= p.num_pages) {  // skip the bad page: load page 0, report
-            atomicOr(p.status, FA_DEV_BAD_PAGE);
+            if (leader) atomicOr(p.status, FA_DEV_BAD_PAGE);
             phys = 0;
           }
           y = n0 - lp * p.page_size;
           z = phys * p.H + (it.bh - b * p.H);
         }
         const void* map = is_v ? (const void*)&tmV : (const void*)&tmK;
-        for (int c = 0; c < C::KCH; ++c)
-          tma_load_3d(dst + c * (BN * 128), map, B(bars->full[slot]), c * 64, y, z);
+        if (leader)
+          for (int c = 0; c < C::KCH; ++c)
+            tma_load_3d(dst + c * (BN * 128), map, B(bars->full[slot]), c * 64, y, z);
         fills[slot] = pos / C::NSLOT + 1;  // uses of this slot so far
         ++pos;
       };
@@ -824,8 +828,14 @@ __global__ void __launch_bounds__(kThreads128, 1)
         for (int q = 0; q < 2; ++q)
           if (qfills[q] > 0) wait_quiet(B(bars->q_full[q]), (qfills[q] - 1) & 1, wc);
       }
-    } else if (warp == kMmaWarp128 && lane == 0) {
+    } else if (warp == kMmaWarp128) {
       // ---------------------------------------------------------- MMA issuer
+      // The whole warp runs the loop and the waits; one elected lane issues the MMAs and
+      // the commits that track them (a commit covers the MMAs of the thread issuing it).
+      const bool leader = elect_one();
+      auto commit = [&](uint64_t& bar) {
+        if (leader) umma_commit(B(bar));
+      };
       uint32_t pos = 0, ii = 0, g = 0;
       bool ok = true;
       int kc = 0;
@@ -834,9 +844,12 @@ __global__ void __launch_bounds__(kThreads128, 1)
         const int slot = pos % C::NSLOT;
         if (!(ok = mbar_wait(B(bars->full[slot]), (pos / C::NSLOT) & 1, wc))) return;
         tc_fence_after();
-        issue_qk<D, BN, BF16>(tmem + sbuf * BN, sQ + qb * C::Q_BYTES, sRing + slot * C::TILE_BYTES);
-        umma_commit(B(bars->s_full[sbuf]));
-        if constexpr (!C::kRelease) umma_commit(B(bars->empty[slot]));
+        if (leader) {
+          issue_qk<D, BN, BF16>(tmem + sbuf * BN, sQ + qb * C::Q_BYTES,
+                                sRing + slot * C::TILE_BYTES);
+          umma_commit(B(bars->s_full[sbuf]));
+          if constexpr (!C::kRelease) umma_commit(B(bars->empty[slot]));
+        }
         ++pos;
       };
       bool has = next_item<BM>(sched, p, cta, G, BN, kc, cur, false);
@@ -844,7 +857,7 @@ __global__ void __launch_bounds__(kThreads128, 1)
         if ((ok = mbar_wait(B(bars->q_full[0]), 0, wc))) {
           tc_fence_after();
           issue_s(0, 0);
-          if (ok && cur.n == 1) umma_commit(B(bars->q_empty[0]));
+          if (ok && cur.n == 1) commit(bars->q_empty[0]);
         }
       }
       while (has && ok) {
@@ -854,7 +867,7 @@ __global__ void __launch_bounds__(kThreads128, 1)
           // score tile of the following tile, into the other S buffer
           if (j + 1 < cur.n) {
             issue_s((g + 1) & 1, buf);
-            if (ok && j + 2 == cur.n) umma_commit(B(bars->q_empty[buf]));
+            if (ok && j + 2 == cur.n) commit(bars->q_empty[buf]);
           } else {
             has_nxt = next_item<BM>(sched, p, cta, G, BN, kc, nxt, false);
             if (has_nxt) {
@@ -862,7 +875,7 @@ __global__ void __launch_bounds__(kThreads128, 1)
               if (!(ok = mbar_wait(B(bars->q_full[nb]), ((ii + 1) >> 1) & 1, wc))) break;
               tc_fence_after();
               issue_s((g + 1) & 1, nb);
-              if (ok && nxt.n == 1) umma_commit(B(bars->q_empty[nb]));
+              if (ok && nxt.n == 1) commit(bars->q_empty[nb]);
             }
           }
           if (!ok) break;
@@ -876,18 +889,20 @@ __global__ void __launch_bounds__(kThreads128, 1)
           const int slot = pos % C::NSLOT;
           if (!(ok = mbar_wait(B(bars->full[slot]), (pos / C::NSLOT) & 1, wc))) break;
           tc_fence_after();
-          issue_pv<D, BN, BF16>(tmem + 2 * BN + buf * D, tmem + (g & 1) * BN,
-                                sRing + slot * C::TILE_BYTES, j > 0);
-          umma_commit(B(bars->pv_done[g & 1]));
-          if constexpr (!C::kRelease) umma_commit(B(bars->empty[slot]));
+          if (leader) {
+            issue_pv<D, BN, BF16>(tmem + 2 * BN + buf * D, tmem + (g & 1) * BN,
+                                  sRing + slot * C::TILE_BYTES, j > 0);
+            umma_commit(B(bars->pv_done[g & 1]));
+            if constexpr (!C::kRelease) umma_commit(B(bars->empty[slot]));
+            if (j + 1 == cur.n) umma_commit(B(bars->o_full[buf]));
+          }
           ++pos;
-          if (j + 1 == cur.n) umma_commit(B(bars->o_full[buf]));
         }
         ++ii;
         cur = nxt;
         has = has_nxt;
       }
-      umma_commit(B(bars->final_mma));  // all MMAs done before TMEM is released
+      if (leader) umma_commit(B(bars->final_mma));  // all MMAs done before TMEM is released
       wait_quiet(B(bars->final_mma), 0, wc);
     }
     __syncwarp();

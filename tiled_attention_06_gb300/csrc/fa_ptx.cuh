@@ -81,6 +81,17 @@ static __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, 
   }
 }
 
+// True in exactly one lane of the (converged) warp. Roles that issue tcgen05 work run the
+// whole warp through their loop and let the elected lane issue: the loop's values then
+// stay warp-uniform, which makes each issue far cheaper than from a lone divergent lane.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t e;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(e));
+  return e != 0;
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const void* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
