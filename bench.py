@@ -57,12 +57,13 @@ MODE_NAME = {0: "none", 1: "causal", 2: "causal_window", 3: "band", 4: "prefix_l
 # capture of each kernel, with the SHA-256 of the kernel sources it was taken on; the
 # figure is reported only while those sources are unchanged. Summaries: profiles/.
 NCU_TRAFFIC = {
-    # causal 4k B4 H16 capture: 205.2 MB read + 47.8 MB written, scaled x2 to B4 H32
-    "prefill": {"bytes": 506.1e6, "sources": ['fa_prefill.cu', 'fa_ptx.cuh', 'fa_plan.h', 'fa_internal.h'],
-                "sha256": "304d6733acbbe0c8ae027f3792dcbcae599d972eabfc8871bf7fef618d1bd5fe"},
+    # prefill_bm256_kernel, causal 4k B4 H16 capture: 210.0 MB read + 45.2 MB written,
+    # scaled x2 to B4 H32
+    "prefill": {"bytes": 510.4e6, "sources": ['fa_prefill.cu', 'fa_ptx.cuh', 'fa_plan.h', 'fa_internal.h'],
+                "sha256": "ebd61437eeb257d160c5aafba635f1a244d401713ce0cf28c75b8efa4a3442c1"},
     # paged decode B8 capture: 551.7 MB for 547.5 MB algorithmic, scaled to 2410.7 MB
     "decode": {"bytes": 2.4291e9, "sources": ['fa_decode.cu', 'fa_ptx.cuh', 'fa_internal.h'],
-               "sha256": "aa077b8c828bb7b55ef689b682b38da17331a89330bf7f61610628865b9f6cc6"},
+               "sha256": "94ab1a109d1f1e044ba6420afb1d0675b650cff976eaee5dc6f6c8bf144f74d6"},
 }
 
 
@@ -334,7 +335,7 @@ def run_ours(args, rank, world):
                               "(% of 8 TB/s)",
                     "value": value, "unit": "TFLOP/s", "higher_is_better": True,
                     "dtype": pcfg["dtype"]})
-        bm = args.block_m or fa.fa_fwd_block_m()
+        bm = args.block_m or fa.fa_fwd_default_block_m(pcfg["mode"])
         res["roofline"] = {"kernel": f"prefill_bm{bm}_kernel<{pcfg['d']},128,{pcfg['dtype']}>",
                            "bound": "tensor",
                            "achieved": achieved, "peak": tc_peak, "unit": "TFLOP/s",

@@ -104,8 +104,8 @@ typedef struct fa_fwd_params {
   float scale;
   int mask_mode, window, n_global, dtype;
   int block_n;        /* key-block size: 0 = default (128), else 64 or 128 */
-  int block_m;        /* query rows per work item: 0 = default (128), or 256 (two
-                         128-row tiles sharing every K/V tile) */
+  int block_m;        /* query rows per work item: 0 = fa_fwd_default_block_m(mask_mode),
+                         else 128 or 256 (two 128-row tiles sharing every K/V tile) */
   int num_ctas;       /* persistent grid size: 0 = one CTA per SM */
   int group_heads;    /* (batch, head) pairs scheduled together: 0 = sized for L2 */
   uint32_t timeout_us; /* per-wait time limit: 0 = 1 s */
@@ -120,6 +120,11 @@ fa_status fa_fwd_ex(const fa_fwd_params* params, fa_stream_t stream);
 
 /* Query rows per tensor-core tile (128): the row granularity of the fa_fwd_ex trace. */
 int fa_fwd_block_m(void);
+
+/* Query rows per work item that fa_fwd (and fa_fwd_ex with block_m = 0) uses for a mask:
+ * 256 (two 128-row tiles sharing every K/V tile) except for FA_MASK_BAND, whose narrow
+ * key ranges favour 128. fa_fwd_paged always uses 128. Returns 0 for an unknown mask. */
+int fa_fwd_default_block_m(int mask_mode);
 
 /*
  * fa_decode_paged - one query token per sequence against a paged KV cache

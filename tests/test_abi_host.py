@@ -64,6 +64,8 @@ def test_struct_layouts_match_header(tmp_path):
 def test_version_and_block_m(L):
     assert L.fa_version() >= 100
     assert L.fa_fwd_block_m() == 128
+    assert [L.fa_fwd_default_block_m(m) for m in range(5)] == [256, 256, 256, 128, 256]
+    assert L.fa_fwd_default_block_m(5) == 0 and L.fa_fwd_default_block_m(-1) == 0
 
 
 def test_workspace_size_and_split_rule(L):

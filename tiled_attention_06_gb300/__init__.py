@@ -17,6 +17,7 @@ __all__ = [
     "fa_decode_workspace_size", "fa_decode_default_pages_per_split",
     "fa_get_device_status",
     "fa_selftest_timeout", "fa_last_error_string", "fa_version", "fa_fwd_block_m",
+    "fa_fwd_default_block_m",
     "FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_CUDA", "FA_ERR_TIMEOUT",
     "FA_ERR_BAD_PAGE", "FA_F16", "FA_BF16", "FA_MASK_NONE", "FA_MASK_CAUSAL",
     "FA_MASK_CAUSAL_WINDOW", "FA_MASK_BAND", "FA_MASK_PREFIX_LM",
@@ -75,6 +76,8 @@ def lib():
         L.fa_fwd_ex.argtypes = [ctypes.POINTER(FwdParams), _vp]
         L.fa_fwd_block_m.restype = _i
         L.fa_fwd_block_m.argtypes = []
+        L.fa_fwd_default_block_m.restype = _i
+        L.fa_fwd_default_block_m.argtypes = [_i]
         L.fa_decode_paged.restype = _i
         L.fa_decode_paged.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i,
                                       _f, _i, _vp, _sz, _vp]
@@ -152,6 +155,10 @@ def fa_version():
 
 def fa_fwd_block_m():
     return lib().fa_fwd_block_m()
+
+
+def fa_fwd_default_block_m(mask_mode):
+    return lib().fa_fwd_default_block_m(mask_mode)
 
 
 def fa_fwd(q, k, v, o, lse, scale, mask_mode=FA_MASK_NONE, window=0, n_global=0, stream=None):

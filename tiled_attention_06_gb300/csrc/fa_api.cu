@@ -199,6 +199,11 @@ const char* fa_last_error_string(void) { return t_last_error.c_str(); }
 
 int fa_fwd_block_m(void) { return fa::prefill_tile_rows(); }
 
+int fa_fwd_default_block_m(int mask_mode) {
+  if (mask_mode < FA_MASK_NONE || mask_mode > FA_MASK_PREFIX_LM) return 0;
+  return mask_mode == FA_MASK_BAND ? 128 : 256;
+}
+
 }  // extern "C"
 
 namespace {
@@ -220,7 +225,7 @@ fa_status run_fwd(const fa_fwd_params& a, const PagedKV* pg, fa_stream_t stream)
   DeviceInfo dev;
   if ((st = device_info(&dev)) != FA_OK) return st;
 
-  const int BM = a.block_m ? a.block_m : 128;
+  const int BM = a.block_m ? a.block_m : fa_fwd_default_block_m(a.mask_mode);
   const int BN = a.block_n ? a.block_n : 128;
   const int BH = a.B * a.H;
   fa::PrefillLaunch L;

@@ -401,7 +401,8 @@ __global__ void __launch_bounds__(kThreads256, 1)
     regs_decrease<kRegsProducer>();
     if (warp == kTmaWarp256) {
     // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
+    {
+      const bool leader = elect_one();
       uint32_t pos = 0, ii = 0;
       uint32_t fills[8] = {0, 0, 0, 0, 0, 0, 0, 0};
       uint32_t qfills[2] = {0, 0};
@@ -416,8 +417,8 @@ __global__ void __launch_bounds__(kThreads256, 1)
         if (n == 0) continue;
         for (int q = 0; q < 2 && ok; ++q) {
           if (ii > 0 && !(ok = mbar_wait(B(bars->q_empty[q]), (ii - 1) & 1, wc))) break;
-          mbar_arrive_expect_tx(B(bars->q_full[q]), C::QT_BYTES);
-          for (int c = 0; c < C::KCH; ++c)
+          if (leader) mbar_arrive_expect_tx(B(bars->q_full[q]), C::QT_BYTES);
+          if (leader) for (int c = 0; c < C::KCH; ++c)
             tma_load_3d(sQ + q * C::QT_BYTES + c * (kTile * 128), &tmQ, B(bars->q_full[q]),
                         c * 64, mb * BM + q * kTile, bh);
           qfills[q] = ii + 1;
@@ -427,10 +428,10 @@ __global__ void __launch_bounds__(kThreads256, 1)
           const uint32_t use = pos / C::NSLOT;
           if (!(ok = mbar_wait(B(bars->empty[slot]), (use & 1) ^ 1, wc))) break;
           const uint32_t dst = sRing + slot * C::TILE_BYTES;
-          mbar_arrive_expect_tx(B(bars->full[slot]), C::TILE_BYTES);
+          if (leader) mbar_arrive_expect_tx(B(bars->full[slot]), C::TILE_BYTES);
           const int n0 = range_nb(rg, s / 2) * BN;
           const void* map = (s & 1) ? (const void*)&tmV : (const void*)&tmK;
-          for (int c = 0; c < C::KCH; ++c)
+          if (leader) for (int c = 0; c < C::KCH; ++c)
             tma_load_3d(dst + c * (BN * 128), map, B(bars->full[slot]), c * 64, n0, bh);
           fills[slot] = use + 1;
           ++pos;
@@ -447,7 +448,8 @@ __global__ void __launch_bounds__(kThreads256, 1)
     __syncwarp();
     } else if (warp == kMmaWarp256) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    {
+      const bool leader = elect_one();
       const uint32_t tS[2] = {tmem, tmem + BN};
       const uint32_t tO[2] = {tmem + 2 * BN, tmem + 2 * BN + D};
       uint32_t pos = 0, ii = 0, tc = 0;
@@ -466,12 +468,13 @@ __global__ void __launch_bounds__(kThreads256, 1)
           for (int q = 0; q < 2 && ok; ++q) {
             if (!(ok = mbar_wait(B(bars->q_full[q]), ii & 1, wc))) break;
             tc_fence_after();
-            issue_qk<D, BN, BF16>(tS[q], sQ + q * C::QT_BYTES, sRing + slot * C::TILE_BYTES);
-            umma_commit(B(bars->s_full[q]));
-            if (n == 1) umma_commit(B(bars->q_empty[q]));
+            if (leader)
+              issue_qk<D, BN, BF16>(tS[q], sQ + q * C::QT_BYTES, sRing + slot * C::TILE_BYTES);
+            if (leader) umma_commit(B(bars->s_full[q]));
+            if (leader && n == 1) umma_commit(B(bars->q_empty[q]));
           }
           if (!ok) break;
-          umma_commit(B(bars->empty[slot]));
+          if (leader) umma_commit(B(bars->empty[slot]));
           ++pos;
         }
         for (int j = 0; j < n && ok; ++j) {
@@ -486,18 +489,21 @@ __global__ void __launch_bounds__(kThreads256, 1)
               if (!(ok = mbar_wait(B(bars->o_empty[q]), (ii - 1) & 1, wc))) break;
               tc_fence_after();
             }
-            issue_pv<D, BN, BF16>(tO[q], tS[q], sRing + vslot * C::TILE_BYTES, j > 0);
-            if (j == n - 1) umma_commit(B(bars->pv_done[q]));
-            if (q == 1) umma_commit(B(bars->empty[vslot]));
+            if (leader)
+              issue_pv<D, BN, BF16>(tO[q], tS[q], sRing + vslot * C::TILE_BYTES, j > 0);
+            if (leader && j == n - 1) umma_commit(B(bars->pv_done[q]));
+            if (leader && q == 1) umma_commit(B(bars->empty[vslot]));
             if (j + 1 < n) {  // S(j+1) overwrites P(j) only after PV(j) in the pipe
               if (q == 0) {
                 if (!(ok = mbar_wait(B(bars->full[kslot]), ((pos + 1) / C::NSLOT) & 1, wc))) break;
                 tc_fence_after();
               }
-              issue_qk<D, BN, BF16>(tS[q], sQ + q * C::QT_BYTES, sRing + kslot * C::TILE_BYTES);
-              umma_commit(B(bars->s_full[q]));
-              if (j + 2 == n) umma_commit(B(bars->q_empty[q]));
-              if (q == 1) umma_commit(B(bars->empty[kslot]));
+              if (leader)
+                issue_qk<D, BN, BF16>(tS[q], sQ + q * C::QT_BYTES,
+                                      sRing + kslot * C::TILE_BYTES);
+              if (leader) umma_commit(B(bars->s_full[q]));
+              if (leader && j + 2 == n) umma_commit(B(bars->q_empty[q]));
+              if (leader && q == 1) umma_commit(B(bars->empty[kslot]));
             }
           }
           pos += (j + 1 < n) ? 2 : 1;
@@ -505,7 +511,7 @@ __global__ void __launch_bounds__(kThreads256, 1)
         }
         ++ii;
       }
-      umma_commit(B(bars->final_mma));  // all MMAs done before TMEM is released
+      if (leader) umma_commit(B(bars->final_mma));  // all MMAs done before TMEM is released
       wait_quiet(B(bars->final_mma), 0, wc);
     }
     __syncwarp();
