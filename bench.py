@@ -636,7 +636,8 @@ def run_next_rows(args, fa, workload, peaks, peak_kind, stream, world):
         res.update({"metric": "multimodal attention layer TFLOP/s (three-call split + merge)",
                     "value": val, "unit": "TFLOP/s", "dtype": c["dtype"],
                     "ms_per_step": total_ms / K, "gpu_launches": 4 * K,
-                    "roofline": {"kernel": "prefill_bm128_kernel x3 + merge", "bound": "tensor",
+                    "roofline": {"kernel": "prefill_bm256_kernel x3 + merge_kernel",
+                                 "bound": "tensor",
                                  "achieved": val, "peak": tc_peak, "unit": "TFLOP/s",
                                  "frac": val / tc_peak, "traffic": None,
                                  "algorithmic_flops": flops},
