@@ -61,8 +61,9 @@ NCU_TRAFFIC = {
     # scaled x2 to B4 H32
     "prefill": {"bytes": 510.4e6, "sources": ['fa_prefill.cu', 'fa_ptx.cuh', 'fa_plan.h', 'fa_internal.h'],
                 "sha256": "ebd61437eeb257d160c5aafba635f1a244d401713ce0cf28c75b8efa4a3442c1"},
-    # paged decode B8 capture: 551.7 MB for 547.5 MB algorithmic, scaled to 2410.7 MB
-    "decode": {"bytes": 2.4291e9, "sources": ['fa_decode.cu', 'fa_ptx.cuh', 'fa_internal.h'],
+    # paged decode B8 capture: 547.5 MB read + 3.7 MB written for 547.5 MB algorithmic,
+    # scaled to the bench call's 2410.7 MB algorithmic
+    "decode": {"bytes": 2.4268e9, "sources": ['fa_decode.cu', 'fa_ptx.cuh', 'fa_internal.h'],
                "sha256": "94ab1a109d1f1e044ba6420afb1d0675b650cff976eaee5dc6f6c8bf144f74d6"},
 }
 
@@ -597,7 +598,9 @@ def run_next_rows(args, fa, workload, peaks, peak_kind, stream, world):
         res.update({"metric": "chunked prefill through a paged KV cache TFLOP/s",
                     "value": pf, "unit": "TFLOP/s", "dtype": c["dtype"],
                     "ms_per_step": (ms[0] + ms[1]) / K, "gpu_launches": 2 * K,
-                    "roofline": {"kernel": "prefill_bm128_kernel (paged)", "bound": "tensor",
+                    "roofline": {"kernel": "prefill_bm%d_kernel (paged)"
+                                           % fa.fa_fwd_default_block_m(fa.FA_MASK_CAUSAL),
+                                 "bound": "tensor",
                                  "achieved": pf, "peak": tc_peak, "unit": "TFLOP/s",
                                  "frac": pf / tc_peak, "traffic": None,
                                  "algorithmic_flops": flops},

@@ -123,7 +123,7 @@ int fa_fwd_block_m(void);
 
 /* Query rows per work item that fa_fwd (and fa_fwd_ex with block_m = 0) uses for a mask:
  * 256 (two 128-row tiles sharing every K/V tile) except for FA_MASK_BAND, whose narrow
- * key ranges favour 128. fa_fwd_paged always uses 128. Returns 0 for an unknown mask. */
+ * key ranges favour 128. fa_fwd_paged uses the same choice. Returns 0 for an unknown mask. */
 int fa_fwd_default_block_m(int mask_mode);
 
 /*

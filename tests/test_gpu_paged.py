@@ -87,7 +87,8 @@ def test_append_writes_rows_and_zero_tails_bit_exact():
 @pytest.mark.parametrize("page,d,dt", [(64, 64, torch.float16), (128, 128, torch.bfloat16),
                                        (256, 128, torch.float16)])
 @pytest.mark.parametrize("mode,w,g", [(fa.FA_MASK_CAUSAL, 0, 0), (fa.FA_MASK_NONE, 0, 0),
-                                      (fa.FA_MASK_CAUSAL_WINDOW, 300, 16)])
+                                      (fa.FA_MASK_CAUSAL_WINDOW, 300, 16),
+                                      (fa.FA_MASK_BAND, 100, 0), (fa.FA_MASK_PREFIX_LM, 0, 450)])
 def test_chunked_prefill_matches_oracle(page, d, dt, mode, w, g):
     B, H, chunk = 4, 3, 200
     ctx0 = [0, 57, 600, 1000]

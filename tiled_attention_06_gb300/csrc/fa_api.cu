@@ -340,7 +340,7 @@ fa_status fa_fwd_paged(const void* q, const void* k_pages, const void* v_pages,
   a.window = window;
   a.n_global = n_global;
   a.dtype = dtype;
-  a.block_m = 128;                         // per-sequence key counts: one-tile kernel
+  a.block_m = fa_fwd_default_block_m(mask_mode);
   a.block_n = page_size % 128 == 0 ? 128 : 64;  // a K/V tile never crosses a page
   fa_status st = check_fwd(a);
   if (st != FA_OK) return st;

@@ -214,11 +214,11 @@ __device__ __forceinline__ bool softmax_cols(uint32_t t_lane, uint32_t s_col, ui
 // A whole row per thread.
 template <int D, int BN, bool BF16, typename PreRescale>
 __device__ __forceinline__ bool softmax_tile(uint32_t t_lane, uint32_t s_col, uint32_t o_col,
-                                             bool full, int n0, int pos_q,
+                                             bool full, int n0, int pos_q, int sk,
                                              const PrefillParams& p, float& m_ref, float& l,
                                              PreRescale before_rescale) {
   // (a whole row of S in registers leaves no room for the polynomial's temporaries)
-  return softmax_cols<BN, D, BF16, 0>(t_lane, s_col, s_col, o_col, full, n0, pos_q, p.Sk, p, m_ref,
+  return softmax_cols<BN, D, BF16, 0>(t_lane, s_col, s_col, o_col, full, n0, pos_q, sk, p, m_ref,
                                    l, [](float m) { return m; }, before_rescale);
 }
 
@@ -255,6 +255,33 @@ __device__ __forceinline__ void store_zero_row(size_t orow, const PrefillParams&
   uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + orow * D);
   for (int c = 0; c < D / 8; ++c) dst[c] = make_uint4(0, 0, 0, 0);
   if (p.lse) p.lse[orow] = -INFINITY;
+}
+
+// Keys of (batch, head) bh: Sk for contiguous K/V; the sequence's own length (clamped
+// to the table's capacity) for a paged cache.
+__device__ __forceinline__ int item_sk(const PrefillParams& p, int bh) {
+  if (!p.block_table) return p.Sk;
+  const int c = p.seq_k[bh / p.H];
+  return c < 0 ? 0 : (c > p.Sk ? p.Sk : c);
+}
+
+// TMA coordinates (row y, plane z) of the BN-key K/V tile at key n0 of (batch, head) bh:
+// (n0, bh) for contiguous K/V; for a paged cache the tile's rows lie in one page, at
+// (offset in the page, physical page * H + head). A table entry out of range is reported
+// (by `report` lanes) and page 0 is read instead.
+__device__ __forceinline__ void kv_tile_coords(const PrefillParams& p, int bh, int n0, bool report,
+                                               int& y, int& z) {
+  y = n0;
+  z = bh;
+  if (!p.block_table) return;
+  const int b = bh / p.H, lp = n0 / p.page_size;
+  int phys = p.block_table[static_cast<size_t>(b) * p.max_pages + lp];
+  if (phys < 0 || phys >= p.num_pages) {
+    if (report) atomicOr(p.status, FA_DEV_BAD_PAGE);
+    phys = 0;
+  }
+  y = n0 - lp * p.page_size;
+  z = phys * p.H + (bh - b * p.H);
 }
 
 // Wait that ignores the abort flag (used while winding down).
@@ -412,7 +439,7 @@ __global__ void __launch_bounds__(kThreads256, 1)
         if (t < 0) continue;
         int bh, mb;
         item_coords(t, p, bh, mb);
-        const Range rg = key_range(mb * BM, min(mb * BM + BM, p.Sq), BN, p.Sk, p);
+        const Range rg = key_range(mb * BM, min(mb * BM + BM, p.Sq), BN, item_sk(p, bh), p);
         const int n = range_count(rg);
         if (n == 0) continue;
         for (int q = 0; q < 2 && ok; ++q) {
@@ -429,10 +456,12 @@ __global__ void __launch_bounds__(kThreads256, 1)
           if (!(ok = mbar_wait(B(bars->empty[slot]), (use & 1) ^ 1, wc))) break;
           const uint32_t dst = sRing + slot * C::TILE_BYTES;
           if (leader) mbar_arrive_expect_tx(B(bars->full[slot]), C::TILE_BYTES);
-          const int n0 = range_nb(rg, s / 2) * BN;
+          int y, z;
+          kv_tile_coords(p, bh, range_nb(rg, s / 2) * BN, leader, y, z);
           const void* map = (s & 1) ? (const void*)&tmV : (const void*)&tmK;
-          if (leader) for (int c = 0; c < C::KCH; ++c)
-            tma_load_3d(dst + c * (BN * 128), map, B(bars->full[slot]), c * 64, n0, bh);
+          if (leader)
+            for (int c = 0; c < C::KCH; ++c)
+              tma_load_3d(dst + c * (BN * 128), map, B(bars->full[slot]), c * 64, y, z);
           fills[slot] = use + 1;
           ++pos;
         }
@@ -459,7 +488,7 @@ __global__ void __launch_bounds__(kThreads256, 1)
         if (t < 0) continue;
         int bh, mb;
         item_coords(t, p, bh, mb);
-        const Range rg = key_range(mb * BM, min(mb * BM + BM, p.Sq), BN, p.Sk, p);
+        const Range rg = key_range(mb * BM, min(mb * BM + BM, p.Sq), BN, item_sk(p, bh), p);
         const int n = range_count(rg);
         if (n == 0) continue;
         {  // S_A(0), S_B(0) with K0
@@ -526,7 +555,6 @@ __global__ void __launch_bounds__(kThreads256, 1)
     const int row = (warp % 4) * 32 + lane;
     const uint32_t t_lane = tmem + (static_cast<uint32_t>((warp % 4) * 32) << 16);
     const uint32_t s_col = q * BN, o_col = 2 * BN + q * D;
-    const int delta = p.Sk - p.Sq;
     uint32_t ii = 0, tc = 0;
     bool ok = true;
     int t;
@@ -534,7 +562,8 @@ __global__ void __launch_bounds__(kThreads256, 1)
       if (t < 0) continue;
       int bh, mb;
       item_coords(t, p, bh, mb);
-      const Range rg = key_range(mb * BM, min(mb * BM + BM, p.Sq), BN, p.Sk, p);
+      const int sk = item_sk(p, bh);
+      const Range rg = key_range(mb * BM, min(mb * BM + BM, p.Sq), BN, sk, p);
       const int n = range_count(rg);
       const int m0 = mb * BM + q * kTile;  // first row of this tile
       const int qrow = m0 + row;
@@ -543,12 +572,12 @@ __global__ void __launch_bounds__(kThreads256, 1)
         if (qrow < p.Sq) store_zero_row<D>(orow, p);
         continue;
       }
-      const Range mine = key_range(m0, min(m0 + kTile, p.Sq), BN, p.Sk, p);
-      const int pos_q = qrow + delta;
+      const Range mine = key_range(m0, min(m0 + kTile, p.Sq), BN, sk, p);
+      const int pos_q = qrow + sk - p.Sq;  // key position of this query
       float m_ref = -INFINITY, l = 0.f;
       for (int j = 0; j < n; ++j) {
         const int nb = range_nb(rg, j);
-        const bool full = tile_full<BN>(m0, nb, p.Sk, p);
+        const bool full = tile_full<BN>(m0, nb, sk, p);
         ok = mbar_wait(B(bars->s_full[q]), tc & 1, wc);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
@@ -558,7 +587,7 @@ __global__ void __launch_bounds__(kThreads256, 1)
                                m0 / kTile) * p.nnb + nb,
                     16 + (full ? 2 : 1));
         // S(j) was issued after PV(j-1), so O needs no wait before a rescale
-        ok = softmax_tile<D, BN, BF16>(t_lane, s_col, o_col, full, nb * BN, pos_q, p, m_ref, l,
+        ok = softmax_tile<D, BN, BF16>(t_lane, s_col, o_col, full, nb * BN, pos_q, sk, p, m_ref, l,
                                        [] { return true; });
         tc_fence_before();
         mbar_arrive(B(bars->p_full[q]));
@@ -645,13 +674,6 @@ struct ItemRef {
   Range rg;
 };
 
-// Keys of (batch, head) bh: Sk for contiguous K/V; the sequence's own length (clamped
-// to the table's capacity) for a paged cache.
-__device__ __forceinline__ int item_sk(const PrefillParams& p, int bh) {
-  if (!p.block_table) return p.Sk;
-  const int c = p.seq_k[bh / p.H];
-  return c < 0 ? 0 : (c > p.Sk ? p.Sk : c);
-}
 
 // Next item of this CTA (empty ones included when `with_empty`): false when none is left.
 template <int BM>
@@ -786,18 +808,8 @@ __global__ void __launch_bounds__(kThreads128, 1)
         }
         const uint32_t dst = sRing + slot * C::TILE_BYTES;
         if (leader) mbar_arrive_expect_tx(B(bars->full[slot]), C::TILE_BYTES);
-        const int n0 = range_nb(it.rg, j) * BN;
-        int y = n0, z = it.bh;
-        if (p.block_table) {  // the tile's rows lie in one page: (page, offset) of key n0
-          const int b = it.bh / p.H, lp = n0 / p.page_size;
-          int phys = p.block_table[static_cast<size_t>(b) * p.max_pages + lp];
-          if (phys < 0 || phys >= p.num_pages) {  // skip the bad page: load page 0, report
-            if (leader) atomicOr(p.status, FA_DEV_BAD_PAGE);
-            phys = 0;
-          }
-          y = n0 - lp * p.page_size;
-          z = phys * p.H + (it.bh - b * p.H);
-        }
+        int y, z;
+        kv_tile_coords(p, it.bh, range_nb(it.rg, j) * BN, leader, y, z);
         const void* map = is_v ? (const void*)&tmV : (const void*)&tmK;
         if (leader)
           for (int c = 0; c < C::KCH; ++c)
