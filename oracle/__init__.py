@@ -59,6 +59,14 @@ def lib():
                                          ctypes.c_int, _i64, _i64, ctypes.c_int]
         L.or_combine_partials.restype = None
         L.or_combine_partials.argtypes = [_vp, _vp, _vp, _i64, _i64, _vp, _vp]
+        L.or_attention_layout.restype = ctypes.c_int
+        L.or_attention_layout.argtypes = [_vp, _vp, _vp, ctypes.c_int, _vp, _vp, _i64, _i64,
+                                          _i64, _i64, _i64, ctypes.c_double, _vp, _i64, _vp,
+                                          _i64, ctypes.c_int]
+        L.or_count_visible_layout.restype = _i64
+        L.or_count_visible_layout.argtypes = [_i64, _i64, _i64, _vp, _i64]
+        L.or_tile_class_layout.restype = ctypes.c_int
+        L.or_tile_class_layout.argtypes = [_i64] * 7 + [_vp, _i64]
         L.or_decode_split_tokens.restype = None
         L.or_decode_split_tokens.argtypes = [_i64, _i64, _i64, _i64,
                                              ctypes.POINTER(_i64), ctypes.POINTER(_i64)]
@@ -217,3 +225,47 @@ def threads_used(nthreads=0):
     if nthreads > 0:
         return nthreads
     return len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+
+
+def _layout(layout, H, Sq, Sk, blk):
+    lay = np.ascontiguousarray(np.asarray(layout, dtype=np.uint8))
+    want = (H, -(-Sq // blk), -(-Sk // blk))
+    if lay.shape != want:
+        raise ValueError(f"layout shape {lay.shape}, want {want}")
+    return lay
+
+
+def attention_layout(q, k, v, scale, layout, blk=128, rows=None, nthreads=0):
+    """Block-sparse attention: query i of head h sees key j iff
+    layout[h, i // blk, j // blk] != 0 (layout uint8 [H, ceil(Sq/blk), ceil(Sk/blk)], the
+    same for every batch entry). Returns (o, lse) as attention()."""
+    q, k, v = _cpu(q), _cpu(k), _cpu(v)
+    B, H, Sq, d = q.shape
+    Sk = k.shape[2]
+    lay = _layout(layout, H, Sq, Sk, blk)
+    if rows is None:
+        o = np.zeros((B, H, Sq, d))
+        lse = np.zeros((B, H, Sq))
+        rp, nr = None, 0
+    else:
+        rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+        o = np.zeros((rows.size, d))
+        lse = np.zeros(rows.size)
+        rp, nr = rows.ctypes.data, rows.size
+    rc = lib().or_attention_layout(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                   _dtype_code(q, k, v), o.ctypes.data, lse.ctypes.data, B, H,
+                                   Sq, Sk, d, float(scale), lay.ctypes.data, blk, rp, nr,
+                                   nthreads)
+    if rc != 0:
+        raise ValueError("or_attention_layout rejected its arguments")
+    return o, lse
+
+
+def count_visible_layout(H, Sq, Sk, layout, blk=128):
+    lay = _layout(layout, H, Sq, Sk, blk)
+    return int(lib().or_count_visible_layout(H, Sq, Sk, lay.ctypes.data, blk))
+
+
+def tile_class_layout(h, mb, nb, BM, BN, Sq, Sk, layout, blk=128):
+    lay = _layout(layout, layout.shape[0], Sq, Sk, blk)
+    return int(lib().or_tile_class_layout(h, mb, nb, BM, BN, Sq, Sk, lay.ctypes.data, blk))

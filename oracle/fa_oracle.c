@@ -33,6 +33,13 @@
  *                          permuted tables) and against or_decode_paged (Sq = 1)
  *   or_combine_partials    pinned by split invariance against unsplit softmax
  *   or_decode_split_tokens pinned by partition invariants (cover, disjoint)
+ *   or_attention_layout    pinned against or_attention (all-ones layout = no mask;
+ *                          block 1 with a lower-triangular layout = causal), against
+ *                          torch SDPA in float64 with the layout expanded into an
+ *                          explicit boolean mask, and by key-block permutation
+ *                          invariance
+ *   or_count_visible_layout / or_tile_class_layout
+ *                          pinned by closed-form counts and hand-classified grids
  */
 #include "fa_oracle.h"
 
@@ -597,4 +604,104 @@ void or_decode_split_tokens(int64_t ctx_len, int64_t page_size,
     int64_t a = split * span, b = a + span;
     *t0 = a < ctx_len ? a : ctx_len;
     *t1 = b < ctx_len ? b : ctx_len;
+}
+
+/* ------------------------------------------------------------------ */
+/* block-sparse layouts                                                */
+/* ------------------------------------------------------------------ */
+
+/*
+ * Block-sparse attention: [boost] scenario 3 names block-sparse FlashAttention as
+ * a variant beside prefix-LM and defines it no further. It is read here as the
+ * usual block layout: query i of head h sees key j iff
+ *     layout[(h * nqb + i / blk) * nkb + j / blk] != 0,
+ * with nqb = ceil(Sq / blk) and nkb = ceil(Sk / blk); one layout serves every
+ * batch entry. No alignment between query and key positions is involved.
+ */
+static int layout_visible(const uint8_t* layout, int64_t h, int64_t i, int64_t j,
+                          int64_t nqb, int64_t nkb, int64_t blk) {
+    return layout[(h * nqb + i / blk) * nkb + j / blk] != 0;
+}
+
+/*
+ * Attention under a block layout, by the definition (attend_row), for every row
+ * (rows == NULL; o [B,H,Sq,d], lse [B,H,Sq]) or for rows[r] = (b*H + h)*Sq + i
+ * (o [nrows,d], lse [nrows]). Returns 0, or -1 on a bad argument.
+ */
+int or_attention_layout(const void* q, const void* k, const void* v, int dtype,
+                        double* o, double* lse, int64_t B, int64_t H, int64_t Sq,
+                        int64_t Sk, int64_t d, double scale, const uint8_t* layout,
+                        int64_t blk, const int64_t* rows, int64_t nrows, int nthreads) {
+    if (B < 0 || H < 0 || Sq < 0 || Sk < 0 || d <= 0 || blk <= 0) return -1;
+    if (!layout && B * H * Sq > 0) return -1;
+    const int64_t nqb = (Sq + blk - 1) / blk, nkb = (Sk + blk - 1) / blk;
+    const int64_t n_out = rows ? nrows : B * H * Sq;
+    for (int64_t r = 0; r < n_out; ++r)
+        if (rows && (rows[r] < 0 || rows[r] >= B * H * Sq)) return -1;
+#ifdef _OPENMP
+    if (nthreads <= 0) nthreads = omp_get_max_threads();
+#pragma omp parallel num_threads(nthreads)
+#endif
+    {
+        const size_t cap = (size_t)(Sk > 0 ? Sk : 1);
+        double* qrow = (double*)malloc(sizeof(double) * (size_t)d);
+        double* kd = (double*)malloc(sizeof(double) * cap * (size_t)d);
+        double* vd = (double*)malloc(sizeof(double) * cap * (size_t)d);
+        double* s = (double*)malloc(sizeof(double) * cap);
+        const double** kr = (const double**)malloc(sizeof(double*) * cap);
+        const double** vr = (const double**)malloc(sizeof(double*) * cap);
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 16)
+#endif
+        for (int64_t r = 0; r < n_out; ++r) {
+            const int64_t row = rows ? rows[r] : r;
+            const int64_t bh = row / Sq, i = row % Sq, h = bh % H;
+            for (int64_t c = 0; c < d; ++c) qrow[c] = or_elem(q, row * d + c, dtype);
+            int64_t n = 0;
+            for (int64_t j = 0; j < Sk; ++j) {
+                if (!layout_visible(layout, h, i, j, nqb, nkb, blk)) continue;
+                for (int64_t c = 0; c < d; ++c) {
+                    kd[n * d + c] = or_elem(k, (bh * Sk + j) * d + c, dtype);
+                    vd[n * d + c] = or_elem(v, (bh * Sk + j) * d + c, dtype);
+                }
+                kr[n] = kd + n * d;
+                vr[n] = vd + n * d;
+                ++n;
+            }
+            double err;
+            attend_row(qrow, kr, vr, n, d, scale, s, o + r * d, lse + r, &err);
+        }
+        free(qrow);
+        free(kd);
+        free(vd);
+        free(s);
+        free(kr);
+        free(vr);
+    }
+    return 0;
+}
+
+/* Visible (query, key) pairs of all H heads under a layout, by brute force. */
+int64_t or_count_visible_layout(int64_t H, int64_t Sq, int64_t Sk, const uint8_t* layout,
+                                int64_t blk) {
+    const int64_t nqb = (Sq + blk - 1) / blk, nkb = (Sk + blk - 1) / blk;
+    int64_t n = 0;
+    for (int64_t h = 0; h < H; ++h)
+        for (int64_t i = 0; i < Sq; ++i)
+            for (int64_t j = 0; j < Sk; ++j) n += layout_visible(layout, h, i, j, nqb, nkb, blk);
+    return n;
+}
+
+/* Class of the BM x BN tile (mb, nb) of head h under a layout, by brute force over
+ * its pairs (rows and keys past the ends count as not visible). */
+int or_tile_class_layout(int64_t h, int64_t mb, int64_t nb, int64_t BM, int64_t BN,
+                         int64_t Sq, int64_t Sk, const uint8_t* layout, int64_t blk) {
+    const int64_t nqb = (Sq + blk - 1) / blk, nkb = (Sk + blk - 1) / blk;
+    int64_t vis = 0;
+    for (int64_t i = mb * BM; i < mb * BM + BM; ++i)
+        for (int64_t j = nb * BN; j < nb * BN + BN; ++j)
+            if (i < Sq && j < Sk) vis += layout_visible(layout, h, i, j, nqb, nkb, blk);
+    if (vis == 0) return OR_TILE_EMPTY;
+    if (vis == BM * BN) return OR_TILE_FULL;
+    return OR_TILE_PARTIAL;
 }

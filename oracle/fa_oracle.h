@@ -69,6 +69,18 @@ int or_attention_paged(const void* q, const void* k_pages, const void* v_pages, 
                        double scale, int mask_mode, int64_t window, int64_t n_global,
                        int nthreads);
 
+/* Attention under a block-sparse layout uint8 [H][ceil(Sq/blk)][ceil(Sk/blk)] shared by
+   every batch entry: query i of head h sees key j iff its block is non-zero. rows as in
+   or_attention (NULL: every row). */
+int or_attention_layout(const void* q, const void* k, const void* v, int dtype,
+                        double* o, double* lse, int64_t B, int64_t H, int64_t Sq,
+                        int64_t Sk, int64_t d, double scale, const uint8_t* layout,
+                        int64_t blk, const int64_t* rows, int64_t nrows, int nthreads);
+int64_t or_count_visible_layout(int64_t H, int64_t Sq, int64_t Sk, const uint8_t* layout,
+                                int64_t blk);
+int or_tile_class_layout(int64_t h, int64_t mb, int64_t nb, int64_t BM, int64_t BN,
+                         int64_t Sq, int64_t Sk, const uint8_t* layout, int64_t blk);
+
 void or_combine_partials(const double* m, const double* l, const double* acc,
                          int64_t nsplit, int64_t d, double* o, double* lse);
 

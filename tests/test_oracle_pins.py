@@ -603,3 +603,76 @@ def test_paged_prefill_identity_table_and_single_query():
                                     di.ctx_lens, 0.5, MASK_CAUSAL)
     np.testing.assert_allclose(op[:, :, 0], od, rtol=0, atol=1e-13)
     np.testing.assert_allclose(lp[:, :, 0], ld, rtol=0, atol=1e-13)
+
+
+# --------------------------------------------------------------------------- #
+# block-sparse layouts                                                        #
+# --------------------------------------------------------------------------- #
+
+def _rand_layout(H, Sq, Sk, blk, seed, density=0.5):
+    rng = np.random.default_rng(seed)
+    return (rng.random((H, -(-Sq // blk), -(-Sk // blk))) < density).astype(np.uint8)
+
+
+def test_layout_all_ones_is_no_mask_and_tril_block1_is_causal():
+    q, k, v = (torch.randn(2, 3, 37, 16, generator=torch.Generator().manual_seed(s))
+               .to(torch.bfloat16) for s in (1, 2, 3))
+    ones = np.ones((3, 2, 2), dtype=np.uint8)  # blk 32 over 37 rows / keys
+    o, lse = oracle.attention_layout(q, k, v, 0.25, ones, blk=32)
+    o2, lse2 = oracle.attention(q, k, v, 0.25, MASK_NONE)
+    assert np.array_equal(o, o2) and np.array_equal(lse, lse2)
+    tril = np.broadcast_to(np.tril(np.ones((37, 37), dtype=np.uint8)), (3, 37, 37))
+    o, lse = oracle.attention_layout(q, k, v, 0.25, tril, blk=1)
+    o2, lse2 = oracle.attention(q, k, v, 0.25, MASK_CAUSAL)
+    assert np.array_equal(o, o2) and np.array_equal(lse, lse2)
+
+
+@pytest.mark.parametrize("Sq,Sk,blk", [(40, 40, 8), (33, 70, 16), (70, 33, 16), (5, 9, 4)])
+def test_layout_matches_sdpa_with_expanded_mask(Sq, Sk, blk):
+    H = 3
+    g = torch.Generator().manual_seed(Sq * 100 + Sk)
+    q = torch.randn(2, H, Sq, 16, generator=g).to(torch.float16)
+    k = torch.randn(2, H, Sk, 16, generator=g).to(torch.float16)
+    v = torch.randn(2, H, Sk, 16, generator=g).to(torch.float16)
+    lay = _rand_layout(H, Sq, Sk, blk, seed=Sq + Sk)
+    lay[0, 0, :] = 0  # head 0's first query block sees nothing
+    o, lse = oracle.attention_layout(q, k, v, 0.3, lay, blk=blk)
+    # the layout blown up to one flag per (query, key), built here with np.kron
+    full = np.stack([np.kron(lay[h], np.ones((blk, blk), dtype=np.uint8))[:Sq, :Sk]
+                     for h in range(H)]).astype(bool)
+    mask = torch.from_numpy(full)[None].expand(2, H, Sq, Sk)
+    seen = mask.any(-1)
+    ref = torch.nn.functional.scaled_dot_product_attention(q.double(), k.double(), v.double(),
+                                                           attn_mask=mask, scale=0.3)
+    rows = seen.numpy()
+    np.testing.assert_allclose(o[rows], ref.numpy()[rows], rtol=0, atol=1e-12)
+    assert np.all(o[~rows] == 0) and np.all(np.isneginf(lse[~rows]))
+    s = torch.einsum("bhid,bhjd->bhij", q.double(), k.double()) * 0.3
+    want = torch.logsumexp(s.masked_fill(~mask, -math.inf), dim=-1).numpy()
+    np.testing.assert_allclose(lse[rows], want[rows], rtol=0, atol=1e-12)
+    assert oracle.count_visible_layout(H, Sq, Sk, lay, blk) == int(full.sum())
+
+
+def test_layout_key_block_permutation_invariance():
+    H, S, blk = 2, 48, 16
+    g = torch.Generator().manual_seed(7)
+    q, k, v = (torch.randn(1, H, S, 8, generator=g).to(torch.bfloat16) for _ in range(3))
+    lay = _rand_layout(H, S, S, blk, seed=3, density=0.6)
+    perm = [2, 0, 1]  # move whole key blocks, and the layout's columns with them
+    idx = torch.cat([torch.arange(p * blk, (p + 1) * blk) for p in perm])
+    o1, l1 = oracle.attention_layout(q, k, v, 0.5, lay, blk=blk)
+    o2, l2 = oracle.attention_layout(q, k[:, :, idx], v[:, :, idx], 0.5, lay[:, :, perm],
+                                     blk=blk)
+    np.testing.assert_allclose(o1, o2, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(l1, l2, rtol=0, atol=1e-13)
+
+
+def test_layout_counts_and_tile_classes():
+    lay = np.array([[[1, 0], [1, 1]]], dtype=np.uint8)  # one head, 2 x 2 blocks of 4
+    # query rows 0-3 see keys 0-3; rows 4-6 (Sq = 7) see keys 0-5 (Sk = 6)
+    assert oracle.count_visible_layout(1, 7, 6, lay, 4) == 4 * 4 + 3 * 6
+    # 4x4 tiles: (0,0) full, (0,1) empty, (1,0) partial (3 of 4 rows), (1,1) partial
+    classes = [[oracle.tile_class_layout(0, mb, nb, 4, 4, 7, 6, lay, 4) for nb in range(2)]
+               for mb in range(2)]
+    assert classes == [[oracle.TILE_FULL, oracle.TILE_EMPTY],
+                       [oracle.TILE_PARTIAL, oracle.TILE_PARTIAL]]
