@@ -25,6 +25,7 @@ import subprocess
 import sys
 import time
 
+import numpy as np
 import torch
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -47,20 +48,25 @@ PREFILL = {
                    factor=1.0),
     "prefixlm4k": dict(B=4, H=32, S=4096, d=128, dtype="bf16", mode=4, window=0, n_global=1024,
                        factor=1.0),
+    # BigBird-shaped layout of 128 x 128 blocks (the pages give none): local +-1 block,
+    # 1 global block row and column, 2 random blocks per row, seeded
+    "blocksparse4k": dict(B=4, H=32, S=4096, d=128, dtype="bf16", mode=5, window=0, n_global=0,
+                          factor=1.0, layout=dict(local=1, n_global=1, n_random=2)),
 }
 DECODE = dict(B=32, H=32, d=128, page=256, pool=1200, max_ctx=8192, dtype="f16")
 PREFIX_WORKLOADS = ("default", "decode", "causal2k", "causal4k", "noncausal4k", "window32k",
                     "band4k", "prefixlm4k")
-MODE_NAME = {0: "none", 1: "causal", 2: "causal_window", 3: "band", 4: "prefix_lm"}
+MODE_NAME = {0: "none", 1: "causal", 2: "causal_window", 3: "band", 4: "prefix_lm",
+             5: "block_sparse"}
 
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu
 # capture of each kernel, with the SHA-256 of the kernel sources it was taken on; the
 # figure is reported only while those sources are unchanged. Summaries: profiles/.
 NCU_TRAFFIC = {
-    # prefill_bm256_kernel, causal 4k B4 H16 capture: 210.0 MB read + 45.2 MB written,
+    # prefill_bm256_kernel, causal 4k B4 H16 capture: 210.3 MB read + 45.0 MB written,
     # scaled x2 to B4 H32
-    "prefill": {"bytes": 510.4e6, "sources": ['fa_prefill.cu', 'fa_ptx.cuh', 'fa_plan.h', 'fa_internal.h'],
-                "sha256": "ebd61437eeb257d160c5aafba635f1a244d401713ce0cf28c75b8efa4a3442c1"},
+    "prefill": {"bytes": 510.6e6, "sources": ['fa_prefill.cu', 'fa_ptx.cuh', 'fa_plan.h', 'fa_internal.h'],
+                "sha256": "263ae657df70fa1a5e1478f561972a8fc09a654a0429156dce7227aaeceb93dc"},
     # paged decode B8 capture: 547.5 MB read + 3.7 MB written for 547.5 MB algorithmic,
     # scaled to the bench call's 2410.7 MB algorithmic
     "decode": {"bytes": 2.4268e9, "sources": ['fa_decode.cu', 'fa_ptx.cuh', 'fa_internal.h'],
@@ -110,7 +116,27 @@ def visible_pairs(Sq, Sk, mode, window=0, n_global=0):
     return sum(row_visible(i + delta, Sk, mode, window, n_global) for i in range(Sq))
 
 
-def prefill_flops(cfg):
+def layout_pairs(layout, Sq, Sk, block=128, heads=None):
+    """Visible (query, key) pairs of a block layout [H, nqb, nkb], summed over its heads
+    (or the listed ones): each set block counts its rows x keys, clipped at Sq and Sk."""
+    lay = np.asarray(layout, dtype=np.int64)
+    if heads is not None:
+        lay = lay[list(heads)]
+    rows = np.minimum(block, Sq - block * np.arange(lay.shape[1]))
+    keys = np.minimum(block, Sk - block * np.arange(lay.shape[2]))
+    return int(np.einsum("hij,i,j->", lay, rows, keys))
+
+
+def make_layout(cfg):
+    from tiled_attention_06_gb300 import inputs
+    return inputs.block_layout(cfg["H"], cfg["S"], cfg["S"], **cfg["layout"])
+
+
+def prefill_flops(cfg, layout=None):
+    if cfg["mode"] == 5:
+        if layout is None:
+            layout = make_layout(cfg)
+        return 4.0 * cfg["B"] * cfg["d"] * layout_pairs(layout, cfg["S"], cfg["S"])
     return 4.0 * cfg["B"] * cfg["H"] * cfg["d"] * visible_pairs(cfg["S"], cfg["S"], cfg["mode"],
                                                                 cfg["window"], cfg["n_global"])
 
@@ -246,12 +272,16 @@ def run_ours(args, rank, world):
     with_decode = workload in ("default", "decode")
 
     # ---- inputs, resident in HBM before timing
+    layout = lay_d = None
     if pcfg:
         q, k, v = make_prefill(pcfg, dev)
         qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
         od = torch.empty_like(qd)
         ld = torch.empty(qd.shape[:3], dtype=torch.float32, device=dev)
-        pflops = prefill_flops(pcfg)
+        if pcfg["mode"] == 5:
+            layout = make_layout(pcfg)
+            lay_d = layout.to(dev)
+        pflops = prefill_flops(pcfg, layout)
         scale = 1 / math.sqrt(pcfg["d"])
     if with_decode:
         di = make_decode(dev)
@@ -269,6 +299,8 @@ def run_ours(args, rank, world):
     def prefill_call(**ex):
         if args.block_m and "block_m" not in ex:
             ex["block_m"] = args.block_m
+        if lay_d is not None:
+            ex["block_layout"] = lay_d
         if ex:
             fa.fa_fwd_ex(qd, kd, vd, od, ld, scale, pcfg["mode"], pcfg["window"],
                          pcfg["n_global"], stream=stream, **ex)
@@ -365,7 +397,8 @@ def run_ours(args, rank, world):
     res["config"] = workload_config(pcfg, with_decode, world)
 
     # ---- end to end through the public API with host buffers
-    res["e2e"] = e2e_prefill(fa, pcfg, q, k, v, pflops, scale, stream, world, args) if pcfg \
+    res["e2e"] = e2e_prefill(fa, pcfg, q, k, v, pflops, scale, stream, world, args, layout) \
+        if pcfg \
         else e2e_decode(fa, di, dbytes, dscale, ws, dk, dv, stream, world, args)
     # ---- CPU baseline: the oracle on a bounded sample, rank 0 only
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -392,9 +425,14 @@ def workload_config(pcfg, with_decode, world):
     return cfg
 
 
-def e2e_prefill(fa, pcfg, q, k, v, pflops, scale, stream, world, args):
+def e2e_prefill(fa, pcfg, q, k, v, pflops, scale, stream, world, args, layout=None):
     dev = torch.device("cuda", torch.cuda.current_device())
     hq, hk, hv = q.pin_memory(), k.pin_memory(), v.pin_memory()
+    ins = [hq, hk, hv]
+    if layout is not None:
+        hlay = layout.pin_memory()
+        lay_d = torch.empty_like(hlay, device=dev)
+        ins.append(hlay)
     ho = torch.empty(q.shape, dtype=q.dtype).pin_memory()
     hl = torch.empty(q.shape[:3], dtype=torch.float32).pin_memory()
     qd, kd, vd = torch.empty_like(hq, device=dev), torch.empty_like(hk, device=dev), \
@@ -406,8 +444,13 @@ def e2e_prefill(fa, pcfg, q, k, v, pflops, scale, stream, world, args):
         qd.copy_(hq, non_blocking=True)
         kd.copy_(hk, non_blocking=True)
         vd.copy_(hv, non_blocking=True)
-        fa.fa_fwd(qd, kd, vd, od, ld, scale, pcfg["mode"], pcfg["window"], pcfg["n_global"],
-                  stream=stream)
+        if layout is not None:
+            lay_d.copy_(hlay, non_blocking=True)
+            fa.fa_fwd_ex(qd, kd, vd, od, ld, scale, pcfg["mode"], block_layout=lay_d,
+                         stream=stream)
+        else:
+            fa.fa_fwd(qd, kd, vd, od, ld, scale, pcfg["mode"], pcfg["window"],
+                      pcfg["n_global"], stream=stream)
         ho.copy_(od, non_blocking=True)
         hl.copy_(ld, non_blocking=True)
 
@@ -423,7 +466,7 @@ def e2e_prefill(fa, pcfg, q, k, v, pflops, scale, stream, world, args):
     e1.record(stream)
     torch.cuda.synchronize()
     secs = max_over_ranks(e0.elapsed_time(e1) / 1e3, world)
-    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
+    h2d = sum(t.numel() * t.element_size() for t in ins)
     d2h = ho.numel() * ho.element_size() + hl.numel() * 4
     return {"value": aggregate(pflops * K, secs, world) / 1e12, "unit": "TFLOP/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": K,
@@ -472,10 +515,16 @@ def oracle_prefill_sample(pcfg, q, k, v, n_heads):
     import oracle
     S = pcfg["S"]
     rows = np.arange(n_heads * S, dtype=np.int64)
-    pairs = n_heads * visible_pairs(S, S, pcfg["mode"], pcfg["window"], pcfg["n_global"])
     t0 = time.perf_counter()
-    oracle.attention(q, k, v, 1 / math.sqrt(pcfg["d"]), pcfg["mode"], pcfg["window"],
-                     pcfg["n_global"], rows=rows)
+    if pcfg["mode"] == 5:  # the first n_heads (batch, head) pairs: heads 0.. of batch 0, ...
+        layout = make_layout(pcfg)
+        pairs = layout_pairs(layout, S, S, heads=[bh % pcfg["H"] for bh in range(n_heads)])
+        t0 = time.perf_counter()
+        oracle.attention_layout(q, k, v, 1 / math.sqrt(pcfg["d"]), layout, rows=rows)
+    else:
+        pairs = n_heads * visible_pairs(S, S, pcfg["mode"], pcfg["window"], pcfg["n_global"])
+        oracle.attention(q, k, v, 1 / math.sqrt(pcfg["d"]), pcfg["mode"], pcfg["window"],
+                         pcfg["n_global"], rows=rows)
     secs = time.perf_counter() - t0
     return 4.0 * pairs * pcfg["d"], secs, oracle.threads_used()
 
@@ -753,7 +802,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="default",
                     choices=["default", "causal2k", "causal4k", "noncausal4k", "window32k",
-                             "band4k", "prefixlm4k", "chunked", "multimodal",
+                             "band4k", "prefixlm4k", "blocksparse4k", "chunked", "multimodal",
                              "decode", "sweep"])
     ap.add_argument("--batch", type=int, default=None, help="override B (small profiling cases)")
     ap.add_argument("--heads", type=int, default=None, help="override H (small profiling cases)")

@@ -29,6 +29,11 @@
  *                          prefix) are seen by every query, the rest causally (the
  *                          prefix-LM variant named in "ascend-transformer-boost 实战",
  *                          scenario 3); n_global >= 0.
+ *   FA_MASK_BLOCK_SPARSE   layout[h][i / 128][j / 128] != 0: a caller's block layout,
+ *                          uint8 [H][ceil(Sq/128)][ceil(Sk/128)], one per head and the same
+ *                          for every batch entry (the block-sparse variant that
+ *                          "ascend-transformer-boost 实战" names beside prefix-LM, read as
+ *                          the usual block layout). fa_fwd_ex only (params.block_layout).
  * A query that sees no key gets O = 0 and LSE = -inf.
  *
  * Conventions for every call:
@@ -70,8 +75,12 @@ enum {
   FA_MASK_CAUSAL = 1,
   FA_MASK_CAUSAL_WINDOW = 2,
   FA_MASK_BAND = 3,
-  FA_MASK_PREFIX_LM = 4
+  FA_MASK_PREFIX_LM = 4,
+  FA_MASK_BLOCK_SPARSE = 5
 };
+
+/* Block size of a block-sparse layout (query rows x keys). */
+#define FA_LAYOUT_BLOCK 128
 
 /*
  * fa_fwd - attention forward (prefill) over contiguous BHSD tensors.
@@ -114,6 +123,9 @@ typedef struct fa_fwd_params {
    * computes for those 128 queries adds 16 + class (1 partial, 2 full); tiles the mask
    * skips stay 0. */
   int32_t* trace;
+  /* FA_MASK_BLOCK_SPARSE: device pointer to the layout described above (owned by the
+   * caller, read during the call); ignored for the other masks. */
+  const uint8_t* block_layout;
 } fa_fwd_params;
 
 fa_status fa_fwd_ex(const fa_fwd_params* params, fa_stream_t stream);
@@ -123,7 +135,9 @@ int fa_fwd_block_m(void);
 
 /* Query rows per work item that fa_fwd (and fa_fwd_ex with block_m = 0) uses for a mask:
  * 256 (two 128-row tiles sharing every K/V tile) except for FA_MASK_BAND, whose narrow
- * key ranges favour 128. fa_fwd_paged uses the same choice. Returns 0 for an unknown mask. */
+ * key ranges favour 128, and FA_MASK_BLOCK_SPARSE, where a 256-row item would visit the
+ * union of two layout rows. fa_fwd_paged uses the same choice. Returns 0 for an unknown
+ * mask. */
 int fa_fwd_default_block_m(int mask_mode);
 
 /*

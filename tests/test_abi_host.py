@@ -64,8 +64,8 @@ def test_struct_layouts_match_header(tmp_path):
 def test_version_and_block_m(L):
     assert L.fa_version() >= 100
     assert L.fa_fwd_block_m() == 128
-    assert [L.fa_fwd_default_block_m(m) for m in range(5)] == [256, 256, 256, 128, 256]
-    assert L.fa_fwd_default_block_m(5) == 0 and L.fa_fwd_default_block_m(-1) == 0
+    assert [L.fa_fwd_default_block_m(m) for m in range(6)] == [256, 256, 256, 128, 256, 128]
+    assert L.fa_fwd_default_block_m(6) == 0 and L.fa_fwd_default_block_m(-1) == 0
 
 
 def test_workspace_size_and_split_rule(L):
@@ -98,7 +98,8 @@ def _fwd(L, **kw):
     (dict(d=96), fa.FA_ERR_UNSUPPORTED),
     (dict(d=256), fa.FA_ERR_UNSUPPORTED),
     (dict(dtype=2), fa.FA_ERR_UNSUPPORTED),
-    (dict(mask_mode=5), fa.FA_ERR_INVALID_ARG),
+    (dict(mask_mode=5), fa.FA_ERR_INVALID_ARG),  # block-sparse without a layout
+    (dict(mask_mode=6), fa.FA_ERR_INVALID_ARG),
     (dict(mask_mode=-1), fa.FA_ERR_INVALID_ARG),
     (dict(mask_mode=3, window=-1), fa.FA_ERR_INVALID_ARG),
     (dict(mask_mode=4, n_global=-1), fa.FA_ERR_INVALID_ARG),

@@ -8,6 +8,7 @@ import torch
 import torch.multiprocessing as mp
 
 import bench
+import numpy as np
 import oracle
 
 
@@ -73,3 +74,21 @@ def test_two_rank_aggregation_over_gloo():
         t, v = out[r]
         assert t == 2.5                      # the slowest rank's time
         assert v == pytest.approx(200.0 / 2.5)  # both ranks' units over that time
+
+
+@pytest.mark.parametrize("H,Sq,Sk,blk", [(2, 300, 300, 128), (3, 130, 257, 128), (1, 9, 7, 4)])
+def test_layout_pairs_match_oracle_count(H, Sq, Sk, blk):
+    from tiled_attention_06_gb300 import inputs
+    lay = inputs.block_layout(H, Sq, Sk, block=blk, seed=H + Sq)
+    assert bench.layout_pairs(lay, Sq, Sk, blk) == oracle.count_visible_layout(H, Sq, Sk,
+                                                                             lay.numpy(), blk)
+
+
+def test_bigbird_layout_shape():
+    from tiled_attention_06_gb300 import inputs
+    lay = inputs.block_layout(4, 4096, 4096, seed=0).numpy()
+    assert lay.shape == (4, 32, 32) and lay.dtype == np.uint8
+    i, j = np.indices((32, 32))
+    assert np.all(lay[:, np.abs(i - j) <= 1] == 1)       # local band
+    assert np.all(lay[:, 0, :] == 1) and np.all(lay[:, :, 0] == 1)  # global block
+    assert np.all(lay[:, 1:].sum(-1) <= 3 + 1 + 2)       # band, global column, two random

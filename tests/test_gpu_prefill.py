@@ -187,3 +187,74 @@ def test_sliding_window_32k_sampled():
     ref_o, ref_l = oracle.attention(q, k, v, scale, oracle.MASK_CAUSAL_WINDOW, 2048, 64,
                                     rows=rows)
     compare(pick_rows(o, rows, S), pick_rows(lse, rows, S), ref_o, ref_l, "window 32k")
+
+
+# --------------------------------------------------------------------------- block-sparse
+def _layout(H, Sq, Sk, seed, density=0.45):
+    g = torch.Generator().manual_seed(seed)
+    nq, nk = -(-Sq // fa.FA_LAYOUT_BLOCK), -(-Sk // fa.FA_LAYOUT_BLOCK)
+    lay = (torch.rand(H, nq, nk, generator=g) < density).to(torch.uint8)
+    lay[0, 0, :] = 0  # one query block of head 0 sees nothing
+    return lay
+
+
+def run_sparse(q, k, v, scale, lay, **ex):
+    dev = torch.device("cuda")
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    o = torch.empty_like(qd)
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+    fa.fa_fwd_ex(qd, kd, vd, o, lse, scale, fa.FA_MASK_BLOCK_SPARSE,
+                 block_layout=lay.to(dev), **ex)
+    torch.cuda.synchronize()
+    assert fa.fa_get_device_status() == fa.FA_OK
+    return o, lse
+
+
+@pytest.mark.parametrize("Sq,Sk", [(1, 1), (127, 129), (200, 333), (384, 384), (520, 257)])
+@pytest.mark.parametrize("d,dt", [(64, "f16"), (128, "bf16")])
+@pytest.mark.parametrize("bn", [64, 128])
+@pytest.mark.parametrize("bm", [128, 256])
+def test_block_sparse_small(Sq, Sk, d, dt, bn, bm):
+    q, k, v = inputs.prefill_inputs(2, 3, Sq, Sk, d, DT[dt], seed=Sq + 7 * Sk)
+    lay = _layout(3, Sq, Sk, seed=Sq * Sk)
+    scale = 1 / math.sqrt(d)
+    o, lse = run_sparse(q, k, v, scale, lay, block_n=bn, block_m=bm)
+    ref_o, ref_l = oracle.attention_layout(q, k, v, scale, lay.numpy())
+    compare(o, lse, ref_o, ref_l, f"block-sparse {Sq}x{Sk} d{d} bn{bn} bm{bm}")
+
+
+@pytest.mark.parametrize("bn", [64, 128])
+@pytest.mark.parametrize("bm", [128, 256])
+def test_block_sparse_trace_is_bit_exact(bn, bm):
+    """Tiles the kernel visits, with their classes, equal the oracle's brute-force
+    classification under the layout; a 256-row item visits only its tiles' blocks."""
+    B, H, Sq, Sk, d = 1, 2, 900, 1100, 64
+    q, k, v = inputs.prefill_inputs(B, H, Sq, Sk, d, torch.float16, seed=5)
+    lay = _layout(H, Sq, Sk, seed=11, density=0.35)
+    BM = fa.fa_fwd_block_m()
+    nmb, nnb = -(-Sq // BM), -(-Sk // bn)
+    trace = torch.zeros(B * H * nmb * nnb, dtype=torch.int32, device="cuda")
+    o, lse = run_sparse(q, k, v, 0.125, lay, block_n=bn, block_m=bm, trace=trace)
+    got = trace.cpu().numpy().reshape(B * H, nmb, nnb)
+    for h in range(H):
+        want = np.zeros((nmb, nnb), dtype=np.int32)
+        for mb in range(nmb):
+            for nb in range(nnb):
+                c = oracle.tile_class_layout(h, mb, nb, BM, bn, Sq, Sk, lay.numpy())
+                want[mb, nb] = 0 if c == oracle.TILE_EMPTY else 16 + c
+        assert np.array_equal(got[h], want), f"head {h}"
+    ref_o, ref_l = oracle.attention_layout(q, k, v, 0.125, lay.numpy())
+    compare(o, lse, ref_o, ref_l, "block-sparse trace case")
+
+
+def test_block_sparse_4k_bigbird_sampled():
+    """The bench's block-sparse configuration: B=4, H=32, S=4096, d=128, bf16 with the
+    seeded BigBird-shaped layout; sampled rows of every head."""
+    B, H, S, d = 4, 32, 4096, 128
+    q, k, v = inputs.prefill_inputs(B, H, S, S, d, torch.bfloat16, seed=0)
+    lay = inputs.block_layout(H, S, S)
+    scale = 1 / math.sqrt(d)
+    o, lse = run_sparse(q, k, v, scale, lay)
+    rows = sample_rows(B, H, S, fa.fa_fwd_block_m(), n_random=128, seed=3)
+    ref_o, ref_l = oracle.attention_layout(q, k, v, scale, lay.numpy(), rows=rows)
+    compare(pick_rows(o, rows, S), pick_rows(lse, rows, S), ref_o, ref_l, "block-sparse 4k")

@@ -20,12 +20,15 @@ __all__ = [
     "fa_fwd_default_block_m",
     "FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_CUDA", "FA_ERR_TIMEOUT",
     "FA_ERR_BAD_PAGE", "FA_F16", "FA_BF16", "FA_MASK_NONE", "FA_MASK_CAUSAL",
-    "FA_MASK_CAUSAL_WINDOW", "FA_MASK_BAND", "FA_MASK_PREFIX_LM",
+    "FA_MASK_CAUSAL_WINDOW", "FA_MASK_BAND", "FA_MASK_PREFIX_LM", "FA_MASK_BLOCK_SPARSE",
+    "FA_LAYOUT_BLOCK",
 ]
 
 FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT, FA_ERR_BAD_PAGE = range(6)
 FA_F16, FA_BF16 = 0, 1
 FA_MASK_NONE, FA_MASK_CAUSAL, FA_MASK_CAUSAL_WINDOW, FA_MASK_BAND, FA_MASK_PREFIX_LM = 0, 1, 2, 3, 4
+FA_MASK_BLOCK_SPARSE = 5
+FA_LAYOUT_BLOCK = 128
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libfa.so")
 
@@ -48,7 +51,7 @@ class FwdParams(ctypes.Structure):
                 ("mask_mode", _i), ("window", _i), ("n_global", _i), ("dtype", _i),
                 ("block_n", _i), ("block_m", _i), ("num_ctas", _i), ("group_heads", _i),
                 ("timeout_us", _u32),
-                ("trace", _vp)]
+                ("trace", _vp), ("block_layout", _vp)]
 
 
 class DecodeParams(ctypes.Structure):
@@ -176,12 +179,15 @@ def fa_fwd(q, k, v, o, lse, scale, mask_mode=FA_MASK_NONE, window=0, n_global=0,
 
 def fa_fwd_ex(q, k, v, o, lse, scale, mask_mode=FA_MASK_NONE, window=0, n_global=0,
               block_n=0, block_m=0, num_ctas=0, group_heads=0, timeout_us=0, trace=None,
-              stream=None):
-    _need_cuda_contig(q=q, k=k, v=v, o=o, lse=lse, trace=trace)
+              block_layout=None, stream=None):
+    """fa_fwd with the tuning and debug fields of fa_fwd_params. block_layout: uint8 CUDA
+    tensor [H, ceil(Sq/128), ceil(Sk/128)] for FA_MASK_BLOCK_SPARSE."""
+    _need_cuda_contig(q=q, k=k, v=v, o=o, lse=lse, trace=trace, block_layout=block_layout)
     B, H, Sq, d = q.shape
     p = FwdParams(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), _ptr(lse), B, H, Sq,
                   k.shape[2], d, float(scale), mask_mode, window, n_global, _dtype_code(q),
-                  block_n, block_m, num_ctas, group_heads, timeout_us, _ptr(trace))
+                  block_n, block_m, num_ctas, group_heads, timeout_us, _ptr(trace),
+                  _ptr(block_layout))
     _check(lib().fa_fwd_ex(ctypes.byref(p), _stream(stream)))
 
 

@@ -135,7 +135,7 @@ const fa::PrefillSched* plan_for(const fa::PrefillParams& p, int BM, int BN, int
     for (int t = 0; t < p.total_items; ++t) {
       int bh, mb;
       fa::item_coords(t, p, bh, mb);
-      const fa::Range r = fa::key_range(mb * BM, std::min(mb * BM + BM, p.Sq), BN, p.Sk, p);
+      const fa::Range r = fa::key_range(mb * BM, std::min(mb * BM + BM, p.Sq), BN, p.Sk, p, 0);
       const int n = fa::range_count(r);
       Slot s = free_at.top();
       free_at.pop();
@@ -169,8 +169,10 @@ fa_status check_fwd(const fa_fwd_params& p) {
   if (p.d != 64 && p.d != 128) return fail(FA_ERR_UNSUPPORTED, "head dim %d (supported: 64, 128)", p.d);
   if (p.dtype != FA_F16 && p.dtype != FA_BF16) return fail(FA_ERR_UNSUPPORTED, "dtype %d", p.dtype);
   if (!std::isfinite(p.scale)) return fail(FA_ERR_INVALID_ARG, "scale must be finite");
-  if (p.mask_mode < FA_MASK_NONE || p.mask_mode > FA_MASK_PREFIX_LM)
+  if (p.mask_mode < FA_MASK_NONE || p.mask_mode > FA_MASK_BLOCK_SPARSE)
     return fail(FA_ERR_INVALID_ARG, "mask_mode %d", p.mask_mode);
+  if (p.mask_mode == FA_MASK_BLOCK_SPARSE && !p.block_layout && p.Sq > 0)
+    return fail(FA_ERR_INVALID_ARG, "BLOCK_SPARSE needs params.block_layout");
   if (p.mask_mode == FA_MASK_CAUSAL_WINDOW && (p.window < 1 || p.n_global < 0))
     return fail(FA_ERR_INVALID_ARG, "CAUSAL_WINDOW needs window >= 1 and n_global >= 0");
   if (p.mask_mode == FA_MASK_BAND && p.window < 0)
@@ -200,8 +202,10 @@ const char* fa_last_error_string(void) { return t_last_error.c_str(); }
 int fa_fwd_block_m(void) { return fa::prefill_tile_rows(); }
 
 int fa_fwd_default_block_m(int mask_mode) {
-  if (mask_mode < FA_MASK_NONE || mask_mode > FA_MASK_PREFIX_LM) return 0;
-  return mask_mode == FA_MASK_BAND ? 128 : 256;
+  if (mask_mode < FA_MASK_NONE || mask_mode > FA_MASK_BLOCK_SPARSE) return 0;
+  // the band's narrow key ranges, and block-sparse rows whose union over two query
+  // blocks is much larger than either, favour one tile per item
+  return mask_mode == FA_MASK_BAND || mask_mode == FA_MASK_BLOCK_SPARSE ? 128 : 256;
 }
 
 }  // extern "C"
@@ -262,6 +266,12 @@ fa_status run_fwd(const fa_fwd_params& a, const PagedKV* pg, fa_stream_t stream)
   p.status = dev.status;
   p.timeout_ns = static_cast<uint64_t>(a.timeout_us ? a.timeout_us : 1000000u) * 1000u;
   p.trace = a.trace;
+  p.H = a.H;
+  if (a.mask_mode == FA_MASK_BLOCK_SPARSE) {  // planned as dense: the layout is on the device
+    p.layout = a.block_layout;
+    p.lnqb = (a.Sq + FA_LAYOUT_BLOCK - 1) / FA_LAYOUT_BLOCK;
+    p.lnkb = (a.Sk + FA_LAYOUT_BLOCK - 1) / FA_LAYOUT_BLOCK;
+  }
   L.grid = a.num_ctas ? a.num_ctas : dev.sms;
   if (L.grid > p.total_items) L.grid = p.total_items;
   L.sched = plan_for(p, BM, BN, L.grid);

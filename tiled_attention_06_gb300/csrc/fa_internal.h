@@ -33,6 +33,9 @@ struct PrefillParams {
   const int32_t* block_table;
   const int32_t* seq_k;
   int H, page_size, max_pages, num_pages;
+  // Block-sparse layout uint8 [H, lnqb, lnkb] (128 x 128 blocks), or nullptr.
+  const uint8_t* layout;
+  int lnqb, lnkb;
 };
 
 struct PrefillSched;  // fa_plan.h

@@ -17,9 +17,14 @@ namespace fa {
 
 // Key blocks visited by the query rows [m0, m1): [0, a_end) then [b_start, b_end),
 // a_end <= b_start. Closed form of the mask: every block inside holds at least one
-// visible pair for these rows, every block outside holds none.
+// visible pair for these rows, every block outside holds none. A block-sparse mask
+// (device code only) visits the blocks of [0, b_end) whose layout byte is set in the
+// row of either query block (la, lb; key block nb -> layout column nb >> shift).
 struct Range {
   int a_end, b_start, b_end;
+  const uint8_t* la;
+  const uint8_t* lb;
+  int shift;
 };
 
 FA_HD int imin(int a, int b) { return a < b ? a : b; }
@@ -27,11 +32,20 @@ FA_HD int imax(int a, int b) { return a > b ? a : b; }
 
 // `sk` is the number of keys of this (batch, head): p.Sk for contiguous K/V, the
 // sequence's own length for a paged cache.
-FA_HD Range key_range(int m0, int m1, int BN, int sk, const PrefillParams& p) {
+FA_HD Range key_range(int m0, int m1, int BN, int sk, const PrefillParams& p, int bh) {
   const int nnb = (sk + BN - 1) / BN;
   Range r{0, 0, nnb};
   if (m0 >= m1 || nnb == 0) return Range{0, 0, 0};
   if (p.mask_mode == FA_MASK_NONE) return r;
+  if (p.mask_mode == FA_MASK_BLOCK_SPARSE) {
+#if defined(__CUDA_ARCH__)  // the layout is device memory: the host plans with every block
+    const uint8_t* head = p.layout + static_cast<size_t>(bh % p.H) * p.lnqb * p.lnkb;
+    r.la = head + static_cast<size_t>(m0 / 128) * p.lnkb;
+    r.lb = m1 - m0 > 128 ? r.la + p.lnkb : nullptr;
+    r.shift = BN == 64 ? 1 : 0;
+#endif
+    return r;
+  }
   const int delta = sk - p.Sq;
   const int r_lo = m0 + delta;      // key position of the first row
   const int r_hi = m1 - 1 + delta;  // key position of the last row
@@ -62,9 +76,28 @@ FA_HD Range key_range(int m0, int m1, int BN, int sk, const PrefillParams& p) {
   return r;
 }
 
-FA_HD int range_count(const Range& r) { return r.a_end + r.b_end - r.b_start; }
-FA_HD int range_nb(const Range& r, int t) { return t < r.a_end ? t : r.b_start + (t - r.a_end); }
+FA_HD bool range_vis(const Range& r, int nb) {  // block-sparse: is block nb visited
+  return (r.la[nb >> r.shift] | (r.lb ? r.lb[nb >> r.shift] : 0)) != 0;
+}
+FA_HD int range_count(const Range& r) {
+  if (!r.la) return r.a_end + r.b_end - r.b_start;
+  int n = 0;
+  for (int nb = 0; nb < r.b_end; ++nb) n += range_vis(r, nb);
+  return n;
+}
+// The key block visited after block nb (the first one for nb = -1); callers ask for no
+// more than range_count blocks.
+FA_HD int range_next(const Range& r, int nb) {
+  int t = nb + 1;
+  if (r.la) {
+    while (t < r.b_end && !range_vis(r, t)) ++t;
+    return t;
+  }
+  if (t >= r.a_end && t < r.b_start) t = r.b_start;
+  return t;
+}
 FA_HD bool range_has(const Range& r, int nb) {
+  if (r.la) return nb >= 0 && nb < r.b_end && range_vis(r, nb);
   return nb < r.a_end || (nb >= r.b_start && nb < r.b_end);
 }
 

@@ -63,13 +63,23 @@ constexpr int pow2_at_least(int x) {
 
 // ------------------------------------------------------------------ shared helpers
 
+// Block-sparse: the layout byte of the 128-row query tile at m0 and the 128 keys holding
+// key block nb, for (batch, head) bh.
+template <int BN>
+__device__ __forceinline__ bool layout_bit(int bh, int m0, int nb, const PrefillParams& p) {
+  const size_t row = static_cast<size_t>(bh % p.H) * p.lnqb + m0 / kTile;
+  return p.layout[row * p.lnkb + (nb * BN) / 128] != 0;
+}
+
 // True when every (row, key) pair of the 128-row tile at m0 and key block nb is in range
 // and visible.
 template <int BN>
-__device__ __forceinline__ bool tile_full(int m0, int nb, int sk, const PrefillParams& p) {
+__device__ __forceinline__ bool tile_full(int m0, int nb, int sk, int bh,
+                                          const PrefillParams& p) {
   const int n0 = nb * BN, n1 = n0 + BN;
   if (m0 + kTile > p.Sq || n1 > sk) return false;
   if (p.mask_mode == FA_MASK_NONE) return true;
+  if (p.mask_mode == FA_MASK_BLOCK_SPARSE) return layout_bit<BN>(bh, m0, nb, p);
   const int delta = sk - p.Sq;
   const int r_lo = m0 + delta, r_hi = m0 + kTile - 1 + delta;
   if (p.mask_mode == FA_MASK_BAND)  // the largest |pos - j| of the tile is within w
@@ -115,7 +125,7 @@ __device__ __forceinline__ bool softmax_cols(uint32_t t_lane, uint32_t s_col, ui
   tmem_ld_wait<NC>(s);
   if (!full) {
     int lim = min(pos_q, sk - 1) - n0;
-    if (p.mask_mode == FA_MASK_NONE) lim = sk - 1 - n0;
+    if (p.mask_mode == FA_MASK_NONE || p.mask_mode == FA_MASK_BLOCK_SPARSE) lim = sk - 1 - n0;
     int lo = INT_MIN, gl = INT_MIN;
     if (p.mask_mode == FA_MASK_CAUSAL_WINDOW) {
       lo = pos_q - p.window + 1 - n0;
@@ -439,7 +449,7 @@ __global__ void __launch_bounds__(kThreads256, 1)
         if (t < 0) continue;
         int bh, mb;
         item_coords(t, p, bh, mb);
-        const Range rg = key_range(mb * BM, min(mb * BM + BM, p.Sq), BN, item_sk(p, bh), p);
+        const Range rg = key_range(mb * BM, min(mb * BM + BM, p.Sq), BN, item_sk(p, bh), p, bh);
         const int n = range_count(rg);
         if (n == 0) continue;
         for (int q = 0; q < 2 && ok; ++q) {
@@ -450,14 +460,16 @@ __global__ void __launch_bounds__(kThreads256, 1)
                         c * 64, mb * BM + q * kTile, bh);
           qfills[q] = ii + 1;
         }
+        int nb = -1;
         for (int s = 0; s < 2 * n && ok; ++s) {  // K0, V0, K1, V1, ...
+          if ((s & 1) == 0) nb = range_next(rg, nb);
           const int slot = pos % C::NSLOT;
           const uint32_t use = pos / C::NSLOT;
           if (!(ok = mbar_wait(B(bars->empty[slot]), (use & 1) ^ 1, wc))) break;
           const uint32_t dst = sRing + slot * C::TILE_BYTES;
           if (leader) mbar_arrive_expect_tx(B(bars->full[slot]), C::TILE_BYTES);
           int y, z;
-          kv_tile_coords(p, bh, range_nb(rg, s / 2) * BN, leader, y, z);
+          kv_tile_coords(p, bh, nb * BN, leader, y, z);
           const void* map = (s & 1) ? (const void*)&tmV : (const void*)&tmK;
           if (leader)
             for (int c = 0; c < C::KCH; ++c)
@@ -488,7 +500,7 @@ __global__ void __launch_bounds__(kThreads256, 1)
         if (t < 0) continue;
         int bh, mb;
         item_coords(t, p, bh, mb);
-        const Range rg = key_range(mb * BM, min(mb * BM + BM, p.Sq), BN, item_sk(p, bh), p);
+        const Range rg = key_range(mb * BM, min(mb * BM + BM, p.Sq), BN, item_sk(p, bh), p, bh);
         const int n = range_count(rg);
         if (n == 0) continue;
         {  // S_A(0), S_B(0) with K0
@@ -563,7 +575,7 @@ __global__ void __launch_bounds__(kThreads256, 1)
       int bh, mb;
       item_coords(t, p, bh, mb);
       const int sk = item_sk(p, bh);
-      const Range rg = key_range(mb * BM, min(mb * BM + BM, p.Sq), BN, sk, p);
+      const Range rg = key_range(mb * BM, min(mb * BM + BM, p.Sq), BN, sk, p, bh);
       const int n = range_count(rg);
       const int m0 = mb * BM + q * kTile;  // first row of this tile
       const int qrow = m0 + row;
@@ -572,12 +584,17 @@ __global__ void __launch_bounds__(kThreads256, 1)
         if (qrow < p.Sq) store_zero_row<D>(orow, p);
         continue;
       }
-      const Range mine = key_range(m0, min(m0 + kTile, p.Sq), BN, sk, p);
+      const Range mine = key_range(m0, min(m0 + kTile, p.Sq), BN, sk, p, bh);
       const int pos_q = qrow + sk - p.Sq;  // key position of this query
       float m_ref = -INFINITY, l = 0.f;
+      int nb = -1;
       for (int j = 0; j < n; ++j) {
-        const int nb = range_nb(rg, j);
-        const bool full = tile_full<BN>(m0, nb, sk, p);
+        nb = range_next(rg, nb);
+        const bool full = tile_full<BN>(m0, nb, sk, bh, p);
+        // a block-sparse item visits the blocks of either tile: one that is off for this
+        // tile is masked whole (as if it held no key)
+        const bool off = p.mask_mode == FA_MASK_BLOCK_SPARSE && !range_has(mine, nb);
+        const int sk_t = off ? nb * BN : sk;
         ok = mbar_wait(B(bars->s_full[q]), tc & 1, wc);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
@@ -587,8 +604,8 @@ __global__ void __launch_bounds__(kThreads256, 1)
                                m0 / kTile) * p.nnb + nb,
                     16 + (full ? 2 : 1));
         // S(j) was issued after PV(j-1), so O needs no wait before a rescale
-        ok = softmax_tile<D, BN, BF16>(t_lane, s_col, o_col, full, nb * BN, pos_q, sk, p, m_ref, l,
-                                       [] { return true; });
+        ok = softmax_tile<D, BN, BF16>(t_lane, s_col, o_col, full, nb * BN, pos_q, sk_t, p,
+                                       m_ref, l, [] { return true; });
         tc_fence_before();
         mbar_arrive(B(bars->p_full[q]));
         ++tc;
@@ -685,7 +702,7 @@ __device__ __forceinline__ bool next_item(const PrefillSched& s, const PrefillPa
     if (t < 0) continue;
     item_coords(t, p, it.bh, it.mb);
     it.sk = item_sk(p, it.bh);
-    it.rg = key_range(it.mb * BM, min(it.mb * BM + BM, p.Sq), BN, it.sk, p);
+    it.rg = key_range(it.mb * BM, min(it.mb * BM + BM, p.Sq), BN, it.sk, p, it.bh);
     it.n = range_count(it.rg);
     if (it.n > 0 || with_empty) return true;
   }
@@ -789,7 +806,7 @@ __global__ void __launch_bounds__(kThreads128, 1)
         }
         qfills[qb] = (idx >> 1) + 1;
       };
-      auto emit = [&](const ItemRef& it, int j, bool is_v) {
+      auto emit = [&](const ItemRef& it, int nb, bool is_v) {
         const int slot = pos % C::NSLOT;
         if constexpr (!C::kRelease) {
           if (!(ok = mbar_wait(B(bars->empty[slot]), ((pos / C::NSLOT) & 1) ^ 1, wc))) return;
@@ -809,7 +826,7 @@ __global__ void __launch_bounds__(kThreads128, 1)
         const uint32_t dst = sRing + slot * C::TILE_BYTES;
         if (leader) mbar_arrive_expect_tx(B(bars->full[slot]), C::TILE_BYTES);
         int y, z;
-        kv_tile_coords(p, it.bh, range_nb(it.rg, j) * BN, leader, y, z);
+        kv_tile_coords(p, it.bh, nb * BN, leader, y, z);
         const void* map = is_v ? (const void*)&tmV : (const void*)&tmK;
         if (leader)
           for (int c = 0; c < C::KCH; ++c)
@@ -818,23 +835,29 @@ __global__ void __launch_bounds__(kThreads128, 1)
         ++pos;
       };
       bool has = next_item<BM>(sched, p, cta, G, BN, kc, cur, false);
+      int nb_cur = -1;  // key block of the current tile
       if (has) {
         load_q(cur, 0);
-        if (ok) emit(cur, 0, false);
+        nb_cur = range_next(cur.rg, -1);
+        if (ok) emit(cur, nb_cur, false);
       }
       while (has && ok) {
         bool has_nxt = false;
         for (int j = 0; j < cur.n && ok; ++j) {
+          int nb_next = -1;  // key block of the following tile
           if (j + 1 < cur.n) {
-            emit(cur, j + 1, false);
+            nb_next = range_next(cur.rg, nb_cur);
+            emit(cur, nb_next, false);
           } else {
             has_nxt = next_item<BM>(sched, p, cta, G, BN, kc, nxt, false);
             if (has_nxt) {
               load_q(nxt, ii + 1);
-              if (ok) emit(nxt, 0, false);
+              nb_next = range_next(nxt.rg, -1);
+              if (ok) emit(nxt, nb_next, false);
             }
           }
-          if (ok) emit(cur, j, true);
+          if (ok) emit(cur, nb_cur, true);
+          nb_cur = nb_next;
         }
         ++ii;
         cur = nxt;
@@ -976,9 +999,10 @@ __global__ void __launch_bounds__(kThreads128, 1)
       const int m0 = it.mb * BM;
       const int pos_q = m0 + row + it.sk - p.Sq;  // key position of this query
       float m_ref = -INFINITY, l = 0.f;
+      int nb = -1;
       for (int j = 0; j < it.n; ++j, ++g) {
-        const int nb = range_nb(it.rg, j);
-        const bool full = tile_full<BN>(m0, nb, it.sk, p);
+        nb = range_next(it.rg, nb);
+        const bool full = tile_full<BN>(m0, nb, it.sk, it.bh, p);
         ok = mbar_wait(B(bars->s_full[g & 1]), (g >> 1) & 1, wc);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;

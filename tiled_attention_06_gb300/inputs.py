@@ -92,3 +92,19 @@ def decode_inputs(B=32, H=32, d=128, page_size=256, num_pages=1200, max_ctx=8192
             kp[pg, :, tail:, :] = float("nan")
             vp[pg, :, tail:, :] = float("nan")
     return DecodeInputs(q, kp, vp, table, ctx.to(torch.int32), page_size)
+
+
+def block_layout(H, Sq, Sk, block=128, local=1, n_global=1, n_random=2, seed=0):
+    """Seeded block-sparse layout uint8 [H, ceil(Sq/block), ceil(Sk/block)] with the
+    BigBird shape: per head, block (i, j) is on when |i - j| <= local, when i or j is one
+    of the first n_global blocks, or when j is one of n_random blocks drawn for row i."""
+    nq, nk = -(-Sq // block), -(-Sk // block)
+    g = torch.Generator().manual_seed(seed)
+    i = torch.arange(nq)[:, None]
+    j = torch.arange(nk)[None, :]
+    base = ((i - j).abs() <= local) | (i < n_global) | (j < n_global)
+    lay = base.expand(H, nq, nk).clone()
+    if n_random > 0 and nk > 0:
+        pick = torch.rand(H, nq, nk, generator=g).argsort(dim=-1)[..., :min(n_random, nk)]
+        lay.scatter_(-1, pick, True)
+    return lay.to(torch.uint8)
