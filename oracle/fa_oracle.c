@@ -40,6 +40,10 @@
  *                          invariance
  *   or_count_visible_layout / or_tile_class_layout
  *                          pinned by closed-form counts and hand-classified grids
+ *   or_attention_backward  pinned by central finite differences of or_attention in
+ *                          FP64, by torch autograd on SDPA in float64 with an explicit
+ *                          mask, and by closed forms (zero queries: dK = 0; a row with one
+ *                          visible key: dQ = 0; rows of dS sum to 0)
  */
 #include "fa_oracle.h"
 
@@ -704,4 +708,104 @@ int or_tile_class_layout(int64_t h, int64_t mb, int64_t nb, int64_t BM, int64_t 
     if (vis == 0) return OR_TILE_EMPTY;
     if (vis == BM * BN) return OR_TILE_FULL;
     return OR_TILE_PARTIAL;
+}
+
+/* ------------------------------------------------------------------ */
+/* backward                                                            */
+/* ------------------------------------------------------------------ */
+
+/*
+ * Gradients of O = softmax(scale Q K^T + mask) V for an upstream gradient dO: the
+ * backward pass that the pages' remark on re-reading the scores refers to (they print
+ * no formula), written out by the chain rule per (batch, head) and row i:
+ *   s_ij = scale Q_i.K_j and P_ij = exp(s_ij - LSE_i) over the visible j,
+ *   dV_j += P_ij dO_i,   dP_ij = dO_i.V_j,   D_i = sum_j P_ij dP_ij,
+ *   dS_ij = P_ij (dP_ij - D_i),   dQ_i = scale sum_j dS_ij K_j,   dK_j += scale dS_ij Q_i.
+ * Inputs q, k, v, dout share one dtype; dq [B,H,Sq,d], dk and dv [B,H,Sk,d] are FP64.
+ * A row that sees no key contributes nothing. Returns 0, or -1 on a bad argument.
+ */
+int or_attention_backward(const void* q, const void* k, const void* v, const void* dout,
+                          int dtype, double* dq, double* dk, double* dv, int64_t B, int64_t H,
+                          int64_t Sq, int64_t Sk, int64_t d, double scale, int mask_mode,
+                          int64_t window, int64_t n_global, int nthreads) {
+    if (B < 0 || H < 0 || Sq < 0 || Sk < 0 || d <= 0) return -1;
+    if (mask_mode < OR_MASK_NONE || mask_mode > OR_MASK_PREFIX_LM) return -1;
+    if (mask_mode == OR_MASK_CAUSAL_WINDOW && (window < 1 || n_global < 0)) return -1;
+    if (mask_mode == OR_MASK_BAND && window < 0) return -1;
+    if (mask_mode == OR_MASK_PREFIX_LM && n_global < 0) return -1;
+    memset(dq, 0, sizeof(double) * (size_t)(B * H * Sq * d));
+    memset(dk, 0, sizeof(double) * (size_t)(B * H * Sk * d));
+    memset(dv, 0, sizeof(double) * (size_t)(B * H * Sk * d));
+#ifdef _OPENMP
+    if (nthreads <= 0) nthreads = omp_get_max_threads();
+#pragma omp parallel num_threads(nthreads)
+#endif
+    {
+        const size_t kc = (size_t)(Sk > 0 ? Sk : 1);
+        double* qd = (double*)malloc(sizeof(double) * (size_t)(Sq > 0 ? Sq : 1) * (size_t)d);
+        double* gd = (double*)malloc(sizeof(double) * (size_t)(Sq > 0 ? Sq : 1) * (size_t)d);
+        double* kd = (double*)malloc(sizeof(double) * kc * (size_t)d);
+        double* vd = (double*)malloc(sizeof(double) * kc * (size_t)d);
+        double* s = (double*)malloc(sizeof(double) * kc);
+        double* dp = (double*)malloc(sizeof(double) * kc);
+        int64_t* vis = (int64_t*)malloc(sizeof(int64_t) * kc);
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 1)
+#endif
+        for (int64_t bh = 0; bh < B * H; ++bh) {
+            or_decode((const char*)q + (size_t)(bh * Sq * d) * elem_size(dtype), qd, Sq * d, dtype);
+            or_decode((const char*)dout + (size_t)(bh * Sq * d) * elem_size(dtype), gd, Sq * d,
+                      dtype);
+            or_decode((const char*)k + (size_t)(bh * Sk * d) * elem_size(dtype), kd, Sk * d, dtype);
+            or_decode((const char*)v + (size_t)(bh * Sk * d) * elem_size(dtype), vd, Sk * d, dtype);
+            double* dqb = dq + bh * Sq * d;
+            double* dkb = dk + bh * Sk * d;
+            double* dvb = dv + bh * Sk * d;
+            for (int64_t i = 0; i < Sq; ++i) {
+                const double* qi = qd + i * d;
+                const double* gi = gd + i * d;
+                int64_t n = 0;
+                double m = -INFINITY;
+                for (int64_t j = 0; j < Sk; ++j) {
+                    if (!or_visible(i, j, Sq, Sk, mask_mode, window, n_global)) continue;
+                    double dot = 0.0;
+                    for (int64_t c = 0; c < d; ++c) dot += qi[c] * kd[j * d + c];
+                    vis[n] = j;
+                    s[n] = scale * dot;
+                    if (s[n] > m) m = s[n];
+                    ++n;
+                }
+                if (n == 0) continue;
+                double z = 0.0;
+                for (int64_t t = 0; t < n; ++t) z += exp(s[t] - m);
+                const double lse = m + log(z);
+                double D = 0.0;
+                for (int64_t t = 0; t < n; ++t) {
+                    const int64_t j = vis[t];
+                    s[t] = exp(s[t] - lse); /* P_ij */
+                    double g = 0.0;
+                    for (int64_t c = 0; c < d; ++c) g += gi[c] * vd[j * d + c];
+                    dp[t] = g;
+                    D += s[t] * g;
+                }
+                for (int64_t t = 0; t < n; ++t) {
+                    const int64_t j = vis[t];
+                    const double p = s[t], ds = p * (dp[t] - D);
+                    for (int64_t c = 0; c < d; ++c) {
+                        dvb[j * d + c] += p * gi[c];
+                        dqb[i * d + c] += scale * ds * kd[j * d + c];
+                        dkb[j * d + c] += scale * ds * qi[c];
+                    }
+                }
+            }
+        }
+        free(qd);
+        free(gd);
+        free(kd);
+        free(vd);
+        free(s);
+        free(dp);
+        free(vis);
+    }
+    return 0;
 }

@@ -81,6 +81,13 @@ int64_t or_count_visible_layout(int64_t H, int64_t Sq, int64_t Sk, const uint8_t
 int or_tile_class_layout(int64_t h, int64_t mb, int64_t nb, int64_t BM, int64_t BN,
                          int64_t Sq, int64_t Sk, const uint8_t* layout, int64_t blk);
 
+/* Gradients dq [B,H,Sq,d], dk and dv [B,H,Sk,d] (FP64) of attention for the upstream
+   gradient dout [B,H,Sq,d] (same dtype as q, k, v), by the chain rule. */
+int or_attention_backward(const void* q, const void* k, const void* v, const void* dout,
+                          int dtype, double* dq, double* dk, double* dv, int64_t B, int64_t H,
+                          int64_t Sq, int64_t Sk, int64_t d, double scale, int mask_mode,
+                          int64_t window, int64_t n_global, int nthreads);
+
 void or_combine_partials(const double* m, const double* l, const double* acc,
                          int64_t nsplit, int64_t d, double* o, double* lse);
 

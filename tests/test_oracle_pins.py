@@ -676,3 +676,83 @@ def test_layout_counts_and_tile_classes():
                for mb in range(2)]
     assert classes == [[oracle.TILE_FULL, oracle.TILE_EMPTY],
                        [oracle.TILE_PARTIAL, oracle.TILE_PARTIAL]]
+
+
+# --------------------------------------------------------------------------- #
+# backward                                                                    #
+# --------------------------------------------------------------------------- #
+
+def _explicit_mask(Sq, Sk, mode, w, g):
+    """Visibility built here from index arithmetic (query i at key position i + Sk - Sq)."""
+    i = torch.arange(Sq)[:, None] + (Sk - Sq)
+    j = torch.arange(Sk)[None, :]
+    if mode == MASK_NONE:
+        return torch.ones(Sq, Sk, dtype=torch.bool)
+    if mode == MASK_CAUSAL:
+        return j <= i
+    if mode == MASK_CAUSAL_WINDOW:
+        return (j <= i) & ((i - j < w) | (j < g))
+    if mode == MASK_BAND:
+        return (j - i).abs() <= w
+    return (j <= i) | (j < g)  # prefix-LM
+
+
+@pytest.mark.parametrize("mode,w,g", [(MASK_NONE, 0, 0), (MASK_CAUSAL, 0, 0),
+                                      (MASK_CAUSAL_WINDOW, 5, 2), (MASK_BAND, 3, 0),
+                                      (MASK_PREFIX_LM, 0, 4)])
+@pytest.mark.parametrize("Sq,Sk", [(17, 17), (9, 23), (23, 9)])
+def test_backward_matches_autograd(mode, w, g, Sq, Sk):
+    gen = torch.Generator().manual_seed(Sq * 31 + Sk + mode)
+    q, k, v, do = (torch.randn(2, 3, n, 16, generator=gen).to(torch.bfloat16)
+                   for n in (Sq, Sk, Sk, Sq))
+    dq, dk, dv = oracle.attention_backward(q, k, v, do, 0.3, mode, w, g)
+    mask = _explicit_mask(Sq, Sk, mode, w, g)
+    seen = mask.any(-1)
+    qq, kk, vv = (t.double().requires_grad_() for t in (q, k, v))
+    o = torch.nn.functional.scaled_dot_product_attention(qq, kk, vv, attn_mask=mask, scale=0.3)
+    # rows that see no key give NaN in SDPA and contribute nothing by definition
+    o = torch.where(seen[None, None, :, None], o, torch.zeros_like(o))
+    o.backward(do.double())
+    for got, ref in ((dq, qq.grad), (dk, kk.grad), (dv, vv.grad)):
+        ref = torch.nan_to_num(ref, nan=0.0).numpy()
+        np.testing.assert_allclose(got, ref, rtol=0, atol=1e-12)
+
+
+def test_backward_central_differences():
+    """dL/dx for L = sum(G * O) by central differences of the FP64 forward."""
+    gen = torch.Generator().manual_seed(5)
+    q, k, v, G = (torch.randn(1, 2, n, 4, generator=gen, dtype=torch.float64)
+                  for n in (6, 7, 7, 6))
+    dq, dk, dv = oracle.attention_backward(q, k, v, G, 0.7, MASK_CAUSAL)
+    eps = 1e-6
+
+    def loss(qx, kx, vx):
+        o, _ = oracle.attention(qx, kx, vx, 0.7, MASK_CAUSAL)
+        return float((o * G.numpy()).sum())
+
+    for which, grad in ((0, dq), (1, dk), (2, dv)):
+        for idx in [(0, 0, 0, 0), (0, 1, 3, 2), (0, 1, 5, 3)]:
+            plus = [t.clone() for t in (q, k, v)]
+            minus = [t.clone() for t in (q, k, v)]
+            plus[which][idx] += eps
+            minus[which][idx] -= eps
+            fd = (loss(*plus) - loss(*minus)) / (2 * eps)
+            assert abs(fd - grad[idx]) < 1e-7, (which, idx, fd, grad[idx])
+
+
+def test_backward_closed_forms():
+    gen = torch.Generator().manual_seed(9)
+    q, k, v, do = (torch.randn(1, 2, 8, 8, generator=gen).to(torch.float16) for _ in range(4))
+    # zero queries: every score is 0, dK = scale * sum_i dS_ij Q_i = 0
+    _, dk, _ = oracle.attention_backward(torch.zeros_like(q), k, v, do, 0.5, MASK_NONE)
+    assert np.all(dk == 0)
+    # one visible key (causal row 0): P = 1, dS = 0, so dQ_0 = 0 and dV_0 gets dO_0 from it
+    dq, _, dv = oracle.attention_backward(q, k, v, do, 0.5, MASK_CAUSAL)
+    assert np.all(dq[:, :, 0] == 0)
+    # identical keys: dQ_i = scale * K * sum_j dS_ij = 0 because each row of dS sums to 0
+    kc = k[:, :, :1].expand(-1, -1, 8, -1).contiguous()
+    dq, _, _ = oracle.attention_backward(q, kc, v, do, 0.5, MASK_NONE)
+    np.testing.assert_allclose(dq, 0.0, atol=1e-13)
+    # a row's dV contributions sum to dO_i: sum_j dV_j = sum_i dO_i (P rows sum to 1)
+    _, _, dv = oracle.attention_backward(q, k, v, do, 0.5, MASK_NONE)
+    np.testing.assert_allclose(dv.sum(axis=2), do.double().numpy().sum(axis=2), atol=1e-12)
