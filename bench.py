@@ -65,7 +65,8 @@ MODE_NAME = {0: "none", 1: "causal", 2: "causal_window", 3: "band", 4: "prefix_l
 NCU_TRAFFIC = {
     # prefill_bm256_kernel, causal 4k B4 H16 capture: 210.3 MB read + 45.0 MB written,
     # scaled x2 to B4 H32
-    "prefill": {"bytes": 510.6e6, "sources": ['fa_prefill.cu', 'fa_ptx.cuh', 'fa_plan.h', 'fa_internal.h'],
+    "prefill": {"bytes": 510.6e6,
+                "sources": ['fa_prefill.cu', 'fa_mma.cuh', 'fa_ptx.cuh', 'fa_plan.h', 'fa_internal.h'],
                 "sha256": "263ae657df70fa1a5e1478f561972a8fc09a654a0429156dce7227aaeceb93dc"},
     # paged decode B8 capture: 547.5 MB read + 3.7 MB written for 547.5 MB algorithmic,
     # scaled to the bench call's 2410.7 MB algorithmic

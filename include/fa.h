@@ -141,6 +141,26 @@ int fa_fwd_block_m(void);
 int fa_fwd_default_block_m(int mask_mode);
 
 /*
+ * fa_bwd - gradients of fa_fwd for an upstream gradient dout: with P the softmax of
+ * fa_fwd (recomputed from the saved LSE, as the pages' remark on re-reading the scores in
+ * the backward pass implies; zwxr.cn article on ops-transformer, section 3.1) and
+ * D_i = dout_i . o_i,
+ *     dv = P^T dout,  dS = P (dout v^T - D),  dq = scale dS k,  dk = scale dS^T q.
+ *   q, o, dout, dq [B, H, Sq, d]; k, v, dk, dv [B, H, Sk, d]: dtype, contiguous, device
+ *   lse        [B, H, Sq] float32, the natural-log LSE that fa_fwd returned with o
+ *   workspace  device scratch of at least fa_bwd_workspace_size(B, H, Sq) bytes, 16-byte
+ *              aligned, owned by the caller (holds D)
+ *   d, scale, mask_mode / window / n_global, dtype as for fa_fwd; FA_MASK_BLOCK_SPARSE is
+ *   FA_ERR_UNSUPPORTED. dq, dk and dv are written (RN from FP32 accumulators); a key no
+ *   query sees gets dk = dv = 0, a query that sees no key dq = 0.
+ */
+size_t fa_bwd_workspace_size(int B, int H, int Sq);
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                 const float* lse, void* dq, void* dk, void* dv, void* workspace,
+                 size_t workspace_bytes, int B, int H, int Sq, int Sk, int d, float scale,
+                 int mask_mode, int window, int n_global, int dtype, fa_stream_t stream);
+
+/*
  * fa_decode_paged - one query token per sequence against a paged KV cache
  * ("ascend-transformer-boost 实战" (ai6s.net), scenario 2: the cache is cut into
  * fixed-size pages, 256 tokens in the pages' example, and new pages are taken as a

@@ -179,3 +179,23 @@ def test_merge_rejects_bad_arguments(L):
     assert L.fa_merge_partials(A, A, A, A, A, None, -1, 64, 0, None) == fa.FA_ERR_INVALID_ARG
     assert L.fa_merge_partials(None, None, None, None, None, None, 0, 64, 0, None) == fa.FA_OK
 
+
+
+def test_bwd_rejects_bad_arguments(L):
+    A = 1 << 20  # a 16-byte-aligned fake address; nothing is launched
+    base = dict(q=A, k=A, v=A, o=A, dout=A, lse=A, dq=A, dk=A, dv=A, ws=A, wsb=1 << 20, B=1,
+                H=2, Sq=64, Sk=64, d=64, scale=0.125, mode=0, w=0, g=0, dtype=0)
+
+    def call(**kw):
+        a = dict(base, **kw)
+        return L.fa_bwd(a["q"], a["k"], a["v"], a["o"], a["dout"], a["lse"], a["dq"], a["dk"],
+                        a["dv"], a["ws"], a["wsb"], a["B"], a["H"], a["Sq"], a["Sk"], a["d"],
+                        a["scale"], a["mode"], a["w"], a["g"], a["dtype"], None)
+    assert call(mode=5) == fa.FA_ERR_UNSUPPORTED
+    assert call(d=96) == fa.FA_ERR_UNSUPPORTED
+    assert call(ws=None) == fa.FA_ERR_INVALID_ARG
+    assert call(wsb=16) == fa.FA_ERR_INVALID_ARG
+    assert call(dout=None) == fa.FA_ERR_INVALID_ARG
+    assert call(dk=A + 8) == fa.FA_ERR_INVALID_ARG
+    assert call(mode=2, w=0) == fa.FA_ERR_INVALID_ARG
+    assert L.fa_bwd_workspace_size(2, 3, 100) == 2 * 3 * 100 * 4

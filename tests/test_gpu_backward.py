@@ -1,0 +1,107 @@
+"""GPU parity of fa_bwd (through the C ABI) against the FP64 oracle's backward.
+
+Tolerance: P and dS are rounded to the 16-bit input type before their MMAs (relative error
+2^-9 for bf16, 2^-12 for fp16) and dq, dk, dv once more on output, with FP32 accumulation;
+errors of the summed terms are independent, so the error relative to the tensor's scale
+stays near 2^-8. Checked: max |err| <= 2e-2 * max |ref| and mean |err| <= 4e-3 * mean |ref|
+for every gradient tensor; exact zeros where no tile contributes (a key no query sees, a
+query that sees no key), and |err| <= 1e-5 where the definition's zero is a cancellation
+(one visible key: dP - D = dO.V - dO.O with O = V)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import tiled_attention_06_gb300 as fa
+from tiled_attention_06_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+DT = {"f16": torch.float16, "bf16": torch.bfloat16}
+MASKS = {"none": (fa.FA_MASK_NONE, 0, 0), "causal": (fa.FA_MASK_CAUSAL, 0, 0),
+         "window": (fa.FA_MASK_CAUSAL_WINDOW, 50, 5), "band": (fa.FA_MASK_BAND, 40, 0),
+         "prefix": (fa.FA_MASK_PREFIX_LM, 0, 70)}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from tiled_attention_06_gb300 import build
+    build.build()
+    fa.lib()
+
+
+def fwd_bwd(q, k, v, dout, scale, mode, w, g):
+    dev = torch.device("cuda")
+    qd, kd, vd, gd = q.to(dev), k.to(dev), v.to(dev), dout.to(dev)
+    o = torch.empty_like(qd)
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+    fa.fa_fwd(qd, kd, vd, o, lse, scale, mode, w, g)
+    dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+    B, H, Sq, _ = q.shape
+    ws = torch.empty(max(fa.fa_bwd_workspace_size(B, H, Sq), 16), dtype=torch.uint8, device=dev)
+    fa.fa_bwd(qd, kd, vd, o, gd, lse, dq, dk, dv, ws, scale, mode, w, g)
+    torch.cuda.synchronize()
+    assert fa.fa_get_device_status() == fa.FA_OK
+    return dq.float().cpu().numpy(), dk.float().cpu().numpy(), dv.float().cpu().numpy()
+
+
+def compare_grad(got, ref, what):
+    assert np.all(np.isfinite(got)), f"{what}: non-finite"
+    err = np.abs(got - ref)
+    scale = np.abs(ref)
+    if scale.max() == 0:  # zero by cancellation (dP - D): FP32 rounding of the two terms
+        assert err.max() <= 1e-5, f"{what}: want ~0, max |got| {err.max():.3e}"
+        return
+    assert err.max() <= 2e-2 * scale.max(), f"{what}: max err {err.max():.3e} vs {scale.max():.3e}"
+    assert err.mean() <= 4e-3 * scale.mean(), \
+        f"{what}: mean err {err.mean():.3e} vs mean |ref| {scale.mean():.3e}"
+
+
+def check(q, k, v, dout, scale, mask, what):
+    mode, w, g = MASKS[mask]
+    dq, dk, dv = fwd_bwd(q, k, v, dout, scale, mode, w, g)
+    rq, rk, rv = oracle.attention_backward(q, k, v, dout, scale, mode, w, g)
+    compare_grad(dq, rq, what + " dq")
+    compare_grad(dk, rk, what + " dk")
+    compare_grad(dv, rv, what + " dv")
+
+
+SHAPES = [(1, 1), (64, 64), (127, 129), (129, 127), (200, 333), (333, 200), (384, 384)]
+
+
+@pytest.mark.parametrize("Sq,Sk", SHAPES)
+@pytest.mark.parametrize("d,dt", [(64, "f16"), (128, "bf16")])
+@pytest.mark.parametrize("mask", list(MASKS))
+def test_backward_small_shapes(Sq, Sk, d, dt, mask):
+    q, k, v = inputs.prefill_inputs(2, 2, Sq, Sk, d, DT[dt], seed=Sq * 10 + Sk)
+    dout = inputs.prefill_inputs(2, 2, Sq, Sq, d, DT[dt], seed=Sq + 99)[0]
+    check(q, k, v, dout, 1 / math.sqrt(d), mask, f"{Sq}x{Sk} d{d} {dt} {mask}")
+
+
+def test_backward_empty_sides():
+    q, k, v = inputs.prefill_inputs(1, 2, 0, 130, 64, torch.float16, seed=1)
+    dout = torch.zeros(1, 2, 0, 64, dtype=torch.float16)
+    dq, dk, dv = fwd_bwd(q, k, v, dout, 0.125, fa.FA_MASK_NONE, 0, 0)
+    assert np.all(dk == 0) and np.all(dv == 0)  # no query: every key's gradients are 0
+    q, k, v = inputs.prefill_inputs(1, 2, 70, 0, 64, torch.float16, seed=2)
+    dout = inputs.prefill_inputs(1, 2, 70, 70, 64, torch.float16, seed=3)[0]
+    dq, dk, dv = fwd_bwd(q, k, v, dout, 0.125, fa.FA_MASK_NONE, 0, 0)
+    assert np.all(dq == 0)
+
+
+def test_backward_rows_without_keys():
+    """Sq > Sk under a causal mask: the first Sq - Sk queries see no key."""
+    q, k, v = inputs.prefill_inputs(1, 2, 300, 100, 128, torch.bfloat16, seed=4)
+    dout = inputs.prefill_inputs(1, 2, 300, 300, 128, torch.bfloat16, seed=5)[0]
+    dq, _, _ = fwd_bwd(q, k, v, dout, 0.088, fa.FA_MASK_CAUSAL, 0, 0)
+    assert np.all(dq[:, :, :200] == 0)
+    check(q, k, v, dout, 0.088, "causal", "Sq > Sk")
+
+
+def test_backward_causal_2k_full():
+    """B=1, H=2, S=2048, d=128, bf16, causal: every gradient element against the oracle."""
+    q, k, v = inputs.prefill_inputs(1, 2, 2048, 2048, 128, torch.bfloat16, seed=0)
+    dout = inputs.prefill_inputs(1, 2, 2048, 2048, 128, torch.bfloat16, seed=1)[0]
+    check(q, k, v, dout, 1 / math.sqrt(128), "causal", "causal 2k")

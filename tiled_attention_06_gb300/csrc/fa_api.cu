@@ -549,6 +549,80 @@ fa_status fa_decode_paged_noalloc(const void* q, const void* k_pages, const void
   return FA_OK;
 }
 
+size_t fa_bwd_workspace_size(int B, int H, int Sq) {
+  if (B < 1 || H < 1 || Sq < 0) return 0;
+  return static_cast<size_t>(B) * H * (Sq > 0 ? Sq : 1) * sizeof(float);
+}
+
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                 const float* lse, void* dq, void* dk, void* dv, void* workspace,
+                 size_t workspace_bytes, int B, int H, int Sq, int Sk, int d, float scale,
+                 int mask_mode, int window, int n_global, int dtype, fa_stream_t stream) {
+  fa_fwd_params a;  // the forward's checks cover q, k, v, sizes, mask and dtype
+  std::memset(&a, 0, sizeof a);
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.o = dq;  // any non-null 16-byte-aligned output passes the output check
+  a.B = B;
+  a.H = H;
+  a.Sq = Sq;
+  a.Sk = Sk;
+  a.d = d;
+  a.scale = scale;
+  a.mask_mode = mask_mode;
+  a.window = window;
+  a.n_global = n_global;
+  a.dtype = dtype;
+  if (mask_mode == FA_MASK_BLOCK_SPARSE)
+    return fail(FA_ERR_UNSUPPORTED, "fa_bwd: block-sparse layouts are not supported");
+  fa_status st = check_fwd(a);
+  if (st != FA_OK) return st;
+  if (Sq == 0 && Sk == 0) return FA_OK;
+  if ((Sq > 0 && (!o || !dout || !lse || !dq)) || (Sk > 0 && (!dk || !dv)))
+    return fail(FA_ERR_INVALID_ARG, "o, dout, lse, dq, dk and dv must be non-null");
+  if (!aligned16(o) || !aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return fail(FA_ERR_INVALID_ARG, "o, dout, dq, dk and dv must be 16-byte aligned");
+  if (lse && !aligned4(lse)) return fail(FA_ERR_INVALID_ARG, "lse must be 4-byte aligned");
+  const size_t need = fa_bwd_workspace_size(B, H, Sq);
+  if (Sq > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace)))
+    return fail(FA_ERR_INVALID_ARG, "workspace: %zu bytes, 16-byte aligned, needed", need);
+  DeviceInfo dev;
+  if ((st = device_info(&dev)) != FA_OK) return st;
+  const int BH = B * H;
+  const bool bf16 = dtype == FA_BF16;
+  fa::BwdLaunch L;
+  std::memset(&L, 0, sizeof L);
+  fa::PrefillParams& p = L.p;
+  p.BH = BH;
+  p.H = H;
+  p.Sq = Sq;
+  p.Sk = Sk;
+  p.mask_mode = mask_mode;
+  p.window = (mask_mode == FA_MASK_CAUSAL_WINDOW || mask_mode == FA_MASK_BAND) ? window : 0;
+  p.n_global = (mask_mode == FA_MASK_CAUSAL_WINDOW || mask_mode == FA_MASK_PREFIX_LM) ? n_global : 0;
+  p.sl2 = scale * 1.4426950408889634f;
+  p.status = dev.status;
+  p.timeout_ns = 1000000000ull;
+  L.b.lse = lse;
+  L.b.dsum = static_cast<float*>(workspace);
+  L.b.dq = dq;
+  L.b.dk = dk;
+  L.b.dv = dv;
+  L.b.scale = scale;
+  L.o = o;
+  L.dout = dout;
+  const void* qmap = Sq ? q : k;  // a map needs a valid address even when nothing is loaded
+  const void* kmap = Sk ? k : q;
+  if ((st = make_map(&L.tmQ, qmap, bf16, d, Sq, BH, 128)) != FA_OK) return st;
+  if ((st = make_map(&L.tmdO, Sq ? dout : k, bf16, d, Sq, BH, 128)) != FA_OK) return st;
+  if ((st = make_map(&L.tmK, kmap, bf16, d, Sk, BH, 128)) != FA_OK) return st;
+  if ((st = make_map(&L.tmV, Sk ? v : q, bf16, d, Sk, BH, 128)) != FA_OK) return st;
+  cudaError_t e = fa::launch_backward(L, d, bf16, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "backward launch");
+  return FA_OK;
+}
+
 fa_status fa_merge_partials(const void* o_a, const float* lse_a, const void* o_b,
                             const float* lse_b, void* o, float* lse, int64_t rows, int d,
                             int dtype, fa_stream_t stream) {

@@ -1,0 +1,605 @@
+// FlashAttention backward for sm_103a: the gradients of O = softmax(scale Q K^T + mask) V,
+// recomputing the scores from the saved LSE instead of storing them (the reason the
+// pages give for re-reading the scores in the backward pass; "zwxr.cn article on
+// ops-transformer", section 3.1, and the ops-transformer overview, section 二.1).
+// Per (batch, head), with D_i = dO_i . O_i:
+//   P = exp(scale Q K^T - LSE), dV = P^T dO, dP = dO V^T, dS = P (dP - D),
+//   dQ = scale dS K, dK = scale dS^T Q.
+//
+// Three kernels, each step on the tensor cores where it is a contraction:
+//   bwd_prep_kernel   D_i, one FP32 per query row (HBM-bound).
+//   bwd_dkdv_kernel   one CTA per (batch*head, block of 128 keys); TMEM lane = key. For
+//                     each block of 128 queries that sees these keys: S^T = K Q^T and
+//                     dP^T = V dO^T (tcgen05, A and B from shared memory), P^T and
+//                     dS^T = P^T (dP^T - D) by the elementwise warpgroup, rounded to 16
+//                     bits over their own TMEM columns, then dV += P^T dO and
+//                     dK += dS^T Q (tcgen05, A from TMEM).
+//   bwd_dq_kernel     one CTA per (batch*head, block of 128 queries); TMEM lane = query.
+//                     For each block of 128 keys the queries see: S = Q K^T, dP = dO V^T,
+//                     dS = P (dP - D), dQ += dS K.
+// The dQ kernel recomputes S and dP rather than exchanging dS with the dK/dV kernel, so
+// no FP32 atomics and no second pass over dQ are needed.
+//
+// Roles (192 threads): warps 0-3 elementwise + epilogue (one TMEM lane per thread), warp 4
+// TMA, warp 5 MMA (warp-wide, one elected lane issues). Every wait is bounded.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <climits>
+#include <cstdint>
+
+#include "fa_internal.h"
+#include "fa_mma.cuh"
+#include "fa_plan.h"
+#include "fa_ptx.cuh"
+
+namespace fa {
+namespace {
+
+constexpr int kBT = 128;  // rows of a query or key tile
+constexpr int kBwdThreads = 192;
+constexpr int kBwdTmaWarp = 4;
+constexpr int kBwdMmaWarp = 5;
+
+template <int D>
+struct BwdCfg {
+  static constexpr int KCH = D / 64;
+  static constexpr int TILE = kBT * D * 2;  // one 128-row 16-bit tile
+  // two resident tiles + two stages of two streamed tiles + barriers, 1 KB aligned; at
+  // least half the SM's shared memory, so that one CTA (which takes all 512 TMEM columns)
+  // is resident per SM
+  static constexpr int SMEM_USED = 1024 + 6 * TILE + 1024;
+  static constexpr int SMEM = SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024;
+  static_assert(SMEM <= 232448, "shared memory over budget");
+};
+
+struct BwdBars {
+  uint64_t res_full;       // the CTA's resident tiles landed
+  uint64_t st_full[2];     // streamed tiles of stage s landed
+  uint64_t st_empty[2];    // MMAs done with stage s
+  uint64_t s_full;         // S and dP of the current tile in TMEM
+  uint64_t p_full;         // P and dS (16-bit) written back
+  uint64_t acc_full;       // every MMA of the CTA complete
+  uint32_t tmem_base;
+  uint32_t abort;
+};
+
+// Key positions are the query index plus delta = Sk - Sq (queries aligned to the last
+// Sq keys), as in the forward.
+
+// Keys visible to query i in the columns of the key tile at n0, as in the forward's
+// partial-tile mask: column c is visible iff c <= lim and (c >= lo or c < gl).
+struct ColMask {
+  int lim, lo, gl;
+};
+__device__ __forceinline__ ColMask key_cols(int i, int n0, int sk, const PrefillParams& p) {
+  ColMask m{INT_MIN, INT_MIN, INT_MIN};
+  if (i >= p.Sq) return m;  // lim = INT_MIN: nothing
+  const int pos = i + sk - p.Sq;
+  m.lim = min(pos, sk - 1) - n0;
+  switch (p.mask_mode) {
+    case FA_MASK_NONE:
+      m.lim = sk - 1 - n0;
+      break;
+    case FA_MASK_CAUSAL_WINDOW:
+      m.lo = pos - p.window + 1 - n0;
+      m.gl = p.n_global - n0;
+      break;
+    case FA_MASK_BAND: {
+      const long long hi = static_cast<long long>(pos) + p.window;
+      m.lim = static_cast<int>((hi < sk - 1 ? hi : sk - 1) - n0);
+      const long long l0 = static_cast<long long>(pos) - p.window - n0;
+      m.lo = l0 < INT_MIN ? INT_MIN : static_cast<int>(l0);
+      break;
+    }
+    case FA_MASK_PREFIX_LM:
+      m.lim = min(max(pos, p.n_global - 1), sk - 1) - n0;
+      break;
+    default:
+      break;
+  }
+  return m;
+}
+
+// Queries that see key j, as the interval [lo, hi] of columns of the query tile at m0
+// (the transpose of the same masks); empty when lo > hi.
+struct RowSpan {
+  int lo, hi;
+};
+__device__ __forceinline__ RowSpan query_cols(int j, int m0, int sk, const PrefillParams& p) {
+  const long long delta = static_cast<long long>(sk) - p.Sq;
+  long long lo = 0, hi = static_cast<long long>(p.Sq) - 1;  // query indices
+  if (j >= sk) return RowSpan{1, 0};
+  switch (p.mask_mode) {
+    case FA_MASK_CAUSAL:  // pos >= j
+      lo = j - delta;
+      break;
+    case FA_MASK_CAUSAL_WINDOW:  // pos >= j and (pos - j < w or j < g)
+      lo = j - delta;
+      if (j >= p.n_global) hi = min(hi, j - delta + p.window - 1);
+      break;
+    case FA_MASK_BAND:  // |pos - j| <= w
+      lo = j - delta - p.window;
+      hi = min(hi, j - delta + p.window);
+      break;
+    case FA_MASK_PREFIX_LM:  // pos >= j or j < g
+      if (j >= p.n_global) lo = j - delta;
+      break;
+    default:
+      break;
+  }
+  if (lo < 0) lo = 0;
+  lo -= m0;
+  hi -= m0;
+  return RowSpan{static_cast<int>(lo < -1 ? -1 : (lo > kBT ? kBT : lo)),
+                 static_cast<int>(hi < -1 ? -1 : (hi > kBT ? kBT : hi))};
+}
+
+__device__ __forceinline__ void wait_quiet_b(uint32_t bar, uint32_t parity, const WaitCtx& wc) {
+  volatile uint32_t zero = 0;
+  WaitCtx w2 = wc;
+  w2.abort = &zero;
+  mbar_wait(bar, parity, w2);
+}
+
+// D_i = sum_c dO_ic O_ic in FP32: d/8 lanes per row, one 16-byte load of each per lane,
+// xor-shuffle reduction inside the row's lanes.
+template <int D, bool BF16>
+__global__ void __launch_bounds__(256) bwd_prep_kernel(const uint4* __restrict__ o,
+                                                       const uint4* __restrict__ dout,
+                                                       float* __restrict__ dsum, int64_t rows) {
+  constexpr int LPR = D / 8;  // lanes per row
+  constexpr int RPW = 32 / LPR;
+  const int lane = threadIdx.x % 32;
+  const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) / 32;
+  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * blockDim.x / 32;
+  for (int64_t r0 = warp * RPW; r0 < rows; r0 += nwarps * RPW) {
+    const int64_t row = r0 + lane / LPR;
+    float acc = 0.f;
+    if (row < rows) {
+      const uint4 a = o[row * LPR + lane % LPR], b = dout[row * LPR + lane % LPR];
+      const uint32_t* ap = reinterpret_cast<const uint32_t*>(&a);
+      const uint32_t* bp = reinterpret_cast<const uint32_t*>(&b);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        float2 x, y;
+        if (BF16) {
+          x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(ap + e));
+          y = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(bp + e));
+        } else {
+          x = __half22float2(*reinterpret_cast<const __half2*>(ap + e));
+          y = __half22float2(*reinterpret_cast<const __half2*>(bp + e));
+        }
+        acc += x.x * y.x + x.y * y.y;
+      }
+    }
+#pragma unroll
+    for (int off = LPR / 2; off > 0; off /= 2) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (row < rows && lane % LPR == 0) dsum[row] = acc;
+  }
+}
+
+// Does the query block qb see any key of key block kb (the forward's key ranges)?
+__device__ __forceinline__ bool tile_visited(int qb, int kb, int bh, const PrefillParams& p) {
+  const Range r = key_range(qb * kBT, min(qb * kBT + kBT, p.Sq), kBT, p.Sk, p, bh);
+  return range_has(r, kb);
+}
+
+// The next query block after qb that sees key block kb, or nqb.
+__device__ __forceinline__ int next_qb(int qb, int kb, int bh, const PrefillParams& p, int nqb) {
+  do {
+    ++qb;
+  } while (qb < nqb && !tile_visited(qb, kb, bh, p));
+  return qb;
+}
+
+template <int D, bool BF16>
+__device__ __forceinline__ void store_tile_row(void* out, size_t row, const uint32_t* v,
+                                               float mul, int c0) {
+  uint32_t pk[16];
+#pragma unroll
+  for (int e = 0; e < 16; ++e) {
+    const float a = __uint_as_float(v[2 * e]) * mul, b = __uint_as_float(v[2 * e + 1]) * mul;
+    pk[e] = BF16 ? cvt_pack_bf16(a, b) : cvt_pack_f16(a, b);
+  }
+  uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(out) + row * D + c0);
+#pragma unroll
+  for (int e = 0; e < 4; ++e) dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+}
+
+// Common CTA setup: barriers, TMEM, descriptor prefetch. Returns the TMEM base.
+__device__ __forceinline__ uint32_t bwd_setup(BwdBars* bars, const CUtensorMap* m0,
+                                              const CUtensorMap* m1, const CUtensorMap* m2,
+                                              const CUtensorMap* m3) {
+  const int warp = threadIdx.x / 32;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bars->res_full), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&bars->st_full[i]), 1);
+      mbar_init(smem_u32(&bars->st_empty[i]), 1);
+    }
+    mbar_init(smem_u32(&bars->s_full), 1);
+    mbar_init(smem_u32(&bars->p_full), 128);
+    mbar_init(smem_u32(&bars->acc_full), 1);
+    bars->abort = 0;
+    mbar_fence_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_u32(&bars->tmem_base), 512);
+    tmem_relinquish();
+  }
+  if (warp == kBwdTmaWarp && threadIdx.x % 32 == 0) {
+    tma_prefetch_desc(m0);
+    tma_prefetch_desc(m1);
+    tma_prefetch_desc(m2);
+    tma_prefetch_desc(m3);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  return bars->tmem_base;
+}
+
+__device__ __forceinline__ void bwd_teardown(uint32_t tmem) {
+  tc_fence_before();
+  __syncthreads();
+  if (threadIdx.x / 32 == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// dK and dV of one block of 128 keys. TMEM: S^T [0,128) (P^T packed over its first 64
+// columns), dP^T [128,256) (dS^T packed over [128,192)), dV [256,256+D), dK [256+D,256+2D).
+// Shared memory: K, V (resident), then (Q, dO) in two stages.
+template <int D, bool BF16>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ,
+                    const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV,
+                    const __grid_constant__ CUtensorMap tmdO, const PrefillParams p,
+                    const BwdParams b) {
+  using C = BwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (base - raw);
+  const uint32_t sK = base, sV = base + C::TILE;
+  const uint32_t sSt = base + 2 * C::TILE;  // stage s: Q at sSt + 2s TILE, dO one TILE on
+  BwdBars* bars = reinterpret_cast<BwdBars*>(smem + 6 * C::TILE);
+  auto B = [&](uint64_t& x) { return smem_u32(&x); };
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int nkb = (p.Sk + kBT - 1) / kBT, nqb = (p.Sq + kBT - 1) / kBT;
+  const int bh = blockIdx.x / nkb, kb = blockIdx.x % nkb;
+  const uint32_t tmem = bwd_setup(bars, &tmQ, &tmK, &tmV, &tmdO);
+  const WaitCtx wc{&bars->abort, p.status, p.timeout_ns};
+
+  if (warp == kBwdTmaWarp) {
+    // ------------------------------------------------------------ TMA
+    const bool leader = elect_one();
+    bool ok = true;
+    uint32_t fills[2] = {0, 0}, res = 0;
+    if (leader) {
+      mbar_arrive_expect_tx(B(bars->res_full), 2 * C::TILE);
+      for (int c = 0; c < C::KCH; ++c) {
+        tma_load_3d(sK + c * (kBT * 128), &tmK, B(bars->res_full), c * 64, kb * kBT, bh);
+        tma_load_3d(sV + c * (kBT * 128), &tmV, B(bars->res_full), c * 64, kb * kBT, bh);
+      }
+    }
+    res = 1;
+    int t = 0;
+    for (int qb = next_qb(-1, kb, bh, p, nqb); qb < nqb && ok; qb = next_qb(qb, kb, bh, p, nqb), ++t) {
+      const int s = t & 1;
+      if (t >= 2 && !(ok = mbar_wait(B(bars->st_empty[s]), ((t >> 1) - 1) & 1, wc))) break;
+      const uint32_t sq = sSt + 2 * s * C::TILE, sdo = sq + C::TILE;
+      if (leader) {
+        mbar_arrive_expect_tx(B(bars->st_full[s]), 2 * C::TILE);
+        for (int c = 0; c < C::KCH; ++c) {
+          tma_load_3d(sq + c * (kBT * 128), &tmQ, B(bars->st_full[s]), c * 64, qb * kBT, bh);
+          tma_load_3d(sdo + c * (kBT * 128), &tmdO, B(bars->st_full[s]), c * 64, qb * kBT, bh);
+        }
+      }
+      fills[s] = (t >> 1) + 1;
+    }
+    if (!ok) {  // every load issued lands before the CTA exits
+      if (res) wait_quiet_b(B(bars->res_full), 0, wc);
+      for (int s = 0; s < 2; ++s)
+        if (fills[s] > 0) wait_quiet_b(B(bars->st_full[s]), (fills[s] - 1) & 1, wc);
+    }
+    __syncwarp();
+  } else if (warp == kBwdMmaWarp) {
+    // ------------------------------------------------------------ MMA
+    const bool leader = elect_one();
+    bool ok = mbar_wait(B(bars->res_full), 0, wc);
+    int t = 0;
+    for (int qb = next_qb(-1, kb, bh, p, nqb); qb < nqb && ok; qb = next_qb(qb, kb, bh, p, nqb), ++t) {
+      const int s = t & 1;
+      if (!(ok = mbar_wait(B(bars->st_full[s]), (t >> 1) & 1, wc))) break;
+      tc_fence_after();
+      const uint32_t sq = sSt + 2 * s * C::TILE, sdo = sq + C::TILE;
+      if (leader) {
+        issue_qk<D, kBT, BF16>(tmem, sK, sq);          // S^T = K Q^T
+        issue_qk<D, kBT, BF16>(tmem + 128, sV, sdo);   // dP^T = V dO^T
+        umma_commit(B(bars->s_full));
+      }
+      if (!(ok = mbar_wait(B(bars->p_full), t & 1, wc))) break;
+      tc_fence_after();
+      if (leader) {
+        issue_pv<D, kBT, BF16>(tmem + 256, tmem, sdo, t > 0);           // dV += P^T dO
+        issue_pv<D, kBT, BF16>(tmem + 256 + D, tmem + 128, sq, t > 0);  // dK += dS^T Q
+        umma_commit(B(bars->st_empty[s]));
+      }
+    }
+    if (leader) umma_commit(B(bars->acc_full));  // every MMA above done (or none issued)
+    wait_quiet_b(B(bars->acc_full), 0, wc);
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ elementwise + epilogue
+    const int row = warp * 32 + lane;  // key row of the tile (= TMEM lane)
+    const int j = kb * kBT + row;
+    const uint32_t t_lane = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const float* lse = b.lse + static_cast<size_t>(bh) * p.Sq;
+    const float* dsum = b.dsum + static_cast<size_t>(bh) * p.Sq;
+    bool ok = true;
+    int t = 0;
+    for (int qb = next_qb(-1, kb, bh, p, nqb); qb < nqb && ok; qb = next_qb(qb, kb, bh, p, nqb), ++t) {
+      ok = mbar_wait(B(bars->s_full), t & 1, wc);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      const int m0 = qb * kBT;
+      const RowSpan vis = query_cols(j, m0, p.Sk, p);
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {  // 32 queries at a time
+        uint32_t sv[32], dp[32];
+        tmem_ld32(t_lane + c * 32, sv);
+        tmem_ld32(t_lane + 128 + c * 32, dp);
+        float l2[32], dd[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {  // per-query statistics (the same for every lane)
+          const int col = c * 32 + e;
+          const bool in = m0 + col < p.Sq;
+          l2[e] = in ? __ldg(lse + m0 + col) * 1.4426950408889634f : 0.f;
+          dd[e] = in ? __ldg(dsum + m0 + col) : 0.f;
+        }
+        tmem_ld_wait<32>(sv);
+        tmem_ld_wait<32>(dp);
+        uint32_t pp[16], ds[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          float pv[2], dv[2];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int col = c * 32 + e + u;
+            const bool on = col >= vis.lo && col <= vis.hi;
+            pv[u] = on ? ex2_approx(__uint_as_float(sv[e + u]) * p.sl2 - l2[e + u]) : 0.f;
+            dv[u] = pv[u] * (__uint_as_float(dp[e + u]) - dd[e + u]);
+          }
+          pp[e / 2] = BF16 ? cvt_pack_bf16(pv[0], pv[1]) : cvt_pack_f16(pv[0], pv[1]);
+          ds[e / 2] = BF16 ? cvt_pack_bf16(dv[0], dv[1]) : cvt_pack_f16(dv[0], dv[1]);
+        }
+        tmem_st16(t_lane + c * 16, pp);        // P^T over S^T columns already read
+        tmem_st16(t_lane + 128 + c * 16, ds);  // dS^T over dP^T columns already read
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(B(bars->p_full));
+    }
+    // epilogue: dV and scale * dK of this thread's key
+    if (ok) {
+      ok = mbar_wait(B(bars->acc_full), 0, wc);
+      ok = __all_sync(0xffffffffu, ok);
+    }
+    if (ok) {
+      tc_fence_after();
+      const size_t orow = static_cast<size_t>(bh) * p.Sk + j;
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t v[32], k[32];
+        tmem_ld32(t_lane + 256 + c * 32, v);
+        tmem_ld32(t_lane + 256 + D + c * 32, k);
+        tmem_ld_wait<32>(v);
+        tmem_ld_wait<32>(k);
+        if (t == 0) {  // no query sees these keys: the gradients are 0, not TMEM contents
+#pragma unroll
+          for (int e = 0; e < 32; ++e) v[e] = k[e] = 0u;
+        }
+        if (j < p.Sk) {
+          store_tile_row<D, BF16>(b.dv, orow, v, 1.f, c * 32);
+          store_tile_row<D, BF16>(b.dk, orow, k, b.scale, c * 32);
+        }
+      }
+    }
+  }
+  bwd_teardown(tmem);
+}
+
+// dQ of one block of 128 queries. TMEM: S [0,128), dP [128,256) (dS packed over
+// [128,192)), dQ [256,256+D). Shared memory: Q, dO (resident), then (K, V) in two stages.
+template <int D, bool BF16>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV,
+                  const __grid_constant__ CUtensorMap tmdO, const PrefillParams p,
+                  const BwdParams b) {
+  using C = BwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (base - raw);
+  const uint32_t sQ = base, sdO = base + C::TILE;
+  const uint32_t sSt = base + 2 * C::TILE;  // stage s: K at sSt + 2s TILE, V one TILE on
+  BwdBars* bars = reinterpret_cast<BwdBars*>(smem + 6 * C::TILE);
+  auto B = [&](uint64_t& x) { return smem_u32(&x); };
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int nqb = (p.Sq + kBT - 1) / kBT;
+  const int bh = blockIdx.x / nqb, qb = blockIdx.x % nqb;
+  const Range rg = key_range(qb * kBT, min(qb * kBT + kBT, p.Sq), kBT, p.Sk, p, bh);
+  const int n = range_count(rg);
+  const uint32_t tmem = bwd_setup(bars, &tmQ, &tmK, &tmV, &tmdO);
+  const WaitCtx wc{&bars->abort, p.status, p.timeout_ns};
+
+  if (warp == kBwdTmaWarp) {
+    // ------------------------------------------------------------ TMA
+    const bool leader = elect_one();
+    bool ok = true;
+    uint32_t fills[2] = {0, 0};
+    if (n > 0) {
+      if (leader) {
+        mbar_arrive_expect_tx(B(bars->res_full), 2 * C::TILE);
+        for (int c = 0; c < C::KCH; ++c) {
+          tma_load_3d(sQ + c * (kBT * 128), &tmQ, B(bars->res_full), c * 64, qb * kBT, bh);
+          tma_load_3d(sdO + c * (kBT * 128), &tmdO, B(bars->res_full), c * 64, qb * kBT, bh);
+        }
+      }
+      int nb = -1;
+      for (int t = 0; t < n && ok; ++t) {
+        nb = range_next(rg, nb);
+        const int s = t & 1;
+        if (t >= 2 && !(ok = mbar_wait(B(bars->st_empty[s]), ((t >> 1) - 1) & 1, wc))) break;
+        const uint32_t sk_ = sSt + 2 * s * C::TILE, sv = sk_ + C::TILE;
+        if (leader) {
+          mbar_arrive_expect_tx(B(bars->st_full[s]), 2 * C::TILE);
+          for (int c = 0; c < C::KCH; ++c) {
+            tma_load_3d(sk_ + c * (kBT * 128), &tmK, B(bars->st_full[s]), c * 64, nb * kBT, bh);
+            tma_load_3d(sv + c * (kBT * 128), &tmV, B(bars->st_full[s]), c * 64, nb * kBT, bh);
+          }
+        }
+        fills[s] = (t >> 1) + 1;
+      }
+      if (!ok) {  // every load issued lands before the CTA exits
+        wait_quiet_b(B(bars->res_full), 0, wc);
+        for (int s = 0; s < 2; ++s)
+          if (fills[s] > 0) wait_quiet_b(B(bars->st_full[s]), (fills[s] - 1) & 1, wc);
+      }
+    }
+    __syncwarp();
+  } else if (warp == kBwdMmaWarp) {
+    // ------------------------------------------------------------ MMA
+    const bool leader = elect_one();
+    bool ok = n == 0 || mbar_wait(B(bars->res_full), 0, wc);
+    for (int t = 0; t < n && ok; ++t) {
+      const int s = t & 1;
+      if (!(ok = mbar_wait(B(bars->st_full[s]), (t >> 1) & 1, wc))) break;
+      tc_fence_after();
+      const uint32_t sk_ = sSt + 2 * s * C::TILE, sv = sk_ + C::TILE;
+      if (leader) {
+        issue_qk<D, kBT, BF16>(tmem, sQ, sk_);         // S = Q K^T
+        issue_qk<D, kBT, BF16>(tmem + 128, sdO, sv);   // dP = dO V^T
+        umma_commit(B(bars->s_full));
+      }
+      if (!(ok = mbar_wait(B(bars->p_full), t & 1, wc))) break;
+      tc_fence_after();
+      if (leader) {
+        issue_pv<D, kBT, BF16>(tmem + 256, tmem + 128, sk_, t > 0);  // dQ += dS K
+        umma_commit(B(bars->st_empty[s]));
+      }
+    }
+    if (leader) umma_commit(B(bars->acc_full));
+    wait_quiet_b(B(bars->acc_full), 0, wc);
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ elementwise + epilogue
+    const int row = warp * 32 + lane;  // query row of the tile (= TMEM lane)
+    const int i = qb * kBT + row;
+    const uint32_t t_lane = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const bool in = i < p.Sq;
+    const size_t srow = static_cast<size_t>(bh) * p.Sq + (in ? i : 0);
+    const float l2 = in ? b.lse[srow] * 1.4426950408889634f : 0.f;
+    const float dd = in ? b.dsum[srow] : 0.f;
+    bool ok = true;
+    int nb = -1;
+    for (int t = 0; t < n && ok; ++t) {
+      nb = range_next(rg, nb);
+      ok = mbar_wait(B(bars->s_full), t & 1, wc);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      const ColMask cm = key_cols(i, nb * kBT, p.Sk, p);
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {  // 32 keys at a time
+        uint32_t sv[32], dp[32];
+        tmem_ld32(t_lane + c * 32, sv);
+        tmem_ld32(t_lane + 128 + c * 32, dp);
+        tmem_ld_wait<32>(sv);
+        tmem_ld_wait<32>(dp);
+        uint32_t ds[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          float dv[2];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int col = c * 32 + e + u;
+            const bool on = col <= cm.lim && (col >= cm.lo || col < cm.gl);
+            const float pv = on ? ex2_approx(__uint_as_float(sv[e + u]) * p.sl2 - l2) : 0.f;
+            dv[u] = pv * (__uint_as_float(dp[e + u]) - dd);
+          }
+          ds[e / 2] = BF16 ? cvt_pack_bf16(dv[0], dv[1]) : cvt_pack_f16(dv[0], dv[1]);
+        }
+        tmem_st16(t_lane + 128 + c * 16, ds);  // dS over dP columns already read
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(B(bars->p_full));
+    }
+    if (ok) {
+      ok = mbar_wait(B(bars->acc_full), 0, wc);
+      ok = __all_sync(0xffffffffu, ok);
+    }
+    if (ok) {  // the TMEM loads are warp-collective: every lane runs them, valid rows store
+      tc_fence_after();
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t q[32];
+        tmem_ld32(t_lane + 256 + c * 32, q);
+        tmem_ld_wait<32>(q);
+        if (n == 0)
+#pragma unroll
+          for (int e = 0; e < 32; ++e) q[e] = 0u;
+        if (in) store_tile_row<D, BF16>(b.dq, srow, q, b.scale, c * 32);
+      }
+    }
+  }
+  bwd_teardown(tmem);
+}
+
+template <int D, bool BF16>
+cudaError_t launch_bwd_t(const BwdLaunch& L, cudaStream_t stream) {
+  const int64_t rows = static_cast<int64_t>(L.p.BH) * L.p.Sq;
+  if (rows > 0) {
+    const int blocks = static_cast<int>((rows + 63) / 64 < 4096 ? (rows + 63) / 64 : 4096);
+    bwd_prep_kernel<D, BF16><<<blocks, 256, 0, stream>>>(
+        static_cast<const uint4*>(L.o), static_cast<const uint4*>(L.dout),
+        const_cast<float*>(L.b.dsum), rows);
+  }
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  constexpr int smem = BwdCfg<D>::SMEM;
+  const int nkb = (L.p.Sk + kBT - 1) / kBT, nqb = (L.p.Sq + kBT - 1) / kBT;
+  if (nkb > 0) {  // with Sq = 0 it still writes the (zero) gradients of every key
+    auto k1 = bwd_dkdv_kernel<D, BF16>;
+    if ((e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)))
+      return e;
+    k1<<<L.p.BH * nkb, kBwdThreads, smem, stream>>>(L.tmQ, L.tmK, L.tmV, L.tmdO, L.p, L.b);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  if (nqb > 0) {
+    auto k2 = bwd_dq_kernel<D, BF16>;
+    if ((e = cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)))
+      return e;
+    k2<<<L.p.BH * nqb, kBwdThreads, smem, stream>>>(L.tmQ, L.tmK, L.tmV, L.tmdO, L.p, L.b);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t launch_backward(const BwdLaunch& L, int D, bool bf16, cudaStream_t stream) {
+  if (D == 128) return bf16 ? launch_bwd_t<128, true>(L, stream) : launch_bwd_t<128, false>(L, stream);
+  if (D == 64) return bf16 ? launch_bwd_t<64, true>(L, stream) : launch_bwd_t<64, false>(L, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace fa

@@ -51,6 +51,26 @@ int prefill_tile_rows();
 cudaError_t launch_prefill(const PrefillLaunch& L, int D, int BN, int BM, bool bf16,
                            cudaStream_t stream);
 
+// Backward: what the kernels read besides the forward's parameters.
+struct BwdParams {
+  const float* lse;   // [B,H,Sq] natural-log LSE of the forward
+  const float* dsum;  // [B,H,Sq] D_i = dO_i . O_i (written by the first kernel)
+  void* dq;           // [B,H,Sq,d] 16-bit
+  void* dk;           // [B,H,Sk,d]
+  void* dv;
+  float scale;
+};
+
+struct BwdLaunch {
+  CUtensorMap tmQ, tmK, tmV, tmdO;
+  PrefillParams p;  // sizes, mask, sl2, status, timeout (contiguous K/V)
+  BwdParams b;
+  const void* o;     // forward output [B,H,Sq,d]
+  const void* dout;  // upstream gradient [B,H,Sq,d]
+};
+
+cudaError_t launch_backward(const BwdLaunch& L, int D, bool bf16, cudaStream_t stream);
+
 struct DecodeParams {
   const void* q;            // [B,H,D]
   const void* k_pages;      // [num_pages,H,page_size,D]

@@ -41,6 +41,7 @@
 #include "fa_internal.h"
 #include "fa_plan.h"
 #include "fa_ptx.cuh"
+#include "fa_mma.cuh"
 
 namespace fa {
 namespace {
@@ -300,46 +301,6 @@ __device__ __forceinline__ void wait_quiet(uint32_t bar, uint32_t parity, const 
   WaitCtx w2 = wc;
   w2.abort = &zero;
   mbar_wait(bar, parity, w2);
-}
-
-// S = Q K^T for one 128-row tile: D/16 MMAs of K = 16, both operands K-major in
-// 128-byte-swizzled shared memory (rows of 128 bytes, 8-row groups 1024 bytes apart,
-// one region per 64 elements of d). The descriptors are built once; each MMA adds a
-// compile-time offset to the start-address field (addresses stay below 256 KB, so the
-// 14-bit field never carries), which keeps the issuing thread's dependency chain short.
-template <int D, int BN, bool BF16>
-__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_smem, uint32_t k_smem) {
-  constexpr uint32_t id = idesc_f16(BF16, kTile, BN, false);
-  const uint64_t a0 = smem_desc_sw128(q_smem, 16, 1024);
-  const uint64_t b0 = smem_desc_sw128(k_smem, 16, 1024);
-  if constexpr (D == 128) {
-    constexpr int QC = kTile * 128 / 16, KC = BN * 128 / 16;  // next 64-element region
-    umma_ss8<2, 4, 6, QC, QC + 2, QC + 4, QC + 6, 2, 4, 6, KC, KC + 2, KC + 4, KC + 6>(d_tmem, a0,
-                                                                                       b0, id);
-  } else {
-#pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk)
-      umma_ss(d_tmem, a0 + static_cast<uint64_t>(kk * 2), b0 + static_cast<uint64_t>(kk * 2), id,
-              kk > 0);
-  }
-}
-
-// O (+)= P V: A = P from TMEM (BN/2 packed columns), B = V (BN keys x D) MN-major in
-// shared memory: 16 keys per MMA = two 8-row groups (1024 bytes apart), the second
-// 64-element half of d one region (BN*128 bytes) further.
-template <int D, int BN, bool BF16>
-__device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint32_t v_smem,
-                                         bool accumulate) {
-  constexpr uint32_t id = idesc_f16(BF16, kTile, D, true);
-  const uint64_t b0 = smem_desc_sw128(v_smem, BN * 128, 1024);
-  if constexpr (BN == 128) {
-    umma_ts8<16 * 128 / 16>(o_tmem, p_tmem, b0, id, accumulate ? 1u : 0u);
-  } else {
-#pragma unroll
-    for (int kk = 0; kk < BN / 16; ++kk)
-      umma_ts(o_tmem, p_tmem + kk * 8, b0 + static_cast<uint64_t>(kk * 128), id,
-              (accumulate || kk > 0) ? 1u : 0u);
-  }
 }
 
 // ------------------------------------------------------------------ BM = 256 kernel
