@@ -63,15 +63,15 @@ MODE_NAME = {0: "none", 1: "causal", 2: "causal_window", 3: "band", 4: "prefix_l
 # capture of each kernel, with the SHA-256 of the kernel sources it was taken on; the
 # figure is reported only while those sources are unchanged. Summaries: profiles/.
 NCU_TRAFFIC = {
-    # prefill_bm256_kernel, causal 4k B4 H16 capture: 210.3 MB read + 45.0 MB written,
+    # prefill_bm256_kernel, causal 4k B4 H16 capture: 210.0 MB read + 44.9 MB written,
     # scaled x2 to B4 H32
-    "prefill": {"bytes": 510.6e6,
+    "prefill": {"bytes": 509.9e6,
                 "sources": ['fa_prefill.cu', 'fa_mma.cuh', 'fa_ptx.cuh', 'fa_plan.h', 'fa_internal.h'],
-                "sha256": "263ae657df70fa1a5e1478f561972a8fc09a654a0429156dce7227aaeceb93dc"},
-    # paged decode B8 capture: 547.5 MB read + 3.7 MB written for 547.5 MB algorithmic,
+                "sha256": "dadd82474dedcecc15e5acb626be3e0d5c7d3fb9712f4823f4121c2002f89bdf"},
+    # paged decode B8 capture: 547.5 MB read + 3.9 MB written for 547.5 MB algorithmic,
     # scaled to the bench call's 2410.7 MB algorithmic
-    "decode": {"bytes": 2.4268e9, "sources": ['fa_decode.cu', 'fa_ptx.cuh', 'fa_internal.h'],
-               "sha256": "94ab1a109d1f1e044ba6420afb1d0675b650cff976eaee5dc6f6c8bf144f74d6"},
+    "decode": {"bytes": 2.4278e9, "sources": ['fa_decode.cu', 'fa_ptx.cuh', 'fa_internal.h'],
+               "sha256": "3ec77d7ddf3681b62ba8e849bf549f1385f5998dccb94cc92541a7462b7a836c"},
 }
 
 
@@ -268,6 +268,8 @@ def run_ours(args, rank, world):
     workload = "default" if args.workload == "default" else args.workload
     if workload in ("chunked", "multimodal"):
         return run_next_rows(args, fa, workload, peaks, peak_kind, stream, world)
+    if workload == "bwd4k":
+        return run_backward(args, fa, peaks, stream, world)
     pcfg = PREFILL["causal4k" if workload in ("default", "sweep") else workload] \
         if workload != "decode" else None
     with_decode = workload in ("default", "decode")
@@ -702,6 +704,43 @@ def run_next_rows(args, fa, workload, peaks, peak_kind, stream, world):
     return res
 
 
+def run_backward(args, fa, peaks, stream, world):
+    """Backward of the causal 4k bf16 prefill (B4 H32 S4096 d128): fa_bwd after one fa_fwd,
+    timed with CUDA events. Work counted: the five products of the backward (S recomputed,
+    dP, dV, dK, dQ) over the visible pairs, 2.5x the forward's."""
+    from tiled_attention_06_gb300 import inputs
+    cfg = PREFILL["causal4k"]
+    dev = torch.device("cuda", torch.cuda.current_device())
+    q, k, v = (t.to(dev) for t in make_prefill(cfg, dev))
+    dout = inputs.prefill_inputs(cfg["B"], cfg["H"], cfg["S"], cfg["S"], cfg["d"],
+                                 inputs.DTYPES[cfg["dtype"]], seed=1)[0].to(dev)
+    scale = 1 / math.sqrt(cfg["d"])
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+    fa.fa_fwd(q, k, v, o, lse, scale, cfg["mode"], stream=stream)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(fa.fa_bwd_workspace_size(cfg["B"], cfg["H"], cfg["S"]), dtype=torch.uint8,
+                     device=dev)
+    K, W = args.steps, args.warmup
+    ms = timed([lambda: fa.fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, ws, scale, cfg["mode"],
+                                  stream=stream)], K, W, stream)[0]
+    assert fa.fa_get_device_status() == fa.FA_OK
+    flops = 2.5 * prefill_flops(cfg)
+    val = aggregate(flops * K, max_over_ranks(ms / 1e3, world), world) / 1e12
+    tc_peak = float(peaks["bf16_tflops"])
+    achieved = flops * K / (ms / 1e3) / 1e12
+    return {"n_gpus": world, "steps": K, "warmup": W, "scaling": "weak", "vs_baseline": None,
+            "higher_is_better": True, "data": "synthetic (seeded N(0,1))",
+            "metric": "attention backward TFLOP/s (5 products over visible pairs)",
+            "value": val, "unit": "TFLOP/s", "dtype": cfg["dtype"], "ms_per_step": ms / K,
+            "gpu_launches": 3 * K,
+            "roofline": {"kernel": "bwd_dkdv_kernel + bwd_dq_kernel (+ bwd_prep_kernel)",
+                         "bound": "tensor", "achieved": achieved, "peak": tc_peak,
+                         "unit": "TFLOP/s", "frac": achieved / tc_peak, "traffic": None,
+                         "algorithmic_flops": flops},
+            "config": {"workload": "backward of causal prefill B4 H32 S4096 d128 bf16"}}
+
+
 # --------------------------------------------------------------------------- reference arm
 def run_reference(args, rank, world):
     """The oracle as it stands, on the host cores: each step is a bounded sample of the
@@ -804,6 +843,7 @@ def main(argv=None):
     ap.add_argument("--workload", default="default",
                     choices=["default", "causal2k", "causal4k", "noncausal4k", "window32k",
                              "band4k", "prefixlm4k", "blocksparse4k", "chunked", "multimodal",
+                             "bwd4k",
                              "decode", "sweep"])
     ap.add_argument("--batch", type=int, default=None, help="override B (small profiling cases)")
     ap.add_argument("--heads", type=int, default=None, help="override H (small profiling cases)")
