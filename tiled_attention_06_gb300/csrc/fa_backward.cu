@@ -49,7 +49,8 @@ struct BwdCfg {
   // two resident tiles + two stages of two streamed tiles + barriers, 1 KB aligned; at
   // least half the SM's shared memory, so that one CTA (which takes all 512 TMEM columns)
   // is resident per SM
-  static constexpr int SMEM_USED = 1024 + 6 * TILE + 1024;
+  static constexpr int STATS = 2 * kBT * 4;  // per stage: LSE * log2(e) and D of 128 queries
+  static constexpr int SMEM_USED = 1024 + 6 * TILE + 2 * STATS + 1024;
   static constexpr int SMEM = SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024;
   static_assert(SMEM <= 232448, "shared memory over budget");
 };
@@ -58,8 +59,8 @@ struct BwdBars {
   uint64_t res_full;       // the CTA's resident tiles landed
   uint64_t st_full[2];     // streamed tiles of stage s landed
   uint64_t st_empty[2];    // MMAs done with stage s
-  uint64_t s_full;         // S and dP of the current tile in TMEM
-  uint64_t p_full;         // P and dS (16-bit) written back
+  uint64_t s_full[2];      // S and dP of half u of the current tile in TMEM
+  uint64_t p_full[2];      // P and dS (16-bit) of half u written back
   uint64_t acc_full;       // every MMA of the CTA complete
   uint32_t tmem_base;
   uint32_t abort;
@@ -180,6 +181,36 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const uint4* __restrict__
   }
 }
 
+// Half-tile MMAs: every tile of 128 queries (or keys) is processed as two halves u of 64,
+// so that the tensor core works on one half while the elementwise warps work on the other.
+// X_u = A B_u^T: A a resident 128-row tile, B_u rows [64u, 64u+64) of a 128-row tile (both
+// K-major, 128-byte swizzled, regions of 64 elements of d 16 KB apart); M = 128, N = 64.
+template <int D, bool BF16>
+__device__ __forceinline__ void issue_s_half(uint32_t d_tmem, uint32_t a_smem, uint32_t b_smem,
+                                             int u) {
+  constexpr uint32_t id = idesc_f16(BF16, kBT, 64, false);
+  const uint64_t a0 = smem_desc_sw128(a_smem, 16, 1024);
+  const uint64_t b0 = smem_desc_sw128(b_smem + u * 64 * 128, 16, 1024);
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint64_t off = static_cast<uint64_t>((kk / 4) * (kBT * 128 / 16) + (kk % 4) * 2);
+    umma_ss(d_tmem, a0 + off, b0 + off, id, kk > 0 ? 1u : 0u);
+  }
+}
+
+// Y (+)= A_u B_u: A_u 64 packed 16-bit columns in TMEM (K = 64), B_u rows [64u, 64u+64) of a
+// 128-row tile used MN-major (N = D; 16 rows = 2048 bytes per MMA).
+template <int D, bool BF16>
+__device__ __forceinline__ void issue_pv_half(uint32_t y_tmem, uint32_t a_tmem, uint32_t b_smem,
+                                              int u, bool accumulate) {
+  constexpr uint32_t id = idesc_f16(BF16, kBT, D, true);
+  const uint64_t b0 = smem_desc_sw128(b_smem + u * 64 * 128, kBT * 128, 1024);
+#pragma unroll
+  for (int kk = 0; kk < 4; ++kk)
+    umma_ts(y_tmem, a_tmem + kk * 8, b0 + static_cast<uint64_t>(kk * 128), id,
+            (accumulate || kk > 0) ? 1u : 0u);
+}
+
 // Does the query block qb see any key of key block kb (the forward's key ranges)?
 __device__ __forceinline__ bool tile_visited(int qb, int kb, int bh, const PrefillParams& p) {
   const Range r = key_range(qb * kBT, min(qb * kBT + kBT, p.Sq), kBT, p.Sk, p, bh);
@@ -219,8 +250,10 @@ __device__ __forceinline__ uint32_t bwd_setup(BwdBars* bars, const CUtensorMap* 
       mbar_init(smem_u32(&bars->st_full[i]), 1);
       mbar_init(smem_u32(&bars->st_empty[i]), 1);
     }
-    mbar_init(smem_u32(&bars->s_full), 1);
-    mbar_init(smem_u32(&bars->p_full), 128);
+    for (int u = 0; u < 2; ++u) {
+      mbar_init(smem_u32(&bars->s_full[u]), 1);
+      mbar_init(smem_u32(&bars->p_full[u]), 128);
+    }
     mbar_init(smem_u32(&bars->acc_full), 1);
     bars->abort = 0;
     mbar_fence_init();
@@ -267,7 +300,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   uint8_t* smem = smem_raw + (base - raw);
   const uint32_t sK = base, sV = base + C::TILE;
   const uint32_t sSt = base + 2 * C::TILE;  // stage s: Q at sSt + 2s TILE, dO one TILE on
-  BwdBars* bars = reinterpret_cast<BwdBars*>(smem + 6 * C::TILE);
+  float* stats = reinterpret_cast<float*>(smem + 6 * C::TILE);  // [stage][LSE2 | D][128]
+  BwdBars* bars = reinterpret_cast<BwdBars*>(smem + 6 * C::TILE + 2 * C::STATS);
   auto B = [&](uint64_t& x) { return smem_u32(&x); };
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int nkb = (p.Sk + kBT - 1) / kBT, nqb = (p.Sq + kBT - 1) / kBT;
@@ -293,6 +327,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int s = t & 1;
       if (t >= 2 && !(ok = mbar_wait(B(bars->st_empty[s]), ((t >> 1) - 1) & 1, wc))) break;
       const uint32_t sq = sSt + 2 * s * C::TILE, sdo = sq + C::TILE;
+      {  // LSE * log2(e) and D of the tile's 128 queries, 4 per lane (0 past Sq)
+        float* st = stats + s * 2 * kBT;
+        const size_t r0 = static_cast<size_t>(bh) * p.Sq;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int col = lane * 4 + e, i = qb * kBT + col;
+          st[col] = i < p.Sq ? __ldg(b.lse + r0 + i) * 1.4426950408889634f : 0.f;
+          st[kBT + col] = i < p.Sq ? __ldg(b.dsum + r0 + i) : 0.f;
+        }
+        __syncwarp();  // the leader's arrive below releases every lane's writes
+      }
       if (leader) {
         mbar_arrive_expect_tx(B(bars->st_full[s]), 2 * C::TILE);
         for (int c = 0; c < C::KCH; ++c) {
@@ -311,25 +356,49 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   } else if (warp == kBwdMmaWarp) {
     // ------------------------------------------------------------ MMA
     const bool leader = elect_one();
+    // Per tile t and half u: wait for P^T_u / dS^T_u, then dV += P^T_u dO_u and
+    // dK += dS^T_u Q_u, then the scores of half u of the next tile into the columns just
+    // read (MMAs of one thread execute in order). The tensor core works on one half
+    // while the elementwise warps work on the other.
     bool ok = mbar_wait(B(bars->res_full), 0, wc);
+    int qb = ok ? next_qb(-1, kb, bh, p, nqb) : nqb;
+    auto scores = [&](int stage, int u) {  // S^T_u = K Q_u^T, dP^T_u = V dO_u^T
+      const uint32_t sq = sSt + 2 * stage * C::TILE;
+      issue_s_half<D, BF16>(tmem + 64 * u, sK, sq, u);
+      issue_s_half<D, BF16>(tmem + 128 + 64 * u, sV, sq + C::TILE, u);
+      umma_commit(B(bars->s_full[u]));
+    };
+    if (qb < nqb && (ok = mbar_wait(B(bars->st_full[0]), 0, wc))) {
+      tc_fence_after();
+      if (leader) {
+        scores(0, 0);
+        scores(0, 1);
+      }
+    }
     int t = 0;
-    for (int qb = next_qb(-1, kb, bh, p, nqb); qb < nqb && ok; qb = next_qb(qb, kb, bh, p, nqb), ++t) {
+    while (qb < nqb && ok) {
       const int s = t & 1;
-      if (!(ok = mbar_wait(B(bars->st_full[s]), (t >> 1) & 1, wc))) break;
-      tc_fence_after();
       const uint32_t sq = sSt + 2 * s * C::TILE, sdo = sq + C::TILE;
-      if (leader) {
-        issue_qk<D, kBT, BF16>(tmem, sK, sq);          // S^T = K Q^T
-        issue_qk<D, kBT, BF16>(tmem + 128, sV, sdo);   // dP^T = V dO^T
-        umma_commit(B(bars->s_full));
+      const int qn = next_qb(qb, kb, bh, p, nqb);
+      for (int u = 0; u < 2 && ok; ++u) {
+        if (!(ok = mbar_wait(B(bars->p_full[u]), t & 1, wc))) break;
+        tc_fence_after();
+        if (leader) {
+          issue_pv_half<D, BF16>(tmem + 256, tmem + 64 * u, sdo, u, t > 0 || u > 0);
+          issue_pv_half<D, BF16>(tmem + 256 + D, tmem + 128 + 64 * u, sq, u, t > 0 || u > 0);
+        }
+        if (qn < nqb) {
+          if (u == 0) {
+            if (!(ok = mbar_wait(B(bars->st_full[(t + 1) & 1]), ((t + 1) >> 1) & 1, wc))) break;
+            tc_fence_after();
+          }
+          if (leader) scores((t + 1) & 1, u);
+        }
       }
-      if (!(ok = mbar_wait(B(bars->p_full), t & 1, wc))) break;
-      tc_fence_after();
-      if (leader) {
-        issue_pv<D, kBT, BF16>(tmem + 256, tmem, sdo, t > 0);           // dV += P^T dO
-        issue_pv<D, kBT, BF16>(tmem + 256 + D, tmem + 128, sq, t > 0);  // dK += dS^T Q
-        umma_commit(B(bars->st_empty[s]));
-      }
+      if (!ok) break;
+      if (leader) umma_commit(B(bars->st_empty[s]));  // stage s free once these are done
+      qb = qn;
+      ++t;
     }
     if (leader) umma_commit(B(bars->acc_full));  // every MMA above done (or none issued)
     wait_quiet_b(B(bars->acc_full), 0, wc);
@@ -339,52 +408,57 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int row = warp * 32 + lane;  // key row of the tile (= TMEM lane)
     const int j = kb * kBT + row;
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-    const float* lse = b.lse + static_cast<size_t>(bh) * p.Sq;
-    const float* dsum = b.dsum + static_cast<size_t>(bh) * p.Sq;
     bool ok = true;
     int t = 0;
     for (int qb = next_qb(-1, kb, bh, p, nqb); qb < nqb && ok; qb = next_qb(qb, kb, bh, p, nqb), ++t) {
-      ok = mbar_wait(B(bars->s_full), t & 1, wc);
+      // the stage's statistics: no barrier can be a phase ahead, as the MMAs of this tile
+      // need the P and dS this warpgroup has not written yet
+      ok = mbar_wait(B(bars->st_full[t & 1]), (t >> 1) & 1, wc);
       ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
-      tc_fence_after();
-      const int m0 = qb * kBT;
-      const RowSpan vis = query_cols(j, m0, p.Sk, p);
+      const float4* st4 = reinterpret_cast<const float4*>(stats + (t & 1) * 2 * kBT);
+      for (int u = 0; u < 2 && ok; ++u) {  // halves of 64 queries
+        ok = mbar_wait(B(bars->s_full[u]), t & 1, wc);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after();
+        const int m0 = qb * kBT + 64 * u;
+        const RowSpan vis = query_cols(j, m0, p.Sk, p);
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {  // 32 queries at a time
-        uint32_t sv[32], dp[32];
-        tmem_ld32(t_lane + c * 32, sv);
-        tmem_ld32(t_lane + 128 + c * 32, dp);
-        float l2[32], dd[32];
+        for (int c = 0; c < 2; ++c) {  // 32 queries at a time
+          uint32_t sv[32], dp[32];
+          tmem_ld32(t_lane + 64 * u + c * 32, sv);
+          tmem_ld32(t_lane + 128 + 64 * u + c * 32, dp);
+          float l2[32], dd[32];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {  // per-query statistics (the same for every lane)
-          const int col = c * 32 + e;
-          const bool in = m0 + col < p.Sq;
-          l2[e] = in ? __ldg(lse + m0 + col) * 1.4426950408889634f : 0.f;
-          dd[e] = in ? __ldg(dsum + m0 + col) : 0.f;
-        }
-        tmem_ld_wait<32>(sv);
-        tmem_ld_wait<32>(dp);
-        uint32_t pp[16], ds[16];
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          float pv[2], dv[2];
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int col = c * 32 + e + u;
-            const bool on = col >= vis.lo && col <= vis.hi;
-            pv[u] = on ? ex2_approx(__uint_as_float(sv[e + u]) * p.sl2 - l2[e + u]) : 0.f;
-            dv[u] = pv[u] * (__uint_as_float(dp[e + u]) - dd[e + u]);
+          for (int e = 0; e < 8; ++e) {  // per-query statistics (the same for every lane)
+            const float4 a = st4[(64 * u + c * 32) / 4 + e];
+            const float4 d = st4[(kBT + 64 * u + c * 32) / 4 + e];
+            l2[4 * e] = a.x, l2[4 * e + 1] = a.y, l2[4 * e + 2] = a.z, l2[4 * e + 3] = a.w;
+            dd[4 * e] = d.x, dd[4 * e + 1] = d.y, dd[4 * e + 2] = d.z, dd[4 * e + 3] = d.w;
           }
-          pp[e / 2] = BF16 ? cvt_pack_bf16(pv[0], pv[1]) : cvt_pack_f16(pv[0], pv[1]);
-          ds[e / 2] = BF16 ? cvt_pack_bf16(dv[0], dv[1]) : cvt_pack_f16(dv[0], dv[1]);
+          tmem_ld_wait<32>(sv);
+          tmem_ld_wait<32>(dp);
+          uint32_t pp[16], ds[16];
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            float pv[2], dv[2];
+#pragma unroll
+            for (int w = 0; w < 2; ++w) {
+              const int col = c * 32 + e + w;
+              const bool on = col >= vis.lo && col <= vis.hi;
+              pv[w] = on ? ex2_approx(__uint_as_float(sv[e + w]) * p.sl2 - l2[e + w]) : 0.f;
+              dv[w] = pv[w] * (__uint_as_float(dp[e + w]) - dd[e + w]);
+            }
+            pp[e / 2] = BF16 ? cvt_pack_bf16(pv[0], pv[1]) : cvt_pack_f16(pv[0], pv[1]);
+            ds[e / 2] = BF16 ? cvt_pack_bf16(dv[0], dv[1]) : cvt_pack_f16(dv[0], dv[1]);
+          }
+          tmem_st16(t_lane + 64 * u + c * 16, pp);        // P^T_u over columns already read
+          tmem_st16(t_lane + 128 + 64 * u + c * 16, ds);  // dS^T_u likewise
         }
-        tmem_st16(t_lane + c * 16, pp);        // P^T over S^T columns already read
-        tmem_st16(t_lane + 128 + c * 16, ds);  // dS^T over dP^T columns already read
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(B(bars->p_full[u]));
       }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(B(bars->p_full));
     }
     // epilogue: dV and scale * dK of this thread's key
     if (ok) {
@@ -430,7 +504,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   uint8_t* smem = smem_raw + (base - raw);
   const uint32_t sQ = base, sdO = base + C::TILE;
   const uint32_t sSt = base + 2 * C::TILE;  // stage s: K at sSt + 2s TILE, V one TILE on
-  BwdBars* bars = reinterpret_cast<BwdBars*>(smem + 6 * C::TILE);
+  BwdBars* bars = reinterpret_cast<BwdBars*>(smem + 6 * C::TILE + 2 * C::STATS);
   auto B = [&](uint64_t& x) { return smem_u32(&x); };
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int nqb = (p.Sq + kBT - 1) / kBT;
@@ -478,23 +552,39 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   } else if (warp == kBwdMmaWarp) {
     // ------------------------------------------------------------ MMA
     const bool leader = elect_one();
+    // Per tile t and half u (64 keys): wait for dS_u, dQ += dS_u K_u, then the scores of
+    // half u of the next tile (as in the dK/dV kernel).
     bool ok = n == 0 || mbar_wait(B(bars->res_full), 0, wc);
+    auto scores = [&](int stage, int u) {  // S_u = Q K_u^T, dP_u = dO V_u^T
+      const uint32_t sk_ = sSt + 2 * stage * C::TILE;
+      issue_s_half<D, BF16>(tmem + 64 * u, sQ, sk_, u);
+      issue_s_half<D, BF16>(tmem + 128 + 64 * u, sdO, sk_ + C::TILE, u);
+      umma_commit(B(bars->s_full[u]));
+    };
+    if (n > 0 && ok && (ok = mbar_wait(B(bars->st_full[0]), 0, wc))) {
+      tc_fence_after();
+      if (leader) {
+        scores(0, 0);
+        scores(0, 1);
+      }
+    }
     for (int t = 0; t < n && ok; ++t) {
       const int s = t & 1;
-      if (!(ok = mbar_wait(B(bars->st_full[s]), (t >> 1) & 1, wc))) break;
-      tc_fence_after();
-      const uint32_t sk_ = sSt + 2 * s * C::TILE, sv = sk_ + C::TILE;
-      if (leader) {
-        issue_qk<D, kBT, BF16>(tmem, sQ, sk_);         // S = Q K^T
-        issue_qk<D, kBT, BF16>(tmem + 128, sdO, sv);   // dP = dO V^T
-        umma_commit(B(bars->s_full));
+      const uint32_t sk_ = sSt + 2 * s * C::TILE;
+      for (int u = 0; u < 2 && ok; ++u) {
+        if (!(ok = mbar_wait(B(bars->p_full[u]), t & 1, wc))) break;
+        tc_fence_after();
+        if (leader) issue_pv_half<D, BF16>(tmem + 256, tmem + 128 + 64 * u, sk_, u, t > 0 || u > 0);
+        if (t + 1 < n) {
+          if (u == 0) {
+            if (!(ok = mbar_wait(B(bars->st_full[(t + 1) & 1]), ((t + 1) >> 1) & 1, wc))) break;
+            tc_fence_after();
+          }
+          if (leader) scores((t + 1) & 1, u);
+        }
       }
-      if (!(ok = mbar_wait(B(bars->p_full), t & 1, wc))) break;
-      tc_fence_after();
-      if (leader) {
-        issue_pv<D, kBT, BF16>(tmem + 256, tmem + 128, sk_, t > 0);  // dQ += dS K
-        umma_commit(B(bars->st_empty[s]));
-      }
+      if (!ok) break;
+      if (leader) umma_commit(B(bars->st_empty[s]));
     }
     if (leader) umma_commit(B(bars->acc_full));
     wait_quiet_b(B(bars->acc_full), 0, wc);
@@ -512,36 +602,38 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     int nb = -1;
     for (int t = 0; t < n && ok; ++t) {
       nb = range_next(rg, nb);
-      ok = mbar_wait(B(bars->s_full), t & 1, wc);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
-      tc_fence_after();
-      const ColMask cm = key_cols(i, nb * kBT, p.Sk, p);
+      for (int u = 0; u < 2 && ok; ++u) {  // halves of 64 keys
+        ok = mbar_wait(B(bars->s_full[u]), t & 1, wc);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after();
+        const ColMask cm = key_cols(i, nb * kBT + 64 * u, p.Sk, p);
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {  // 32 keys at a time
-        uint32_t sv[32], dp[32];
-        tmem_ld32(t_lane + c * 32, sv);
-        tmem_ld32(t_lane + 128 + c * 32, dp);
-        tmem_ld_wait<32>(sv);
-        tmem_ld_wait<32>(dp);
-        uint32_t ds[16];
+        for (int c = 0; c < 2; ++c) {  // 32 keys at a time
+          uint32_t sv[32], dp[32];
+          tmem_ld32(t_lane + 64 * u + c * 32, sv);
+          tmem_ld32(t_lane + 128 + 64 * u + c * 32, dp);
+          tmem_ld_wait<32>(sv);
+          tmem_ld_wait<32>(dp);
+          uint32_t ds[16];
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          float dv[2];
+          for (int e = 0; e < 32; e += 2) {
+            float dv[2];
 #pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int col = c * 32 + e + u;
-            const bool on = col <= cm.lim && (col >= cm.lo || col < cm.gl);
-            const float pv = on ? ex2_approx(__uint_as_float(sv[e + u]) * p.sl2 - l2) : 0.f;
-            dv[u] = pv * (__uint_as_float(dp[e + u]) - dd);
+            for (int w = 0; w < 2; ++w) {
+              const int col = c * 32 + e + w;
+              const bool on = col <= cm.lim && (col >= cm.lo || col < cm.gl);
+              const float pv = on ? ex2_approx(__uint_as_float(sv[e + w]) * p.sl2 - l2) : 0.f;
+              dv[w] = pv * (__uint_as_float(dp[e + w]) - dd);
+            }
+            ds[e / 2] = BF16 ? cvt_pack_bf16(dv[0], dv[1]) : cvt_pack_f16(dv[0], dv[1]);
           }
-          ds[e / 2] = BF16 ? cvt_pack_bf16(dv[0], dv[1]) : cvt_pack_f16(dv[0], dv[1]);
+          tmem_st16(t_lane + 128 + 64 * u + c * 16, ds);  // dS_u over columns already read
         }
-        tmem_st16(t_lane + 128 + c * 16, ds);  // dS over dP columns already read
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(B(bars->p_full[u]));
       }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(B(bars->p_full));
     }
     if (ok) {
       ok = mbar_wait(B(bars->acc_full), 0, wc);
