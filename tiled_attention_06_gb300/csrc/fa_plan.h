@@ -17,10 +17,15 @@ namespace fa {
 
 // Key blocks visited by the query rows [m0, m1): [0, a_end) then [b_start, b_end),
 // a_end <= b_start. Closed form of the mask: every block inside holds at least one
-// visible pair for these rows, every block outside holds none. A block-sparse mask
-// (device code only) visits the blocks of [0, b_end) whose layout byte is set in the
-// row of either query block (la, lb; key block nb -> layout column nb >> shift).
+// visible pair for these rows, every block outside holds none.
 struct Range {
+  int a_end, b_start, b_end;
+};
+
+// A block-sparse mask (device code only) visits the blocks of [0, b_end) whose layout
+// byte is set in the row of either query block (la, lb; key block nb -> layout column
+// nb >> shift). Kept apart from Range so that the other masks carry none of it.
+struct SparseRange {
   int a_end, b_start, b_end;
   const uint8_t* la;
   const uint8_t* lb;
@@ -33,19 +38,12 @@ FA_HD int imax(int a, int b) { return a > b ? a : b; }
 // `sk` is the number of keys of this (batch, head): p.Sk for contiguous K/V, the
 // sequence's own length for a paged cache.
 FA_HD Range key_range(int m0, int m1, int BN, int sk, const PrefillParams& p, int bh) {
+  (void)bh;
   const int nnb = (sk + BN - 1) / BN;
   Range r{0, 0, nnb};
   if (m0 >= m1 || nnb == 0) return Range{0, 0, 0};
   if (p.mask_mode == FA_MASK_NONE) return r;
-  if (p.mask_mode == FA_MASK_BLOCK_SPARSE) {
-#if defined(__CUDA_ARCH__)  // the layout is device memory: the host plans with every block
-    const uint8_t* head = p.layout + static_cast<size_t>(bh % p.H) * p.lnqb * p.lnkb;
-    r.la = head + static_cast<size_t>(m0 / 128) * p.lnkb;
-    r.lb = m1 - m0 > 128 ? r.la + p.lnkb : nullptr;
-    r.shift = BN == 64 ? 1 : 0;
-#endif
-    return r;
-  }
+  if (p.mask_mode == FA_MASK_BLOCK_SPARSE) return r;  // every block (see key_range_sparse)
   const int delta = sk - p.Sq;
   const int r_lo = m0 + delta;      // key position of the first row
   const int r_hi = m1 - 1 + delta;  // key position of the last row
@@ -76,30 +74,44 @@ FA_HD Range key_range(int m0, int m1, int BN, int sk, const PrefillParams& p, in
   return r;
 }
 
-FA_HD bool range_vis(const Range& r, int nb) {  // block-sparse: is block nb visited
+FA_HD int range_count(const Range& r) { return r.a_end + r.b_end - r.b_start; }
+// The key block visited after block nb (the first one for nb = -1); callers ask for no
+// more than range_count blocks.
+FA_HD int range_next(const Range& r, int nb) {
+  const int t = nb + 1;
+  return (t >= r.a_end && t < r.b_start) ? r.b_start : t;
+}
+FA_HD bool range_has(const Range& r, int nb) {
+  return nb < r.a_end || (nb >= r.b_start && nb < r.b_end);
+}
+
+#if defined(__CUDACC__)
+// Block-sparse ranges: the layout rows of the query blocks of [m0, m1) (at most two).
+__device__ __forceinline__ SparseRange key_range_sparse(int m0, int m1, int BN, int sk,
+                                                        const PrefillParams& p, int bh) {
+  const int nnb = (sk + BN - 1) / BN;
+  if (m0 >= m1 || nnb == 0) return SparseRange{0, 0, 0, nullptr, nullptr, 0};
+  const uint8_t* head = p.layout + static_cast<size_t>(bh % p.H) * p.lnqb * p.lnkb;
+  const uint8_t* la = head + static_cast<size_t>(m0 / 128) * p.lnkb;
+  return SparseRange{0, 0, nnb, la, m1 - m0 > 128 ? la + p.lnkb : nullptr, BN == 64 ? 1 : 0};
+}
+__device__ __forceinline__ bool range_vis(const SparseRange& r, int nb) {
   return (r.la[nb >> r.shift] | (r.lb ? r.lb[nb >> r.shift] : 0)) != 0;
 }
-FA_HD int range_count(const Range& r) {
-  if (!r.la) return r.a_end + r.b_end - r.b_start;
+__device__ __forceinline__ int range_count(const SparseRange& r) {
   int n = 0;
   for (int nb = 0; nb < r.b_end; ++nb) n += range_vis(r, nb);
   return n;
 }
-// The key block visited after block nb (the first one for nb = -1); callers ask for no
-// more than range_count blocks.
-FA_HD int range_next(const Range& r, int nb) {
+__device__ __forceinline__ int range_next(const SparseRange& r, int nb) {
   int t = nb + 1;
-  if (r.la) {
-    while (t < r.b_end && !range_vis(r, t)) ++t;
-    return t;
-  }
-  if (t >= r.a_end && t < r.b_start) t = r.b_start;
+  while (t < r.b_end && !range_vis(r, t)) ++t;
   return t;
 }
-FA_HD bool range_has(const Range& r, int nb) {
-  if (r.la) return nb >= 0 && nb < r.b_end && range_vis(r, nb);
-  return nb < r.a_end || (nb >= r.b_start && nb < r.b_end);
+__device__ __forceinline__ bool range_has(const SparseRange& r, int nb) {
+  return r.la && nb >= 0 && nb < r.b_end && range_vis(r, nb);
 }
+#endif
 
 // Work item t -> (batch*head, query block). Order: groups of `group_heads` heads; inside
 // a group, query blocks from the last (most keys under a causal mask) to the first;

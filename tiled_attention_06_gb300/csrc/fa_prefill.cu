@@ -74,13 +74,13 @@ __device__ __forceinline__ bool layout_bit(int bh, int m0, int nb, const Prefill
 
 // True when every (row, key) pair of the 128-row tile at m0 and key block nb is in range
 // and visible.
-template <int BN>
+template <int BN, bool SPARSE>
 __device__ __forceinline__ bool tile_full(int m0, int nb, int sk, int bh,
                                           const PrefillParams& p) {
   const int n0 = nb * BN, n1 = n0 + BN;
   if (m0 + kTile > p.Sq || n1 > sk) return false;
+  if constexpr (SPARSE) return layout_bit<BN>(bh, m0, nb, p);
   if (p.mask_mode == FA_MASK_NONE) return true;
-  if (p.mask_mode == FA_MASK_BLOCK_SPARSE) return layout_bit<BN>(bh, m0, nb, p);
   const int delta = sk - p.Sq;
   const int r_lo = m0 + delta, r_hi = m0 + kTile - 1 + delta;
   if (p.mask_mode == FA_MASK_BAND)  // the largest |pos - j| of the tile is within w
@@ -90,6 +90,17 @@ __device__ __forceinline__ bool tile_full(int m0, int nb, int sk, int bh,
   if (n1 - 1 > r_lo) return false;
   if (p.mask_mode == FA_MASK_CAUSAL) return true;
   return n1 <= p.n_global || r_hi - max(n0, p.n_global) < p.window;
+}
+
+// The key blocks visited by query rows [m0, m1). The kernels are built twice: block-sparse
+// (a scan of the layout rows, SparseRange) and every other mask (closed-form Range).
+template <bool SPARSE>
+__device__ __forceinline__ auto item_range(int m0, int m1, int BN, int sk, const PrefillParams& p,
+                                           int bh) {
+  if constexpr (SPARSE)
+    return key_range_sparse(m0, m1, BN, sk, p, bh);
+  else
+    return key_range(m0, m1, BN, sk, p, bh);
 }
 
 __device__ __forceinline__ uint32_t pack2(float a, float b, bool bf16) {
@@ -340,7 +351,7 @@ struct Bars256 {
   uint32_t abort;
 };
 
-template <int D, int BN, bool BF16>
+template <int D, int BN, bool BF16, bool SPARSE>
 __global__ void __launch_bounds__(kThreads256, 1)
     prefill_bm256_kernel(const __grid_constant__ CUtensorMap tmQ,
                          const __grid_constant__ CUtensorMap tmK,
@@ -410,7 +421,7 @@ __global__ void __launch_bounds__(kThreads256, 1)
         if (t < 0) continue;
         int bh, mb;
         item_coords(t, p, bh, mb);
-        const Range rg = key_range(mb * BM, min(mb * BM + BM, p.Sq), BN, item_sk(p, bh), p, bh);
+        const auto rg = item_range<SPARSE>(mb * BM, min(mb * BM + BM, p.Sq), BN, item_sk(p, bh), p, bh);
         const int n = range_count(rg);
         if (n == 0) continue;
         for (int q = 0; q < 2 && ok; ++q) {
@@ -461,7 +472,7 @@ __global__ void __launch_bounds__(kThreads256, 1)
         if (t < 0) continue;
         int bh, mb;
         item_coords(t, p, bh, mb);
-        const Range rg = key_range(mb * BM, min(mb * BM + BM, p.Sq), BN, item_sk(p, bh), p, bh);
+        const auto rg = item_range<SPARSE>(mb * BM, min(mb * BM + BM, p.Sq), BN, item_sk(p, bh), p, bh);
         const int n = range_count(rg);
         if (n == 0) continue;
         {  // S_A(0), S_B(0) with K0
@@ -536,7 +547,7 @@ __global__ void __launch_bounds__(kThreads256, 1)
       int bh, mb;
       item_coords(t, p, bh, mb);
       const int sk = item_sk(p, bh);
-      const Range rg = key_range(mb * BM, min(mb * BM + BM, p.Sq), BN, sk, p, bh);
+      const auto rg = item_range<SPARSE>(mb * BM, min(mb * BM + BM, p.Sq), BN, sk, p, bh);
       const int n = range_count(rg);
       const int m0 = mb * BM + q * kTile;  // first row of this tile
       const int qrow = m0 + row;
@@ -545,16 +556,16 @@ __global__ void __launch_bounds__(kThreads256, 1)
         if (qrow < p.Sq) store_zero_row<D>(orow, p);
         continue;
       }
-      const Range mine = key_range(m0, min(m0 + kTile, p.Sq), BN, sk, p, bh);
+      const auto mine = item_range<SPARSE>(m0, min(m0 + kTile, p.Sq), BN, sk, p, bh);
       const int pos_q = qrow + sk - p.Sq;  // key position of this query
       float m_ref = -INFINITY, l = 0.f;
       int nb = -1;
       for (int j = 0; j < n; ++j) {
         nb = range_next(rg, nb);
-        const bool full = tile_full<BN>(m0, nb, sk, bh, p);
+        const bool full = tile_full<BN, SPARSE>(m0, nb, sk, bh, p);
         // a block-sparse item visits the blocks of either tile: one that is off for this
         // tile is masked whole (as if it held no key)
-        const bool off = p.mask_mode == FA_MASK_BLOCK_SPARSE && !range_has(mine, nb);
+        const bool off = SPARSE && !range_has(mine, nb);
         const int sk_t = off ? nb * BN : sk;
         ok = mbar_wait(B(bars->s_full[q]), tc & 1, wc);
         ok = __all_sync(0xffffffffu, ok);
@@ -647,30 +658,32 @@ struct Bars128 {
   uint32_t abort;
 };
 
+template <bool SPARSE>
 struct ItemRef {
   int bh, mb, n, sk;
-  Range rg;
+  std::conditional_t<SPARSE, SparseRange, Range> rg;
 };
 
 
 // Next item of this CTA (empty ones included when `with_empty`): false when none is left.
-template <int BM>
+template <int BM, bool SPARSE>
 __device__ __forceinline__ bool next_item(const PrefillSched& s, const PrefillParams& p, int cta,
-                                          int G, int BN, int& k, ItemRef& it, bool with_empty) {
+                                          int G, int BN, int& k, ItemRef<SPARSE>& it,
+                                          bool with_empty) {
   int t;
   while (item_at(s, p, cta, G, k, t)) {
     ++k;
     if (t < 0) continue;
     item_coords(t, p, it.bh, it.mb);
     it.sk = item_sk(p, it.bh);
-    it.rg = key_range(it.mb * BM, min(it.mb * BM + BM, p.Sq), BN, it.sk, p, it.bh);
+    it.rg = item_range<SPARSE>(it.mb * BM, min(it.mb * BM + BM, p.Sq), BN, it.sk, p, it.bh);
     it.n = range_count(it.rg);
     if (it.n > 0 || with_empty) return true;
   }
   return false;
 }
 
-template <int D, int BN, bool BF16>
+template <int D, int BN, bool BF16, bool SPARSE>
 __global__ void __launch_bounds__(kThreads128, 1)
     prefill_bm128_kernel(const __grid_constant__ CUtensorMap tmQ,
                          const __grid_constant__ CUtensorMap tmK,
@@ -754,8 +767,8 @@ __global__ void __launch_bounds__(kThreads128, 1)
       uint32_t nk = 0, nv = 0;  // K and V tiles loaded so far
       bool ok = true;
       int kc = 0;
-      ItemRef cur, nxt;
-      auto load_q = [&](const ItemRef& it, uint32_t idx) {
+      ItemRef<SPARSE> cur, nxt;
+      auto load_q = [&](const ItemRef<SPARSE>& it, uint32_t idx) {
         const int qb = idx & 1;
         if (idx >= 2 && !(ok = mbar_wait(B(bars->q_empty[qb]), ((idx >> 1) - 1) & 1, wc)))
           return;
@@ -767,7 +780,7 @@ __global__ void __launch_bounds__(kThreads128, 1)
         }
         qfills[qb] = (idx >> 1) + 1;
       };
-      auto emit = [&](const ItemRef& it, int nb, bool is_v) {
+      auto emit = [&](const ItemRef<SPARSE>& it, int nb, bool is_v) {
         const int slot = pos % C::NSLOT;
         if constexpr (!C::kRelease) {
           if (!(ok = mbar_wait(B(bars->empty[slot]), ((pos / C::NSLOT) & 1) ^ 1, wc))) return;
@@ -795,7 +808,7 @@ __global__ void __launch_bounds__(kThreads128, 1)
         fills[slot] = pos / C::NSLOT + 1;  // uses of this slot so far
         ++pos;
       };
-      bool has = next_item<BM>(sched, p, cta, G, BN, kc, cur, false);
+      bool has = next_item<BM, SPARSE>(sched, p, cta, G, BN, kc, cur, false);
       int nb_cur = -1;  // key block of the current tile
       if (has) {
         load_q(cur, 0);
@@ -810,7 +823,7 @@ __global__ void __launch_bounds__(kThreads128, 1)
             nb_next = range_next(cur.rg, nb_cur);
             emit(cur, nb_next, false);
           } else {
-            has_nxt = next_item<BM>(sched, p, cta, G, BN, kc, nxt, false);
+            has_nxt = next_item<BM, SPARSE>(sched, p, cta, G, BN, kc, nxt, false);
             if (has_nxt) {
               load_q(nxt, ii + 1);
               nb_next = range_next(nxt.rg, -1);
@@ -841,7 +854,7 @@ __global__ void __launch_bounds__(kThreads128, 1)
       uint32_t pos = 0, ii = 0, g = 0;
       bool ok = true;
       int kc = 0;
-      ItemRef cur, nxt;
+      ItemRef<SPARSE> cur, nxt;
       auto issue_s = [&](uint32_t sbuf, uint32_t qb) {
         const int slot = pos % C::NSLOT;
         if (!(ok = mbar_wait(B(bars->full[slot]), (pos / C::NSLOT) & 1, wc))) return;
@@ -854,7 +867,7 @@ __global__ void __launch_bounds__(kThreads128, 1)
         }
         ++pos;
       };
-      bool has = next_item<BM>(sched, p, cta, G, BN, kc, cur, false);
+      bool has = next_item<BM, SPARSE>(sched, p, cta, G, BN, kc, cur, false);
       if (has) {
         if ((ok = mbar_wait(B(bars->q_full[0]), 0, wc))) {
           tc_fence_after();
@@ -871,7 +884,7 @@ __global__ void __launch_bounds__(kThreads128, 1)
             issue_s((g + 1) & 1, buf);
             if (ok && j + 2 == cur.n) commit(bars->q_empty[buf]);
           } else {
-            has_nxt = next_item<BM>(sched, p, cta, G, BN, kc, nxt, false);
+            has_nxt = next_item<BM, SPARSE>(sched, p, cta, G, BN, kc, nxt, false);
             if (has_nxt) {
               const uint32_t nb = (ii + 1) & 1;
               if (!(ok = mbar_wait(B(bars->q_full[nb]), ((ii + 1) >> 1) & 1, wc))) break;
@@ -919,8 +932,8 @@ __global__ void __launch_bounds__(kThreads128, 1)
     uint32_t ii = 0;
     bool ok = true;
     int kc = 0;
-    ItemRef it;
-    while (ok && next_item<BM>(sched, p, cta, G, BN, kc, it, true)) {
+    ItemRef<SPARSE> it;
+    while (ok && next_item<BM, SPARSE>(sched, p, cta, G, BN, kc, it, true)) {
       const int qrow = it.mb * BM + row;
       const size_t orow = static_cast<size_t>(it.bh) * p.Sq + qrow;
       if (it.n == 0) {  // no row of this item sees a key
@@ -954,8 +967,8 @@ __global__ void __launch_bounds__(kThreads128, 1)
     uint32_t ii = 0, g = 0;
     bool ok = true;
     int kc = 0;
-    ItemRef it;
-    while (ok && next_item<BM>(sched, p, cta, G, BN, kc, it, false)) {
+    ItemRef<SPARSE> it;
+    while (ok && next_item<BM, SPARSE>(sched, p, cta, G, BN, kc, it, false)) {
       const uint32_t buf = ii & 1;
       const int m0 = it.mb * BM;
       const int pos_q = m0 + row + it.sk - p.Sq;  // key position of this query
@@ -963,7 +976,7 @@ __global__ void __launch_bounds__(kThreads128, 1)
       int nb = -1;
       for (int j = 0; j < it.n; ++j, ++g) {
         nb = range_next(it.rg, nb);
-        const bool full = tile_full<BN>(m0, nb, it.sk, it.bh, p);
+        const bool full = tile_full<BN, SPARSE>(m0, nb, it.sk, it.bh, p);
         ok = mbar_wait(B(bars->s_full[g & 1]), (g >> 1) & 1, wc);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
@@ -1027,10 +1040,10 @@ __global__ void __launch_bounds__(kThreads128, 1)
   }
 }
 
-template <int D, int BN, bool BF16>
-cudaError_t launch_t(const PrefillLaunch& L, int BM, cudaStream_t stream) {
+template <int D, int BN, bool BF16, bool SPARSE>
+cudaError_t launch_k(const PrefillLaunch& L, int BM, cudaStream_t stream) {
   if (BM == 256) {
-    auto kern = prefill_bm256_kernel<D, BN, BF16>;
+    auto kern = prefill_bm256_kernel<D, BN, BF16, SPARSE>;
     constexpr int smem = Cfg256<D, BN>::SMEM;
     // setmaxnreg.inc can only hand out registers the CTA was launched with; a build whose
     // launch register count is below the split would make the softmax warps wait forever,
@@ -1044,7 +1057,7 @@ cudaError_t launch_t(const PrefillLaunch& L, int BM, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     kern<<<L.grid, kThreads256, smem, stream>>>(L.tmQ, L.tmK, L.tmV, L.p, *L.sched);
   } else {
-    auto kern = prefill_bm128_kernel<D, BN, BF16>;
+    auto kern = prefill_bm128_kernel<D, BN, BF16, SPARSE>;
     constexpr int smem = Cfg128<D, BN>::SMEM;
     cudaFuncAttributes fattr;
     cudaError_t e = cudaFuncGetAttributes(&fattr, kern);
@@ -1057,6 +1070,12 @@ cudaError_t launch_t(const PrefillLaunch& L, int BM, cudaStream_t stream) {
     kern<<<L.grid, kThreads128, smem, stream>>>(L.tmQ, L.tmK, L.tmV, L.p, *L.sched);
   }
   return cudaGetLastError();
+}
+
+template <int D, int BN, bool BF16>
+cudaError_t launch_t(const PrefillLaunch& L, int BM, cudaStream_t stream) {
+  return L.p.mask_mode == FA_MASK_BLOCK_SPARSE ? launch_k<D, BN, BF16, true>(L, BM, stream)
+                                               : launch_k<D, BN, BF16, false>(L, BM, stream);
 }
 
 }  // namespace
