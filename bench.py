@@ -52,9 +52,13 @@ PREFILL = {
     # 1 global block row and column, 2 random blocks per row, seeded
     "blocksparse4k": dict(B=4, H=32, S=4096, d=128, dtype="bf16", mode=5, window=0, n_global=0,
                           factor=1.0, layout=dict(local=1, n_global=1, n_random=2)),
+    # FP32 inputs and output (each product formed from bf16 high and low parts)
+    "causal4k_f32": dict(B=4, H=32, S=4096, d=128, dtype="f32", mode=1, window=0, n_global=0,
+                         factor=1.0),
 }
 DECODE = dict(B=32, H=32, d=128, page=256, pool=1200, max_ctx=8192, dtype="f16")
-PREFIX_WORKLOADS = ("default", "decode", "causal2k", "causal4k", "noncausal4k", "window32k",
+PREFIX_WORKLOADS = ("default", "decode", "causal2k", "causal4k", "causal4k_f32", "noncausal4k",
+                    "window32k",
                     "band4k", "prefixlm4k")
 MODE_NAME = {0: "none", 1: "causal", 2: "causal_window", 3: "band", 4: "prefix_lm",
              5: "block_sparse"}
@@ -72,6 +76,10 @@ NCU_TRAFFIC = {
     # scaled to the bench call's 2410.7 MB algorithmic
     "decode": {"bytes": 2.4278e9, "sources": ['fa_decode.cu', 'fa_ptx.cuh', 'fa_internal.h'],
                "sha256": "3ec77d7ddf3681b62ba8e849bf549f1385f5998dccb94cc92541a7462b7a836c"},
+    # FP32 inputs: not captured yet
+    "prefill_f32": {"bytes": None, "sources": ['fa_prefill.cu', 'fa_prefill_split.cu',
+                                               'fa_mma.cuh', 'fa_ptx.cuh', 'fa_plan.h',
+                                               'fa_internal.h'], "sha256": None},
 }
 
 
@@ -286,6 +294,10 @@ def run_ours(args, rank, world):
             lay_d = layout.to(dev)
         pflops = prefill_flops(pcfg, layout)
         scale = 1 / math.sqrt(pcfg["d"])
+        f32 = pcfg["dtype"] == "f32"
+        ws32 = torch.empty(max(fa.fa_fwd_workspace_size(pcfg["B"], pcfg["H"], pcfg["S"], pcfg["S"],
+                                                        pcfg["d"], fa.FA_F32), 16),
+                           dtype=torch.uint8, device=dev) if f32 else None
     if with_decode:
         di = make_decode(dev)
         dq, dk, dv = di.q.to(dev), di.k_pages.to(dev), di.v_pages.to(dev)
@@ -304,6 +316,8 @@ def run_ours(args, rank, world):
             ex["block_m"] = args.block_m
         if lay_d is not None:
             ex["block_layout"] = lay_d
+        if ws32 is not None:
+            ex["workspace"] = ws32
         if ex:
             fa.fa_fwd_ex(qd, kd, vd, od, ld, scale, pcfg["mode"], pcfg["window"],
                          pcfg["n_global"], stream=stream, **ex)
@@ -354,7 +368,8 @@ def run_ours(args, rank, world):
     d_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
     total_ms = ev[0][0].elapsed_time(ev[K - 1][2])
     total_ms = max_over_ranks(total_ms, world)
-    launches = K * ((1 if pcfg else 0) + (2 if with_decode else 0))
+    # an FP32 prefill is two launches: the split into bf16 planes and the prefill kernel
+    launches = K * ((0 if not pcfg else 2 if f32 else 1) + (2 if with_decode else 0))
 
     res = {"n_gpus": world, "steps": K, "warmup": W, "ms_per_step": total_ms / K,
            "scaling": "weak", "vs_baseline": None, "data": "synthetic (seeded N(0,1), "
@@ -372,14 +387,22 @@ def run_ours(args, rank, world):
                     "value": value, "unit": "TFLOP/s", "higher_is_better": True,
                     "dtype": pcfg["dtype"]})
         bm = args.block_m or fa.fa_fwd_default_block_m(pcfg["mode"])
-        res["roofline"] = {"kernel": f"prefill_bm{bm}_kernel<{pcfg['d']},128,{pcfg['dtype']}>",
+        kname = (f"split_bf16_kernel + prefill_bm256_kernel<{pcfg['d']},64,bf16 split> "
+                 "(timed together: one fa_fwd_ex call)" if f32 else
+                 f"prefill_bm{bm}_kernel<{pcfg['d']},128,{pcfg['dtype']}>")
+        res["roofline"] = {"kernel": kname,
                            "bound": "tensor",
                            "achieved": achieved, "peak": tc_peak, "unit": "TFLOP/s",
                            "frac": achieved / tc_peak,
                            "peak_source": f"{peak_kind} bf16 burst (MEASURED_PEAKS.json)"
                            if peak_kind == "measured" else "fallback 1.9 PFLOP/s",
-                           "traffic": ncu_traffic("prefill", args.prefill_traffic), "algorithmic_flops": pflops,
+                           "traffic": ncu_traffic("prefill_f32" if f32 else "prefill",
+                                                  args.prefill_traffic),
+                           "algorithmic_flops": pflops,
                            "ms_per_launch": p_avg * 1e3}
+        if f32:  # the tensor cores run three bf16 products per product of the method
+            res["roofline"]["tensor_flops_executed"] = 3 * pflops
+            res["roofline"]["tensor_frac"] = 3 * achieved / tc_peak
     if with_decode:
         d_sum = max_over_ranks(sum(d_ms) / 1e3, world)
         d_avg = sum(d_ms) / K / 1e3
@@ -400,7 +423,8 @@ def run_ours(args, rank, world):
     res["config"] = workload_config(pcfg, with_decode, world)
 
     # ---- end to end through the public API with host buffers
-    res["e2e"] = e2e_prefill(fa, pcfg, q, k, v, pflops, scale, stream, world, args, layout) \
+    res["e2e"] = e2e_prefill(fa, pcfg, q, k, v, pflops, scale, stream, world, args, layout,
+                             ws32) \
         if pcfg \
         else e2e_decode(fa, di, dbytes, dscale, ws, dk, dv, stream, world, args)
     # ---- CPU baseline: the oracle on a bounded sample, rank 0 only
@@ -428,7 +452,7 @@ def workload_config(pcfg, with_decode, world):
     return cfg
 
 
-def e2e_prefill(fa, pcfg, q, k, v, pflops, scale, stream, world, args, layout=None):
+def e2e_prefill(fa, pcfg, q, k, v, pflops, scale, stream, world, args, layout=None, ws32=None):
     dev = torch.device("cuda", torch.cuda.current_device())
     hq, hk, hv = q.pin_memory(), k.pin_memory(), v.pin_memory()
     ins = [hq, hk, hv]
@@ -451,6 +475,9 @@ def e2e_prefill(fa, pcfg, q, k, v, pflops, scale, stream, world, args, layout=No
             lay_d.copy_(hlay, non_blocking=True)
             fa.fa_fwd_ex(qd, kd, vd, od, ld, scale, pcfg["mode"], block_layout=lay_d,
                          stream=stream)
+        elif ws32 is not None:
+            fa.fa_fwd_ex(qd, kd, vd, od, ld, scale, pcfg["mode"], pcfg["window"],
+                         pcfg["n_global"], workspace=ws32, stream=stream)
         else:
             fa.fa_fwd(qd, kd, vd, od, ld, scale, pcfg["mode"], pcfg["window"],
                       pcfg["n_global"], stream=stream)
@@ -473,7 +500,9 @@ def e2e_prefill(fa, pcfg, q, k, v, pflops, scale, stream, world, args, layout=No
     d2h = ho.numel() * ho.element_size() + hl.numel() * 4
     return {"value": aggregate(pflops * K, secs, world) / 1e12, "unit": "TFLOP/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": K,
-            "api": "tiled_attention_06_gb300.fa_fwd (C ABI fa_fwd) with pinned host buffers"}
+            "api": ("tiled_attention_06_gb300.fa_fwd_ex (C ABI fa_fwd_ex)" if ws32 is not None
+                    or layout is not None else "tiled_attention_06_gb300.fa_fwd (C ABI fa_fwd)")
+                   + " with pinned host buffers"}
 
 
 def e2e_decode(fa, di, dbytes, dscale, ws, dk, dv, stream, world, args):
@@ -841,7 +870,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="default",
-                    choices=["default", "causal2k", "causal4k", "noncausal4k", "window32k",
+                    choices=["default", "causal2k", "causal4k", "causal4k_f32", "noncausal4k",
+                             "window32k",
                              "band4k", "prefixlm4k", "blocksparse4k", "chunked", "multimodal",
                              "bwd4k",
                              "decode", "sweep"])

@@ -69,7 +69,8 @@ typedef enum {
   FA_ERR_BAD_PAGE = 5     /* a block-table entry or context length was out of range */
 } fa_status;
 
-enum { FA_F16 = 0, FA_BF16 = 1 };
+/* FA_F32: FP32 inputs and output, fa_fwd_ex over contiguous K/V only (see fa_fwd_params). */
+enum { FA_F16 = 0, FA_BF16 = 1, FA_F32 = 2 };
 enum {
   FA_MASK_NONE = 0,
   FA_MASK_CAUSAL = 1,
@@ -96,7 +97,8 @@ enum {
  *          FA_MASK_CAUSAL_WINDOW, window >= 0 for FA_MASK_BAND, n_global >= 0 for
  *          FA_MASK_PREFIX_LM; a parameter the mode does not use is ignored.
  *   dtype  FA_F16 or FA_BF16 (added before `stream`: a signature without it could
- *          not tell fp16 inputs from bf16 inputs)
+ *          not tell fp16 inputs from bf16 inputs). FA_F32 needs a workspace and is taken
+ *          by fa_fwd_ex only; fa_fwd returns FA_ERR_INVALID_ARG for it (Sq > 0).
  */
 fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                  int Sq, int Sk, int d, float scale, int mask_mode, int window, int n_global,
@@ -126,9 +128,24 @@ typedef struct fa_fwd_params {
   /* FA_MASK_BLOCK_SPARSE: device pointer to the layout described above (owned by the
    * caller, read during the call); ignored for the other masks. */
   const uint8_t* block_layout;
+  /* FA_F32 (FP32 q, k, v and o, same shapes): device scratch of at least
+   * fa_fwd_workspace_size(...) bytes, 16-byte aligned, owned by the caller and overwritten
+   * by the call; unused for 16-bit inputs. Each input element x is held there as
+   * hi = bf16(x) and lo = bf16(x - hi) (hi + lo = x to 2^-16 relative), and every product
+   * of the method (Q K^T and P V) is formed as hi*hi + hi*lo + lo*hi on the bf16 tensor
+   * cores with FP32 accumulation, P being split the same way; block_n is 64 (0 or 64
+   * accepted) and block_m 256 (0 or 256 accepted). Accuracy: the products' relative error
+   * stays near 2^-15, far inside the 1e-3 bound on O that FP32 inputs are held to. */
+  void* workspace;
+  size_t workspace_bytes;
 } fa_fwd_params;
 
 fa_status fa_fwd_ex(const fa_fwd_params* params, fa_stream_t stream);
+
+/* Bytes of workspace fa_fwd_ex needs: 4 * d * B * H * (Sq + 2 * Sk) for FA_F32 (a bf16
+ * high and low plane of every Q, K and V element), 0 for FA_F16 / FA_BF16 and for
+ * invalid sizes. */
+size_t fa_fwd_workspace_size(int B, int H, int Sq, int Sk, int d, int dtype);
 
 /* Query rows per tensor-core tile (128): the row granularity of the fa_fwd_ex trace. */
 int fa_fwd_block_m(void);

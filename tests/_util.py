@@ -8,20 +8,24 @@ import torch
 O_MAX = 2e-2
 O_MEAN = 2e-3
 LSE_MAX = 1e-3
+# FP32 inputs: max |dO| 1e-3 (the bound stated for FP32 inputs); mean one tenth of it,
+# the same ratio as the 16-bit bounds; LSE as for 16-bit inputs.
+O_MAX_F32 = 1e-3
+O_MEAN_F32 = 1e-4
 
 
 def to_np(t):
     return t.detach().float().cpu().double().numpy()
 
 
-def compare(o_gpu, lse_gpu, o_ref, lse_ref, what=""):
+def compare(o_gpu, lse_gpu, o_ref, lse_ref, what="", o_max=O_MAX, o_mean=O_MEAN):
     """Element-by-element comparison; -inf LSE must match exactly."""
     og = to_np(o_gpu).reshape(o_ref.shape)
     assert np.all(np.isfinite(og)), f"{what}: non-finite output"
     err = np.abs(og - o_ref)
     mx, mean = float(err.max(initial=0.0)), float(err.mean()) if err.size else 0.0
-    assert mx <= O_MAX, f"{what}: max |dO| {mx:.3e} > {O_MAX}"
-    assert mean <= O_MEAN, f"{what}: mean |dO| {mean:.3e} > {O_MEAN}"
+    assert mx <= o_max, f"{what}: max |dO| {mx:.3e} > {o_max}"
+    assert mean <= o_mean, f"{what}: mean |dO| {mean:.3e} > {o_mean}"
     if lse_gpu is not None:
         lg = to_np(lse_gpu).reshape(lse_ref.shape)
         ninf_ref = np.isneginf(lse_ref)

@@ -97,7 +97,8 @@ def _fwd(L, **kw):
     (dict(Sq=-1), fa.FA_ERR_INVALID_ARG),
     (dict(d=96), fa.FA_ERR_UNSUPPORTED),
     (dict(d=256), fa.FA_ERR_UNSUPPORTED),
-    (dict(dtype=2), fa.FA_ERR_UNSUPPORTED),
+    (dict(dtype=2), fa.FA_ERR_INVALID_ARG),  # FP32: fa_fwd_ex with a workspace only
+    (dict(dtype=3), fa.FA_ERR_UNSUPPORTED),
     (dict(mask_mode=5), fa.FA_ERR_INVALID_ARG),  # block-sparse without a layout
     (dict(mask_mode=6), fa.FA_ERR_INVALID_ARG),
     (dict(mask_mode=-1), fa.FA_ERR_INVALID_ARG),
@@ -123,6 +124,37 @@ def test_fwd_ex_rejects_bad_plan(L):
     p = fa.FwdParams(A, A, A, A, None, 1, 1, 4, 4, 64, 0.125, 0, 0, 0, 0, 0, 64, 0, 0, 0, None)
     assert L.fa_fwd_ex(ctypes.byref(p), None) == fa.FA_ERR_UNSUPPORTED
     assert L.fa_fwd_ex(None, None) == fa.FA_ERR_INVALID_ARG
+
+
+def test_fwd_workspace_size(L):
+    # FP32: a bf16 high and low plane of every Q, K, V element; nothing for 16-bit inputs
+    assert L.fa_fwd_workspace_size(4, 32, 4096, 4096, 128, fa.FA_F32) == 4 * 128 * 4 * 32 * 3 * 4096
+    assert L.fa_fwd_workspace_size(1, 2, 100, 7, 64, fa.FA_F32) == 4 * 64 * 2 * (100 + 14)
+    assert L.fa_fwd_workspace_size(1, 2, 100, 7, 64, fa.FA_BF16) == 0
+    assert L.fa_fwd_workspace_size(0, 2, 100, 7, 64, fa.FA_F32) == 0
+    assert fa.fa_fwd_workspace_size(1, 1, 0, 0, 64, fa.FA_F32) == 0
+
+
+def _fwd32(L, ws=A, wsb=None, block_n=0, block_m=0, Sq=4, Sk=4):
+    need = L.fa_fwd_workspace_size(1, 1, Sq, Sk, 64, fa.FA_F32)
+    p = fa.FwdParams(A, A, A, A, None, 1, 1, Sq, Sk, 64, 0.125, 0, 0, 0, fa.FA_F32, block_n,
+                     block_m, 0, 0, 0, None, None, ws, need if wsb is None else wsb)
+    return L.fa_fwd_ex(ctypes.byref(p), None)
+
+
+def test_fwd_f32_argument_checks(L):
+    assert _fwd32(L, ws=None) == fa.FA_ERR_INVALID_ARG
+    assert _fwd32(L, ws=A + 8) == fa.FA_ERR_INVALID_ARG
+    assert _fwd32(L, wsb=16) == fa.FA_ERR_INVALID_ARG
+    assert "needs" in fa.fa_last_error_string()
+    assert _fwd32(L, block_n=128) == fa.FA_ERR_UNSUPPORTED
+    assert _fwd32(L, block_m=128) == fa.FA_ERR_UNSUPPORTED
+    assert _fwd32(L, ws=None, Sq=0) == fa.FA_OK  # nothing to compute, nothing needed
+    # the paged prefill and the backward take 16-bit inputs only
+    assert L.fa_fwd_paged(A, A, A, A, A, A, None, 1, 1, 4, 64, 256, 1, 1, 0.125, 0, 0, 0,
+                          fa.FA_F32, None) == fa.FA_ERR_UNSUPPORTED
+    assert L.fa_bwd(A, A, A, A, A, A, A, A, A, A, 1 << 20, 1, 1, 4, 4, 64, 0.125, 0, 0, 0,
+                    fa.FA_F32, None) == fa.FA_ERR_UNSUPPORTED
 
 
 def _dec(L, **kw):

@@ -17,15 +17,15 @@ __all__ = [
     "fa_decode_workspace_size", "fa_decode_default_pages_per_split",
     "fa_get_device_status",
     "fa_selftest_timeout", "fa_last_error_string", "fa_version", "fa_fwd_block_m",
-    "fa_fwd_default_block_m", "fa_bwd", "fa_bwd_workspace_size",
+    "fa_fwd_default_block_m", "fa_bwd", "fa_bwd_workspace_size", "fa_fwd_workspace_size",
     "FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_CUDA", "FA_ERR_TIMEOUT",
-    "FA_ERR_BAD_PAGE", "FA_F16", "FA_BF16", "FA_MASK_NONE", "FA_MASK_CAUSAL",
+    "FA_ERR_BAD_PAGE", "FA_F16", "FA_BF16", "FA_F32", "FA_MASK_NONE", "FA_MASK_CAUSAL",
     "FA_MASK_CAUSAL_WINDOW", "FA_MASK_BAND", "FA_MASK_PREFIX_LM", "FA_MASK_BLOCK_SPARSE",
     "FA_LAYOUT_BLOCK",
 ]
 
 FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT, FA_ERR_BAD_PAGE = range(6)
-FA_F16, FA_BF16 = 0, 1
+FA_F16, FA_BF16, FA_F32 = 0, 1, 2
 FA_MASK_NONE, FA_MASK_CAUSAL, FA_MASK_CAUSAL_WINDOW, FA_MASK_BAND, FA_MASK_PREFIX_LM = 0, 1, 2, 3, 4
 FA_MASK_BLOCK_SPARSE = 5
 FA_LAYOUT_BLOCK = 128
@@ -51,7 +51,8 @@ class FwdParams(ctypes.Structure):
                 ("mask_mode", _i), ("window", _i), ("n_global", _i), ("dtype", _i),
                 ("block_n", _i), ("block_m", _i), ("num_ctas", _i), ("group_heads", _i),
                 ("timeout_us", _u32),
-                ("trace", _vp), ("block_layout", _vp)]
+                ("trace", _vp), ("block_layout", _vp), ("workspace", _vp),
+                ("workspace_bytes", _sz)]
 
 
 class DecodeParams(ctypes.Structure):
@@ -81,6 +82,8 @@ def lib():
         L.fa_fwd_block_m.argtypes = []
         L.fa_fwd_default_block_m.restype = _i
         L.fa_fwd_default_block_m.argtypes = [_i]
+        L.fa_fwd_workspace_size.restype = _sz
+        L.fa_fwd_workspace_size.argtypes = [_i] * 6
         L.fa_bwd_workspace_size.restype = _sz
         L.fa_bwd_workspace_size.argtypes = [_i, _i, _i]
         L.fa_bwd.restype = _i
@@ -139,7 +142,9 @@ def _dtype_code(t):
         return FA_F16
     if t.dtype == torch.bfloat16:
         return FA_BF16
-    raise FaError(FA_ERR_UNSUPPORTED, f"dtype {t.dtype} (float16 or bfloat16)")
+    if t.dtype == torch.float32:  # fa_fwd / fa_fwd_ex only; the other calls refuse it
+        return FA_F32
+    raise FaError(FA_ERR_UNSUPPORTED, f"dtype {t.dtype} (float16, bfloat16 or float32)")
 
 
 def _need_cuda_contig(**ts):
@@ -168,6 +173,10 @@ def fa_fwd_default_block_m(mask_mode):
     return lib().fa_fwd_default_block_m(mask_mode)
 
 
+def fa_fwd_workspace_size(B, H, Sq, Sk, d, dtype):
+    return lib().fa_fwd_workspace_size(B, H, Sq, Sk, d, dtype)
+
+
 def fa_bwd_workspace_size(B, H, Sq):
     return lib().fa_bwd_workspace_size(B, H, Sq)
 
@@ -191,7 +200,10 @@ def fa_fwd(q, k, v, o, lse, scale, mask_mode=FA_MASK_NONE, window=0, n_global=0,
     """O = softmax(scale Q K^T + mask) V into `o` (and LSE into `lse`, may be None).
 
     q [B,H,Sq,d], k/v [B,H,Sk,d], o like q, lse float32 [B,H,Sq]; CUDA, contiguous.
+    float32 inputs go through fa_fwd_ex, which needs a workspace (allocated here).
     """
+    if q.dtype == torch.float32:
+        return fa_fwd_ex(q, k, v, o, lse, scale, mask_mode, window, n_global, stream=stream)
     _need_cuda_contig(q=q, k=k, v=v, o=o, lse=lse)
     B, H, Sq, d = q.shape
     Sk = k.shape[2]
@@ -202,15 +214,23 @@ def fa_fwd(q, k, v, o, lse, scale, mask_mode=FA_MASK_NONE, window=0, n_global=0,
 
 def fa_fwd_ex(q, k, v, o, lse, scale, mask_mode=FA_MASK_NONE, window=0, n_global=0,
               block_n=0, block_m=0, num_ctas=0, group_heads=0, timeout_us=0, trace=None,
-              block_layout=None, stream=None):
+              block_layout=None, workspace=None, stream=None):
     """fa_fwd with the tuning and debug fields of fa_fwd_params. block_layout: uint8 CUDA
-    tensor [H, ceil(Sq/128), ceil(Sk/128)] for FA_MASK_BLOCK_SPARSE."""
-    _need_cuda_contig(q=q, k=k, v=v, o=o, lse=lse, trace=trace, block_layout=block_layout)
+    tensor [H, ceil(Sq/128), ceil(Sk/128)] for FA_MASK_BLOCK_SPARSE. workspace: CUDA byte
+    tensor of fa_fwd_workspace_size(...) bytes for float32 inputs (allocated here when
+    None)."""
+    _need_cuda_contig(q=q, k=k, v=v, o=o, lse=lse, trace=trace, block_layout=block_layout,
+                      workspace=workspace)
     B, H, Sq, d = q.shape
+    dt = _dtype_code(q)
+    if workspace is None and dt == FA_F32:
+        workspace = torch.empty(max(fa_fwd_workspace_size(B, H, Sq, k.shape[2], d, dt), 16),
+                                dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     p = FwdParams(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), _ptr(lse), B, H, Sq,
-                  k.shape[2], d, float(scale), mask_mode, window, n_global, _dtype_code(q),
+                  k.shape[2], d, float(scale), mask_mode, window, n_global, dt,
                   block_n, block_m, num_ctas, group_heads, timeout_us, _ptr(trace),
-                  _ptr(block_layout))
+                  _ptr(block_layout), _ptr(workspace), ws_bytes)
     _check(lib().fa_fwd_ex(ctypes.byref(p), _stream(stream)))
 
 

@@ -156,7 +156,14 @@ const fa::PrefillSched* plan_for(const fa::PrefillParams& p, int BM, int BN, int
   return out;
 }
 
-fa_status check_fwd(const fa_fwd_params& p) {
+size_t fwd_workspace_bytes(int B, int H, int Sq, int Sk, int d, int dtype) {
+  if (dtype != FA_F32 || B < 1 || H < 1 || Sq < 0 || Sk < 0 || d < 1) return 0;
+  // a bf16 high and low plane of every Q, K and V element
+  return static_cast<size_t>(4) * d * B * H * (static_cast<size_t>(Sq) + 2 * static_cast<size_t>(Sk));
+}
+
+// allow_f32: FP32 inputs are taken by fa_fwd_ex (contiguous K/V, with a workspace) only.
+fa_status check_fwd(const fa_fwd_params& p, bool allow_f32 = false) {
   // q and o may be null only when Sq == 0, k and v only when Sk == 0
   if ((p.Sq > 0 && (!p.q || !p.o)) || (p.Sk > 0 && (!p.k || !p.v)))
     return fail(FA_ERR_INVALID_ARG, "q, k, v and o must be non-null");
@@ -167,7 +174,9 @@ fa_status check_fwd(const fa_fwd_params& p) {
     return fail(FA_ERR_INVALID_ARG, "need B >= 1, H >= 1, Sq >= 0, Sk >= 0 (got %d %d %d %d)", p.B,
                 p.H, p.Sq, p.Sk);
   if (p.d != 64 && p.d != 128) return fail(FA_ERR_UNSUPPORTED, "head dim %d (supported: 64, 128)", p.d);
-  if (p.dtype != FA_F16 && p.dtype != FA_BF16) return fail(FA_ERR_UNSUPPORTED, "dtype %d", p.dtype);
+  if (p.dtype != FA_F16 && p.dtype != FA_BF16 && !(allow_f32 && p.dtype == FA_F32))
+    return fail(FA_ERR_UNSUPPORTED, "dtype %d%s", p.dtype,
+                p.dtype == FA_F32 ? " (FP32 inputs: fa_fwd_ex over contiguous K/V)" : "");
   if (!std::isfinite(p.scale)) return fail(FA_ERR_INVALID_ARG, "scale must be finite");
   if (p.mask_mode < FA_MASK_NONE || p.mask_mode > FA_MASK_BLOCK_SPARSE)
     return fail(FA_ERR_INVALID_ARG, "mask_mode %d", p.mask_mode);
@@ -188,6 +197,18 @@ fa_status check_fwd(const fa_fwd_params& p) {
   if (p.block_m != 0 && p.block_m != 128 && p.block_m != 256)
     return fail(FA_ERR_UNSUPPORTED, "block_m %d (supported: 128, 256)", p.block_m);
   if (p.num_ctas < 0 || p.group_heads < 0) return fail(FA_ERR_INVALID_ARG, "negative plan parameter");
+  if (p.dtype == FA_F32) {
+    if (p.block_n != 0 && p.block_n != fa::kSplitBlockN)
+      return fail(FA_ERR_UNSUPPORTED, "block_n %d with FA_F32 (supported: 64)", p.block_n);
+    if (p.block_m != 0 && p.block_m != 256)
+      return fail(FA_ERR_UNSUPPORTED, "block_m %d with FA_F32 (supported: 256)", p.block_m);
+    const size_t need = fwd_workspace_bytes(p.B, p.H, p.Sq, p.Sk, p.d, p.dtype);
+    if (p.Sq > 0 && (!p.workspace || !aligned16(p.workspace)))
+      return fail(FA_ERR_INVALID_ARG, "FA_F32 needs a 16-byte aligned workspace");
+    if (p.Sq > 0 && p.workspace_bytes < need)
+      return fail(FA_ERR_INVALID_ARG, "workspace has %zu bytes, FA_F32 needs %zu",
+                  p.workspace_bytes, need);
+  }
   return FA_OK;
 }
 
@@ -200,6 +221,10 @@ int fa_version(void) { return 100; }
 const char* fa_last_error_string(void) { return t_last_error.c_str(); }
 
 int fa_fwd_block_m(void) { return fa::prefill_tile_rows(); }
+
+size_t fa_fwd_workspace_size(int B, int H, int Sq, int Sk, int d, int dtype) {
+  return fwd_workspace_bytes(B, H, Sq, Sk, d, dtype);
+}
 
 int fa_fwd_default_block_m(int mask_mode) {
   if (mask_mode < FA_MASK_NONE || mask_mode > FA_MASK_BLOCK_SPARSE) return 0;
@@ -229,8 +254,9 @@ fa_status run_fwd(const fa_fwd_params& a, const PagedKV* pg, fa_stream_t stream)
   DeviceInfo dev;
   if ((st = device_info(&dev)) != FA_OK) return st;
 
-  const int BM = a.block_m ? a.block_m : fa_fwd_default_block_m(a.mask_mode);
-  const int BN = a.block_n ? a.block_n : 128;
+  const bool f32 = a.dtype == FA_F32;  // split into bf16 planes; 256-row items, 64-key blocks
+  const int BM = f32 ? 256 : (a.block_m ? a.block_m : fa_fwd_default_block_m(a.mask_mode));
+  const int BN = f32 ? fa::kSplitBlockN : (a.block_n ? a.block_n : 128);
   const int BH = a.B * a.H;
   fa::PrefillLaunch L;
   std::memset(&L, 0, sizeof L);
@@ -257,7 +283,7 @@ fa_status run_fwd(const fa_fwd_params& a, const PagedKV* pg, fa_stream_t stream)
     const long long band = 2LL * a.window + BM + BN;
     if (band < kv_keys) kv_keys = band;
   }
-  const long long kv_bytes = kv_keys * a.d * 4 + 1;
+  const long long kv_bytes = kv_keys * a.d * (f32 ? 8 : 4) + 1;
   long long hg = a.group_heads ? a.group_heads : (48LL << 20) / kv_bytes;
   if (hg < 1) hg = 1;
   if (hg > BH) hg = BH;
@@ -276,6 +302,29 @@ fa_status run_fwd(const fa_fwd_params& a, const PagedKV* pg, fa_stream_t stream)
   if (L.grid > p.total_items) L.grid = p.total_items;
   L.sched = plan_for(p, BM, BN, L.grid);
 
+  const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  if (f32) {
+    // workspace planes Q_hi Q_lo K_hi K_lo V_hi V_lo, each [B*H, S, d] bf16: the maps see
+    // a tensor's two planes as one [2*B*H, S, d] tensor
+    uint16_t* qh = static_cast<uint16_t*>(a.workspace);
+    const size_t nq = static_cast<size_t>(BH) * a.Sq * a.d, nk = static_cast<size_t>(BH) * a.Sk * a.d;
+    uint16_t* kh = qh + 2 * nq;
+    uint16_t* vh = kh + 2 * nk;
+    const fa::SplitArgs sa{{static_cast<const float*>(a.q), static_cast<const float*>(a.k),
+                            static_cast<const float*>(a.v)},
+                           {qh, kh, vh},
+                           {qh + nq, kh + nk, vh + nk},
+                           {nq / 8, nk / 8, nk / 8}};
+    cudaError_t e = fa::launch_split_bf16(sa, dev.sms, cs);
+    if (e != cudaSuccess) return cuda_fail(e, "split launch");
+    if ((st = make_map(&L.tmQ, qh, true, a.d, a.Sq, 2 * BH, fa::prefill_tile_rows())) != FA_OK)
+      return st;
+    if ((st = make_map(&L.tmK, a.Sk ? kh : qh, true, a.d, a.Sk, 2 * BH, BN)) != FA_OK) return st;
+    if ((st = make_map(&L.tmV, a.Sk ? vh : qh, true, a.d, a.Sk, 2 * BH, BN)) != FA_OK) return st;
+    e = fa::launch_prefill_split(L, a.d, cs);
+    if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+    return FA_OK;
+  }
   const bool bf16 = a.dtype == FA_BF16;
   if ((st = make_map(&L.tmQ, a.q, bf16, a.d, a.Sq, BH, fa::prefill_tile_rows())) != FA_OK)
     return st;
@@ -298,7 +347,7 @@ fa_status run_fwd(const fa_fwd_params& a, const PagedKV* pg, fa_stream_t stream)
     if ((st = make_map(&L.tmK, a.Sk ? a.k : a.q, bf16, a.d, a.Sk, BH, BN)) != FA_OK) return st;
     if ((st = make_map(&L.tmV, a.Sk ? a.v : a.q, bf16, a.d, a.Sk, BH, BN)) != FA_OK) return st;
   }
-  cudaError_t e = fa::launch_prefill(L, a.d, BN, BM, bf16, reinterpret_cast<cudaStream_t>(stream));
+  cudaError_t e = fa::launch_prefill(L, a.d, BN, BM, bf16, cs);
   if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
   return FA_OK;
 }
@@ -309,7 +358,7 @@ extern "C" {
 
 fa_status fa_fwd_ex(const fa_fwd_params* params, fa_stream_t stream) {
   if (!params) return fail(FA_ERR_INVALID_ARG, "params is null");
-  fa_status st = check_fwd(*params);
+  fa_status st = check_fwd(*params, true);
   if (st != FA_OK) return st;
   return run_fwd(*params, nullptr, stream);
 }
@@ -379,6 +428,10 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
   p.window = window;
   p.n_global = n_global;
   p.dtype = dtype;
+  if (dtype == FA_F32 && Sq > 0)
+    return fail(FA_ERR_INVALID_ARG,
+                "FA_F32 inputs need a workspace: call fa_fwd_ex with params.workspace of "
+                "fa_fwd_workspace_size() bytes");
   return fa_fwd_ex(&p, stream);
 }
 

@@ -15,7 +15,7 @@ namespace fa {
 enum : uint32_t { FA_DEV_TIMEOUT = 1u, FA_DEV_BAD_PAGE = 2u };
 
 struct PrefillParams {
-  void* o;            // [B,H,Sq,D] 16-bit
+  void* o;            // [B,H,Sq,D] 16-bit (FP32 for FP32 inputs)
   float* lse;         // [B,H,Sq] or nullptr
   int BH, Sq, Sk;
   int nmb, nnb;       // query blocks (BM rows per work item), key blocks (BN keys)
@@ -50,6 +50,20 @@ struct PrefillLaunch {
 int prefill_tile_rows();
 cudaError_t launch_prefill(const PrefillLaunch& L, int D, int BN, int BM, bool bf16,
                            cudaStream_t stream);
+
+// FP32 inputs. Step 1 splits Q, K and V (n8[t] groups of 8 elements each) into bf16 high
+// and low planes; step 2 is the 256-row prefill kernel over those planes (tensor maps of
+// [2*BH, S, d] bf16: plane bh the high parts, BH + bh the low parts) with key blocks of
+// kSplitBlockN, writing FP32 O.
+constexpr int kSplitBlockN = 64;
+struct SplitArgs {
+  const float* src[3];
+  uint16_t* hi[3];
+  uint16_t* lo[3];
+  size_t n8[3];
+};
+cudaError_t launch_split_bf16(const SplitArgs& a, int sms, cudaStream_t stream);
+cudaError_t launch_prefill_split(const PrefillLaunch& L, int D, cudaStream_t stream);
 
 // Backward: what the kernels read besides the forward's parameters.
 struct BwdParams {

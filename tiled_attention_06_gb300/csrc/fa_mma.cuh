@@ -17,20 +17,21 @@ constexpr int kMmaM = 128;  // rows of one tcgen05 M=128 tile (= TMEM lanes)
 // one region per 64 elements of d). The descriptors are built once; each MMA adds a
 // compile-time offset to the start-address field (addresses stay below 256 KB, so the
 // 14-bit field never carries), which keeps the issuing thread's dependency chain short.
-template <int D, int BN, bool BF16>
+// ACC: add to S instead of overwriting it.
+template <int D, int BN, bool BF16, bool ACC = false>
 __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_smem, uint32_t k_smem) {
   constexpr uint32_t id = idesc_f16(BF16, kMmaM, BN, false);
   const uint64_t a0 = smem_desc_sw128(q_smem, 16, 1024);
   const uint64_t b0 = smem_desc_sw128(k_smem, 16, 1024);
   if constexpr (D == 128) {
     constexpr int QC = kMmaM * 128 / 16, KC = BN * 128 / 16;  // next 64-element region
-    umma_ss8<2, 4, 6, QC, QC + 2, QC + 4, QC + 6, 2, 4, 6, KC, KC + 2, KC + 4, KC + 6>(d_tmem, a0,
-                                                                                       b0, id);
+    umma_ss8<2, 4, 6, QC, QC + 2, QC + 4, QC + 6, 2, 4, 6, KC, KC + 2, KC + 4, KC + 6, ACC>(
+        d_tmem, a0, b0, id);
   } else {
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk)
       umma_ss(d_tmem, a0 + static_cast<uint64_t>(kk * 2), b0 + static_cast<uint64_t>(kk * 2), id,
-              kk > 0);
+              (ACC || kk > 0) ? 1u : 0u);
   }
 }
 

@@ -119,15 +119,20 @@ __device__ __forceinline__ uint32_t pack2(float a, float b, bool bf16) {
 // columns at o_col) and l are rescaled when the max rose by more than kTau (warp-uniform
 // decision; `before_rescale` makes O safe to touch and returns false on abort); and
 // P = 2^(S*sl2 - m) is written as packed 16-bit pairs to NC/2 columns at p_col.
+// SPLIT (FP32 inputs): P is written as two bf16 parts, P_hi = bf16(P) at p_col and
+// P_lo = bf16(P - P_hi) at p_col + NC/2, so that P_hi + P_lo holds P to 2^-16.
 // l accumulates the sum over this thread's NC columns. Returns false on abort.
-template <int NC, int ON, bool BF16, int POLY, typename Exchange, typename PreRescale>
+template <int NC, int ON, bool BF16, int POLY, bool SPLIT, typename Exchange,
+          typename PreRescale>
 __device__ __forceinline__ bool softmax_cols(uint32_t t_lane, uint32_t s_col, uint32_t p_col,
                                              uint32_t o_col, bool full, int n0, int pos_q,
                                              int sk, const PrefillParams& p, float& m_ref,
                                              float& l, Exchange exchange,
                                              PreRescale before_rescale) {
   static_assert(NC == 32 || NC % 64 == 0, "column count");
+  static_assert(!SPLIT || (BF16 && NC % 64 == 0 && POLY == 0), "split P: bf16, 64-column groups");
   uint32_t s[NC];
+  uint32_t lo[SPLIT ? NC / 2 : 1];
   if constexpr (NC == 32) {
     tmem_ld32(t_lane + s_col, s);
   } else {
@@ -209,7 +214,11 @@ __device__ __forceinline__ bool softmax_cols(uint32_t t_lane, uint32_t s_col, ui
         p1 = ex2_approx(x1);
       }
       acc[(c / 2) & 3] = f2_add(acc[(c / 2) & 3], f2(p0, p1));
-      s[c / 2] = BF16 ? cvt_pack_bf16(p0, p1) : cvt_pack_f16(p0, p1);
+      const uint32_t hi = BF16 ? cvt_pack_bf16(p0, p1) : cvt_pack_f16(p0, p1);
+      s[c / 2] = hi;
+      if constexpr (SPLIT)  // residuals against the bf16 values (low half: p0)
+        lo[c / 2] = cvt_pack_bf16(p0 - __uint_as_float(hi << 16),
+                                  p1 - __uint_as_float(hi & 0xffff0000u));
     }
   };
   if constexpr (POLY > 0) {
@@ -229,24 +238,29 @@ __device__ __forceinline__ bool softmax_cols(uint32_t t_lane, uint32_t s_col, ui
 #pragma unroll
     for (int c = 0; c < NC / 64; ++c) tmem_st32(t_lane + p_col + c * 32, s + c * 32);
   }
+  if constexpr (SPLIT) {
+#pragma unroll
+    for (int c = 0; c < NC / 64; ++c) tmem_st32(t_lane + p_col + NC / 2 + c * 32, lo + c * 32);
+  }
   tmem_st_wait();
   return true;
 }
 
 // A whole row per thread.
-template <int D, int BN, bool BF16, typename PreRescale>
+template <int D, int BN, bool BF16, bool SPLIT, typename PreRescale>
 __device__ __forceinline__ bool softmax_tile(uint32_t t_lane, uint32_t s_col, uint32_t o_col,
                                              bool full, int n0, int pos_q, int sk,
                                              const PrefillParams& p, float& m_ref, float& l,
                                              PreRescale before_rescale) {
   // (a whole row of S in registers leaves no room for the polynomial's temporaries)
-  return softmax_cols<BN, D, BF16, 0>(t_lane, s_col, s_col, o_col, full, n0, pos_q, sk, p, m_ref,
-                                   l, [](float m) { return m; }, before_rescale);
+  return softmax_cols<BN, D, BF16, 0, SPLIT>(t_lane, s_col, s_col, o_col, full, n0, pos_q, sk,
+                                             p, m_ref, l, [](float m) { return m; },
+                                             before_rescale);
 }
 
-// Epilogue for one thread's row: O (D columns at o_col) / l rounded to the dtype, and
-// LSE = (m + log2 l) ln 2. Rows past Sq are not stored.
-template <int D, bool BF16>
+// Epilogue for one thread's row: O (D columns at o_col) / l rounded to the dtype (FP32
+// when OUT_F32), and LSE = (m + log2 l) ln 2. Rows past Sq are not stored.
+template <int D, bool BF16, bool OUT_F32 = false>
 __device__ __forceinline__ void store_row(uint32_t t_lane, uint32_t o_col, bool valid,
                                           size_t orow, float m_ref, float l,
                                           const PrefillParams& p) {
@@ -256,7 +270,15 @@ __device__ __forceinline__ void store_row(uint32_t t_lane, uint32_t o_col, bool 
     uint32_t ov[32];
     tmem_ld32(t_lane + o_col + c * 32, ov);
     tmem_ld_wait<32>(ov);
-    if (valid) {
+    if (OUT_F32 && valid) {
+      float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + orow * D + c * 32);
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        dst[e] = make_float4(__uint_as_float(ov[4 * e]) * inv_l,
+                             __uint_as_float(ov[4 * e + 1]) * inv_l,
+                             __uint_as_float(ov[4 * e + 2]) * inv_l,
+                             __uint_as_float(ov[4 * e + 3]) * inv_l);
+    } else if (valid) {
       uint32_t pk[16];
 #pragma unroll
       for (int e = 0; e < 16; ++e)
@@ -272,10 +294,11 @@ __device__ __forceinline__ void store_row(uint32_t t_lane, uint32_t o_col, bool 
     p.lse[orow] = l > 0.f ? (m_ref + lg2_approx(l)) * 0.69314718055994531f : -INFINITY;
 }
 
-template <int D>
+template <int D, bool OUT_F32 = false>
 __device__ __forceinline__ void store_zero_row(size_t orow, const PrefillParams& p) {
-  uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + orow * D);
-  for (int c = 0; c < D / 8; ++c) dst[c] = make_uint4(0, 0, 0, 0);
+  constexpr int ESZ = OUT_F32 ? 4 : 2;  // bytes per element
+  uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.o) + orow * D * ESZ);
+  for (int c = 0; c < D * ESZ / 16; ++c) dst[c] = make_uint4(0, 0, 0, 0);
   if (p.lse) p.lse[orow] = -INFINITY;
 }
 
@@ -326,12 +349,16 @@ constexpr int kMmaWarp256 = 9;
 constexpr uint32_t kRegsSoftmax = 200;
 constexpr uint32_t kRegsProducer = 104;
 
-template <int D, int BN>
+// SPLIT (FP32 inputs): every Q, K and V tile is held as two bf16 planes, the high parts
+// then the low parts.
+template <int D, int BN, bool SPLIT = false>
 struct Cfg256 {
   static constexpr int KCH = D / 64;
-  static constexpr int QT_BYTES = kTile * D * 2;     // one 128-row Q tile
-  static constexpr int Q_BYTES = 2 * QT_BYTES;
-  static constexpr int TILE_BYTES = BN * D * 2;      // one K or V tile
+  static constexpr int PLANES = SPLIT ? 2 : 1;
+  static constexpr int QT_BYTES = kTile * D * 2;     // one plane of one 128-row Q tile
+  static constexpr int Q_BYTES = 2 * PLANES * QT_BYTES;
+  static constexpr int PLANE_BYTES = BN * D * 2;     // one plane of one K or V tile
+  static constexpr int TILE_BYTES = PLANES * PLANE_BYTES;
   static constexpr int BAR_BYTES = 1024;
   static constexpr int NSLOT_FIT = (int)((kSmemLimit - 1024 - BAR_BYTES - Q_BYTES) / TILE_BYTES);
   static constexpr int NSLOT = NSLOT_FIT > 8 ? 8 : NSLOT_FIT;
@@ -351,13 +378,17 @@ struct Bars256 {
   uint32_t abort;
 };
 
-template <int D, int BN, bool BF16, bool SPARSE>
+// SPLIT: FP32 inputs given as bf16 high and low planes (the tensor maps' planes bh and
+// BH + bh); each product is formed as hi*hi + hi*lo + lo*hi in the FP32 accumulator, P is
+// split the same way in TMEM, and O is written in FP32.
+template <int D, int BN, bool BF16, bool SPARSE, bool SPLIT>
 __global__ void __launch_bounds__(kThreads256, 1)
     prefill_bm256_kernel(const __grid_constant__ CUtensorMap tmQ,
                          const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV, const PrefillParams p,
                          const __grid_constant__ PrefillSched sched) {
-  using C = Cfg256<D, BN>;
+  using C = Cfg256<D, BN, SPLIT>;
+  static_assert(!SPLIT || BF16, "split planes are bf16");
   constexpr int BM = 2 * kTile;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -426,10 +457,12 @@ __global__ void __launch_bounds__(kThreads256, 1)
         if (n == 0) continue;
         for (int q = 0; q < 2 && ok; ++q) {
           if (ii > 0 && !(ok = mbar_wait(B(bars->q_empty[q]), (ii - 1) & 1, wc))) break;
-          if (leader) mbar_arrive_expect_tx(B(bars->q_full[q]), C::QT_BYTES);
-          if (leader) for (int c = 0; c < C::KCH; ++c)
-            tma_load_3d(sQ + q * C::QT_BYTES + c * (kTile * 128), &tmQ, B(bars->q_full[q]),
-                        c * 64, mb * BM + q * kTile, bh);
+          if (leader) mbar_arrive_expect_tx(B(bars->q_full[q]), C::PLANES * C::QT_BYTES);
+          if (leader)
+            for (int h = 0; h < C::PLANES; ++h)
+              for (int c = 0; c < C::KCH; ++c)
+                tma_load_3d(sQ + (q * C::PLANES + h) * C::QT_BYTES + c * (kTile * 128), &tmQ,
+                            B(bars->q_full[q]), c * 64, mb * BM + q * kTile, bh + h * p.BH);
           qfills[q] = ii + 1;
         }
         int nb = -1;
@@ -444,8 +477,10 @@ __global__ void __launch_bounds__(kThreads256, 1)
           kv_tile_coords(p, bh, nb * BN, leader, y, z);
           const void* map = (s & 1) ? (const void*)&tmV : (const void*)&tmK;
           if (leader)
-            for (int c = 0; c < C::KCH; ++c)
-              tma_load_3d(dst + c * (BN * 128), map, B(bars->full[slot]), c * 64, y, z);
+            for (int h = 0; h < C::PLANES; ++h)
+              for (int c = 0; c < C::KCH; ++c)
+                tma_load_3d(dst + h * C::PLANE_BYTES + c * (BN * 128), map, B(bars->full[slot]),
+                            c * 64, y, z + h * p.BH);
           fills[slot] = use + 1;
           ++pos;
         }
@@ -465,6 +500,24 @@ __global__ void __launch_bounds__(kThreads256, 1)
       const bool leader = elect_one();
       const uint32_t tS[2] = {tmem, tmem + BN};
       const uint32_t tO[2] = {tmem + 2 * BN, tmem + 2 * BN + D};
+      // S_q = Q_q K^T and O_q (+)= P_q V with the operands in ring slot `slot` (issuing lane)
+      auto qk = [&](int q, int slot) {
+        const uint32_t qa = sQ + q * C::PLANES * C::QT_BYTES;
+        const uint32_t kb = sRing + slot * C::TILE_BYTES;
+        issue_qk<D, BN, BF16>(tS[q], qa, kb);
+        if constexpr (SPLIT) {  // + Q_hi K_lo + Q_lo K_hi
+          issue_qk<D, BN, BF16, true>(tS[q], qa, kb + C::PLANE_BYTES);
+          issue_qk<D, BN, BF16, true>(tS[q], qa + C::QT_BYTES, kb);
+        }
+      };
+      auto pv = [&](int q, int slot, bool acc) {
+        const uint32_t vb = sRing + slot * C::TILE_BYTES;
+        issue_pv<D, BN, BF16>(tO[q], tS[q], vb, acc);
+        if constexpr (SPLIT) {  // + P_hi V_lo + P_lo V_hi
+          issue_pv<D, BN, BF16>(tO[q], tS[q], vb + C::PLANE_BYTES, true);
+          issue_pv<D, BN, BF16>(tO[q], tS[q] + BN / 2, vb, true);
+        }
+      };
       uint32_t pos = 0, ii = 0, tc = 0;
       bool ok = true;
       int t;
@@ -481,8 +534,7 @@ __global__ void __launch_bounds__(kThreads256, 1)
           for (int q = 0; q < 2 && ok; ++q) {
             if (!(ok = mbar_wait(B(bars->q_full[q]), ii & 1, wc))) break;
             tc_fence_after();
-            if (leader)
-              issue_qk<D, BN, BF16>(tS[q], sQ + q * C::QT_BYTES, sRing + slot * C::TILE_BYTES);
+            if (leader) qk(q, slot);
             if (leader) umma_commit(B(bars->s_full[q]));
             if (leader && n == 1) umma_commit(B(bars->q_empty[q]));
           }
@@ -502,8 +554,7 @@ __global__ void __launch_bounds__(kThreads256, 1)
               if (!(ok = mbar_wait(B(bars->o_empty[q]), (ii - 1) & 1, wc))) break;
               tc_fence_after();
             }
-            if (leader)
-              issue_pv<D, BN, BF16>(tO[q], tS[q], sRing + vslot * C::TILE_BYTES, j > 0);
+            if (leader) pv(q, vslot, j > 0);
             if (leader && j == n - 1) umma_commit(B(bars->pv_done[q]));
             if (leader && q == 1) umma_commit(B(bars->empty[vslot]));
             if (j + 1 < n) {  // S(j+1) overwrites P(j) only after PV(j) in the pipe
@@ -511,9 +562,7 @@ __global__ void __launch_bounds__(kThreads256, 1)
                 if (!(ok = mbar_wait(B(bars->full[kslot]), ((pos + 1) / C::NSLOT) & 1, wc))) break;
                 tc_fence_after();
               }
-              if (leader)
-                issue_qk<D, BN, BF16>(tS[q], sQ + q * C::QT_BYTES,
-                                      sRing + kslot * C::TILE_BYTES);
+              if (leader) qk(q, kslot);
               if (leader) umma_commit(B(bars->s_full[q]));
               if (leader && j + 2 == n) umma_commit(B(bars->q_empty[q]));
               if (leader && q == 1) umma_commit(B(bars->empty[kslot]));
@@ -553,7 +602,7 @@ __global__ void __launch_bounds__(kThreads256, 1)
       const int qrow = m0 + row;
       const size_t orow = static_cast<size_t>(bh) * p.Sq + qrow;
       if (n == 0) {  // nothing visible for any row of the item
-        if (qrow < p.Sq) store_zero_row<D>(orow, p);
+        if (qrow < p.Sq) store_zero_row<D, SPLIT>(orow, p);
         continue;
       }
       const auto mine = item_range<SPARSE>(m0, min(m0 + kTile, p.Sq), BN, sk, p, bh);
@@ -576,7 +625,7 @@ __global__ void __launch_bounds__(kThreads256, 1)
                                m0 / kTile) * p.nnb + nb,
                     16 + (full ? 2 : 1));
         // S(j) was issued after PV(j-1), so O needs no wait before a rescale
-        ok = softmax_tile<D, BN, BF16>(t_lane, s_col, o_col, full, nb * BN, pos_q, sk_t, p,
+        ok = softmax_tile<D, BN, BF16, SPLIT>(t_lane, s_col, o_col, full, nb * BN, pos_q, sk_t, p,
                                        m_ref, l, [] { return true; });
         tc_fence_before();
         mbar_arrive(B(bars->p_full[q]));
@@ -587,7 +636,7 @@ __global__ void __launch_bounds__(kThreads256, 1)
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      store_row<D, BF16>(t_lane, o_col, qrow < p.Sq, orow, m_ref, l, p);
+      store_row<D, BF16, SPLIT>(t_lane, o_col, qrow < p.Sq, orow, m_ref, l, p);
       tc_fence_before();
       mbar_arrive(B(bars->o_empty[q]));
       ++ii;
@@ -1007,7 +1056,7 @@ __global__ void __launch_bounds__(kThreads128, 1)
           return w;
         };
         const uint32_t s_col = (g & 1) * BN;
-        ok = softmax_cols<BN / 2, D / 2, BF16, kExp2Poly>(t_lane, s_col + half * (BN / 2),
+        ok = softmax_cols<BN / 2, D / 2, BF16, kExp2Poly, false>(t_lane, s_col + half * (BN / 2),
                                                s_col + half * (BN / 4),
                                                2 * BN + buf * D + half * (D / 2), full,
                                                nb * BN + half * (BN / 2), pos_q, it.sk, p, m_ref,
@@ -1040,11 +1089,11 @@ __global__ void __launch_bounds__(kThreads128, 1)
   }
 }
 
-template <int D, int BN, bool BF16, bool SPARSE>
+template <int D, int BN, bool BF16, bool SPARSE, bool SPLIT = false>
 cudaError_t launch_k(const PrefillLaunch& L, int BM, cudaStream_t stream) {
-  if (BM == 256) {
-    auto kern = prefill_bm256_kernel<D, BN, BF16, SPARSE>;
-    constexpr int smem = Cfg256<D, BN>::SMEM;
+  if (SPLIT || BM == 256) {
+    auto kern = prefill_bm256_kernel<D, BN, BF16, SPARSE, SPLIT>;
+    constexpr int smem = Cfg256<D, BN, SPLIT>::SMEM;
     // setmaxnreg.inc can only hand out registers the CTA was launched with; a build whose
     // launch register count is below the split would make the softmax warps wait forever,
     // so such a build is refused here instead of launched.
@@ -1056,7 +1105,7 @@ cudaError_t launch_k(const PrefillLaunch& L, int BM, cudaStream_t stream) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     kern<<<L.grid, kThreads256, smem, stream>>>(L.tmQ, L.tmK, L.tmV, L.p, *L.sched);
-  } else {
+  } else if constexpr (!SPLIT) {
     auto kern = prefill_bm128_kernel<D, BN, BF16, SPARSE>;
     constexpr int smem = Cfg128<D, BN>::SMEM;
     cudaFuncAttributes fattr;
@@ -1072,14 +1121,52 @@ cudaError_t launch_k(const PrefillLaunch& L, int BM, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+#ifndef FA_PREFILL_SPLIT_TU
 template <int D, int BN, bool BF16>
 cudaError_t launch_t(const PrefillLaunch& L, int BM, cudaStream_t stream) {
   return L.p.mask_mode == FA_MASK_BLOCK_SPARSE ? launch_k<D, BN, BF16, true>(L, BM, stream)
                                                : launch_k<D, BN, BF16, false>(L, BM, stream);
 }
+#else
+// FP32 inputs, step 1: x -> (hi, lo) = (bf16(x), bf16(x - hi)), eight elements per
+// thread and iteration, over the three tensors Q, K, V in one launch. x - hi is exact in
+// FP32 (hi is x rounded to 8 significant bits), so hi + lo equals x to 2^-16 relative:
+// the split of the "bf16x3" products of Henry, Tang and Heinecke, "Leveraging the bfloat16
+// Artificial Intelligence Datatype For Higher-Precision Computations" (ARITH 2019).
+__global__ void __launch_bounds__(256) split_bf16_kernel(const SplitArgs a) {
+  const size_t n0 = a.n8[0], n01 = n0 + a.n8[1], total = n01 + a.n8[2];
+  const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+  for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += stride) {
+    const int t = i < n0 ? 0 : (i < n01 ? 1 : 2);
+    const size_t j = i - (t == 0 ? 0 : (t == 1 ? n0 : n01));
+    const float* src = t == 0 ? a.src[0] : (t == 1 ? a.src[1] : a.src[2]);
+    uint16_t* hi = t == 0 ? a.hi[0] : (t == 1 ? a.hi[1] : a.hi[2]);
+    uint16_t* lo = t == 0 ? a.lo[0] : (t == 1 ? a.lo[1] : a.lo[2]);
+    const float4* x4 = reinterpret_cast<const float4*>(src) + 2 * j;
+    const float4 u = __ldcs(x4), w = __ldcs(x4 + 1);
+    const float x[8] = {u.x, u.y, u.z, u.w, w.x, w.y, w.z, w.w};
+    uint32_t h[4], l[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      h[e] = cvt_pack_bf16(x[2 * e], x[2 * e + 1]);  // low half: the even element
+      l[e] = cvt_pack_bf16(x[2 * e] - __uint_as_float(h[e] << 16),
+                           x[2 * e + 1] - __uint_as_float(h[e] & 0xffff0000u));
+    }
+    reinterpret_cast<uint4*>(hi)[j] = make_uint4(h[0], h[1], h[2], h[3]);
+    reinterpret_cast<uint4*>(lo)[j] = make_uint4(l[0], l[1], l[2], l[3]);
+  }
+}
+
+template <int D, bool SPARSE>
+cudaError_t launch_split_t(const PrefillLaunch& L, cudaStream_t stream) {
+  return launch_k<D, kSplitBlockN, true, SPARSE, true>(L, 256, stream);
+}
+#endif
 
 }  // namespace
 
+#ifndef FA_PREFILL_SPLIT_TU
 int prefill_tile_rows() { return kTile; }
 
 cudaError_t launch_prefill(const PrefillLaunch& L, int D, int BN, int BM, bool bf16,
@@ -1098,5 +1185,24 @@ cudaError_t launch_prefill(const PrefillLaunch& L, int D, int BN, int BM, bool b
 #undef FA_CASE
   return cudaErrorInvalidValue;
 }
+#else
+cudaError_t launch_split_bf16(const SplitArgs& a, int sms, cudaStream_t stream) {
+  const size_t total = a.n8[0] + a.n8[1] + a.n8[2];
+  if (total == 0) return cudaSuccess;
+  size_t blocks = (total + 255) / 256;
+  const size_t cap = static_cast<size_t>(sms > 0 ? sms : 1) * 8;  // 8 x 256 threads per SM
+  if (blocks > cap) blocks = cap;
+  split_bf16_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prefill_split(const PrefillLaunch& L, int D, cudaStream_t stream) {
+  const bool sparse = L.p.mask_mode == FA_MASK_BLOCK_SPARSE;
+  if (D == 64) return sparse ? launch_split_t<64, true>(L, stream) : launch_split_t<64, false>(L, stream);
+  if (D == 128)
+    return sparse ? launch_split_t<128, true>(L, stream) : launch_split_t<128, false>(L, stream);
+  return cudaErrorInvalidValue;
+}
+#endif
 
 }  // namespace fa

@@ -176,10 +176,11 @@ __device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64
 
 // Eight SS MMAs into one accumulator, in one PTX block: operand descriptors are the
 // bases a0/b0 plus the immediate offsets A1..A7 / B1..B7 (in 16-byte units); the
-// first MMA overwrites D, the rest accumulate.
-#define FA_UMMA_SS8_BODY                                                              \
+// first MMA overwrites D (FIRST = "ne", a false predicate) or accumulates ("eq"), the
+// rest accumulate.
+#define FA_UMMA_SS8_BODY(FIRST)                                                       \
   "{\n\t.reg .pred pf, pt;\n\t.reg .b64 da, db;\n\t"                              \
-  "setp.ne.b32 pf, %3, %3;\n\tsetp.eq.b32 pt, %3, %3;\n\t"                          \
+  "setp." FIRST ".b32 pf, %3, %3;\n\tsetp.eq.b32 pt, %3, %3;\n\t"                   \
   "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, pf;\n\t"                     \
   "add.s64 da, %1, %4;\n\tadd.s64 db, %2, %11;\n\t"                                 \
   "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, pt;\n\t"                     \
@@ -197,13 +198,19 @@ __device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64
   "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, pt;\n\t}"
 
 template <int A1, int A2, int A3, int A4, int A5, int A6, int A7, int B1, int B2, int B3,
-          int B4, int B5, int B6, int B7>
+          int B4, int B5, int B6, int B7, bool ACC = false>
 __device__ __forceinline__ void umma_ss8(uint32_t d_tmem, uint64_t a0, uint64_t b0,
                                          uint32_t idesc) {
-  asm volatile(FA_UMMA_SS8_BODY::"r"(d_tmem), "l"(a0), "l"(b0), "r"(idesc), "n"(A1), "n"(A2),
-               "n"(A3), "n"(A4), "n"(A5), "n"(A6), "n"(A7), "n"(B1), "n"(B2), "n"(B3), "n"(B4),
-               "n"(B5), "n"(B6), "n"(B7)
-               : "memory");
+  if constexpr (ACC)
+    asm volatile(FA_UMMA_SS8_BODY("eq")::"r"(d_tmem), "l"(a0), "l"(b0), "r"(idesc), "n"(A1),
+                 "n"(A2), "n"(A3), "n"(A4), "n"(A5), "n"(A6), "n"(A7), "n"(B1), "n"(B2), "n"(B3),
+                 "n"(B4), "n"(B5), "n"(B6), "n"(B7)
+                 : "memory");
+  else
+    asm volatile(FA_UMMA_SS8_BODY("ne")::"r"(d_tmem), "l"(a0), "l"(b0), "r"(idesc), "n"(A1),
+                 "n"(A2), "n"(A3), "n"(A4), "n"(A5), "n"(A6), "n"(A7), "n"(B1), "n"(B2), "n"(B3),
+                 "n"(B4), "n"(B5), "n"(B6), "n"(B7)
+                 : "memory");
 }
 
 // Eight TS MMAs (A from TMEM at a_tmem + 8k columns, B descriptor b0 + k*BSTEP): the

@@ -26,6 +26,19 @@ def prefill_inputs(B, H, Sq, Sk, d, dtype=torch.float16, factor=1.0, seed=0):
     return q, k, v
 
 
+def f32_resolution_inputs(B, H, Sq, Sk, d, seed=0):
+    """float32 q, k ~ N(0,1) * 2 and v ~ 1 + N(0,1) / 4: with scale 1/8 and d = 64 the
+    logits spread over about +-10, and V's values sit near 1, where bf16's step is 2^-7.
+
+    Draw order: q, k, v.
+    """
+    g = torch.Generator().manual_seed(seed)
+    q = torch.randn(B, H, Sq, d, generator=g) * 2.0
+    k = torch.randn(B, H, Sk, d, generator=g) * 2.0
+    v = 1.0 + torch.randn(B, H, Sk, d, generator=g) / 4.0
+    return q, k, v
+
+
 @dataclass
 class DecodeInputs:
     q: torch.Tensor            # [B,H,d]
