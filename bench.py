@@ -67,19 +67,22 @@ MODE_NAME = {0: "none", 1: "causal", 2: "causal_window", 3: "band", 4: "prefix_l
 # capture of each kernel, with the SHA-256 of the kernel sources it was taken on; the
 # figure is reported only while those sources are unchanged. Summaries: profiles/.
 NCU_TRAFFIC = {
-    # prefill_bm256_kernel, causal 4k B4 H16 capture: 210.0 MB read + 44.9 MB written,
+    # prefill_bm256_kernel, causal 4k B4 H16 capture: 209.9 MB read + 44.9 MB written,
     # scaled x2 to B4 H32
-    "prefill": {"bytes": 509.9e6,
+    "prefill": {"bytes": 509.66e6,
                 "sources": ['fa_prefill.cu', 'fa_mma.cuh', 'fa_ptx.cuh', 'fa_plan.h', 'fa_internal.h'],
-                "sha256": "dadd82474dedcecc15e5acb626be3e0d5c7d3fb9712f4823f4121c2002f89bdf"},
+                "sha256": "b7e4ab2327cfbbbfde58dc5fcf910fb7190965025cd61fa74ad05e372389afa8"},
     # paged decode B8 capture: 547.5 MB read + 3.9 MB written for 547.5 MB algorithmic,
     # scaled to the bench call's 2410.7 MB algorithmic
     "decode": {"bytes": 2.4278e9, "sources": ['fa_decode.cu', 'fa_ptx.cuh', 'fa_internal.h'],
                "sha256": "3ec77d7ddf3681b62ba8e849bf549f1385f5998dccb94cc92541a7462b7a836c"},
-    # FP32 inputs: not captured yet
-    "prefill_f32": {"bytes": None, "sources": ['fa_prefill.cu', 'fa_prefill_split.cu',
-                                               'fa_mma.cuh', 'fa_ptx.cuh', 'fa_plan.h',
-                                               'fa_internal.h'], "sha256": None},
+    # FP32 inputs, causal 4k B4 H16 capture of one call: split_bf16_kernel 402.7 MB read +
+    # 346.1 MB written, prefill_bm256_kernel (split) 408.7 MB read + 108.7 MB written;
+    # scaled x2 to B4 H32
+    "prefill_f32": {"bytes": 2532.4e6,
+                    "sources": ['fa_prefill.cu', 'fa_prefill_split.cu', 'fa_mma.cuh', 'fa_ptx.cuh',
+                                'fa_plan.h', 'fa_internal.h'],
+                    "sha256": "23801671820a0eb2ce009e5c311f59fbc684673078861974fa757874b33c1eec"},
 }
 
 

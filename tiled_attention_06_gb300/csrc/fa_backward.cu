@@ -20,8 +20,10 @@
 // The dQ kernel recomputes S and dP rather than exchanging dS with the dK/dV kernel, so
 // no FP32 atomics and no second pass over dQ are needed.
 //
-// Roles (192 threads): warps 0-3 elementwise + epilogue (one TMEM lane per thread), warp 4
-// TMA, warp 5 MMA (warp-wide, one elected lane issues). Every wait is bounded.
+// Roles (320 threads): two elementwise warpgroups, warps 0-3 for the first 64-wide half of
+// every tile and warps 4-7 for the second (one TMEM lane per thread; they share the
+// epilogue), warp 8 TMA, warp 9 MMA (warp-wide, one elected lane issues). Every wait is
+// bounded.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -38,9 +40,9 @@ namespace fa {
 namespace {
 
 constexpr int kBT = 128;  // rows of a query or key tile
-constexpr int kBwdThreads = 192;
-constexpr int kBwdTmaWarp = 4;
-constexpr int kBwdMmaWarp = 5;
+constexpr int kBwdThreads = 320;
+constexpr int kBwdTmaWarp = 8;
+constexpr int kBwdMmaWarp = 9;
 
 template <int D>
 struct BwdCfg {
@@ -405,9 +407,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ elementwise + epilogue
-    const int row = warp * 32 + lane;  // key row of the tile (= TMEM lane)
+    const int u = warp / 4;  // this warpgroup's half of every tile (64 queries)
+    const int row = (warp % 4) * 32 + lane;  // key row of the tile (= TMEM lane)
     const int j = kb * kBT + row;
-    const uint32_t t_lane = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const uint32_t t_lane = tmem + (static_cast<uint32_t>((warp % 4) * 32) << 16);
     bool ok = true;
     int t = 0;
     for (int qb = next_qb(-1, kb, bh, p, nqb); qb < nqb && ok; qb = next_qb(qb, kb, bh, p, nqb), ++t) {
@@ -416,7 +419,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       ok = mbar_wait(B(bars->st_full[t & 1]), (t >> 1) & 1, wc);
       ok = __all_sync(0xffffffffu, ok);
       const float4* st4 = reinterpret_cast<const float4*>(stats + (t & 1) * 2 * kBT);
-      for (int u = 0; u < 2 && ok; ++u) {  // halves of 64 queries
+      if (ok) {
         ok = mbar_wait(B(bars->s_full[u]), t & 1, wc);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
@@ -460,7 +463,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_arrive(B(bars->p_full[u]));
       }
     }
-    // epilogue: dV and scale * dK of this thread's key
+    // epilogue of this thread's key: dV (first warpgroup) or scale * dK (second)
     if (ok) {
       ok = mbar_wait(B(bars->acc_full), 0, wc);
       ok = __all_sync(0xffffffffu, ok);
@@ -470,19 +473,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const size_t orow = static_cast<size_t>(bh) * p.Sk + j;
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
-        uint32_t v[32], k[32];
-        tmem_ld32(t_lane + 256 + c * 32, v);
-        tmem_ld32(t_lane + 256 + D + c * 32, k);
+        uint32_t v[32];
+        tmem_ld32(t_lane + 256 + u * D + c * 32, v);
         tmem_ld_wait<32>(v);
-        tmem_ld_wait<32>(k);
         if (t == 0) {  // no query sees these keys: the gradients are 0, not TMEM contents
 #pragma unroll
-          for (int e = 0; e < 32; ++e) v[e] = k[e] = 0u;
+          for (int e = 0; e < 32; ++e) v[e] = 0u;
         }
-        if (j < p.Sk) {
-          store_tile_row<D, BF16>(b.dv, orow, v, 1.f, c * 32);
-          store_tile_row<D, BF16>(b.dk, orow, k, b.scale, c * 32);
-        }
+        if (j < p.Sk) store_tile_row<D, BF16>(u ? b.dk : b.dv, orow, v, u ? b.scale : 1.f, c * 32);
       }
     }
   }
@@ -591,9 +589,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ elementwise + epilogue
-    const int row = warp * 32 + lane;  // query row of the tile (= TMEM lane)
+    const int u = warp / 4;  // this warpgroup's half of every tile (64 keys)
+    const int row = (warp % 4) * 32 + lane;  // query row of the tile (= TMEM lane)
     const int i = qb * kBT + row;
-    const uint32_t t_lane = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const uint32_t t_lane = tmem + (static_cast<uint32_t>((warp % 4) * 32) << 16);
     const bool in = i < p.Sq;
     const size_t srow = static_cast<size_t>(bh) * p.Sq + (in ? i : 0);
     const float l2 = in ? b.lse[srow] * 1.4426950408889634f : 0.f;
@@ -602,7 +601,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     int nb = -1;
     for (int t = 0; t < n && ok; ++t) {
       nb = range_next(rg, nb);
-      for (int u = 0; u < 2 && ok; ++u) {  // halves of 64 keys
+      {
         ok = mbar_wait(B(bars->s_full[u]), t & 1, wc);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
@@ -642,7 +641,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (ok) {  // the TMEM loads are warp-collective: every lane runs them, valid rows store
       tc_fence_after();
 #pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = u * (D / 64); c < (u + 1) * (D / 64); ++c) {  // this warpgroup's half of d
         uint32_t q[32];
         tmem_ld32(t_lane + 256 + c * 32, q);
         tmem_ld_wait<32>(q);

@@ -14,22 +14,26 @@
 //
 // Two kernels share the helpers in this file:
 //
-// prefill_bm128_kernel (default): a work item is 128 query rows of one (batch, head).
+// prefill_bm128_kernel (the band and block-sparse masks, or block_m = 128): a work item is
+//   128 query rows of one (batch, head).
 //   warps 0-7   softmax: two warpgroups, each owning half of every score row (TMEM lane =
 //               row); partial row maxima are swapped through shared memory; P (16-bit)
 //               overwrites S in TMEM; lazy rescale of O.
 //   warps 8-11  epilogue: O / l and LSE of the previous item from the second O buffer.
 //   warp 12     TMA producer: Q (double buffered), then K(0), and per tile K(t+1), V(t)
 //               through a ring of shared-memory slots.
-//   warp 13     MMA issuer (one thread): S(t+1) = Q K(t+1)^T, then O += P(t) V(t).
+//   warp 13     MMA issuer (one elected lane): S(t+1) = Q K(t+1)^T, then O += P(t) V(t).
 //   TMEM columns: S0 [0,BN), S1 [BN,2BN), O0 [2BN,2BN+D), O1 [2BN+D,2BN+2D).
 //
-// prefill_bm256_kernel: a work item is 256 query rows held as two 128-row tiles A and B
-// that share every K/V tile; one softmax warpgroup per tile (a whole row per thread,
-// which also writes the epilogue), a TMA warp and an MMA warp. Tensor-pipe order
+// prefill_bm256_kernel (default for the other masks): a work item is 256 query rows held
+// as two 128-row tiles A and B that share every K/V tile; one softmax warpgroup per tile (a
+// whole row per thread, which also writes the epilogue), a TMA warp and an MMA warp.
+// Tensor-pipe order
 //   S_A(0) S_B(0) | PV_A(0) S_A(1) | PV_B(0) S_B(1) | ...
 // so that one tile's softmax runs while the tensor core works for the other.
 //   TMEM columns: S_A [0,BN), S_B [BN,2BN), O_A [2BN,2BN+D), O_B [2BN+D,2BN+2D).
+//   Its SPLIT build (FP32 inputs, fa_prefill_split.cu) reads bf16 high and low planes of
+//   Q, K, V and forms each product from both parts.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -660,7 +664,7 @@ __global__ void __launch_bounds__(kThreads256, 1)
 //               that every scheduler has two independent softmax streams
 //   warps 8-11  epilogue: O / l from TMEM to global memory, LSE; it works on the
 //               previous item while the softmax warps start the next one
-//   warp 12     TMA producer, warp 13 MMA issuer (one thread each), warps 14-15 idle
+//   warp 12     TMA producer, warp 13 MMA issuer (one elected lane each), warps 14-15 idle
 // TMEM: S0 [0,BN), S1 [BN,2BN) hold the score tiles of consecutive tiles; O0, O1
 // (D columns each, from 2BN) hold the outputs of consecutive items. Q is double
 // buffered in shared memory, so the first score tile of the next item is computed while
