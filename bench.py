@@ -208,10 +208,15 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
+    # where the raw samples go: --clock-log PATH, else the system's temporary directory
+    log_path = None
+
     def __init__(self, device_index):
+        import tempfile
         self.idx = device_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        self.path = ClockSampler.log_path or os.path.join(tempfile.gettempdir(),
+                                                          f"fa_clocks_{os.getpid()}.csv")
 
     def start(self):
         try:
@@ -649,19 +654,26 @@ MULTIMODAL = dict(B=4, H=32, d=128, V=576, T=2048, dtype="bf16")
 
 
 def timed(calls, K, W, stream):
-    """Run each zero-argument call per step; CUDA-event milliseconds of each, summed."""
+    """Run each zero-argument call per step; CUDA-event milliseconds of each, summed, and
+    the SM clocks sampled during the timed steps."""
     for _ in range(W):
         for c in calls:
             c()
     torch.cuda.synchronize()
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)] for _ in range(K)]
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    time.sleep(0.3)
+    torch.cuda.synchronize()
     for i in range(K):
         ev[i][0].record(stream)
         for j, c in enumerate(calls):
             c()
             ev[i][j + 1].record(stream)
     torch.cuda.synchronize()
-    return [sum(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(K)) for j in range(len(calls))]
+    clk = clocks.stop()
+    return [sum(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(K))
+            for j in range(len(calls))], clk
 
 
 def run_next_rows(args, fa, workload, peaks, peak_kind, stream, world):
@@ -701,9 +713,9 @@ def run_next_rows(args, fa, workload, peaks, peak_kind, stream, world):
         lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
         scale = 1 / math.sqrt(d)
         # every step appends the same chunk at the same place, then runs its prefill
-        ms = timed([lambda: fa.fa_kv_append(kn, vn, kp, vp, tab, c0, stream=stream),
-                    lambda: fa.fa_fwd_paged(q, kp, vp, tab, ctx, o, lse, scale,
-                                            fa.FA_MASK_CAUSAL, stream=stream)], K, W, stream)
+        ms, clk = timed([lambda: fa.fa_kv_append(kn, vn, kp, vp, tab, c0, stream=stream),
+                         lambda: fa.fa_fwd_paged(q, kp, vp, tab, ctx, o, lse, scale,
+                                                 fa.FA_MASK_CAUSAL, stream=stream)], K, W, stream)
         assert fa.fa_get_device_status() == fa.FA_OK
         pairs = sum(visible_pairs(T, t, 1) for t in total)
         flops = 4.0 * H * d * pairs
@@ -711,7 +723,7 @@ def run_next_rows(args, fa, workload, peaks, peak_kind, stream, world):
         pf = flops * K / (ms[1] / 1e3) / 1e12
         res.update({"metric": "chunked prefill through a paged KV cache TFLOP/s",
                     "value": pf, "unit": "TFLOP/s", "dtype": c["dtype"],
-                    "ms_per_step": (ms[0] + ms[1]) / K, "gpu_launches": 2 * K,
+                    "ms_per_step": (ms[0] + ms[1]) / K, "gpu_launches": 2 * K, "clocks": clk,
                     "roofline": {"kernel": "prefill_bm%d_kernel (paged)"
                                            % fa.fa_fwd_default_block_m(fa.FA_MASK_CAUSAL),
                                  "bound": "tensor",
@@ -742,9 +754,9 @@ def run_next_rows(args, fa, workload, peaks, peak_kind, stream, world):
                  lambda: fa.fa_fwd(qt, kt, vt, ott, ltt, scale, fa.FA_MASK_CAUSAL, stream=stream),
                  lambda: fa.fa_fwd(qt, kv_, vv, otv, ltv, scale, fa.FA_MASK_NONE, stream=stream),
                  lambda: fa.fa_merge_partials(ott, ltt, otv, ltv, ot, lt, stream=stream)]
-        ms = timed(split, K, W, stream)
-        one = timed([lambda: fa.fa_fwd(qt, k, v, o1, l1, scale, fa.FA_MASK_CAUSAL,
-                                       stream=stream)], K, W, stream)
+        ms, clk = timed(split, K, W, stream)
+        one, _ = timed([lambda: fa.fa_fwd(qt, k, v, o1, l1, scale, fa.FA_MASK_CAUSAL,
+                                          stream=stream)], K, W, stream)
         assert fa.fa_get_device_status() == fa.FA_OK
         pairs = V * V + T * (T + 1) // 2 + T * V
         flops = 4.0 * B * H * d * pairs
@@ -752,7 +764,7 @@ def run_next_rows(args, fa, workload, peaks, peak_kind, stream, world):
         val = flops * K / (total_ms / 1e3) / 1e12
         res.update({"metric": "multimodal attention layer TFLOP/s (three-call split + merge)",
                     "value": val, "unit": "TFLOP/s", "dtype": c["dtype"],
-                    "ms_per_step": total_ms / K, "gpu_launches": 4 * K,
+                    "ms_per_step": total_ms / K, "gpu_launches": 4 * K, "clocks": clk,
                     "roofline": {"kernel": "prefill_bm256_kernel x3 + merge_kernel",
                                  "bound": "tensor",
                                  "achieved": val, "peak": tc_peak, "unit": "TFLOP/s",
@@ -784,8 +796,9 @@ def run_backward(args, fa, peaks, stream, world):
     ws = torch.empty(fa.fa_bwd_workspace_size(cfg["B"], cfg["H"], cfg["S"]), dtype=torch.uint8,
                      device=dev)
     K, W = args.steps, args.warmup
-    ms = timed([lambda: fa.fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, ws, scale, cfg["mode"],
-                                  stream=stream)], K, W, stream)[0]
+    ms, clk = timed([lambda: fa.fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, ws, scale, cfg["mode"],
+                                       stream=stream)], K, W, stream)
+    ms = ms[0]
     assert fa.fa_get_device_status() == fa.FA_OK
     flops = 2.5 * prefill_flops(cfg)
     val = aggregate(flops * K, max_over_ranks(ms / 1e3, world), world) / 1e12
@@ -795,7 +808,7 @@ def run_backward(args, fa, peaks, stream, world):
             "higher_is_better": True, "data": "synthetic (seeded N(0,1))",
             "metric": "attention backward TFLOP/s (5 products over visible pairs)",
             "value": val, "unit": "TFLOP/s", "dtype": cfg["dtype"], "ms_per_step": ms / K,
-            "gpu_launches": 3 * K,
+            "gpu_launches": 3 * K, "clocks": clk,
             "roofline": {"kernel": "bwd_dkdv_kernel + bwd_dq_kernel (+ bwd_prep_kernel)",
                          "bound": "tensor", "achieved": achieved, "peak": tc_peak,
                          "unit": "TFLOP/s", "frac": achieved / tc_peak, "traffic": None,
@@ -872,7 +885,8 @@ def run_reference(args, rank, world):
 # --------------------------------------------------------------------------- tile sweep
 def run_sweep(args, fa, prefill_call, pflops, peaks, peak_kind, pcfg):
     """Tile-size sweep of the causal 4k prefill: query rows per work item (BLOCK_M 128 or
-    256; 64 is not built) x key-block size (BLOCK_N 64 or 128)."""
+    256; 64 is not built: an M = 64 tensor-core tile uses half the TMEM lanes) x key-block
+    size (BLOCK_N 64 or 128)."""
     lines = []
     for bm in (128, 256):
         for bn in (64, 128):
@@ -919,11 +933,14 @@ def main(argv=None):
                     help="decode pages per split-K partial (0 = library default)")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--clock-log", default=None,
+                    help="file for the raw nvidia-smi clock samples (default: a temporary file)")
     ap.add_argument("--prefill-traffic", type=float, default=None,
                     help="DRAM bytes per prefill launch from an ncu capture of this kernel")
     ap.add_argument("--decode-traffic", type=float, default=None,
                     help="DRAM bytes per decode call from an ncu capture")
     args = ap.parse_args(argv)
+    ClockSampler.log_path = args.clock_log
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     for cfg in list(PREFILL.values()) + [DECODE]:
