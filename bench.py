@@ -64,22 +64,23 @@ MODE_NAME = {0: "none", 1: "causal", 2: "causal_window", 3: "band", 4: "prefix_l
              5: "block_sparse"}
 
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu
-# capture of each kernel, with the SHA-256 of the kernel sources it was taken on; the
-# figure is reported only while those sources are unchanged. Summaries: profiles/.
+# capture of each kernel, with the workloads it holds for and the SHA-256 of the kernel
+# sources it was taken on; the figure is reported only for those workloads and only while
+# those sources are unchanged. Summaries: profiles/.
 NCU_TRAFFIC = {
     # prefill_bm256_kernel, causal 4k B4 H16 capture: 209.9 MB read + 44.9 MB written,
     # scaled x2 to B4 H32
-    "prefill": {"bytes": 509.66e6,
+    "prefill": {"bytes": 509.66e6, "workloads": ("default", "causal4k"),
                 "sources": ['fa_prefill.cu', 'fa_mma.cuh', 'fa_ptx.cuh', 'fa_plan.h', 'fa_internal.h'],
                 "sha256": "b7e4ab2327cfbbbfde58dc5fcf910fb7190965025cd61fa74ad05e372389afa8"},
     # paged decode B8 capture: 547.5 MB read + 3.7 MB written for 547.5 MB algorithmic,
     # scaled to the bench call's 2410.7 MB algorithmic
-    "decode": {"bytes": 2.427e9, "sources": ['fa_decode.cu', 'fa_ptx.cuh', 'fa_internal.h'],
+    "decode": {"workloads": ("default", "decode"), "bytes": 2.427e9, "sources": ['fa_decode.cu', 'fa_ptx.cuh', 'fa_internal.h'],
                "sha256": "ace52fe8e324b0324a5f68d0ea68dcf6a326d5325938ad1e673f61568f53ee40"},
     # FP32 inputs, causal 4k B4 H16 capture of one call: split_bf16_kernel 402.7 MB read +
     # 346.1 MB written, prefill_bm256_kernel (split) 408.7 MB read + 108.7 MB written;
     # scaled x2 to B4 H32
-    "prefill_f32": {"bytes": 2532.4e6,
+    "prefill_f32": {"bytes": 2532.4e6, "workloads": ("causal4k_f32",),
                     "sources": ['fa_prefill.cu', 'fa_prefill_split.cu', 'fa_mma.cuh', 'fa_ptx.cuh',
                                 'fa_plan.h', 'fa_internal.h'],
                     "sha256": "23801671820a0eb2ce009e5c311f59fbc684673078861974fa757874b33c1eec"},
@@ -95,11 +96,12 @@ def sources_sha(names):
     return h.hexdigest()
 
 
-def ncu_traffic(kind, override):
+def ncu_traffic(kind, workload, override):
     if override is not None:
         return override
     t = NCU_TRAFFIC[kind]
-    if t["bytes"] is None or t["sha256"] != sources_sha(t["sources"]):
+    if t["bytes"] is None or workload not in t["workloads"] or \
+            t["sha256"] != sources_sha(t["sources"]):
         return None
     return t["bytes"]
 
@@ -384,6 +386,8 @@ def run_ours(args, rank, world):
            "shapes of the pages' workloads; no dataset)", "gpu_launches": launches,
            "clocks": clk}
     hbm_peak = float(peaks["hbm_gbs"])
+    # captured traffic holds for the workloads' own shapes only
+    tkey = None if (args.batch or args.heads or args.pool or args.dtype) else workload
     if pcfg:
         p_sum = max_over_ranks(sum(p_ms) / 1e3, world)
         p_avg = sum(p_ms) / K / 1e3
@@ -405,7 +409,7 @@ def run_ours(args, rank, world):
                            "peak_source": f"{peak_kind} bf16 burst (MEASURED_PEAKS.json)"
                            if peak_kind == "measured" else "fallback 1.9 PFLOP/s",
                            "traffic": ncu_traffic("prefill_f32" if f32 else "prefill",
-                                                  args.prefill_traffic),
+                                                  tkey, args.prefill_traffic),
                            "algorithmic_flops": pflops,
                            "ms_per_launch": p_avg * 1e3}
         if f32:  # the tensor cores run three bf16 products per product of the method
@@ -420,7 +424,7 @@ def run_ours(args, rank, world):
                             "bound": "hbm", "achieved": dbytes / d_avg / 1e9, "peak": hbm_peak,
                             "unit": "GB/s", "frac": dbytes / d_avg / 1e9 / hbm_peak,
                             "peak_source": f"{peak_kind} copy bandwidth",
-                            "traffic": ncu_traffic("decode", args.decode_traffic), "algorithmic_bytes": dbytes,
+                            "traffic": ncu_traffic("decode", tkey, args.decode_traffic), "algorithmic_bytes": dbytes,
                             "ms_per_call": d_avg * 1e3}}
         if pcfg:
             res["decode"] = dec

@@ -92,3 +92,15 @@ def test_bigbird_layout_shape():
     assert np.all(lay[:, np.abs(i - j) <= 1] == 1)       # local band
     assert np.all(lay[:, 0, :] == 1) and np.all(lay[:, :, 0] == 1)  # global block
     assert np.all(lay[:, 1:].sum(-1) <= 3 + 1 + 2)       # band, global column, two random
+
+
+def test_captured_traffic_only_for_its_workloads():
+    """A captured DRAM figure is reported only for the workloads it was taken on (and only
+    while the kernel sources hash as captured); an explicit figure always wins."""
+    for kind, t in bench.NCU_TRAFFIC.items():
+        current = t["bytes"] is not None and t["sha256"] == bench.sources_sha(t["sources"])
+        for w in t["workloads"]:
+            assert bench.ncu_traffic(kind, w, None) == (t["bytes"] if current else None)
+        for w in ("band4k", "blocksparse4k", "window32k", None):
+            assert w in t["workloads"] or bench.ncu_traffic(kind, w, None) is None
+        assert bench.ncu_traffic(kind, "band4k", 123.0) == 123.0
