@@ -327,16 +327,24 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     int t = 0;
     for (int qb = next_qb(-1, kb, bh, p, nqb); qb < nqb && ok; qb = next_qb(qb, kb, bh, p, nqb), ++t) {
       const int s = t & 1;
+      // LSE and D of the tile's 128 queries, 4 per lane (0 past Sq), loaded before the wait
+      // for the stage so that their latency overlaps it
+      float lv[4], dv[4];
+      const size_t r0 = static_cast<size_t>(bh) * p.Sq;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int i = qb * kBT + lane * 4 + e;
+        lv[e] = i < p.Sq ? __ldg(b.lse + r0 + i) : 0.f;
+        dv[e] = i < p.Sq ? __ldg(b.dsum + r0 + i) : 0.f;
+      }
       if (t >= 2 && !(ok = mbar_wait(B(bars->st_empty[s]), ((t >> 1) - 1) & 1, wc))) break;
       const uint32_t sq = sSt + 2 * s * C::TILE, sdo = sq + C::TILE;
-      {  // LSE * log2(e) and D of the tile's 128 queries, 4 per lane (0 past Sq)
+      {  // the stage's statistics: LSE * log2(e) and D
         float* st = stats + s * 2 * kBT;
-        const size_t r0 = static_cast<size_t>(bh) * p.Sq;
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const int col = lane * 4 + e, i = qb * kBT + col;
-          st[col] = i < p.Sq ? __ldg(b.lse + r0 + i) * 1.4426950408889634f : 0.f;
-          st[kBT + col] = i < p.Sq ? __ldg(b.dsum + r0 + i) : 0.f;
+          st[lane * 4 + e] = lv[e] * 1.4426950408889634f;
+          st[kBT + lane * 4 + e] = dv[e];
         }
         __syncwarp();  // the leader's arrive below releases every lane's writes
       }
