@@ -667,10 +667,11 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
   L.dout = dout;
   const void* qmap = Sq ? q : k;  // a map needs a valid address even when nothing is loaded
   const void* kmap = Sk ? k : q;
-  if ((st = make_map(&L.tmQ, qmap, bf16, d, Sq, BH, 128)) != FA_OK) return st;
-  if ((st = make_map(&L.tmdO, Sq ? dout : k, bf16, d, Sq, BH, 128)) != FA_OK) return st;
-  if ((st = make_map(&L.tmK, kmap, bf16, d, Sk, BH, 128)) != FA_OK) return st;
-  if ((st = make_map(&L.tmV, Sk ? v : q, bf16, d, Sk, BH, 128)) != FA_OK) return st;
+  const int box = fa::kBwdBoxRows;
+  if ((st = make_map(&L.tmQ, qmap, bf16, d, Sq, BH, box)) != FA_OK) return st;
+  if ((st = make_map(&L.tmdO, Sq ? dout : k, bf16, d, Sq, BH, box)) != FA_OK) return st;
+  if ((st = make_map(&L.tmK, kmap, bf16, d, Sk, BH, box)) != FA_OK) return st;
+  if ((st = make_map(&L.tmV, Sk ? v : q, bf16, d, Sk, BH, box)) != FA_OK) return st;
   cudaError_t e = fa::launch_backward(L, d, bf16, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "backward launch");
   return FA_OK;

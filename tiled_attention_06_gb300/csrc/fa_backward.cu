@@ -44,29 +44,42 @@ constexpr int kBwdThreads = 320;
 constexpr int kBwdTmaWarp = 8;
 constexpr int kBwdMmaWarp = 9;
 
+// The streamed side moves in halves of 64 rows (kBwdBoxRows, the tensor maps' box height):
+// stage h holds one half of each of the two streamed tiles, and is released as soon as the
+// MMAs of that half are done, so the next loads start half a tile earlier than whole-tile
+// stages would let them.
+constexpr int kHalf = kBwdBoxRows;
+constexpr int kStages = 4;
+static_assert(kHalf * 2 == kBT, "two halves per tile");
+
 template <int D>
 struct BwdCfg {
-  static constexpr int KCH = D / 64;
-  static constexpr int TILE = kBT * D * 2;  // one 128-row 16-bit tile
-  // two resident tiles + two stages of two streamed tiles + barriers, 1 KB aligned; at
-  // least half the SM's shared memory, so that one CTA (which takes all 512 TMEM columns)
-  // is resident per SM
-  static constexpr int STATS = 2 * kBT * 4;  // per stage: LSE * log2(e) and D of 128 queries
-  static constexpr int SMEM_USED = 1024 + 6 * TILE + 2 * STATS + 1024;
+  static constexpr int TILE = kBT * D * 2;   // one 128-row 16-bit tile (resident)
+  static constexpr int HTILE = kHalf * D * 2;  // one 64-row half (streamed)
+  // two resident tiles + four stages of two streamed halves + statistics + barriers, 1 KB
+  // aligned; at least half the SM's shared memory, so that one CTA (which takes all 512
+  // TMEM columns) is resident per SM
+  static constexpr int STATS = 2 * kHalf * 4;  // per stage: LSE * log2(e) and D of 64 queries
+  static constexpr int SMEM_USED = 1024 + 2 * TILE + kStages * 2 * HTILE + kStages * STATS + 1024;
   static constexpr int SMEM = SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024;
   static_assert(SMEM <= 232448, "shared memory over budget");
 };
 
 struct BwdBars {
-  uint64_t res_full;       // the CTA's resident tiles landed
-  uint64_t st_full[2];     // streamed tiles of stage s landed
-  uint64_t st_empty[2];    // MMAs done with stage s
-  uint64_t s_full[2];      // S and dP of half u of the current tile in TMEM
-  uint64_t p_full[2];      // P and dS (16-bit) of half u written back
-  uint64_t acc_full;       // every MMA of the CTA complete
+  uint64_t res_full;              // the CTA's resident tiles landed
+  uint64_t st_full[kStages];      // streamed halves of stage h landed
+  uint64_t st_empty[kStages];     // MMAs done with stage h
+  uint64_t s_full[2];             // S and dP of half u of the current tile in TMEM
+  uint64_t p_full[2];             // P and dS (16-bit) of half u written back
+  uint64_t acc_full;              // every MMA of the CTA complete
   uint32_t tmem_base;
   uint32_t abort;
 };
+
+// Half g = 2 t + u of the stream (tile t, half u) lives in stage g % kStages; its fills and
+// releases alternate parity every kStages halves.
+__device__ __forceinline__ int stage_of(int g) { return g % kStages; }
+__device__ __forceinline__ uint32_t stage_parity(int g) { return (g / kStages) & 1; }
 
 // Key positions are the query index plus delta = Sk - Sq (queries aligned to the last
 // Sq keys), as in the forward.
@@ -185,32 +198,54 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const uint4* __restrict__
 
 // Half-tile MMAs: every tile of 128 queries (or keys) is processed as two halves u of 64,
 // so that the tensor core works on one half while the elementwise warps work on the other.
-// X_u = A B_u^T: A a resident 128-row tile, B_u rows [64u, 64u+64) of a 128-row tile (both
-// K-major, 128-byte swizzled, regions of 64 elements of d 16 KB apart); M = 128, N = 64.
+// X_u = A B_u^T: A a resident 128-row tile (regions of 64 elements of d 16 KB apart), B_u a
+// streamed 64-row half (regions 8 KB apart), both K-major and 128-byte swizzled; M = 128,
+// N = 64.
 template <int D, bool BF16>
-__device__ __forceinline__ void issue_s_half(uint32_t d_tmem, uint32_t a_smem, uint32_t b_smem,
-                                             int u) {
-  constexpr uint32_t id = idesc_f16(BF16, kBT, 64, false);
+__device__ __forceinline__ void issue_s_half(uint32_t d_tmem, uint32_t a_smem, uint32_t b_half) {
+  constexpr uint32_t id = idesc_f16(BF16, kBT, kHalf, false);
   const uint64_t a0 = smem_desc_sw128(a_smem, 16, 1024);
-  const uint64_t b0 = smem_desc_sw128(b_smem + u * 64 * 128, 16, 1024);
+  const uint64_t b0 = smem_desc_sw128(b_half, 16, 1024);
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
-    const uint64_t off = static_cast<uint64_t>((kk / 4) * (kBT * 128 / 16) + (kk % 4) * 2);
-    umma_ss(d_tmem, a0 + off, b0 + off, id, kk > 0 ? 1u : 0u);
+    const uint64_t a_off = static_cast<uint64_t>((kk / 4) * (kBT * 128 / 16) + (kk % 4) * 2);
+    const uint64_t b_off = static_cast<uint64_t>((kk / 4) * (kHalf * 128 / 16) + (kk % 4) * 2);
+    umma_ss(d_tmem, a0 + a_off, b0 + b_off, id, kk > 0 ? 1u : 0u);
   }
 }
 
-// Y (+)= A_u B_u: A_u 64 packed 16-bit columns in TMEM (K = 64), B_u rows [64u, 64u+64) of a
-// 128-row tile used MN-major (N = D; 16 rows = 2048 bytes per MMA).
+// Y (+)= A_u B_u: A_u 64 packed 16-bit columns in TMEM (K = 64), B_u a streamed 64-row half
+// used MN-major (N = D, its second 64 elements of d 8 KB on; 16 rows = 2048 bytes per MMA).
 template <int D, bool BF16>
-__device__ __forceinline__ void issue_pv_half(uint32_t y_tmem, uint32_t a_tmem, uint32_t b_smem,
-                                              int u, bool accumulate) {
+__device__ __forceinline__ void issue_pv_half(uint32_t y_tmem, uint32_t a_tmem, uint32_t b_half,
+                                              bool accumulate) {
   constexpr uint32_t id = idesc_f16(BF16, kBT, D, true);
-  const uint64_t b0 = smem_desc_sw128(b_smem + u * 64 * 128, kBT * 128, 1024);
+  const uint64_t b0 = smem_desc_sw128(b_half, kHalf * 128, 1024);
 #pragma unroll
-  for (int kk = 0; kk < 4; ++kk)
+  for (int kk = 0; kk < kHalf / 16; ++kk)
     umma_ts(y_tmem, a_tmem + kk * 8, b0 + static_cast<uint64_t>(kk * 128), id,
             (accumulate || kk > 0) ? 1u : 0u);
+}
+
+// A resident 128-row tile as two 64-row boxes per 64-element region of d (the region's
+// second box 8 KB after the first, which is the 128-row box's layout).
+template <int D>
+__device__ __forceinline__ void load_resident(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                              int row0, int bh) {
+#pragma unroll
+  for (int c = 0; c < D / 64; ++c)
+#pragma unroll
+    for (int r = 0; r < 2; ++r)
+      tma_load_3d(dst + c * (kBT * 128) + r * (kHalf * 128), map, bar, c * 64, row0 + r * kHalf,
+                  bh);
+}
+
+// A streamed 64-row half: one box per 64-element region of d, regions 8 KB apart.
+template <int D>
+__device__ __forceinline__ void load_half(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                          int row0, int bh) {
+#pragma unroll
+  for (int c = 0; c < D / 64; ++c) tma_load_3d(dst + c * (kHalf * 128), map, bar, c * 64, row0, bh);
 }
 
 // Does the query block qb see any key of key block kb (the forward's key ranges)?
@@ -248,7 +283,7 @@ __device__ __forceinline__ uint32_t bwd_setup(BwdBars* bars, const CUtensorMap* 
   const int warp = threadIdx.x / 32;
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(&bars->res_full), 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kStages; ++i) {
       mbar_init(smem_u32(&bars->st_full[i]), 1);
       mbar_init(smem_u32(&bars->st_empty[i]), 1);
     }
@@ -287,7 +322,7 @@ __device__ __forceinline__ void bwd_teardown(uint32_t tmem) {
 
 // dK and dV of one block of 128 keys. TMEM: S^T [0,128) (P^T packed over its first 64
 // columns), dP^T [128,256) (dS^T packed over [128,192)), dV [256,256+D), dK [256+D,256+2D).
-// Shared memory: K, V (resident), then (Q, dO) in two stages.
+// Shared memory: K, V (resident), then (Q, dO) halves of 64 queries in four stages.
 template <int D, bool BF16>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ,
@@ -301,9 +336,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* smem = smem_raw + (base - raw);
   const uint32_t sK = base, sV = base + C::TILE;
-  const uint32_t sSt = base + 2 * C::TILE;  // stage s: Q at sSt + 2s TILE, dO one TILE on
-  float* stats = reinterpret_cast<float*>(smem + 6 * C::TILE);  // [stage][LSE2 | D][128]
-  BwdBars* bars = reinterpret_cast<BwdBars*>(smem + 6 * C::TILE + 2 * C::STATS);
+  const uint32_t sSt = base + 2 * C::TILE;  // stage h: Q half at sSt + 2h HTILE, dO half one on
+  auto sQh = [&](int h) { return sSt + 2 * h * C::HTILE; };
+  auto sdOh = [&](int h) { return sSt + (2 * h + 1) * C::HTILE; };
+  // [stage][LSE2 | D][64]
+  float* stats = reinterpret_cast<float*>(smem + 2 * C::TILE + kStages * 2 * C::HTILE);
+  BwdBars* bars = reinterpret_cast<BwdBars*>(reinterpret_cast<uint8_t*>(stats) + kStages * C::STATS);
   auto B = [&](uint64_t& x) { return smem_u32(&x); };
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int nkb = (p.Sk + kBT - 1) / kBT, nqb = (p.Sq + kBT - 1) / kBT;
@@ -315,98 +353,88 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // ------------------------------------------------------------ TMA
     const bool leader = elect_one();
     bool ok = true;
-    uint32_t fills[2] = {0, 0}, res = 0;
+    uint32_t fills[kStages] = {0, 0, 0, 0};
     if (leader) {
       mbar_arrive_expect_tx(B(bars->res_full), 2 * C::TILE);
-      for (int c = 0; c < C::KCH; ++c) {
-        tma_load_3d(sK + c * (kBT * 128), &tmK, B(bars->res_full), c * 64, kb * kBT, bh);
-        tma_load_3d(sV + c * (kBT * 128), &tmV, B(bars->res_full), c * 64, kb * kBT, bh);
-      }
+      load_resident<D>(sK, &tmK, B(bars->res_full), kb * kBT, bh);
+      load_resident<D>(sV, &tmV, B(bars->res_full), kb * kBT, bh);
     }
-    res = 1;
-    int t = 0;
-    for (int qb = next_qb(-1, kb, bh, p, nqb); qb < nqb && ok; qb = next_qb(qb, kb, bh, p, nqb), ++t) {
-      const int s = t & 1;
-      // LSE and D of the tile's 128 queries, 4 per lane (0 past Sq), loaded before the wait
-      // for the stage so that their latency overlaps it
-      float lv[4], dv[4];
-      const size_t r0 = static_cast<size_t>(bh) * p.Sq;
+    int g = 0;  // half index of the stream
+    for (int qb = next_qb(-1, kb, bh, p, nqb); qb < nqb && ok; qb = next_qb(qb, kb, bh, p, nqb)) {
+      for (int u = 0; u < 2 && ok; ++u, ++g) {
+        const int h = stage_of(g);
+        // LSE and D of the half's 64 queries, 2 per lane (0 past Sq), loaded before the
+        // wait for the stage so that their latency overlaps it
+        float lv[2], dv[2];
+        const size_t r0 = static_cast<size_t>(bh) * p.Sq;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int i = qb * kBT + lane * 4 + e;
-        lv[e] = i < p.Sq ? __ldg(b.lse + r0 + i) : 0.f;
-        dv[e] = i < p.Sq ? __ldg(b.dsum + r0 + i) : 0.f;
-      }
-      if (t >= 2 && !(ok = mbar_wait(B(bars->st_empty[s]), ((t >> 1) - 1) & 1, wc))) break;
-      const uint32_t sq = sSt + 2 * s * C::TILE, sdo = sq + C::TILE;
-      {  // the stage's statistics: LSE * log2(e) and D
-        float* st = stats + s * 2 * kBT;
+        for (int e = 0; e < 2; ++e) {
+          const int i = qb * kBT + u * kHalf + lane * 2 + e;
+          lv[e] = i < p.Sq ? __ldg(b.lse + r0 + i) : 0.f;
+          dv[e] = i < p.Sq ? __ldg(b.dsum + r0 + i) : 0.f;
+        }
+        if (g >= kStages && !(ok = mbar_wait(B(bars->st_empty[h]), stage_parity(g - kStages), wc)))
+          break;
+        {  // the stage's statistics: LSE * log2(e) and D
+          float* st = stats + h * 2 * kHalf;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          st[lane * 4 + e] = lv[e] * 1.4426950408889634f;
-          st[kBT + lane * 4 + e] = dv[e];
+          for (int e = 0; e < 2; ++e) {
+            st[lane * 2 + e] = lv[e] * 1.4426950408889634f;
+            st[kHalf + lane * 2 + e] = dv[e];
+          }
+          __syncwarp();  // the leader's arrive below releases every lane's writes
         }
-        __syncwarp();  // the leader's arrive below releases every lane's writes
-      }
-      if (leader) {
-        mbar_arrive_expect_tx(B(bars->st_full[s]), 2 * C::TILE);
-        for (int c = 0; c < C::KCH; ++c) {
-          tma_load_3d(sq + c * (kBT * 128), &tmQ, B(bars->st_full[s]), c * 64, qb * kBT, bh);
-          tma_load_3d(sdo + c * (kBT * 128), &tmdO, B(bars->st_full[s]), c * 64, qb * kBT, bh);
+        if (leader) {
+          mbar_arrive_expect_tx(B(bars->st_full[h]), 2 * C::HTILE);
+          load_half<D>(sQh(h), &tmQ, B(bars->st_full[h]), qb * kBT + u * kHalf, bh);
+          load_half<D>(sdOh(h), &tmdO, B(bars->st_full[h]), qb * kBT + u * kHalf, bh);
         }
+        fills[h] = g / kStages + 1;
       }
-      fills[s] = (t >> 1) + 1;
     }
     if (!ok) {  // every load issued lands before the CTA exits
-      if (res) wait_quiet_b(B(bars->res_full), 0, wc);
-      for (int s = 0; s < 2; ++s)
-        if (fills[s] > 0) wait_quiet_b(B(bars->st_full[s]), (fills[s] - 1) & 1, wc);
+      wait_quiet_b(B(bars->res_full), 0, wc);
+      for (int h = 0; h < kStages; ++h)
+        if (fills[h] > 0) wait_quiet_b(B(bars->st_full[h]), (fills[h] - 1) & 1, wc);
     }
     __syncwarp();
   } else if (warp == kBwdMmaWarp) {
     // ------------------------------------------------------------ MMA
     const bool leader = elect_one();
     // Per tile t and half u: wait for P^T_u / dS^T_u, then dV += P^T_u dO_u and
-    // dK += dS^T_u Q_u, then the scores of half u of the next tile into the columns just
-    // read (MMAs of one thread execute in order). The tensor core works on one half
-    // while the elementwise warps work on the other.
+    // dK += dS^T_u Q_u, release the half's stage, then the scores of half u of the next tile
+    // into the columns just read (MMAs of one thread execute in order). The tensor core works
+    // on one half while the elementwise warps work on the other.
     bool ok = mbar_wait(B(bars->res_full), 0, wc);
     int qb = ok ? next_qb(-1, kb, bh, p, nqb) : nqb;
-    auto scores = [&](int stage, int u) {  // S^T_u = K Q_u^T, dP^T_u = V dO_u^T
-      const uint32_t sq = sSt + 2 * stage * C::TILE;
-      issue_s_half<D, BF16>(tmem + 64 * u, sK, sq, u);
-      issue_s_half<D, BF16>(tmem + 128 + 64 * u, sV, sq + C::TILE, u);
-      umma_commit(B(bars->s_full[u]));
-    };
-    if (qb < nqb && (ok = mbar_wait(B(bars->st_full[0]), 0, wc))) {
+    // S^T_u = K Q_u^T, dP^T_u = V dO_u^T for stream half g (= 2 t + u) once it has landed
+    auto scores = [&](int g, int u) {
+      if (!(ok = mbar_wait(B(bars->st_full[stage_of(g)]), stage_parity(g), wc))) return;
       tc_fence_after();
       if (leader) {
-        scores(0, 0);
-        scores(0, 1);
+        issue_s_half<D, BF16>(tmem + 64 * u, sK, sQh(stage_of(g)));
+        issue_s_half<D, BF16>(tmem + 128 + 64 * u, sV, sdOh(stage_of(g)));
+        umma_commit(B(bars->s_full[u]));
       }
+    };
+    if (qb < nqb && ok) {
+      scores(0, 0);
+      if (ok) scores(1, 1);
     }
     int t = 0;
     while (qb < nqb && ok) {
-      const int s = t & 1;
-      const uint32_t sq = sSt + 2 * s * C::TILE, sdo = sq + C::TILE;
       const int qn = next_qb(qb, kb, bh, p, nqb);
       for (int u = 0; u < 2 && ok; ++u) {
+        const int g = 2 * t + u, h = stage_of(g);
         if (!(ok = mbar_wait(B(bars->p_full[u]), t & 1, wc))) break;
         tc_fence_after();
         if (leader) {
-          issue_pv_half<D, BF16>(tmem + 256, tmem + 64 * u, sdo, u, t > 0 || u > 0);
-          issue_pv_half<D, BF16>(tmem + 256 + D, tmem + 128 + 64 * u, sq, u, t > 0 || u > 0);
+          issue_pv_half<D, BF16>(tmem + 256, tmem + 64 * u, sdOh(h), t > 0 || u > 0);
+          issue_pv_half<D, BF16>(tmem + 256 + D, tmem + 128 + 64 * u, sQh(h), t > 0 || u > 0);
+          umma_commit(B(bars->st_empty[h]));  // stage h free once these are done
         }
-        if (qn < nqb) {
-          if (u == 0) {
-            if (!(ok = mbar_wait(B(bars->st_full[(t + 1) & 1]), ((t + 1) >> 1) & 1, wc))) break;
-            tc_fence_after();
-          }
-          if (leader) scores((t + 1) & 1, u);
-        }
+        if (qn < nqb) scores(g + 2, u);
       }
-      if (!ok) break;
-      if (leader) umma_commit(B(bars->st_empty[s]));  // stage s free once these are done
       qb = qn;
       ++t;
     }
@@ -422,11 +450,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     bool ok = true;
     int t = 0;
     for (int qb = next_qb(-1, kb, bh, p, nqb); qb < nqb && ok; qb = next_qb(qb, kb, bh, p, nqb), ++t) {
-      // the stage's statistics: no barrier can be a phase ahead, as the MMAs of this tile
-      // need the P and dS this warpgroup has not written yet
-      ok = mbar_wait(B(bars->st_full[t & 1]), (t >> 1) & 1, wc);
+      const int g = 2 * t + u, h = stage_of(g);
+      // the stage's statistics: the stage cannot be refilled before this warpgroup has
+      // written the P and dS that the MMAs reading it wait for
+      ok = mbar_wait(B(bars->st_full[h]), stage_parity(g), wc);
       ok = __all_sync(0xffffffffu, ok);
-      const float4* st4 = reinterpret_cast<const float4*>(stats + (t & 1) * 2 * kBT);
+      const float4* st4 = reinterpret_cast<const float4*>(stats + h * 2 * kHalf);
       if (ok) {
         ok = mbar_wait(B(bars->s_full[u]), t & 1, wc);
         ok = __all_sync(0xffffffffu, ok);
@@ -442,8 +471,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           float l2[32], dd[32];
 #pragma unroll
           for (int e = 0; e < 8; ++e) {  // per-query statistics (the same for every lane)
-            const float4 a = st4[(64 * u + c * 32) / 4 + e];
-            const float4 d = st4[(kBT + 64 * u + c * 32) / 4 + e];
+            const float4 a = st4[(c * 32) / 4 + e];
+            const float4 d = st4[(kHalf + c * 32) / 4 + e];
             l2[4 * e] = a.x, l2[4 * e + 1] = a.y, l2[4 * e + 2] = a.z, l2[4 * e + 3] = a.w;
             dd[4 * e] = d.x, dd[4 * e + 1] = d.y, dd[4 * e + 2] = d.z, dd[4 * e + 3] = d.w;
           }
@@ -496,7 +525,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 }
 
 // dQ of one block of 128 queries. TMEM: S [0,128), dP [128,256) (dS packed over
-// [128,192)), dQ [256,256+D). Shared memory: Q, dO (resident), then (K, V) in two stages.
+// [128,192)), dQ [256,256+D). Shared memory: Q, dO (resident), then (K, V) halves of 64 keys
+// in four stages.
 template <int D, bool BF16>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -509,8 +539,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* smem = smem_raw + (base - raw);
   const uint32_t sQ = base, sdO = base + C::TILE;
-  const uint32_t sSt = base + 2 * C::TILE;  // stage s: K at sSt + 2s TILE, V one TILE on
-  BwdBars* bars = reinterpret_cast<BwdBars*>(smem + 6 * C::TILE + 2 * C::STATS);
+  const uint32_t sSt = base + 2 * C::TILE;  // stage h: K half at sSt + 2h HTILE, V half one on
+  auto sKh = [&](int h) { return sSt + 2 * h * C::HTILE; };
+  auto sVh = [&](int h) { return sSt + (2 * h + 1) * C::HTILE; };
+  BwdBars* bars = reinterpret_cast<BwdBars*>(smem + 2 * C::TILE + kStages * 2 * C::HTILE +
+                                             kStages * C::STATS);
   auto B = [&](uint64_t& x) { return smem_u32(&x); };
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int nqb = (p.Sq + kBT - 1) / kBT;
@@ -524,73 +557,67 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // ------------------------------------------------------------ TMA
     const bool leader = elect_one();
     bool ok = true;
-    uint32_t fills[2] = {0, 0};
+    uint32_t fills[kStages] = {0, 0, 0, 0};
     if (n > 0) {
       if (leader) {
         mbar_arrive_expect_tx(B(bars->res_full), 2 * C::TILE);
-        for (int c = 0; c < C::KCH; ++c) {
-          tma_load_3d(sQ + c * (kBT * 128), &tmQ, B(bars->res_full), c * 64, qb * kBT, bh);
-          tma_load_3d(sdO + c * (kBT * 128), &tmdO, B(bars->res_full), c * 64, qb * kBT, bh);
-        }
+        load_resident<D>(sQ, &tmQ, B(bars->res_full), qb * kBT, bh);
+        load_resident<D>(sdO, &tmdO, B(bars->res_full), qb * kBT, bh);
       }
-      int nb = -1;
+      int nb = -1, g = 0;
       for (int t = 0; t < n && ok; ++t) {
         nb = range_next(rg, nb);
-        const int s = t & 1;
-        if (t >= 2 && !(ok = mbar_wait(B(bars->st_empty[s]), ((t >> 1) - 1) & 1, wc))) break;
-        const uint32_t sk_ = sSt + 2 * s * C::TILE, sv = sk_ + C::TILE;
-        if (leader) {
-          mbar_arrive_expect_tx(B(bars->st_full[s]), 2 * C::TILE);
-          for (int c = 0; c < C::KCH; ++c) {
-            tma_load_3d(sk_ + c * (kBT * 128), &tmK, B(bars->st_full[s]), c * 64, nb * kBT, bh);
-            tma_load_3d(sv + c * (kBT * 128), &tmV, B(bars->st_full[s]), c * 64, nb * kBT, bh);
+        for (int u = 0; u < 2 && ok; ++u, ++g) {
+          const int h = stage_of(g);
+          if (g >= kStages &&
+              !(ok = mbar_wait(B(bars->st_empty[h]), stage_parity(g - kStages), wc)))
+            break;
+          if (leader) {
+            mbar_arrive_expect_tx(B(bars->st_full[h]), 2 * C::HTILE);
+            load_half<D>(sKh(h), &tmK, B(bars->st_full[h]), nb * kBT + u * kHalf, bh);
+            load_half<D>(sVh(h), &tmV, B(bars->st_full[h]), nb * kBT + u * kHalf, bh);
           }
+          fills[h] = g / kStages + 1;
         }
-        fills[s] = (t >> 1) + 1;
       }
       if (!ok) {  // every load issued lands before the CTA exits
         wait_quiet_b(B(bars->res_full), 0, wc);
-        for (int s = 0; s < 2; ++s)
-          if (fills[s] > 0) wait_quiet_b(B(bars->st_full[s]), (fills[s] - 1) & 1, wc);
+        for (int h = 0; h < kStages; ++h)
+          if (fills[h] > 0) wait_quiet_b(B(bars->st_full[h]), (fills[h] - 1) & 1, wc);
       }
     }
     __syncwarp();
   } else if (warp == kBwdMmaWarp) {
     // ------------------------------------------------------------ MMA
     const bool leader = elect_one();
-    // Per tile t and half u (64 keys): wait for dS_u, dQ += dS_u K_u, then the scores of
-    // half u of the next tile (as in the dK/dV kernel).
+    // Per tile t and half u (64 keys): wait for dS_u, dQ += dS_u K_u, release the half's
+    // stage, then the scores of half u of the next tile (as in the dK/dV kernel).
     bool ok = n == 0 || mbar_wait(B(bars->res_full), 0, wc);
-    auto scores = [&](int stage, int u) {  // S_u = Q K_u^T, dP_u = dO V_u^T
-      const uint32_t sk_ = sSt + 2 * stage * C::TILE;
-      issue_s_half<D, BF16>(tmem + 64 * u, sQ, sk_, u);
-      issue_s_half<D, BF16>(tmem + 128 + 64 * u, sdO, sk_ + C::TILE, u);
-      umma_commit(B(bars->s_full[u]));
-    };
-    if (n > 0 && ok && (ok = mbar_wait(B(bars->st_full[0]), 0, wc))) {
+    // S_u = Q K_u^T, dP_u = dO V_u^T for stream half g (= 2 t + u) once it has landed
+    auto scores = [&](int g, int u) {
+      if (!(ok = mbar_wait(B(bars->st_full[stage_of(g)]), stage_parity(g), wc))) return;
       tc_fence_after();
       if (leader) {
-        scores(0, 0);
-        scores(0, 1);
+        issue_s_half<D, BF16>(tmem + 64 * u, sQ, sKh(stage_of(g)));
+        issue_s_half<D, BF16>(tmem + 128 + 64 * u, sdO, sVh(stage_of(g)));
+        umma_commit(B(bars->s_full[u]));
       }
+    };
+    if (n > 0 && ok) {
+      scores(0, 0);
+      if (ok) scores(1, 1);
     }
     for (int t = 0; t < n && ok; ++t) {
-      const int s = t & 1;
-      const uint32_t sk_ = sSt + 2 * s * C::TILE;
       for (int u = 0; u < 2 && ok; ++u) {
+        const int g = 2 * t + u, h = stage_of(g);
         if (!(ok = mbar_wait(B(bars->p_full[u]), t & 1, wc))) break;
         tc_fence_after();
-        if (leader) issue_pv_half<D, BF16>(tmem + 256, tmem + 128 + 64 * u, sk_, u, t > 0 || u > 0);
-        if (t + 1 < n) {
-          if (u == 0) {
-            if (!(ok = mbar_wait(B(bars->st_full[(t + 1) & 1]), ((t + 1) >> 1) & 1, wc))) break;
-            tc_fence_after();
-          }
-          if (leader) scores((t + 1) & 1, u);
+        if (leader) {
+          issue_pv_half<D, BF16>(tmem + 256, tmem + 128 + 64 * u, sKh(h), t > 0 || u > 0);
+          umma_commit(B(bars->st_empty[h]));  // stage h free once this is done
         }
+        if (t + 1 < n) scores(g + 2, u);
       }
-      if (!ok) break;
-      if (leader) umma_commit(B(bars->st_empty[s]));
     }
     if (leader) umma_commit(B(bars->acc_full));
     wait_quiet_b(B(bars->acc_full), 0, wc);
