@@ -19,6 +19,7 @@
 #include <vector>
 
 #include "fa.h"
+#include "fa_bwd_tiles.h"
 #include "fa_internal.h"
 #include "fa_plan.h"
 

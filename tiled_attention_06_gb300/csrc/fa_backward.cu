@@ -31,6 +31,7 @@
 #include <climits>
 #include <cstdint>
 
+#include "fa_bwd_tiles.h"
 #include "fa_internal.h"
 #include "fa_mma.cuh"
 #include "fa_plan.h"

@@ -75,10 +75,6 @@ struct BwdParams {
   float scale;
 };
 
-// Rows of one TMA box of the backward's tensor maps (Q, dO, K, V): the streamed side of each
-// backward kernel moves in 64-row halves.
-constexpr int kBwdBoxRows = 64;
-
 struct BwdLaunch {
   CUtensorMap tmQ, tmK, tmV, tmdO;
   PrefillParams p;  // sizes, mask, sl2, status, timeout (contiguous K/V)
