@@ -150,6 +150,10 @@ def test_fwd_f32_argument_checks(L):
     assert _fwd32(L, block_n=128) == fa.FA_ERR_UNSUPPORTED
     assert _fwd32(L, block_m=128) == fa.FA_ERR_UNSUPPORTED
     assert _fwd32(L, ws=None, Sq=0) == fa.FA_OK  # nothing to compute, nothing needed
+    # the split planes double B * H in the tensor maps: B * H is capped at 2^29
+    p = fa.FwdParams(A, A, A, A, None, 1 << 15, 1 << 15, 4, 4, 64, 0.125, 0, 0, 0, fa.FA_F32, 0,
+                     0, 0, 0, 0, None, None, A, 1 << 40)
+    assert L.fa_fwd_ex(ctypes.byref(p), None) == fa.FA_ERR_INVALID_ARG
     # the paged prefill and the backward take 16-bit inputs only
     assert L.fa_fwd_paged(A, A, A, A, A, A, None, 1, 1, 4, 64, 256, 1, 1, 0.125, 0, 0, 0,
                           fa.FA_F32, None) == fa.FA_ERR_UNSUPPORTED

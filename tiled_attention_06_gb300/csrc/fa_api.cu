@@ -199,6 +199,8 @@ fa_status check_fwd(const fa_fwd_params& p, bool allow_f32 = false) {
     return fail(FA_ERR_UNSUPPORTED, "block_m %d (supported: 128, 256)", p.block_m);
   if (p.num_ctas < 0 || p.group_heads < 0) return fail(FA_ERR_INVALID_ARG, "negative plan parameter");
   if (p.dtype == FA_F32) {
+    if (BH > (1LL << 29))  // the tensor maps see 2 * B * H planes
+      return fail(FA_ERR_INVALID_ARG, "FA_F32: B * H above 2^29");
     if (p.block_n != 0 && p.block_n != fa::kSplitBlockN)
       return fail(FA_ERR_UNSUPPORTED, "block_n %d with FA_F32 (supported: 64)", p.block_n);
     if (p.block_m != 0 && p.block_m != 256)
