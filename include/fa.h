@@ -47,6 +47,9 @@
  *     that ran past its time limit) are recorded in a device status word and
  *     reported by fa_get_device_status().
  *   - fa_last_error_string() describes the last non-FA_OK status of this thread.
+ *   - The library looks up a few device addresses (its status word, the scratch of
+ *     fa_decode_paged_noalloc) once per device and keeps them; a process that calls
+ *     cudaDeviceReset must not call the library afterwards.
  */
 #ifndef FA_H
 #define FA_H
@@ -138,6 +141,12 @@ typedef struct fa_fwd_params {
    * stays near 2^-15, far inside the 1e-3 bound on O that FP32 inputs are held to. */
   void* workspace;
   size_t workspace_bytes;
+  /* Optional int32 [B*H, ceil(Sq/128)], zeroed by the caller: for every 128-query tile, the
+   * number of (query row, key tile) steps at which the row's running maximum rose by more
+   * than the lazy-rescale threshold (8 in log2 units) and its partial output and sum were
+   * rescaled (the correction step of the per-block (m, l, O) recurrence, zwxr.cn article
+   * on ops-transformer, section 3.1). For tests: it shows which inputs reach that step. */
+  int32_t* rescale_count;
 } fa_fwd_params;
 
 fa_status fa_fwd_ex(const fa_fwd_params* params, fa_stream_t stream);
@@ -306,11 +315,13 @@ fa_status fa_merge_partials(const void* o_a, const float* lse_a, const void* o_b
  *   and `workspace_bytes`; the caller still owns and passes every input and output.
  *   The split partials go to a scratch array built into the library: 16 MiB on every
  *   GPU that loads it, held until the process exits. The call allocates nothing.
- *   The split size is fa_decode_paged's default, made coarser when needed to fit;
- *   if even one split per sequence does not fit (B*H*(d+2)*4 bytes > 16 MiB) the call
- *   returns FA_ERR_INVALID_ARG and launches nothing.
+ *   The split size is fa_decode_paged's default; the partials fit whenever
+ *   B*H*(d+2)*4 bytes (one split per sequence) do, i.e. B*H <= 32263 at d = 128, and
+ *   beyond that the call returns FA_ERR_INVALID_ARG and launches nothing.
  *   The first call on each device, with that device current, looks up the scratch
- *   array's device address; make that first call before any stream capture.
+ *   array's device address and keeps it; make that first call before any stream
+ *   capture. After cudaDeviceReset in this process that address is stale: calls made
+ *   after a reset are not supported.
  *   Every call on a device shares the one array: calls whose kernels overlap on the
  *   GPU (for example on two streams) race and must be ordered by the caller.
  */

@@ -67,6 +67,10 @@ def lib():
         L.or_count_visible_layout.argtypes = [_i64, _i64, _i64, _vp, _i64]
         L.or_tile_class_layout.restype = ctypes.c_int
         L.or_tile_class_layout.argtypes = [_i64] * 7 + [_vp, _i64]
+        L.or_rescale_events.restype = ctypes.c_int
+        L.or_rescale_events.argtypes = [_vp, _vp, ctypes.c_int] + [_i64] * 5 + [
+            ctypes.c_double, ctypes.c_int, _i64, _i64, _vp, _i64, _i64, ctypes.c_double, _i64,
+            ctypes.c_double, _vp, _vp, ctypes.c_int]
         L.or_attention_backward.restype = ctypes.c_int
         L.or_attention_backward.argtypes = [_vp, _vp, _vp, _vp, ctypes.c_int, _vp, _vp, _vp,
                                             _i64, _i64, _i64, _i64, _i64, ctypes.c_double,
@@ -159,6 +163,29 @@ def online_attention(q, k, v, scale, mask_mode=MASK_NONE, window=0, n_global=0,
     if rc != 0:
         raise ValueError("or_online_attention rejected its arguments")
     return o, lse
+
+
+def rescale_events(q, k, scale, block_n, tau, mask_mode=MASK_NONE, window=0, n_global=0,
+                   layout=None, blk=128, tile_rows=128, eps=1e-3, nthreads=0):
+    """Rescales of the lazy online recurrence (threshold tau in natural-log units, key
+    blocks of block_n in ascending order), summed per tile of tile_rows query rows:
+    (counts, near) int64 [B*H, ceil(Sq/tile_rows)], near = decisions within eps of the
+    threshold. layout: block-sparse visibility instead of mask_mode."""
+    q, k = _cpu(q), _cpu(k)
+    B, H, Sq, d = q.shape
+    Sk = k.shape[2]
+    nt = -(-Sq // tile_rows)
+    counts = np.zeros((B * H, nt), dtype=np.int64)
+    near = np.zeros((B * H, nt), dtype=np.int64)
+    lay = None if layout is None else _layout(layout, H, Sq, Sk, blk)
+    rc = lib().or_rescale_events(q.data_ptr(), k.data_ptr(), _dtype_code(q, k), B, H, Sq, Sk,
+                                 d, float(scale), mask_mode, window, n_global,
+                                 None if lay is None else lay.ctypes.data, blk, block_n,
+                                 float(tau), tile_rows, float(eps), counts.ctypes.data,
+                                 near.ctypes.data, nthreads)
+    if rc != 0:
+        raise ValueError("or_rescale_events rejected its arguments")
+    return counts, near
 
 
 def decode_paged(q, k_pages, v_pages, block_table, ctx_lens, scale, bh_list=None, nthreads=0):

@@ -403,6 +403,97 @@ int or_online_attention(const void* q, const void* k, const void* v, int dtype,
     return 0;
 }
 
+static int layout_visible(const uint8_t* layout, int64_t h, int64_t i, int64_t j,
+                          int64_t nqb, int64_t nkb, int64_t blk);
+static int layout_blk_bad(const uint8_t* layout, int64_t blk) { return layout && blk <= 0; }
+
+/*
+ * How often the lazy form of the recurrence above (OR_REC_UNNORMALISED with
+ * threshold tau > 0, natural-log units) rescales: for every row, walk the keys
+ * in blocks of block_n in ascending order, skip the blocks in which the row sees
+ * no key, take the first visible block's maximum as the reference m, and count a
+ * rescale at every later block whose maximum exceeds m + tau (m then moves up
+ * to it). This is the correction step of the per-block (m, l, O) update
+ * ([Ascend-FA] 3.1, O * exp(m - m_new)), taken only when the maximum has risen
+ * far enough. Scores are s_j = scale * q . k_j in FP64 from the stored input
+ * values.
+ *
+ * The counts are summed per tile of tile_rows consecutive query rows of one
+ * (batch, head): counts[bh * ntiles + i / tile_rows], ntiles = ceil(Sq /
+ * tile_rows). near[...] counts, likewise, the decisions whose margin
+ * |(block max - m) - tau| is below eps: a computation in lower precision may
+ * take those the other way. layout != NULL selects the block-sparse visibility
+ * (blocks of blk, as or_attention_layout; mask_mode is then ignored).
+ * Returns 0, or -1 on a bad argument.
+ */
+int or_rescale_events(const void* q, const void* k, int dtype, int64_t B, int64_t H,
+                      int64_t Sq, int64_t Sk, int64_t d, double scale, int mask_mode,
+                      int64_t window, int64_t n_global, const uint8_t* layout, int64_t blk,
+                      int64_t block_n, double tau, int64_t tile_rows, double eps,
+                      int64_t* counts, int64_t* near, int nthreads) {
+    if (B < 0 || H < 0 || Sq < 0 || Sk < 0 || d <= 0 || block_n < 1 || tile_rows < 1)
+        return -1;
+    if (!(tau > 0.0) || layout_blk_bad(layout, blk)) return -1;
+    const int64_t ntiles = (Sq + tile_rows - 1) / tile_rows;
+    const int64_t nqb = layout ? (Sq + blk - 1) / blk : 0, nkb = layout ? (Sk + blk - 1) / blk : 0;
+    for (int64_t t = 0; t < B * H * ntiles; ++t) counts[t] = near[t] = 0;
+#ifdef _OPENMP
+    if (nthreads <= 0) nthreads = omp_get_max_threads();
+#pragma omp parallel num_threads(nthreads)
+#endif
+    {
+        double* qrow = (double*)malloc(sizeof(double) * (size_t)d);
+        double* kd = (double*)malloc(sizeof(double) * (size_t)(Sk > 0 ? Sk : 1) * (size_t)d);
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 1)
+#endif
+        for (int64_t bh = 0; bh < B * H; ++bh) {
+            const int64_t h = bh % (H > 0 ? H : 1);
+            or_decode((const char*)k + (size_t)(bh * Sk * d) * elem_size(dtype), kd, Sk * d, dtype);
+            for (int64_t i = 0; i < Sq; ++i) {
+                for (int64_t c = 0; c < d; ++c) qrow[c] = or_elem(q, (bh * Sq + i) * d + c, dtype);
+                double m = -INFINITY;
+                int64_t n_ev = 0, n_near = 0;
+                for (int64_t j0 = 0; j0 < Sk; j0 += block_n) {
+                    const int64_t j1 = (j0 + block_n < Sk) ? j0 + block_n : Sk;
+                    double bmax = -INFINITY;
+                    for (int64_t j = j0; j < j1; ++j) {
+                        const int vis = layout ? layout_visible(layout, h, i, j, nqb, nkb, blk)
+                                               : or_visible(i, j, Sq, Sk, mask_mode, window,
+                                                            n_global);
+                        if (!vis) continue;
+                        double dot = 0.0;
+                        for (int64_t c = 0; c < d; ++c) dot += qrow[c] * kd[j * d + c];
+                        if (scale * dot > bmax) bmax = scale * dot;
+                    }
+                    if (bmax == -INFINITY) continue; /* the row sees nothing here */
+                    if (m == -INFINITY) {
+                        m = bmax;
+                        continue;
+                    }
+                    if (fabs((bmax - m) - tau) < eps) ++n_near;
+                    if (bmax - m > tau) {
+                        ++n_ev;
+                        m = bmax;
+                    }
+                }
+                const int64_t t = bh * ntiles + i / tile_rows;
+#ifdef _OPENMP
+#pragma omp atomic
+#endif
+                counts[t] += n_ev;
+#ifdef _OPENMP
+#pragma omp atomic
+#endif
+                near[t] += n_near;
+            }
+        }
+        free(qrow);
+        free(kd);
+    }
+    return 0;
+}
+
 /* ------------------------------------------------------------------ */
 /* paged-KV decode                                                     */
 /* ------------------------------------------------------------------ */

@@ -55,6 +55,16 @@ int or_online_attention(const void* q, const void* k, const void* v, int dtype,
                         int mask_mode, int64_t window, int64_t n_global,
                         int64_t block_n, double tau, int variant);
 
+/* Rescale events of the lazy online recurrence (threshold tau, natural-log
+   units), summed per tile of tile_rows query rows: counts and near-threshold
+   decisions (|margin| < eps), each int64 [B*H*ceil(Sq/tile_rows)]. layout may
+   be NULL (closed-form mask) or a block layout as in or_attention_layout. */
+int or_rescale_events(const void* q, const void* k, int dtype, int64_t B, int64_t H,
+                      int64_t Sq, int64_t Sk, int64_t d, double scale, int mask_mode,
+                      int64_t window, int64_t n_global, const uint8_t* layout, int64_t blk,
+                      int64_t block_n, double tau, int64_t tile_rows, double eps,
+                      int64_t* counts, int64_t* near, int nthreads);
+
 int or_decode_paged(const void* q, const void* k_pages, const void* v_pages,
                     int dtype, const int32_t* block_table,
                     const int32_t* ctx_lens, double* o, double* lse, int64_t B,

@@ -756,3 +756,107 @@ def test_backward_closed_forms():
     # a row's dV contributions sum to dO_i: sum_j dV_j = sum_i dO_i (P rows sum to 1)
     _, _, dv = oracle.attention_backward(q, k, v, do, 0.5, MASK_NONE)
     np.testing.assert_allclose(dv.sum(axis=2), do.double().numpy().sum(axis=2), atol=1e-12)
+
+
+# --------------------------------------------------------------------------- #
+# rescale events of the lazy recurrence                                       #
+# --------------------------------------------------------------------------- #
+
+TAU = 8 * math.log(2)  # the kernels' threshold, 8 in log2 units, here in natural-log units
+
+
+def _lazy_count_closed_form(rises, tau):
+    """Rescales of a row whose visible blocks have maxima rising by rises[t] over the
+    previous block: the reference moves only when the rise accumulated since it was last
+    moved exceeds tau."""
+    acc, n = 0.0, 0
+    for r in rises:
+        acc += r
+        if acc > tau:
+            n, acc = n + 1, 0.0
+    return n
+
+
+@pytest.mark.parametrize("block_n", [64, 128, 48])
+@pytest.mark.parametrize("scale", [1 / 8, 1 / 512])
+def test_rescale_events_closed_form_on_a_noiseless_ramp(block_n, scale):
+    """q = 1, k_j = j / 8 (exact in fp16): s_j = scale * d * j / 8 rises by the same
+    amount per key, so a row's block maxima sit at the block's last visible key. Each row's
+    count follows from those rises in closed form: every block after the first when a
+    block's rise exceeds tau (scale 1/8), only every ceil(tau / rise)-th block when it does
+    not (scale 1/512: the lazy threshold, not an eager max update)."""
+    d, S = 64, 700
+    q = torch.ones(1, 1, S, d, dtype=torch.float16)
+    k = (torch.arange(S, dtype=torch.float32)[:, None] / 8).expand(S, d).reshape(1, 1, S, d)
+    k = k.to(torch.float16)
+    assert torch.equal(k.float()[0, 0, :, 0] * 8, torch.arange(S, dtype=torch.float32))
+    delta = scale * d / 8  # score rise per key
+    for mode in (MASK_NONE, MASK_CAUSAL):
+        counts, near = oracle.rescale_events(q, k, scale, block_n, TAU, mode, tile_rows=1)
+        assert near.sum() == 0
+        for i in range(S):
+            last = S - 1 if mode == MASK_NONE else i  # last visible key of row i
+            ends = [min(t + block_n, last + 1) - 1 for t in range(0, last + 1, block_n)]
+            rises = [(ends[t] - ends[t - 1]) * delta for t in range(1, len(ends))]
+            assert counts[0, i] == _lazy_count_closed_form(rises, TAU), (mode, i)
+    # the same keys in descending order: the first block holds every row's maximum
+    kd = k.flip(2).contiguous()
+    counts, _ = oracle.rescale_events(q, kd, scale, block_n, TAU, MASK_NONE)
+    assert counts.sum() == 0
+
+
+def _brute_rescales(q, k, scale, block_n, tau, vis):
+    """Rescale count of every row by a plain Python walk over the blocks."""
+    qd, kd = q.double().numpy()[0, 0], k.double().numpy()[0, 0]
+    out = []
+    for i in range(qd.shape[0]):
+        m, n = None, 0
+        for j0 in range(0, kd.shape[0], block_n):
+            js = [j for j in range(j0, min(j0 + block_n, kd.shape[0])) if vis(i, j)]
+            if not js:
+                continue
+            b = max(scale * float(qd[i] @ kd[j]) for j in js)
+            if m is None:
+                m = b
+            elif b - m > tau:
+                m, n = b, n + 1
+        out.append(n)
+    return np.array(out)
+
+
+@pytest.mark.parametrize("mask,w,g", [("none", 0, 0), ("causal", 0, 0), ("window", 40, 5),
+                                      ("band", 30, 0), ("prefix", 0, 50), ("layout", 0, 0)])
+def test_rescale_events_match_brute_force(mask, w, g):
+    """Random wide scores (q, k ~ N(0,1) * 3): the per-row counts equal a plain Python walk
+    of the blocks, for every mask and a block layout."""
+    Sq, Sk, d, bn = 150, 260, 32, 16
+    q, k, _ = inputs.prefill_inputs(1, 1, Sq, Sk, d, torch.bfloat16, factor=3.0, seed=17)
+    scale = 1 / math.sqrt(d)
+    mode = {"none": MASK_NONE, "causal": MASK_CAUSAL, "window": MASK_CAUSAL_WINDOW,
+            "band": MASK_BAND, "prefix": MASK_PREFIX_LM, "layout": MASK_NONE}[mask]
+    if mask == "layout":
+        lay = inputs.block_layout(1, Sq, Sk, block=64, local=0, n_global=0, n_random=2, seed=3)
+        def vis(i, j):
+            return bool(lay[0, i // 64, j // 64])
+        counts, near = oracle.rescale_events(q, k, scale, bn, TAU, layout=lay.numpy(), blk=64,
+                                             tile_rows=1)
+    else:
+        def vis(i, j):
+            return oracle.visible(i, j, Sq, Sk, mode, w, g)
+        counts, near = oracle.rescale_events(q, k, scale, bn, TAU, mode, w, g, tile_rows=1)
+    want = _brute_rescales(q, k, scale, bn, TAU, vis)
+    assert want.sum() > 20  # the inputs do reach the rescale step
+    assert np.array_equal(counts[0], want)
+    # per-tile sums are the row counts added up
+    c128, _ = oracle.rescale_events(q, k, scale, bn, TAU, mode, w, g, tile_rows=128,
+                                    layout=lay.numpy() if mask == "layout" else None, blk=64)
+    assert c128[0].tolist() == [int(want[:128].sum()), int(want[128:].sum())]
+
+
+def test_rescale_events_threshold_limits():
+    """A threshold above every rise gives no rescale; tau must be positive."""
+    q, k, _ = inputs.prefill_inputs(1, 2, 64, 300, 64, torch.float16, factor=2.0, seed=4)
+    counts, _ = oracle.rescale_events(q, k, 0.125, 32, 1e9)
+    assert counts.sum() == 0
+    with pytest.raises(ValueError):
+        oracle.rescale_events(q, k, 0.125, 32, 0.0)

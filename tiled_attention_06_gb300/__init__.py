@@ -52,7 +52,7 @@ class FwdParams(ctypes.Structure):
                 ("block_n", _i), ("block_m", _i), ("num_ctas", _i), ("group_heads", _i),
                 ("timeout_us", _u32),
                 ("trace", _vp), ("block_layout", _vp), ("workspace", _vp),
-                ("workspace_bytes", _sz)]
+                ("workspace_bytes", _sz), ("rescale_count", _vp)]
 
 
 class DecodeParams(ctypes.Structure):
@@ -214,13 +214,14 @@ def fa_fwd(q, k, v, o, lse, scale, mask_mode=FA_MASK_NONE, window=0, n_global=0,
 
 def fa_fwd_ex(q, k, v, o, lse, scale, mask_mode=FA_MASK_NONE, window=0, n_global=0,
               block_n=0, block_m=0, num_ctas=0, group_heads=0, timeout_us=0, trace=None,
-              block_layout=None, workspace=None, stream=None):
+              block_layout=None, workspace=None, rescale_count=None, stream=None):
     """fa_fwd with the tuning and debug fields of fa_fwd_params. block_layout: uint8 CUDA
     tensor [H, ceil(Sq/128), ceil(Sk/128)] for FA_MASK_BLOCK_SPARSE. workspace: CUDA byte
     tensor of fa_fwd_workspace_size(...) bytes for float32 inputs (allocated here when
-    None)."""
+    None). rescale_count: zeroed int32 CUDA tensor [B*H, ceil(Sq/128)] that counts the
+    rows whose output was rescaled, per 128-query tile."""
     _need_cuda_contig(q=q, k=k, v=v, o=o, lse=lse, trace=trace, block_layout=block_layout,
-                      workspace=workspace)
+                      workspace=workspace, rescale_count=rescale_count)
     B, H, Sq, d = q.shape
     dt = _dtype_code(q)
     if workspace is None and dt == FA_F32:
@@ -230,7 +231,7 @@ def fa_fwd_ex(q, k, v, o, lse, scale, mask_mode=FA_MASK_NONE, window=0, n_global
     p = FwdParams(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), _ptr(lse), B, H, Sq,
                   k.shape[2], d, float(scale), mask_mode, window, n_global, dt,
                   block_n, block_m, num_ctas, group_heads, timeout_us, _ptr(trace),
-                  _ptr(block_layout), _ptr(workspace), ws_bytes)
+                  _ptr(block_layout), _ptr(workspace), ws_bytes, _ptr(rescale_count))
     _check(lib().fa_fwd_ex(ctypes.byref(p), _stream(stream)))
 
 

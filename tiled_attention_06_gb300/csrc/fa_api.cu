@@ -295,6 +295,7 @@ fa_status run_fwd(const fa_fwd_params& a, const PagedKV* pg, fa_stream_t stream)
   p.status = dev.status;
   p.timeout_ns = static_cast<uint64_t>(a.timeout_us ? a.timeout_us : 1000000u) * 1000u;
   p.trace = a.trace;
+  p.rescales = a.rescale_count;
   p.H = a.H;
   if (a.mask_mode == FA_MASK_BLOCK_SPARSE) {  // planned as dense: the layout is on the device
     p.layout = a.block_layout;
@@ -561,23 +562,20 @@ fa_status fa_decode_paged_noalloc(const void* q, const void* k_pages, const void
   const long long pool = static_cast<long long>(num_pages) * H * page_size * d;
   if (max_ctx > (1LL << 30) || static_cast<long long>(B) * H > (1LL << 30) || pool > (1LL << 46))
     return fail(FA_ERR_INVALID_ARG, "problem too large");
-  // Pick the split size as fa_decode_paged does, then coarsen it until the partials
-  // fit in the library's fixed scratch array.
+  // The split size is fa_decode_paged's default. That default keeps B*H*splits at or
+  // below 16384 whenever one split per sequence allows it (16384*(d+2)*4 bytes, 8.5 MB
+  // at d = 128, fit the scratch), and is one split per sequence otherwise, so the
+  // partials fit exactly when B*H*(d+2)*4 bytes do.
   const size_t cap = fa::noalloc_scratch_bytes();
-  auto partial_bytes = [&](int pps_) {
-    const long long ns = (max_pages_per_seq + pps_ - 1) / pps_;
-    return static_cast<size_t>(B) * H * ns * (d + 2) * sizeof(float);
-  };
-  int pps = fa_decode_default_pages_per_split(B, H, max_pages_per_seq);
-  while (partial_bytes(pps) > cap && pps < max_pages_per_seq) {
-    pps *= 2;
-    if (pps > max_pages_per_seq) pps = max_pages_per_seq;
-  }
-  if (partial_bytes(pps) > cap)
+  const int pps = fa_decode_default_pages_per_split(B, H, max_pages_per_seq);
+  const size_t partial_bytes = static_cast<size_t>(B) * H *
+                               ((max_pages_per_seq + pps - 1) / pps) * (d + 2) * sizeof(float);
+  if (partial_bytes > cap)
     return fail(FA_ERR_INVALID_ARG,
-                "B*H*(d+2)*4 = %zu bytes of split partials exceed the %zu-byte scratch of "
-                "fa_decode_paged_noalloc; use fa_decode_paged with a workspace",
-                partial_bytes(pps), cap);
+                "%zu bytes of split partials exceed the %zu-byte scratch of "
+                "fa_decode_paged_noalloc (B*H*(d+2)*4 must fit); use fa_decode_paged with a "
+                "workspace",
+                partial_bytes, cap);
   DeviceInfo dev;
   fa_status st = device_info(&dev);
   if (st != FA_OK) return st;

@@ -26,6 +26,7 @@ struct PrefillParams {
   uint32_t* status;   // device status word
   uint64_t timeout_ns;
   int32_t* trace;     // optional [BH, ceil(Sq/128), nnb] visit log (16 + class per visit)
+  int32_t* rescales;  // optional [BH, ceil(Sq/128)]: (row, key tile) pairs whose O was rescaled
   // Paged K/V (chunked prefill into a paged cache). block_table == nullptr: K and V are
   // contiguous [B,H,Sk,d]. Otherwise K/V tile rows come from pools [num_pages,H,page,d]
   // through block_table [B, max_pages], sequence b has seq_k[b] keys and Sk is only the

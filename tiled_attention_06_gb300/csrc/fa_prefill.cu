@@ -52,12 +52,6 @@ namespace {
 
 constexpr int kTile = 128;                // rows of one tcgen05 M=128 tile (= TMEM lanes)
 constexpr float kTau = 8.0f;              // lazy-rescale threshold, log2 units
-#ifndef FA_EXP2_POLY_PAIRS
-#define FA_EXP2_POLY_PAIRS 0
-#endif
-// of every 8 exponential pairs on a full tile, how many use the polynomial exponential
-constexpr int kExp2Poly = FA_EXP2_POLY_PAIRS;
-static_assert(kExp2Poly >= 0 && kExp2Poly <= 8, "pairs out of 8");
 constexpr uint32_t kSmemLimit = 232448;   // 227 KB opt-in dynamic shared memory per CTA
 
 constexpr int pow2_at_least(int x) {
@@ -125,16 +119,18 @@ __device__ __forceinline__ uint32_t pack2(float a, float b, bool bf16) {
 // P = 2^(S*sl2 - m) is written as packed 16-bit pairs to NC/2 columns at p_col.
 // SPLIT (FP32 inputs): P is written as two bf16 parts, P_hi = bf16(P) at p_col and
 // P_lo = bf16(P - P_hi) at p_col + NC/2, so that P_hi + P_lo holds P to 2^-16.
-// l accumulates the sum over this thread's NC columns. Returns false on abort.
-template <int NC, int ON, bool BF16, int POLY, bool SPLIT, typename Exchange,
+// l accumulates the sum over this thread's NC columns. With p.rescales set, the rows
+// rescaled are counted for the 128-row tile (rs_bh, rs_m0) when rs_bh >= 0. Returns
+// false on abort.
+template <int NC, int ON, bool BF16, bool SPLIT, typename Exchange,
           typename PreRescale>
 __device__ __forceinline__ bool softmax_cols(uint32_t t_lane, uint32_t s_col, uint32_t p_col,
                                              uint32_t o_col, bool full, int n0, int pos_q,
                                              int sk, const PrefillParams& p, float& m_ref,
                                              float& l, Exchange exchange,
-                                             PreRescale before_rescale) {
+                                             PreRescale before_rescale, int rs_bh, int rs_m0) {
   static_assert(NC == 32 || NC % 64 == 0, "column count");
-  static_assert(!SPLIT || (BF16 && NC % 64 == 0 && POLY == 0), "split P: bf16, 64-column groups");
+  static_assert(!SPLIT || (BF16 && NC % 64 == 0), "split P: bf16, 64-column groups");
   uint32_t s[NC];
   uint32_t lo[SPLIT ? NC / 2 : 1];
   if constexpr (NC == 32) {
@@ -180,6 +176,13 @@ __device__ __forceinline__ bool softmax_cols(uint32_t t_lane, uint32_t s_col, ui
   const bool need = (m_ref != -INFINITY) && (m_new > m_ref + kTau);
   if (m_ref == -INFINITY) m_ref = m_new;
   if (__any_sync(0xffffffffu, need)) {
+    if (p.rescales && rs_bh >= 0) {  // debug count: one atomic per warp
+      const uint32_t who = __ballot_sync(0xffffffffu, need);
+      if ((threadIdx.x & 31) == 0)
+        atomicAdd(p.rescales + static_cast<size_t>(rs_bh) * ((p.Sq + kTile - 1) / kTile) +
+                      rs_m0 / kTile,
+                  __popc(who));
+    }
     if (!before_rescale()) return false;
     const float alpha = need ? ex2_approx(m_ref - m_new) : 1.f;
     if (need) {
@@ -197,41 +200,23 @@ __device__ __forceinline__ bool softmax_cols(uint32_t t_lane, uint32_t s_col, ui
     }
   }
   // P = 2^(S*sl2 - m): the exponent argument two lanes at a time, one exponential per
-  // element, the row sum in four packed pairs. On full tiles (every S finite) POLY of
-  // every 8 pairs take the polynomial exponential, which runs on the FMA pipe, so that the
-  // MUFU unit (16 exponentials per clock per SM, as many cycles per 128x128 tile as its
-  // MMAs) is no longer the limit. Masked (-inf) entries always take ex2, which gives 0.
+  // element (masked -inf entries give 0), the row sum in four packed pairs.
   const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
   const uint64_t scale2 = f2(p.sl2, p.sl2), neg_m2 = f2(-m_use, -m_use);
   uint64_t acc[4] = {0, 0, 0, 0};
-  auto exp_pairs = [&](auto use_poly) {
 #pragma unroll
-    for (int c = 0; c < NC; c += 2) {
-      const uint64_t x =
-          f2_fma(f2(__uint_as_float(s[c]), __uint_as_float(s[c + 1])), scale2, neg_m2);
-      float x0, x1, p0, p1;
-      f2_split(x, x0, x1);
-      if (decltype(use_poly)::value && ((c / 2) & 7) >= 8 - POLY) {
-        exp2_poly_x2(x0, x1, p0, p1);
-      } else {
-        p0 = ex2_approx(x0);
-        p1 = ex2_approx(x1);
-      }
-      acc[(c / 2) & 3] = f2_add(acc[(c / 2) & 3], f2(p0, p1));
-      const uint32_t hi = BF16 ? cvt_pack_bf16(p0, p1) : cvt_pack_f16(p0, p1);
-      s[c / 2] = hi;
-      if constexpr (SPLIT)  // residuals against the bf16 values (low half: p0)
-        lo[c / 2] = cvt_pack_bf16(p0 - __uint_as_float(hi << 16),
-                                  p1 - __uint_as_float(hi & 0xffff0000u));
-    }
-  };
-  if constexpr (POLY > 0) {
-    if (full)
-      exp_pairs(std::true_type{});
-    else
-      exp_pairs(std::false_type{});
-  } else {
-    exp_pairs(std::false_type{});
+  for (int c = 0; c < NC; c += 2) {
+    const uint64_t x =
+        f2_fma(f2(__uint_as_float(s[c]), __uint_as_float(s[c + 1])), scale2, neg_m2);
+    float x0, x1;
+    f2_split(x, x0, x1);
+    const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+    acc[(c / 2) & 3] = f2_add(acc[(c / 2) & 3], f2(p0, p1));
+    const uint32_t hi = BF16 ? cvt_pack_bf16(p0, p1) : cvt_pack_f16(p0, p1);
+    s[c / 2] = hi;
+    if constexpr (SPLIT)  // residuals against the bf16 values (low half: p0)
+      lo[c / 2] = cvt_pack_bf16(p0 - __uint_as_float(hi << 16),
+                                p1 - __uint_as_float(hi & 0xffff0000u));
   }
   float a0, a1;
   f2_split(f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3])), a0, a1);
@@ -255,11 +240,10 @@ template <int D, int BN, bool BF16, bool SPLIT, typename PreRescale>
 __device__ __forceinline__ bool softmax_tile(uint32_t t_lane, uint32_t s_col, uint32_t o_col,
                                              bool full, int n0, int pos_q, int sk,
                                              const PrefillParams& p, float& m_ref, float& l,
-                                             PreRescale before_rescale) {
-  // (a whole row of S in registers leaves no room for the polynomial's temporaries)
-  return softmax_cols<BN, D, BF16, 0, SPLIT>(t_lane, s_col, s_col, o_col, full, n0, pos_q, sk,
-                                             p, m_ref, l, [](float m) { return m; },
-                                             before_rescale);
+                                             PreRescale before_rescale, int rs_bh, int rs_m0) {
+  return softmax_cols<BN, D, BF16, SPLIT>(t_lane, s_col, s_col, o_col, full, n0, pos_q, sk,
+                                          p, m_ref, l, [](float m) { return m; },
+                                          before_rescale, rs_bh, rs_m0);
 }
 
 // Epilogue for one thread's row: O (D columns at o_col) / l rounded to the dtype (FP32
@@ -630,7 +614,7 @@ __global__ void __launch_bounds__(kThreads256, 1)
                     16 + (full ? 2 : 1));
         // S(j) was issued after PV(j-1), so O needs no wait before a rescale
         ok = softmax_tile<D, BN, BF16, SPLIT>(t_lane, s_col, o_col, full, nb * BN, pos_q, sk_t, p,
-                                       m_ref, l, [] { return true; });
+                                              m_ref, l, [] { return true; }, bh, m0);
         tc_fence_before();
         mbar_arrive(B(bars->p_full[q]));
         ++tc;
@@ -1060,11 +1044,11 @@ __global__ void __launch_bounds__(kThreads128, 1)
           return w;
         };
         const uint32_t s_col = (g & 1) * BN;
-        ok = softmax_cols<BN / 2, D / 2, BF16, kExp2Poly, false>(t_lane, s_col + half * (BN / 2),
+        ok = softmax_cols<BN / 2, D / 2, BF16, false>(t_lane, s_col + half * (BN / 2),
                                                s_col + half * (BN / 4),
                                                2 * BN + buf * D + half * (D / 2), full,
                                                nb * BN + half * (BN / 2), pos_q, it.sk, p, m_ref,
-                                               l, exchange, wait_pv);
+                                               l, exchange, wait_pv, half == 0 ? it.bh : -1, m0);
         if (!ok || !x_ok) {
           ok = false;
           break;

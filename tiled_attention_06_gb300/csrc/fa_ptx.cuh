@@ -374,30 +374,6 @@ __device__ __forceinline__ float ex2_approx(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
-// 2^x for two finite lanes on the FMA and integer pipes instead of the MUFU unit.
-// Range reduction (Cody-Waite with one constant): r = rint(x) by adding and then
-// subtracting 1.5 * 2^23, whose ulp is 1 (exact for |x| < 2^22), and f = x - r, exactly,
-// in [-1/2, 1/2]. 2^f: degree-3 discrete minimax polynomial in relative error on
-// [-1/2, 1/2] (max relative error 7.5e-5; coefficients printed by exp2_poly_fit.py).
-// 2^r: the low bits of x + 1.5 * 2^23 hold r in two's complement, so shifting them left by
-// 23 gives r in the exponent field, added to the polynomial's bits. x is clamped at -126
-// so that the exponent cannot wrap: the result for x < -126 is below 2^-125, not 0.
-__device__ __forceinline__ void exp2_poly_x2(float x0, float x1, float& y0, float& y1) {
-  constexpr float kShift = 12582912.0f;  // 1.5 * 2^23
-  constexpr float kC0 = 9.999280572e-01f, kC1 = 6.932609677e-01f, kC2 = 2.426111251e-01f,
-                  kC3 = 5.517166853e-02f;
-  const uint64_t x = f2(fmaxf(x0, -126.f), fmaxf(x1, -126.f));
-  const uint64_t t = f2_add(x, f2(kShift, kShift));
-  const uint64_t f = f2_fma(f2_add(t, f2(-kShift, -kShift)), f2(-1.f, -1.f), x);
-  uint64_t p = f2_fma(f2(kC3, kC3), f, f2(kC2, kC2));
-  p = f2_fma(p, f, f2(kC1, kC1));
-  p = f2_fma(p, f, f2(kC0, kC0));
-  float p0, p1, t0, t1;
-  f2_split(p, p0, p1);
-  f2_split(t, t0, t1);
-  y0 = __int_as_float(__float_as_int(p0) + (__float_as_int(t0) << 23));
-  y1 = __int_as_float(__float_as_int(p1) + (__float_as_int(t1) << 23));
-}
 __device__ __forceinline__ float lg2_approx(float x) {
   float y;
   asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
