@@ -33,6 +33,15 @@ sys.path.insert(0, ROOT)
 
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# Nominal dense FP16/BF16 tensor-core rate of one GPU: NVIDIA's HGX B300 figure, 36 PFLOPS
+# FP16/BF16 for 8 GPUs, which NVIDIA quotes with 2:4 sparsity, halved for dense math.
+NOMINAL_BF16_TFLOPS = 2250.0
+NOMINAL_SOURCE = ("NVIDIA HGX B300 spec: FP16/BF16 tensor core 36 PFLOPS per 8 GPUs with 2:4 "
+                  "sparsity = 2.25 PFLOP/s dense per GPU")
+# Untimed steps run back to back while the clock sampler is on, just before the timed
+# ones, so that the sampled clocks show the kernels under sustained load even when the
+# timed region itself is short.
+CLOCK_SOAK_S = 1.5
 
 PREFILL = {
     "causal2k": dict(B=4, H=32, S=2048, d=128, dtype="f16", mode=1, window=0, n_global=0,
@@ -359,6 +368,16 @@ def run_ours(args, rank, world):
     clocks = ClockSampler(dev.index)
     clocks.start()
     time.sleep(0.3)
+    soak, t_soak = 0, time.perf_counter()
+    while time.perf_counter() - t_soak < CLOCK_SOAK_S:
+        for _ in range(8):
+            if pcfg:
+                prefill_call()
+            if with_decode:
+                decode_call()
+        soak += 8
+        torch.cuda.synchronize()
+    t_soak = time.perf_counter() - t_soak
     barrier(world)
     torch.cuda.synchronize()
     for i in range(K):
@@ -381,6 +400,9 @@ def run_ours(args, rank, world):
     # an FP32 prefill is two launches: the split into bf16 planes and the prefill kernel
     launches = K * ((0 if not pcfg else 2 if f32 else 1) + (2 if with_decode else 0))
 
+    clk["soak"] = {"steps": soak, "seconds": round(t_soak, 3),
+                   "note": "clocks sampled over untimed back-to-back steps just before the "
+                           "timed ones, and during them"}
     res = {"n_gpus": world, "steps": K, "warmup": W, "ms_per_step": total_ms / K,
            "scaling": "weak", "vs_baseline": None, "data": "synthetic (seeded N(0,1), "
            "shapes of the pages' workloads; no dataset)", "gpu_launches": launches,
@@ -411,7 +433,10 @@ def run_ours(args, rank, world):
                            "traffic": ncu_traffic("prefill_f32" if f32 else "prefill",
                                                   tkey, args.prefill_traffic),
                            "algorithmic_flops": pflops,
-                           "ms_per_launch": p_avg * 1e3}
+                           "ms_per_launch": p_avg * 1e3,
+                           "peak_nominal": NOMINAL_BF16_TFLOPS,
+                           "frac_nominal": achieved / NOMINAL_BF16_TFLOPS,
+                           "nominal_source": NOMINAL_SOURCE}
         if f32:  # the tensor cores run three bf16 products per product of the method
             res["roofline"]["tensor_flops_executed"] = 3 * pflops
             res["roofline"]["tensor_frac"] = 3 * achieved / tc_peak
@@ -462,6 +487,54 @@ def workload_config(pcfg, with_decode, world):
     cfg["parallelism"] = f"replicas x{world}" if world > 1 else "single GPU"
     cfg["l2"] = "inputs larger than L2 (no flush)"
     return cfg
+
+
+def measure_link(h2d_bytes, d2h_bytes, dev, reps=3):
+    """Pinned host <-> device copy bandwidth on this machine, the limit of an end-to-end call:
+    one cudaMemcpyAsync (tensor.copy_) of the step's input bytes host to device, one of its
+    output bytes device to host, and both directions at once on two streams; CUDA events,
+    best of `reps`. GB/s = bytes moved / time."""
+    hin = torch.empty(h2d_bytes, dtype=torch.uint8).pin_memory()
+    hout = torch.empty(d2h_bytes, dtype=torch.uint8).pin_memory()
+    din = torch.empty(h2d_bytes, dtype=torch.uint8, device=dev)
+    dout = torch.empty(d2h_bytes, dtype=torch.uint8, device=dev)
+    s1, s2 = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+
+    def best(fn):
+        t = []
+        for _ in range(reps + 1):
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s1)
+            fn()
+            s1.wait_stream(s2)
+            e1.record(s1)
+            torch.cuda.synchronize()
+            t.append(e0.elapsed_time(e1) / 1e3)
+        return min(t[1:])
+
+    def h2d():
+        with torch.cuda.stream(s1):
+            din.copy_(hin, non_blocking=True)
+
+    def d2h():
+        with torch.cuda.stream(s1):
+            hout.copy_(dout, non_blocking=True)
+
+    def both():
+        s2.wait_stream(s1)
+        with torch.cuda.stream(s1):
+            din.copy_(hin, non_blocking=True)
+        with torch.cuda.stream(s2):
+            hout.copy_(dout, non_blocking=True)
+
+    t_in, t_out, t_both = best(h2d), best(d2h), best(both)
+    del hin, hout, din, dout
+    return {"h2d_gbs": h2d_bytes / t_in / 1e9, "d2h_gbs": d2h_bytes / t_out / 1e9,
+            "both_ms": t_both * 1e3, "h2d_ms": t_in * 1e3, "d2h_ms": t_out * 1e3,
+            "how": "pinned tensor.copy_ (one cudaMemcpyAsync) of the step's input bytes H2D "
+                   "and output bytes D2H, alone and both at once on two streams; best of "
+                   f"{reps}, CUDA events"}
 
 
 def e2e_prefill(fa, pcfg, q, k, v, pflops, scale, stream, world, args, layout=None, ws32=None):
@@ -541,8 +614,15 @@ def e2e_prefill(fa, pcfg, q, k, v, pflops, scale, stream, world, args, layout=No
     d2h = ho.numel() * ho.element_size() + hl.numel() * 4
     api = ("tiled_attention_06_gb300.fa_fwd_ex (C ABI fa_fwd_ex)" if ws32 is not None
            or layout is not None else "tiled_attention_06_gb300.fa_fwd (C ABI fa_fwd)")
+    link = measure_link(h2d, d2h, dev)
+    # with copies in, the call and copies out overlapped, a step can be no shorter than
+    # the copies of its bytes both ways at once
+    step_ms = secs / K * 1e3
+    link["step_ms"] = step_ms
+    link["frac_of_link"] = link["both_ms"] / step_ms
     return {"value": aggregate(pflops * K, secs, world) / 1e12, "unit": "TFLOP/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": K,
+            "h2d_gbs_achieved": h2d / (step_ms / 1e3) / 1e9, "link": link,
             "api": api + " with pinned host buffers; steps pipelined over two device buffer "
                          "sets (copies in / call / copies out on three streams)"}
 
@@ -668,7 +748,15 @@ def timed(calls, K, W, stream):
     clocks = ClockSampler(torch.cuda.current_device())
     clocks.start()
     time.sleep(0.3)
+    soak, t_soak = 0, time.perf_counter()
+    while time.perf_counter() - t_soak < CLOCK_SOAK_S:
+        for c in calls:
+            c()
+        soak += 1
+        if soak % 8 == 0:
+            torch.cuda.synchronize()
     torch.cuda.synchronize()
+    t_soak = time.perf_counter() - t_soak
     for i in range(K):
         ev[i][0].record(stream)
         for j, c in enumerate(calls):
@@ -676,6 +764,7 @@ def timed(calls, K, W, stream):
             ev[i][j + 1].record(stream)
     torch.cuda.synchronize()
     clk = clocks.stop()
+    clk["soak"] = {"steps": soak, "seconds": round(t_soak, 3)}
     return [sum(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(K))
             for j in range(len(calls))], clk
 
@@ -821,68 +910,90 @@ def run_backward(args, fa, peaks, stream, world):
 
 
 # --------------------------------------------------------------------------- reference arm
-def run_reference(args, rank, world):
-    """The oracle as it stands, on the host cores: each step is a bounded sample of the
-    same workload (the last 256 query rows of one (batch, head) of the prefill, and
-    one sequence of the decode)."""
-    import numpy as np
+def reference_rows(S, n_bh, rows_per_bh, seed=0):
+    """Seeded query rows for the reference arm: rows_per_bh distinct rows of every one of
+    the n_bh (batch, head) pairs, as flat ids bh * S + i, and the rows' positions."""
+    g = torch.Generator().manual_seed(seed)
+    pos = torch.randperm(S, generator=g)[:min(rows_per_bh, S)].sort().values.numpy()
+    flat = (np.arange(n_bh, dtype=np.int64)[:, None] * S + pos[None, :]).reshape(-1)
+    return flat, pos
 
+
+def run_reference(args, rank, world):
+    """The oracle as it stands, on the host cores, on the workload of our arm.
+
+    Each step is a bounded sample of that workload. Prefill: the same seeded 512 query
+    rows of every (batch, head) pair (the oracle parallelises over (batch, head) pairs, so
+    every core has pairs to work on); decode (when our arm's step has one): every
+    sequence with all its heads. Prefill and decode are timed apart, like our arm's."""
     import oracle
-    from tiled_attention_06_gb300 import inputs
     workload = args.workload if args.workload in PREFIX_WORKLOADS else "default"
     pcfg = None if workload == "decode" else PREFILL["causal4k" if workload == "default"
                                                      else workload]
+    with_decode = workload in ("default", "decode")
     res = {"impl": "reference", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
            "scaling": "weak", "vs_baseline": None, "data": "synthetic (seeded N(0,1))",
            "gpu_launches": 0}
-    rows_per = 256
+    cores = oracle.threads_used()
     if pcfg:
         q, k, v = make_prefill(pcfg, None)
-        S = pcfg["S"]
-        BH = pcfg["B"] * pcfg["H"]
-        pairs_per_step = sum(visible_pairs_row(i, S, pcfg) for i in range(S - rows_per, S))
+        S, BH = pcfg["S"], pcfg["B"] * pcfg["H"]
+        rows, pos = reference_rows(S, BH, 512)
+        pflops_step = 4.0 * pcfg["d"] * BH * sum(visible_pairs_row(int(i), S, pcfg) for i in pos)
+        psample = (f"FP64 oracle, the same {len(pos)} seeded query rows of each of the {BH} "
+                   "(batch, head) pairs per step")
 
-        def step(i):
-            bh = i % BH
-            rows = np.arange(bh * S + S - rows_per, bh * S + S, dtype=np.int64)
+        def pstep():
             oracle.attention(q, k, v, 1 / math.sqrt(pcfg["d"]), pcfg["mode"], pcfg["window"],
                              pcfg["n_global"], rows=rows)
-        units = 4.0 * pairs_per_step * pcfg["d"]
-        unit, scale_div, metric = "TFLOP/s", 1e12, ("attention fwd TFLOP/s (% BF16 TC peak); "
-                                                    "paged decode HBM GB/s (% of 8 TB/s)")
-        sample = f"last {rows_per} query rows of one (batch, head) per step"
-        dtype = pcfg["dtype"]
-    else:
+    if with_decode:
         di = make_decode(None)
+        dbytes_step = decode_bytes(di.ctx_lens.tolist(), di.B, di.H, di.d,
+                                   di.block_table.shape[1])
+        dsample = f"FP64 oracle, all {di.B} sequences with all {di.H} heads per step"
 
-        def step(i):
-            b = i % di.B
+        def dstep():
             oracle.decode_paged(di.q, di.k_pages, di.v_pages, di.block_table, di.ctx_lens,
-                                1 / math.sqrt(di.d), bh_list=np.arange(b * di.H, (b + 1) * di.H))
-        units = None
-        unit, scale_div, metric = "GB/s", 1e9, "paged decode HBM GB/s (% of 8 TB/s)"
-        sample = "one sequence (all heads) per step"
-        dtype = "f16"
-    for i in range(args.warmup):
-        step(i)
-    t0 = time.perf_counter()
-    total_units = 0.0
-    for i in range(args.steps):
-        step(i)
-        if units is None:
-            b = i % di.B
-            total_units += decode_bytes([int(di.ctx_lens[b])], 1, di.H, di.d,
-                                        di.block_table.shape[1])
+                                1 / math.sqrt(di.d))
+    for _ in range(args.warmup):
+        if pcfg:
+            pstep()
+        if with_decode:
+            dstep()
+    p_s = d_s = 0.0
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        if pcfg:
+            pstep()
+        t1 = time.perf_counter()
+        if with_decode:
+            dstep()
+        t2 = time.perf_counter()
+        p_s += t1 - t0
+        d_s += t2 - t1
+    K = args.steps
+    if pcfg:
+        value = pflops_step * K / p_s / 1e12
+        res.update({"metric": "attention fwd TFLOP/s (% BF16 TC peak); paged decode HBM GB/s "
+                              "(% of 8 TB/s)",
+                    "value": value, "unit": "TFLOP/s", "dtype": pcfg["dtype"]})
+        res["cpu_baseline"] = {"kind": "oracle", "value": value, "unit": "TFLOP/s",
+                               "cores": cores, "sample": psample, "cpu": cpu_model(),
+                               "seconds": p_s}
+    if with_decode:
+        dval = dbytes_step * K / d_s / 1e9
+        dec = {"value": dval, "unit": "GB/s", "cores": cores, "sample": dsample, "seconds": d_s}
+        if pcfg:
+            res["decode"] = {"value": dval, "unit": "GB/s"}
+            res["cpu_baseline"]["decode"] = dec
         else:
-            total_units += units
-    secs = time.perf_counter() - t0
-    value = total_units / secs / scale_div
-    res.update({"metric": metric, "value": value, "unit": unit, "higher_is_better": True,
-                "ms_per_step": secs / args.steps * 1e3, "dtype": dtype,
-                "config": workload_config(pcfg, pcfg is None, 1)})
-    res["cpu_baseline"] = {"kind": "oracle", "value": value, "unit": unit,
-                           "cores": oracle.threads_used(), "sample": sample, "cpu": cpu_model()}
-    res["e2e"] = {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+            res.update({"metric": "paged decode HBM GB/s (% of 8 TB/s)", "value": dval,
+                        "unit": "GB/s", "dtype": "f16"})
+            res["cpu_baseline"] = dict(kind="oracle", cpu=cpu_model(), **dec)
+    res.update({"higher_is_better": True, "ms_per_step": (p_s + d_s) / K * 1e3,
+                "config": workload_config(pcfg, with_decode, 1)})
+    res["e2e"] = {"value": res["value"], "unit": res["unit"], "h2d_bytes_per_step": 0,
+                  "d2h_bytes_per_step": 0}
     return res
 
 

@@ -49,9 +49,14 @@ def _built():
 
 def climbing(B, H, Sq, Sk, d, dtype, kind, scale, bn, seed):
     """'up': scores rise by RISE_LOG2 per bn-key tile; 'down': they fall as much; 'wide':
-    q, k ~ N(0,1) * 4."""
+    q, k ~ N(0,1) * 4 and v ~ N(0,1) / 2. Such wide scores put nearly all of a row's
+    weight on one key, so O is close to a single V row; with v ~ N(0,1) that row can
+    exceed 4, where one bf16 rounding of O alone may cost 2^-6, and P's own rounding
+    (2^-9 relative) comes on top. Halving V keeps that sum inside the 2e-2 bound the
+    16-bit tests use, which still leaves any wrong rescale visible."""
     if kind == "wide":
-        return inputs.climbing_inputs(B, H, Sq, Sk, d, dtype, step=0.0, wide=4.0, seed=seed)
+        return inputs.climbing_inputs(B, H, Sq, Sk, d, dtype, step=0.0, wide=4.0, v_scale=0.5,
+                                      seed=seed)
     step = RISE_LOG2 * math.log(2) / (scale * bn)  # raw q.k rise per key
     return inputs.climbing_inputs(B, H, Sq, Sk, d, dtype, step=step if kind == "up" else -step,
                                   seed=seed)

@@ -39,22 +39,23 @@ def f32_resolution_inputs(B, H, Sq, Sk, d, seed=0):
     return q, k, v
 
 
-def climbing_inputs(B, H, Sq, Sk, d, dtype=torch.float16, step=0.0, wide=1.0, seed=0):
+def climbing_inputs(B, H, Sq, Sk, d, dtype=torch.float16, step=0.0, wide=1.0, v_scale=1.0,
+                    seed=0):
     """q, k, v whose scores climb (step > 0) or fall (step < 0) along the key axis.
 
     q = N(0,1) * wide + 1 and k_j = N(0,1) * wide + a_j with a_j = step * j / d (step > 0)
     or step * (j - Sk + 1) / d (step < 0), every component of a row shifted alike; then
     q . k_j = |step| * j + (a zero-mean part), so the raw dot product rises by about |step|
-    per key for ascending keys (falls for step < 0) whatever the query. v ~ N(0,1). With
-    step = 0 and wide > 1 the scores are only wider (N(0, wide^4)-like). The values are
-    drawn in float32 and cast to `dtype`.
+    per key for ascending keys (falls for step < 0) whatever the query.
+    v ~ N(0,1) * v_scale. With step = 0 and wide > 1 the scores are only wider
+    (N(0, wide^4)-like). The values are drawn in float32 and cast to `dtype`.
 
     Draw order: q, k, v.
     """
     g = torch.Generator().manual_seed(seed)
     q = torch.randn(B, H, Sq, d, generator=g) * wide + (1.0 if step != 0 else 0.0)
     k = torch.randn(B, H, Sk, d, generator=g) * wide
-    v = torch.randn(B, H, Sk, d, generator=g)
+    v = torch.randn(B, H, Sk, d, generator=g) * v_scale
     if step != 0:
         j = torch.arange(Sk, dtype=torch.float32)
         a = (step * j if step > 0 else step * (j - (Sk - 1))) / d
