@@ -369,7 +369,7 @@ def run_ours(args, rank, world):
     clocks.start()
     time.sleep(0.3)
     soak, t_soak = 0, time.perf_counter()
-    while time.perf_counter() - t_soak < CLOCK_SOAK_S:
+    while time.perf_counter() - t_soak < args.clock_soak:
         for _ in range(8):
             if pcfg:
                 prefill_call()
@@ -428,6 +428,8 @@ def run_ours(args, rank, world):
                            "bound": "tensor",
                            "achieved": achieved, "peak": tc_peak, "unit": "TFLOP/s",
                            "frac": achieved / tc_peak,
+                           "frac_of_sustained": achieved / float(
+                               peaks.get("bf16_tflops_sustained", FALLBACK["bf16_tflops_sustained"])),
                            "peak_source": f"{peak_kind} bf16 burst (MEASURED_PEAKS.json)"
                            if peak_kind == "measured" else "fallback 1.9 PFLOP/s",
                            "traffic": ncu_traffic("prefill_f32" if f32 else "prefill",
@@ -737,7 +739,7 @@ CHUNKED = dict(B=8, H=32, d=128, page=256, pool=600, chunk=512, max_ctx0=7680, d
 MULTIMODAL = dict(B=4, H=32, d=128, V=576, T=2048, dtype="bf16")
 
 
-def timed(calls, K, W, stream):
+def timed(calls, K, W, stream, soak_s=CLOCK_SOAK_S):
     """Run each zero-argument call per step; CUDA-event milliseconds of each, summed, and
     the SM clocks sampled during the timed steps."""
     for _ in range(W):
@@ -749,7 +751,7 @@ def timed(calls, K, W, stream):
     clocks.start()
     time.sleep(0.3)
     soak, t_soak = 0, time.perf_counter()
-    while time.perf_counter() - t_soak < CLOCK_SOAK_S:
+    while time.perf_counter() - t_soak < soak_s:
         for c in calls:
             c()
         soak += 1
@@ -808,7 +810,8 @@ def run_next_rows(args, fa, workload, peaks, peak_kind, stream, world):
         # every step appends the same chunk at the same place, then runs its prefill
         ms, clk = timed([lambda: fa.fa_kv_append(kn, vn, kp, vp, tab, c0, stream=stream),
                          lambda: fa.fa_fwd_paged(q, kp, vp, tab, ctx, o, lse, scale,
-                                                 fa.FA_MASK_CAUSAL, stream=stream)], K, W, stream)
+                                                 fa.FA_MASK_CAUSAL, stream=stream)], K, W, stream,
+                        args.clock_soak)
         assert fa.fa_get_device_status() == fa.FA_OK
         pairs = sum(visible_pairs(T, t, 1) for t in total)
         flops = 4.0 * H * d * pairs
@@ -847,9 +850,9 @@ def run_next_rows(args, fa, workload, peaks, peak_kind, stream, world):
                  lambda: fa.fa_fwd(qt, kt, vt, ott, ltt, scale, fa.FA_MASK_CAUSAL, stream=stream),
                  lambda: fa.fa_fwd(qt, kv_, vv, otv, ltv, scale, fa.FA_MASK_NONE, stream=stream),
                  lambda: fa.fa_merge_partials(ott, ltt, otv, ltv, ot, lt, stream=stream)]
-        ms, clk = timed(split, K, W, stream)
+        ms, clk = timed(split, K, W, stream, args.clock_soak)
         one, _ = timed([lambda: fa.fa_fwd(qt, k, v, o1, l1, scale, fa.FA_MASK_CAUSAL,
-                                          stream=stream)], K, W, stream)
+                                          stream=stream)], K, W, stream, 0.0)
         assert fa.fa_get_device_status() == fa.FA_OK
         pairs = V * V + T * (T + 1) // 2 + T * V
         flops = 4.0 * B * H * d * pairs
@@ -890,7 +893,7 @@ def run_backward(args, fa, peaks, stream, world):
                      device=dev)
     K, W = args.steps, args.warmup
     ms, clk = timed([lambda: fa.fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, ws, scale, cfg["mode"],
-                                       stream=stream)], K, W, stream)
+                                       stream=stream)], K, W, stream, args.clock_soak)
     ms = ms[0]
     assert fa.fa_get_device_status() == fa.FA_OK
     flops = 2.5 * prefill_flops(cfg)
@@ -999,11 +1002,11 @@ def run_reference(args, rank, world):
 
 # --------------------------------------------------------------------------- tile sweep
 def run_sweep(args, fa, prefill_call, pflops, peaks, peak_kind, pcfg):
-    """Tile-size sweep of the causal 4k prefill: query rows per work item (BLOCK_M 128 or
-    256; 64 is not built: an M = 64 tensor-core tile uses half the TMEM lanes) x key-block
+    """Tile-size sweep of the causal 4k prefill: query rows per work item (BLOCK_M 64, 128
+    or 256; 64 runs tcgen05 MMAs with M = 64, 256 two 128-row tiles per item) x key-block
     size (BLOCK_N 64 or 128)."""
     lines = []
-    for bm in (128, 256):
+    for bm in (64, 128, 256):
         for bn in (64, 128):
             for _ in range(3):
                 prefill_call(block_n=bn, block_m=bm)
@@ -1022,7 +1025,7 @@ def run_sweep(args, fa, prefill_call, pflops, peaks, peak_kind, pcfg):
             "unit": "TFLOP/s", "sweep": lines, "config": workload_config(pcfg, False, 1),
             "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
             "ms_per_step": min(l["ms"] for l in lines), "dtype": pcfg["dtype"],
-            "gpu_launches": 4 * (3 + max(5, args.steps // 4))}
+            "gpu_launches": 6 * (3 + max(5, args.steps // 4))}
 
 
 def main(argv=None):
@@ -1047,6 +1050,9 @@ def main(argv=None):
     ap.add_argument("--pages-per-split", type=int, default=0,
                     help="decode pages per split-K partial (0 = library default)")
     ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--clock-soak", type=float, default=CLOCK_SOAK_S,
+                    help="seconds of untimed steps run while the clocks are sampled, just "
+                         "before the timed ones (0 = none)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--clock-log", default=None,
                     help="file for the raw nvidia-smi clock samples (default: a temporary file)")

@@ -119,14 +119,15 @@ typedef struct fa_fwd_params {
   int mask_mode, window, n_global, dtype;
   int block_n;        /* key-block size: 0 = default (128), else 64 or 128 */
   int block_m;        /* query rows per work item: 0 = fa_fwd_default_block_m(mask_mode),
-                         else 128 or 256 (two 128-row tiles sharing every K/V tile) */
+                         else 64 (tensor-core tiles of 64 rows), 128, or 256 (two 128-row
+                         tiles sharing every K/V tile) */
   int num_ctas;       /* persistent grid size: 0 = one CTA per SM */
   int group_heads;    /* (batch, head) pairs scheduled together: 0 = sized for L2 */
   uint32_t timeout_us; /* per-wait time limit: 0 = 1 s */
-  /* Optional visit log, int32 [B*H, ceil(Sq/128), ceil(Sk/block_n)] (one row per
-   * 128-query tile whatever block_m is), zeroed by the caller. Every tile the kernel
-   * computes for those 128 queries adds 16 + class (1 partial, 2 full); tiles the mask
-   * skips stay 0. */
+  /* Optional visit log, int32 [B*H, ceil(Sq/T), ceil(Sk/block_n)] with T the rows of a
+   * tensor-core tile (128, or 64 when block_m is 64), zeroed by the caller. Every tile the
+   * kernel computes for those T queries adds 16 + class (1 partial, 2 full); tiles the
+   * mask skips stay 0. */
   int32_t* trace;
   /* FA_MASK_BLOCK_SPARSE: device pointer to the layout described above (owned by the
    * caller, read during the call); ignored for the other masks. */

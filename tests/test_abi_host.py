@@ -121,8 +121,10 @@ def test_fwd_empty_query_is_a_no_op(L):
 def test_fwd_ex_rejects_bad_plan(L):
     p = fa.FwdParams(A, A, A, A, None, 1, 1, 4, 4, 64, 0.125, 0, 0, 0, 0, 96, 0, 0, 0, 0, None)
     assert L.fa_fwd_ex(ctypes.byref(p), None) == fa.FA_ERR_UNSUPPORTED
-    p = fa.FwdParams(A, A, A, A, None, 1, 1, 4, 4, 64, 0.125, 0, 0, 0, 0, 0, 64, 0, 0, 0, None)
-    assert L.fa_fwd_ex(ctypes.byref(p), None) == fa.FA_ERR_UNSUPPORTED
+    for bm in (32, 96, 512):  # block_m: 64, 128 or 256
+        p = fa.FwdParams(A, A, A, A, None, 1, 1, 4, 4, 64, 0.125, 0, 0, 0, 0, 0, bm, 0, 0, 0,
+                         None)
+        assert L.fa_fwd_ex(ctypes.byref(p), None) == fa.FA_ERR_UNSUPPORTED
     assert L.fa_fwd_ex(None, None) == fa.FA_ERR_INVALID_ARG
 
 

@@ -58,7 +58,7 @@ SHAPES = [(1, 1), (63, 63), (65, 65), (127, 129), (129, 127), (200, 333), (257, 
 @pytest.mark.parametrize("d,dt", [(64, "f16"), (128, "bf16"), (128, "f16")])
 @pytest.mark.parametrize("mask", ["none", "causal", "window", "band", "prefix"])
 @pytest.mark.parametrize("bn", [64, 128])
-@pytest.mark.parametrize("bm", [128, 256])
+@pytest.mark.parametrize("bm", [64, 128, 256])
 def test_small_shapes(Sq, Sk, d, dt, mask, bn, bm):
     q, k, v = inputs.prefill_inputs(2, 3, Sq, Sk, d, DT[dt], seed=Sq * 1000 + Sk)
     mode, w, g = MASKS[mask]
@@ -72,14 +72,15 @@ def test_small_shapes(Sq, Sk, d, dt, mask, bn, bm):
                                       ("window", 129, 300), ("none", 0, 0), ("band", 0, 0),
                                       ("band", 150, 0), ("prefix", 0, 0), ("prefix", 0, 300)])
 @pytest.mark.parametrize("Sq,Sk,bn", [(1000, 1000, 128), (700, 1100, 64), (1100, 700, 128)])
-@pytest.mark.parametrize("bm", [128, 256])
+@pytest.mark.parametrize("bm", [64, 128, 256])
 def test_tile_trace_is_bit_exact(mask, w, g, Sq, Sk, bn, bm):
     """The tiles the kernel visits, and the class it gives each, equal the oracle's
-    brute-force tile classification; no tile is visited twice."""
+    brute-force tile classification; no tile is visited twice. The trace has one row per
+    tensor-core tile of queries: 128 rows, 64 for 64-row items."""
     mode = MODES[mask]
     B, H, d = 1, 2, 64
     q, k, v = inputs.prefill_inputs(B, H, Sq, Sk, d, torch.float16, seed=3)
-    BM = fa.fa_fwd_block_m()
+    BM = 64 if bm == 64 else fa.fa_fwd_block_m()
     nmb, nnb = -(-Sq // BM), -(-Sk // bn)
     trace = torch.zeros(B * H * nmb * nnb, dtype=torch.int32, device="cuda")
     o, lse = run_fwd(q, k, v, 0.125, mode, w, g, block_n=bn, block_m=bm, trace=trace)
@@ -145,7 +146,7 @@ def test_schedule_does_not_change_results():
     """Every work item is computed the same way whatever CTA runs it: outputs are
     bit-identical for any persistent grid size and head grouping."""
     q, k, v = inputs.prefill_inputs(2, 5, 700, 700, 128, torch.bfloat16, seed=9)
-    for bm in (128, 256):
+    for bm in (64, 128, 256):
         o0, l0 = run_fwd(q, k, v, 0.088, fa.FA_MASK_CAUSAL, block_m=bm)
         for ctas, hg in [(1, 1), (7, 3), (37, 0), (1000, 10)]:
             o1, l1 = run_fwd(q, k, v, 0.088, fa.FA_MASK_CAUSAL, num_ctas=ctas, group_heads=hg,
@@ -213,7 +214,7 @@ def run_sparse(q, k, v, scale, lay, **ex):
 @pytest.mark.parametrize("Sq,Sk", [(1, 1), (127, 129), (200, 333), (384, 384), (520, 257)])
 @pytest.mark.parametrize("d,dt", [(64, "f16"), (128, "bf16")])
 @pytest.mark.parametrize("bn", [64, 128])
-@pytest.mark.parametrize("bm", [128, 256])
+@pytest.mark.parametrize("bm", [64, 128, 256])
 def test_block_sparse_small(Sq, Sk, d, dt, bn, bm):
     q, k, v = inputs.prefill_inputs(2, 3, Sq, Sk, d, DT[dt], seed=Sq + 7 * Sk)
     lay = _layout(3, Sq, Sk, seed=Sq * Sk)
@@ -224,14 +225,14 @@ def test_block_sparse_small(Sq, Sk, d, dt, bn, bm):
 
 
 @pytest.mark.parametrize("bn", [64, 128])
-@pytest.mark.parametrize("bm", [128, 256])
+@pytest.mark.parametrize("bm", [64, 128, 256])
 def test_block_sparse_trace_is_bit_exact(bn, bm):
     """Tiles the kernel visits, with their classes, equal the oracle's brute-force
     classification under the layout; a 256-row item visits only its tiles' blocks."""
     B, H, Sq, Sk, d = 1, 2, 900, 1100, 64
     q, k, v = inputs.prefill_inputs(B, H, Sq, Sk, d, torch.float16, seed=5)
     lay = _layout(H, Sq, Sk, seed=11, density=0.35)
-    BM = fa.fa_fwd_block_m()
+    BM = 64 if bm == 64 else fa.fa_fwd_block_m()
     nmb, nnb = -(-Sq // BM), -(-Sk // bn)
     trace = torch.zeros(B * H * nmb * nnb, dtype=torch.int32, device="cuda")
     o, lse = run_sparse(q, k, v, 0.125, lay, block_n=bn, block_m=bm, trace=trace)

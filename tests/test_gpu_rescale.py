@@ -98,7 +98,7 @@ SHAPES = [(384, 384), (257, 700)]
 @pytest.mark.parametrize("d,dt", [(64, "f16"), (64, "bf16"), (128, "f16"), (128, "bf16")])
 @pytest.mark.parametrize("mask", list(MASKS))
 @pytest.mark.parametrize("bn", [64, 128])
-@pytest.mark.parametrize("bm", [128, 256])
+@pytest.mark.parametrize("bm", [64, 128, 256])
 @pytest.mark.parametrize("kind", ["up", "wide"])
 def test_rescale_small(Sq, Sk, d, dt, mask, bn, bm, kind):
     scale = 1 / math.sqrt(d)
@@ -115,7 +115,7 @@ def test_rescale_small(Sq, Sk, d, dt, mask, bn, bm, kind):
 
 
 @pytest.mark.parametrize("bn", [64, 128])
-@pytest.mark.parametrize("bm", [128, 256])
+@pytest.mark.parametrize("bm", [64, 128, 256])
 @pytest.mark.parametrize("mask", ["none", "causal", "window"])
 def test_falling_scores_never_rescale(bn, bm, mask):
     """Control: when the first visited key tile holds every row's maximum, nothing is
@@ -132,7 +132,7 @@ def test_falling_scores_never_rescale(bn, bm, mask):
 
 
 @pytest.mark.parametrize("bn", [64, 128])
-@pytest.mark.parametrize("bm", [128, 256])
+@pytest.mark.parametrize("bm", [64, 128, 256])
 @pytest.mark.parametrize("kind", ["up", "wide"])
 def test_rescale_block_sparse(bn, bm, kind):
     d, Sq, Sk = 128, 520, 640
@@ -196,7 +196,7 @@ def test_rescale_f32_inputs():
         check_counts(cnt, q, k, scale, 64, mode, 0, 0, f"f32 mode {mode}")
 
 
-@pytest.mark.parametrize("bm", [128, 256])
+@pytest.mark.parametrize("bm", [64, 128, 256])
 @pytest.mark.parametrize("mode", [fa.FA_MASK_CAUSAL, fa.FA_MASK_NONE])
 def test_rescale_4k_sampled(bm, mode):
     """4k keys (32 key tiles per row, every one a rescale for most rows, while the previous

@@ -195,8 +195,8 @@ fa_status check_fwd(const fa_fwd_params& p, bool allow_f32 = false) {
     return fail(FA_ERR_INVALID_ARG, "problem too large for 32-bit tile indices");
   if (p.block_n != 0 && p.block_n != 64 && p.block_n != 128)
     return fail(FA_ERR_UNSUPPORTED, "block_n %d (supported: 64, 128)", p.block_n);
-  if (p.block_m != 0 && p.block_m != 128 && p.block_m != 256)
-    return fail(FA_ERR_UNSUPPORTED, "block_m %d (supported: 128, 256)", p.block_m);
+  if (p.block_m != 0 && p.block_m != 64 && p.block_m != 128 && p.block_m != 256)
+    return fail(FA_ERR_UNSUPPORTED, "block_m %d (supported: 64, 128, 256)", p.block_m);
   if (p.num_ctas < 0 || p.group_heads < 0) return fail(FA_ERR_INVALID_ARG, "negative plan parameter");
   if (p.dtype == FA_F32) {
     if (BH > (1LL << 29))  // the tensor maps see 2 * B * H planes
@@ -330,8 +330,9 @@ fa_status run_fwd(const fa_fwd_params& a, const PagedKV* pg, fa_stream_t stream)
     return FA_OK;
   }
   const bool bf16 = a.dtype == FA_BF16;
-  if ((st = make_map(&L.tmQ, a.q, bf16, a.d, a.Sq, BH, fa::prefill_tile_rows())) != FA_OK)
-    return st;
+  // one Q box is one tensor-core tile: 64 rows for 64-row items, else 128
+  const int q_rows = BM == 64 ? 64 : fa::prefill_tile_rows();
+  if ((st = make_map(&L.tmQ, a.q, bf16, a.d, a.Sq, BH, q_rows)) != FA_OK) return st;
   if (pg) {
     // pools [num_pages, H, page, d] seen as (d, page, num_pages*H); a tile is BN rows of
     // one (page, head)

@@ -325,7 +325,7 @@ __device__ __forceinline__ void bwd_teardown(uint32_t tmem) {
 // columns), dP^T [128,256) (dS^T packed over [128,192)), dV [256,256+D), dK [256+D,256+2D).
 // Shared memory: K, V (resident), then (Q, dO) halves of 64 queries in four stages.
 template <int D, bool BF16>
-__global__ void __launch_bounds__(kBwdThreads, 1)
+__global__ void __maxnreg__(200)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ,
                     const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV,
@@ -464,38 +464,35 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tc_fence_after();
         const int m0 = qb * kBT + 64 * u;
         const RowSpan vis = query_cols(j, m0, p.Sk, p);
-#pragma unroll 1
-        for (int c = 0; c < 2; ++c) {  // 32 queries at a time
-          uint32_t sv[32], dp[32];
-          tmem_ld32(t_lane + 64 * u + c * 32, sv);
-          tmem_ld32(t_lane + 128 + 64 * u + c * 32, dp);
-          float l2[32], dd[32];
+        // all 64 columns of S^T_u and dP^T_u in one round trip to TMEM
+        uint32_t sv[64], dp[64];
+        tmem_ld32(t_lane + 64 * u, sv);
+        tmem_ld32(t_lane + 64 * u + 32, sv + 32);
+        tmem_ld32(t_lane + 128 + 64 * u, dp);
+        tmem_ld32(t_lane + 128 + 64 * u + 32, dp + 32);
+        tmem_ld_wait<64>(sv);
+        tmem_ld_tie<64>(dp);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {  // per-query statistics (the same for every lane)
-            const float4 a = st4[(c * 32) / 4 + e];
-            const float4 d = st4[(kHalf + c * 32) / 4 + e];
-            l2[4 * e] = a.x, l2[4 * e + 1] = a.y, l2[4 * e + 2] = a.z, l2[4 * e + 3] = a.w;
-            dd[4 * e] = d.x, dd[4 * e + 1] = d.y, dd[4 * e + 2] = d.z, dd[4 * e + 3] = d.w;
+        for (int e = 0; e < 64; e += 4) {  // 4 queries at a time; statistics from shared memory
+          const float4 a = st4[e / 4];
+          const float4 d = st4[(kHalf + e) / 4];
+          const float l2[4] = {a.x, a.y, a.z, a.w}, dd[4] = {d.x, d.y, d.z, d.w};
+          float pv[4], dv[4];
+#pragma unroll
+          for (int w = 0; w < 4; ++w) {
+            const int col = e + w;
+            const bool on = col >= vis.lo && col <= vis.hi;
+            pv[w] = on ? ex2_approx(__uint_as_float(sv[e + w]) * p.sl2 - l2[w]) : 0.f;
+            dv[w] = pv[w] * (__uint_as_float(dp[e + w]) - dd[w]);
           }
-          tmem_ld_wait<32>(sv);
-          tmem_ld_wait<32>(dp);
-          uint32_t pp[16], ds[16];
-#pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            float pv[2], dv[2];
-#pragma unroll
-            for (int w = 0; w < 2; ++w) {
-              const int col = c * 32 + e + w;
-              const bool on = col >= vis.lo && col <= vis.hi;
-              pv[w] = on ? ex2_approx(__uint_as_float(sv[e + w]) * p.sl2 - l2[e + w]) : 0.f;
-              dv[w] = pv[w] * (__uint_as_float(dp[e + w]) - dd[e + w]);
-            }
-            pp[e / 2] = BF16 ? cvt_pack_bf16(pv[0], pv[1]) : cvt_pack_f16(pv[0], pv[1]);
-            ds[e / 2] = BF16 ? cvt_pack_bf16(dv[0], dv[1]) : cvt_pack_f16(dv[0], dv[1]);
-          }
-          tmem_st16(t_lane + 64 * u + c * 16, pp);        // P^T_u over columns already read
-          tmem_st16(t_lane + 128 + 64 * u + c * 16, ds);  // dS^T_u likewise
+          // packed over the columns already read (P^T_u and dS^T_u: 32 columns each)
+          sv[e / 2] = BF16 ? cvt_pack_bf16(pv[0], pv[1]) : cvt_pack_f16(pv[0], pv[1]);
+          sv[e / 2 + 1] = BF16 ? cvt_pack_bf16(pv[2], pv[3]) : cvt_pack_f16(pv[2], pv[3]);
+          dp[e / 2] = BF16 ? cvt_pack_bf16(dv[0], dv[1]) : cvt_pack_f16(dv[0], dv[1]);
+          dp[e / 2 + 1] = BF16 ? cvt_pack_bf16(dv[2], dv[3]) : cvt_pack_f16(dv[2], dv[3]);
         }
+        tmem_st32(t_lane + 64 * u, sv);        // P^T_u over columns already read
+        tmem_st32(t_lane + 128 + 64 * u, dp);  // dS^T_u likewise
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(B(bars->p_full[u]));
@@ -643,28 +640,27 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (!ok) break;
         tc_fence_after();
         const ColMask cm = key_cols(i, nb * kBT + 64 * u, p.Sk, p);
-#pragma unroll 1
-        for (int c = 0; c < 2; ++c) {  // 32 keys at a time
-          uint32_t sv[32], dp[32];
-          tmem_ld32(t_lane + 64 * u + c * 32, sv);
-          tmem_ld32(t_lane + 128 + 64 * u + c * 32, dp);
-          tmem_ld_wait<32>(sv);
-          tmem_ld_wait<32>(dp);
-          uint32_t ds[16];
+        // all 64 columns of S_u and dP_u in one round trip to TMEM
+        uint32_t sv[64], dp[64];
+        tmem_ld32(t_lane + 64 * u, sv);
+        tmem_ld32(t_lane + 64 * u + 32, sv + 32);
+        tmem_ld32(t_lane + 128 + 64 * u, dp);
+        tmem_ld32(t_lane + 128 + 64 * u + 32, dp + 32);
+        tmem_ld_wait<64>(sv);
+        tmem_ld_tie<64>(dp);
 #pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            float dv[2];
+        for (int e = 0; e < 64; e += 2) {
+          float dv[2];
 #pragma unroll
-            for (int w = 0; w < 2; ++w) {
-              const int col = c * 32 + e + w;
-              const bool on = col <= cm.lim && (col >= cm.lo || col < cm.gl);
-              const float pv = on ? ex2_approx(__uint_as_float(sv[e + w]) * p.sl2 - l2) : 0.f;
-              dv[w] = pv * (__uint_as_float(dp[e + w]) - dd);
-            }
-            ds[e / 2] = BF16 ? cvt_pack_bf16(dv[0], dv[1]) : cvt_pack_f16(dv[0], dv[1]);
+          for (int w = 0; w < 2; ++w) {
+            const int col = e + w;
+            const bool on = col <= cm.lim && (col >= cm.lo || col < cm.gl);
+            const float pv = on ? ex2_approx(__uint_as_float(sv[e + w]) * p.sl2 - l2) : 0.f;
+            dv[w] = pv * (__uint_as_float(dp[e + w]) - dd);
           }
-          tmem_st16(t_lane + 128 + 64 * u + c * 16, ds);  // dS_u over columns already read
+          dp[e / 2] = BF16 ? cvt_pack_bf16(dv[0], dv[1]) : cvt_pack_f16(dv[0], dv[1]);
         }
+        tmem_st32(t_lane + 128 + 64 * u, dp);  // dS_u over columns already read
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(B(bars->p_full[u]));

@@ -54,3 +54,38 @@ __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint3
 }
 
 }  // namespace fa
+
+namespace fa {
+
+// The same two products for a 64-row query tile (tcgen05 M = 64, BLOCK_M = 64 work items).
+// S = Q K^T: Q a 64-row tile (regions of 64 elements of d, 8 KB apart), K as in issue_qk.
+template <int D, int BN, bool BF16>
+__device__ __forceinline__ void issue_qk_m64(uint32_t d_tmem, uint32_t q_smem, uint32_t k_smem) {
+  constexpr uint32_t id = idesc_f16(BF16, 64, BN, false);
+  const uint64_t a0 = smem_desc_sw128(q_smem, 16, 1024);
+  const uint64_t b0 = smem_desc_sw128(k_smem, 16, 1024);
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint64_t a_off = static_cast<uint64_t>((kk / 4) * (64 * 128 / 16) + (kk % 4) * 2);
+    const uint64_t b_off = static_cast<uint64_t>((kk / 4) * (BN * 128 / 16) + (kk % 4) * 2);
+    umma_ss(d_tmem, a0 + a_off, b0 + b_off, id, kk > 0 ? 1u : 0u);
+  }
+}
+
+// O (+)= P V for a 64-row tile with P in shared memory: P [64 x BN] 16-bit, K-major,
+// 128-byte swizzled (regions of 64 keys, 8 KB apart); V [BN x D] MN-major as in issue_pv.
+template <int D, int BN, bool BF16>
+__device__ __forceinline__ void issue_pv_m64(uint32_t o_tmem, uint32_t p_smem, uint32_t v_smem,
+                                             bool accumulate) {
+  constexpr uint32_t id = idesc_f16(BF16, 64, D, true);
+  const uint64_t a0 = smem_desc_sw128(p_smem, 16, 1024);
+  const uint64_t b0 = smem_desc_sw128(v_smem, BN * 128, 1024);
+#pragma unroll
+  for (int kk = 0; kk < BN / 16; ++kk) {
+    const uint64_t a_off = static_cast<uint64_t>((kk / 4) * (64 * 128 / 16) + (kk % 4) * 2);
+    umma_ss(o_tmem, a0 + a_off, b0 + static_cast<uint64_t>(kk * 128), id,
+            (accumulate || kk > 0) ? 1u : 0u);
+  }
+}
+
+}  // namespace fa

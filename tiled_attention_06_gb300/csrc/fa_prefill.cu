@@ -38,6 +38,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <atomic>
 #include <climits>
 #include <cstdint>
 #include <type_traits>
@@ -72,15 +73,15 @@ __device__ __forceinline__ bool layout_bit(int bh, int m0, int nb, const Prefill
 
 // True when every (row, key) pair of the 128-row tile at m0 and key block nb is in range
 // and visible.
-template <int BN, bool SPARSE>
+template <int BN, bool SPARSE, int TM = kTile>
 __device__ __forceinline__ bool tile_full(int m0, int nb, int sk, int bh,
                                           const PrefillParams& p) {
   const int n0 = nb * BN, n1 = n0 + BN;
-  if (m0 + kTile > p.Sq || n1 > sk) return false;
+  if (m0 + TM > p.Sq || n1 > sk) return false;
   if constexpr (SPARSE) return layout_bit<BN>(bh, m0, nb, p);
   if (p.mask_mode == FA_MASK_NONE) return true;
   const int delta = sk - p.Sq;
-  const int r_lo = m0 + delta, r_hi = m0 + kTile - 1 + delta;
+  const int r_lo = m0 + delta, r_hi = m0 + TM - 1 + delta;
   if (p.mask_mode == FA_MASK_BAND)  // the largest |pos - j| of the tile is within w
     return static_cast<long long>(r_hi) - n0 <= p.window &&
            static_cast<long long>(n1 - 1) - r_lo <= p.window;
@@ -120,15 +121,18 @@ __device__ __forceinline__ uint32_t pack2(float a, float b, bool bf16) {
 // SPLIT (FP32 inputs): P is written as two bf16 parts, P_hi = bf16(P) at p_col and
 // P_lo = bf16(P - P_hi) at p_col + NC/2, so that P_hi + P_lo holds P to 2^-16.
 // l accumulates the sum over this thread's NC columns. With p.rescales set, the rows
-// rescaled are counted for the 128-row tile (rs_bh, rs_m0) when rs_bh >= 0. Returns
-// false on abort.
-template <int NC, int ON, bool BF16, bool SPLIT, typename Exchange,
+// rescaled are counted for the 128-row tile (rs_bh, rs_m0) when rs_bh >= 0. P_SMEM (the
+// 64-row kernel): P goes instead to row p_row of a 64-row, 128-byte-swizzled K-major tile
+// at shared address p_col (regions of 64 keys 8 KB apart), when p_row >= 0, followed by a
+// proxy fence so that the tensor core sees it. Returns false on abort.
+template <int NC, int ON, bool BF16, bool SPLIT, bool P_SMEM = false, typename Exchange,
           typename PreRescale>
 __device__ __forceinline__ bool softmax_cols(uint32_t t_lane, uint32_t s_col, uint32_t p_col,
                                              uint32_t o_col, bool full, int n0, int pos_q,
                                              int sk, const PrefillParams& p, float& m_ref,
                                              float& l, Exchange exchange,
-                                             PreRescale before_rescale, int rs_bh, int rs_m0) {
+                                             PreRescale before_rescale, int rs_bh, int rs_m0,
+                                             int p_row = -1) {
   static_assert(NC == 32 || NC % 64 == 0, "column count");
   static_assert(!SPLIT || (BF16 && NC % 64 == 0), "split P: bf16, 64-column groups");
   uint32_t s[NC];
@@ -176,9 +180,9 @@ __device__ __forceinline__ bool softmax_cols(uint32_t t_lane, uint32_t s_col, ui
   const bool need = (m_ref != -INFINITY) && (m_new > m_ref + kTau);
   if (m_ref == -INFINITY) m_ref = m_new;
   if (__any_sync(0xffffffffu, need)) {
-    if (p.rescales && rs_bh >= 0) {  // debug count: one atomic per warp
-      const uint32_t who = __ballot_sync(0xffffffffu, need);
-      if ((threadIdx.x & 31) == 0)
+    if (p.rescales) {  // debug count: one atomic per warp (the ballot is warp-wide)
+      const uint32_t who = __ballot_sync(0xffffffffu, need && rs_bh >= 0);
+      if ((threadIdx.x & 31) == 0 && who != 0u && rs_bh >= 0)
         atomicAdd(p.rescales + static_cast<size_t>(rs_bh) * ((p.Sq + kTile - 1) / kTile) +
                       rs_m0 / kTile,
                   __popc(who));
@@ -221,6 +225,18 @@ __device__ __forceinline__ bool softmax_cols(uint32_t t_lane, uint32_t s_col, ui
   float a0, a1;
   f2_split(f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3])), a0, a1);
   l += a0 + a1;
+  if constexpr (P_SMEM) {
+    if (p_row >= 0) {
+#pragma unroll
+      for (int k = 0; k < NC / 8; ++k)  // 16-byte chunk k holds keys 8k .. 8k+7
+        st_shared_v4(p_col + (k / 8) * (64 * 128) + p_row * 128 +
+                         ((static_cast<uint32_t>(k % 8) ^ (p_row & 7)) << 4),
+                     s[4 * k], s[4 * k + 1], s[4 * k + 2], s[4 * k + 3]);
+    }
+    fence_proxy_async_smem();
+    tmem_st_wait();  // a rescale of O above must land before the next P.V reads it
+    return true;
+  }
   if constexpr (NC == 32) {
     tmem_st16(t_lane + p_col, s);
   } else {
@@ -1077,32 +1093,370 @@ __global__ void __launch_bounds__(kThreads128, 1)
   }
 }
 
+// ------------------------------------------------------------------ BM = 64 kernel
+//
+// One 64-row query tile per work item, on tcgen05 MMAs with M = 64: the BLOCK_M = 64 point
+// of the tile-size tuning the ops-transformer overview describes (section 三.1, 64x64,
+// 128x128 and 256x256 blocks). Roles (192 threads):
+//   warps 0-3   softmax and epilogue. The accumulator of an M = 64 MMA occupies TMEM
+//               lanes 0-15 of each warp's 32-lane quarter (row 16w + l in lane 32w + l),
+//               so lanes 0-15 of each warp own a row; lanes 16-31 take part in the
+//               warp-wide TMEM loads and stores but own nothing.
+//   warp 4      TMA producer: Q (double buffered), then K of the next tile and V of the
+//               current one, as in the 128-row kernel.
+//   warp 5      MMA issuer (elected lane): S(g+1) = Q K^T, then O += P(g) V(g).
+// P is written to shared memory (two 64 x BN buffers) rather than TMEM and the P.V MMA
+// reads both operands from shared memory.
+// TMEM: S0 [0,BN), S1 [BN,2BN), O0 [2BN,2BN+D), O1 [2BN+D,2BN+2D) (items alternate).
+constexpr int kTile64 = 64;
+constexpr int kThreads64 = 192;
+constexpr int kTmaWarp64 = 4;
+constexpr int kMmaWarp64 = 5;
+
+template <int D, int BN>
+struct Cfg64 {
+  static constexpr int KCH = D / 64;
+  static constexpr int Q_BYTES = kTile64 * D * 2;   // one Q buffer
+  static constexpr int P_BYTES = kTile64 * BN * 2;  // one P buffer
+  static constexpr int TILE_BYTES = BN * D * 2;
+  static constexpr int BAR_BYTES = 1024;
+  static constexpr int NSLOT_FIT =
+      (int)((kSmemLimit - 1024 - BAR_BYTES - 2 * Q_BYTES - 2 * P_BYTES) / TILE_BYTES);
+  static constexpr int NSLOT = NSLOT_FIT > 8 ? 8 : NSLOT_FIT;
+  static constexpr int SMEM = 1024 + 2 * Q_BYTES + 2 * P_BYTES + NSLOT * TILE_BYTES + BAR_BYTES;
+  static constexpr int TMEM_COLS = pow2_at_least(2 * BN + 2 * D);
+  static_assert(NSLOT >= 3, "shared memory ring too small");
+  static_assert(SMEM <= (int)kSmemLimit, "shared memory over budget");
+  static_assert(2 * BN + 2 * D <= 512, "TMEM over budget");
+};
+
+struct Bars64 {
+  uint64_t full[8], empty[8];
+  uint64_t q_full[2], q_empty[2];
+  uint64_t s_full[2], p_full[2], pv_done[2], o_empty[2];
+  uint64_t final_mma;
+  uint32_t tmem_base;
+  uint32_t abort;
+};
+
+template <int D, int BN, bool BF16, bool SPARSE>
+__global__ void __launch_bounds__(kThreads64, 1)
+    prefill_bm64_kernel(const __grid_constant__ CUtensorMap tmQ,
+                        const __grid_constant__ CUtensorMap tmK,
+                        const __grid_constant__ CUtensorMap tmV, const PrefillParams p,
+                        const __grid_constant__ PrefillSched sched) {
+  using C = Cfg64<D, BN>;
+  constexpr int BM = kTile64;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (base - raw);
+  const uint32_t sQ = base;                          // two Q buffers
+  const uint32_t sP = base + 2 * C::Q_BYTES;         // two P buffers
+  const uint32_t sRing = sP + 2 * C::P_BYTES;
+  Bars64* bars = reinterpret_cast<Bars64*>(smem + 2 * C::Q_BYTES + 2 * C::P_BYTES +
+                                           C::NSLOT * C::TILE_BYTES);
+  auto B = [&](uint64_t& b) { return smem_u32(&b); };
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::NSLOT; ++i) {
+      mbar_init(B(bars->full[i]), 1);
+      mbar_init(B(bars->empty[i]), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(B(bars->q_full[i]), 1);
+      mbar_init(B(bars->q_empty[i]), 1);
+      mbar_init(B(bars->s_full[i]), 1);
+      mbar_init(B(bars->p_full[i]), 128);
+      mbar_init(B(bars->pv_done[i]), 1);
+      mbar_init(B(bars->o_empty[i]), 128);
+    }
+    mbar_init(B(bars->final_mma), 1);
+    bars->abort = 0;
+    mbar_fence_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_u32(&bars->tmem_base), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  if (warp == kTmaWarp64 && lane == 0) {
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+  const WaitCtx wc{&bars->abort, p.status, p.timeout_ns};
+  const int G = gridDim.x;
+  const int cta = blockIdx.x;
+
+  if (warp == kTmaWarp64) {
+    // ------------------------------------------------------------ TMA producer
+    const bool leader = elect_one();
+    uint32_t pos = 0, ii = 0;
+    uint32_t fills[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    uint32_t qfills[2] = {0, 0};
+    bool ok = true;
+    int kc = 0;
+    ItemRef<SPARSE> cur, nxt;
+    auto load_q = [&](const ItemRef<SPARSE>& it, uint32_t idx) {
+      const int qb = idx & 1;
+      if (idx >= 2 && !(ok = mbar_wait(B(bars->q_empty[qb]), ((idx >> 1) - 1) & 1, wc))) return;
+      if (leader) {
+        mbar_arrive_expect_tx(B(bars->q_full[qb]), C::Q_BYTES);
+        for (int c = 0; c < C::KCH; ++c)
+          tma_load_3d(sQ + qb * C::Q_BYTES + c * (BM * 128), &tmQ, B(bars->q_full[qb]), c * 64,
+                      it.mb * BM, it.bh);
+      }
+      qfills[qb] = (idx >> 1) + 1;
+    };
+    auto emit = [&](const ItemRef<SPARSE>& it, int nb, bool is_v) {
+      const int slot = pos % C::NSLOT;
+      if (!(ok = mbar_wait(B(bars->empty[slot]), ((pos / C::NSLOT) & 1) ^ 1, wc))) return;
+      const uint32_t dst = sRing + slot * C::TILE_BYTES;
+      if (leader) mbar_arrive_expect_tx(B(bars->full[slot]), C::TILE_BYTES);
+      int y, z;
+      kv_tile_coords(p, it.bh, nb * BN, leader, y, z);
+      const void* map = is_v ? (const void*)&tmV : (const void*)&tmK;
+      if (leader)
+        for (int c = 0; c < C::KCH; ++c)
+          tma_load_3d(dst + c * (BN * 128), map, B(bars->full[slot]), c * 64, y, z);
+      fills[slot] = pos / C::NSLOT + 1;
+      ++pos;
+    };
+    // loads in the MMA's consumption order: Q and K(0) of the first item, then per tile K
+    // of the following tile (the next item's Q first when it starts one), V
+    bool has = next_item<BM, SPARSE>(sched, p, cta, G, BN, kc, cur, false);
+    int nb_cur = -1;
+    if (has) {
+      load_q(cur, 0);
+      nb_cur = range_next(cur.rg, -1);
+      if (ok) emit(cur, nb_cur, false);
+    }
+    while (has && ok) {
+      bool has_nxt = false;
+      for (int j = 0; j < cur.n && ok; ++j) {
+        int nb_next = -1;
+        if (j + 1 < cur.n) {
+          nb_next = range_next(cur.rg, nb_cur);
+          emit(cur, nb_next, false);
+        } else {
+          has_nxt = next_item<BM, SPARSE>(sched, p, cta, G, BN, kc, nxt, false);
+          if (has_nxt) {
+            load_q(nxt, ii + 1);
+            nb_next = range_next(nxt.rg, -1);
+            if (ok) emit(nxt, nb_next, false);
+          }
+        }
+        if (ok) emit(cur, nb_cur, true);
+        nb_cur = nb_next;
+      }
+      ++ii;
+      cur = nxt;
+      has = has_nxt;
+    }
+    if (!ok) {  // wind down: every load this thread issued lands before the CTA exits
+      for (int s = 0; s < C::NSLOT; ++s)
+        if (fills[s] > 0) wait_quiet(B(bars->full[s]), (fills[s] - 1) & 1, wc);
+      for (int q = 0; q < 2; ++q)
+        if (qfills[q] > 0) wait_quiet(B(bars->q_full[q]), (qfills[q] - 1) & 1, wc);
+    }
+    __syncwarp();
+  } else if (warp == kMmaWarp64) {
+    // ------------------------------------------------------------ MMA issuer
+    // Pipe order S(0) S(1) PV(0) S(2) PV(1) ...: S(g) is issued after PV(g-2), so the
+    // softmax's wait for S(g) also covers the P buffer and S columns that PV(g-2) read.
+    const bool leader = elect_one();
+    uint32_t pos = 0, ii = 0, g = 0;
+    bool ok = true;
+    int kc = 0;
+    ItemRef<SPARSE> cur, nxt;
+    auto issue_s = [&](uint32_t sbuf, uint32_t qb) {
+      const int slot = pos % C::NSLOT;
+      if (!(ok = mbar_wait(B(bars->full[slot]), (pos / C::NSLOT) & 1, wc))) return;
+      tc_fence_after();
+      if (leader) {
+        issue_qk_m64<D, BN, BF16>(tmem + sbuf * BN, sQ + qb * C::Q_BYTES,
+                                  sRing + slot * C::TILE_BYTES);
+        umma_commit(B(bars->s_full[sbuf]));
+        umma_commit(B(bars->empty[slot]));
+      }
+      ++pos;
+    };
+    bool has = next_item<BM, SPARSE>(sched, p, cta, G, BN, kc, cur, false);
+    if (has && (ok = mbar_wait(B(bars->q_full[0]), 0, wc))) {
+      tc_fence_after();
+      issue_s(0, 0);
+      if (ok && cur.n == 1 && leader) umma_commit(B(bars->q_empty[0]));
+    }
+    while (has && ok) {
+      const uint32_t buf = ii & 1;
+      bool has_nxt = false;
+      for (int j = 0; j < cur.n && ok; ++j, ++g) {
+        if (j + 1 < cur.n) {  // scores of the following tile, into the other S buffer
+          issue_s((g + 1) & 1, buf);
+          if (ok && j + 2 == cur.n && leader) umma_commit(B(bars->q_empty[buf]));
+        } else {
+          has_nxt = next_item<BM, SPARSE>(sched, p, cta, G, BN, kc, nxt, false);
+          if (has_nxt) {
+            const uint32_t nb = (ii + 1) & 1;
+            if (!(ok = mbar_wait(B(bars->q_full[nb]), ((ii + 1) >> 1) & 1, wc))) break;
+            tc_fence_after();
+            issue_s((g + 1) & 1, nb);
+            if (ok && nxt.n == 1 && leader) umma_commit(B(bars->q_empty[nb]));
+          }
+        }
+        if (!ok) break;
+        // O(item) += P(g) V(g)
+        if (!(ok = mbar_wait(B(bars->p_full[g & 1]), (g >> 1) & 1, wc))) break;
+        tc_fence_after();
+        if (j == 0 && ii >= 2) {  // the epilogue of two items back has read this O
+          if (!(ok = mbar_wait(B(bars->o_empty[buf]), ((ii >> 1) - 1) & 1, wc))) break;
+          tc_fence_after();
+        }
+        const int slot = pos % C::NSLOT;
+        if (!(ok = mbar_wait(B(bars->full[slot]), (pos / C::NSLOT) & 1, wc))) break;
+        tc_fence_after();
+        if (leader) {
+          issue_pv_m64<D, BN, BF16>(tmem + 2 * BN + buf * D, sP + (g & 1) * C::P_BYTES,
+                                    sRing + slot * C::TILE_BYTES, j > 0);
+          umma_commit(B(bars->pv_done[g & 1]));
+          umma_commit(B(bars->empty[slot]));
+        }
+        ++pos;
+      }
+      ++ii;
+      cur = nxt;
+      has = has_nxt;
+    }
+    if (leader) umma_commit(B(bars->final_mma));  // all MMAs done before TMEM is released
+    wait_quiet(B(bars->final_mma), 0, wc);
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax + epilogue
+    const bool mine = lane < 16;  // this lane owns a row of the tile
+    const int row = (warp % 4) * 16 + (lane & 15);
+    const uint32_t t_lane = tmem + (static_cast<uint32_t>((warp % 4) * 32) << 16);
+    uint32_t ii = 0, g = 0;
+    bool ok = true;
+    int kc = 0;
+    ItemRef<SPARSE> it;
+    while (ok && next_item<BM, SPARSE>(sched, p, cta, G, BN, kc, it, true)) {
+      const int m0 = it.mb * BM;
+      const int qrow = m0 + row;
+      const size_t orow = static_cast<size_t>(it.bh) * p.Sq + qrow;
+      if (it.n == 0) {  // no row of this item sees a key
+        if (mine && qrow < p.Sq) store_zero_row<D>(orow, p);
+        continue;
+      }
+      const uint32_t buf = ii & 1;
+      const int pos_q = qrow + it.sk - p.Sq;  // key position of this query
+      float m_ref = -INFINITY, l = 0.f;
+      int nb = -1;
+      for (int j = 0; j < it.n; ++j, ++g) {
+        nb = range_next(it.rg, nb);
+        const bool full = tile_full<BN, SPARSE, BM>(m0, nb, it.sk, it.bh, p);
+        ok = mbar_wait(B(bars->s_full[g & 1]), (g >> 1) & 1, wc);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after();
+        if (p.trace && warp == 0 && lane == 0)
+          atomicAdd(p.trace + (static_cast<size_t>(it.bh) * p.nmb + it.mb) * p.nnb + nb,
+                    16 + (full ? 2 : 1));
+        // O must hold every earlier P.V product of this item before it is rescaled
+        const uint32_t pc = g - 1;
+        auto wait_pv = [&]() {
+          bool w = mbar_wait(B(bars->pv_done[pc & 1]), (pc >> 1) & 1, wc);
+          w = __all_sync(0xffffffffu, w);
+          if (w) tc_fence_after();
+          return w;
+        };
+        // lanes that own no row see every key masked (a query at position -1 with no
+        // keys), so they never ask for a rescale and write no P
+        ok = softmax_cols<BN, D, BF16, false, true>(
+            t_lane, (g & 1) * BN, sP + (g & 1) * C::P_BYTES, 2 * BN + buf * D, full && mine,
+            nb * BN, mine ? pos_q : -1, mine ? it.sk : 0, p, m_ref, l,
+            [](float m) { return m; }, wait_pv, mine ? it.bh : -1, m0, mine ? row : -1);
+        if (!ok) break;
+        tc_fence_before();
+        mbar_arrive(B(bars->p_full[g & 1]));
+      }
+      if (!ok) break;
+      // epilogue: the item's last P.V, then O / l and LSE
+      const uint32_t pl = g - 1;
+      ok = mbar_wait(B(bars->pv_done[pl & 1]), (pl >> 1) & 1, wc);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      store_row<D, BF16>(t_lane, 2 * BN + buf * D, mine && qrow < p.Sq, orow, m_ref, l, p);
+      tc_fence_before();
+      mbar_arrive(B(bars->o_empty[buf]));
+      ++ii;
+    }
+    tc_fence_before();
+    __syncthreads();  // teardown
+    if (warp == 0) {
+      tc_fence_after();
+      tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+    return;
+  }
+  tc_fence_before();
+  __syncthreads();  // teardown
+}
+
+// Once per kernel and device (the attributes belong to the device's copy of the kernel):
+// check that the launch register count covers the kernel's setmaxnreg split (setmaxnreg.inc
+// can only hand out registers the CTA was launched with, so a build below the split would
+// make the softmax warps wait forever: it is refused instead of launched), and raise the
+// dynamic shared-memory limit.
+template <auto KERN>
+cudaError_t prepare_kernel(int threads, int split_regs_x128, int smem) {
+  static std::atomic<uint64_t> ready{0};  // this kernel: one bit per device index below 64
+  const auto kern = KERN;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = dev < 64 ? (uint64_t{1} << dev) : 0;
+  if (bit && (ready.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  cudaFuncAttributes fattr;
+  if ((e = cudaFuncGetAttributes(&fattr, kern)) != cudaSuccess) return e;
+  if (fattr.numRegs * threads < split_regs_x128 * 128) return cudaErrorInvalidConfiguration;
+  if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) !=
+      cudaSuccess)
+    return e;
+  ready.fetch_or(bit, std::memory_order_acq_rel);
+  return cudaSuccess;
+}
+
 template <int D, int BN, bool BF16, bool SPARSE, bool SPLIT = false>
 cudaError_t launch_k(const PrefillLaunch& L, int BM, cudaStream_t stream) {
+  if constexpr (!SPLIT) {
+    if (BM == 64) {
+      auto kern = prefill_bm64_kernel<D, BN, BF16, SPARSE>;
+      constexpr int smem = Cfg64<D, BN>::SMEM;
+      cudaError_t e = prepare_kernel<prefill_bm64_kernel<D, BN, BF16, SPARSE>>(kThreads64, 0, smem);
+      if (e != cudaSuccess) return e;
+      kern<<<L.grid, kThreads64, smem, stream>>>(L.tmQ, L.tmK, L.tmV, L.p, *L.sched);
+      return cudaGetLastError();
+    }
+  }
   if (SPLIT || BM == 256) {
     auto kern = prefill_bm256_kernel<D, BN, BF16, SPARSE, SPLIT>;
     constexpr int smem = Cfg256<D, BN, SPLIT>::SMEM;
-    // setmaxnreg.inc can only hand out registers the CTA was launched with; a build whose
-    // launch register count is below the split would make the softmax warps wait forever,
-    // so such a build is refused here instead of launched.
-    cudaFuncAttributes fattr;
-    cudaError_t e = cudaFuncGetAttributes(&fattr, kern);
-    if (e != cudaSuccess) return e;
-    if (fattr.numRegs * kThreads256 < 128 * static_cast<int>(2 * kRegsSoftmax + kRegsProducer))
-      return cudaErrorInvalidConfiguration;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e = prepare_kernel<prefill_bm256_kernel<D, BN, BF16, SPARSE, SPLIT>>(
+        kThreads256, 2 * kRegsSoftmax + kRegsProducer, smem);
     if (e != cudaSuccess) return e;
     kern<<<L.grid, kThreads256, smem, stream>>>(L.tmQ, L.tmK, L.tmV, L.p, *L.sched);
   } else if constexpr (!SPLIT) {
     auto kern = prefill_bm128_kernel<D, BN, BF16, SPARSE>;
     constexpr int smem = Cfg128<D, BN>::SMEM;
-    cudaFuncAttributes fattr;
-    cudaError_t e = cudaFuncGetAttributes(&fattr, kern);
-    if (e != cudaSuccess) return e;
-    if (fattr.numRegs * kThreads128 <
-        128 * static_cast<int>(kRegs128Softmax + kRegs128Epilogue + kRegs128Producer))
-      return cudaErrorInvalidConfiguration;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e = prepare_kernel<prefill_bm128_kernel<D, BN, BF16, SPARSE>>(
+        kThreads128, kRegs128Softmax + kRegs128Epilogue + kRegs128Producer, smem);
     if (e != cudaSuccess) return e;
     kern<<<L.grid, kThreads128, smem, stream>>>(L.tmQ, L.tmK, L.tmV, L.p, *L.sched);
   }
@@ -1159,7 +1513,7 @@ int prefill_tile_rows() { return kTile; }
 
 cudaError_t launch_prefill(const PrefillLaunch& L, int D, int BN, int BM, bool bf16,
                            cudaStream_t stream) {
-  if (BM != 128 && BM != 256) return cudaErrorInvalidValue;
+  if (BM != 64 && BM != 128 && BM != 256) return cudaErrorInvalidValue;
 #define FA_CASE(d_, bn_, bf_) \
   if (D == d_ && BN == bn_ && bf16 == bf_) return launch_t<d_, bn_, bf_>(L, BM, stream);
   FA_CASE(64, 64, false)
