@@ -325,7 +325,7 @@ __device__ __forceinline__ void bwd_teardown(uint32_t tmem) {
 // columns), dP^T [128,256) (dS^T packed over [128,192)), dV [256,256+D), dK [256+D,256+2D).
 // Shared memory: K, V (resident), then (Q, dO) halves of 64 queries in four stages.
 template <int D, bool BF16>
-__global__ void __maxnreg__(200)
+__global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ,
                     const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV,
