@@ -77,22 +77,22 @@ MODE_NAME = {0: "none", 1: "causal", 2: "causal_window", 3: "band", 4: "prefix_l
 # sources it was taken on; the figure is reported only for those workloads and only while
 # those sources are unchanged. Summaries: profiles/.
 NCU_TRAFFIC = {
-    # prefill_bm256_kernel, causal 4k B4 H16 capture: 209.9 MB read + 44.9 MB written,
+    # prefill_bm256_kernel, causal 4k B4 H16 capture: 210.0 MB read + 44.3 MB written,
     # scaled x2 to B4 H32
-    "prefill": {"bytes": 509.66e6, "workloads": ("default", "causal4k"),
+    "prefill": {"bytes": 508.68e6, "workloads": ("default", "causal4k"),
                 "sources": ['fa_prefill.cu', 'fa_mma.cuh', 'fa_ptx.cuh', 'fa_plan.h', 'fa_internal.h'],
-                "sha256": "b7e4ab2327cfbbbfde58dc5fcf910fb7190965025cd61fa74ad05e372389afa8"},
-    # paged decode B8 capture: 547.5 MB read + 3.7 MB written for 547.5 MB algorithmic,
+                "sha256": "39f8278a15397c9e404ec0b5a6dab4065b83b4909bcdb490f2cf7fd839b75553"},
+    # paged decode B8 capture: 547.5 MB read + 4.1 MB written for 547.5 MB algorithmic,
     # scaled to the bench call's 2410.7 MB algorithmic
-    "decode": {"workloads": ("default", "decode"), "bytes": 2.427e9, "sources": ['fa_decode.cu', 'fa_ptx.cuh', 'fa_internal.h'],
-               "sha256": "ace52fe8e324b0324a5f68d0ea68dcf6a326d5325938ad1e673f61568f53ee40"},
+    "decode": {"workloads": ("default", "decode"), "bytes": 2.4289e9, "sources": ['fa_decode.cu', 'fa_ptx.cuh', 'fa_internal.h'],
+               "sha256": "698725ea6088b201241ad6575f28f0d7b50601934668e924a540d97a9217fcbe"},
     # FP32 inputs, causal 4k B4 H16 capture of one call: split_bf16_kernel 402.7 MB read +
-    # 346.1 MB written, prefill_bm256_kernel (split) 408.7 MB read + 108.7 MB written;
+    # 345.8 MB written, prefill_bm256_kernel (split) 408.5 MB read + 109.2 MB written;
     # scaled x2 to B4 H32
-    "prefill_f32": {"bytes": 2532.4e6, "workloads": ("causal4k_f32",),
+    "prefill_f32": {"bytes": 2532.5e6, "workloads": ("causal4k_f32",),
                     "sources": ['fa_prefill.cu', 'fa_prefill_split.cu', 'fa_mma.cuh', 'fa_ptx.cuh',
                                 'fa_plan.h', 'fa_internal.h'],
-                    "sha256": "23801671820a0eb2ce009e5c311f59fbc684673078861974fa757874b33c1eec"},
+                    "sha256": "d250971345639f581f6a1087fbebc4fce78df80424acaddc88bfa1ac77caf4ec"},
 }
 
 
