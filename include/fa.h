@@ -157,7 +157,8 @@ fa_status fa_fwd_ex(const fa_fwd_params* params, fa_stream_t stream);
  * invalid sizes. */
 size_t fa_fwd_workspace_size(int B, int H, int Sq, int Sk, int d, int dtype);
 
-/* Query rows per tensor-core tile (128): the row granularity of the fa_fwd_ex trace. */
+/* Query rows per tensor-core tile of the 128- and 256-row items (128): the row granularity of
+ * the fa_fwd_ex trace; items of block_m = 64 use 64-row tiles, and so do their trace rows. */
 int fa_fwd_block_m(void);
 
 /* Query rows per work item that fa_fwd (and fa_fwd_ex with block_m = 0) uses for a mask:

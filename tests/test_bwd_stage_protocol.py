@@ -4,8 +4,9 @@ Four agents run their programs against phase-counting barriers, one step at a ti
 random order: the TMA warp fills stage g % 4 with stream half g (g = 2 t + u: tile t,
 half u) after the MMAs of half g - 4 released it; the MMA warp issues the scores of a half
 once it has landed, then, per tile and half, waits for the elementwise warpgroup's P and
-dS, issues the half's products and releases its stage; elementwise warpgroup u waits for
-its half's statistics and scores and hands back P and dS. Every schedule must finish, and
+dS, issues the half's products and releases its stage; the two elementwise warpgroups of
+half u (one per 32 columns of it) each wait for the half's statistics and scores and hand
+back their part of P and dS: the half's barrier completes when both have. Every schedule must finish, and
 every wait must see the phase it means (try_wait.parity succeeds as soon as the phase of
 that parity is the latest completed one, so a wait one fill behind would pass silently).
 """
@@ -34,7 +35,7 @@ def run(n_tiles, seed):
     rnd = random.Random(seed)
     st_full = [Bar(1) for _ in range(STAGES)]
     st_empty = [Bar(1) for _ in range(STAGES)]
-    s_full, p_full = [Bar(1), Bar(1)], [Bar(128), Bar(128)]
+    s_full, p_full = [Bar(1), Bar(1)], [Bar(256), Bar(256)]
     holds = [None] * STAGES
 
     def tma():
@@ -69,7 +70,7 @@ def run(n_tiles, seed):
                     yield from scores(g + 2, u)
                 yield
 
-    def warpgroup(u):
+    def warpgroup(u, sub):
         for t in range(n_tiles):
             g = 2 * t + u
             while not st_full[g % STAGES].ready((g // STAGES) & 1):
@@ -82,7 +83,8 @@ def run(n_tiles, seed):
                 p_full[u].arrive()
             yield
 
-    agents = {"tma": tma(), "mma": mma(), "wg0": warpgroup(0), "wg1": warpgroup(1)}
+    agents = {"tma": tma(), "mma": mma(), "wg00": warpgroup(0, 0), "wg01": warpgroup(0, 1),
+              "wg10": warpgroup(1, 0), "wg11": warpgroup(1, 1)}
     for _ in range(200000):
         if not agents:
             return

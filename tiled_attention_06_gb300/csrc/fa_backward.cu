@@ -20,10 +20,11 @@
 // The dQ kernel recomputes S and dP rather than exchanging dS with the dK/dV kernel, so
 // no FP32 atomics and no second pass over dQ are needed.
 //
-// Roles (320 threads): two elementwise warpgroups, warps 0-3 for the first 64-wide half of
-// every tile and warps 4-7 for the second (one TMEM lane per thread; they share the
-// epilogue), warp 8 TMA, warp 9 MMA (warp-wide, one elected lane issues). Every wait is
-// bounded.
+// Roles (576 threads): four elementwise warpgroups, two per 64-wide half of every tile
+// (warps 0-7 the first half, 8-15 the second; in each pair the first warpgroup takes the
+// half's first 32 columns, the second the last 32; one TMEM lane per thread; all four
+// share the epilogue), warp 16 TMA, warp 17 MMA (warp-wide, one elected lane issues).
+// Every wait is bounded.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -41,9 +42,10 @@ namespace fa {
 namespace {
 
 constexpr int kBT = 128;  // rows of a query or key tile
-constexpr int kBwdThreads = 320;
-constexpr int kBwdTmaWarp = 8;
-constexpr int kBwdMmaWarp = 9;
+constexpr int kBwdThreads = 576;
+constexpr int kBwdTmaWarp = 16;
+constexpr int kBwdMmaWarp = 17;
+constexpr int kBwdEwPerHalf = 256;  // elementwise threads per half (two warpgroups)
 
 // The streamed side moves in halves of 64 rows (kBwdBoxRows, the tensor maps' box height):
 // stage h holds one half of each of the two streamed tiles, and is released as soon as the
@@ -215,8 +217,10 @@ __device__ __forceinline__ void issue_s_half(uint32_t d_tmem, uint32_t a_smem, u
   }
 }
 
-// Y (+)= A_u B_u: A_u 64 packed 16-bit columns in TMEM (K = 64), B_u a streamed 64-row half
-// used MN-major (N = D, its second 64 elements of d 8 KB on; 16 rows = 2048 bytes per MMA).
+// Y (+)= A_u B_u: A_u the half's 64 elements of K as packed 16-bit values in TMEM, written
+// by the two elementwise warpgroups of the half over their own columns: K-elements 0-31 in
+// columns [a, a+16), 32-63 in [a+32, a+48); B_u a streamed 64-row half used MN-major (N = D,
+// its second 64 elements of d 8 KB on; 16 rows = 2048 bytes per MMA).
 template <int D, bool BF16>
 __device__ __forceinline__ void issue_pv_half(uint32_t y_tmem, uint32_t a_tmem, uint32_t b_half,
                                               bool accumulate) {
@@ -224,8 +228,8 @@ __device__ __forceinline__ void issue_pv_half(uint32_t y_tmem, uint32_t a_tmem, 
   const uint64_t b0 = smem_desc_sw128(b_half, kHalf * 128, 1024);
 #pragma unroll
   for (int kk = 0; kk < kHalf / 16; ++kk)
-    umma_ts(y_tmem, a_tmem + kk * 8, b0 + static_cast<uint64_t>(kk * 128), id,
-            (accumulate || kk > 0) ? 1u : 0u);
+    umma_ts(y_tmem, a_tmem + (kk / 2) * 32 + (kk % 2) * 8, b0 + static_cast<uint64_t>(kk * 128),
+            id, (accumulate || kk > 0) ? 1u : 0u);
 }
 
 // A resident 128-row tile as two 64-row boxes per 64-element region of d (the region's
@@ -290,7 +294,7 @@ __device__ __forceinline__ uint32_t bwd_setup(BwdBars* bars, const CUtensorMap* 
     }
     for (int u = 0; u < 2; ++u) {
       mbar_init(smem_u32(&bars->s_full[u]), 1);
-      mbar_init(smem_u32(&bars->p_full[u]), 128);
+      mbar_init(smem_u32(&bars->p_full[u]), kBwdEwPerHalf);
     }
     mbar_init(smem_u32(&bars->acc_full), 1);
     bars->abort = 0;
@@ -444,10 +448,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ elementwise + epilogue
-    const int u = warp / 4;  // this warpgroup's half of every tile (64 queries)
+    const int grp = warp / 4;  // 0..3: half u = grp / 2, columns [32 sub, 32 sub + 32) of it
+    const int u = grp / 2, sub = grp % 2;
     const int row = (warp % 4) * 32 + lane;  // key row of the tile (= TMEM lane)
     const int j = kb * kBT + row;
     const uint32_t t_lane = tmem + (static_cast<uint32_t>((warp % 4) * 32) << 16);
+    const uint32_t c_s = 64 * u + 32 * sub;  // this thread's S^T columns; dP^T 128 further
     bool ok = true;
     int t = 0;
     for (int qb = next_qb(-1, kb, bh, p, nqb); qb < nqb && ok; qb = next_qb(qb, kb, bh, p, nqb), ++t) {
@@ -456,26 +462,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // written the P and dS that the MMAs reading it wait for
       ok = mbar_wait(B(bars->st_full[h]), stage_parity(g), wc);
       ok = __all_sync(0xffffffffu, ok);
-      const float4* st4 = reinterpret_cast<const float4*>(stats + h * 2 * kHalf);
+      const float4* st4 = reinterpret_cast<const float4*>(stats + h * 2 * kHalf + 32 * sub);
       if (ok) {
         ok = mbar_wait(B(bars->s_full[u]), t & 1, wc);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_fence_after();
-        const int m0 = qb * kBT + 64 * u;
+        const int m0 = qb * kBT + 64 * u + 32 * sub;
         const RowSpan vis = query_cols(j, m0, p.Sk, p);
-        // all 64 columns of S^T_u and dP^T_u in one round trip to TMEM
-        uint32_t sv[64], dp[64];
-        tmem_ld32(t_lane + 64 * u, sv);
-        tmem_ld32(t_lane + 64 * u + 32, sv + 32);
-        tmem_ld32(t_lane + 128 + 64 * u, dp);
-        tmem_ld32(t_lane + 128 + 64 * u + 32, dp + 32);
-        tmem_ld_wait<64>(sv);
-        tmem_ld_tie<64>(dp);
+        uint32_t sv[32], dp[32];
+        tmem_ld32(t_lane + c_s, sv);
+        tmem_ld32(t_lane + 128 + c_s, dp);
+        tmem_ld_wait<32>(sv);
+        tmem_ld_tie<32>(dp);
 #pragma unroll
-        for (int e = 0; e < 64; e += 4) {  // 4 queries at a time; statistics from shared memory
+        for (int e = 0; e < 32; e += 4) {  // 4 queries at a time; statistics from shared memory
           const float4 a = st4[e / 4];
-          const float4 d = st4[(kHalf + e) / 4];
+          const float4 d = st4[kHalf / 4 + e / 4];
           const float l2[4] = {a.x, a.y, a.z, a.w}, dd[4] = {d.x, d.y, d.z, d.w};
           float pv[4], dv[4];
 #pragma unroll
@@ -485,20 +488,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             pv[w] = on ? ex2_approx(__uint_as_float(sv[e + w]) * p.sl2 - l2[w]) : 0.f;
             dv[w] = pv[w] * (__uint_as_float(dp[e + w]) - dd[w]);
           }
-          // packed over the columns already read (P^T_u and dS^T_u: 32 columns each)
+          // packed over this thread's columns already read (16 each for P^T and dS^T)
           sv[e / 2] = BF16 ? cvt_pack_bf16(pv[0], pv[1]) : cvt_pack_f16(pv[0], pv[1]);
           sv[e / 2 + 1] = BF16 ? cvt_pack_bf16(pv[2], pv[3]) : cvt_pack_f16(pv[2], pv[3]);
           dp[e / 2] = BF16 ? cvt_pack_bf16(dv[0], dv[1]) : cvt_pack_f16(dv[0], dv[1]);
           dp[e / 2 + 1] = BF16 ? cvt_pack_bf16(dv[2], dv[3]) : cvt_pack_f16(dv[2], dv[3]);
         }
-        tmem_st32(t_lane + 64 * u, sv);        // P^T_u over columns already read
-        tmem_st32(t_lane + 128 + 64 * u, dp);  // dS^T_u likewise
+        tmem_st16(t_lane + c_s, sv);        // P^T over columns already read
+        tmem_st16(t_lane + 128 + c_s, dp);  // dS^T likewise
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(B(bars->p_full[u]));
       }
     }
-    // epilogue of this thread's key: dV (first warpgroup) or scale * dK (second)
+    // epilogue of this thread's key: warpgroups 0, 1 write halves of dV, 2, 3 halves of
+    // scale * dK (D/2 columns each)
     if (ok) {
       ok = mbar_wait(B(bars->acc_full), 0, wc);
       ok = __all_sync(0xffffffffu, ok);
@@ -506,16 +510,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (ok) {
       tc_fence_after();
       const size_t orow = static_cast<size_t>(bh) * p.Sk + j;
+      const bool is_k = grp >= 2;
+      const int c_lo = (grp % 2) * (D / 64);
 #pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = c_lo; c < c_lo + D / 64; ++c) {
         uint32_t v[32];
-        tmem_ld32(t_lane + 256 + u * D + c * 32, v);
+        tmem_ld32(t_lane + 256 + (is_k ? D : 0) + c * 32, v);
         tmem_ld_wait<32>(v);
         if (t == 0) {  // no query sees these keys: the gradients are 0, not TMEM contents
 #pragma unroll
           for (int e = 0; e < 32; ++e) v[e] = 0u;
         }
-        if (j < p.Sk) store_tile_row<D, BF16>(u ? b.dk : b.dv, orow, v, u ? b.scale : 1.f, c * 32);
+        if (j < p.Sk)
+          store_tile_row<D, BF16>(is_k ? b.dk : b.dv, orow, v, is_k ? b.scale : 1.f, c * 32);
       }
     }
   }
@@ -622,10 +629,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ elementwise + epilogue
-    const int u = warp / 4;  // this warpgroup's half of every tile (64 keys)
+    const int grp = warp / 4;  // 0..3: half u = grp / 2 (64 keys), keys [32 sub, 32 sub + 32)
+    const int u = grp / 2, sub = grp % 2;
     const int row = (warp % 4) * 32 + lane;  // query row of the tile (= TMEM lane)
     const int i = qb * kBT + row;
     const uint32_t t_lane = tmem + (static_cast<uint32_t>((warp % 4) * 32) << 16);
+    const uint32_t c_s = 64 * u + 32 * sub;  // this thread's S columns; dP 128 further
     const bool in = i < p.Sq;
     const size_t srow = static_cast<size_t>(bh) * p.Sq + (in ? i : 0);
     const float l2 = in ? b.lse[srow] * 1.4426950408889634f : 0.f;
@@ -639,17 +648,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_fence_after();
-        const ColMask cm = key_cols(i, nb * kBT + 64 * u, p.Sk, p);
-        // all 64 columns of S_u and dP_u in one round trip to TMEM
-        uint32_t sv[64], dp[64];
-        tmem_ld32(t_lane + 64 * u, sv);
-        tmem_ld32(t_lane + 64 * u + 32, sv + 32);
-        tmem_ld32(t_lane + 128 + 64 * u, dp);
-        tmem_ld32(t_lane + 128 + 64 * u + 32, dp + 32);
-        tmem_ld_wait<64>(sv);
-        tmem_ld_tie<64>(dp);
+        const ColMask cm = key_cols(i, nb * kBT + 64 * u + 32 * sub, p.Sk, p);
+        uint32_t sv[32], dp[32];
+        tmem_ld32(t_lane + c_s, sv);
+        tmem_ld32(t_lane + 128 + c_s, dp);
+        tmem_ld_wait<32>(sv);
+        tmem_ld_tie<32>(dp);
 #pragma unroll
-        for (int e = 0; e < 64; e += 2) {
+        for (int e = 0; e < 32; e += 2) {
           float dv[2];
 #pragma unroll
           for (int w = 0; w < 2; ++w) {
@@ -660,7 +666,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           }
           dp[e / 2] = BF16 ? cvt_pack_bf16(dv[0], dv[1]) : cvt_pack_f16(dv[0], dv[1]);
         }
-        tmem_st32(t_lane + 128 + 64 * u, dp);  // dS_u over columns already read
+        tmem_st16(t_lane + 128 + c_s, dp);  // dS over this thread's columns already read
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(B(bars->p_full[u]));
@@ -672,8 +678,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     if (ok) {  // the TMEM loads are warp-collective: every lane runs them, valid rows store
       tc_fence_after();
+      // D/32 chunks of 32 columns over the four warpgroups
 #pragma unroll 1
-      for (int c = u * (D / 64); c < (u + 1) * (D / 64); ++c) {  // this warpgroup's half of d
+      for (int c = grp; c < D / 32; c += 4) {
         uint32_t q[32];
         tmem_ld32(t_lane + 256 + c * 32, q);
         tmem_ld_wait<32>(q);
