@@ -33,11 +33,14 @@ sys.path.insert(0, ROOT)
 
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-# Nominal dense FP16/BF16 tensor-core rate of one GPU: NVIDIA's HGX B300 figure, 36 PFLOPS
-# FP16/BF16 for 8 GPUs, which NVIDIA quotes with 2:4 sparsity, halved for dense math.
-NOMINAL_BF16_TFLOPS = 2250.0
-NOMINAL_SOURCE = ("NVIDIA HGX B300 spec: FP16/BF16 tensor core 36 PFLOPS per 8 GPUs with 2:4 "
-                  "sparsity = 2.25 PFLOP/s dense per GPU")
+# Nominal dense FP16/BF16 tensor-core rate of one GB300: NVIDIA's GB300 NVL72 figure, 360
+# PFLOPS FP16/BF16 for 72 GPUs, which NVIDIA quotes with 2:4 sparsity, halved for dense math.
+# A chain of tcgen05 128x128x16 bf16 MMAs on this GPU runs one MMA per 65 SM cycles, about
+# 8050 FLOP per cycle per SM, i.e. 2.53 PFLOP/s at 2070 MHz on 152 SMs: the same figure.
+NOMINAL_BF16_TFLOPS = 2500.0
+NOMINAL_SOURCE = ("NVIDIA GB300 NVL72 spec: FP16/BF16 tensor core 360 PFLOPS per 72 GPUs with "
+                  "2:4 sparsity = 2.5 PFLOP/s dense per GPU (a tcgen05 MMA chain measures 2.53 at "
+                  "2070 MHz)")
 # Untimed steps run back to back while the clock sampler is on, just before the timed
 # ones, so that the sampled clocks show the kernels under sustained load even when the
 # timed region itself is short.
