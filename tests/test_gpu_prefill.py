@@ -259,3 +259,30 @@ def test_block_sparse_4k_bigbird_sampled():
     rows = sample_rows(B, H, S, fa.fa_fwd_block_m(), n_random=128, seed=3)
     ref_o, ref_l = oracle.attention_layout(q, k, v, scale, lay.numpy(), rows=rows)
     compare(pick_rows(o, rows, S), pick_rows(lse, rows, S), ref_o, ref_l, "block-sparse 4k")
+
+
+@pytest.mark.parametrize("dt", ["bf16", "f32"])
+def test_output_only_16_byte_aligned(dt):
+    """The API asks O to be 16-byte aligned only; the epilogue's 32-byte stores must fall back
+    when O sits 16 bytes past a 32-byte boundary."""
+    B, H, S, d = 1, 3, 300, 128
+    scale = 1 / math.sqrt(d)
+    dev = torch.device("cuda")
+    dtype = torch.bfloat16 if dt == "bf16" else torch.float32
+    q, k, v = inputs.prefill_inputs(B, H, S, S, d, dtype, seed=31)
+    step = 16 // torch.empty(0, dtype=dtype).element_size()  # elements in 16 bytes
+    buf = torch.full((q.numel() + 64,), float("nan"), dtype=dtype, device=dev)
+    assert buf.data_ptr() % 32 == 0
+    o = buf[step:step + q.numel()].view(q.shape)
+    assert o.data_ptr() % 32 == 16
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+    for mode in (fa.FA_MASK_CAUSAL, fa.FA_MASK_NONE):
+        fa.fa_fwd(q.to(dev), k.to(dev), v.to(dev), o, lse, scale, mode)
+        torch.cuda.synchronize()
+        assert fa.fa_get_device_status() == fa.FA_OK
+        ref_o, ref_l = oracle.attention(q, k, v, scale, mode)
+        if dt == "f32":
+            compare(o, lse, ref_o, ref_l, f"16-byte aligned O, mode {mode}", o_max=1e-3, o_mean=1e-4)
+        else:
+            compare(o, lse, ref_o, ref_l, f"16-byte aligned O, mode {mode}")
+        assert torch.isnan(buf[:step].float()).all() and torch.isnan(buf[step + q.numel():].float()).all()

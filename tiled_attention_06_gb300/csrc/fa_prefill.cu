@@ -274,24 +274,38 @@ __device__ __forceinline__ void store_row(uint32_t t_lane, uint32_t o_col, bool 
     uint32_t ov[32];
     tmem_ld32(t_lane + o_col + c * 32, ov);
     tmem_ld_wait<32>(ov);
+    // 32-byte stores when O is 32-byte aligned (a row's chunk of 32 columns then starts on a
+    // 32-byte boundary too), else 16-byte ones; the choice is the same for the whole launch
+    const bool wide = (reinterpret_cast<uintptr_t>(p.o) & 31u) == 0;
     if (OUT_F32 && valid) {
-      float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + orow * D + c * 32);
 #pragma unroll
-      for (int e = 0; e < 8; ++e)
-        dst[e] = make_float4(__uint_as_float(ov[4 * e]) * inv_l,
-                             __uint_as_float(ov[4 * e + 1]) * inv_l,
-                             __uint_as_float(ov[4 * e + 2]) * inv_l,
-                             __uint_as_float(ov[4 * e + 3]) * inv_l);
+      for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * inv_l);
+      float* dst = static_cast<float*>(p.o) + orow * D + c * 32;
+      if (wide) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) st_global_v8(dst + 8 * e, ov + 8 * e);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          reinterpret_cast<uint4*>(dst)[e] =
+              make_uint4(ov[4 * e], ov[4 * e + 1], ov[4 * e + 2], ov[4 * e + 3]);
+      }
     } else if (valid) {
       uint32_t pk[16];
 #pragma unroll
       for (int e = 0; e < 16; ++e)
         pk[e] = pack2(__uint_as_float(ov[2 * e]) * inv_l, __uint_as_float(ov[2 * e + 1]) * inv_l,
                       BF16);
-      uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + orow * D + c * 32);
+      uint16_t* dst = static_cast<uint16_t*>(p.o) + orow * D + c * 32;
+      if (wide) {
+        st_global_v8(dst, pk);
+        st_global_v8(dst + 16, pk + 8);
+      } else {
 #pragma unroll
-      for (int e = 0; e < 4; ++e)
-        dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+        for (int e = 0; e < 4; ++e)
+          reinterpret_cast<uint4*>(dst)[e] =
+              make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+      }
     }
   }
   if (valid && p.lse)
