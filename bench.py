@@ -778,8 +778,9 @@ def run_next_rows(args, fa, workload, peaks, peak_kind, stream, world):
     """chunked: append a 512-token chunk to each of 8 paged sequences (contexts up to
     7.7k, 256-token pages, fp16) and run its causal prefill through the block table.
     multimodal: LLaVA-shaped vision 576 + text 2048 tokens (B=4, H=32, d=128, bf16) as
-    three calls (vision full, text causal, text-to-vision) plus the LSE merge; the same
-    layer as two calls (vision, text over [vision; text] keys) is timed beside it."""
+    three calls (vision full, text causal, text-to-vision) plus the LSE merge; beside it,
+    the text rows as one causal call over [vision; text] keys, and the whole layer as one
+    prefix-LM call over [vision; text] with the vision tokens as the prefix."""
     from tiled_attention_06_gb300 import inputs
     dev = torch.device("cuda", torch.cuda.current_device())
     K, W = args.steps, args.warmup
@@ -856,6 +857,9 @@ def run_next_rows(args, fa, workload, peaks, peak_kind, stream, world):
         ms, clk = timed(split, K, W, stream, args.clock_soak)
         one, _ = timed([lambda: fa.fa_fwd(qt, k, v, o1, l1, scale, fa.FA_MASK_CAUSAL,
                                           stream=stream)], K, W, stream, 0.0)
+        oa, la = torch.empty_like(q), torch.empty(B, H, V + T, device=dev)
+        plm, _ = timed([lambda: fa.fa_fwd(q, k, v, oa, la, scale, fa.FA_MASK_PREFIX_LM,
+                                          n_global=V, stream=stream)], K, W, stream, 0.0)
         assert fa.fa_get_device_status() == fa.FA_OK
         pairs = V * V + T * (T + 1) // 2 + T * V
         flops = 4.0 * B * H * d * pairs
@@ -872,6 +876,9 @@ def run_next_rows(args, fa, workload, peaks, peak_kind, stream, world):
                     "calls_ms": {"vision": ms[0] / K, "text_causal": ms[1] / K,
                                  "text_to_vision": ms[2] / K, "merge": ms[3] / K},
                     "text_rows_one_call_ms": one[0] / K,
+                    "prefix_lm_one_call": {"ms": plm[0] / K,
+                                           "value": flops * K / (plm[0] / 1e3) / 1e12,
+                                           "unit": "TFLOP/s"},
                     "config": {"workload": f"vision {V} + text {T} tokens, B{B} H{H} d{d} "
                                            f"{c['dtype']}"}})
     return res

@@ -5,7 +5,8 @@ into a vision-internal call, a text-internal causal call and a text-to-vision cr
 with identical results. Here the text queries' part of that layer (all vision keys plus
 causal text keys) is also a single causal call over the concatenated keys (queries
 aligned to the last keys), so the three-call split merged by LSE must match both that
-single call and the FP64 oracle.
+single call and the FP64 oracle. The whole layer, vision rows included, is also one
+prefix-LM call over the concatenated tokens with the vision tokens as the prefix.
 """
 import math
 
@@ -29,10 +30,11 @@ def _built():
     fa.lib()
 
 
-def fwd(q, k, v, scale, mode):
+def fwd(q, k, v, scale, mode, n_global=0):
     o = torch.empty_like(q)
     lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
-    fa.fa_fwd(q.contiguous(), k.contiguous(), v.contiguous(), o, lse, scale, mode)
+    fa.fa_fwd(q.contiguous(), k.contiguous(), v.contiguous(), o, lse, scale, mode,
+              n_global=n_global)
     return o, lse
 
 
@@ -103,3 +105,33 @@ def test_multimodal_three_call_split(V, T, H):
     # split and single call agree with each other beyond the oracle tolerance
     diff = (o_txt.float() - o_one.float()).abs().max().item()
     assert diff <= 1.6e-2
+
+
+@pytest.mark.parametrize("V,T,H", [(96, 300, 2), (576, 2048, 8)])
+def test_multimodal_layer_is_one_prefix_lm_call(V, T, H):
+    """The whole layer, vision and text rows together, as one prefix-LM call over the
+    concatenated [vision; text] tokens with the V vision tokens as the prefix: a vision
+    query sees every vision key (j < V), and no text key since j <= i < V; a text query
+    sees every vision key and the text keys up to its own position. So the vision rows
+    equal call 1 of the split and the text rows the merged calls 2 and 3."""
+    d, dt = 128, torch.bfloat16
+    S = V + T
+    q, k, v = inputs.prefill_inputs(1, H, S, S, d, dt, seed=3 * S)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    scale = 1 / math.sqrt(d)
+    o_all, l_all = fwd(qd, kd, vd, scale, fa.FA_MASK_PREFIX_LM, n_global=V)
+    o_vis, l_vis = fwd(qd[:, :, :V], kd[:, :, :V], vd[:, :, :V], scale, fa.FA_MASK_NONE)
+    o_tt, l_tt = fwd(qd[:, :, V:], kd[:, :, V:], vd[:, :, V:], scale, fa.FA_MASK_CAUSAL)
+    o_tv, l_tv = fwd(qd[:, :, V:], kd[:, :, :V], vd[:, :, :V], scale, fa.FA_MASK_NONE)
+    o_txt, l_txt = torch.empty_like(o_tt), torch.empty_like(l_tt)
+    fa.fa_merge_partials(o_tt, l_tt, o_tv, l_tv, o_txt, l_txt)
+    torch.cuda.synchronize()
+    assert fa.fa_get_device_status() == fa.FA_OK
+    ref_o, ref_l = oracle.attention(q, k, v, scale, oracle.MASK_PREFIX_LM, 0, V)
+    compare(o_all, l_all, ref_o, ref_l, "prefix-LM over [vision; text]")
+    # against the split, row block by row block
+    for rows, (o_s, l_s) in ((slice(0, V), (o_vis, l_vis)), (slice(V, S), (o_txt, l_txt))):
+        diff = (o_all[:, :, rows].float() - o_s.float()).abs().max().item()
+        assert diff <= 1.6e-2
+        ldiff = (l_all[:, :, rows] - l_s).abs().max().item()
+        assert ldiff <= 1e-3
