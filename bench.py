@@ -887,7 +887,7 @@ def run_next_rows(args, fa, workload, peaks, peak_kind, stream, world):
 def run_backward(args, fa, peaks, stream, world):
     """Backward of the causal 4k bf16 prefill (B4 H32 S4096 d128): fa_bwd after one fa_fwd,
     timed with CUDA events. Work counted: the five products of the backward (S recomputed,
-    dP, dV, dK, dQ) over the visible pairs, 2.5x the forward's."""
+    dP, dV, dK, dQ) over the visible pairs, 2.5x the forward's; each is computed once."""
     from tiled_attention_06_gb300 import inputs
     cfg = PREFILL["causal4k"]
     dev = torch.device("cuda", torch.cuda.current_device())
@@ -915,7 +915,7 @@ def run_backward(args, fa, peaks, stream, world):
             "metric": "attention backward TFLOP/s (5 products over visible pairs)",
             "value": val, "unit": "TFLOP/s", "dtype": cfg["dtype"], "ms_per_step": ms / K,
             "gpu_launches": 3 * K, "clocks": clk,
-            "roofline": {"kernel": "bwd_dkdv_kernel + bwd_dq_kernel (+ bwd_prep_kernel)",
+            "roofline": {"kernel": "bwd_dkdv_kernel (+ bwd_prep_kernel, bwd_dq_convert_kernel)",
                          "bound": "tensor", "achieved": achieved, "peak": tc_peak,
                          "unit": "TFLOP/s", "frac": achieved / tc_peak, "traffic": None,
                          "algorithmic_flops": flops},

@@ -176,11 +176,15 @@ int fa_fwd_default_block_m(int mask_mode);
  *     dv = P^T dout,  dS = P (dout v^T - D),  dq = scale dS k,  dk = scale dS^T q.
  *   q, o, dout, dq [B, H, Sq, d]; k, v, dk, dv [B, H, Sk, d]: dtype, contiguous, device
  *   lse        [B, H, Sq] float32, the natural-log LSE that fa_fwd returned with o
- *   workspace  device scratch of at least fa_bwd_workspace_size(B, H, Sq) bytes, 16-byte
- *              aligned, owned by the caller (holds D)
+ *   workspace  device scratch, 16-byte aligned, owned by the caller: an FP32 dq
+ *              accumulator [B, H, Sq, d] followed by D [B, H, Sq], i.e. B*H*Sq*(d+1)*4
+ *              bytes; fa_bwd_workspace_size(B, H, Sq) returns that size for d = 128, enough
+ *              for every supported d. Its contents on entry do not matter.
  *   d, scale, mask_mode / window / n_global, dtype as for fa_fwd; FA_MASK_BLOCK_SPARSE is
  *   FA_ERR_UNSUPPORTED. dq, dk and dv are written (RN from FP32 accumulators); a key no
- *   query sees gets dk = dv = 0, a query that sees no key dq = 0.
+ *   query sees gets dk = dv = 0, a query that sees no key dq = 0. dq sums the
+ *   contributions of the key blocks with FP32 atomic additions, so its last bit can differ
+ *   between runs; dk and dv are the same on every run.
  */
 size_t fa_bwd_workspace_size(int B, int H, int Sq);
 fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
@@ -336,7 +340,10 @@ fa_status fa_decode_paged_noalloc(const void* q, const void* k_pages, const void
 /*
  * fa_get_device_status - synchronise `stream`, then read and clear the device
  * status word. Returns FA_OK, FA_ERR_BAD_PAGE or FA_ERR_TIMEOUT (FA_ERR_CUDA if the
- * stream itself failed).
+ * stream itself failed). FA_ERR_UNSUPPORTED means that a backward kernel found its dynamic
+ * shared memory starting more than 256 bytes past a 1024-byte boundary, which its layout
+ * at d = 128 cannot absorb, and wrote nothing (dynamic shared memory starts on such a
+ * boundary on the devices this library targets).
  */
 fa_status fa_get_device_status(fa_stream_t stream);
 

@@ -604,9 +604,16 @@ fa_status fa_decode_paged_noalloc(const void* q, const void* k_pages, const void
   return FA_OK;
 }
 
+// Workspace of fa_bwd at head dimension d: the FP32 dQ accumulator [B,H,Sq,d] first, then
+// D [B,H,Sq]; fa_bwd_workspace_size covers the largest supported d.
+static size_t bwd_workspace_bytes(int B, int H, int Sq, int d) {
+  return static_cast<size_t>(B) * H * (Sq > 0 ? Sq : 1) * (static_cast<size_t>(d) + 1) *
+         sizeof(float);
+}
+
 size_t fa_bwd_workspace_size(int B, int H, int Sq) {
   if (B < 1 || H < 1 || Sq < 0) return 0;
-  return static_cast<size_t>(B) * H * (Sq > 0 ? Sq : 1) * sizeof(float);
+  return bwd_workspace_bytes(B, H, Sq, 128);
 }
 
 fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
@@ -639,7 +646,7 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
   if (!aligned16(o) || !aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
     return fail(FA_ERR_INVALID_ARG, "o, dout, dq, dk and dv must be 16-byte aligned");
   if (lse && !aligned4(lse)) return fail(FA_ERR_INVALID_ARG, "lse must be 4-byte aligned");
-  const size_t need = fa_bwd_workspace_size(B, H, Sq);
+  const size_t need = bwd_workspace_bytes(B, H, Sq, d);
   if (Sq > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace)))
     return fail(FA_ERR_INVALID_ARG, "workspace: %zu bytes, 16-byte aligned, needed", need);
   DeviceInfo dev;
@@ -660,7 +667,8 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
   p.status = dev.status;
   p.timeout_ns = 1000000000ull;
   L.b.lse = lse;
-  L.b.dsum = static_cast<float*>(workspace);
+  L.b.dqacc = static_cast<float*>(workspace);
+  L.b.dsum = static_cast<float*>(workspace) + static_cast<size_t>(BH) * Sq * d;
   L.b.dq = dq;
   L.b.dk = dk;
   L.b.dv = dv;
@@ -748,6 +756,9 @@ fa_status fa_get_device_status(fa_stream_t stream) {
   if (e != cudaSuccess) return cuda_fail(e, "clearing the device status word");
   if (word & fa::FA_DEV_TIMEOUT) return fail(FA_ERR_TIMEOUT, "a kernel gave up on a pipeline wait");
   if (word & fa::FA_DEV_BAD_PAGE) return fail(FA_ERR_BAD_PAGE, "a block-table entry or context length was out of range");
+  if (word & fa::FA_DEV_SMEM_BASE)
+    return fail(FA_ERR_UNSUPPORTED, "a kernel's dynamic shared memory did not start close enough "
+                "to a 1024-byte boundary for its layout; its outputs were not written");
   return FA_OK;
 }
 

@@ -7,24 +7,27 @@
 //   dQ = scale dS K, dK = scale dS^T Q.
 //
 // Three kernels, each step on the tensor cores where it is a contraction:
-//   bwd_prep_kernel   D_i, one FP32 per query row (HBM-bound).
+//   bwd_prep_kernel   D_i, one FP32 per query row (HBM-bound), and zeros the FP32 dQ
+//                     accumulator of the row.
 //   bwd_dkdv_kernel   one CTA per (batch*head, block of 128 keys); TMEM lane = key. For
-//                     each block of 128 queries that sees these keys: S^T = K Q^T and
-//                     dP^T = V dO^T (tcgen05, A and B from shared memory), P^T and
-//                     dS^T = P^T (dP^T - D) by the elementwise warpgroup, rounded to 16
-//                     bits over their own TMEM columns, then dV += P^T dO and
-//                     dK += dS^T Q (tcgen05, A from TMEM).
-//   bwd_dq_kernel     one CTA per (batch*head, block of 128 queries); TMEM lane = query.
-//                     For each block of 128 keys the queries see: S = Q K^T, dP = dO V^T,
-//                     dS = P (dP - D), dQ += dS K.
-// The dQ kernel recomputes S and dP rather than exchanging dS with the dK/dV kernel, so
-// no FP32 atomics and no second pass over dQ are needed.
+//                     each block of 128 queries that sees these keys, in two halves of 64
+//                     queries: S^T = K Q^T and dP^T = V dO^T (tcgen05, A and B from shared
+//                     memory); P^T and dS^T = P^T (dP^T - D) by the elementwise warps, P^T
+//                     rounded to 16 bits over its own TMEM columns and dS^T into shared
+//                     memory; then dV += P^T dO (A from TMEM), dK += dS^T Q and
+//                     dQ^T = K^T dS^T (A and B from shared memory; TMEM lane = element of
+//                     d), the last added by the elementwise warps into an FP32 dQ
+//                     accumulator in global memory (coalesced reductions, 128 bytes per
+//                     warp instruction).
+//   bwd_dq_convert_kernel  dq = scale * accumulator, rounded to 16 bits (HBM-bound).
+// Each visible (query block, key block) pair is visited once: five products over the
+// visible pairs, none recomputed.
 //
-// Roles (576 threads): four elementwise warpgroups, two per 64-wide half of every tile
-// (warps 0-7 the first half, 8-15 the second; in each pair the first warpgroup takes the
-// half's first 32 columns, the second the last 32; one TMEM lane per thread; all four
-// share the epilogue), warp 16 TMA, warp 17 MMA (warp-wide, one elected lane issues).
-// Every wait is bounded.
+// Roles of the dK/dV kernel (576 threads): four elementwise warpgroups, two per 64-wide
+// half of every tile (warps 0-7 the first half, 8-15 the second; in each pair the first
+// warpgroup takes the half's first 32 columns, the second the last 32; one TMEM lane per
+// thread; all four share the epilogue), warp 16 TMA, warp 17 MMA (warp-wide, one elected
+// lane issues). Every wait is bounded.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -59,25 +62,36 @@ template <int D>
 struct BwdCfg {
   static constexpr int TILE = kBT * D * 2;   // one 128-row 16-bit tile (resident)
   static constexpr int HTILE = kHalf * D * 2;  // one 64-row half (streamed)
-  // two resident tiles + four stages of two streamed halves + statistics + barriers, 1 KB
-  // aligned; at least half the SM's shared memory, so that one CTA (which takes all 512
-  // TMEM columns) is resident per SM
+  static constexpr int DS = kBT * kHalf * 2;   // dS^T of one half: 128 keys x 64 queries
   static constexpr int STATS = 2 * kHalf * 4;  // per stage: LSE * log2(e) and D of 64 queries
-  static constexpr int SMEM_USED = 1024 + 2 * TILE + kStages * 2 * HTILE + kStages * STATS + 1024;
-  static constexpr int SMEM = SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024;
-  static_assert(SMEM <= 232448, "shared memory over budget");
+  static constexpr int BARS = 256;             // BwdBars, rounded up
+  // From a 1024-byte aligned base: K, V (resident), four stages of two streamed halves,
+  // dS^T of both halves, statistics, barriers.
+  static constexpr int BODY = 2 * TILE + kStages * 2 * HTILE + 2 * DS + kStages * STATS + BARS;
+  // The allocation leaves room to align the base when the device's dynamic shared memory
+  // does not start 1024-byte aligned, up to the per-block limit; the kernel checks that its
+  // base fits (at d = 128 it does when the allocation starts at most 768 bytes short of a
+  // 1024-byte boundary, and the usual start is on one).
+  static constexpr int WANT = BODY + 1023;
+  static constexpr int SMEM = WANT < 232448 ? WANT : 232448;
+  static_assert(BODY + 768 <= SMEM, "shared memory over budget");
+  // over half the SM's shared memory: one CTA (which takes all 512 TMEM columns) per SM
+  static_assert(BODY > 116 * 1024, "two CTAs would share an SM");
 };
 
 struct BwdBars {
   uint64_t res_full;              // the CTA's resident tiles landed
   uint64_t st_full[kStages];      // streamed halves of stage h landed
   uint64_t st_empty[kStages];     // MMAs done with stage h
-  uint64_t s_full[2];             // S and dP of half u of the current tile in TMEM
-  uint64_t p_full[2];             // P and dS (16-bit) of half u written back
+  uint64_t s_full[2];             // S^T and dP^T of half u of the current tile in TMEM
+  uint64_t p_full[2];             // P^T (TMEM) and dS^T (shared memory) of half u written
+  uint64_t dq_full[2];            // dQ^T of half u in TMEM (over the dP^T columns)
+  uint64_t dq_read[2];            // the elementwise warps of half u have read dQ^T
   uint64_t acc_full;              // every MMA of the CTA complete
   uint32_t tmem_base;
   uint32_t abort;
 };
+static_assert(sizeof(BwdBars) <= 256, "barrier block over its reserve");
 
 // Half g = 2 t + u of the stream (tile t, half u) lives in stage g % kStages; its fills and
 // releases alternate parity every kStages halves.
@@ -86,40 +100,6 @@ __device__ __forceinline__ uint32_t stage_parity(int g) { return (g / kStages) &
 
 // Key positions are the query index plus delta = Sk - Sq (queries aligned to the last
 // Sq keys), as in the forward.
-
-// Keys visible to query i in the columns of the key tile at n0, as in the forward's
-// partial-tile mask: column c is visible iff c <= lim and (c >= lo or c < gl).
-struct ColMask {
-  int lim, lo, gl;
-};
-__device__ __forceinline__ ColMask key_cols(int i, int n0, int sk, const PrefillParams& p) {
-  ColMask m{INT_MIN, INT_MIN, INT_MIN};
-  if (i >= p.Sq) return m;  // lim = INT_MIN: nothing
-  const int pos = i + sk - p.Sq;
-  m.lim = min(pos, sk - 1) - n0;
-  switch (p.mask_mode) {
-    case FA_MASK_NONE:
-      m.lim = sk - 1 - n0;
-      break;
-    case FA_MASK_CAUSAL_WINDOW:
-      m.lo = pos - p.window + 1 - n0;
-      m.gl = p.n_global - n0;
-      break;
-    case FA_MASK_BAND: {
-      const long long hi = static_cast<long long>(pos) + p.window;
-      m.lim = static_cast<int>((hi < sk - 1 ? hi : sk - 1) - n0);
-      const long long l0 = static_cast<long long>(pos) - p.window - n0;
-      m.lo = l0 < INT_MIN ? INT_MIN : static_cast<int>(l0);
-      break;
-    }
-    case FA_MASK_PREFIX_LM:
-      m.lim = min(max(pos, p.n_global - 1), sk - 1) - n0;
-      break;
-    default:
-      break;
-  }
-  return m;
-}
 
 // Queries that see key j, as the interval [lo, hi] of columns of the query tile at m0
 // (the transpose of the same masks); empty when lo > hi.
@@ -163,11 +143,13 @@ __device__ __forceinline__ void wait_quiet_b(uint32_t bar, uint32_t parity, cons
 }
 
 // D_i = sum_c dO_ic O_ic in FP32: d/8 lanes per row, one 16-byte load of each per lane,
-// xor-shuffle reduction inside the row's lanes.
+// xor-shuffle reduction inside the row's lanes. Each lane also zeros its 8 elements of the
+// row's FP32 dQ accumulator.
 template <int D, bool BF16>
 __global__ void __launch_bounds__(256) bwd_prep_kernel(const uint4* __restrict__ o,
                                                        const uint4* __restrict__ dout,
-                                                       float* __restrict__ dsum, int64_t rows) {
+                                                       float* __restrict__ dsum,
+                                                       float4* __restrict__ dqacc, int64_t rows) {
   constexpr int LPR = D / 8;  // lanes per row
   constexpr int RPW = 32 / LPR;
   const int lane = threadIdx.x % 32;
@@ -192,10 +174,31 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const uint4* __restrict__
         }
         acc += x.x * y.x + x.y * y.y;
       }
+      const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+      dqacc[(row * LPR + lane % LPR) * 2] = z;
+      dqacc[(row * LPR + lane % LPR) * 2 + 1] = z;
     }
 #pragma unroll
     for (int off = LPR / 2; off > 0; off /= 2) acc += __shfl_xor_sync(0xffffffffu, acc, off);
     if (row < rows && lane % LPR == 0) dsum[row] = acc;
+  }
+}
+
+// dq = scale * accumulator, rounded to 16 bits: eight elements per thread per step.
+template <bool BF16>
+__global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const float4* __restrict__ acc,
+                                                             uint4* __restrict__ dq, float scale,
+                                                             int64_t n8) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8; i += stride) {
+    const float4 a = acc[2 * i], b = acc[2 * i + 1];
+    const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    uint32_t pk[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      pk[e] = BF16 ? cvt_pack_bf16(v[2 * e] * scale, v[2 * e + 1] * scale)
+                   : cvt_pack_f16(v[2 * e] * scale, v[2 * e + 1] * scale);
+    dq[i] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
   }
 }
 
@@ -230,6 +233,36 @@ __device__ __forceinline__ void issue_pv_half(uint32_t y_tmem, uint32_t a_tmem, 
   for (int kk = 0; kk < kHalf / 16; ++kk)
     umma_ts(y_tmem, a_tmem + (kk / 2) * 32 + (kk % 2) * 8, b0 + static_cast<uint64_t>(kk * 128),
             id, (accumulate || kk > 0) ? 1u : 0u);
+}
+
+// dK (+)= dS^T_u Q_u: A = dS^T_u in shared memory (128 keys x 64 queries, K-major, one
+// 128-byte swizzled region), B = Q_u, the streamed 64-row half used MN-major as in
+// issue_pv_half.
+template <int D, bool BF16>
+__device__ __forceinline__ void issue_dk_half(uint32_t y_tmem, uint32_t ds, uint32_t b_half,
+                                              bool accumulate) {
+  constexpr uint32_t id = idesc_f16(BF16, kBT, D, true);
+  const uint64_t a0 = smem_desc_sw128(ds, 16, 1024);
+  const uint64_t b0 = smem_desc_sw128(b_half, kHalf * 128, 1024);
+#pragma unroll
+  for (int kk = 0; kk < kHalf / 16; ++kk)
+    umma_ss(y_tmem, a0 + static_cast<uint64_t>(kk * 2), b0 + static_cast<uint64_t>(kk * 128), id,
+            (accumulate || kk > 0) ? 1u : 0u);
+}
+
+// dQ^T_u = K^T dS^T_u (M = D elements of d, N = 64 queries, K = 128 keys): A = the resident
+// K tile read MN-major (its 64-element regions of d 16 KB apart), B = dS^T_u read MN-major
+// (keys are its rows); 16 keys = 2048 bytes per MMA in both. With D = 64 the accumulator
+// takes the M = 64 layout: row r of dQ^T in TMEM lane 32 (r / 16) + r % 16.
+template <int D, bool BF16>
+__device__ __forceinline__ void issue_dq_half(uint32_t y_tmem, uint32_t k_smem, uint32_t ds) {
+  constexpr uint32_t id = idesc_f16(BF16, D, kHalf, true, true);
+  const uint64_t a0 = smem_desc_sw128(k_smem, kBT * 128, 1024);
+  const uint64_t b0 = smem_desc_sw128(ds, kBT * 128, 1024);
+#pragma unroll
+  for (int kk = 0; kk < kBT / 16; ++kk)
+    umma_ss(y_tmem, a0 + static_cast<uint64_t>(kk * 128), b0 + static_cast<uint64_t>(kk * 128), id,
+            kk > 0 ? 1u : 0u);
 }
 
 // A resident 128-row tile as two 64-row boxes per 64-element region of d (the region's
@@ -295,6 +328,8 @@ __device__ __forceinline__ uint32_t bwd_setup(BwdBars* bars, const CUtensorMap* 
     for (int u = 0; u < 2; ++u) {
       mbar_init(smem_u32(&bars->s_full[u]), 1);
       mbar_init(smem_u32(&bars->p_full[u]), kBwdEwPerHalf);
+      mbar_init(smem_u32(&bars->dq_full[u]), 1);
+      mbar_init(smem_u32(&bars->dq_read[u]), kBwdEwPerHalf);
     }
     mbar_init(smem_u32(&bars->acc_full), 1);
     bars->abort = 0;
@@ -325,9 +360,11 @@ __device__ __forceinline__ void bwd_teardown(uint32_t tmem) {
   }
 }
 
-// dK and dV of one block of 128 keys. TMEM: S^T [0,128) (P^T packed over its first 64
-// columns), dP^T [128,256) (dS^T packed over [128,192)), dV [256,256+D), dK [256+D,256+2D).
-// Shared memory: K, V (resident), then (Q, dO) halves of 64 queries in four stages.
+// dK, dV and the dQ contributions of one block of 128 keys. TMEM: S^T [0,128) (P^T packed
+// over the first 16 of every 32 columns), dP^T [128,256) (dQ^T of half u over [128+64u,
+// 192+64u) once dP^T has been read), dV [256,256+D), dK [256+D,256+2D). Shared memory
+// from a 1024-byte aligned base: K, V (resident), (Q, dO) halves of 64 queries in four
+// stages, dS^T of each half, the stages' statistics, the barriers.
 template <int D, bool BF16>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ,
@@ -339,13 +376,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
+  if (base - raw + C::BODY > static_cast<uint32_t>(C::SMEM)) {  // uniform over the CTA
+    if (threadIdx.x == 0) atomicOr(p.status, FA_DEV_SMEM_BASE);
+    return;
+  }
   uint8_t* smem = smem_raw + (base - raw);
   const uint32_t sK = base, sV = base + C::TILE;
   const uint32_t sSt = base + 2 * C::TILE;  // stage h: Q half at sSt + 2h HTILE, dO half one on
   auto sQh = [&](int h) { return sSt + 2 * h * C::HTILE; };
   auto sdOh = [&](int h) { return sSt + (2 * h + 1) * C::HTILE; };
+  const uint32_t sDS = sSt + kStages * 2 * C::HTILE;  // dS^T of half u at sDS + u DS
   // [stage][LSE2 | D][64]
-  float* stats = reinterpret_cast<float*>(smem + 2 * C::TILE + kStages * 2 * C::HTILE);
+  float* stats = reinterpret_cast<float*>(smem + 2 * C::TILE + kStages * 2 * C::HTILE + 2 * C::DS);
   BwdBars* bars = reinterpret_cast<BwdBars*>(reinterpret_cast<uint8_t*>(stats) + kStages * C::STATS);
   auto B = [&](uint64_t& x) { return smem_u32(&x); };
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -406,25 +448,29 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   } else if (warp == kBwdMmaWarp) {
     // ------------------------------------------------------------ MMA
     const bool leader = elect_one();
-    // Per tile t and half u: wait for P^T_u / dS^T_u, then dV += P^T_u dO_u and
-    // dK += dS^T_u Q_u, release the half's stage, then the scores of half u of the next tile
-    // into the columns just read (MMAs of one thread execute in order). The tensor core works
-    // on one half while the elementwise warps work on the other.
+    // Per tile t and half u: wait for P^T_u / dS^T_u; dV += P^T_u dO_u, dK += dS^T_u Q_u,
+    // release the half's stage, dQ^T_u = K^T dS^T_u over the dP^T_u columns; then S^T_u of
+    // the next tile over the columns that dV has just read (MMAs of one thread execute in
+    // order) and, once the elementwise warps have read dQ^T_u, dP^T_u of the next tile. The
+    // tensor core works on one half while the elementwise warps work on the other.
     bool ok = mbar_wait(B(bars->res_full), 0, wc);
     int qb = ok ? next_qb(-1, kb, bh, p, nqb) : nqb;
-    // S^T_u = K Q_u^T, dP^T_u = V dO_u^T for stream half g (= 2 t + u) once it has landed
-    auto scores = [&](int g, int u) {
+    auto s_half = [&](int g, int u) {  // S^T_u = K Q_u^T once stream half g has landed
       if (!(ok = mbar_wait(B(bars->st_full[stage_of(g)]), stage_parity(g), wc))) return;
       tc_fence_after();
+      if (leader) issue_s_half<D, BF16>(tmem + 64 * u, sK, sQh(stage_of(g)));
+    };
+    auto dp_half = [&](int g, int u) {  // dP^T_u = V dO_u^T (stage g already landed)
       if (leader) {
-        issue_s_half<D, BF16>(tmem + 64 * u, sK, sQh(stage_of(g)));
         issue_s_half<D, BF16>(tmem + 128 + 64 * u, sV, sdOh(stage_of(g)));
         umma_commit(B(bars->s_full[u]));
       }
     };
     if (qb < nqb && ok) {
-      scores(0, 0);
-      if (ok) scores(1, 1);
+      s_half(0, 0);
+      if (ok) dp_half(0, 0);
+      if (ok) s_half(1, 1);
+      if (ok) dp_half(1, 1);
     }
     int t = 0;
     while (qb < nqb && ok) {
@@ -434,11 +480,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (!(ok = mbar_wait(B(bars->p_full[u]), t & 1, wc))) break;
         tc_fence_after();
         if (leader) {
-          issue_pv_half<D, BF16>(tmem + 256, tmem + 64 * u, sdOh(h), t > 0 || u > 0);
-          issue_pv_half<D, BF16>(tmem + 256 + D, tmem + 128 + 64 * u, sQh(h), t > 0 || u > 0);
+          const bool acc = t > 0 || u > 0;
+          issue_pv_half<D, BF16>(tmem + 256, tmem + 64 * u, sdOh(h), acc);
+          issue_dk_half<D, BF16>(tmem + 256 + D, sDS + u * C::DS, sQh(h), acc);
           umma_commit(B(bars->st_empty[h]));  // stage h free once these are done
+          issue_dq_half<D, BF16>(tmem + 128 + 64 * u, sK, sDS + u * C::DS);
+          umma_commit(B(bars->dq_full[u]));
         }
-        if (qn < nqb) scores(g + 2, u);
+        if (qn < nqb) {
+          s_half(g + 2, u);
+          if (!ok || !(ok = mbar_wait(B(bars->dq_read[u]), t & 1, wc))) break;
+          tc_fence_after();
+          dp_half(g + 2, u);
+        }
       }
       qb = qn;
       ++t;
@@ -454,6 +508,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int j = kb * kBT + row;
     const uint32_t t_lane = tmem + (static_cast<uint32_t>((warp % 4) * 32) << 16);
     const uint32_t c_s = 64 * u + 32 * sub;  // this thread's S^T columns; dP^T 128 further
+    // this thread's part of dS^T_u: 16-byte chunks 4 sub .. 4 sub + 3 of key row `row`
+    // (128-byte swizzle: chunk c of row r at position c ^ (r % 8))
+    const uint32_t ds_row = sDS + u * C::DS + row * 128;
+    // its TMEM lane in dQ^T_u is an element of d (with D = 64 only lanes 0-15 of each
+    // quarter hold one), and its columns the same 32 queries
+    const int dcol = D == 128 ? row : (lane < 16 ? (warp % 4) * 16 + lane : -1);
+    float* dq_col = b.dqacc + static_cast<size_t>(bh) * p.Sq * D + (dcol < 0 ? 0 : dcol);
     bool ok = true;
     int t = 0;
     for (int qb = next_qb(-1, kb, bh, p, nqb); qb < nqb && ok; qb = next_qb(qb, kb, bh, p, nqb), ++t) {
@@ -494,11 +555,31 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           dp[e / 2] = BF16 ? cvt_pack_bf16(dv[0], dv[1]) : cvt_pack_f16(dv[0], dv[1]);
           dp[e / 2 + 1] = BF16 ? cvt_pack_bf16(dv[2], dv[3]) : cvt_pack_f16(dv[2], dv[3]);
         }
-        tmem_st16(t_lane + c_s, sv);        // P^T over columns already read
-        tmem_st16(t_lane + 128 + c_s, dp);  // dS^T likewise
+        tmem_st16(t_lane + c_s, sv);  // P^T over columns already read
+#pragma unroll
+        for (int i = 0; i < 4; ++i)   // dS^T into shared memory for the dK and dQ MMAs
+          st_shared_v4(ds_row + ((static_cast<uint32_t>(4 * sub + i) ^ (row & 7)) << 4),
+                       dp[4 * i], dp[4 * i + 1], dp[4 * i + 2], dp[4 * i + 3]);
         tmem_st_wait();
+        fence_proxy_async_smem();  // the MMAs read dS^T through the async proxy
         tc_fence_before();
         mbar_arrive(B(bars->p_full[u]));
+        // this half's dQ^T: read it, hand the columns back, add it into the accumulator
+        ok = mbar_wait(B(bars->dq_full[u]), t & 1, wc);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t dq[32];
+        tmem_ld32(t_lane + 128 + c_s, dq);
+        tmem_ld_wait<32>(dq);
+        tc_fence_before();
+        mbar_arrive(B(bars->dq_read[u]));
+        if (dcol >= 0) {  // for each query: one warp instruction adds 32 consecutive floats
+          const int nq = min(32, p.Sq - m0);
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (e < nq) atomicAdd(dq_col + static_cast<size_t>(m0 + e) * D, __uint_as_float(dq[e]));
+        }
       }
     }
     // epilogue of this thread's key: warpgroups 0, 1 write halves of dV, 2, 3 halves of
@@ -529,171 +610,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   bwd_teardown(tmem);
 }
 
-// dQ of one block of 128 queries. TMEM: S [0,128), dP [128,256) (dS packed over
-// [128,192)), dQ [256,256+D). Shared memory: Q, dO (resident), then (K, V) halves of 64 keys
-// in four stages.
-template <int D, bool BF16>
-__global__ void __launch_bounds__(kBwdThreads, 1)
-    bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                  const __grid_constant__ CUtensorMap tmV,
-                  const __grid_constant__ CUtensorMap tmdO, const PrefillParams p,
-                  const BwdParams b) {
-  using C = BwdCfg<D>;
-  extern __shared__ uint8_t smem_raw[];
-  const uint32_t raw = smem_u32(smem_raw);
-  const uint32_t base = (raw + 1023u) & ~1023u;
-  uint8_t* smem = smem_raw + (base - raw);
-  const uint32_t sQ = base, sdO = base + C::TILE;
-  const uint32_t sSt = base + 2 * C::TILE;  // stage h: K half at sSt + 2h HTILE, V half one on
-  auto sKh = [&](int h) { return sSt + 2 * h * C::HTILE; };
-  auto sVh = [&](int h) { return sSt + (2 * h + 1) * C::HTILE; };
-  BwdBars* bars = reinterpret_cast<BwdBars*>(smem + 2 * C::TILE + kStages * 2 * C::HTILE +
-                                             kStages * C::STATS);
-  auto B = [&](uint64_t& x) { return smem_u32(&x); };
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int nqb = (p.Sq + kBT - 1) / kBT;
-  const int bh = blockIdx.x / nqb, qb = blockIdx.x % nqb;
-  const Range rg = key_range(qb * kBT, min(qb * kBT + kBT, p.Sq), kBT, p.Sk, p, bh);
-  const int n = range_count(rg);
-  const uint32_t tmem = bwd_setup(bars, &tmQ, &tmK, &tmV, &tmdO);
-  const WaitCtx wc{&bars->abort, p.status, p.timeout_ns};
-
-  if (warp == kBwdTmaWarp) {
-    // ------------------------------------------------------------ TMA
-    const bool leader = elect_one();
-    bool ok = true;
-    uint32_t fills[kStages] = {0, 0, 0, 0};
-    if (n > 0) {
-      if (leader) {
-        mbar_arrive_expect_tx(B(bars->res_full), 2 * C::TILE);
-        load_resident<D>(sQ, &tmQ, B(bars->res_full), qb * kBT, bh);
-        load_resident<D>(sdO, &tmdO, B(bars->res_full), qb * kBT, bh);
-      }
-      int nb = -1, g = 0;
-      for (int t = 0; t < n && ok; ++t) {
-        nb = range_next(rg, nb);
-        for (int u = 0; u < 2 && ok; ++u, ++g) {
-          const int h = stage_of(g);
-          if (g >= kStages &&
-              !(ok = mbar_wait(B(bars->st_empty[h]), stage_parity(g - kStages), wc)))
-            break;
-          if (leader) {
-            mbar_arrive_expect_tx(B(bars->st_full[h]), 2 * C::HTILE);
-            load_half<D>(sKh(h), &tmK, B(bars->st_full[h]), nb * kBT + u * kHalf, bh);
-            load_half<D>(sVh(h), &tmV, B(bars->st_full[h]), nb * kBT + u * kHalf, bh);
-          }
-          fills[h] = g / kStages + 1;
-        }
-      }
-      if (!ok) {  // every load issued lands before the CTA exits
-        wait_quiet_b(B(bars->res_full), 0, wc);
-        for (int h = 0; h < kStages; ++h)
-          if (fills[h] > 0) wait_quiet_b(B(bars->st_full[h]), (fills[h] - 1) & 1, wc);
-      }
-    }
-    __syncwarp();
-  } else if (warp == kBwdMmaWarp) {
-    // ------------------------------------------------------------ MMA
-    const bool leader = elect_one();
-    // Per tile t and half u (64 keys): wait for dS_u, dQ += dS_u K_u, release the half's
-    // stage, then the scores of half u of the next tile (as in the dK/dV kernel).
-    bool ok = n == 0 || mbar_wait(B(bars->res_full), 0, wc);
-    // S_u = Q K_u^T, dP_u = dO V_u^T for stream half g (= 2 t + u) once it has landed
-    auto scores = [&](int g, int u) {
-      if (!(ok = mbar_wait(B(bars->st_full[stage_of(g)]), stage_parity(g), wc))) return;
-      tc_fence_after();
-      if (leader) {
-        issue_s_half<D, BF16>(tmem + 64 * u, sQ, sKh(stage_of(g)));
-        issue_s_half<D, BF16>(tmem + 128 + 64 * u, sdO, sVh(stage_of(g)));
-        umma_commit(B(bars->s_full[u]));
-      }
-    };
-    if (n > 0 && ok) {
-      scores(0, 0);
-      if (ok) scores(1, 1);
-    }
-    for (int t = 0; t < n && ok; ++t) {
-      for (int u = 0; u < 2 && ok; ++u) {
-        const int g = 2 * t + u, h = stage_of(g);
-        if (!(ok = mbar_wait(B(bars->p_full[u]), t & 1, wc))) break;
-        tc_fence_after();
-        if (leader) {
-          issue_pv_half<D, BF16>(tmem + 256, tmem + 128 + 64 * u, sKh(h), t > 0 || u > 0);
-          umma_commit(B(bars->st_empty[h]));  // stage h free once this is done
-        }
-        if (t + 1 < n) scores(g + 2, u);
-      }
-    }
-    if (leader) umma_commit(B(bars->acc_full));
-    wait_quiet_b(B(bars->acc_full), 0, wc);
-    __syncwarp();
-  } else {
-    // ------------------------------------------------------------ elementwise + epilogue
-    const int grp = warp / 4;  // 0..3: half u = grp / 2 (64 keys), keys [32 sub, 32 sub + 32)
-    const int u = grp / 2, sub = grp % 2;
-    const int row = (warp % 4) * 32 + lane;  // query row of the tile (= TMEM lane)
-    const int i = qb * kBT + row;
-    const uint32_t t_lane = tmem + (static_cast<uint32_t>((warp % 4) * 32) << 16);
-    const uint32_t c_s = 64 * u + 32 * sub;  // this thread's S columns; dP 128 further
-    const bool in = i < p.Sq;
-    const size_t srow = static_cast<size_t>(bh) * p.Sq + (in ? i : 0);
-    const float l2 = in ? b.lse[srow] * 1.4426950408889634f : 0.f;
-    const float dd = in ? b.dsum[srow] : 0.f;
-    bool ok = true;
-    int nb = -1;
-    for (int t = 0; t < n && ok; ++t) {
-      nb = range_next(rg, nb);
-      {
-        ok = mbar_wait(B(bars->s_full[u]), t & 1, wc);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) break;
-        tc_fence_after();
-        const ColMask cm = key_cols(i, nb * kBT + 64 * u + 32 * sub, p.Sk, p);
-        uint32_t sv[32], dp[32];
-        tmem_ld32(t_lane + c_s, sv);
-        tmem_ld32(t_lane + 128 + c_s, dp);
-        tmem_ld_wait<32>(sv);
-        tmem_ld_tie<32>(dp);
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          float dv[2];
-#pragma unroll
-          for (int w = 0; w < 2; ++w) {
-            const int col = e + w;
-            const bool on = col <= cm.lim && (col >= cm.lo || col < cm.gl);
-            const float pv = on ? ex2_approx(__uint_as_float(sv[e + w]) * p.sl2 - l2) : 0.f;
-            dv[w] = pv * (__uint_as_float(dp[e + w]) - dd);
-          }
-          dp[e / 2] = BF16 ? cvt_pack_bf16(dv[0], dv[1]) : cvt_pack_f16(dv[0], dv[1]);
-        }
-        tmem_st16(t_lane + 128 + c_s, dp);  // dS over this thread's columns already read
-        tmem_st_wait();
-        tc_fence_before();
-        mbar_arrive(B(bars->p_full[u]));
-      }
-    }
-    if (ok) {
-      ok = mbar_wait(B(bars->acc_full), 0, wc);
-      ok = __all_sync(0xffffffffu, ok);
-    }
-    if (ok) {  // the TMEM loads are warp-collective: every lane runs them, valid rows store
-      tc_fence_after();
-      // D/32 chunks of 32 columns over the four warpgroups
-#pragma unroll 1
-      for (int c = grp; c < D / 32; c += 4) {
-        uint32_t q[32];
-        tmem_ld32(t_lane + 256 + c * 32, q);
-        tmem_ld_wait<32>(q);
-        if (n == 0)
-#pragma unroll
-          for (int e = 0; e < 32; ++e) q[e] = 0u;
-        if (in) store_tile_row<D, BF16>(b.dq, srow, q, b.scale, c * 32);
-      }
-    }
-  }
-  bwd_teardown(tmem);
-}
-
 template <int D, bool BF16>
 cudaError_t launch_bwd_t(const BwdLaunch& L, cudaStream_t stream) {
   const int64_t rows = static_cast<int64_t>(L.p.BH) * L.p.Sq;
@@ -701,12 +617,12 @@ cudaError_t launch_bwd_t(const BwdLaunch& L, cudaStream_t stream) {
     const int blocks = static_cast<int>((rows + 63) / 64 < 4096 ? (rows + 63) / 64 : 4096);
     bwd_prep_kernel<D, BF16><<<blocks, 256, 0, stream>>>(
         static_cast<const uint4*>(L.o), static_cast<const uint4*>(L.dout),
-        const_cast<float*>(L.b.dsum), rows);
+        const_cast<float*>(L.b.dsum), reinterpret_cast<float4*>(L.b.dqacc), rows);
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   constexpr int smem = BwdCfg<D>::SMEM;
-  const int nkb = (L.p.Sk + kBT - 1) / kBT, nqb = (L.p.Sq + kBT - 1) / kBT;
+  const int nkb = (L.p.Sk + kBT - 1) / kBT;
   if (nkb > 0) {  // with Sq = 0 it still writes the (zero) gradients of every key
     auto k1 = bwd_dkdv_kernel<D, BF16>;
     if ((e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)))
@@ -714,11 +630,11 @@ cudaError_t launch_bwd_t(const BwdLaunch& L, cudaStream_t stream) {
     k1<<<L.p.BH * nkb, kBwdThreads, smem, stream>>>(L.tmQ, L.tmK, L.tmV, L.tmdO, L.p, L.b);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  if (nqb > 0) {
-    auto k2 = bwd_dq_kernel<D, BF16>;
-    if ((e = cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)))
-      return e;
-    k2<<<L.p.BH * nqb, kBwdThreads, smem, stream>>>(L.tmQ, L.tmK, L.tmV, L.tmdO, L.p, L.b);
+  if (rows > 0) {  // with Sk = 0 the accumulator stays 0 and so does dq
+    const int64_t n8 = rows * D / 8;
+    const int blocks = static_cast<int>((n8 + 255) / 256 < 8192 ? (n8 + 255) / 256 : 8192);
+    bwd_dq_convert_kernel<BF16><<<blocks, 256, 0, stream>>>(
+        reinterpret_cast<const float4*>(L.b.dqacc), static_cast<uint4*>(L.b.dq), L.b.scale, n8);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   return cudaSuccess;

@@ -12,7 +12,9 @@
 namespace fa {
 
 // bits of the device status word
-enum : uint32_t { FA_DEV_TIMEOUT = 1u, FA_DEV_BAD_PAGE = 2u };
+// FA_DEV_SMEM_BASE: a kernel found its dynamic shared memory too far from a 1024-byte
+// boundary for its layout and did nothing.
+enum : uint32_t { FA_DEV_TIMEOUT = 1u, FA_DEV_BAD_PAGE = 2u, FA_DEV_SMEM_BASE = 4u };
 
 struct PrefillParams {
   void* o;            // [B,H,Sq,D] 16-bit (FP32 for FP32 inputs)
@@ -70,6 +72,7 @@ cudaError_t launch_prefill_split(const PrefillLaunch& L, int D, cudaStream_t str
 struct BwdParams {
   const float* lse;   // [B,H,Sq] natural-log LSE of the forward
   const float* dsum;  // [B,H,Sq] D_i = dO_i . O_i (written by the first kernel)
+  float* dqacc;       // [B,H,Sq,d] FP32 dQ accumulator (zeroed by the first kernel)
   void* dq;           // [B,H,Sq,d] 16-bit
   void* dk;           // [B,H,Sk,d]
   void* dv;
