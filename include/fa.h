@@ -177,9 +177,10 @@ int fa_fwd_default_block_m(int mask_mode);
  *   q, o, dout, dq [B, H, Sq, d]; k, v, dk, dv [B, H, Sk, d]: dtype, contiguous, device
  *   lse        [B, H, Sq] float32, the natural-log LSE that fa_fwd returned with o
  *   workspace  device scratch, 16-byte aligned, owned by the caller: an FP32 dq
- *              accumulator [B, H, Sq, d] followed by D [B, H, Sq], i.e. B*H*Sq*(d+1)*4
- *              bytes; fa_bwd_workspace_size(B, H, Sq) returns that size for d = 128, enough
- *              for every supported d. Its contents on entry do not matter.
+ *              accumulator of B*H*ceil(Sq/4)*4*d floats followed by D [B, H, Sq], i.e.
+ *              B*H*(ceil(Sq/4)*4*d + Sq)*4 bytes; fa_bwd_workspace_size(B, H, Sq) returns
+ *              that size for d = 128, enough for every supported d. Its contents on entry
+ *              do not matter.
  *   d, scale, mask_mode / window / n_global, dtype as for fa_fwd; FA_MASK_BLOCK_SPARSE is
  *   FA_ERR_UNSUPPORTED. dq, dk and dv are written (RN from FP32 accumulators); a key no
  *   query sees gets dk = dv = 0, a query that sees no key dq = 0. dq sums the

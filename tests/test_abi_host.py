@@ -236,4 +236,5 @@ def test_bwd_rejects_bad_arguments(L):
     assert call(dout=None) == fa.FA_ERR_INVALID_ARG
     assert call(dk=A + 8) == fa.FA_ERR_INVALID_ARG
     assert call(mode=2, w=0) == fa.FA_ERR_INVALID_ARG
-    assert L.fa_bwd_workspace_size(2, 3, 100) == 2 * 3 * 100 * 129 * 4  # dq accumulator at d = 128, D
+    assert L.fa_bwd_workspace_size(2, 3, 100) == 2 * 3 * (100 * 128 + 100) * 4  # dq accumulator at d = 128, D
+    assert L.fa_bwd_workspace_size(1, 1, 5) == (8 * 128 + 5) * 4  # Sq rounded up to 4 for the accumulator

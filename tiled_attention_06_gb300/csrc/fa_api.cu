@@ -604,10 +604,11 @@ fa_status fa_decode_paged_noalloc(const void* q, const void* k_pages, const void
   return FA_OK;
 }
 
-// Workspace of fa_bwd at head dimension d: the FP32 dQ accumulator [B,H,Sq,d] first, then
-// D [B,H,Sq]; fa_bwd_workspace_size covers the largest supported d.
+// Workspace of fa_bwd at head dimension d: the FP32 dQ accumulator [B*H][ceil(Sq/4)][d][4]
+// first, then D [B,H,Sq]; fa_bwd_workspace_size covers the largest supported d.
 static size_t bwd_workspace_bytes(int B, int H, int Sq, int d) {
-  return static_cast<size_t>(B) * H * (Sq > 0 ? Sq : 1) * (static_cast<size_t>(d) + 1) *
+  const size_t s = Sq > 0 ? static_cast<size_t>(Sq) : 1;
+  return static_cast<size_t>(B) * H * ((s + 3) / 4 * 4 * static_cast<size_t>(d) + s) *
          sizeof(float);
 }
 
@@ -668,7 +669,7 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
   p.timeout_ns = 1000000000ull;
   L.b.lse = lse;
   L.b.dqacc = static_cast<float*>(workspace);
-  L.b.dsum = static_cast<float*>(workspace) + static_cast<size_t>(BH) * Sq * d;
+  L.b.dsum = static_cast<float*>(workspace) + static_cast<size_t>(BH) * ((Sq + 3) / 4) * 4 * d;
   L.b.dq = dq;
   L.b.dk = dk;
   L.b.dv = dv;

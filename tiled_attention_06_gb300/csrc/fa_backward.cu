@@ -8,7 +8,7 @@
 //
 // Three kernels, each step on the tensor cores where it is a contraction:
 //   bwd_prep_kernel   D_i, one FP32 per query row (HBM-bound), and zeros the FP32 dQ
-//                     accumulator of the row.
+//                     accumulator.
 //   bwd_dkdv_kernel   one CTA per (batch*head, block of 128 keys); TMEM lane = key. For
 //                     each block of 128 queries that sees these keys, in two halves of 64
 //                     queries: S^T = K Q^T and dP^T = V dO^T (tcgen05, A and B from shared
@@ -17,8 +17,10 @@
 //                     memory; then dV += P^T dO (A from TMEM), dK += dS^T Q and
 //                     dQ^T = K^T dS^T (A and B from shared memory; TMEM lane = element of
 //                     d), the last added by the elementwise warps into an FP32 dQ
-//                     accumulator in global memory (coalesced reductions, 128 bytes per
-//                     warp instruction).
+//                     accumulator in global memory laid out [B*H][ceil(Sq/4)][d][4] (query
+//                     q, element c at ((q/4) d + c) 4 + q%4), so that one thread adds four
+//                     consecutive queries of its element in one 16-byte reduction and one
+//                     warp instruction covers 512 contiguous bytes.
 //   bwd_dq_convert_kernel  dq = scale * accumulator, rounded to 16 bits (HBM-bound).
 // Each visible (query block, key block) pair is visited once: five products over the
 // visible pairs, none recomputed.
@@ -143,13 +145,20 @@ __device__ __forceinline__ void wait_quiet_b(uint32_t bar, uint32_t parity, cons
 }
 
 // D_i = sum_c dO_ic O_ic in FP32: d/8 lanes per row, one 16-byte load of each per lane,
-// xor-shuffle reduction inside the row's lanes. Each lane also zeros its 8 elements of the
-// row's FP32 dQ accumulator.
+// xor-shuffle reduction inside the row's lanes. The grid also zeros the n4 float4s of the
+// FP32 dQ accumulator.
 template <int D, bool BF16>
 __global__ void __launch_bounds__(256) bwd_prep_kernel(const uint4* __restrict__ o,
                                                        const uint4* __restrict__ dout,
                                                        float* __restrict__ dsum,
-                                                       float4* __restrict__ dqacc, int64_t rows) {
+                                                       float4* __restrict__ dqacc, int64_t rows,
+                                                       int64_t n4) {
+  {
+    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4; i += stride)
+      dqacc[i] = z;
+  }
   constexpr int LPR = D / 8;  // lanes per row
   constexpr int RPW = 32 / LPR;
   const int lane = threadIdx.x % 32;
@@ -174,9 +183,6 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const uint4* __restrict__
         }
         acc += x.x * y.x + x.y * y.y;
       }
-      const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-      dqacc[(row * LPR + lane % LPR) * 2] = z;
-      dqacc[(row * LPR + lane % LPR) * 2 + 1] = z;
     }
 #pragma unroll
     for (int off = LPR / 2; off > 0; off /= 2) acc += __shfl_xor_sync(0xffffffffu, acc, off);
@@ -184,21 +190,39 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const uint4* __restrict__
   }
 }
 
-// dq = scale * accumulator, rounded to 16 bits: eight elements per thread per step.
-template <bool BF16>
+// dq = scale * accumulator, rounded to 16 bits. One thread per (batch*head, group of four
+// queries, eight elements of d): eight float4 loads (128 contiguous bytes of the
+// accumulator), one 16-byte store per query of the group.
+template <int D, bool BF16>
 __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const float4* __restrict__ acc,
                                                              uint4* __restrict__ dq, float scale,
-                                                             int64_t n8) {
+                                                             int Sq, int64_t n) {
+  const int sq4 = (Sq + 3) / 4;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8; i += stride) {
-    const float4 a = acc[2 * i], b = acc[2 * i + 1];
-    const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-    uint32_t pk[4];
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) {
+    const int c8 = static_cast<int>(i % (D / 8));  // elements 8 c8 .. 8 c8 + 7
+    const int64_t grp = i / (D / 8);                // bh * sq4 + q / 4
+    const int q0 = static_cast<int>(grp % sq4) * 4;
+    const int64_t bh = grp / sq4;
+    float v[8][4];
 #pragma unroll
-    for (int e = 0; e < 4; ++e)
-      pk[e] = BF16 ? cvt_pack_bf16(v[2 * e] * scale, v[2 * e + 1] * scale)
-                   : cvt_pack_f16(v[2 * e] * scale, v[2 * e + 1] * scale);
-    dq[i] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+    for (int e = 0; e < 8; ++e) {
+      const float4 a = acc[grp * D + c8 * 8 + e];
+      v[e][0] = a.x;
+      v[e][1] = a.y;
+      v[e][2] = a.z;
+      v[e][3] = a.w;
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if (q0 + j >= Sq) break;
+      uint32_t pk[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        pk[e] = BF16 ? cvt_pack_bf16(v[2 * e][j] * scale, v[2 * e + 1][j] * scale)
+                     : cvt_pack_f16(v[2 * e][j] * scale, v[2 * e + 1][j] * scale);
+      dq[((bh * Sq + q0 + j) * D) / 8 + c8] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+    }
   }
 }
 
@@ -514,7 +538,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // its TMEM lane in dQ^T_u is an element of d (with D = 64 only lanes 0-15 of each
     // quarter hold one), and its columns the same 32 queries
     const int dcol = D == 128 ? row : (lane < 16 ? (warp % 4) * 16 + lane : -1);
-    float* dq_col = b.dqacc + static_cast<size_t>(bh) * p.Sq * D + (dcol < 0 ? 0 : dcol);
+    const int sq4 = (p.Sq + 3) / 4;
+    float* dq_col = b.dqacc + (static_cast<size_t>(bh) * sq4 * D + (dcol < 0 ? 0 : dcol)) * 4;
     bool ok = true;
     int t = 0;
     for (int qb = next_qb(-1, kb, bh, p, nqb); qb < nqb && ok; qb = next_qb(qb, kb, bh, p, nqb), ++t) {
@@ -574,11 +599,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tmem_ld_wait<32>(dq);
         tc_fence_before();
         mbar_arrive(B(bars->dq_read[u]));
-        if (dcol >= 0) {  // for each query: one warp instruction adds 32 consecutive floats
-          const int nq = min(32, p.Sq - m0);
+        if (dcol >= 0) {  // per four queries: one warp instruction adds 512 contiguous bytes
+          const int ng = min(8, (p.Sq - m0 + 3) / 4);  // groups holding a query below Sq
 #pragma unroll
-          for (int e = 0; e < 32; ++e)
-            if (e < nq) atomicAdd(dq_col + static_cast<size_t>(m0 + e) * D, __uint_as_float(dq[e]));
+          for (int e = 0; e < 8; ++e)
+            if (e < ng)
+              red_add_v4_f32(dq_col + static_cast<size_t>(m0 / 4 + e) * D * 4, dq[4 * e],
+                             dq[4 * e + 1], dq[4 * e + 2], dq[4 * e + 3]);
         }
       }
     }
@@ -615,9 +642,10 @@ cudaError_t launch_bwd_t(const BwdLaunch& L, cudaStream_t stream) {
   const int64_t rows = static_cast<int64_t>(L.p.BH) * L.p.Sq;
   if (rows > 0) {
     const int blocks = static_cast<int>((rows + 63) / 64 < 4096 ? (rows + 63) / 64 : 4096);
+    const int64_t n4 = static_cast<int64_t>(L.p.BH) * ((L.p.Sq + 3) / 4) * D;
     bwd_prep_kernel<D, BF16><<<blocks, 256, 0, stream>>>(
         static_cast<const uint4*>(L.o), static_cast<const uint4*>(L.dout),
-        const_cast<float*>(L.b.dsum), reinterpret_cast<float4*>(L.b.dqacc), rows);
+        const_cast<float*>(L.b.dsum), reinterpret_cast<float4*>(L.b.dqacc), rows, n4);
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -631,10 +659,11 @@ cudaError_t launch_bwd_t(const BwdLaunch& L, cudaStream_t stream) {
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (rows > 0) {  // with Sk = 0 the accumulator stays 0 and so does dq
-    const int64_t n8 = rows * D / 8;
-    const int blocks = static_cast<int>((n8 + 255) / 256 < 8192 ? (n8 + 255) / 256 : 8192);
-    bwd_dq_convert_kernel<BF16><<<blocks, 256, 0, stream>>>(
-        reinterpret_cast<const float4*>(L.b.dqacc), static_cast<uint4*>(L.b.dq), L.b.scale, n8);
+    const int64_t n = static_cast<int64_t>(L.p.BH) * ((L.p.Sq + 3) / 4) * (D / 8);
+    const int blocks = static_cast<int>((n + 255) / 256 < 8192 ? (n + 255) / 256 : 8192);
+    bwd_dq_convert_kernel<D, BF16><<<blocks, 256, 0, stream>>>(
+        reinterpret_cast<const float4*>(L.b.dqacc), static_cast<uint4*>(L.b.dq), L.b.scale,
+        L.p.Sq, n);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   return cudaSuccess;

@@ -398,6 +398,15 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                : "memory");
 }
 // Make this thread's shared-memory writes visible to the async proxy (the tensor core).
+// Four FP32 additions to consecutive words of global memory in one reduction (16-byte
+// aligned address; no value returned).
+__device__ __forceinline__ void red_add_v4_f32(float* addr, uint32_t a, uint32_t b, uint32_t c,
+                                               uint32_t d) {
+  asm volatile("red.relaxed.gpu.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "r"(a),
+               "r"(b), "r"(c), "r"(d)
+               : "memory");
+}
+
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
