@@ -190,39 +190,44 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const uint4* __restrict__
   }
 }
 
-// dq = scale * accumulator, rounded to 16 bits. One thread per (batch*head, group of four
-// queries, eight elements of d): eight float4 loads (128 contiguous bytes of the
-// accumulator), one 16-byte store per query of the group.
+// dq = scale * accumulator, rounded to 16 bits. A block takes 32 queries of one (batch,
+// head): it loads their [8 groups][D][4] accumulator floats as contiguous float4s, transposes
+// them through shared memory (one padded row per query) and writes each query's row as
+// 16-byte chunks of 8 elements, consecutive threads on consecutive chunks.
 template <int D, bool BF16>
 __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const float4* __restrict__ acc,
                                                              uint4* __restrict__ dq, float scale,
-                                                             int Sq, int64_t n) {
+                                                             int Sq, int64_t nblk) {
+  constexpr int G = 8;  // groups of four queries per block
+  __shared__ __align__(16) float tile[G * 4][D + 4];  // rows of (D + 4) * 4 bytes: 16-byte aligned
   const int sq4 = (Sq + 3) / 4;
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) {
-    const int c8 = static_cast<int>(i % (D / 8));  // elements 8 c8 .. 8 c8 + 7
-    const int64_t grp = i / (D / 8);                // bh * sq4 + q / 4
-    const int q0 = static_cast<int>(grp % sq4) * 4;
-    const int64_t bh = grp / sq4;
-    float v[8][4];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const float4 a = acc[grp * D + c8 * 8 + e];
-      v[e][0] = a.x;
-      v[e][1] = a.y;
-      v[e][2] = a.z;
-      v[e][3] = a.w;
+  const int per_bh = (sq4 + G - 1) / G;
+  for (int64_t blk = blockIdx.x; blk < nblk; blk += gridDim.x) {
+    const int64_t bh = blk / per_bh;
+    const int g0 = static_cast<int>(blk % per_bh) * G;
+    const int ng = min(G, sq4 - g0);
+    const float4* src = acc + (bh * sq4 + g0) * D;
+    for (int i = threadIdx.x; i < ng * D; i += blockDim.x) {
+      const float4 v = src[i];
+      const int g = i / D, c = i % D;
+      tile[4 * g][c] = v.x;
+      tile[4 * g + 1][c] = v.y;
+      tile[4 * g + 2][c] = v.z;
+      tile[4 * g + 3][c] = v.w;
     }
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      if (q0 + j >= Sq) break;
-      uint32_t pk[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e)
-        pk[e] = BF16 ? cvt_pack_bf16(v[2 * e][j] * scale, v[2 * e + 1][j] * scale)
-                     : cvt_pack_f16(v[2 * e][j] * scale, v[2 * e + 1][j] * scale);
-      dq[((bh * Sq + q0 + j) * D) / 8 + c8] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+    __syncthreads();
+    const int nq = min(G * 4, Sq - g0 * 4);
+    for (int i = threadIdx.x; i < nq * (D / 8); i += blockDim.x) {
+      const int qq = i / (D / 8), c8 = i % (D / 8);
+      const float4 lo = *reinterpret_cast<const float4*>(&tile[qq][8 * c8]);
+      const float4 hi = *reinterpret_cast<const float4*>(&tile[qq][8 * c8 + 4]);
+      const uint32_t p0 = BF16 ? cvt_pack_bf16(lo.x * scale, lo.y * scale) : cvt_pack_f16(lo.x * scale, lo.y * scale);
+      const uint32_t p1 = BF16 ? cvt_pack_bf16(lo.z * scale, lo.w * scale) : cvt_pack_f16(lo.z * scale, lo.w * scale);
+      const uint32_t p2 = BF16 ? cvt_pack_bf16(hi.x * scale, hi.y * scale) : cvt_pack_f16(hi.x * scale, hi.y * scale);
+      const uint32_t p3 = BF16 ? cvt_pack_bf16(hi.z * scale, hi.w * scale) : cvt_pack_f16(hi.z * scale, hi.w * scale);
+      dq[((bh * Sq + g0 * 4 + qq) * D) / 8 + c8] = make_uint4(p0, p1, p2, p3);
     }
+    __syncthreads();
   }
 }
 
@@ -641,7 +646,7 @@ template <int D, bool BF16>
 cudaError_t launch_bwd_t(const BwdLaunch& L, cudaStream_t stream) {
   const int64_t rows = static_cast<int64_t>(L.p.BH) * L.p.Sq;
   if (rows > 0) {
-    const int blocks = static_cast<int>((rows + 63) / 64 < 4096 ? (rows + 63) / 64 : 4096);
+    const int blocks = static_cast<int>((rows + 63) / 64 < 16384 ? (rows + 63) / 64 : 16384);
     const int64_t n4 = static_cast<int64_t>(L.p.BH) * ((L.p.Sq + 3) / 4) * D;
     bwd_prep_kernel<D, BF16><<<blocks, 256, 0, stream>>>(
         static_cast<const uint4*>(L.o), static_cast<const uint4*>(L.dout),
@@ -659,11 +664,11 @@ cudaError_t launch_bwd_t(const BwdLaunch& L, cudaStream_t stream) {
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (rows > 0) {  // with Sk = 0 the accumulator stays 0 and so does dq
-    const int64_t n = static_cast<int64_t>(L.p.BH) * ((L.p.Sq + 3) / 4) * (D / 8);
-    const int blocks = static_cast<int>((n + 255) / 256 < 8192 ? (n + 255) / 256 : 8192);
+    const int64_t nblk = static_cast<int64_t>(L.p.BH) * (((L.p.Sq + 3) / 4 + 7) / 8);
+    const int blocks = static_cast<int>(nblk < 16384 ? nblk : 16384);
     bwd_dq_convert_kernel<D, BF16><<<blocks, 256, 0, stream>>>(
         reinterpret_cast<const float4*>(L.b.dqacc), static_cast<uint4*>(L.b.dq), L.b.scale,
-        L.p.Sq, n);
+        L.p.Sq, nblk);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   return cudaSuccess;
