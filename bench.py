@@ -776,7 +776,9 @@ def timed(calls, K, W, stream, soak_s=CLOCK_SOAK_S):
 
 def run_next_rows(args, fa, workload, peaks, peak_kind, stream, world):
     """chunked: append a 512-token chunk to each of 8 paged sequences (contexts up to
-    7.7k, 256-token pages, fp16) and run its causal prefill through the block table.
+    7.7k, 256-token pages, fp16) and run its causal prefill through the block table, with
+    the lengths also given on the host for the work plan (the call without them is timed
+    beside it).
     multimodal: LLaVA-shaped vision 576 + text 2048 tokens (B=4, H=32, d=128, bf16) as
     three calls (vision full, text causal, text-to-vision) plus the LSE merge; beside it,
     the text rows as one causal call over [vision; text] keys, and the whole layer as one
@@ -811,11 +813,17 @@ def run_next_rows(args, fa, workload, peaks, peak_kind, stream, world):
         o = torch.empty_like(q)
         lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
         scale = 1 / math.sqrt(d)
-        # every step appends the same chunk at the same place, then runs its prefill
+        # every step appends the same chunk at the same place, then runs its prefill; the
+        # lengths are also given on the host, for the work plan
+        ctx_host = torch.tensor(total, dtype=torch.int32)
         ms, clk = timed([lambda: fa.fa_kv_append(kn, vn, kp, vp, tab, c0, stream=stream),
                          lambda: fa.fa_fwd_paged(q, kp, vp, tab, ctx, o, lse, scale,
-                                                 fa.FA_MASK_CAUSAL, stream=stream)], K, W, stream,
+                                                 fa.FA_MASK_CAUSAL, stream=stream,
+                                                 ctx_lens_host=ctx_host)], K, W, stream,
                         args.clock_soak)
+        unplanned, _ = timed([lambda: fa.fa_fwd_paged(q, kp, vp, tab, ctx, o, lse, scale,
+                                                      fa.FA_MASK_CAUSAL, stream=stream)],
+                             K, W, stream, 0.0)
         assert fa.fa_get_device_status() == fa.FA_OK
         pairs = sum(visible_pairs(T, t, 1) for t in total)
         flops = 4.0 * H * d * pairs
@@ -832,6 +840,11 @@ def run_next_rows(args, fa, workload, peaks, peak_kind, stream, world):
                                  "algorithmic_flops": flops},
                     "append": {"value": app_bytes * K / (ms[0] / 1e3) / 1e9, "unit": "GB/s",
                                "ms_per_call": ms[0] / K},
+                    "without_host_lengths": {"value": flops * K / (unplanned[0] / 1e3) / 1e12,
+                                             "unit": "TFLOP/s",
+                                             "api": "fa_fwd_paged (every item weighed by the "
+                                                    "pool capacity)"},
+                    "api": "fa_fwd_paged_host_lens (lengths also on the host for the plan)",
                     "config": {"workload": f"append {T} tokens + causal chunked prefill, B{B} "
                                            f"H{H} d{d} {c['dtype']}, ctx0~U[0,{c['max_ctx0']}], "
                                            f"page {c['page']}, pool {c['pool']}"}})

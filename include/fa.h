@@ -296,6 +296,24 @@ fa_status fa_fwd_paged(const void* q, const void* k_pages, const void* v_pages,
                        int dtype, fa_stream_t stream);
 
 /*
+ * fa_fwd_paged_host_lens - fa_fwd_paged for a caller that also holds the context lengths in
+ * HOST memory: ctx_lens_host[B] (int32, read during the call) should equal ctx_lens on the
+ * device. The lengths on the device still decide what is computed; the host copy only
+ * plans the work, weighing every (sequence, head, query block) item by the keys it visits
+ * and handing the longest items out first, where fa_fwd_paged, which cannot read device
+ * lengths without synchronising, weighs every item by the pool capacity
+ * page_size*max_pages_per_seq. With sequences of different lengths that balances the SMs'
+ * work; the results are the same as fa_fwd_paged's, bit for bit, whatever the host copy
+ * holds (a wrong copy only costs balance). ctx_lens_host = NULL is fa_fwd_paged.
+ */
+fa_status fa_fwd_paged_host_lens(const void* q, const void* k_pages, const void* v_pages,
+                                 const int32_t* block_table, const int32_t* ctx_lens,
+                                 const int32_t* ctx_lens_host, void* o, float* lse, int B, int H,
+                                 int Sq, int d, int page_size, int max_pages_per_seq,
+                                 int num_pages, float scale, int mask_mode, int window,
+                                 int n_global, int dtype, fa_stream_t stream);
+
+/*
  * fa_merge_partials - combine two attention results that cover disjoint key sets of the
  * same queries (for example the text-to-text causal call and the text-to-vision cross
  * call of a multimodal layer). Splitting an attention into such calls is exact

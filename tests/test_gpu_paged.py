@@ -146,3 +146,31 @@ def test_paged_prefill_reports_bad_page():
                     device=dev), o, None, 0.125)
     assert fa.fa_get_device_status() == fa.FA_ERR_BAD_PAGE
     assert fa.fa_get_device_status() == fa.FA_OK
+
+
+@pytest.mark.parametrize("mode,w,g", [(fa.FA_MASK_CAUSAL, 0, 0), (fa.FA_MASK_CAUSAL_WINDOW, 300, 7)])
+def test_host_lengths_plan_gives_the_same_output(mode, w, g):
+    """fa_fwd_paged_host_lens only changes which CTA runs which item: with the right host
+    lengths, with wrong ones and with none, every output bit and LSE bit is the same."""
+    B, H, d, page, chunk = 6, 4, 128, 256, 300
+    ctx0 = [5000, 0, 1200, 3100, 77, 2600]
+    q, kp, vp, table, total, _, _ = build_cache(B, H, d, page, 160, ctx0, chunk,
+                                                torch.bfloat16, seed=7)
+    qd, tab = q.cuda(), table.cuda()
+    ctx = torch.tensor(total, dtype=torch.int32, device="cuda")
+    scale = 1 / math.sqrt(d)
+    outs = []
+    for host in (None, torch.tensor(total, dtype=torch.int32),
+                 torch.tensor([1, 9000, 0, -5, 4000, 300], dtype=torch.int32)):
+        o = torch.empty_like(qd)
+        lse = torch.empty(qd.shape[:3], dtype=torch.float32, device="cuda")
+        fa.fa_fwd_paged(qd, kp, vp, tab, ctx, o, lse, scale, mode, w, g, ctx_lens_host=host)
+        torch.cuda.synchronize()
+        assert fa.fa_get_device_status() == fa.FA_OK
+        outs.append((o, lse))
+    for o, lse in outs[1:]:
+        assert torch.equal(o.view(torch.int16), outs[0][0].view(torch.int16))
+        assert torch.equal(lse.view(torch.int32), outs[0][1].view(torch.int32))
+    with pytest.raises(ValueError):
+        fa.fa_fwd_paged(qd, kp, vp, tab, ctx, outs[0][0], None, scale,
+                        ctx_lens_host=torch.tensor(total[:3], dtype=torch.int32))

@@ -13,7 +13,8 @@ import torch
 
 __all__ = [
     "FaError", "lib", "fa_fwd", "fa_fwd_ex", "fa_decode_paged", "fa_decode_paged_ex",
-    "fa_decode_paged_noalloc", "fa_merge_partials", "fa_fwd_paged", "fa_kv_append",
+    "fa_decode_paged_noalloc", "fa_merge_partials", "fa_fwd_paged", "fa_fwd_paged_host_lens",
+    "fa_kv_append",
     "fa_decode_workspace_size", "fa_decode_default_pages_per_split",
     "fa_get_device_status",
     "fa_selftest_timeout", "fa_last_error_string", "fa_version", "fa_fwd_block_m",
@@ -99,6 +100,8 @@ def lib():
         L.fa_fwd_paged.restype = _i
         L.fa_fwd_paged.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i,
                                    _f, _i, _i, _i, _i, _vp]
+        L.fa_fwd_paged_host_lens.restype = _i
+        L.fa_fwd_paged_host_lens.argtypes = [_vp] * 8 + [_i] * 7 + [_f] + [_i] * 4 + [_vp]
         L.fa_kv_append.restype = _i
         L.fa_kv_append.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i,
                                    _i, _vp]
@@ -294,18 +297,32 @@ def fa_decode_paged_noalloc(q, k_pages, v_pages, block_table, ctx_lens, o, lse, 
 
 
 def fa_fwd_paged(q, k_pages, v_pages, block_table, ctx_lens, o, lse, scale,
-                 mask_mode=FA_MASK_CAUSAL, window=0, n_global=0, stream=None):
+                 mask_mode=FA_MASK_CAUSAL, window=0, n_global=0, stream=None,
+                 ctx_lens_host=None):
     """Chunked prefill against a paged cache: q/o [B,H,Sq,d] are the last Sq tokens of
     each sequence; pools [num_pages,H,page,d]; block_table int32 [B,max_pages];
-    ctx_lens int32 [B] (cached tokens, the chunk included)."""
+    ctx_lens int32 [B] (cached tokens, the chunk included). ctx_lens_host: the same
+    lengths as a CPU int32 tensor, for the work plan (fa_fwd_paged_host_lens)."""
     _need_cuda_contig(q=q, k_pages=k_pages, v_pages=v_pages, block_table=block_table,
                       ctx_lens=ctx_lens, o=o, lse=lse)
     B, H, Sq, d = q.shape
     P, _, page, _ = k_pages.shape
-    _check(lib().fa_fwd_paged(q.data_ptr(), k_pages.data_ptr(), v_pages.data_ptr(),
-                              block_table.data_ptr(), ctx_lens.data_ptr(), o.data_ptr(),
-                              _ptr(lse), B, H, Sq, d, page, block_table.shape[1], P, float(scale),
-                              mask_mode, window, n_global, _dtype_code(q), _stream(stream)))
+    if ctx_lens_host is None:
+        _check(lib().fa_fwd_paged(q.data_ptr(), k_pages.data_ptr(), v_pages.data_ptr(),
+                                  block_table.data_ptr(), ctx_lens.data_ptr(), o.data_ptr(),
+                                  _ptr(lse), B, H, Sq, d, page, block_table.shape[1], P,
+                                  float(scale), mask_mode, window, n_global, _dtype_code(q),
+                                  _stream(stream)))
+        return
+    if (ctx_lens_host.device.type != "cpu" or ctx_lens_host.dtype != torch.int32
+            or not ctx_lens_host.is_contiguous() or ctx_lens_host.numel() != B):
+        raise ValueError("ctx_lens_host must be a contiguous CPU int32 tensor of B entries")
+    _check(lib().fa_fwd_paged_host_lens(q.data_ptr(), k_pages.data_ptr(), v_pages.data_ptr(),
+                                        block_table.data_ptr(), ctx_lens.data_ptr(),
+                                        ctx_lens_host.data_ptr(), o.data_ptr(), _ptr(lse), B, H,
+                                        Sq, d, page, block_table.shape[1], P, float(scale),
+                                        mask_mode, window, n_global, _dtype_code(q),
+                                        _stream(stream)))
 
 
 def fa_kv_append(k_new, v_new, k_pages, v_pages, block_table, ctx_lens, new_lens=None,

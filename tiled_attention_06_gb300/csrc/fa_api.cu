@@ -5,6 +5,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <array>
 #include <cmath>
 #include <cstdarg>
@@ -157,6 +158,49 @@ const fa::PrefillSched* plan_for(const fa::PrefillParams& p, int BM, int BN, int
   return out;
 }
 
+// The same list schedule for a paged prefill whose sequence lengths the caller also gave
+// in host memory: every item is weighed by the key blocks its rows really visit (its
+// sequence's length, clamped to the pool capacity, not the capacity itself) and the items
+// are taken longest first. Only the assignment of items to CTAs changes, so the results are
+// those of the unplanned call. Built per call (it depends on the lengths), into `plan`.
+void plan_with_lengths(const fa::PrefillParams& p, int BM, int BN, int grid,
+                       const int32_t* sk_host, int cap, fa::PrefillSched* plan) {
+  std::memset(plan, 0, sizeof(fa::PrefillSched));
+  if (grid > fa::kSchedMaxCtas || p.total_items > fa::kSchedMaxItems) return;
+  std::vector<std::pair<int, int>> order;  // (cost, item)
+  order.reserve(p.total_items);
+  for (int t = 0; t < p.total_items; ++t) {
+    int bh, mb;
+    fa::item_coords(t, p, bh, mb);
+    const int len = sk_host[bh / p.H];
+    const int sk = len < 0 ? 0 : (len > cap ? cap : len);
+    const fa::Range r = fa::key_range(mb * BM, std::min(mb * BM + BM, p.Sq), BN, sk, p, 0);
+    order.push_back({fa::range_count(r), t});
+  }
+  std::stable_sort(order.begin(), order.end(),
+                   [](const std::pair<int, int>& x, const std::pair<int, int>& y) {
+                     return x.first > y.first;
+                   });
+  using Slot = std::pair<double, int>;  // (busy until, cta)
+  std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> free_at;
+  for (int c = 0; c < grid; ++c) free_at.push({0.0, c});
+  std::vector<std::vector<uint16_t>> lists(grid);
+  for (const auto& ct : order) {
+    Slot sl = free_at.top();
+    free_at.pop();
+    lists[sl.second].push_back(static_cast<uint16_t>(ct.second));
+    sl.first += ct.first + kItemOverheadTiles;
+    free_at.push(sl);
+  }
+  int k = 0;
+  for (int c = 0; c < grid; ++c) {
+    plan->offs[c] = static_cast<uint16_t>(k);
+    for (uint16_t t : lists[c]) plan->items[k++] = t;
+  }
+  plan->offs[grid] = static_cast<uint16_t>(k);
+  plan->enabled = 1;
+}
+
 size_t fwd_workspace_bytes(int B, int H, int Sq, int Sk, int d, int dtype) {
   if (dtype != FA_F32 || B < 1 || H < 1 || Sq < 0 || Sk < 0 || d < 1) return 0;
   // a bf16 high and low plane of every Q, K and V element
@@ -251,7 +295,8 @@ struct PagedKV {
 
 // Plan and launch one prefill. `a` has passed check_fwd; with `pg` set, a.Sk is the
 // table's capacity and K/V come from the pools.
-fa_status run_fwd(const fa_fwd_params& a, const PagedKV* pg, fa_stream_t stream) {
+fa_status run_fwd(const fa_fwd_params& a, const PagedKV* pg, fa_stream_t stream,
+                  const int32_t* sk_host = nullptr) {
   fa_status st;
   if (a.Sq == 0) return FA_OK;  // nothing to compute
   DeviceInfo dev;
@@ -304,7 +349,14 @@ fa_status run_fwd(const fa_fwd_params& a, const PagedKV* pg, fa_stream_t stream)
   }
   L.grid = a.num_ctas ? a.num_ctas : dev.sms;
   if (L.grid > p.total_items) L.grid = p.total_items;
-  L.sched = plan_for(p, BM, BN, L.grid);
+  if (pg && sk_host) {  // the launch copies the plan, so one buffer per thread is enough
+    static thread_local std::unique_ptr<fa::PrefillSched> hinted;
+    if (!hinted) hinted = std::make_unique<fa::PrefillSched>();
+    plan_with_lengths(p, BM, BN, L.grid, sk_host, a.Sk, hinted.get());
+    L.sched = hinted.get();
+  } else {
+    L.sched = plan_for(p, BM, BN, L.grid);
+  }
 
   const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   if (f32) {
@@ -368,11 +420,12 @@ fa_status fa_fwd_ex(const fa_fwd_params* params, fa_stream_t stream) {
   return run_fwd(*params, nullptr, stream);
 }
 
-fa_status fa_fwd_paged(const void* q, const void* k_pages, const void* v_pages,
-                       const int32_t* block_table, const int32_t* ctx_lens, void* o, float* lse,
-                       int B, int H, int Sq, int d, int page_size, int max_pages_per_seq,
-                       int num_pages, float scale, int mask_mode, int window, int n_global,
-                       int dtype, fa_stream_t stream) {
+static fa_status fwd_paged(const void* q, const void* k_pages, const void* v_pages,
+                           const int32_t* block_table, const int32_t* ctx_lens,
+                           const int32_t* ctx_lens_host, void* o, float* lse, int B, int H,
+                           int Sq, int d, int page_size, int max_pages_per_seq, int num_pages,
+                           float scale, int mask_mode, int window, int n_global, int dtype,
+                           fa_stream_t stream) {
   if (!k_pages || !v_pages || !block_table || !ctx_lens)
     return fail(FA_ERR_INVALID_ARG, "k_pages, v_pages, block_table and ctx_lens must be non-null");
   if (!aligned16(k_pages) || !aligned16(v_pages))
@@ -410,7 +463,28 @@ fa_status fa_fwd_paged(const void* q, const void* k_pages, const void* v_pages,
   if (st != FA_OK) return st;
   const PagedKV pg{k_pages, v_pages, block_table, ctx_lens, page_size, max_pages_per_seq,
                    num_pages};
-  return run_fwd(a, &pg, stream);
+  return run_fwd(a, &pg, stream, ctx_lens_host);
+}
+
+fa_status fa_fwd_paged(const void* q, const void* k_pages, const void* v_pages,
+                       const int32_t* block_table, const int32_t* ctx_lens, void* o, float* lse,
+                       int B, int H, int Sq, int d, int page_size, int max_pages_per_seq,
+                       int num_pages, float scale, int mask_mode, int window, int n_global,
+                       int dtype, fa_stream_t stream) {
+  return fwd_paged(q, k_pages, v_pages, block_table, ctx_lens, nullptr, o, lse, B, H, Sq, d,
+                   page_size, max_pages_per_seq, num_pages, scale, mask_mode, window, n_global,
+                   dtype, stream);
+}
+
+fa_status fa_fwd_paged_host_lens(const void* q, const void* k_pages, const void* v_pages,
+                                 const int32_t* block_table, const int32_t* ctx_lens,
+                                 const int32_t* ctx_lens_host, void* o, float* lse, int B, int H,
+                                 int Sq, int d, int page_size, int max_pages_per_seq,
+                                 int num_pages, float scale, int mask_mode, int window,
+                                 int n_global, int dtype, fa_stream_t stream) {
+  return fwd_paged(q, k_pages, v_pages, block_table, ctx_lens, ctx_lens_host, o, lse, B, H, Sq,
+                   d, page_size, max_pages_per_seq, num_pages, scale, mask_mode, window,
+                   n_global, dtype, stream);
 }
 
 fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
