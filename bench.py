@@ -333,11 +333,13 @@ def run_ours(args, rank, world):
         dbytes = decode_bytes(di.ctx_lens.tolist(), DECODE["B"], DECODE["H"], DECODE["d"], mp)
         dscale = 1 / math.sqrt(DECODE["d"])
 
-    def prefill_call(**ex):
+    def prefill_call(host_layout=True, **ex):
         if args.block_m and "block_m" not in ex:
             ex["block_m"] = args.block_m
         if lay_d is not None:
             ex["block_layout"] = lay_d
+            if host_layout:  # the layout also on the host, for the work plan
+                ex["block_layout_host"] = layout
         if ws32 is not None:
             ex["workspace"] = ws32
         if ex:
@@ -462,6 +464,17 @@ def run_ours(args, rank, world):
             res.update({"metric": "paged decode HBM GB/s (% of 8 TB/s)", "value": dval,
                         "unit": "GB/s", "higher_is_better": True, "dtype": "f16",
                         "roofline": dec["roofline"]})
+    if lay_d is not None:  # the same calls planned without the host copy of the layout
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(K):
+            prefill_call(host_layout=False)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        res["without_host_layout"] = {"value": pflops * K / (e0.elapsed_time(e1) / 1e3) / 1e12,
+                                      "unit": "TFLOP/s",
+                                      "api": "fa_fwd_ex without block_layout_host (every item "
+                                             "planned as dense)"}
     res["config"] = workload_config(pcfg, with_decode, world)
 
     # ---- end to end through the public API with host buffers
@@ -587,7 +600,7 @@ def e2e_prefill(fa, pcfg, q, k, v, pflops, scale, stream, world, args, layout=No
             stream.wait_event(out_done[n])  # this set's O and LSE have been copied out
         if hlay is not None:
             fa.fa_fwd_ex(b["q"], b["k"], b["v"], b["o"], b["l"], scale, pcfg["mode"],
-                         block_layout=b["lay"], stream=stream)
+                         block_layout=b["lay"], block_layout_host=hlay, stream=stream)
         elif ws32 is not None:
             fa.fa_fwd_ex(b["q"], b["k"], b["v"], b["o"], b["l"], scale, pcfg["mode"],
                          pcfg["window"], pcfg["n_global"], workspace=ws32, stream=stream)

@@ -148,6 +148,12 @@ typedef struct fa_fwd_params {
    * rescaled (the correction step of the per-block (m, l, O) recurrence, zwxr.cn article
    * on ops-transformer, section 3.1). For tests: it shows which inputs reach that step. */
   int32_t* rescale_count;
+  /* Optional, FA_MASK_BLOCK_SPARSE: the same layout as block_layout in HOST memory (read
+   * during the call). The device layout decides what is computed; this copy only plans the
+   * work, weighing every work item by the key blocks its rows visit and handing the longest
+   * items out first, where without it every item is weighed as dense. Results are the same,
+   * bit for bit, whatever it holds (a wrong copy only costs balance). */
+  const uint8_t* block_layout_host;
 } fa_fwd_params;
 
 fa_status fa_fwd_ex(const fa_fwd_params* params, fa_stream_t stream);

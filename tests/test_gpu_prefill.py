@@ -248,6 +248,24 @@ def test_block_sparse_trace_is_bit_exact(bn, bm):
     compare(o, lse, ref_o, ref_l, "block-sparse trace case")
 
 
+@pytest.mark.parametrize("bm", [64, 128, 256])
+def test_block_sparse_host_layout_plan_gives_the_same_output(bm):
+    """block_layout_host only changes which CTA runs which item: with the right host copy,
+    a wrong one and none, every output bit and LSE bit is the same."""
+    B, H, Sq, Sk, d = 2, 3, 1100, 900, 128
+    q, k, v = inputs.prefill_inputs(B, H, Sq, Sk, d, torch.bfloat16, seed=41)
+    lay = _layout(H, Sq, Sk, seed=5, density=0.3)
+    lay[1, 2, :] = 1  # one query block of head 1 sees every key block
+    wrong = torch.flip(lay, dims=[1]).contiguous()
+    outs = [run_sparse(q, k, v, 0.1, lay, block_m=bm, **ex)
+            for ex in ({}, {"block_layout_host": lay}, {"block_layout_host": wrong})]
+    for o, lse in outs[1:]:
+        assert torch.equal(o.view(torch.int16), outs[0][0].view(torch.int16))
+        assert torch.equal(lse.view(torch.int32), outs[0][1].view(torch.int32))
+    with pytest.raises(ValueError):
+        run_sparse(q, k, v, 0.1, lay, block_layout_host=lay[:, :-1].contiguous())
+
+
 def test_block_sparse_4k_bigbird_sampled():
     """The bench's block-sparse configuration: B=4, H=32, S=4096, d=128, bf16 with the
     seeded BigBird-shaped layout; sampled rows of every head."""
@@ -255,7 +273,7 @@ def test_block_sparse_4k_bigbird_sampled():
     q, k, v = inputs.prefill_inputs(B, H, S, S, d, torch.bfloat16, seed=0)
     lay = inputs.block_layout(H, S, S)
     scale = 1 / math.sqrt(d)
-    o, lse = run_sparse(q, k, v, scale, lay)
+    o, lse = run_sparse(q, k, v, scale, lay, block_layout_host=lay)
     rows = sample_rows(B, H, S, fa.fa_fwd_block_m(), n_random=128, seed=3)
     ref_o, ref_l = oracle.attention_layout(q, k, v, scale, lay.numpy(), rows=rows)
     compare(pick_rows(o, rows, S), pick_rows(lse, rows, S), ref_o, ref_l, "block-sparse 4k")

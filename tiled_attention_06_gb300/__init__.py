@@ -53,7 +53,7 @@ class FwdParams(ctypes.Structure):
                 ("block_n", _i), ("block_m", _i), ("num_ctas", _i), ("group_heads", _i),
                 ("timeout_us", _u32),
                 ("trace", _vp), ("block_layout", _vp), ("workspace", _vp),
-                ("workspace_bytes", _sz), ("rescale_count", _vp)]
+                ("workspace_bytes", _sz), ("rescale_count", _vp), ("block_layout_host", _vp)]
 
 
 class DecodeParams(ctypes.Structure):
@@ -217,9 +217,11 @@ def fa_fwd(q, k, v, o, lse, scale, mask_mode=FA_MASK_NONE, window=0, n_global=0,
 
 def fa_fwd_ex(q, k, v, o, lse, scale, mask_mode=FA_MASK_NONE, window=0, n_global=0,
               block_n=0, block_m=0, num_ctas=0, group_heads=0, timeout_us=0, trace=None,
-              block_layout=None, workspace=None, rescale_count=None, stream=None):
+              block_layout=None, workspace=None, rescale_count=None, stream=None,
+              block_layout_host=None):
     """fa_fwd with the tuning and debug fields of fa_fwd_params. block_layout: uint8 CUDA
-    tensor [H, ceil(Sq/128), ceil(Sk/128)] for FA_MASK_BLOCK_SPARSE. workspace: CUDA byte
+    tensor [H, ceil(Sq/128), ceil(Sk/128)] for FA_MASK_BLOCK_SPARSE; block_layout_host:
+    the same layout as a contiguous CPU uint8 tensor, for the work plan. workspace: CUDA byte
     tensor of fa_fwd_workspace_size(...) bytes for float32 inputs (allocated here when
     None). rescale_count: zeroed int32 CUDA tensor [B*H, ceil(Sq/128)] that counts the
     rows whose output was rescaled, per 128-query tile."""
@@ -231,10 +233,17 @@ def fa_fwd_ex(q, k, v, o, lse, scale, mask_mode=FA_MASK_NONE, window=0, n_global
         workspace = torch.empty(max(fa_fwd_workspace_size(B, H, Sq, k.shape[2], d, dt), 16),
                                 dtype=torch.uint8, device=q.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    if block_layout_host is not None:
+        want = (H, -(-Sq // 128), -(-k.shape[2] // 128))
+        if (block_layout_host.device.type != "cpu" or block_layout_host.dtype != torch.uint8
+                or not block_layout_host.is_contiguous()
+                or tuple(block_layout_host.shape) != want):
+            raise ValueError(f"block_layout_host must be a contiguous CPU uint8 tensor {want}")
     p = FwdParams(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), _ptr(lse), B, H, Sq,
                   k.shape[2], d, float(scale), mask_mode, window, n_global, dt,
                   block_n, block_m, num_ctas, group_heads, timeout_us, _ptr(trace),
-                  _ptr(block_layout), _ptr(workspace), ws_bytes, _ptr(rescale_count))
+                  _ptr(block_layout), _ptr(workspace), ws_bytes, _ptr(rescale_count),
+                  None if block_layout_host is None else block_layout_host.data_ptr())
     _check(lib().fa_fwd_ex(ctypes.byref(p), _stream(stream)))
 
 
