@@ -75,6 +75,10 @@ def lib():
         L.or_attention_backward.argtypes = [_vp, _vp, _vp, _vp, ctypes.c_int, _vp, _vp, _vp,
                                             _i64, _i64, _i64, _i64, _i64, ctypes.c_double,
                                             ctypes.c_int, _i64, _i64, ctypes.c_int]
+        L.or_attention_backward_layout.restype = ctypes.c_int
+        L.or_attention_backward_layout.argtypes = [_vp, _vp, _vp, _vp, ctypes.c_int, _vp, _vp,
+                                                   _vp, _i64, _i64, _i64, _i64, _i64,
+                                                   ctypes.c_double, _vp, _i64, ctypes.c_int]
         L.or_decode_split_tokens.restype = None
         L.or_decode_split_tokens.argtypes = [_i64, _i64, _i64, _i64,
                                              ctypes.POINTER(_i64), ctypes.POINTER(_i64)]
@@ -300,6 +304,26 @@ def count_visible_layout(H, Sq, Sk, layout, blk=128):
 def tile_class_layout(h, mb, nb, BM, BN, Sq, Sk, layout, blk=128):
     lay = _layout(layout, layout.shape[0], Sq, Sk, blk)
     return int(lib().or_tile_class_layout(h, mb, nb, BM, BN, Sq, Sk, lay.ctypes.data, blk))
+
+
+def attention_backward_layout(q, k, v, dout, scale, layout, blk=128, nthreads=0):
+    """Gradients (dq, dk, dv) in float64 of block-sparse attention (layout as in
+    attention_layout) for the upstream gradient dout."""
+    q, k, v, dout = _cpu(q), _cpu(k), _cpu(v), _cpu(dout)
+    B, H, Sq, d = q.shape
+    Sk = k.shape[2]
+    lay = _layout(layout, H, Sq, Sk, blk)
+    dq = np.zeros((B, H, Sq, d))
+    dk = np.zeros((B, H, Sk, d))
+    dv = np.zeros((B, H, Sk, d))
+    rc = lib().or_attention_backward_layout(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                            dout.data_ptr(), _dtype_code(q, k, v, dout),
+                                            dq.ctypes.data, dk.ctypes.data, dv.ctypes.data, B, H,
+                                            Sq, Sk, d, float(scale), lay.ctypes.data, blk,
+                                            nthreads)
+    if rc != 0:
+        raise ValueError("or_attention_backward_layout rejected its arguments")
+    return dq, dk, dv
 
 
 def attention_backward(q, k, v, dout, scale, mask_mode=MASK_NONE, window=0, n_global=0,

@@ -44,6 +44,11 @@
  *                          FP64, by torch autograd on SDPA in float64 with an explicit
  *                          mask, and by closed forms (zero queries: dK = 0; a row with one
  *                          visible key: dQ = 0; rows of dS sum to 0)
+ *   or_attention_backward_layout
+ *                          pinned by torch autograd on SDPA in float64 with the layout
+ *                          expanded into an explicit mask, against or_attention_backward
+ *                          (block 1 with a lower-triangular layout = causal), and per head
+ *                          (heads with different layouts)
  */
 #include "fa_oracle.h"
 
@@ -815,15 +820,12 @@ int or_tile_class_layout(int64_t h, int64_t mb, int64_t nb, int64_t BM, int64_t 
  * Inputs q, k, v, dout share one dtype; dq [B,H,Sq,d], dk and dv [B,H,Sk,d] are FP64.
  * A row that sees no key contributes nothing. Returns 0, or -1 on a bad argument.
  */
-int or_attention_backward(const void* q, const void* k, const void* v, const void* dout,
-                          int dtype, double* dq, double* dk, double* dv, int64_t B, int64_t H,
-                          int64_t Sq, int64_t Sk, int64_t d, double scale, int mask_mode,
-                          int64_t window, int64_t n_global, int nthreads) {
-    if (B < 0 || H < 0 || Sq < 0 || Sk < 0 || d <= 0) return -1;
-    if (mask_mode < OR_MASK_NONE || mask_mode > OR_MASK_PREFIX_LM) return -1;
-    if (mask_mode == OR_MASK_CAUSAL_WINDOW && (window < 1 || n_global < 0)) return -1;
-    if (mask_mode == OR_MASK_BAND && window < 0) return -1;
-    if (mask_mode == OR_MASK_PREFIX_LM && n_global < 0) return -1;
+static int backward_impl(const void* q, const void* k, const void* v, const void* dout,
+                         int dtype, double* dq, double* dk, double* dv, int64_t B, int64_t H,
+                         int64_t Sq, int64_t Sk, int64_t d, double scale, int mask_mode,
+                         int64_t window, int64_t n_global, const unsigned char* layout,
+                         int64_t blk, int nthreads) {
+    const int64_t lnq = layout ? (Sq + blk - 1) / blk : 0, lnk = layout ? (Sk + blk - 1) / blk : 0;
     memset(dq, 0, sizeof(double) * (size_t)(B * H * Sq * d));
     memset(dk, 0, sizeof(double) * (size_t)(B * H * Sk * d));
     memset(dv, 0, sizeof(double) * (size_t)(B * H * Sk * d));
@@ -858,7 +860,10 @@ int or_attention_backward(const void* q, const void* k, const void* v, const voi
                 int64_t n = 0;
                 double m = -INFINITY;
                 for (int64_t j = 0; j < Sk; ++j) {
-                    if (!or_visible(i, j, Sq, Sk, mask_mode, window, n_global)) continue;
+                    const int seen =
+                        layout ? layout[((bh % H) * lnq + i / blk) * lnk + j / blk] != 0
+                               : or_visible(i, j, Sq, Sk, mask_mode, window, n_global);
+                    if (!seen) continue;
                     double dot = 0.0;
                     for (int64_t c = 0; c < d; ++c) dot += qi[c] * kd[j * d + c];
                     vis[n] = j;
@@ -899,4 +904,31 @@ int or_attention_backward(const void* q, const void* k, const void* v, const voi
         free(vis);
     }
     return 0;
+}
+
+int or_attention_backward(const void* q, const void* k, const void* v, const void* dout,
+                          int dtype, double* dq, double* dk, double* dv, int64_t B, int64_t H,
+                          int64_t Sq, int64_t Sk, int64_t d, double scale, int mask_mode,
+                          int64_t window, int64_t n_global, int nthreads) {
+    if (B < 0 || H < 0 || Sq < 0 || Sk < 0 || d <= 0) return -1;
+    if (mask_mode < OR_MASK_NONE || mask_mode > OR_MASK_PREFIX_LM) return -1;
+    if (mask_mode == OR_MASK_CAUSAL_WINDOW && (window < 1 || n_global < 0)) return -1;
+    if (mask_mode == OR_MASK_BAND && window < 0) return -1;
+    if (mask_mode == OR_MASK_PREFIX_LM && n_global < 0) return -1;
+    return backward_impl(q, k, v, dout, dtype, dq, dk, dv, B, H, Sq, Sk, d, scale, mask_mode,
+                         window, n_global, NULL, 1, nthreads);
+}
+
+/*
+ * The same gradients under a block layout (as or_attention_layout): query i of head h sees
+ * key j iff layout[h][i / blk][j / blk] != 0, layout uint8 [H][ceil(Sq/blk)][ceil(Sk/blk)].
+ * Returns 0, or -1 on a bad argument.
+ */
+int or_attention_backward_layout(const void* q, const void* k, const void* v, const void* dout,
+                                 int dtype, double* dq, double* dk, double* dv, int64_t B,
+                                 int64_t H, int64_t Sq, int64_t Sk, int64_t d, double scale,
+                                 const unsigned char* layout, int64_t blk, int nthreads) {
+    if (B < 0 || H < 0 || Sq < 0 || Sk < 0 || d <= 0 || blk < 1 || !layout) return -1;
+    return backward_impl(q, k, v, dout, dtype, dq, dk, dv, B, H, Sq, Sk, d, scale, OR_MASK_NONE,
+                         0, 0, layout, blk, nthreads);
 }

@@ -97,6 +97,10 @@ int or_attention_backward(const void* q, const void* k, const void* v, const voi
                           int dtype, double* dq, double* dk, double* dv, int64_t B, int64_t H,
                           int64_t Sq, int64_t Sk, int64_t d, double scale, int mask_mode,
                           int64_t window, int64_t n_global, int nthreads);
+int or_attention_backward_layout(const void* q, const void* k, const void* v, const void* dout,
+                                 int dtype, double* dq, double* dk, double* dv, int64_t B,
+                                 int64_t H, int64_t Sq, int64_t Sk, int64_t d, double scale,
+                                 const unsigned char* layout, int64_t blk, int nthreads);
 
 void or_combine_partials(const double* m, const double* l, const double* acc,
                          int64_t nsplit, int64_t d, double* o, double* lse);

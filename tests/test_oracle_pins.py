@@ -860,3 +860,43 @@ def test_rescale_events_threshold_limits():
     assert counts.sum() == 0
     with pytest.raises(ValueError):
         oracle.rescale_events(q, k, 0.125, 32, 0.0)
+
+
+@pytest.mark.parametrize("Sq,Sk,blk", [(40, 40, 8), (33, 70, 16), (70, 33, 16)])
+def test_backward_layout_matches_autograd_with_expanded_mask(Sq, Sk, blk):
+    """Block-sparse gradients against torch autograd on float64 SDPA with the layout blown up
+    into one flag per (query, key); the heads have different layouts and one query block of
+    head 0 sees nothing."""
+    H = 3
+    gen = torch.Generator().manual_seed(Sq * 7 + Sk)
+    q, k, v, do = (torch.randn(2, H, n, 16, generator=gen).to(torch.float16)
+                   for n in (Sq, Sk, Sk, Sq))
+    lay = _rand_layout(H, Sq, Sk, blk, seed=Sq * Sk, density=0.5)
+    lay[0, 0, :] = 0
+    dq, dk, dv = oracle.attention_backward_layout(q, k, v, do, 0.3, lay, blk=blk)
+    full = np.stack([np.kron(lay[h], np.ones((blk, blk), dtype=np.uint8))[:Sq, :Sk]
+                     for h in range(H)]).astype(bool)
+    mask = torch.from_numpy(full)[None].expand(2, H, Sq, Sk)
+    seen = mask.any(-1)
+    qq, kk, vv = (t.double().requires_grad_() for t in (q, k, v))
+    o = torch.nn.functional.scaled_dot_product_attention(qq, kk, vv, attn_mask=mask, scale=0.3)
+    o = torch.where(seen[..., None], o, torch.zeros_like(o))
+    o.backward(do.double())
+    for got, ref in ((dq, qq.grad), (dk, kk.grad), (dv, vv.grad)):
+        ref = torch.nan_to_num(ref, nan=0.0).numpy()
+        np.testing.assert_allclose(got, ref, rtol=0, atol=1e-12)
+    assert np.all(dq[:, 0, :blk] == 0)  # the query block that sees nothing
+
+
+def test_backward_layout_block1_tril_is_causal_per_head():
+    """Block 1: a lower-triangular layout gives the causal gradients and an all-ones layout
+    the unmasked ones, each for its own head."""
+    S, H = 12, 2
+    gen = torch.Generator().manual_seed(3)
+    q, k, v, do = (torch.randn(1, H, S, 8, generator=gen).to(torch.bfloat16) for _ in range(4))
+    lay = np.stack([np.ones((S, S), dtype=np.uint8), np.tril(np.ones((S, S), dtype=np.uint8))])
+    got = oracle.attention_backward_layout(q, k, v, do, 0.5, lay, blk=1)
+    dense = oracle.attention_backward(q, k, v, do, 0.5, MASK_NONE)
+    causal = oracle.attention_backward(q, k, v, do, 0.5, MASK_CAUSAL)
+    for g_, d_, c_ in zip(got, dense, causal):
+        assert np.array_equal(g_[:, 0], d_[:, 0]) and np.array_equal(g_[:, 1], c_[:, 1])
