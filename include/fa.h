@@ -187,9 +187,10 @@ int fa_fwd_default_block_m(int mask_mode);
  *              B*H*(ceil(Sq/4)*4*d + Sq)*4 bytes; fa_bwd_workspace_size(B, H, Sq) returns
  *              that size for d = 128, enough for every supported d. Its contents on entry
  *              do not matter.
- *   d, scale, mask_mode / window / n_global, dtype as for fa_fwd; FA_MASK_BLOCK_SPARSE is
- *   FA_ERR_UNSUPPORTED. dq, dk and dv are written (RN from FP32 accumulators); a key no
- *   query sees gets dk = dv = 0, a query that sees no key dq = 0. dq sums the
+ *   d, scale, mask_mode / window / n_global, dtype as for fa_fwd; FA_MASK_BLOCK_SPARSE goes
+ *   through fa_bwd_block_sparse (here it is FA_ERR_UNSUPPORTED). dq, dk and dv are written
+ *   (RN from FP32 accumulators); a key no query sees gets dk = dv = 0, a query that sees no
+ *   key dq = 0. dq sums the
  *   contributions of the key blocks with FP32 atomic additions, so its last bit can differ
  *   between runs; dk and dv are the same on every run.
  */
@@ -198,6 +199,18 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
                  const float* lse, void* dq, void* dk, void* dv, void* workspace,
                  size_t workspace_bytes, int B, int H, int Sq, int Sk, int d, float scale,
                  int mask_mode, int window, int n_global, int dtype, fa_stream_t stream);
+
+/*
+ * fa_bwd_block_sparse - fa_bwd under FA_MASK_BLOCK_SPARSE: block_layout is the device layout
+ * of the forward call, uint8 [H][ceil(Sq/128)][ceil(Sk/128)] (query i of head h sees key j
+ * iff block_layout[h][i/128][j/128] != 0; read during the call). Every other argument as for
+ * fa_bwd. A key no query sees gets dk = dv = 0, a query that sees no key dq = 0.
+ */
+fa_status fa_bwd_block_sparse(const void* q, const void* k, const void* v, const void* o,
+                              const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                              void* workspace, size_t workspace_bytes, int B, int H, int Sq,
+                              int Sk, int d, float scale, const uint8_t* block_layout, int dtype,
+                              fa_stream_t stream);
 
 /*
  * fa_decode_paged - one query token per sequence against a paged KV cache

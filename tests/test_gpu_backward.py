@@ -105,3 +105,45 @@ def test_backward_causal_2k_full():
     q, k, v = inputs.prefill_inputs(1, 2, 2048, 2048, 128, torch.bfloat16, seed=0)
     dout = inputs.prefill_inputs(1, 2, 2048, 2048, 128, torch.bfloat16, seed=1)[0]
     check(q, k, v, dout, 1 / math.sqrt(128), "causal", "causal 2k")
+
+
+def _layout(H, Sq, Sk, seed, density=0.4):
+    g = torch.Generator().manual_seed(seed)
+    nq, nk = -(-Sq // fa.FA_LAYOUT_BLOCK), -(-Sk // fa.FA_LAYOUT_BLOCK)
+    lay = (torch.rand(H, nq, nk, generator=g) < density).to(torch.uint8)
+    lay[0, 0, :] = 0          # a query block of head 0 sees nothing
+    lay[-1, -1, :] = 1        # a query block of the last head sees every key block but one:
+    lay[-1, :, 0] = 0         # key block 0 of the last head, which no query sees
+    return lay
+
+
+@pytest.mark.parametrize("Sq,Sk", [(127, 129), (200, 333), (384, 384), (520, 257)])
+@pytest.mark.parametrize("d,dt", [(64, "f16"), (128, "bf16")])
+def test_backward_block_sparse(Sq, Sk, d, dt):
+    """fa_bwd_block_sparse against the oracle's backward under the same layout; exact zeros
+    for the query block that sees nothing and the key block no query sees."""
+    B, H = 2, 3
+    q, k, v = inputs.prefill_inputs(B, H, Sq, Sk, d, DT[dt], seed=Sq * 3 + Sk)
+    dout = inputs.prefill_inputs(B, H, Sq, Sq, d, DT[dt], seed=Sq + 5)[0]
+    lay = _layout(H, Sq, Sk, seed=Sq + Sk)
+    scale = 1 / math.sqrt(d)
+    dev = torch.device("cuda")
+    qd, kd, vd, gd, ld = q.to(dev), k.to(dev), v.to(dev), dout.to(dev), lay.to(dev)
+    o = torch.empty_like(qd)
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+    fa.fa_fwd_ex(qd, kd, vd, o, lse, scale, fa.FA_MASK_BLOCK_SPARSE, block_layout=ld)
+    dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+    ws = torch.empty(fa.fa_bwd_workspace_size(B, H, Sq), dtype=torch.uint8, device=dev)
+    fa.fa_bwd_block_sparse(qd, kd, vd, o, gd, lse, dq, dk, dv, ws, scale, ld)
+    torch.cuda.synchronize()
+    assert fa.fa_get_device_status() == fa.FA_OK
+    rq, rk, rv = oracle.attention_backward_layout(q, k, v, dout, scale, lay.numpy())
+    got = [t.float().cpu().numpy() for t in (dq, dk, dv)]
+    what = f"block-sparse {Sq}x{Sk} d{d} {dt}"
+    compare_grad(got[0], rq, what + " dq")
+    compare_grad(got[1], rk, what + " dk")
+    compare_grad(got[2], rv, what + " dv")
+    assert np.all(got[0][:, 0, :min(128, Sq)] == 0)
+    assert np.all(got[1][:, -1, :min(128, Sk)] == 0) and np.all(got[2][:, -1, :min(128, Sk)] == 0)
+    with pytest.raises(fa.FaError):  # a layout mask without a layout is refused
+        fa.fa_bwd(qd, kd, vd, o, gd, lse, dq, dk, dv, ws, scale, fa.FA_MASK_BLOCK_SPARSE)

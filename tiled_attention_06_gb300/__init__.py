@@ -18,7 +18,7 @@ __all__ = [
     "fa_decode_workspace_size", "fa_decode_default_pages_per_split",
     "fa_get_device_status",
     "fa_selftest_timeout", "fa_last_error_string", "fa_version", "fa_fwd_block_m",
-    "fa_fwd_default_block_m", "fa_bwd", "fa_bwd_workspace_size", "fa_fwd_workspace_size",
+    "fa_fwd_default_block_m", "fa_bwd", "fa_bwd_block_sparse", "fa_bwd_workspace_size", "fa_fwd_workspace_size",
     "FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_CUDA", "FA_ERR_TIMEOUT",
     "FA_ERR_BAD_PAGE", "FA_F16", "FA_BF16", "FA_F32", "FA_MASK_NONE", "FA_MASK_CAUSAL",
     "FA_MASK_CAUSAL_WINDOW", "FA_MASK_BAND", "FA_MASK_PREFIX_LM", "FA_MASK_BLOCK_SPARSE",
@@ -89,6 +89,8 @@ def lib():
         L.fa_bwd_workspace_size.argtypes = [_i, _i, _i]
         L.fa_bwd.restype = _i
         L.fa_bwd.argtypes = [_vp] * 10 + [_sz] + [_i] * 5 + [_f] + [_i] * 4 + [_vp]
+        L.fa_bwd_block_sparse.restype = _i
+        L.fa_bwd_block_sparse.argtypes = [_vp] * 10 + [_sz] + [_i] * 5 + [_f, _vp, _i, _vp]
         L.fa_decode_paged.restype = _i
         L.fa_decode_paged.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i,
                                       _f, _i, _vp, _sz, _vp]
@@ -185,18 +187,33 @@ def fa_bwd_workspace_size(B, H, Sq):
 
 
 def fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, workspace, scale, mask_mode=FA_MASK_NONE,
-           window=0, n_global=0, stream=None):
+           window=0, n_global=0, stream=None, block_layout=None):
     """Gradients dq, dk, dv of fa_fwd for the upstream gradient dout (all [B,H,S,d]
     CUDA tensors of one 16-bit dtype; lse the float32 [B,H,Sq] fa_fwd returned; workspace
-    a CUDA byte tensor of fa_bwd_workspace_size(B, H, Sq) bytes)."""
+    a CUDA byte tensor of fa_bwd_workspace_size(B, H, Sq) bytes). FA_MASK_BLOCK_SPARSE takes
+    block_layout, the uint8 CUDA layout of the forward call (fa_bwd_block_sparse)."""
     _need_cuda_contig(q=q, k=k, v=v, o=o, dout=dout, lse=lse, dq=dq, dk=dk, dv=dv,
-                      workspace=workspace)
+                      workspace=workspace, block_layout=block_layout)
     B, H, Sq, d = q.shape
+    if mask_mode == FA_MASK_BLOCK_SPARSE:
+        _check(lib().fa_bwd_block_sparse(
+            q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(),
+            lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), workspace.data_ptr(),
+            workspace.numel() * workspace.element_size(), B, H, Sq, k.shape[2], d, float(scale),
+            _ptr(block_layout), _dtype_code(q), _stream(stream)))
+        return
     _check(lib().fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(),
                         lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
                         workspace.data_ptr(), workspace.numel() * workspace.element_size(), B,
                         H, Sq, k.shape[2], d, float(scale), mask_mode, window, n_global,
                         _dtype_code(q), _stream(stream)))
+
+
+def fa_bwd_block_sparse(q, k, v, o, dout, lse, dq, dk, dv, workspace, scale, block_layout,
+                        stream=None):
+    """fa_bwd under FA_MASK_BLOCK_SPARSE with the forward call's device layout."""
+    fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, workspace, scale, FA_MASK_BLOCK_SPARSE,
+           stream=stream, block_layout=block_layout)
 
 
 def fa_fwd(q, k, v, o, lse, scale, mask_mode=FA_MASK_NONE, window=0, n_global=0, stream=None):
@@ -332,6 +349,13 @@ def fa_fwd_paged(q, k_pages, v_pages, block_table, ctx_lens, o, lse, scale,
                                         Sq, d, page, block_table.shape[1], P, float(scale),
                                         mask_mode, window, n_global, _dtype_code(q),
                                         _stream(stream)))
+
+
+def fa_fwd_paged_host_lens(q, k_pages, v_pages, block_table, ctx_lens, ctx_lens_host, o, lse,
+                           scale, mask_mode=FA_MASK_CAUSAL, window=0, n_global=0, stream=None):
+    """fa_fwd_paged with the lengths also in host memory (a CPU int32 tensor) for the plan."""
+    fa_fwd_paged(q, k_pages, v_pages, block_table, ctx_lens, o, lse, scale, mask_mode, window,
+                 n_global, stream, ctx_lens_host=ctx_lens_host)
 
 
 def fa_kv_append(k_new, v_new, k_pages, v_pages, block_table, ctx_lens, new_lens=None,

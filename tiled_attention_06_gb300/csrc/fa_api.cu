@@ -760,10 +760,11 @@ size_t fa_bwd_workspace_size(int B, int H, int Sq) {
   return bwd_workspace_bytes(B, H, Sq, 128);
 }
 
-fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
-                 const float* lse, void* dq, void* dk, void* dv, void* workspace,
-                 size_t workspace_bytes, int B, int H, int Sq, int Sk, int d, float scale,
-                 int mask_mode, int window, int n_global, int dtype, fa_stream_t stream) {
+static fa_status bwd(const void* q, const void* k, const void* v, const void* o,
+                     const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                     void* workspace, size_t workspace_bytes, int B, int H, int Sq, int Sk, int d,
+                     float scale, int mask_mode, int window, int n_global,
+                     const uint8_t* layout, int dtype, fa_stream_t stream) {
   fa_fwd_params a;  // the forward's checks cover q, k, v, sizes, mask and dtype
   std::memset(&a, 0, sizeof a);
   a.q = q;
@@ -780,8 +781,7 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
   a.window = window;
   a.n_global = n_global;
   a.dtype = dtype;
-  if (mask_mode == FA_MASK_BLOCK_SPARSE)
-    return fail(FA_ERR_UNSUPPORTED, "fa_bwd: block-sparse layouts are not supported");
+  a.block_layout = layout;
   fa_status st = check_fwd(a);
   if (st != FA_OK) return st;
   if (Sq == 0 && Sk == 0) return FA_OK;
@@ -810,6 +810,11 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
   p.sl2 = scale * 1.4426950408889634f;
   p.status = dev.status;
   p.timeout_ns = 1000000000ull;
+  if (mask_mode == FA_MASK_BLOCK_SPARSE) {  // one layout block is one backward tile (128 x 128)
+    p.layout = layout;
+    p.lnqb = (Sq + FA_LAYOUT_BLOCK - 1) / FA_LAYOUT_BLOCK;
+    p.lnkb = (Sk + FA_LAYOUT_BLOCK - 1) / FA_LAYOUT_BLOCK;
+  }
   L.b.lse = lse;
   L.b.dqacc = static_cast<float*>(workspace);
   L.b.dsum = static_cast<float*>(workspace) + static_cast<size_t>(BH) * ((Sq + 3) / 4) * 4 * d;
@@ -829,6 +834,25 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
   cudaError_t e = fa::launch_backward(L, d, bf16, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "backward launch");
   return FA_OK;
+}
+
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                 const float* lse, void* dq, void* dk, void* dv, void* workspace,
+                 size_t workspace_bytes, int B, int H, int Sq, int Sk, int d, float scale,
+                 int mask_mode, int window, int n_global, int dtype, fa_stream_t stream) {
+  if (mask_mode == FA_MASK_BLOCK_SPARSE)
+    return fail(FA_ERR_UNSUPPORTED, "fa_bwd: a block layout goes through fa_bwd_block_sparse");
+  return bwd(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, B, H, Sq, Sk, d,
+             scale, mask_mode, window, n_global, nullptr, dtype, stream);
+}
+
+fa_status fa_bwd_block_sparse(const void* q, const void* k, const void* v, const void* o,
+                              const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                              void* workspace, size_t workspace_bytes, int B, int H, int Sq,
+                              int Sk, int d, float scale, const uint8_t* block_layout, int dtype,
+                              fa_stream_t stream) {
+  return bwd(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, B, H, Sq, Sk, d,
+             scale, FA_MASK_BLOCK_SPARSE, 0, 0, block_layout, dtype, stream);
 }
 
 fa_status fa_merge_partials(const void* o_a, const float* lse_a, const void* o_b,

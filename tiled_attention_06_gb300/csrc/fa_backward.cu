@@ -315,8 +315,11 @@ __device__ __forceinline__ void load_half(uint32_t dst, const CUtensorMap* map, 
   for (int c = 0; c < D / 64; ++c) tma_load_3d(dst + c * (kHalf * 128), map, bar, c * 64, row0, bh);
 }
 
-// Does the query block qb see any key of key block kb (the forward's key ranges)?
+// Does the query block qb see any key of key block kb (the forward's key ranges; for a
+// block layout, its 128 x 128 block, which is then seen whole)?
 __device__ __forceinline__ bool tile_visited(int qb, int kb, int bh, const PrefillParams& p) {
+  if (p.mask_mode == FA_MASK_BLOCK_SPARSE)
+    return p.layout[(static_cast<size_t>(bh % p.H) * p.lnqb + qb) * p.lnkb + kb] != 0;
   const Range r = key_range(qb * kBT, min(qb * kBT + kBT, p.Sq), kBT, p.Sk, p, bh);
   return range_has(r, kb);
 }
