@@ -298,8 +298,8 @@ def run_ours(args, rank, world):
     workload = "default" if args.workload == "default" else args.workload
     if workload in ("chunked", "multimodal"):
         return run_next_rows(args, fa, workload, peaks, peak_kind, stream, world)
-    if workload == "bwd4k":
-        return run_backward(args, fa, peaks, stream, world)
+    if workload in ("bwd4k", "bwd_blocksparse4k"):
+        return run_backward(args, fa, peaks, stream, world, workload)
     pcfg = PREFILL["causal4k" if workload in ("default", "sweep") else workload] \
         if workload != "decode" else None
     with_decode = workload in ("default", "decode")
@@ -910,12 +910,14 @@ def run_next_rows(args, fa, workload, peaks, peak_kind, stream, world):
     return res
 
 
-def run_backward(args, fa, peaks, stream, world):
-    """Backward of the causal 4k bf16 prefill (B4 H32 S4096 d128): fa_bwd after one fa_fwd,
-    timed with CUDA events. Work counted: the five products of the backward (S recomputed,
-    dP, dV, dK, dQ) over the visible pairs, 2.5x the forward's; each is computed once."""
+def run_backward(args, fa, peaks, stream, world, workload="bwd4k"):
+    """Backward of the causal 4k bf16 prefill (B4 H32 S4096 d128), or of the block-sparse 4k
+    one (the BigBird-shaped layout of blocksparse4k): fa_bwd after one forward call, timed
+    with CUDA events. Work counted: the five products of the backward (S recomputed, dP, dV,
+    dK, dQ) over the visible pairs, 2.5x the forward's; each is computed once."""
     from tiled_attention_06_gb300 import inputs
-    cfg = PREFILL["causal4k"]
+    sparse = workload == "bwd_blocksparse4k"
+    cfg = PREFILL["blocksparse4k" if sparse else "causal4k"]
     dev = torch.device("cuda", torch.cuda.current_device())
     q, k, v = (t.to(dev) for t in make_prefill(cfg, dev))
     dout = inputs.prefill_inputs(cfg["B"], cfg["H"], cfg["S"], cfg["S"], cfg["d"],
@@ -923,16 +925,22 @@ def run_backward(args, fa, peaks, stream, world):
     scale = 1 / math.sqrt(cfg["d"])
     o = torch.empty_like(q)
     lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
-    fa.fa_fwd(q, k, v, o, lse, scale, cfg["mode"], stream=stream)
+    layout = make_layout(cfg) if sparse else None
+    lay_d = layout.to(dev) if sparse else None
+    if sparse:
+        fa.fa_fwd_ex(q, k, v, o, lse, scale, cfg["mode"], block_layout=lay_d, stream=stream)
+    else:
+        fa.fa_fwd(q, k, v, o, lse, scale, cfg["mode"], stream=stream)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     ws = torch.empty(fa.fa_bwd_workspace_size(cfg["B"], cfg["H"], cfg["S"]), dtype=torch.uint8,
                      device=dev)
     K, W = args.steps, args.warmup
     ms, clk = timed([lambda: fa.fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, ws, scale, cfg["mode"],
-                                       stream=stream)], K, W, stream, args.clock_soak)
+                                       stream=stream, block_layout=lay_d)], K, W, stream,
+                    args.clock_soak)
     ms = ms[0]
     assert fa.fa_get_device_status() == fa.FA_OK
-    flops = 2.5 * prefill_flops(cfg)
+    flops = 2.5 * prefill_flops(cfg, layout)
     val = aggregate(flops * K, max_over_ranks(ms / 1e3, world), world) / 1e12
     tc_peak = float(peaks["bf16_tflops"])
     achieved = flops * K / (ms / 1e3) / 1e12
@@ -945,7 +953,9 @@ def run_backward(args, fa, peaks, stream, world):
                          "bound": "tensor", "achieved": achieved, "peak": tc_peak,
                          "unit": "TFLOP/s", "frac": achieved / tc_peak, "traffic": None,
                          "algorithmic_flops": flops},
-            "config": {"workload": "backward of causal prefill B4 H32 S4096 d128 bf16"}}
+            "config": {"workload": ("backward of block-sparse (BigBird layout) prefill"
+                                    if sparse else "backward of causal prefill")
+                                   + " B4 H32 S4096 d128 bf16"}}
 
 
 # --------------------------------------------------------------------------- reference arm
@@ -1074,7 +1084,7 @@ def main(argv=None):
                     choices=["default", "causal2k", "causal4k", "causal4k_f32", "noncausal4k",
                              "window32k",
                              "band4k", "prefixlm4k", "blocksparse4k", "chunked", "multimodal",
-                             "bwd4k",
+                             "bwd4k", "bwd_blocksparse4k",
                              "decode", "sweep"])
     ap.add_argument("--batch", type=int, default=None, help="override B (small profiling cases)")
     ap.add_argument("--heads", type=int, default=None, help="override H (small profiling cases)")
