@@ -148,14 +148,18 @@ def test_paged_prefill_reports_bad_page():
     assert fa.fa_get_device_status() == fa.FA_OK
 
 
-@pytest.mark.parametrize("mode,w,g", [(fa.FA_MASK_CAUSAL, 0, 0), (fa.FA_MASK_CAUSAL_WINDOW, 300, 7)])
-def test_host_lengths_plan_gives_the_same_output(mode, w, g):
+@pytest.mark.parametrize("mode,w,g,page,d,dt", [
+    (fa.FA_MASK_CAUSAL, 0, 0, 256, 128, torch.bfloat16),
+    (fa.FA_MASK_CAUSAL_WINDOW, 300, 7, 256, 128, torch.bfloat16),
+    (fa.FA_MASK_CAUSAL, 0, 0, 64, 64, torch.float16)])
+def test_host_lengths_plan_gives_the_same_output(mode, w, g, page, d, dt):
     """fa_fwd_paged_host_lens only changes which CTA runs which item: with the right host
-    lengths, with wrong ones and with none, every output bit and LSE bit is the same."""
-    B, H, d, page, chunk = 6, 4, 128, 256, 300
+    lengths, with wrong ones and with none, every output bit and LSE bit is the same (256-
+    and 64-token pages, the latter read as 64-key tiles)."""
+    B, H, chunk = 6, 4, 300
     ctx0 = [5000, 0, 1200, 3100, 77, 2600]
-    q, kp, vp, table, total, _, _ = build_cache(B, H, d, page, 160, ctx0, chunk,
-                                                torch.bfloat16, seed=7)
+    q, kp, vp, table, total, _, _ = build_cache(B, H, d, page, (160 * 256) // page, ctx0, chunk,
+                                                dt, seed=7)
     qd, tab = q.cuda(), table.cuda()
     ctx = torch.tensor(total, dtype=torch.int32, device="cuda")
     scale = 1 / math.sqrt(d)
