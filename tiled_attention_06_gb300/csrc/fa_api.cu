@@ -237,15 +237,23 @@ std::vector<int> costs_from_layout(const fa::PrefillParams& p, int BM, int BN,
   return cost;
 }
 
-// Plans built from host data, cached by the shape and an FNV-1a hash of that data (the
+// Plans built from host data, cached by the shape and an FNV-1a-style hash of that data (the
 // lengths, or the layout bytes), so that repeated calls with the same lengths or layout pay
 // for the hash only.
 std::map<std::pair<std::array<int, 12>, uint64_t>, std::unique_ptr<fa::PrefillSched>> g_data_plans;
 
+// FNV-1a over 8-byte words (then the tail bytes): a layout of tens of KB is hashed on every
+// call, so a word at a time.
 uint64_t fnv1a(const void* data, size_t n) {
   const uint8_t* b = static_cast<const uint8_t*>(data);
   uint64_t h = 1469598103934665603ull;
-  for (size_t i = 0; i < n; ++i) h = (h ^ b[i]) * 1099511628211ull;
+  size_t i = 0;
+  for (; i + 8 <= n; i += 8) {
+    uint64_t w;
+    std::memcpy(&w, b + i, 8);
+    h = (h ^ w) * 1099511628211ull;
+  }
+  for (; i < n; ++i) h = (h ^ b[i]) * 1099511628211ull;
   return h;
 }
 
