@@ -147,3 +147,41 @@ def test_backward_block_sparse(Sq, Sk, d, dt):
     assert np.all(got[1][:, -1, :min(128, Sk)] == 0) and np.all(got[2][:, -1, :min(128, Sk)] == 0)
     with pytest.raises(fa.FaError):  # a layout mask without a layout is refused
         fa.fa_bwd(qd, kd, vd, o, gd, lse, dq, dk, dv, ws, scale, fa.FA_MASK_BLOCK_SPARSE)
+
+
+@pytest.mark.parametrize("sparse", [False, True])
+def test_backward_4k_bench_configuration_sampled_heads(sparse):
+    """The bench's backward configurations at full size, B=4 H=32 S=4096 d=128 bf16 (causal,
+    or the BigBird-shaped block layout of the block-sparse bench), run as the bench runs them;
+    the gradients of two (batch, head) pairs checked element by element against the oracle on
+    those heads alone (heads are independent)."""
+    B, H, S, d = 4, 32, 4096, 128
+    q, k, v = inputs.prefill_inputs(B, H, S, S, d, torch.bfloat16, seed=0)
+    dout = inputs.prefill_inputs(B, H, S, S, d, torch.bfloat16, seed=1)[0]
+    scale = 1 / math.sqrt(d)
+    dev = torch.device("cuda")
+    qd, kd, vd, gd = q.to(dev), k.to(dev), v.to(dev), dout.to(dev)
+    o = torch.empty_like(qd)
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+    lay = inputs.block_layout(H, S, S) if sparse else None
+    mode = fa.FA_MASK_BLOCK_SPARSE if sparse else fa.FA_MASK_CAUSAL
+    if sparse:
+        fa.fa_fwd_ex(qd, kd, vd, o, lse, scale, mode, block_layout=lay.to(dev))
+    else:
+        fa.fa_fwd(qd, kd, vd, o, lse, scale, mode)
+    dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+    ws = torch.empty(fa.fa_bwd_workspace_size(B, H, S), dtype=torch.uint8, device=dev)
+    fa.fa_bwd(qd, kd, vd, o, gd, lse, dq, dk, dv, ws, scale, mode,
+              block_layout=lay.to(dev) if sparse else None)
+    torch.cuda.synchronize()
+    assert fa.fa_get_device_status() == fa.FA_OK
+    for b, h in ((0, 0), (3, 29)):
+        sl = (slice(b, b + 1), slice(h, h + 1))
+        args = (q[sl], k[sl], v[sl], dout[sl], scale)
+        if sparse:
+            ref = oracle.attention_backward_layout(*args, lay[h:h + 1].numpy())
+        else:
+            ref = oracle.attention_backward(*args, oracle.MASK_CAUSAL)
+        for got, r, name in zip((dq, dk, dv), ref, ("dq", "dk", "dv")):
+            compare_grad(got[sl].float().cpu().numpy(), r, f"4k {'sparse' if sparse else 'causal'} "
+                                                           f"b{b} h{h} {name}")
