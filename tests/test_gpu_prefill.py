@@ -163,16 +163,18 @@ def test_causal_2k_fp16_full():
     compare(o, lse, ref_o, ref_l, "causal 2k")
 
 
-@pytest.mark.parametrize("mode", [fa.FA_MASK_CAUSAL, fa.FA_MASK_NONE])
-def test_long_4k_bf16_sampled(mode):
-    """B=4, H=32, Sq=Sk=4096, d=128, bf16, N(0,1), causal and non-causal; the oracle
-    checks the first and last query block of every head and 256 random rows."""
+@pytest.mark.parametrize("mode,w,g", [(fa.FA_MASK_CAUSAL, 0, 0), (fa.FA_MASK_NONE, 0, 0),
+                                      (fa.FA_MASK_BAND, 512, 0), (fa.FA_MASK_PREFIX_LM, 0, 1024)])
+def test_long_4k_bf16_sampled(mode, w, g):
+    """B=4, H=32, Sq=Sk=4096, d=128, bf16, N(0,1): causal, non-causal and the bench's band
+    (±512) and prefix-LM (1024-key prefix) configurations, each with its default kernel; the
+    oracle checks the first and last query block of every head and 256 random rows."""
     B, H, S, d = 4, 32, 4096, 128
     q, k, v = inputs.prefill_inputs(B, H, S, S, d, torch.bfloat16, seed=0)
     scale = 1 / math.sqrt(d)
-    o, lse = run_fwd(q, k, v, scale, mode)
+    o, lse = run_fwd(q, k, v, scale, mode, w, g)
     rows = sample_rows(B, H, S, fa.fa_fwd_block_m(), n_random=256, seed=1)
-    ref_o, ref_l = oracle.attention(q, k, v, scale, mode, rows=rows)
+    ref_o, ref_l = oracle.attention(q, k, v, scale, mode, w, g, rows=rows)
     compare(pick_rows(o, rows, S), pick_rows(lse, rows, S), ref_o, ref_l, f"4k mode {mode}")
 
 
