@@ -80,22 +80,22 @@ MODE_NAME = {0: "none", 1: "causal", 2: "causal_window", 3: "band", 4: "prefix_l
 # sources it was taken on; the figure is reported only for those workloads and only while
 # those sources are unchanged. Summaries: profiles/.
 NCU_TRAFFIC = {
-    # prefill_bm256_kernel, causal 4k B4 H16 capture: 213.8 MB read + 47.4 MB written,
+    # prefill_bm256_kernel, causal 4k B4 H16 capture: 214.2 MB read + 47.0 MB written,
     # scaled x2 to B4 H32
-    "prefill": {"bytes": 522.46e6, "workloads": ("default", "causal4k"),
+    "prefill": {"bytes": 522.49e6, "workloads": ("default", "causal4k"),
                 "sources": ['fa_prefill.cu', 'fa_mma.cuh', 'fa_ptx.cuh', 'fa_plan.h', 'fa_internal.h'],
-                "sha256": "78d1e715e32b026fa9d332909b98235846315e4edf9315f99e03956e4be6355b"},
-    # paged decode B8 capture: 547.5 MB read + 4.0 MB written for 547.5 MB algorithmic,
+                "sha256": "27715d57c79c6990c6dc2db0657636d63576aedaaa6cb77aee74433bf3e522fb"},
+    # paged decode B8 capture: 547.5 MB read + 3.7 MB written for 547.5 MB algorithmic,
     # scaled to the bench call's 2410.7 MB algorithmic
-    "decode": {"workloads": ("default", "decode"), "bytes": 2.4283e9, "sources": ['fa_decode.cu', 'fa_ptx.cuh', 'fa_internal.h'],
-               "sha256": "3c9bbadc4842e6650e28d42e87bad49a1c0f11c4f7e62bef5f48e6a2ee932114"},
-    # FP32 inputs, causal 4k B4 H16 capture of one call: split_bf16_kernel 402.7 MB read +
-    # 345.6 MB written, prefill_bm256_kernel (split) 409.8 MB read + 110.7 MB written;
+    "decode": {"workloads": ("default", "decode"), "bytes": 2.4271e9, "sources": ['fa_decode.cu', 'fa_ptx.cuh', 'fa_internal.h'],
+               "sha256": "2799d296869b44f4bd3fb809eb8734fe383e3827f1c0f2c062162cc2df97c5b1"},
+    # FP32 inputs, causal 4k B4 H16 capture of one call: split_bf16_kernel 402.8 MB read +
+    # 345.6 MB written, prefill_bm256_kernel (split) 409.2 MB read + 110.4 MB written;
     # scaled x2 to B4 H32
-    "prefill_f32": {"bytes": 2537.7e6, "workloads": ("causal4k_f32",),
+    "prefill_f32": {"bytes": 2535.9e6, "workloads": ("causal4k_f32",),
                     "sources": ['fa_prefill.cu', 'fa_prefill_split.cu', 'fa_mma.cuh', 'fa_ptx.cuh',
                                 'fa_plan.h', 'fa_internal.h'],
-                    "sha256": "d181605f2781566ccaf0264eec505df0ce3fb9fb14713fd73b7ca713ce62ced3"},
+                    "sha256": "b2c84d2bf45b625746ce2fafb7046a63486bc56c466e4ced97d1fb2d600d9fe7"},
 }
 
 

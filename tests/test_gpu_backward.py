@@ -107,6 +107,19 @@ def test_backward_causal_2k_full():
     check(q, k, v, dout, 1 / math.sqrt(128), "causal", "causal 2k")
 
 
+@pytest.mark.parametrize("mask", ["causal", "band"])
+@pytest.mark.parametrize("d,dt", [(64, "f16"), (128, "bf16")])
+def test_backward_many_heads_launch_groups(mask, d, dt):
+    """B=2, H=55, Sq=Sk=300: 110 heads of three key blocks, 330 CTAs of the dK/dV kernel. Its
+    launch order takes heads in groups whose CTAs make about two waves (on 152 SMs, 102 heads
+    of three CTAs) and, within a group, key block by key block, so here the last group is a
+    partial one of 8 heads. Every gradient of every head against the oracle: a CTA mapped to
+    the wrong (head, key block), or to one twice, leaves some dK and dV rows wrong."""
+    q, k, v = inputs.prefill_inputs(2, 55, 300, 300, d, DT[dt], seed=d + 7)
+    dout = inputs.prefill_inputs(2, 55, 300, 300, d, DT[dt], seed=d + 8)[0]
+    check(q, k, v, dout, 1 / math.sqrt(d), mask, f"110 heads d{d} {dt} {mask}")
+
+
 def _layout(H, Sq, Sk, seed, density=0.4):
     g = torch.Generator().manual_seed(seed)
     nq, nk = -(-Sq // fa.FA_LAYOUT_BLOCK), -(-Sk // fa.FA_LAYOUT_BLOCK)

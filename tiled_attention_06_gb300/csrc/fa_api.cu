@@ -830,6 +830,10 @@ static fa_status bwd(const void* q, const void* k, const void* v, const void* o,
   L.b.dk = dk;
   L.b.dv = dv;
   L.b.scale = scale;
+  {  // the dK/dV kernel's launch order: heads in groups whose CTAs make about two waves
+    const int nkb = (Sk + 127) / 128;
+    L.b.head_group = nkb > 0 ? std::min(BH, std::max(1, (2 * dev.sms + nkb - 1) / nkb)) : 1;
+  }
   L.o = o;
   L.dout = dout;
   const void* qmap = Sq ? q : k;  // a map needs a valid address even when nothing is loaded

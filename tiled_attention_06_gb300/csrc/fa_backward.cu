@@ -9,7 +9,8 @@
 // Three kernels, each step on the tensor cores where it is a contraction:
 //   bwd_prep_kernel   D_i, one FP32 per query row (HBM-bound), and zeros the FP32 dQ
 //                     accumulator.
-//   bwd_dkdv_kernel   one CTA per (batch*head, block of 128 keys); TMEM lane = key. For
+//   bwd_dkdv_kernel   one CTA per (batch*head, block of 128 keys), dispatched in groups of
+//                     heads, key block by key block within a group (bwd_item); TMEM lane = key. For
 //                     each block of 128 queries that sees these keys, in two halves of 64
 //                     queries: S^T = K Q^T and dP^T = V dO^T (tcgen05, A and B from shared
 //                     memory); P^T and dS^T = P^T (dP^T - D) by the elementwise warps, P^T
@@ -324,6 +325,21 @@ __device__ __forceinline__ bool tile_visited(int qb, int kb, int bh, const Prefi
   return range_has(r, kb);
 }
 
+// The (batch*head, key block) of CTA x. Heads go in groups of G (the last group may be
+// smaller); within a group the order is key block-major: key block 0 of every head of the
+// group, then key block 1, and so on. Under the causal, window and prefix masks the low key
+// blocks are seen by the most query blocks, so a group's longest CTAs start first and its
+// last CTAs are short, which evens out the end of the launch; and the CTAs running at one
+// time belong to a few groups, whose streamed Q and dO and whose dQ accumulators stay in L2.
+// With G = 1 this is the plain head-major order.
+__device__ __forceinline__ void bwd_item(int x, int BH, int nkb, int G, int& bh, int& kb) {
+  const int per = G * nkb;
+  const int grp = x / per, w = x - grp * per;
+  const int gs = min(G, BH - grp * G);
+  kb = w / gs;
+  bh = grp * G + (w - kb * gs);
+}
+
 // The next query block after qb that sees key block kb, or nqb.
 __device__ __forceinline__ int next_qb(int qb, int kb, int bh, const PrefillParams& p, int nqb) {
   do {
@@ -424,7 +440,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   auto B = [&](uint64_t& x) { return smem_u32(&x); };
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int nkb = (p.Sk + kBT - 1) / kBT, nqb = (p.Sq + kBT - 1) / kBT;
-  const int bh = blockIdx.x / nkb, kb = blockIdx.x % nkb;
+  int bh, kb;
+  bwd_item(blockIdx.x, p.BH, nkb, b.head_group, bh, kb);
   const uint32_t tmem = bwd_setup(bars, &tmQ, &tmK, &tmV, &tmdO);
   const WaitCtx wc{&bars->abort, p.status, p.timeout_ns};
 

@@ -72,11 +72,12 @@ cudaError_t launch_prefill_split(const PrefillLaunch& L, int D, cudaStream_t str
 struct BwdParams {
   const float* lse;   // [B,H,Sq] natural-log LSE of the forward
   const float* dsum;  // [B,H,Sq] D_i = dO_i . O_i (written by the first kernel)
-  float* dqacc;       // [B,H,Sq,d] FP32 dQ accumulator (zeroed by the first kernel)
+  float* dqacc;       // [B*H][ceil(Sq/4)][d][4] FP32 dQ accumulator (zeroed by the first kernel)
   void* dq;           // [B,H,Sq,d] 16-bit
   void* dk;           // [B,H,Sk,d]
   void* dv;
   float scale;
+  int head_group;  // heads per group of the dK/dV kernel's launch order (1 <= head_group)
 };
 
 struct BwdLaunch {
