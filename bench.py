@@ -85,10 +85,10 @@ NCU_TRAFFIC = {
     "prefill": {"bytes": 522.49e6, "workloads": ("default", "causal4k"),
                 "sources": ['fa_prefill.cu', 'fa_mma.cuh', 'fa_ptx.cuh', 'fa_plan.h', 'fa_internal.h'],
                 "sha256": "27715d57c79c6990c6dc2db0657636d63576aedaaa6cb77aee74433bf3e522fb"},
-    # paged decode B8 capture: 547.5 MB read + 3.7 MB written for 547.5 MB algorithmic,
+    # paged decode B8 capture: 547.5 MB read + 4.1 MB written for 547.5 MB algorithmic,
     # scaled to the bench call's 2410.7 MB algorithmic
-    "decode": {"workloads": ("default", "decode"), "bytes": 2.4271e9, "sources": ['fa_decode.cu', 'fa_ptx.cuh', 'fa_internal.h'],
-               "sha256": "2799d296869b44f4bd3fb809eb8734fe383e3827f1c0f2c062162cc2df97c5b1"},
+    "decode": {"workloads": ("default", "decode"), "bytes": 2.4289e9, "sources": ['fa_decode.cu', 'fa_ptx.cuh', 'fa_internal.h'],
+               "sha256": "f58ddf3a7ba6f1d15da2486cef5923871c31277eeed188e019349a2c65f943d2"},
     # FP32 inputs, causal 4k B4 H16 capture of one call: split_bf16_kernel 402.8 MB read +
     # 345.6 MB written, prefill_bm256_kernel (split) 409.2 MB read + 110.4 MB written;
     # scaled x2 to B4 H32

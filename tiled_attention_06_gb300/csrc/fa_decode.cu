@@ -11,9 +11,9 @@
 //     several tokens in flight per lane. The groups are merged in shared memory and
 //     the split writes its FP32 partial (acc, m, l) to the workspace.
 //   kernel 2 (merge): per (b, h), M = max m_s, L = sum l_s 2^(m_s - M),
-//     O = sum 2^(m_s - M) acc_s / L, LSE = (M + log2 L) ln 2: the same running-max
-//     recurrence as the tiled forward (ops-transformer overview, section 二.1), applied
-//     across splits.
+//     O = sum 2^(m_s - M) acc_s / L, LSE = (M + log2 L) ln 2, formed in one pass over the
+//     splits with the same running-max recurrence as the tiled forward (ops-transformer
+//     overview, section 二.1).
 // Scores are kept in log2 units (q is pre-multiplied by scale*log2(e)).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -211,6 +211,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(const DecodeP
 
 template <int D, bool BF16>
 __global__ void __launch_bounds__(D) decode_merge_kernel(const DecodeParams p) {
+  constexpr int kBatch = 8;  // splits whose loads are in flight together
   const int bh = blockIdx.x;
   const int b = bh / p.H;
   const int e = threadIdx.x;
@@ -218,20 +219,33 @@ __global__ void __launch_bounds__(D) decode_merge_kernel(const DecodeParams p) {
   const int span = p.pages_per_split * p.page_size;
   const int nsplit = (ctx + span - 1) / span;
   const float* part = p.part + static_cast<size_t>(bh) * p.nsplit_max * (D + 2);
-  float M = -INFINITY;
-  for (int s = 0; s < nsplit; ++s) {
-    const float* ps = part + static_cast<size_t>(s) * (D + 2);
-    if (ps[D + 1] > 0.f) M = fmaxf(M, ps[D]);
-  }
-  float a = 0.f, L = 0.f;
-  if (M != -INFINITY) {
-    for (int s = 0; s < nsplit; ++s) {
-      const float* ps = part + static_cast<size_t>(s) * (D + 2);
-      const float ls = ps[D + 1];
-      if (ls > 0.f) {
-        const float w = ex2_approx(ps[D] - M);
-        a = fmaf(w, ps[e], a);
-        L = fmaf(w, ls, L);
+  // One pass with a running maximum (the same recurrence as inside a split), the partials
+  // of kBatch splits loaded before any is used, so that the pass waits for one load
+  // latency per batch rather than two per split.
+  float M = -INFINITY, a = 0.f, L = 0.f;
+  for (int s0 = 0; s0 < nsplit; s0 += kBatch) {
+    float ms[kBatch], ls[kBatch], as[kBatch];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      ls[u] = 0.f;
+      ms[u] = -INFINITY;
+      as[u] = 0.f;
+      if (s0 + u < nsplit) {
+        const float* ps = part + static_cast<size_t>(s0 + u) * (D + 2);
+        ms[u] = ps[D];
+        ls[u] = ps[D + 1];
+        as[u] = ps[e];
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      if (ls[u] > 0.f) {  // a split with no visible token adds nothing
+        const float m_new = fmaxf(M, ms[u]);
+        const float c = ex2_approx(M - m_new);  // M = -inf gives 0
+        const float w = ex2_approx(ms[u] - m_new);
+        a = fmaf(w, as[u], a * c);
+        L = fmaf(w, ls[u], L * c);
+        M = m_new;
       }
     }
   }
