@@ -96,6 +96,25 @@ struct BwdBars {
 };
 static_assert(sizeof(BwdBars) <= 256, "barrier block over its reserve");
 
+// 32 lanes x 16 columns of 32-bit TMEM -> 16 registers per thread, and 8 registers -> 8
+// columns: the elementwise step works on 16 queries at a time.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+      : "memory");
+}
+
 // Half g = 2 t + u of the stream (tile t, half u) lives in stage g % kStages; its fills and
 // releases alternate parity every kStages halves.
 __device__ __forceinline__ int stage_of(int g) { return g % kStages; }
@@ -581,35 +600,39 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tc_fence_after();
         const int m0 = qb * kBT + 64 * u + 32 * sub;
         const RowSpan vis = query_cols(j, m0, p.Sk, p);
-        uint32_t sv[32], dp[32];
-        tmem_ld32(t_lane + c_s, sv);
-        tmem_ld32(t_lane + 128 + c_s, dp);
-        tmem_ld_wait<32>(sv);
-        tmem_ld_tie<32>(dp);
+        // two chunks of 16 queries: P^T of chunk c packed over columns [8c, 8c + 8) of this
+        // thread's 32, which the first chunk has already read
 #pragma unroll
-        for (int e = 0; e < 32; e += 4) {  // 4 queries at a time; statistics from shared memory
-          const float4 a = st4[e / 4];
-          const float4 d = st4[kHalf / 4 + e / 4];
-          const float l2[4] = {a.x, a.y, a.z, a.w}, dd[4] = {d.x, d.y, d.z, d.w};
-          float pv[4], dv[4];
+        for (int c = 0; c < 2; ++c) {
+          uint32_t sv[16], dp[16];
+          tmem_ld16(t_lane + c_s + 16 * c, sv);
+          tmem_ld16(t_lane + 128 + c_s + 16 * c, dp);
+          tmem_ld_wait<16>(sv);
+          tmem_ld_tie<16>(dp);
 #pragma unroll
-          for (int w = 0; w < 4; ++w) {
-            const int col = e + w;
-            const bool on = col >= vis.lo && col <= vis.hi;
-            pv[w] = on ? ex2_approx(__uint_as_float(sv[e + w]) * p.sl2 - l2[w]) : 0.f;
-            dv[w] = pv[w] * (__uint_as_float(dp[e + w]) - dd[w]);
+          for (int e = 0; e < 16; e += 4) {  // 4 queries at a time; statistics from shared memory
+            const float4 a = st4[(16 * c + e) / 4];
+            const float4 d = st4[kHalf / 4 + (16 * c + e) / 4];
+            const float l2[4] = {a.x, a.y, a.z, a.w}, dd[4] = {d.x, d.y, d.z, d.w};
+            float pv[4], dv[4];
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+              const int col = 16 * c + e + w;
+              const bool on = col >= vis.lo && col <= vis.hi;
+              pv[w] = on ? ex2_approx(__uint_as_float(sv[e + w]) * p.sl2 - l2[w]) : 0.f;
+              dv[w] = pv[w] * (__uint_as_float(dp[e + w]) - dd[w]);
+            }
+            sv[e / 2] = BF16 ? cvt_pack_bf16(pv[0], pv[1]) : cvt_pack_f16(pv[0], pv[1]);
+            sv[e / 2 + 1] = BF16 ? cvt_pack_bf16(pv[2], pv[3]) : cvt_pack_f16(pv[2], pv[3]);
+            dp[e / 2] = BF16 ? cvt_pack_bf16(dv[0], dv[1]) : cvt_pack_f16(dv[0], dv[1]);
+            dp[e / 2 + 1] = BF16 ? cvt_pack_bf16(dv[2], dv[3]) : cvt_pack_f16(dv[2], dv[3]);
           }
-          // packed over this thread's columns already read (16 each for P^T and dS^T)
-          sv[e / 2] = BF16 ? cvt_pack_bf16(pv[0], pv[1]) : cvt_pack_f16(pv[0], pv[1]);
-          sv[e / 2 + 1] = BF16 ? cvt_pack_bf16(pv[2], pv[3]) : cvt_pack_f16(pv[2], pv[3]);
-          dp[e / 2] = BF16 ? cvt_pack_bf16(dv[0], dv[1]) : cvt_pack_f16(dv[0], dv[1]);
-          dp[e / 2 + 1] = BF16 ? cvt_pack_bf16(dv[2], dv[3]) : cvt_pack_f16(dv[2], dv[3]);
-        }
-        tmem_st16(t_lane + c_s, sv);  // P^T over columns already read
+          tmem_st8(t_lane + c_s + 8 * c, sv);  // P^T over columns already read
 #pragma unroll
-        for (int i = 0; i < 4; ++i)   // dS^T into shared memory for the dK and dQ MMAs
-          st_shared_v4(ds_row + ((static_cast<uint32_t>(4 * sub + i) ^ (row & 7)) << 4),
-                       dp[4 * i], dp[4 * i + 1], dp[4 * i + 2], dp[4 * i + 3]);
+          for (int i = 0; i < 2; ++i)  // dS^T into shared memory for the dK and dQ MMAs
+            st_shared_v4(ds_row + ((static_cast<uint32_t>(4 * sub + 2 * c + i) ^ (row & 7)) << 4),
+                         dp[4 * i], dp[4 * i + 1], dp[4 * i + 2], dp[4 * i + 3]);
+        }
         tmem_st_wait();
         fence_proxy_async_smem();  // the MMAs read dS^T through the async proxy
         tc_fence_before();
