@@ -453,7 +453,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   auto sQh = [&](int h) { return sSt + 2 * h * C::HTILE; };
   auto sdOh = [&](int h) { return sSt + (2 * h + 1) * C::HTILE; };
   const uint32_t sDS = sSt + kStages * 2 * C::HTILE;  // dS^T of half u at sDS + u DS
-  // [stage][LSE2 | D][64]
+  // [stage][-LSE2 | -D][64]
   float* stats = reinterpret_cast<float*>(smem + 2 * C::TILE + kStages * 2 * C::HTILE + 2 * C::DS);
   BwdBars* bars = reinterpret_cast<BwdBars*>(reinterpret_cast<uint8_t*>(stats) + kStages * C::STATS);
   auto B = [&](uint64_t& x) { return smem_u32(&x); };
@@ -490,12 +490,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         if (g >= kStages && !(ok = mbar_wait(B(bars->st_empty[h]), stage_parity(g - kStages), wc)))
           break;
-        {  // the stage's statistics: LSE * log2(e) and D
+        {  // the stage's statistics, negated: -LSE * log2(e) and -D
           float* st = stats + h * 2 * kHalf;
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
-            st[lane * 2 + e] = lv[e] * 1.4426950408889634f;
-            st[kHalf + lane * 2 + e] = dv[e];
+            st[lane * 2 + e] = -lv[e] * 1.4426950408889634f;
+            st[kHalf + lane * 2 + e] = -dv[e];
           }
           __syncwarp();  // the leader's arrive below releases every lane's writes
         }
@@ -611,16 +611,25 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           tmem_ld_tie<16>(dp);
 #pragma unroll
           for (int e = 0; e < 16; e += 4) {  // 4 queries at a time; statistics from shared memory
+            // negated statistics, two queries per packed FP32 instruction
             const float4 a = st4[(16 * c + e) / 4];
             const float4 d = st4[kHalf / 4 + (16 * c + e) / 4];
-            const float l2[4] = {a.x, a.y, a.z, a.w}, dd[4] = {d.x, d.y, d.z, d.w};
+            const uint64_t nl2[2] = {f2(a.x, a.y), f2(a.z, a.w)}, ndd[2] = {f2(d.x, d.y), f2(d.z, d.w)};
+            const uint64_t sl2 = f2(p.sl2, p.sl2);
             float pv[4], dv[4];
 #pragma unroll
-            for (int w = 0; w < 4; ++w) {
+            for (int w = 0; w < 4; w += 2) {
+              const uint64_t x = f2_fma(f2(__uint_as_float(sv[e + w]), __uint_as_float(sv[e + w + 1])),
+                                        sl2, nl2[w / 2]);
+              float x0, x1;
+              f2_split(x, x0, x1);
               const int col = 16 * c + e + w;
-              const bool on = col >= vis.lo && col <= vis.hi;
-              pv[w] = on ? ex2_approx(__uint_as_float(sv[e + w]) * p.sl2 - l2[w]) : 0.f;
-              dv[w] = pv[w] * (__uint_as_float(dp[e + w]) - dd[w]);
+              pv[w] = (col >= vis.lo && col <= vis.hi) ? ex2_approx(x0) : 0.f;
+              pv[w + 1] = (col + 1 >= vis.lo && col + 1 <= vis.hi) ? ex2_approx(x1) : 0.f;
+              const uint64_t dd2 = f2_add(f2(__uint_as_float(dp[e + w]), __uint_as_float(dp[e + w + 1])),
+                                          ndd[w / 2]);
+              const uint64_t ds2 = f2_fma(f2(pv[w], pv[w + 1]), dd2, f2(0.f, 0.f));
+              f2_split(ds2, dv[w], dv[w + 1]);
             }
             sv[e / 2] = BF16 ? cvt_pack_bf16(pv[0], pv[1]) : cvt_pack_f16(pv[0], pv[1]);
             sv[e / 2 + 1] = BF16 ? cvt_pack_bf16(pv[2], pv[3]) : cvt_pack_f16(pv[2], pv[3]);
