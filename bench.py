@@ -80,22 +80,22 @@ MODE_NAME = {0: "none", 1: "causal", 2: "causal_window", 3: "band", 4: "prefix_l
 # sources it was taken on; the figure is reported only for those workloads and only while
 # those sources are unchanged. Summaries: profiles/.
 NCU_TRAFFIC = {
-    # prefill_bm256_kernel, causal 4k B4 H16 capture: 214.2 MB read + 47.0 MB written,
+    # prefill_bm256_kernel, causal 4k B4 H16 capture: 213.7 MB read + 47.4 MB written,
     # scaled x2 to B4 H32
-    "prefill": {"bytes": 522.49e6, "workloads": ("default", "causal4k"),
+    "prefill": {"bytes": 522.13e6, "workloads": ("default", "causal4k"),
                 "sources": ['fa_prefill.cu', 'fa_mma.cuh', 'fa_ptx.cuh', 'fa_plan.h', 'fa_internal.h'],
-                "sha256": "27715d57c79c6990c6dc2db0657636d63576aedaaa6cb77aee74433bf3e522fb"},
+                "sha256": "c1b9809d6f61876576f34769600da90cb7e0305adedb690f307a790ba94d7552"},
     # paged decode B8 capture: 547.5 MB read + 4.1 MB written for 547.5 MB algorithmic,
     # scaled to the bench call's 2410.7 MB algorithmic
     "decode": {"workloads": ("default", "decode"), "bytes": 2.4289e9, "sources": ['fa_decode.cu', 'fa_ptx.cuh', 'fa_internal.h'],
                "sha256": "f58ddf3a7ba6f1d15da2486cef5923871c31277eeed188e019349a2c65f943d2"},
-    # FP32 inputs, causal 4k B4 H16 capture of one call: split_bf16_kernel 402.8 MB read +
-    # 345.6 MB written, prefill_bm256_kernel (split) 409.2 MB read + 110.4 MB written;
+    # FP32 inputs, causal 4k B4 H16 capture of one call: split_bf16_kernel 402.7 MB read +
+    # 345.3 MB written, prefill_bm256_kernel (split) 409.0 MB read + 110.4 MB written;
     # scaled x2 to B4 H32
-    "prefill_f32": {"bytes": 2535.9e6, "workloads": ("causal4k_f32",),
+    "prefill_f32": {"bytes": 2534.8e6, "workloads": ("causal4k_f32",),
                     "sources": ['fa_prefill.cu', 'fa_prefill_split.cu', 'fa_mma.cuh', 'fa_ptx.cuh',
                                 'fa_plan.h', 'fa_internal.h'],
-                    "sha256": "b2c84d2bf45b625746ce2fafb7046a63486bc56c466e4ced97d1fb2d600d9fe7"},
+                    "sha256": "38ee28e9d1c5bcc0f491957be24204c5a35718fa816be5b62740ffacfc4b37b1"},
 }
 
 

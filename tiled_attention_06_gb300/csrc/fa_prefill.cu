@@ -159,10 +159,20 @@ __device__ __forceinline__ bool softmax_cols(uint32_t t_lane, uint32_t s_col, ui
     } else if (p.mask_mode == FA_MASK_PREFIX_LM) {
       lim = min(max(pos_q, p.n_global - 1), sk - 1) - n0;
     }
+    // per 32 columns, a bit mask of the visible ones: c <= lim and (c >= lo or c < gl)
+    lim = max(lim, -1);
+    lo = max(lo, -1);
+    gl = max(gl, 0);
 #pragma unroll
-    for (int c = 0; c < NC; ++c) {
-      const bool vis = (c <= lim) && (c >= lo || c < gl);
-      if (!vis) s[c] = __float_as_uint(-INFINITY);
+    for (int k = 0; k < NC / 32; ++k) {
+      const int b = lim - 32 * k, a = lo - 32 * k, g = gl - 32 * k;
+      const uint32_t upto = b < 0 ? 0u : (b >= 31 ? 0xffffffffu : (2u << b) - 1u);
+      const uint32_t from = a <= 0 ? 0xffffffffu : (a >= 32 ? 0u : ~((1u << a) - 1u));
+      const uint32_t below = g <= 0 ? 0u : (g >= 32 ? 0xffffffffu : (1u << g) - 1u);
+      const uint32_t mk = upto & (from | below);
+#pragma unroll
+      for (int c = 0; c < 32; ++c)
+        if (!((mk >> c) & 1u)) s[32 * k + c] = __float_as_uint(-INFINITY);
     }
   }
   // partial row max: four independent chains of three-input maxima, then combined
