@@ -37,6 +37,7 @@
 
 #include <climits>
 #include <cstdint>
+#include <type_traits>
 
 #include "fa_bwd_tiles.h"
 #include "fa_internal.h"
@@ -600,48 +601,63 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tc_fence_after();
         const int m0 = qb * kBT + 64 * u + 32 * sub;
         const RowSpan vis = query_cols(j, m0, p.Sk, p);
+        // the queries of this thread's 32 columns that see its key, as a bit mask; a warp
+        // whose 32 keys all see all 32 queries takes the unmasked path
+        uint32_t mk = 0u;
+        if (vis.lo <= vis.hi && vis.hi >= 0 && vis.lo <= 31) {
+          const int lo = max(vis.lo, 0), hi = min(vis.hi, 31);
+          mk = (hi >= 31 ? 0xffffffffu : (2u << hi) - 1u) & ~((1u << lo) - 1u);
+        }
+        const bool all_vis = __all_sync(0xffffffffu, mk == 0xffffffffu);
         // two chunks of 16 queries: P^T of chunk c packed over columns [8c, 8c + 8) of this
         // thread's 32, which the first chunk has already read
+        auto chunks = [&](auto masked) {
+          constexpr bool kMasked = decltype(masked)::value;
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          uint32_t sv[16], dp[16];
-          tmem_ld16(t_lane + c_s + 16 * c, sv);
-          tmem_ld16(t_lane + 128 + c_s + 16 * c, dp);
-          tmem_ld_wait<16>(sv);
-          tmem_ld_tie<16>(dp);
+          for (int c = 0; c < 2; ++c) {
+            uint32_t sv[16], dp[16];
+            tmem_ld16(t_lane + c_s + 16 * c, sv);
+            tmem_ld16(t_lane + 128 + c_s + 16 * c, dp);
+            tmem_ld_wait<16>(sv);
+            tmem_ld_tie<16>(dp);
 #pragma unroll
-          for (int e = 0; e < 16; e += 4) {  // 4 queries at a time; statistics from shared memory
-            // negated statistics, two queries per packed FP32 instruction
-            const float4 a = st4[(16 * c + e) / 4];
-            const float4 d = st4[kHalf / 4 + (16 * c + e) / 4];
-            const uint64_t nl2[2] = {f2(a.x, a.y), f2(a.z, a.w)}, ndd[2] = {f2(d.x, d.y), f2(d.z, d.w)};
-            const uint64_t sl2 = f2(p.sl2, p.sl2);
-            float pv[4], dv[4];
+            for (int e = 0; e < 16; e += 4) {  // 4 queries at a time; statistics from shared memory
+              // negated statistics, two queries per packed FP32 instruction
+              const float4 a = st4[(16 * c + e) / 4];
+              const float4 d = st4[kHalf / 4 + (16 * c + e) / 4];
+              const uint64_t nl2[2] = {f2(a.x, a.y), f2(a.z, a.w)}, ndd[2] = {f2(d.x, d.y), f2(d.z, d.w)};
+              const uint64_t sl2 = f2(p.sl2, p.sl2);
+              float pv[4], dv[4];
 #pragma unroll
-            for (int w = 0; w < 4; w += 2) {
-              const uint64_t x = f2_fma(f2(__uint_as_float(sv[e + w]), __uint_as_float(sv[e + w + 1])),
-                                        sl2, nl2[w / 2]);
-              float x0, x1;
-              f2_split(x, x0, x1);
-              const int col = 16 * c + e + w;
-              pv[w] = (col >= vis.lo && col <= vis.hi) ? ex2_approx(x0) : 0.f;
-              pv[w + 1] = (col + 1 >= vis.lo && col + 1 <= vis.hi) ? ex2_approx(x1) : 0.f;
-              const uint64_t dd2 = f2_add(f2(__uint_as_float(dp[e + w]), __uint_as_float(dp[e + w + 1])),
-                                          ndd[w / 2]);
-              const uint64_t ds2 = f2_fma(f2(pv[w], pv[w + 1]), dd2, f2(0.f, 0.f));
-              f2_split(ds2, dv[w], dv[w + 1]);
+              for (int w = 0; w < 4; w += 2) {
+                const uint64_t x = f2_fma(f2(__uint_as_float(sv[e + w]), __uint_as_float(sv[e + w + 1])),
+                                          sl2, nl2[w / 2]);
+                float x0, x1;
+                f2_split(x, x0, x1);
+                const int col = 16 * c + e + w;
+                pv[w] = (!kMasked || ((mk >> col) & 1u)) ? ex2_approx(x0) : 0.f;
+                pv[w + 1] = (!kMasked || ((mk >> (col + 1)) & 1u)) ? ex2_approx(x1) : 0.f;
+                const uint64_t dd2 = f2_add(f2(__uint_as_float(dp[e + w]), __uint_as_float(dp[e + w + 1])),
+                                            ndd[w / 2]);
+                const uint64_t ds2 = f2_fma(f2(pv[w], pv[w + 1]), dd2, f2(0.f, 0.f));
+                f2_split(ds2, dv[w], dv[w + 1]);
+              }
+              sv[e / 2] = BF16 ? cvt_pack_bf16(pv[0], pv[1]) : cvt_pack_f16(pv[0], pv[1]);
+              sv[e / 2 + 1] = BF16 ? cvt_pack_bf16(pv[2], pv[3]) : cvt_pack_f16(pv[2], pv[3]);
+              dp[e / 2] = BF16 ? cvt_pack_bf16(dv[0], dv[1]) : cvt_pack_f16(dv[0], dv[1]);
+              dp[e / 2 + 1] = BF16 ? cvt_pack_bf16(dv[2], dv[3]) : cvt_pack_f16(dv[2], dv[3]);
             }
-            sv[e / 2] = BF16 ? cvt_pack_bf16(pv[0], pv[1]) : cvt_pack_f16(pv[0], pv[1]);
-            sv[e / 2 + 1] = BF16 ? cvt_pack_bf16(pv[2], pv[3]) : cvt_pack_f16(pv[2], pv[3]);
-            dp[e / 2] = BF16 ? cvt_pack_bf16(dv[0], dv[1]) : cvt_pack_f16(dv[0], dv[1]);
-            dp[e / 2 + 1] = BF16 ? cvt_pack_bf16(dv[2], dv[3]) : cvt_pack_f16(dv[2], dv[3]);
-          }
-          tmem_st8(t_lane + c_s + 8 * c, sv);  // P^T over columns already read
+            tmem_st8(t_lane + c_s + 8 * c, sv);  // P^T over columns already read
 #pragma unroll
-          for (int i = 0; i < 2; ++i)  // dS^T into shared memory for the dK and dQ MMAs
-            st_shared_v4(ds_row + ((static_cast<uint32_t>(4 * sub + 2 * c + i) ^ (row & 7)) << 4),
-                         dp[4 * i], dp[4 * i + 1], dp[4 * i + 2], dp[4 * i + 3]);
-        }
+            for (int i = 0; i < 2; ++i)  // dS^T into shared memory for the dK and dQ MMAs
+              st_shared_v4(ds_row + ((static_cast<uint32_t>(4 * sub + 2 * c + i) ^ (row & 7)) << 4),
+                           dp[4 * i], dp[4 * i + 1], dp[4 * i + 2], dp[4 * i + 3]);
+          }
+        };
+        if (all_vis)
+          chunks(std::false_type{});
+        else
+          chunks(std::true_type{});
         tmem_st_wait();
         fence_proxy_async_smem();  // the MMAs read dS^T through the async proxy
         tc_fence_before();
