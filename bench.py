@@ -85,10 +85,10 @@ NCU_TRAFFIC = {
     "prefill": {"bytes": 522.13e6, "workloads": ("default", "causal4k"),
                 "sources": ['fa_prefill.cu', 'fa_mma.cuh', 'fa_ptx.cuh', 'fa_plan.h', 'fa_internal.h'],
                 "sha256": "c1b9809d6f61876576f34769600da90cb7e0305adedb690f307a790ba94d7552"},
-    # paged decode B8 capture: 547.5 MB read + 4.1 MB written for 547.5 MB algorithmic,
+    # paged decode B8 capture: 547.5 MB read + 4.9 MB written for 547.5 MB algorithmic,
     # scaled to the bench call's 2410.7 MB algorithmic
-    "decode": {"workloads": ("default", "decode"), "bytes": 2.4289e9, "sources": ['fa_decode.cu', 'fa_ptx.cuh', 'fa_internal.h'],
-               "sha256": "f58ddf3a7ba6f1d15da2486cef5923871c31277eeed188e019349a2c65f943d2"},
+    "decode": {"workloads": ("default", "decode"), "bytes": 2.4321e9, "sources": ['fa_decode.cu', 'fa_ptx.cuh', 'fa_internal.h'],
+               "sha256": "8cb2b4a6b72f7981946d2f596fca13eefd0d352127ef81533f9ce99792534363"},
     # FP32 inputs, causal 4k B4 H16 capture of one call: split_bf16_kernel 402.7 MB read +
     # 345.3 MB written, prefill_bm256_kernel (split) 409.0 MB read + 110.4 MB written;
     # scaled x2 to B4 H32

@@ -128,3 +128,37 @@ def test_split_choice_does_not_matter():
     for pps in (1, 2, 4, 7, 20):
         o, lse, _, _ = run_decode(di, 0.09, pages_per_split=pps)
         compare(o, lse, ref_o, ref_l, f"pps {pps}")
+
+
+@pytest.mark.parametrize("d,dt", [(128, torch.float16), (64, torch.bfloat16)])
+def test_pools_only_16_byte_aligned(d, dt):
+    """The split kernel reads 32 bytes of K and V per lane when both pools are 32-byte
+    aligned and 16 bytes per lane otherwise: the same pages read through pools that start
+    16 bytes past a 32-byte boundary take the second path and must give the same results
+    (and the oracle's)."""
+    di = inputs.decode_inputs(B=6, H=4, d=d, page_size=64, num_pages=60, max_ctx=64 * 9,
+                              dtype=dt, seed=23)
+    scale = 1 / math.sqrt(d)
+    ref_o, ref_l = oracle.decode_paged(di.q, di.k_pages, di.v_pages, di.block_table,
+                                       di.ctx_lens, scale)
+    dev = "cuda"
+    shifted = []
+    for pool in (di.k_pages, di.v_pages):
+        flat = torch.empty(pool.numel() + 8, dtype=dt, device=dev)  # 8 elements = 16 bytes
+        view = flat[8:].view(pool.shape)
+        view.copy_(pool.to(dev))
+        assert view.data_ptr() % 32 == 16
+        shifted.append(view)
+    q, bt, cl = di.q.to(dev), di.block_table.to(dev), di.ctx_lens.to(dev)
+    B, H, _ = q.shape
+    mp = bt.shape[1]
+    o = torch.empty_like(q)
+    lse = torch.empty(B, H, dtype=torch.float32, device=dev)
+    ws = torch.empty(fa.fa_decode_workspace_size(B, H, d, mp, di.page_size), dtype=torch.uint8,
+                     device=dev)
+    fa.fa_decode_paged_ex(q, shifted[0], shifted[1], bt, cl, o, lse, scale, ws)
+    torch.cuda.synchronize()
+    assert fa.fa_get_device_status() == fa.FA_OK
+    compare(o, lse, ref_o, ref_l, "16-byte aligned pools")
+    o2, lse2, _, _ = run_decode(di, scale)  # 32-byte aligned pools
+    compare(o2, lse2, ref_o, ref_l, "32-byte aligned pools")

@@ -5,11 +5,12 @@
 // The work is HBM-bound (each cached token is read once, 4*d bytes per head for K and V,
 // for 4*d multiply-adds), so it runs on the CUDA cores with wide coalesced loads:
 //   kernel 1 (split): one CTA per (b*H + h, split). A split is a run of `pages_per_split` pages
-//     of one sequence and one head. A group of d/8 lanes owns one token row: each lane
-//     loads 16 bytes of K and of V, the q.k dot is reduced with xor-shuffles inside the
-//     group, and the group keeps an online softmax state (m, l, acc) in registers,
-//     several tokens in flight per lane. The groups are merged in shared memory and
-//     the split writes its FP32 partial (acc, m, l) to the workspace.
+//     of one sequence and one head. A group of d/16 lanes owns one token row: each lane
+//     loads 32 bytes of K and of V in one access (d/8 lanes and 16 bytes when a pool is
+//     only 16-byte aligned), the q.k dot is reduced with xor-shuffles inside the group,
+//     and the group keeps an online softmax state (m, l, acc) in registers, several
+//     tokens in flight per lane. The groups are merged in shared memory and the split
+//     writes its FP32 partial (acc, m, l) to the workspace.
 //   kernel 2 (merge): per (b, h), M = max m_s, L = sum l_s 2^(m_s - M),
 //     O = sum 2^(m_s - M) acc_s / L, LSE = (M + log2 L) ln 2, formed in one pass over the
 //     splits with the same running-max recurrence as the tiled forward (ops-transformer
@@ -36,6 +37,14 @@ __device__ __forceinline__ uint4 ld_stream(const void* ptr) {
                : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
                : "l"(ptr));
   return r;
+}
+
+// 32 bytes in one access (sm_100 family); the address must be 32-byte aligned.
+__device__ __forceinline__ void ld_stream32(const void* ptr, uint4& a, uint4& b) {
+  asm volatile("ld.global.nc.L1::no_allocate.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(a.x), "=r"(a.y), "=r"(a.z), "=r"(a.w), "=r"(b.x), "=r"(b.y), "=r"(b.z),
+                 "=r"(b.w)
+               : "l"(ptr));
 }
 
 // A context length outside [0, page_size * max_pages] would index past the sequence's
@@ -67,9 +76,10 @@ __device__ __forceinline__ void unpack8(const uint4& u, float* f) {
   }
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, int EPL>
 __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(const DecodeParams p) {
-  constexpr int LPT = D / 8;             // lanes per token row (16 bytes each)
+  constexpr int NV = EPL / 8;            // 16-byte vectors per lane per token row (EPL elements)
+  constexpr int LPT = D / EPL;           // lanes per token row
   constexpr int TPW = 32 / LPT;          // token groups per warp
   constexpr int NG = kDecWarps * TPW;    // token groups per CTA
   __shared__ float sm_m[NG], sm_l[NG];
@@ -99,37 +109,41 @@ __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(const DecodeP
   if (t0 >= t1) return;  // past the end of this sequence: no partial
 
   const int grp = warp * TPW + lane / LPT;  // token group of this lane
-  const int cl = lane % LPT;                // which 8 elements of d
-  float qf[8];
-  {
-    const uint4 qu = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q) +
-                                                     static_cast<size_t>(bh) * D + cl * 8);
-    unpack8<BF16>(qu, qf);
+  const int cl = lane % LPT;                // which EPL elements of d
+  float qf[EPL];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) qf[e] *= p.sl2;
+  for (int v = 0; v < NV; ++v) {
+    const uint4 qu = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q) +
+                                                     static_cast<size_t>(bh) * D + cl * EPL + 8 * v);
+    unpack8<BF16>(qu, qf + 8 * v);
   }
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) qf[e] *= p.sl2;
   const int32_t* table = p.block_table + static_cast<size_t>(b) * p.max_pages;
   const uint16_t* kp = static_cast<const uint16_t*>(p.k_pages);
   const uint16_t* vp = static_cast<const uint16_t*>(p.v_pages);
-  const size_t head_off = static_cast<size_t>(h) * p.page_size * D + cl * 8;
+  const size_t head_off = static_cast<size_t>(h) * p.page_size * D + cl * EPL;
   const size_t page_stride = static_cast<size_t>(p.H) * p.page_size * D;
 
-  float m = -INFINITY, l = 0.f, acc[8];
+  float m = -INFINITY, l = 0.f, acc[EPL];
 #pragma unroll
-  for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+  for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
   bool bad = false;
 
   // the loop bound is warp-uniform so that every lane takes part in every shuffle
   const int sub = lane / LPT;
   for (int wb = t0 + warp * TPW; wb < t1; wb += NG * kUnroll) {
-    uint4 ku[kUnroll], vu[kUnroll];
+    uint4 ku[kUnroll][NV], vu[kUnroll][NV];
     bool live[kUnroll];
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
       const int t = wb + sub + u * NG;
       live[u] = t < t1;
-      ku[u] = make_uint4(0, 0, 0, 0);
-      vu[u] = make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int v = 0; v < NV; ++v) {
+        ku[u][v] = make_uint4(0, 0, 0, 0);
+        vu[u][v] = make_uint4(0, 0, 0, 0);
+      }
       if (live[u]) {
         const int lp = t / p.page_size;
         const int phys = __ldg(table + lp);
@@ -139,19 +153,27 @@ __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(const DecodeP
         } else {
           const size_t off = phys * page_stride + head_off +
                              static_cast<size_t>(t - lp * p.page_size) * D;
-          ku[u] = ld_stream(kp + off);
-          vu[u] = ld_stream(vp + off);
+          if constexpr (NV == 2) {
+            ld_stream32(kp + off, ku[u][0], ku[u][1]);
+            ld_stream32(vp + off, vu[u][0], vu[u][1]);
+          } else {
+            ku[u][0] = ld_stream(kp + off);
+            vu[u][0] = ld_stream(vp + off);
+          }
         }
       }
     }
     float s[kUnroll];
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
-      float kf[8];
-      unpack8<BF16>(ku[u], kf);
       float dot = 0.f;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) dot = fmaf(qf[e], kf[e], dot);
+      for (int v = 0; v < NV; ++v) {
+        float kf[8];
+        unpack8<BF16>(ku[u][v], kf);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) dot = fmaf(qf[8 * v + e], kf[e], dot);
+      }
 #pragma unroll
       for (int off = LPT / 2; off > 0; off /= 2) dot += __shfl_xor_sync(0xffffffffu, dot, off);
       s[u] = live[u] ? dot : -INFINITY;
@@ -164,15 +186,18 @@ __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(const DecodeP
       const float alpha = ex2_approx(m - m_new);  // m = -inf gives 0
       l *= alpha;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) acc[e] *= alpha;
+      for (int e = 0; e < EPL; ++e) acc[e] *= alpha;
 #pragma unroll
       for (int u = 0; u < kUnroll; ++u) {
         const float pu = ex2_approx(s[u] - m_new);
-        float vf[8];
-        unpack8<BF16>(vu[u], vf);
         l += pu;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) acc[e] = fmaf(pu, vf[e], acc[e]);
+        for (int v = 0; v < NV; ++v) {
+          float vf[8];
+          unpack8<BF16>(vu[u][v], vf);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) acc[8 * v + e] = fmaf(pu, vf[e], acc[8 * v + e]);
+        }
       }
       m = m_new;
     }
@@ -185,7 +210,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(const DecodeP
     sm_l[grp] = l;
   }
 #pragma unroll
-  for (int e = 0; e < 8; ++e) sm_acc[grp][cl * 8 + e] = acc[e];
+  for (int e = 0; e < EPL; ++e) sm_acc[grp][cl * EPL + e] = acc[e];
   __syncthreads();
   float* out = p.part + (static_cast<size_t>(bh) * p.nsplit_max + split) * (D + 2);
   for (int e = threadIdx.x; e < D; e += kDecThreads) {
@@ -265,7 +290,11 @@ __global__ void __launch_bounds__(D) decode_merge_kernel(const DecodeParams p) {
 
 template <int D, bool BF16>
 cudaError_t launch_decode_t(const DecodeParams& p, cudaStream_t stream) {
-  decode_split_kernel<D, BF16><<<p.nsplit_max * p.B * p.H, kDecThreads, 0, stream>>>(p);
+  // 32 bytes per lane per token row when both pools are 32-byte aligned, else 16
+  if ((reinterpret_cast<uintptr_t>(p.k_pages) | reinterpret_cast<uintptr_t>(p.v_pages)) % 32 == 0)
+    decode_split_kernel<D, BF16, 16><<<p.nsplit_max * p.B * p.H, kDecThreads, 0, stream>>>(p);
+  else
+    decode_split_kernel<D, BF16, 8><<<p.nsplit_max * p.B * p.H, kDecThreads, 0, stream>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   decode_merge_kernel<D, BF16><<<p.B * p.H, D, 0, stream>>>(p);
