@@ -238,3 +238,72 @@ def test_bwd_rejects_bad_arguments(L):
     assert call(mode=2, w=0) == fa.FA_ERR_INVALID_ARG
     assert L.fa_bwd_workspace_size(2, 3, 100) == 2 * 3 * (100 * 128 + 100) * 4  # dq accumulator at d = 128, D
     assert L.fa_bwd_workspace_size(1, 1, 5) == (8 * 128 + 5) * 4  # Sq rounded up to 4 for the accumulator
+
+
+def test_paged_fwd_rejects_bad_arguments(L):
+    A = 1 << 20  # a 16-byte-aligned fake address; nothing is launched
+    base = dict(q=A, kp=A, vp=A, tab=A, ctx=A, host=A, o=A, lse=A, B=2, H=2, Sq=64, d=64,
+                page=256, mp=4, npages=16, scale=0.125, mode=1, w=0, g=0, dtype=0)
+
+    def calls(**kw):
+        a = dict(base, **kw)
+        r1 = L.fa_fwd_paged(a["q"], a["kp"], a["vp"], a["tab"], a["ctx"], a["o"], a["lse"], a["B"],
+                            a["H"], a["Sq"], a["d"], a["page"], a["mp"], a["npages"], a["scale"],
+                            a["mode"], a["w"], a["g"], a["dtype"], None)
+        r2 = L.fa_fwd_paged_host_lens(a["q"], a["kp"], a["vp"], a["tab"], a["ctx"], a["host"],
+                                      a["o"], a["lse"], a["B"], a["H"], a["Sq"], a["d"], a["page"],
+                                      a["mp"], a["npages"], a["scale"], a["mode"], a["w"], a["g"],
+                                      a["dtype"], None)
+        assert r1 == r2, kw
+        return r1
+    assert calls(kp=None) == fa.FA_ERR_INVALID_ARG
+    assert calls(tab=None) == fa.FA_ERR_INVALID_ARG
+    assert calls(vp=A + 8) == fa.FA_ERR_INVALID_ARG      # pools 16-byte aligned
+    assert calls(ctx=A + 2) == fa.FA_ERR_INVALID_ARG     # lengths 4-byte aligned
+    assert calls(mp=0) == fa.FA_ERR_INVALID_ARG
+    assert calls(page=96) == fa.FA_ERR_UNSUPPORTED       # pages of a multiple of 64 tokens
+    assert calls(page=32) == fa.FA_ERR_UNSUPPORTED
+    assert calls(page=4096, mp=1 << 20) == fa.FA_ERR_INVALID_ARG  # capacity past 2^30
+    assert calls(d=96) == fa.FA_ERR_UNSUPPORTED
+    assert calls(dtype=2) == fa.FA_ERR_UNSUPPORTED       # FP32 inputs are not paged
+    assert calls(mode=2, w=0) == fa.FA_ERR_INVALID_ARG   # a window needs window >= 1
+
+
+def test_bwd_block_sparse_rejects_bad_arguments(L):
+    A = 1 << 20
+    base = dict(q=A, k=A, v=A, o=A, dout=A, lse=A, dq=A, dk=A, dv=A, ws=A, wsb=1 << 20, B=1,
+                H=2, Sq=64, Sk=64, d=64, scale=0.125, lay=A, dtype=0)
+
+    def call(**kw):
+        a = dict(base, **kw)
+        return L.fa_bwd_block_sparse(a["q"], a["k"], a["v"], a["o"], a["dout"], a["lse"], a["dq"],
+                                     a["dk"], a["dv"], a["ws"], a["wsb"], a["B"], a["H"], a["Sq"],
+                                     a["Sk"], a["d"], a["scale"], a["lay"], a["dtype"], None)
+    assert call(lay=None) == fa.FA_ERR_INVALID_ARG
+    assert call(d=96) == fa.FA_ERR_UNSUPPORTED
+    assert call(ws=None) == fa.FA_ERR_INVALID_ARG
+    assert call(wsb=16) == fa.FA_ERR_INVALID_ARG
+    assert call(dq=A + 8) == fa.FA_ERR_INVALID_ARG
+    assert call(dtype=2) == fa.FA_ERR_UNSUPPORTED
+
+
+def test_kv_append_rejects_bad_arguments(L):
+    A = 1 << 20
+    base = dict(kn=A, vn=A, kp=A, vp=A, tab=A, ctx=A, nl=None, B=2, H=2, T=64, d=64, page=256,
+                mp=4, npages=16, dtype=0)
+
+    def call(**kw):
+        a = dict(base, **kw)
+        return L.fa_kv_append(a["kn"], a["vn"], a["kp"], a["vp"], a["tab"], a["ctx"], a["nl"],
+                              a["B"], a["H"], a["T"], a["d"], a["page"], a["mp"], a["npages"],
+                              a["dtype"], None)
+    assert call(T=0) == fa.FA_OK                        # nothing to append: nothing launched
+    assert call(B=0) == fa.FA_ERR_INVALID_ARG
+    assert call(T=-1) == fa.FA_ERR_INVALID_ARG
+    assert call(d=96) == fa.FA_ERR_UNSUPPORTED
+    assert call(dtype=2) == fa.FA_ERR_UNSUPPORTED
+    assert call(page=24) == fa.FA_ERR_UNSUPPORTED       # a multiple of 16 tokens
+    assert call(kp=None) == fa.FA_ERR_INVALID_ARG
+    assert call(vn=A + 8) == fa.FA_ERR_INVALID_ARG
+    assert call(nl=A + 2) == fa.FA_ERR_INVALID_ARG      # new_lens 4-byte aligned
+    assert call(page=4096, mp=1 << 20) == fa.FA_ERR_INVALID_ARG
