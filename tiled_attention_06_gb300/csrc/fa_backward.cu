@@ -712,6 +712,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
 template <int D, bool BF16>
 cudaError_t launch_bwd_t(const BwdLaunch& L, cudaStream_t stream) {
+  if (L.b.head_group < 1) return cudaErrorInvalidValue;  // the launch order divides by it
   const int64_t rows = static_cast<int64_t>(L.p.BH) * L.p.Sq;
   if (rows > 0) {
     const int blocks = static_cast<int>((rows + 63) / 64 < 16384 ? (rows + 63) / 64 : 16384);
