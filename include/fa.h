@@ -235,7 +235,7 @@ fa_status fa_bwd_block_sparse(const void* q, const void* k, const void* v, const
  * Two kernels run on `stream`: split-K partial attention over runs of pages, then
  * the merge of the partials. Pools that both start on a 32-byte boundary are read 32
  * bytes per access, others (16-byte aligned, as every pointer here must be) 16 bytes
- * per access; the two differ only in the FP32 summation order of the q.k dots.
+ * per access; the two differ only in the order of their FP32 sums.
  */
 fa_status fa_decode_paged(const void* q, const void* k_pages, const void* v_pages,
                           const int32_t* block_table, const int32_t* ctx_lens, void* o, float* lse,
